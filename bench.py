@@ -1,0 +1,425 @@
+"""Benchmark of the MXFP4 routed-expert MoE layer on GB300.
+
+Default workload: one Kimi-K3-shaped MoE layer at decode batch 1 (hidden
+7168, 896 MXFP4 experts of 17,547,264 B resident in HBM, top-16, two bf16
+shared experts), synthetic weights and tokens. A step is one forward of the
+whole layer (router, top-k, 16 experts, shared experts, combine) for a fresh
+token. L2 is flushed (a 256 MiB write) before every timed step, outside the
+timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config 1|2|3|4] [--no-cpu-baseline]
+
+Prints one JSON line on rank 0. Under torchrun (N > 1) every rank runs an
+independent replica on its own GPU (the layer does not shard: replicas only);
+time is the max over ranks and the value sums the tokens of all ranks.
+--impl reference times the CPU oracle (the plain reference implementation) on
+the host cores on a bounded sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "K3-shape MoE-layer decode tokens/s; achieved HBM GB/s vs GB300 peak"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+TOKEN_POOL = 64
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    return p.parse_args()
+
+
+# ---- byte accounting ----------------------------------------------------------
+
+def layer_bytes(wl, n_union, T):
+    """Algorithmic HBM bytes of one layer call: router + shared experts + every
+    distinct selected expert read once + x in and out (bf16)."""
+    span = synth.span_bytes(wl.H, wl.I)
+    router = wl.E * wl.H * 4
+    shared = wl.n_shared * 3 * wl.Is * wl.H * 2
+    return router + shared + n_union * span + T * wl.H * 2 * 2
+
+
+def gateup_bytes(wl, n_union, T):
+    """Algorithmic bytes of the gate/up kernel: the gate and up halves of every
+    distinct selected expert (codes + scales), x in, h out (fp32)."""
+    per_expert = 2 * wl.I * wl.H * 17 // 32
+    return n_union * per_expert + T * wl.H * 2 + T * wl.k * wl.I * 4
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def csrc_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "mxfp4_routed_expert_top_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".h", ".cuh")):
+            h.update(name.encode())
+            h.update(open(os.path.join(d, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
+    kernel sources have not changed since it was captured; else None."""
+    try:
+        d = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+        rec = d.get(kernel)
+        if rec and rec.get("csrc_hash") == csrc_hash():
+            return rec["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+# ---- clocks -----------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                f = [v.strip() for v in line.split(",")]
+                if len(f) >= 9 and f[1].replace(".", "").isdigit():
+                    rows.append(f)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---- distributed --------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    import torch.distributed as dist
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist if ws > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def aggregate_over_ranks(dist, seconds, units, device="cpu"):
+    """Max of the elapsed time and sum of the units over ranks (replicas)."""
+    import torch
+    if dist is None:
+        return seconds, units
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ---- CPU oracle baseline ------------------------------------------------------
+
+def cpu_oracle_rate(wl, seconds, max_tokens=None):
+    """Tokens/s of the CPU oracle on the workload's tokens, timed until
+    `seconds` of work (at least one token). Returns (rate, tokens, threads)."""
+    import oracle as orc
+    layers = []
+    for l in range(wl.L):
+        router = synth.router(wl.seed, wl.wcfg, l, wl.E, wl.H)
+        shared = [synth.shared(wl.seed, wl.wcfg, l, s, wl.H, wl.Is)
+                  for s in range(wl.n_shared)]
+        layers.append(orc.Layer(
+            wl.H, wl.E, wl.k, wl.I, wl.Is, router, shared,
+            lambda ly, e: synth.expert_spans(wl.seed, wl.wcfg, ly, e, 1, wl.H, wl.I)[0],
+            layer=l))
+    n, t0 = 0, time.perf_counter()
+    while True:
+        x = synth.token(wl.seed, wl.cfg_id, 100000 + n, wl.H)[None, :]
+        if wl.stack:
+            orc.moe_stack(layers, x, wl.eps)
+        else:
+            orc.moe_layer(layers[0], x)
+        for L in layers:
+            L.clear_cache()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (max_tokens and n >= max_tokens):
+            break
+    return n / el, n, orc.num_threads()
+
+
+# ---- our implementation -------------------------------------------------------
+
+def load_workload(m, wl, torch, stream, chunk=64):
+    span = synth.span_bytes(wl.H, wl.I)
+    buf = torch.empty(chunk * span, dtype=torch.uint8, device="cuda")
+    for l in range(wl.L):
+        router = synth.router(wl.seed, wl.wcfg, l, wl.E, wl.H)
+        shared = [synth.shared(wl.seed, wl.wcfg, l, s, wl.H, wl.Is)
+                  for s in range(wl.n_shared)]
+        m.load_experts(l, router=router, shared=shared)
+        for e0 in range(0, wl.E, chunk):
+            n = min(chunk, wl.E - e0)
+            synth.dev_expert_spans(wl.seed, wl.wcfg, l, e0, n, wl.H, wl.I,
+                                   buf.data_ptr(), stream.cuda_stream)
+            m.load_experts(l, experts=buf, expert_begin=e0, expert_count=n,
+                           src_is_device=True, stream=stream)
+    torch.cuda.synchronize()
+    del buf
+
+
+def run_ours(args):
+    import torch
+    import mxfp4_routed_expert_top_gb300 as dfm
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(ws, "nccl")
+    wl = synth.WORKLOADS[args.config]
+    T = wl.T
+    m = dfm.MoE(wl.H, wl.E, wl.k, wl.I, wl.n_shared, wl.Is, n_layers=wl.L,
+                max_tokens=max(T, 4), rms_eps=wl.eps,
+                flags=dfm.STACK_RMSNORM_RESIDUAL if wl.stack else 0, device=local)
+    stream = torch.cuda.current_stream()
+    load_workload(m, wl, torch, stream)
+
+    # a pool of distinct synthetic tokens (fresh x each step), resident in HBM
+    pool = np.stack([synth.token(wl.seed, wl.cfg_id, 200000 + rank * 100000 + i, wl.H)
+                     for i in range(TOKEN_POOL * T)]).reshape(TOKEN_POOL, T, wl.H)
+    xs = torch.from_numpy(pool.view(np.int16)).cuda()
+    out = torch.empty((T, wl.H), dtype=torch.int16, device="cuda")
+    ids = torch.empty((wl.L, T, wl.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((wl.L, T, wl.k), dtype=torch.float32, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def step(i):
+        m.forward(xs[i % TOKEN_POOL], T, out, ids, w, stream=stream)
+
+    for i in range(args.warmup):
+        flush.fill_(float(i))
+        step(i)
+    m.sync(stream)
+
+    # timed region: K steps, per-step CUDA events around the forward only
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    n_union = []
+    launches = 0
+    with ClockSampler(local) as clk:
+        barrier(dist)
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            step(i)
+            ends[i].record(stream)
+            launches += m.last_launch_count()
+        torch.cuda.synchronize()
+        barrier(dist)
+        wall = time.perf_counter() - wall0
+    m.sync(stream)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    dev_s = sum(step_ms) / 1e3
+    # distinct experts per step (for the byte count), from the ids of the pool
+    for i in range(min(args.steps, TOKEN_POOL)):
+        m.forward(xs[i], T, out, ids, w, stream=stream)
+        n_union.append(len(np.unique(ids[0].cpu().numpy())))
+    u_mean = float(np.mean(n_union))
+
+    # per-kernel device time (same steps, library events on the same stream)
+    m.timing_reset()
+    m.timing_enable(True)
+    for i in range(min(args.steps, 50)):
+        flush.fill_(float(i))
+        step(i)
+    kt = m.timing()
+    m.timing_enable(False)
+
+    # end to end through the public API with host buffers (pinned)
+    hx = torch.from_numpy(pool.view(np.int16)).pin_memory()
+    hout = torch.empty((T, wl.H), dtype=torch.int16).pin_memory()
+    hids = torch.empty((wl.L, T, wl.k), dtype=torch.int32).pin_memory()
+    hw = torch.empty((wl.L, T, wl.k), dtype=torch.float32).pin_memory()
+    e2e_steps = min(args.steps, 50)
+    e2e_t = []
+    for i in range(e2e_steps + 3):
+        flush.fill_(float(i))
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        m.forward_host(hx[i % TOKEN_POOL], T, hout, ids=hids, weights=hw, stream=stream)
+        if i >= 3:
+            e2e_t.append(time.perf_counter() - t0)
+    e2e_s = sum(e2e_t)
+
+    dev_s_max, tokens = aggregate_over_ranks(dist, dev_s, T * args.steps, device="cuda")
+    e2e_max, e2e_tokens = aggregate_over_ranks(dist, e2e_s, T * e2e_steps, device="cuda")
+    if rank != 0:
+        m.close()
+        return None
+
+    peak, peak_kind = measured_peaks()
+    ms = dev_s_max / args.steps * 1e3
+    lb = layer_bytes(wl, u_mean, T) * wl.L
+    gu_n, gu_ms = kt["expert_gateup"]
+    gu_avg_ms = gu_ms / max(gu_n, 1)
+    gu_bytes = gateup_bytes(wl, u_mean, T)
+    gu_gbs = gu_bytes / (gu_avg_ms / 1e3) / 1e9
+    layer_gbs = lb / (ms / 1e3) / 1e9
+    kernels = {k: {"launches": n, "avg_us": round(t / max(n, 1) * 1e3, 2)}
+               for k, (n, t) in kt.items() if n}
+    res = {
+        "metric": METRIC, "value": round(tokens / dev_s_max, 2), "unit": UNIT,
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "impl": "ours",
+        "config": {"workload": wl.name, "hidden": wl.H, "experts": wl.E, "top_k": wl.k,
+                   "inter": wl.I, "shared": wl.n_shared, "tokens_per_step": T,
+                   "layers": wl.L, "weights": "mxfp4 e2m1+e8m0/32, shared bf16",
+                   "l2": "flushed (256 MiB write) before every timed step",
+                   "parallelism": "replicas" if ws > 1 else "single-gpu"},
+        "layer_hbm": {"achieved_gbs": round(layer_gbs, 1), "bytes_per_step": int(lb),
+                      "frac_of_measured": round(layer_gbs / peak, 4),
+                      "frac_of_nominal_8tbs": round(layer_gbs / 8000.0, 4),
+                      "distinct_experts_per_step": u_mean},
+        "roofline": {"bound": "hbm", "kernel": "expert_gateup",
+                     "achieved": round(gu_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gu_gbs / peak, 4), "peak_source": peak_kind,
+                     "bytes_per_launch": int(gu_bytes),
+                     "traffic": recorded_traffic("expert_gateup")},
+        "kernels": kernels,
+        "e2e": {"value": round(e2e_tokens / e2e_max, 2), "unit": UNIT,
+                "h2d_bytes_per_step": T * wl.H * 2,
+                "d2h_bytes_per_step": T * wl.H * 2 + wl.L * T * wl.k * 8},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(wall, 4),
+    }
+    m.close()
+    return res
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return None
+    wl = synth.WORKLOADS[args.config]
+    # each step: one token of the workload through the oracle (a bounded
+    # sample of the workload: the oracle is per-token, so tokens/s carries over)
+    cpu_oracle_rate(wl, 0.0, max_tokens=max(args.warmup, 1))
+    t0 = time.perf_counter()
+    rate, n, threads = cpu_oracle_rate(wl, 0.0, max_tokens=args.steps)
+    el = time.perf_counter() - t0
+    value = n / el
+    return {
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / n * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": wl.name, "tokens_per_step": 1, "layers": wl.L},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
+                         "kind": "oracle",
+                         "sample": "%d tokens of %s, one per step" % (n, wl.name)},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        res = run_reference(args)
+    else:
+        res = run_ours(args)
+        if res is not None and not args.no_cpu_baseline:
+            wl = synth.WORKLOADS[args.config]
+            rate, n, threads = cpu_oracle_rate(wl, args.cpu_seconds)
+            res["cpu_baseline"] = {
+                "value": round(rate, 4), "unit": UNIT,
+                "cores": threads, "kind": "oracle",
+                "sample": "%d tokens of %s through the CPU oracle (%.1f s)" % (
+                    n, wl.name, n / rate)}
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,206 @@
+/*
+ * df_moe.h — C ABI of the GB300 MXFP4 routed-expert MoE layer (sm_103a).
+ *
+ * The operation is the decode-time sparse Mixture-of-Experts layer of a
+ * Kimi-K3-shaped model, as the pages walk through one token (Deltafin
+ * analysis "Kimi K3極限部署技術解析", §5.1; Deltafin README, "How it works"):
+ * the router scores E experts and picks the top k (896 and 16 in K3), each
+ * picked expert runs a SwiGLU FFN whose weights are MXFP4, the expert outputs
+ * are weighted and summed, and the shared experts are added.
+ *
+ *   logits[t][e] = sum_j Wr[e][j] x[t][j]                     (fp32)
+ *   ids[t]       = top-k of logits[t], descending, ties -> lower id
+ *   w[t][i]      = softmax over the k selected logits
+ *   y[t]         = sum_i w[t][i] Wd_e (silu(Wg_e x) * (Wu_e x)),  e = ids[t][i]
+ *                + sum_s Wd_s (silu(Wg_s x) * (Wu_s x))          (shared, bf16)
+ *   out[t]       = residual[t] + y[t]
+ *
+ * MXFP4 (kimi-k3-in-c blog "2.78T 模型塞进 8GB 内存…", section 先把账算明白):
+ * W[r][c] = E2M1(q[r][c]) * 2^(s[r][c/32] - 127), 4-bit codes with one 8-bit
+ * exponent per 32 elements along the input dimension, 0.53125 B/weight.
+ *
+ * Conventions of every call:
+ *   - Pointers marked "device" are CUDA device pointers on the handle's
+ *     device; "host" pointers are ordinary host memory (pinned is faster).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is
+ *     enqueued asynchronously on it unless the call says otherwise.
+ *   - Every call returns DF_MOE_OK (0) or a negative DF_MOE_E* code; the
+ *     message is available from df_moe_last_error(handle) (or, for calls that
+ *     fail before a handle exists, df_moe_last_error(NULL), thread-local).
+ *   - bf16 tensors are passed as 16-bit words (uint16_t / void*).
+ *   - The library owns all weight storage and its workspace. The caller owns
+ *     every input and output buffer.
+ *   - No call is safe to run concurrently with another call on the same
+ *     handle (they share workspace).
+ */
+#ifndef DF_MOE_H
+#define DF_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DF_MOE_API __attribute__((visibility("default")))
+#else
+#define DF_MOE_API
+#endif
+
+#define DF_MOE_OK 0
+#define DF_MOE_EINVAL (-1)   /* invalid argument                              */
+#define DF_MOE_ENOMEM (-2)   /* device or host allocation failed              */
+#define DF_MOE_ECUDA (-3)    /* a CUDA runtime call failed                    */
+#define DF_MOE_ESTATE (-4)   /* forward before every weight was loaded        */
+#define DF_MOE_ERANGE (-5)   /* T > max_tokens, index out of range            */
+#define DF_MOE_ETIMEOUT (-6) /* a bounded device-side wait gave up            */
+#define DF_MOE_EDEVICE (-7)  /* a device-side check recorded an error         */
+
+/* Stack mode: before every layer x is RMS-normalised (unit gain, rms_eps) and
+ * rounded to bf16; after it the layer output is added to x and rounded to
+ * bf16. `out` is the final x. */
+#define DF_MOE_STACK_RMSNORM_RESIDUAL 1u
+
+typedef struct df_moe df_moe; /* opaque, library-owned */
+
+typedef struct {
+  int32_t hidden;       /* H: multiple of 32                                   */
+  int32_t n_experts;    /* E: routed experts per layer, 1..1024                */
+  int32_t top_k;        /* k: experts per token, 1..min(E, 32)                 */
+  int32_t inter;        /* I: routed-expert intermediate, multiple of 32       */
+  int32_t n_shared;     /* shared experts per layer (0..8)                     */
+  int32_t shared_inter; /* Is: shared intermediate, multiple of 32             */
+  int32_t n_layers;     /* L >= 1                                              */
+  int32_t max_tokens;   /* largest T a forward call may use (1..4096)          */
+  float rms_eps;        /* stack mode only                                     */
+  uint32_t flags;       /* DF_MOE_STACK_RMSNORM_RESIDUAL or 0                  */
+} df_moe_config;
+
+/* Weights of one layer, any subset per call (NULL / 0 = leave unchanged). */
+typedef struct {
+  /* fp32 [E][H] row-major. */
+  const float* router;
+  /* expert_count canonical spans back to back, one per expert, expert ids
+   * expert_begin .. expert_begin + expert_count - 1. A span is the six
+   * tensors of one expert, contiguous (Deltafin README, "Techniques / I/O and
+   * streaming": an expert's six tensors are one contiguous range):
+   *   gate_q [I][H/2] | gate_s [I][H/32] | up_q [I][H/2] | up_s [I][H/32] |
+   *   down_q [H][I/2] | down_s [H][I/32]
+   * q bytes hold element 2m in the low nibble and 2m+1 in the high nibble;
+   * s bytes are E8M0 exponents of 32 consecutive elements along the input
+   * dimension. The span is 3*H*I*17/32 bytes (17,547,264 at K3 shape). */
+  const uint8_t* experts;
+  int32_t expert_begin;
+  int32_t expert_count;
+  /* n_shared pointers each, bf16: gate [Is][H], up [Is][H], down [H][Is]. */
+  const uint16_t* const* shared_gate;
+  const uint16_t* const* shared_up;
+  const uint16_t* const* shared_down;
+  /* 1: every pointer above is device memory; 0: host memory. The pointer
+   * arrays themselves are always host memory. */
+  int32_t src_is_device;
+} df_moe_layer_weights;
+
+/* Allocates the weight arenas (one expert-major arena of E spans per layer,
+ * router and shared weights) and the workspace on `cuda_device`.
+ * Errors: EINVAL (bad config), ENOMEM, ECUDA. */
+DF_MOE_API int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out);
+
+/* Frees everything. NULL-safe. The caller must not have work in flight. */
+DF_MOE_API void df_moe_destroy(df_moe* h);
+
+/* Message of the last failing call on h (or of this thread when h is NULL).
+ * Valid until the next call on the same handle/thread. */
+DF_MOE_API const char* df_moe_last_error(const df_moe* h);
+
+/* Bytes of one expert span for this handle's shape / for (H, I). */
+DF_MOE_API size_t df_moe_expert_span_bytes(const df_moe* h);
+DF_MOE_API size_t df_moe_span_bytes_for(int32_t hidden, int32_t inter);
+
+/* Copies the given weights of `layer` into the library's arenas, repacking
+ * expert spans into the kernels' HBM layout (still one contiguous span of the
+ * same size per expert). Host sources are staged through a bounded pinned
+ * buffer; the call returns after the host buffers have been consumed.
+ * Device sources may be freed after `stream` has synchronised.
+ * Errors: EINVAL, ERANGE (layer or expert range), ECUDA. */
+DF_MOE_API int df_moe_load_experts(df_moe* h, int32_t layer,
+                        const df_moe_layer_weights* w, void* stream);
+
+/* One forward pass over T tokens (1 <= T <= max_tokens), asynchronous.
+ *   x_bf16        device [T][H] bf16
+ *   residual_bf16 device [T][H] bf16 or NULL (single-layer mode only)
+ *   out_bf16      device [T][H] bf16 (RNE of the fp32 result)
+ *   out_f32       device [T][H] fp32 or NULL: the fp32 result before rounding
+ *   ids           device [L][T][k] int32, descending logit order
+ *   weights       device [L][T][k] fp32, softmax over the selected logits
+ * Errors: EINVAL, ERANGE (T), ESTATE (weights not loaded), ECUDA, and the
+ * error recorded by an earlier device-side check (EDEVICE / ETIMEOUT). */
+DF_MOE_API int df_moe_forward(df_moe* h, const void* x_bf16, int32_t T,
+                   const void* residual_bf16, void* out_bf16, float* out_f32,
+                   int32_t* ids, float* weights, void* stream);
+
+/* Same, with HOST buffers: copies x (and residual) to the device, runs the
+ * forward, copies the results back and synchronises `stream` before
+ * returning. out_f32, residual, ids and weights may be NULL. */
+DF_MOE_API int df_moe_forward_host(df_moe* h, const uint16_t* x_bf16, int32_t T,
+                        const uint16_t* residual_bf16, uint16_t* out_bf16,
+                        float* out_f32, int32_t* ids, float* weights,
+                        void* stream);
+
+/* Synchronises `stream` and reports any device-side error word. */
+DF_MOE_API int df_moe_sync(df_moe* h, void* stream);
+
+/* ---- single steps (the rows of the hot path, for per-step checks) ---------
+ * Each runs one step of the forward on its own, with the same kernels. */
+
+/* logits device [T][E] fp32 of layer `layer`. */
+DF_MOE_API int df_moe_step_router(df_moe* h, int32_t layer, const void* x_bf16, int32_t T,
+                       float* logits, void* stream);
+/* ids device [T][k], weights device [T][k] from logits device [T][E]. */
+DF_MOE_API int df_moe_step_topk(df_moe* h, const float* logits, int32_t T, int32_t* ids,
+                     float* weights, void* stream);
+/* Counting sort of the T*k assignments a = t*k + j by expert: offs device
+ * [E+1]; tok, slot device [T*k] (segment of expert e ordered by a);
+ * n_union device [1] = number of distinct experts. */
+DF_MOE_API int df_moe_step_group(df_moe* h, const int32_t* ids, int32_t T, int32_t* offs,
+                      int32_t* tok, int32_t* slot, int32_t* n_union,
+                      void* stream);
+/* hbuf device [T*k][I] fp32: silu(Wg x) * (Wu x) of expert ids[t][j] at row
+ * t*k + j. */
+DF_MOE_API int df_moe_step_expert_gateup(df_moe* h, int32_t layer, const void* x_bf16,
+                              int32_t T, const int32_t* ids, float* hbuf,
+                              void* stream);
+/* y device [T][H] fp32 = sum_j weights[t][j] Wd_{ids[t][j]} hbuf[t*k + j]. */
+DF_MOE_API int df_moe_step_expert_down(df_moe* h, int32_t layer, const float* hbuf,
+                            int32_t T, const int32_t* ids,
+                            const float* weights, float* y, void* stream);
+/* y device [T][H] fp32 = sum over shared experts. */
+DF_MOE_API int df_moe_step_shared(df_moe* h, int32_t layer, const void* x_bf16, int32_t T,
+                       float* y, void* stream);
+/* xn device [T][H] bf16 = RNE(x / sqrt(mean(x^2) + rms_eps)). */
+DF_MOE_API int df_moe_step_rmsnorm(df_moe* h, const void* x_bf16, int32_t T, void* xn_bf16,
+                        void* stream);
+
+/* Reads expert `expert` of `layer` back from the device layout into canonical
+ * span order (dst: host, df_moe_expert_span_bytes bytes). Synchronous. */
+DF_MOE_API int df_moe_read_expert_span(df_moe* h, int32_t layer, int32_t expert,
+                            uint8_t* dst);
+
+/* ---- measurement ---------------------------------------------------------
+ * With timing on, every kernel launch of forward is bracketed by CUDA events
+ * on its stream; df_moe_timing_get returns, per kernel kind, the launches and
+ * the summed device time since the last reset. */
+#define DF_MOE_KERNEL_KINDS 12
+DF_MOE_API int df_moe_timing_enable(df_moe* h, int on);
+DF_MOE_API int df_moe_timing_reset(df_moe* h);
+DF_MOE_API int df_moe_timing_get(df_moe* h, int kind, const char** name,
+                      int64_t* launches, double* total_ms);
+/* Kernels launched by the last forward call. */
+DF_MOE_API int df_moe_last_launch_count(const df_moe* h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

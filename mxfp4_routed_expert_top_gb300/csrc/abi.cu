@@ -1,0 +1,708 @@
+// abi.cu — the C ABI (include/df_moe.h): handle, weight arenas, workspace,
+// loading, and the forward orchestration of the kernels.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "df_moe.h"
+#include "internal.h"
+
+using namespace dfm;
+
+namespace {
+
+thread_local std::string g_thread_err;
+
+struct LayerBufs {
+  uint8_t* arena = nullptr;   // E spans, device layout
+  float* router = nullptr;    // [E][H]
+  uint16_t* sh_gate = nullptr;  // [n_s*Is][H]
+  uint16_t* sh_up = nullptr;    // [n_s*Is][H]
+  uint16_t* sh_down = nullptr;  // [H][n_s*Is]
+  bool router_loaded = false;
+  std::vector<uint8_t> shared_loaded;
+  std::vector<uint8_t> expert_loaded;
+  int n_experts_loaded = 0;
+};
+
+struct Pending {
+  int kind;
+  cudaEvent_t a, b;
+};
+
+const char* kKindNames[K_NKINDS] = {"router", "topk", "group", "expert_gateup",
+                                    "expert_down", "combine", "shared_gateup",
+                                    "shared_down", "rmsnorm", "residual",
+                                    "repack", "other"};
+
+}  // namespace
+
+struct df_moe {
+  df_moe_config cfg{};
+  int device = 0;
+  size_t span_bytes = 0;
+  int R = 0;  // n_shared * shared_inter
+  RouterSplit rsplit{};
+  std::vector<LayerBufs> layers;
+  // workspace
+  float* router_part = nullptr;  // [nsplit][Tmax][E]
+  float* logits = nullptr;       // [Tmax][E]
+  int32_t* ids_ws = nullptr;     // [Tmax][k]
+  float* w_ws = nullptr;         // [Tmax][k]
+  Item* items = nullptr;         // [Tmax*k]
+  int32_t* n_items = nullptr;    // [1]
+  int32_t* sorted = nullptr;     // [Tmax*k]
+  float* hbuf = nullptr;         // [Tmax*k][I]
+  float* part = nullptr;         // [Tmax*k][H]
+  float* hsh = nullptr;          // [Tmax][R]
+  float* ysh = nullptr;          // [Tmax][H]
+  uint16_t* xbuf[2] = {nullptr, nullptr};  // [Tmax][H] stack ping-pong
+  uint16_t* xn = nullptr;        // [Tmax][H]
+  uint32_t* err = nullptr;       // device error word
+  // host-API device buffers
+  uint16_t* hx = nullptr;
+  uint16_t* hres = nullptr;
+  uint16_t* hout = nullptr;
+  float* hout32 = nullptr;
+  int32_t* hids = nullptr;
+  float* hw = nullptr;
+  // staging for host-sourced spans
+  uint8_t* staging = nullptr;
+  size_t staging_spans = 0;
+  std::vector<void*> allocs;
+  std::string last_error;
+  // timing
+  bool timing = false;
+  std::vector<Pending> pending;
+  std::vector<cudaEvent_t> event_pool;
+  double kind_ms[K_NKINDS] = {};
+  int64_t kind_n[K_NKINDS] = {};
+  int launches = 0;
+};
+
+namespace {
+
+int fail(df_moe* h, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (h) h->last_error = buf;
+  else g_thread_err = buf;
+  return code;
+}
+
+#define CUDA_OR_FAIL(h, call)                                                  \
+  do {                                                                         \
+    cudaError_t e_ = (call);                                                   \
+    if (e_ != cudaSuccess)                                                     \
+      return fail((h), DF_MOE_ECUDA, "%s failed: %s", #call,                   \
+                  cudaGetErrorString(e_));                                     \
+  } while (0)
+
+template <typename T>
+int dalloc(df_moe* h, T** p, size_t n) {
+  *p = nullptr;
+  if (n == 0) n = 1;
+  cudaError_t e = cudaMalloc((void**)p, n * sizeof(T));
+  if (e != cudaSuccess) {
+    *p = nullptr;
+    cudaGetLastError();
+    return fail(h, DF_MOE_ENOMEM, "cudaMalloc of %zu bytes failed: %s",
+                n * sizeof(T), cudaGetErrorString(e));
+  }
+  h->allocs.push_back(*p);
+  return DF_MOE_OK;
+}
+
+cudaEvent_t get_event(df_moe* h) {
+  if (!h->event_pool.empty()) {
+    cudaEvent_t e = h->event_pool.back();
+    h->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Run one kernel launch, bracketed by events when timing is on.
+template <typename F>
+int run(df_moe* h, int kind, cudaStream_t s, F&& launch) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (h->timing) {
+    a = get_event(h);
+    b = get_event(h);
+    cudaEventRecord(a, s);
+  }
+  cudaError_t e = launch();
+  if (e != cudaSuccess)
+    return fail(h, DF_MOE_ECUDA, "%s launch failed: %s", kKindNames[kind],
+                cudaGetErrorString(e));
+  if (h->timing) {
+    cudaEventRecord(b, s);
+    h->pending.push_back(Pending{kind, a, b});
+  }
+  h->launches += 1;
+  return DF_MOE_OK;
+}
+
+#define RUN(h, kind, s, expr)                                   \
+  do {                                                          \
+    int rc_ = run((h), (kind), (s), [&]() { return (expr); });  \
+    if (rc_) return rc_;                                        \
+  } while (0)
+
+int check_layer_ready(df_moe* h, int l) {
+  const LayerBufs& L = h->layers[l];
+  if (!L.router_loaded)
+    return fail(h, DF_MOE_ESTATE, "layer %d: router not loaded", l);
+  for (int s = 0; s < h->cfg.n_shared; ++s)
+    if (!L.shared_loaded[s])
+      return fail(h, DF_MOE_ESTATE, "layer %d: shared expert %d not loaded", l, s);
+  if (L.n_experts_loaded != h->cfg.n_experts)
+    return fail(h, DF_MOE_ESTATE, "layer %d: %d of %d experts loaded", l,
+                L.n_experts_loaded, h->cfg.n_experts);
+  return DF_MOE_OK;
+}
+
+// Router + top-k (+ grouping) of one layer. ids/w: [T][k] device.
+int route(df_moe* h, int l, const uint16_t* x, int T, int32_t* ids, float* w,
+          cudaStream_t s, float* logits_out, int tg) {
+  const df_moe_config& c = h->cfg;
+  const LayerBufs& L = h->layers[l];
+  RUN(h, K_ROUTER, s, launch_router(L.router, c.n_experts, c.hidden, x, T,
+                                    h->router_part, h->rsplit, s));
+  const bool direct = (T == 1 && tg == 1);
+  RUN(h, K_TOPK, s, launch_topk(h->router_part, h->rsplit.nsplit, T,
+                                c.n_experts, c.top_k, logits_out, ids, w,
+                                direct ? h->items : nullptr, h->n_items,
+                                h->sorted, s));
+  if (!direct)
+    RUN(h, K_GROUP, s, launch_group(ids, T, c.top_k, c.n_experts, nullptr,
+                                    nullptr, nullptr, nullptr, h->items,
+                                    h->n_items, h->sorted, tg, s));
+  return DF_MOE_OK;
+}
+
+int shared_part(df_moe* h, int l, const uint16_t* x, int T, float* ysh,
+                cudaStream_t s) {
+  const df_moe_config& c = h->cfg;
+  const LayerBufs& L = h->layers[l];
+  RUN(h, K_SHARED_GU, s, launch_shared_gateup(L.sh_gate, L.sh_up, h->R,
+                                              c.hidden, x, T, h->hsh, s));
+  RUN(h, K_SHARED_DN, s, launch_shared_down(L.sh_down, c.hidden, h->R, h->hsh,
+                                            T, ysh, s));
+  return DF_MOE_OK;
+}
+
+// One MoE layer: out = residual + routed + shared.
+int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
+                  const uint16_t* residual, uint16_t* out_bf16, float* out_f32,
+                  int32_t* ids, float* w, cudaStream_t s) {
+  const df_moe_config& c = h->cfg;
+  const LayerBufs& L = h->layers[l];
+  const int tg = T == 1 ? 1 : 2;
+  int rc = route(h, l, x, T, ids, w, s, nullptr, tg);
+  if (rc) return rc;
+  if (c.n_shared > 0) {
+    rc = shared_part(h, l, x, T, h->ysh, s);
+    if (rc) return rc;
+  }
+  const int max_items = (T == 1 && tg == 1) ? c.top_k : T * c.top_k;
+  RUN(h, K_GATEUP, s, launch_gateup(L.arena, h->span_bytes, c.hidden, c.inter,
+                                    c.top_k, x, h->items, h->n_items, max_items,
+                                    h->sorted, h->hbuf, tg, s));
+  RUN(h, K_DOWN, s, launch_down(L.arena, h->span_bytes, c.hidden, c.inter,
+                                h->items, h->n_items, max_items, h->sorted,
+                                h->hbuf, h->part, tg, s));
+  RUN(h, K_COMBINE, s, launch_combine(h->part, w, T, c.top_k, c.hidden,
+                                      c.n_shared > 0 ? h->ysh : nullptr,
+                                      residual, out_f32, out_bf16, s));
+  return DF_MOE_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* df_moe_last_error(const df_moe* h) {
+  return h ? h->last_error.c_str() : g_thread_err.c_str();
+}
+
+size_t df_moe_span_bytes_for(int32_t H, int32_t I) {
+  if (H <= 0 || I <= 0) return 0;
+  return span_layout(H, I).bytes;
+}
+
+size_t df_moe_expert_span_bytes(const df_moe* h) { return h ? h->span_bytes : 0; }
+
+void df_moe_destroy(df_moe* h) {
+  if (!h) return;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(h->device);
+  for (auto& p : h->pending) {
+    cudaEventDestroy(p.a);
+    cudaEventDestroy(p.b);
+  }
+  for (auto e : h->event_pool) cudaEventDestroy(e);
+  for (void* p : h->allocs) cudaFree(p);
+  cudaSetDevice(prev);
+  delete h;
+}
+
+int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
+  if (!cfg || !out) return fail(nullptr, DF_MOE_EINVAL, "null argument");
+  *out = nullptr;
+  const df_moe_config c = *cfg;
+  if (c.hidden <= 0 || c.hidden % 32 || c.hidden > 8192)
+    return fail(nullptr, DF_MOE_EINVAL, "hidden must be a multiple of 32 in [32, 8192]");
+  if (c.inter <= 0 || c.inter % 32 || c.inter > 8192)
+    return fail(nullptr, DF_MOE_EINVAL, "inter must be a multiple of 32 in [32, 8192]");
+  if (c.n_experts < 1 || c.n_experts > 1024)
+    return fail(nullptr, DF_MOE_EINVAL, "n_experts must be in [1, 1024]");
+  if (c.top_k < 1 || c.top_k > c.n_experts || c.top_k > 32)
+    return fail(nullptr, DF_MOE_EINVAL, "top_k must be in [1, min(n_experts, 32)]");
+  if (c.n_shared < 0 || c.n_shared > 8)
+    return fail(nullptr, DF_MOE_EINVAL, "n_shared must be in [0, 8]");
+  if (c.n_shared > 0 && (c.shared_inter <= 0 || c.shared_inter % 32 ||
+                         c.n_shared * c.shared_inter > 6144))
+    return fail(nullptr, DF_MOE_EINVAL,
+                "shared_inter must be a multiple of 32 with n_shared*shared_inter <= 6144");
+  if (c.n_layers < 1 || c.n_layers > 64)
+    return fail(nullptr, DF_MOE_EINVAL, "n_layers must be in [1, 64]");
+  if (c.max_tokens < 1 || c.max_tokens > 4096 || c.max_tokens * c.top_k > 65535)
+    return fail(nullptr, DF_MOE_EINVAL,
+                "max_tokens must be in [1, 4096] with max_tokens*top_k <= 65535");
+  if (c.n_layers > 1 && !(c.flags & DF_MOE_STACK_RMSNORM_RESIDUAL))
+    return fail(nullptr, DF_MOE_EINVAL, "n_layers > 1 needs DF_MOE_STACK_RMSNORM_RESIDUAL");
+  if ((c.flags & ~DF_MOE_STACK_RMSNORM_RESIDUAL) != 0)
+    return fail(nullptr, DF_MOE_EINVAL, "unknown flags");
+  if ((c.flags & DF_MOE_STACK_RMSNORM_RESIDUAL) && !(c.rms_eps >= 0.0f))
+    return fail(nullptr, DF_MOE_EINVAL, "rms_eps must be >= 0");
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || cuda_device < 0 ||
+      cuda_device >= ndev) {
+    cudaGetLastError();
+    return fail(nullptr, DF_MOE_EINVAL, "no CUDA device %d", cuda_device);
+  }
+  int prev = 0;
+  cudaGetDevice(&prev);
+  if (cudaSetDevice(cuda_device) != cudaSuccess)
+    return fail(nullptr, DF_MOE_ECUDA, "cudaSetDevice(%d) failed", cuda_device);
+
+  df_moe* h = new df_moe;
+  h->cfg = c;
+  h->device = cuda_device;
+  h->span_bytes = span_layout(c.hidden, c.inter).bytes;
+  h->R = c.n_shared * c.shared_inter;
+  h->rsplit = router_split(c.n_experts, c.hidden);
+  const size_t H = c.hidden, E = c.n_experts, k = c.top_k, I = c.inter;
+  const size_t Tm = c.max_tokens, R = h->R;
+  int rc = DF_MOE_OK;
+  h->layers.resize(c.n_layers);
+  for (int l = 0; l < c.n_layers && !rc; ++l) {
+    LayerBufs& L = h->layers[l];
+    L.shared_loaded.assign(c.n_shared, 0);
+    L.expert_loaded.assign(c.n_experts, 0);
+    rc = dalloc(h, &L.arena, E * h->span_bytes);
+    if (!rc) rc = dalloc(h, &L.router, E * H);
+    if (!rc && R) rc = dalloc(h, &L.sh_gate, R * H);
+    if (!rc && R) rc = dalloc(h, &L.sh_up, R * H);
+    if (!rc && R) rc = dalloc(h, &L.sh_down, H * R);
+  }
+  if (!rc) rc = dalloc(h, &h->router_part, (size_t)h->rsplit.nsplit * Tm * E);
+  if (!rc) rc = dalloc(h, &h->logits, Tm * E);
+  if (!rc) rc = dalloc(h, &h->ids_ws, Tm * k);
+  if (!rc) rc = dalloc(h, &h->w_ws, Tm * k);
+  if (!rc) rc = dalloc(h, &h->items, Tm * k);
+  if (!rc) rc = dalloc(h, &h->n_items, 1);
+  if (!rc) rc = dalloc(h, &h->sorted, Tm * k);
+  if (!rc) rc = dalloc(h, &h->hbuf, Tm * k * I);
+  if (!rc) rc = dalloc(h, &h->part, Tm * k * H);
+  if (!rc && R) rc = dalloc(h, &h->hsh, Tm * R);
+  if (!rc) rc = dalloc(h, &h->ysh, Tm * H);
+  if (!rc) rc = dalloc(h, &h->xbuf[0], Tm * H);
+  if (!rc) rc = dalloc(h, &h->xbuf[1], Tm * H);
+  if (!rc) rc = dalloc(h, &h->xn, Tm * H);
+  if (!rc) rc = dalloc(h, &h->err, 1);
+  if (!rc) rc = dalloc(h, &h->hx, Tm * H);
+  if (!rc) rc = dalloc(h, &h->hres, Tm * H);
+  if (!rc) rc = dalloc(h, &h->hout, Tm * H);
+  if (!rc) rc = dalloc(h, &h->hout32, Tm * H);
+  if (!rc) rc = dalloc(h, &h->hids, (size_t)c.n_layers * Tm * k);
+  if (!rc) rc = dalloc(h, &h->hw, (size_t)c.n_layers * Tm * k);
+  if (!rc && cudaMemset(h->err, 0, sizeof(uint32_t)) != cudaSuccess)
+    rc = fail(h, DF_MOE_ECUDA, "cudaMemset failed");
+  if (rc) {
+    g_thread_err = h->last_error;
+    df_moe_destroy(h);
+    cudaSetDevice(prev);
+    return rc;
+  }
+  cudaSetDevice(prev);
+  *out = h;
+  return DF_MOE_OK;
+}
+
+int df_moe_load_experts(df_moe* h, int32_t layer, const df_moe_layer_weights* w,
+                        void* stream) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  if (!w) return fail(h, DF_MOE_EINVAL, "null weights");
+  const df_moe_config& c = h->cfg;
+  if (layer < 0 || layer >= c.n_layers)
+    return fail(h, DF_MOE_ERANGE, "layer %d out of range", layer);
+  cudaStream_t s = (cudaStream_t)stream;
+  CUDA_OR_FAIL(h, cudaSetDevice(h->device));
+  LayerBufs& L = h->layers[layer];
+  const cudaMemcpyKind kind = w->src_is_device ? cudaMemcpyDeviceToDevice
+                                               : cudaMemcpyHostToDevice;
+  const size_t H = c.hidden, Is = c.shared_inter;
+  if (w->router) {
+    CUDA_OR_FAIL(h, cudaMemcpyAsync(L.router, w->router,
+                                    (size_t)c.n_experts * H * sizeof(float),
+                                    kind, s));
+    L.router_loaded = true;
+  }
+  for (int sidx = 0; sidx < c.n_shared; ++sidx) {
+    const uint16_t* g = w->shared_gate ? w->shared_gate[sidx] : nullptr;
+    const uint16_t* u = w->shared_up ? w->shared_up[sidx] : nullptr;
+    const uint16_t* d = w->shared_down ? w->shared_down[sidx] : nullptr;
+    if (!g && !u && !d) continue;
+    if (!g || !u || !d)
+      return fail(h, DF_MOE_EINVAL, "shared expert %d: gate, up and down go together", sidx);
+    CUDA_OR_FAIL(h, cudaMemcpyAsync(L.sh_gate + sidx * Is * H, g,
+                                    Is * H * sizeof(uint16_t), kind, s));
+    CUDA_OR_FAIL(h, cudaMemcpyAsync(L.sh_up + sidx * Is * H, u,
+                                    Is * H * sizeof(uint16_t), kind, s));
+    // down_s [H][Is] becomes columns sidx*Is .. of down_cat [H][R]
+    CUDA_OR_FAIL(h, cudaMemcpy2DAsync(L.sh_down + sidx * Is, h->R * sizeof(uint16_t),
+                                      d, Is * sizeof(uint16_t), Is * sizeof(uint16_t),
+                                      H, kind, s));
+    L.shared_loaded[sidx] = 1;
+  }
+  if (w->expert_count > 0) {
+    if (!w->experts) return fail(h, DF_MOE_EINVAL, "experts is NULL");
+    if (w->expert_begin < 0 || w->expert_begin + w->expert_count > c.n_experts)
+      return fail(h, DF_MOE_ERANGE, "experts [%d, %d) out of range", w->expert_begin,
+                  w->expert_begin + w->expert_count);
+    uint8_t* dst = L.arena + (size_t)w->expert_begin * h->span_bytes;
+    if (w->src_is_device) {
+      if (!aligned16(w->experts))
+        return fail(h, DF_MOE_EINVAL, "device expert spans must be 16-byte aligned");
+      RUN(h, K_REPACK, s, launch_repack_span(w->experts, dst, w->expert_count,
+                                             c.hidden, c.inter, 0, s));
+    } else {
+      const size_t chunk = 8;
+      if (!h->staging) {
+        h->staging_spans = chunk;
+        int rc = dalloc(h, &h->staging, chunk * h->span_bytes);
+        if (rc) return rc;
+      }
+      for (int e0 = 0; e0 < w->expert_count; e0 += (int)chunk) {
+        const int n = (int)std::min<size_t>(chunk, (size_t)(w->expert_count - e0));
+        CUDA_OR_FAIL(h, cudaMemcpyAsync(h->staging,
+                                        w->experts + (size_t)e0 * h->span_bytes,
+                                        (size_t)n * h->span_bytes,
+                                        cudaMemcpyHostToDevice, s));
+        RUN(h, K_REPACK, s, launch_repack_span(h->staging,
+                                               dst + (size_t)e0 * h->span_bytes,
+                                               n, c.hidden, c.inter, 0, s));
+      }
+      CUDA_OR_FAIL(h, cudaStreamSynchronize(s));
+    }
+    for (int e = w->expert_begin; e < w->expert_begin + w->expert_count; ++e) {
+      if (!L.expert_loaded[e]) {
+        L.expert_loaded[e] = 1;
+        L.n_experts_loaded += 1;
+      }
+    }
+  }
+  return DF_MOE_OK;
+}
+
+int df_moe_forward(df_moe* h, const void* x_bf16, int32_t T,
+                   const void* residual_bf16, void* out_bf16, float* out_f32,
+                   int32_t* ids, float* weights, void* stream) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  const df_moe_config& c = h->cfg;
+  h->launches = 0;
+  if (!x_bf16 || !out_bf16 || !ids || !weights)
+    return fail(h, DF_MOE_EINVAL, "x, out, ids and weights are required");
+  if (T < 1 || T > c.max_tokens)
+    return fail(h, DF_MOE_ERANGE, "T = %d outside [1, %d]", T, c.max_tokens);
+  if (!aligned16(x_bf16) || !aligned16(out_bf16) ||
+      (residual_bf16 && !aligned16(residual_bf16)))
+    return fail(h, DF_MOE_EINVAL, "x, residual and out must be 16-byte aligned");
+  const bool stack = (c.flags & DF_MOE_STACK_RMSNORM_RESIDUAL) != 0;
+  if (stack && residual_bf16)
+    return fail(h, DF_MOE_EINVAL, "stack mode takes no residual (x is the residual)");
+  for (int l = 0; l < c.n_layers; ++l) {
+    int rc = check_layer_ready(h, l);
+    if (rc) return rc;
+  }
+  CUDA_OR_FAIL(h, cudaSetDevice(h->device));
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t Tk = (size_t)T * c.top_k;
+  if (!stack) {
+    return layer_forward(h, 0, (const uint16_t*)x_bf16, T,
+                         (const uint16_t*)residual_bf16, (uint16_t*)out_bf16,
+                         out_f32, ids, weights, s);
+  }
+  const uint16_t* cur = (const uint16_t*)x_bf16;
+  for (int l = 0; l < c.n_layers; ++l) {
+    RUN(h, K_RMSNORM, s, launch_rmsnorm(cur, T, c.hidden, c.rms_eps, h->xn, s));
+    const bool last = l == c.n_layers - 1;
+    uint16_t* nxt = last ? (uint16_t*)out_bf16 : h->xbuf[l & 1];
+    int rc = layer_forward(h, l, h->xn, T, cur, nxt, last ? out_f32 : nullptr,
+                           ids + (size_t)l * Tk, weights + (size_t)l * Tk, s);
+    if (rc) return rc;
+    cur = nxt;
+  }
+  return DF_MOE_OK;
+}
+
+int df_moe_forward_host(df_moe* h, const uint16_t* x_bf16, int32_t T,
+                        const uint16_t* residual_bf16, uint16_t* out_bf16,
+                        float* out_f32, int32_t* ids, float* weights,
+                        void* stream) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  const df_moe_config& c = h->cfg;
+  if (!x_bf16 || !out_bf16)
+    return fail(h, DF_MOE_EINVAL, "x and out are required");
+  if (T < 1 || T > c.max_tokens)
+    return fail(h, DF_MOE_ERANGE, "T = %d outside [1, %d]", T, c.max_tokens);
+  CUDA_OR_FAIL(h, cudaSetDevice(h->device));
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t n = (size_t)T * c.hidden;
+  const size_t nk = (size_t)c.n_layers * T * c.top_k;
+  CUDA_OR_FAIL(h, cudaMemcpyAsync(h->hx, x_bf16, n * 2, cudaMemcpyHostToDevice, s));
+  if (residual_bf16)
+    CUDA_OR_FAIL(h, cudaMemcpyAsync(h->hres, residual_bf16, n * 2,
+                                    cudaMemcpyHostToDevice, s));
+  int rc = df_moe_forward(h, h->hx, T, residual_bf16 ? h->hres : nullptr, h->hout,
+                          out_f32 ? h->hout32 : nullptr, h->hids, h->hw, stream);
+  if (rc) return rc;
+  CUDA_OR_FAIL(h, cudaMemcpyAsync(out_bf16, h->hout, n * 2, cudaMemcpyDeviceToHost, s));
+  if (out_f32)
+    CUDA_OR_FAIL(h, cudaMemcpyAsync(out_f32, h->hout32, n * 4, cudaMemcpyDeviceToHost, s));
+  if (ids)
+    CUDA_OR_FAIL(h, cudaMemcpyAsync(ids, h->hids, nk * 4, cudaMemcpyDeviceToHost, s));
+  if (weights)
+    CUDA_OR_FAIL(h, cudaMemcpyAsync(weights, h->hw, nk * 4, cudaMemcpyDeviceToHost, s));
+  CUDA_OR_FAIL(h, cudaStreamSynchronize(s));
+  return DF_MOE_OK;
+}
+
+int df_moe_sync(df_moe* h, void* stream) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  CUDA_OR_FAIL(h, cudaSetDevice(h->device));
+  CUDA_OR_FAIL(h, cudaStreamSynchronize((cudaStream_t)stream));
+  uint32_t e = 0;
+  CUDA_OR_FAIL(h, cudaMemcpy(&e, h->err, 4, cudaMemcpyDeviceToHost));
+  if (e) {
+    CUDA_OR_FAIL(h, cudaMemset(h->err, 0, 4));
+    if (e & DEV_ERR_TIMEOUT)
+      return fail(h, DF_MOE_ETIMEOUT, "a bounded device wait gave up");
+    return fail(h, DF_MOE_EDEVICE, "device-side check failed (0x%x)", e);
+  }
+  return DF_MOE_OK;
+}
+
+// ---- single steps ----------------------------------------------------------
+
+int df_moe_step_router(df_moe* h, int32_t layer, const void* x_bf16, int32_t T,
+                       float* logits, void* stream) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  const df_moe_config& c = h->cfg;
+  if (layer < 0 || layer >= c.n_layers) return fail(h, DF_MOE_ERANGE, "bad layer");
+  if (T < 1 || T > c.max_tokens) return fail(h, DF_MOE_ERANGE, "bad T");
+  if (!x_bf16 || !logits) return fail(h, DF_MOE_EINVAL, "null pointer");
+  if (!h->layers[layer].router_loaded) return fail(h, DF_MOE_ESTATE, "router not loaded");
+  CUDA_OR_FAIL(h, cudaSetDevice(h->device));
+  cudaStream_t s = (cudaStream_t)stream;
+  return route(h, layer, (const uint16_t*)x_bf16, T, h->ids_ws, h->w_ws, s,
+               logits, 1 + (T > 1));
+}
+
+int df_moe_step_topk(df_moe* h, const float* logits, int32_t T, int32_t* ids,
+                     float* weights, void* stream) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  const df_moe_config& c = h->cfg;
+  if (T < 1 || T > c.max_tokens) return fail(h, DF_MOE_ERANGE, "bad T");
+  if (!logits || !ids || !weights) return fail(h, DF_MOE_EINVAL, "null pointer");
+  CUDA_OR_FAIL(h, cudaSetDevice(h->device));
+  cudaStream_t s = (cudaStream_t)stream;
+  // the top-k kernel sums nsplit partial-logit planes; one plane = logits
+  RUN(h, K_TOPK, s, launch_topk(logits, 1, T, c.n_experts, c.top_k, nullptr,
+                                ids, weights, nullptr, nullptr, nullptr, s));
+  return DF_MOE_OK;
+}
+
+int df_moe_step_group(df_moe* h, const int32_t* ids, int32_t T, int32_t* offs,
+                      int32_t* tok, int32_t* slot, int32_t* n_union,
+                      void* stream) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  const df_moe_config& c = h->cfg;
+  if (T < 1 || T > c.max_tokens) return fail(h, DF_MOE_ERANGE, "bad T");
+  if (!ids || !offs || !tok || !slot || !n_union)
+    return fail(h, DF_MOE_EINVAL, "null pointer");
+  CUDA_OR_FAIL(h, cudaSetDevice(h->device));
+  cudaStream_t s = (cudaStream_t)stream;
+  RUN(h, K_GROUP, s, launch_group(ids, T, c.top_k, c.n_experts, offs, tok, slot,
+                                  n_union, h->items, h->n_items, h->sorted,
+                                  T == 1 ? 1 : 2, s));
+  return DF_MOE_OK;
+}
+
+int df_moe_step_expert_gateup(df_moe* h, int32_t layer, const void* x_bf16,
+                              int32_t T, const int32_t* ids, float* hbuf,
+                              void* stream) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  const df_moe_config& c = h->cfg;
+  if (layer < 0 || layer >= c.n_layers) return fail(h, DF_MOE_ERANGE, "bad layer");
+  if (T < 1 || T > c.max_tokens) return fail(h, DF_MOE_ERANGE, "bad T");
+  if (!x_bf16 || !ids || !hbuf) return fail(h, DF_MOE_EINVAL, "null pointer");
+  if (h->layers[layer].n_experts_loaded != c.n_experts)
+    return fail(h, DF_MOE_ESTATE, "experts not loaded");
+  CUDA_OR_FAIL(h, cudaSetDevice(h->device));
+  cudaStream_t s = (cudaStream_t)stream;
+  const int tg = T == 1 ? 1 : 2;
+  RUN(h, K_GROUP, s, launch_group(ids, T, c.top_k, c.n_experts, nullptr, nullptr,
+                                  nullptr, nullptr, h->items, h->n_items,
+                                  h->sorted, tg, s));
+  RUN(h, K_GATEUP, s, launch_gateup(h->layers[layer].arena, h->span_bytes,
+                                    c.hidden, c.inter, c.top_k,
+                                    (const uint16_t*)x_bf16, h->items, h->n_items,
+                                    T * c.top_k, h->sorted, hbuf, tg, s));
+  return DF_MOE_OK;
+}
+
+int df_moe_step_expert_down(df_moe* h, int32_t layer, const float* hbuf,
+                            int32_t T, const int32_t* ids, const float* weights,
+                            float* y, void* stream) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  const df_moe_config& c = h->cfg;
+  if (layer < 0 || layer >= c.n_layers) return fail(h, DF_MOE_ERANGE, "bad layer");
+  if (T < 1 || T > c.max_tokens) return fail(h, DF_MOE_ERANGE, "bad T");
+  if (!hbuf || !ids || !weights || !y) return fail(h, DF_MOE_EINVAL, "null pointer");
+  if (h->layers[layer].n_experts_loaded != c.n_experts)
+    return fail(h, DF_MOE_ESTATE, "experts not loaded");
+  CUDA_OR_FAIL(h, cudaSetDevice(h->device));
+  cudaStream_t s = (cudaStream_t)stream;
+  const int tg = T == 1 ? 1 : 2;
+  RUN(h, K_GROUP, s, launch_group(ids, T, c.top_k, c.n_experts, nullptr, nullptr,
+                                  nullptr, nullptr, h->items, h->n_items,
+                                  h->sorted, tg, s));
+  RUN(h, K_DOWN, s, launch_down(h->layers[layer].arena, h->span_bytes, c.hidden,
+                                c.inter, h->items, h->n_items, T * c.top_k,
+                                h->sorted, hbuf, h->part, tg, s));
+  RUN(h, K_COMBINE, s, launch_combine(h->part, weights, T, c.top_k, c.hidden,
+                                      nullptr, nullptr, y, nullptr, s));
+  return DF_MOE_OK;
+}
+
+int df_moe_step_shared(df_moe* h, int32_t layer, const void* x_bf16, int32_t T,
+                       float* y, void* stream) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  const df_moe_config& c = h->cfg;
+  if (layer < 0 || layer >= c.n_layers) return fail(h, DF_MOE_ERANGE, "bad layer");
+  if (T < 1 || T > c.max_tokens) return fail(h, DF_MOE_ERANGE, "bad T");
+  if (!x_bf16 || !y) return fail(h, DF_MOE_EINVAL, "null pointer");
+  for (int sidx = 0; sidx < c.n_shared; ++sidx)
+    if (!h->layers[layer].shared_loaded[sidx])
+      return fail(h, DF_MOE_ESTATE, "shared expert %d not loaded", sidx);
+  CUDA_OR_FAIL(h, cudaSetDevice(h->device));
+  cudaStream_t s = (cudaStream_t)stream;
+  if (c.n_shared == 0) {
+    CUDA_OR_FAIL(h, cudaMemsetAsync(y, 0, (size_t)T * c.hidden * 4, s));
+    return DF_MOE_OK;
+  }
+  return shared_part(h, layer, (const uint16_t*)x_bf16, T, y, s);
+}
+
+int df_moe_step_rmsnorm(df_moe* h, const void* x_bf16, int32_t T, void* xn_bf16,
+                        void* stream) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  const df_moe_config& c = h->cfg;
+  if (T < 1 || T > c.max_tokens) return fail(h, DF_MOE_ERANGE, "bad T");
+  if (!x_bf16 || !xn_bf16) return fail(h, DF_MOE_EINVAL, "null pointer");
+  CUDA_OR_FAIL(h, cudaSetDevice(h->device));
+  cudaStream_t s = (cudaStream_t)stream;
+  RUN(h, K_RMSNORM, s, launch_rmsnorm((const uint16_t*)x_bf16, T, c.hidden,
+                                      c.rms_eps, (uint16_t*)xn_bf16, s));
+  return DF_MOE_OK;
+}
+
+int df_moe_read_expert_span(df_moe* h, int32_t layer, int32_t expert,
+                            uint8_t* dst) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  const df_moe_config& c = h->cfg;
+  if (layer < 0 || layer >= c.n_layers || expert < 0 || expert >= c.n_experts)
+    return fail(h, DF_MOE_ERANGE, "layer/expert out of range");
+  if (!dst) return fail(h, DF_MOE_EINVAL, "null dst");
+  CUDA_OR_FAIL(h, cudaSetDevice(h->device));
+  uint8_t* tmp = nullptr;
+  CUDA_OR_FAIL(h, cudaMalloc(&tmp, h->span_bytes));
+  cudaError_t e = launch_repack_span(h->layers[layer].arena +
+                                         (size_t)expert * h->span_bytes,
+                                     tmp, 1, c.hidden, c.inter, 1, nullptr);
+  if (e == cudaSuccess) e = cudaMemcpy(dst, tmp, h->span_bytes, cudaMemcpyDeviceToHost);
+  cudaFree(tmp);
+  if (e != cudaSuccess)
+    return fail(h, DF_MOE_ECUDA, "read-back failed: %s", cudaGetErrorString(e));
+  return DF_MOE_OK;
+}
+
+// ---- timing ------------------------------------------------------------------
+
+int df_moe_timing_enable(df_moe* h, int on) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  h->timing = on != 0;
+  return DF_MOE_OK;
+}
+
+static int drain(df_moe* h) {
+  for (auto& p : h->pending) {
+    CUDA_OR_FAIL(h, cudaEventSynchronize(p.b));
+    float ms = 0.f;
+    CUDA_OR_FAIL(h, cudaEventElapsedTime(&ms, p.a, p.b));
+    h->kind_ms[p.kind] += ms;
+    h->kind_n[p.kind] += 1;
+    h->event_pool.push_back(p.a);
+    h->event_pool.push_back(p.b);
+  }
+  h->pending.clear();
+  return DF_MOE_OK;
+}
+
+int df_moe_timing_reset(df_moe* h) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  int rc = drain(h);
+  for (int i = 0; i < K_NKINDS; ++i) { h->kind_ms[i] = 0; h->kind_n[i] = 0; }
+  return rc;
+}
+
+int df_moe_timing_get(df_moe* h, int kind, const char** name, int64_t* launches,
+                      double* total_ms) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  if (kind < 0 || kind >= K_NKINDS) return fail(h, DF_MOE_ERANGE, "bad kind");
+  int rc = drain(h);
+  if (rc) return rc;
+  if (name) *name = kKindNames[kind];
+  if (launches) *launches = h->kind_n[kind];
+  if (total_ms) *total_ms = h->kind_ms[kind];
+  return DF_MOE_OK;
+}
+
+int df_moe_last_launch_count(const df_moe* h) { return h ? h->launches : 0; }
+
+}  // extern "C"

@@ -279,15 +279,16 @@ int orc_moe_layer(const orc_layer* L, const uint16_t* x, int T,
 
 int orc_moe_stack(const orc_layer* layers, int nl, const uint16_t* x, int T,
                   double eps, uint16_t* x_out, double* last_f64, int32_t* ids,
-                  double* w) {
-  const int H = layers[0].H, k = layers[0].k;
+                  double* w, double* logits) {
+  const int H = layers[0].H, k = layers[0].k, E = layers[0].E;
   std::vector<uint16_t> cur(x, x + (size_t)T * H), xn((size_t)T * H);
   std::vector<double> out((size_t)T * H);
   for (int l = 0; l < nl; ++l) {
     orc_rmsnorm_bf16(cur.data(), T, H, eps, xn.data());
     int rc = orc_moe_layer(&layers[l], xn.data(), T, cur.data(), out.data(),
                            ids + (size_t)l * T * k, w + (size_t)l * T * k,
-                           nullptr, nullptr, nullptr);
+                           logits ? logits + (size_t)l * T * E : nullptr,
+                           nullptr, nullptr);
     if (rc) return rc;
     for (size_t j = 0; j < out.size(); ++j) cur[j] = orc_f64_to_bf16(out[j]);
   }

@@ -110,10 +110,10 @@ int orc_moe_layer(const orc_layer* L, const uint16_t* x, int T,
 
 /* Stack of nl layers: per layer xn = bf16(rmsnorm(x)); x = bf16(x + MoE(xn)).
  * x_out = final bf16 x; last_f64 = x + MoE(xn) of the last layer before
- * rounding; ids/w are [nl][T][k]. */
+ * rounding; ids/w are [nl][T][k]; logits (nullable) [nl][T][E]. */
 int orc_moe_stack(const orc_layer* layers, int nl, const uint16_t* x, int T,
                   double eps, uint16_t* x_out, double* last_f64, int32_t* ids,
-                  double* w);
+                  double* w, double* logits);
 
 int orc_num_threads(void);
 void orc_set_num_threads(int n);

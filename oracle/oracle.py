@@ -73,7 +73,7 @@ def lib():
                                     vp, vp, vp, vp]
         L.orc_moe_layer.restype = i32
         L.orc_moe_stack.argtypes = [ctypes.POINTER(_Layer), i32, vp, i32, dbl, vp,
-                                    vp, vp, vp]
+                                    vp, vp, vp, vp]
         L.orc_moe_stack.restype = i32
         L.orc_num_threads.restype = i32
         L.orc_set_num_threads.argtypes = [i32]
@@ -277,12 +277,14 @@ def moe_stack(layers, x_bf16, eps):
     T, nl = x.shape[0], len(layers)
     arr = (_Layer * nl)(*[l.s for l in layers])
     x_out = np.empty_like(x); last = np.empty((T, H))
+    E = layers[0].s.E
     ids = np.empty((nl, T, k), dtype=np.int32); w = np.empty((nl, T, k))
+    logits = np.empty((nl, T, E))
     rc = lib().orc_moe_stack(arr, nl, _p(x), T, eps, _p(x_out), _p(last), _p(ids),
-                             _p(w))
+                             _p(w), _p(logits))
     if rc:
         raise RuntimeError("oracle: an expert span was unavailable")
-    return dict(x=x_out, last=last, ids=ids, w=w)
+    return dict(x=x_out, last=last, ids=ids, w=w, logits=logits)
 
 
 def num_threads():

@@ -26,6 +26,11 @@ class Workload:
     eps: float = 1e-6
     steps: int = 1       # decode steps (stack workload)
     seed: int = 0
+    weights_cfg: int = -1  # generator key of the weights (-1: cfg_id)
+
+    @property
+    def wcfg(self):
+        return self.cfg_id if self.weights_cfg < 0 else self.weights_cfg
 
 
 K3 = dict(H=7168, I=1536, E=896, k=16, n_shared=2, Is=1536)
@@ -34,7 +39,8 @@ WORKLOADS = {
     0: Workload("tiny-h256-e8-top2", 0, H=256, I=64, E=8, k=2, n_shared=1,
                 Is=64, T=1),
     1: Workload("k3-layer-decode-b1", 1, T=1, **K3),
-    2: Workload("k3-layer-decode-b8", 2, T=8, **K3),
-    3: Workload("k3-layer-prefill-b512", 3, T=512, **K3),
+    # batch 8 and batch 512 run on the same K3 layer as batch 1
+    2: Workload("k3-layer-decode-b8", 2, T=8, weights_cfg=1, **K3),
+    3: Workload("k3-layer-prefill-b512", 3, T=512, weights_cfg=1, **K3),
     4: Workload("k3-stack8-decode", 4, T=1, L=8, stack=True, steps=64, **K3),
 }

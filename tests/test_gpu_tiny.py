@@ -1,0 +1,274 @@
+"""GPU parity on the tiny workload (H=256, I=64, 8 experts, top-2, one shared
+expert): every step of the hot path through the C ABI against the oracle,
+the whole layer, edge and degenerate cases, errors and determinism.
+
+Step tolerances: the kernels accumulate in fp32 over at most a few thousand
+products of exactly-representable weights, so a relative L2 error of 1e-5
+leaves a wide margin over fp32 rounding (~sqrt(K) * 2^-24 ~ 1e-6). The
+layer-output bar is the stated one: relative L2 <= 2e-3 and max-abs error
+<= 1e-2 x output RMS; ids bit-exact as sets, weights within 1e-5.
+"""
+import numpy as np
+import pytest
+
+import oracle as orc
+import synth
+from moe_setup import (Setup, bits_to_f64, check_ids_weights, check_out,
+                       draw_tokens, rel_l2, to_dev_bf16)
+
+pytestmark = pytest.mark.gpu
+
+WL = synth.WORKLOADS[0]
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as t
+    if not t.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return t
+
+
+@pytest.fixture(scope="module")
+def tiny(torch):
+    s = Setup(WL, max_tokens=16)
+    yield s
+    s.close()
+
+
+def test_device_generator_matches_host(torch):
+    n, H, I = 3, WL.H, WL.I
+    span = synth.span_bytes(H, I)
+    buf = torch.empty(n * span, dtype=torch.uint8, device="cuda")
+    synth.dev_expert_spans(WL.seed, WL.wcfg, 0, 2, n, H, I, buf.data_ptr(),
+                           torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    host = synth.expert_spans(WL.seed, WL.wcfg, 0, 2, n, H, I)
+    assert np.array_equal(buf.cpu().numpy().reshape(n, span), host)
+
+
+def test_layout_roundtrip(tiny):
+    span = tiny.m.span_bytes
+    assert span == synth.span_bytes(WL.H, WL.I)
+    for e in range(WL.E):
+        back = np.empty(span, dtype=np.uint8)
+        tiny.m.read_expert_span(0, e, back)
+        assert np.array_equal(back, tiny._span(0, e)), "expert %d" % e
+
+
+def test_router_step(tiny, torch):
+    x = draw_tokens(tiny, 5)
+    logits = torch.empty((5, WL.E), dtype=torch.float32, device="cuda")
+    tiny.m.step_router(0, to_dev_bf16(x), 5, logits)
+    torch.cuda.synchronize()
+    ref = orc.router_logits(tiny.routers[0], x)
+    assert np.max(np.abs(logits.cpu().double().numpy() - ref)) <= 1e-5
+
+
+def test_topk_step(tiny, torch):
+    rng = np.random.default_rng(11)
+    T = 9
+    lg = rng.standard_normal((T, WL.E)).astype(np.float32)
+    lg[0, :] = 0.5  # all tied: the lowest ids win, in order
+    ids = torch.empty((T, WL.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, WL.k), dtype=torch.float32, device="cuda")
+    tiny.m.step_topk(torch.from_numpy(lg).cuda(), T, ids, w)
+    torch.cuda.synchronize()
+    rid, rw = orc.topk_softmax(lg.astype(np.float64), WL.k)
+    assert np.array_equal(ids.cpu().numpy(), rid)  # order too: same fp32 inputs
+    assert np.max(np.abs(w.cpu().double().numpy() - rw)) <= 1e-6
+
+
+@pytest.mark.parametrize("T", [1, 2, 9, 16])
+def test_group_step(tiny, torch, T):
+    rng = np.random.default_rng(T)
+    ids = np.stack([rng.permutation(WL.E)[:WL.k] for _ in range(T)]).astype(np.int32)
+    offs = torch.empty(WL.E + 1, dtype=torch.int32, device="cuda")
+    tok = torch.empty(T * WL.k, dtype=torch.int32, device="cuda")
+    slot = torch.empty(T * WL.k, dtype=torch.int32, device="cuda")
+    nu = torch.empty(1, dtype=torch.int32, device="cuda")
+    tiny.m.step_group(torch.from_numpy(ids).cuda(), T, offs, tok, slot, nu)
+    torch.cuda.synchronize()
+    roffs, rtok, rslot, rn = orc.group(ids, WL.E)
+    assert np.array_equal(offs.cpu().numpy(), roffs)
+    assert np.array_equal(tok.cpu().numpy(), rtok)
+    assert np.array_equal(slot.cpu().numpy(), rslot)
+    assert nu.item() == rn
+
+
+def _oracle_route(tiny, x):
+    return orc.topk_softmax(orc.router_logits(tiny.routers[0], x), WL.k)
+
+
+@pytest.mark.parametrize("T", [1, 3])
+def test_gateup_step(tiny, torch, T):
+    x = draw_tokens(tiny, T, first_id=100)
+    rid, _ = _oracle_route(tiny, x)
+    hbuf = torch.empty((T * WL.k, WL.I), dtype=torch.float32, device="cuda")
+    tiny.m.step_expert_gateup(0, to_dev_bf16(x), T, torch.from_numpy(rid).cuda(), hbuf)
+    torch.cuda.synchronize()
+    got = hbuf.cpu().double().numpy()
+    for t in range(T):
+        for j in range(WL.k):
+            ref = orc.expert_gateup(tiny._span(0, rid[t, j]), WL.H, WL.I, bits_to_f64(x[t]))
+            assert rel_l2(got[t * WL.k + j], ref) <= 1e-5
+
+
+@pytest.mark.parametrize("T", [1, 3])
+def test_down_step(tiny, torch, T):
+    x = draw_tokens(tiny, T, first_id=200)
+    rid, rw = _oracle_route(tiny, x)
+    h = np.stack([orc.expert_gateup(tiny._span(0, rid[t, j]), WL.H, WL.I, bits_to_f64(x[t]))
+                  for t in range(T) for j in range(WL.k)]).astype(np.float32)
+    y = torch.empty((T, WL.H), dtype=torch.float32, device="cuda")
+    tiny.m.step_expert_down(0, torch.from_numpy(h).cuda(), T, torch.from_numpy(rid).cuda(),
+                            torch.from_numpy(rw.astype(np.float32)).cuda(), y)
+    torch.cuda.synchronize()
+    got = y.cpu().double().numpy()
+    for t in range(T):
+        ref = sum(np.float64(np.float32(rw[t, j])) *
+                  orc.expert_down(tiny._span(0, rid[t, j]), WL.H, WL.I,
+                                  h[t * WL.k + j].astype(np.float64))
+                  for j in range(WL.k))
+        assert rel_l2(got[t], ref) <= 1e-5
+
+
+def test_shared_step(tiny, torch):
+    x = draw_tokens(tiny, 2, first_id=300)
+    y = torch.empty((2, WL.H), dtype=torch.float32, device="cuda")
+    tiny.m.step_shared(0, to_dev_bf16(x), 2, y)
+    torch.cuda.synchronize()
+    for t in range(2):
+        ref = sum(orc.shared_ffn(*s, bits_to_f64(x[t])) for s in tiny.shared[0])
+        assert rel_l2(y.cpu().double().numpy()[t], ref) <= 1e-5
+
+
+def _forward(m, x, T, torch, residual=None, L=1, k=WL.k, H=WL.H):
+    out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    out32 = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    ids = torch.empty((L, T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((L, T, k), dtype=torch.float32, device="cuda")
+    m.forward(to_dev_bf16(x), T, out, ids, w, out_f32=out32,
+              residual=None if residual is None else to_dev_bf16(residual))
+    m.sync()
+    return (out.cpu().numpy().view(np.uint16), out32.cpu().double().numpy(),
+            ids.cpu().numpy(), w.cpu().double().numpy())
+
+
+@pytest.mark.parametrize("T", [1, 2, 7, 16])
+def test_forward_matches_oracle(tiny, torch, T):
+    x = draw_tokens(tiny, T, first_id=1000 + 20 * T)
+    res = np.stack([synth.token(WL.seed, WL.cfg_id, 5000 + t, WL.H,
+                                kind=synth.gen.KIND_RESIDUAL) for t in range(T)])
+    out, out32, ids, w = _forward(tiny.m, x, T, torch, residual=res)
+    ref = orc.moe_layer(tiny.layers[0], x, residual=res)
+    check_ids_weights(ids[0], w[0], ref["ids"], ref["w"])
+    check_out(out32, ref["out"])
+    # the bf16 output is the RNE rounding of the fp32 output
+    rne = torch.from_numpy(out32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(out, rne)
+
+
+def test_forward_host_buffers(tiny, torch):
+    T = 3
+    x = draw_tokens(tiny, T, first_id=7000)
+    out = np.empty((T, WL.H), dtype=np.uint16)
+    out32 = np.empty((T, WL.H), dtype=np.float32)
+    ids = np.empty((T, WL.k), dtype=np.int32)
+    w = np.empty((T, WL.k), dtype=np.float32)
+    tiny.m.forward_host(x, T, out, ids=ids, weights=w, out_f32=out32)
+    ref = orc.moe_layer(tiny.layers[0], x)
+    check_ids_weights(ids, w, ref["ids"], ref["w"])
+    check_out(out32, ref["out"])
+
+
+def test_forward_is_deterministic(tiny, torch):
+    x = draw_tokens(tiny, 16, first_id=8000)
+    a = _forward(tiny.m, x, 16, torch)
+    b = _forward(tiny.m, x, 16, torch)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+
+
+def test_errors(tiny, torch):
+    import mxfp4_routed_expert_top_gb300 as dfm
+    x = to_dev_bf16(draw_tokens(tiny, 1, first_id=9000))
+    out = torch.empty((1, WL.H), dtype=torch.int16, device="cuda")
+    ids = torch.empty((1, WL.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((1, WL.k), dtype=torch.float32, device="cuda")
+    for T in (0, 17, -1):
+        with pytest.raises(dfm.DfMoeError) as ei:
+            tiny.m.forward(x, T, out, ids, w)
+        assert ei.value.code == -5
+    with pytest.raises(dfm.DfMoeError) as ei:
+        tiny.m.forward(x, 1, None, ids, w)
+    assert ei.value.code == -1
+    with dfm.MoE(WL.H, WL.E, WL.k, WL.I, WL.n_shared, WL.Is) as fresh:
+        with pytest.raises(dfm.DfMoeError) as ei:
+            fresh.forward(x, 1, out, ids, w)
+        assert ei.value.code == -4  # nothing loaded yet
+        with pytest.raises(dfm.DfMoeError) as ei:
+            fresh.load_experts(1, router=tiny.routers[0])
+        assert ei.value.code == -5  # no layer 1
+    with pytest.raises(dfm.DfMoeError) as ei:
+        dfm.MoE(WL.H + 1, WL.E, WL.k, WL.I, WL.n_shared, WL.Is)
+    assert ei.value.code == -1
+
+
+def _host_handle(torch, spans, router, shared, k=WL.k, n_shared=WL.n_shared, T=4):
+    import mxfp4_routed_expert_top_gb300 as dfm
+    m = dfm.MoE(WL.H, WL.E, k, WL.I, n_shared, WL.Is, max_tokens=T)
+    m.load_experts(0, router=router, experts=spans, expert_begin=0, expert_count=WL.E,
+                   shared=shared if n_shared else None)
+    return m
+
+
+def test_all_zero_codes_leave_shared_only(tiny, torch):
+    spans = synth.expert_spans(WL.seed, WL.wcfg, 0, 0, WL.E, WL.H, WL.I)
+    q = WL.H * WL.I // 2
+    s = WL.H * WL.I // 32
+    for e in range(WL.E):
+        spans[e, 0:q] = 0
+        spans[e, q + s:2 * q + s] = 0
+        spans[e, 2 * q + 2 * s:3 * q + 2 * s] = 0
+    x = draw_tokens(tiny, 2, first_id=9100)
+    with _host_handle(torch, spans, tiny.routers[0], tiny.shared[0]) as m:
+        out, out32, ids, w = _forward(m, x, 2, torch)
+    for t in range(2):
+        ref = orc.shared_ffn(*tiny.shared[0][0], bits_to_f64(x[t]))
+        assert rel_l2(out32[t], ref) <= 1e-5
+
+
+def test_single_nonzero_code_pins_nibble_order(tiny, torch):
+    # one gate weight and one up weight non-zero: g and u each pick one x
+    spans = np.zeros((WL.E, synth.span_bytes(WL.H, WL.I)), dtype=np.uint8)
+    q, s = WL.H * WL.I // 2, WL.H * WL.I // 32
+    spans[:, q:q + s] = 127
+    spans[:, 2 * q + s:2 * q + 2 * s] = 127
+    spans[:, 3 * q + 2 * s:] = 127
+    row, col = 5, 33  # odd column -> high nibble
+    for e in range(WL.E):
+        spans[e, row * (WL.H // 2) + col // 2] = 0x20          # gate[5][33] = 1.0
+        spans[e, q + s + row * (WL.H // 2) + col // 2] = 0x20  # up[5][33] = 1.0
+        # down[9][5] = 1.0 (even column -> low nibble)
+        spans[e, 2 * q + 2 * s + 9 * (WL.I // 2) + 5 // 2] = 0x20 if 5 % 2 else 0x02
+    x = draw_tokens(tiny, 1, first_id=9200)
+    with _host_handle(torch, spans, tiny.routers[0], None, n_shared=0) as m:
+        out, out32, ids, w = _forward(m, x, 1, torch)
+    xv = bits_to_f64(x[0])[col]
+    h = xv / (1 + np.exp(-xv)) * xv
+    expect = np.zeros(WL.H)
+    expect[9] = h  # every expert gives the same y; weights sum to 1
+    assert np.allclose(out32[0], expect, rtol=1e-5, atol=1e-6 * abs(h) + 1e-30)
+
+
+def test_k_equals_e_and_no_shared(tiny, torch):
+    spans = synth.expert_spans(WL.seed, WL.wcfg, 0, 0, WL.E, WL.H, WL.I)
+    x = draw_tokens(tiny, 2, first_id=9300)
+    with _host_handle(torch, spans, tiny.routers[0], None, k=WL.E, n_shared=0) as m:
+        out, out32, ids, w = _forward(m, x, 2, torch, k=WL.E)
+    L = orc.Layer(WL.H, WL.E, WL.E, WL.I, WL.Is, tiny.routers[0], [],
+                  lambda l, e: spans[e])
+    ref = orc.moe_layer(L, x)
+    check_ids_weights(ids[0], w[0], ref["ids"], ref["w"])
+    check_out(out32, ref["out"])
