@@ -200,6 +200,36 @@ DF_MOE_API int df_moe_timing_get(df_moe* h, int kind, const char** name,
 /* Kernels launched by the last forward call. */
 DF_MOE_API int df_moe_last_launch_count(const df_moe* h);
 
+/* ---- routing without any allocation ---------------------------------------
+ * No counterpart in the pages: an addition for callers that must not
+ * allocate device memory, such as a serving engine that has already divided
+ * all of HBM among its own pools, or a decode loop that cannot afford the
+ * device-wide synchronisation a cudaMalloc/cudaFree may cause. It needs no
+ * handle.
+ *
+ * Router GEMV + top-k + softmax over the selected logits (the same kernels
+ * and the same results as df_moe_step_router followed by df_moe_step_topk),
+ * with the partial-logit scratch in a fixed 1 MiB array of device memory that
+ * is part of the library: every GPU that loads the library holds it until the
+ * process exits. The call allocates nothing (no cudaMalloc/cudaFree, no
+ * allocating library routine).
+ *   router  device [E][H] fp32      x_bf16  device [T][H] bf16
+ *   ids     device [T][k] int32     weights device [T][k] fp32
+ * Limits: H a multiple of 32 up to 8192, 1 <= E <= 1024, 1 <= k <=
+ * min(E, 32), and the scratch must hold nsplit*T*E floats (262,144 floats;
+ * nsplit is the router's column split, 3 at H = 7168 and E = 896, so T <= 97
+ * there). Larger calls fail with DF_MOE_ERANGE and a message from
+ * df_moe_last_error(NULL); nothing is launched then.
+ * The first call on each device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any stream
+ * capture. All calls share the one array: calls that overlap on the GPU (on
+ * different streams, or from different threads) race and must be ordered by
+ * the caller. Nothing in it needs clearing between calls: each call writes
+ * every scratch element it later reads. */
+DF_MOE_API int df_moe_route_noalloc(const float* router, int32_t E, int32_t H,
+                                    const void* x_bf16, int32_t T, int32_t k,
+                                    int32_t* ids, float* weights, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,7 @@ SYMBOLS = [
     "df_moe_step_expert_gateup", "df_moe_step_expert_down",
     "df_moe_step_shared", "df_moe_step_rmsnorm", "df_moe_read_expert_span",
     "df_moe_timing_enable", "df_moe_timing_reset", "df_moe_timing_get",
-    "df_moe_last_launch_count",
+    "df_moe_last_launch_count", "df_moe_route_noalloc",
 ]
 
 
@@ -86,6 +86,7 @@ def lib():
         L.df_moe_timing_get.argtypes = [vp, ctypes.c_int, ctypes.POINTER(ctypes.c_char_p),
                                         ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]
         L.df_moe_last_launch_count.argtypes = [vp]
+        L.df_moe_route_noalloc.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, vp]
         for name in SYMBOLS:
             f = getattr(L, name)
             if f.restype is ctypes.c_int:  # default
@@ -96,6 +97,16 @@ def lib():
 
 def span_bytes_for(H, I):
     return lib().df_moe_span_bytes_for(H, I)
+
+
+def route_noalloc(router, E, H, x, T, k, ids, weights, stream=None):
+    """Router + top-k with no device allocation (df_moe_route_noalloc): for
+    callers that must not allocate, e.g. an engine whose memory pools already
+    own all of HBM. Same kernels and results as step_router + step_topk."""
+    rc = lib().df_moe_route_noalloc(_ptr(router), E, H, _ptr(x), T, k, _ptr(ids),
+                                    _ptr(weights), _stream(stream))
+    if rc != OK:
+        raise DfMoeError(rc, lib().df_moe_last_error(None).decode())
 
 
 def _ptr(a):

@@ -706,3 +706,7 @@ int df_moe_timing_get(df_moe* h, int kind, const char** name, int64_t* launches,
 int df_moe_last_launch_count(const df_moe* h) { return h ? h->launches : 0; }
 
 }  // extern "C"
+
+namespace dfm {
+void set_thread_error(const char* msg) { g_thread_err = msg; }
+}  // namespace dfm

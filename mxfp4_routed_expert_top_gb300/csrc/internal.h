@@ -69,6 +69,9 @@ enum KernelKind {
 // Error word bits written by device-side checks.
 enum : uint32_t { DEV_ERR_RANGE = 1u, DEV_ERR_TIMEOUT = 2u };
 
+// Message returned by df_moe_last_error(NULL) on this thread.
+void set_thread_error(const char* msg);
+
 // ---- launchers (each returns cudaGetLastError()) ---------------------------
 // Router K-split: partial logits of `nsplit` column ranges of `split_len`.
 struct RouterSplit { int split_len, nsplit; };
