@@ -217,7 +217,7 @@ DF_MOE_API int df_moe_last_launch_count(const df_moe* h);
  *   ids     device [T][k] int32     weights device [T][k] fp32
  * Limits: H a multiple of 32 up to 8192, 1 <= E <= 1024, 1 <= k <=
  * min(E, 32), and the scratch must hold nsplit*T*E floats (262,144 floats;
- * nsplit is the router's column split, 3 at H = 7168 and E = 896, so T <= 97
+ * nsplit is the router's column split, 4 at H = 7168 and E = 896, so T <= 73
  * there). Larger calls fail with DF_MOE_ERANGE and a message from
  * df_moe_last_error(NULL); nothing is launched then.
  * The first call on each device looks up the array's device address (with

@@ -4,6 +4,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -63,6 +64,7 @@ struct df_moe {
   uint16_t* xbuf[2] = {nullptr, nullptr};  // [Tmax][H] stack ping-pong
   uint16_t* xn = nullptr;        // [Tmax][H]
   uint32_t* err = nullptr;       // device error word
+  unsigned int* counter = nullptr;  // router blocks done (zero between calls)
   // host-API device buffers
   uint16_t* hx = nullptr;
   uint16_t* hres = nullptr;
@@ -176,9 +178,17 @@ int route(df_moe* h, int l, const uint16_t* x, int T, int32_t* ids, float* w,
           cudaStream_t s, float* logits_out, int tg) {
   const df_moe_config& c = h->cfg;
   const LayerBufs& L = h->layers[l];
+  const bool direct = (T == 1 && tg == 1);
+  if (direct && !logits_out) {
+    // one token: the router's last block selects the experts and writes the
+    // work items (no separate top-k launch)
+    const RouterFuse fz{h->counter, c.top_k, ids, w, h->items, h->n_items, h->sorted};
+    RUN(h, K_ROUTER, s, launch_router(L.router, c.n_experts, c.hidden, x, T,
+                                      h->router_part, h->rsplit, s, &fz));
+    return DF_MOE_OK;
+  }
   RUN(h, K_ROUTER, s, launch_router(L.router, c.n_experts, c.hidden, x, T,
                                     h->router_part, h->rsplit, s));
-  const bool direct = (T == 1 && tg == 1);
   RUN(h, K_TOPK, s, launch_topk(h->router_part, h->rsplit.nsplit, T,
                                 c.n_experts, c.top_k, logits_out, ids, w,
                                 direct ? h->items : nullptr, h->n_items,
@@ -195,9 +205,9 @@ int shared_part(df_moe* h, int l, const uint16_t* x, int T, float* ysh,
   const df_moe_config& c = h->cfg;
   const LayerBufs& L = h->layers[l];
   RUN(h, K_SHARED_GU, s, launch_shared_gateup(L.sh_gate, L.sh_up, h->R,
-                                              c.hidden, x, T, h->hsh, s));
+                                              c.hidden, x, T, h->hsh, h->err, s));
   RUN(h, K_SHARED_DN, s, launch_shared_down(L.sh_down, c.hidden, h->R, h->hsh,
-                                            T, ysh, s));
+                                            T, ysh, h->err, s));
   return DF_MOE_OK;
 }
 
@@ -207,20 +217,20 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
                   int32_t* ids, float* w, cudaStream_t s) {
   const df_moe_config& c = h->cfg;
   const LayerBufs& L = h->layers[l];
-  const int tg = T == 1 ? 1 : 2;
+  const int tg = T == 1 ? 1 : kOneItemPerExpert;
   int rc = route(h, l, x, T, ids, w, s, nullptr, tg);
   if (rc) return rc;
   if (c.n_shared > 0) {
     rc = shared_part(h, l, x, T, h->ysh, s);
     if (rc) return rc;
   }
-  const int max_items = (T == 1 && tg == 1) ? c.top_k : T * c.top_k;
+  const int max_items = (T == 1 && tg == 1) ? c.top_k : std::min(T * c.top_k, c.n_experts);
   RUN(h, K_GATEUP, s, launch_gateup(L.arena, h->span_bytes, c.hidden, c.inter,
                                     c.top_k, x, h->items, h->n_items, max_items,
-                                    h->sorted, h->hbuf, tg, s));
+                                    h->sorted, h->hbuf, tg, h->err, s));
   RUN(h, K_DOWN, s, launch_down(L.arena, h->span_bytes, c.hidden, c.inter,
                                 h->items, h->n_items, max_items, h->sorted,
-                                h->hbuf, h->part, tg, s));
+                                h->hbuf, h->part, tg, h->err, s));
   RUN(h, K_COMBINE, s, launch_combine(h->part, w, T, c.top_k, c.hidden,
                                       c.n_shared > 0 ? h->ysh : nullptr,
                                       residual, out_f32, out_bf16, s));
@@ -334,13 +344,15 @@ int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
   if (!rc) rc = dalloc(h, &h->xbuf[1], Tm * H);
   if (!rc) rc = dalloc(h, &h->xn, Tm * H);
   if (!rc) rc = dalloc(h, &h->err, 1);
+  if (!rc) rc = dalloc(h, &h->counter, 1);
   if (!rc) rc = dalloc(h, &h->hx, Tm * H);
   if (!rc) rc = dalloc(h, &h->hres, Tm * H);
   if (!rc) rc = dalloc(h, &h->hout, Tm * H);
   if (!rc) rc = dalloc(h, &h->hout32, Tm * H);
   if (!rc) rc = dalloc(h, &h->hids, (size_t)c.n_layers * Tm * k);
   if (!rc) rc = dalloc(h, &h->hw, (size_t)c.n_layers * Tm * k);
-  if (!rc && cudaMemset(h->err, 0, sizeof(uint32_t)) != cudaSuccess)
+  if (!rc && (cudaMemset(h->err, 0, sizeof(uint32_t)) != cudaSuccess ||
+              cudaMemset(h->counter, 0, sizeof(unsigned int)) != cudaSuccess))
     rc = fail(h, DF_MOE_ECUDA, "cudaMemset failed");
   if (rc) {
     g_thread_err = h->last_error;
@@ -530,7 +542,7 @@ int df_moe_step_router(df_moe* h, int32_t layer, const void* x_bf16, int32_t T,
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
   cudaStream_t s = (cudaStream_t)stream;
   return route(h, layer, (const uint16_t*)x_bf16, T, h->ids_ws, h->w_ws, s,
-               logits, 1 + (T > 1));
+               logits, T == 1 ? 1 : kOneItemPerExpert);
 }
 
 int df_moe_step_topk(df_moe* h, const float* logits, int32_t T, int32_t* ids,
@@ -559,7 +571,7 @@ int df_moe_step_group(df_moe* h, const int32_t* ids, int32_t T, int32_t* offs,
   cudaStream_t s = (cudaStream_t)stream;
   RUN(h, K_GROUP, s, launch_group(ids, T, c.top_k, c.n_experts, offs, tok, slot,
                                   n_union, h->items, h->n_items, h->sorted,
-                                  T == 1 ? 1 : 2, s));
+                                  kOneItemPerExpert, s));
   return DF_MOE_OK;
 }
 
@@ -575,14 +587,14 @@ int df_moe_step_expert_gateup(df_moe* h, int32_t layer, const void* x_bf16,
     return fail(h, DF_MOE_ESTATE, "experts not loaded");
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
   cudaStream_t s = (cudaStream_t)stream;
-  const int tg = T == 1 ? 1 : 2;
+  const int tg = kOneItemPerExpert;
   RUN(h, K_GROUP, s, launch_group(ids, T, c.top_k, c.n_experts, nullptr, nullptr,
                                   nullptr, nullptr, h->items, h->n_items,
                                   h->sorted, tg, s));
   RUN(h, K_GATEUP, s, launch_gateup(h->layers[layer].arena, h->span_bytes,
                                     c.hidden, c.inter, c.top_k,
                                     (const uint16_t*)x_bf16, h->items, h->n_items,
-                                    T * c.top_k, h->sorted, hbuf, tg, s));
+                                    std::min(T * c.top_k, c.n_experts), h->sorted, hbuf, tg, h->err, s));
   return DF_MOE_OK;
 }
 
@@ -598,13 +610,14 @@ int df_moe_step_expert_down(df_moe* h, int32_t layer, const float* hbuf,
     return fail(h, DF_MOE_ESTATE, "experts not loaded");
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
   cudaStream_t s = (cudaStream_t)stream;
-  const int tg = T == 1 ? 1 : 2;
+  const int tg = kOneItemPerExpert;
   RUN(h, K_GROUP, s, launch_group(ids, T, c.top_k, c.n_experts, nullptr, nullptr,
                                   nullptr, nullptr, h->items, h->n_items,
                                   h->sorted, tg, s));
   RUN(h, K_DOWN, s, launch_down(h->layers[layer].arena, h->span_bytes, c.hidden,
-                                c.inter, h->items, h->n_items, T * c.top_k,
-                                h->sorted, hbuf, h->part, tg, s));
+                                c.inter, h->items, h->n_items,
+                                std::min(T * c.top_k, c.n_experts), h->sorted,
+                                hbuf, h->part, tg, h->err, s));
   RUN(h, K_COMBINE, s, launch_combine(h->part, weights, T, c.top_k, c.hidden,
                                       nullptr, nullptr, y, nullptr, s));
   return DF_MOE_OK;

@@ -2,34 +2,48 @@
 // with SwiGLU epilogue, down GEMV, and the weighted combine.
 //
 // The operation is the Deltafin README's fused MXFP4 dequant+GEMV ("Techniques
-// / Compute": decode the 4-bit weights and multiply in one pass, apply the
-// e8m0 scale on the exponent), restated for HBM streaming on sm_103a:
-//   * one 16-byte load per lane = one 32-element MX block of one row;
-//   * E2M1 pairs decoded in registers by the hardware cvt (e2m1x2 -> f16x2);
-//   * the 32 products of a block are summed in fp32 and the block's scale
-//     2^(s-127) is applied once to the block sum (exact: a power of two);
-//   * x for a lane's block stays in registers across the 32 rows of a group.
+// / Compute": decode the 4-bit weights and multiply in one pass, the e8m0
+// scale applied on the exponent), restated for HBM streaming on sm_103a.
+//
+// Why the tensor cores: at the HBM rate GB300 streams ~12.8 T MXFP4 weights/s
+// against ~40 T lane-instructions/s of issue, i.e. about three instructions
+// per weight for everything. A CUDA-core decode + fp32 FMA needs 3.75 (ncu),
+// which makes the GEMV issue-bound. Here a warp decodes E2M1 pairs straight
+// into m16n8k16 A fragments (one hardware cvt per 2 weights) and the tokens
+// ride in the N = 8 columns; the contraction itself costs one warp
+// instruction per 256 weights.
+//
+//   * Persistent CTAs; a CTA holds NS "slots" = one producer warp + one
+//     consumer warp per 512-column chunk. A slot owns a contiguous range of
+//     tiles (16 rows x K of one expert).
+//   * The producer streams each tile's codes (8K bytes) and scales (K/2)
+//     with cp.async.bulk into a shared-memory ring (mbarriers, bounded waits).
+//   * Consumers: one 16-byte lds per lane = its A fragments for 4 k-steps;
+//     every 32-column MX block is accumulated by two MMAs into a temporary
+//     that is scaled by 2^(s-127) (per row) in fp32 and added to the result.
+//   * B (x) fragments live in registers as f16: the gate/up input is bf16,
+//     exact in f16 except |x| < 2^-17 (error <= 2^-25). The down input h
+//     (fp32, |h| up to ~1e5) is scaled per (token, chunk) by a power of two
+//     into f16 range and split into hi and lo columns (~22 bits).
+//   * An item (one expert and all its tokens) is processed in token groups of
+//     8 (gate/up) or 4 (down) against the tile already in shared memory, so
+//     each expert's weights cross HBM once per call.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
-#include <cuda_bf16.h>
-
 #include "internal.h"
+#include "pipeline.cuh"
 
 namespace dfm {
 namespace {
 
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
+constexpr int kMaxWarps = 16;
+constexpr int kMaxStages = 8;
+constexpr int kRedRing = 4;  // epilogue reduction ring depth
+constexpr size_t kSmemBudget = 200 * 1024;
 
-__device__ __forceinline__ float e8m0_to_f32(uint32_t e) {
-  // 2^(e-127): normal for 1..254, 2^-127 (subnormal) for 0, NaN for 255
-  uint32_t bits = e == 0 ? 0x00400000u : (e == 255 ? 0x7FC00000u : e << 23);
-  return __uint_as_float(bits);
+__device__ __forceinline__ float pow2i(int s) {  // 2^s for s in [-126, 127]
+  return __uint_as_float((uint32_t)(127 + s) << 23);
 }
 
 // Four bytes = eight E2M1 codes -> four f16x2 (low nibble in the low half).
@@ -44,215 +58,327 @@ __device__ __forceinline__ void decode_word(uint32_t w, uint32_t (&h)[4]) {
       : "r"(w));
 }
 
-__device__ __forceinline__ float2 h2_to_f2(uint32_t h) {
-  float a, b;
-  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
-      "cvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
-      : "=f"(a), "=f"(b)
-      : "r"(h));
-  return make_float2(a, b);
+// d = A * B (+ c): m16n8k16, f16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4],
+                                         uint32_t b0, uint32_t b1,
+                                         const float (&c)[4]) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1),
+        "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
 }
 
-// Sum over the 32 elements of one block: sum_j E2M1(q_j) * x_j (unscaled).
-__device__ __forceinline__ float block_dot(const uint4 q, const float (&x)[32]) {
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-  float d0 = 0.f, d1 = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t h[4];
-    decode_word(w[i], h);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float2 f = h2_to_f2(h[j]);
-      d0 = fmaf(f.x, x[8 * i + 2 * j], d0);
-      d1 = fmaf(f.y, x[8 * i + 2 * j + 1], d1);
-    }
-  }
-  return d0 + d1;
-}
-
-// Transpose-reduce over the 16 lanes of a half-warp: on entry lane b holds
-// v[p] = partial of pair p; on exit v[0] = sum over the 16 lanes of pair b.
-__device__ __forceinline__ float halfwarp_transpose_reduce(float (&v)[16],
-                                                           int b) {
-#pragma unroll
-  for (int m = 8, n = 8; m >= 1; m >>= 1, n >>= 1) {
-    const bool upper = (b & m) != 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (i < n) {
-        float send = upper ? v[i] : v[i + n];
-        float keep = upper ? v[i + n] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-      }
-    }
-  }
-  return v[0];
-}
-
-// One warp: the 16 pairs of group G, chunk c of an MXFP4 matrix in the
-// pair-chunk layout, against TG right-hand sides held in registers. On exit
-// acc[t][p] holds this lane's partial of pair p (row 2p + r of the group).
-template <int TG>
-__device__ __forceinline__ void mx_group_chunk(const uint8_t* __restrict__ codes,
-                                               const uint8_t* __restrict__ scales,
-                                               int K, int G, int c, int lane,
-                                               const float (&x)[TG][32],
-                                               float (&acc)[TG][16]) {
-  const int r = lane >> 4, b = lane & 15;
-  const int nbc = mx_nbc(K, c);
-#pragma unroll
-  for (int t = 0; t < TG; ++t)
-#pragma unroll
-    for (int p = 0; p < 16; ++p) acc[t][p] = 0.f;
-  if (b >= nbc) return;
-  const size_t lane_off = (size_t)(c << 9) + (size_t)((r * nbc + b) << 4);
-  const uint4 s16 = ldg_stream(scales + (size_t)G * 32 * mx_nb(K) + lane_off);
-  const uint32_t sw[4] = {s16.x, s16.y, s16.z, s16.w};
-  const uint8_t* cp = codes + (size_t)(16 * G) * K + lane_off;
-#pragma unroll
-  for (int p0 = 0; p0 < 16; p0 += 8) {
-    uint4 q[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) q[u] = ldg_stream(cp + (size_t)(p0 + u) * K);
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int p = p0 + u;
-      const float sc = e8m0_to_f32((sw[p >> 2] >> (8 * (p & 3))) & 0xFFu);
-#pragma unroll
-      for (int t = 0; t < TG; ++t) acc[t][p] = block_dot(q[u], x[t]) * sc;
-    }
-  }
+__device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
-constexpr int kMaxChunkWarps = 16;  // K up to 8192
+struct MxvArgs {
+  const uint8_t* arena;
+  size_t span_bytes;
+  int H, I, k;
+  const uint16_t* x;      // gate/up input, bf16 [T][H]
+  const float* hin;       // down input, fp32 [T*k][I]
+  const Item* items;
+  const int32_t* n_items;
+  const int32_t* sorted;
+  float* out;             // gate/up: h [T*k][I]; down: part [T*k][H]
+  uint32_t* err;
+};
 
-// ---------------------------------------------------------------------------
-// gate/up: grid (I/16 groups, items). Block = one warp per K-chunk of H.
-// Output hbuf[a][16G + p] = silu(g) * u for each assignment a of the item.
-// ---------------------------------------------------------------------------
-template <int TG>
-__global__ void __launch_bounds__(kMaxChunkWarps * 32)
-gateup_kernel(const uint8_t* __restrict__ arena, size_t span_bytes, int H,
-              int I, int k, const uint16_t* __restrict__ x,
-              const Item* __restrict__ items, const int32_t* __restrict__ n_items,
-              const int32_t* __restrict__ sorted, float* __restrict__ hbuf) {
-  if ((int)blockIdx.y >= *n_items) return;
-  const Item it = items[blockIdx.y];
-  const int G = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = warp;
-  const SpanLayout L = span_layout(H, I);
-  const uint8_t* span = arena + (size_t)it.e * span_bytes;
-  const int b = lane & 15;
-  const bool act = b < mx_nbc(H, c);
+__host__ __device__ inline size_t align128(size_t v) { return (v + 127) & ~(size_t)127; }
 
-  int a_t[TG];
-  float xr[TG][32];
-#pragma unroll
-  for (int t = 0; t < TG; ++t) {
-    a_t[t] = t < it.cnt ? sorted[it.pos + t] : -1;
-    if (a_t[t] >= 0 && act) {
-      const uint16_t* xp = x + (size_t)(a_t[t] / k) * H + (size_t)(16 * c + b) * 32;
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        uint4 q = *reinterpret_cast<const uint4*>(xp + 8 * v);
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          xr[t][8 * v + 2 * j] = __uint_as_float(w[j] << 16);
-          xr[t][8 * v + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) xr[t][j] = 0.f;
-    }
-  }
-  float acc[TG][16];
-  mx_group_chunk<TG>(span + L.gu_codes, span + L.gu_scales, H, G, c, lane, xr, acc);
+struct SlotGeom {
+  int stages;
+  size_t stage_bytes, red_bytes, bytes;
+};
 
-  __shared__ float red[kMaxChunkWarps][kMaxTG][32];
-#pragma unroll
-  for (int t = 0; t < TG; ++t) {
-    float s = halfwarp_transpose_reduce(acc[t], lane & 15);
-    red[warp][t][lane] = s;  // lane = 16 r + pair
-  }
-  __syncthreads();
-  const int nw = blockDim.x >> 5;
-  for (int o = threadIdx.x; o < TG * 16; o += blockDim.x) {
-    const int t = o >> 4, p = o & 15;
-    const int a = t < it.cnt ? sorted[it.pos + t] : -1;
-    if (a >= 0) {
-      float g = 0.f, u = 0.f;
-      for (int w = 0; w < nw; ++w) { g += red[w][t][p]; u += red[w][t][16 + p]; }
-      hbuf[(size_t)a * I + 16 * G + p] = silu_f(g) * u;
-    }
-  }
+__host__ __device__ inline SlotGeom slot_geom(int K, int NS) {
+  SlotGeom g;
+  const int NCH = mx_nchunks(K);
+  g.stage_bytes = (size_t)8 * K + K / 2;
+  g.red_bytes = (size_t)kRedRing * NCH * 32 * 16;
+  const size_t fixed = g.red_bytes + (2 * kMaxStages + 2 * kRedRing) * 8;
+  const size_t per_slot = kSmemBudget / NS;
+  int st = (int)((per_slot > fixed ? per_slot - fixed : 0) / g.stage_bytes);
+  g.stages = st < 2 ? 2 : (st > kMaxStages ? kMaxStages : st);
+  g.bytes = align128((size_t)g.stages * g.stage_bytes + fixed);
+  return g;
 }
 
-// ---------------------------------------------------------------------------
-// down: grid (H/32 groups, items). Block = one warp per K-chunk of I.
-// Output part[a][32G + 2p + r] = (Wd_e h_a) for each assignment a.
-// ---------------------------------------------------------------------------
-template <int TG>
-__global__ void __launch_bounds__(kMaxChunkWarps * 32)
-down_kernel(const uint8_t* __restrict__ arena, size_t span_bytes, int H, int I,
-            const Item* __restrict__ items, const int32_t* __restrict__ n_items,
-            const int32_t* __restrict__ sorted, const float* __restrict__ hbuf,
-            float* __restrict__ part) {
-  if ((int)blockIdx.y >= *n_items) return;
-  const Item it = items[blockIdx.y];
-  const int G = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int c = warp;
-  const SpanLayout L = span_layout(H, I);
-  const uint8_t* span = arena + (size_t)it.e * span_bytes;
-  const int b = lane & 15;
-  const bool act = b < mx_nbc(I, c);
+__host__ __device__ inline int slots_per_cta(int K) {
+  const int NCH = mx_nchunks(K);
+  const int ns = kMaxWarps / (NCH + 1);
+  return ns > 0 ? ns : 1;
+}
 
-  int a_t[TG];
-  float xr[TG][32];
+// MODE 0: gate/up (K = H, 8 tokens per group), MODE 1: down (K = I, 4 tokens
+// per group, columns 2t / 2t+1 = hi / lo part of token t).
+template <int MODE>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) mxv_kernel(const MxvArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int GT = MODE == 0 ? 8 : 4;  // tokens per group
+  const int K = MODE == 0 ? a.H : a.I;
+  const int NCH = mx_nchunks(K);
+  const int wps = NCH + 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NS = (blockDim.x >> 5) / wps;
+  const int s = warp / wps, role = warp - s * wps;
+  const SlotGeom geo = slot_geom(K, NS);
+  const int S = geo.stages;
+  uint8_t* base = smem + (size_t)s * geo.bytes;
+  uint8_t* ring = base;
+  float* red = reinterpret_cast<float*>(base + (size_t)S * geo.stage_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(
+      reinterpret_cast<uint8_t*>(red) + geo.red_bytes);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* rfull = empty + kMaxStages;   // reduction entry written by all chunks
+  uint64_t* rempty = rfull + kRedRing;    // reduction entry read by its finalizer
+
+  if (role == NCH && lane == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], NCH);
+    }
+    for (int i = 0; i < kRedRing; ++i) {
+      mbar_init(&rfull[i], NCH);
+      mbar_init(&rempty[i], 1);
+    }
+  }
+  fence_barrier_init();
+  __syncthreads();
+
+  pdl_wait();  // items, x and h come from the preceding kernels
+  const SpanLayout L = span_layout(a.H, a.I);
+  const int tpi = MODE == 0 ? (2 * a.I) / 16 : a.H / 16;  // tiles per item
+  const int ntiles = *a.n_items * tpi;
+  const long long nslots = (long long)gridDim.x * NS;
+  const long long gs = (long long)blockIdx.x * NS + s;
+  const int t_begin = (int)(ntiles * gs / nslots);
+  const int t_end = (int)(ntiles * (gs + 1) / nslots);
+  const size_t codes_off = MODE == 0 ? L.gu_codes : L.dn_codes;
+  const size_t scales_off = MODE == 0 ? L.gu_scales : L.dn_scales;
+  const uint32_t codes_bytes = 8u * K, scale_bytes = (uint32_t)K / 2;
+
+  if (role == NCH) {
+    // ---------------- producer: one elected lane ----------------
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      uint32_t stage = 0, phase = 0;
+      int issued = 0;
+      bool ok = true;
+      int cur_item = -1;
+      const uint8_t* span = nullptr;
+      for (int t = t_begin; t < t_end; ++t) {
+        const int item = t / tpi, j = t - item * tpi;
+        if (item != cur_item) {
+          cur_item = item;
+          span = a.arena + (size_t)a.items[item].e * a.span_bytes;
+        }
+        if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
+        uint8_t* dst = ring + (size_t)stage * geo.stage_bytes;
+        mbar_arrive_expect_tx(&full[stage], codes_bytes + scale_bytes);
+        bulk_g2s(dst, span + codes_off + (size_t)j * codes_bytes, codes_bytes,
+                 &full[stage], pol);
+        bulk_g2s(dst + codes_bytes, span + scales_off + (size_t)j * scale_bytes,
+                 scale_bytes, &full[stage], pol);
+        ++issued;
+        if (++stage == (uint32_t)S) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) atomicOr(a.err, DEV_ERR_TIMEOUT);
+      // Every copy this lane issued must land before the CTA may exit: wait
+      // (bounded) for the last armed phase of each stage.
+      for (int i = 0; i < S && i < issued; ++i) {
+        const int n = (issued - i + S - 1) / S;
+        (void)mbar_wait(&full[i], (uint32_t)((n - 1) & 1));
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers: warp `role` = chunk c ----------------
+  const int c = role;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int nv = mx_nv(K, c), nbc = 2 * nv;
+  uint32_t stage = 0, phase = 0;
+  int cur_item = -1, loaded_grp = -1, loaded_tok = -2;
+  Item it{0, 0, 0, 0};
+  int a_lane = -1;     // sorted[pos + lane] of the current item (cnt <= 32)
+  uint32_t bx[32][2];  // B fragments, 2 registers per k-step of the chunk
+  float csc = 1.f;     // down: 2^s of this lane's token (column pair)
+  int n_epi = 0;
+  bool ok = true;
+
+  // assignment of token `ti` of the current item (all lanes must call)
+  auto assignment = [&](int ti) -> int {
+    const int v = __shfl_sync(0xffffffffu, a_lane, ti & 31);
+    if (ti >= it.cnt) return -1;
+    return it.cnt <= 32 ? v : a.sorted[it.pos + ti];
+  };
+
+  for (int t = t_begin; t < t_end && ok; ++t) {
+    const int item = t / tpi, j = t - item * tpi;
+    if (item != cur_item) {
+      cur_item = item;
+      it = a.items[item];
+      a_lane = lane < it.cnt ? a.sorted[it.pos + lane] : -1;
+    }
+    ok = mbar_wait(&full[stage], phase);
+    if (!ok) break;
+    const uint8_t* tile = ring + (size_t)stage * geo.stage_bytes;
+    // scales of rows g and g+8: 2 bytes a row per 64-column group
+    const uint8_t* sp = tile + codes_bytes + 256 * c + g * 2 * nbc;
+
+    for (int grp = 0; grp < it.cnt && ok; grp += GT) {
+      // ---- B fragments of this token group (reloaded only when they change)
+      if (item != loaded_grp >> 16 || grp != (loaded_grp & 0xFFFF)) {
+        if (MODE == 0) {
+          const int aa = assignment(grp + g);
+          const int tok = aa >= 0 ? aa / a.k : -1;
+          if (tok != loaded_tok) {
+            loaded_tok = tok;
 #pragma unroll
-  for (int t = 0; t < TG; ++t) {
-    a_t[t] = t < it.cnt ? sorted[it.pos + t] : -1;
-    if (a_t[t] >= 0 && act) {
-      const float4* hp = reinterpret_cast<const float4*>(
-          hbuf + (size_t)a_t[t] * I + (size_t)(16 * c + b) * 32);
+            for (int ks = 0; ks < 32; ++ks) {
+              uint32_t v0 = 0u, v1 = 0u;
+              if (tok >= 0 && ks < 4 * nv) {
+                const uint16_t* xp = a.x + (size_t)tok * a.H + 512 * c + 16 * ks + 2 * t4;
+                const uint32_t w0 = *reinterpret_cast<const uint32_t*>(xp);
+                const uint32_t w1 = *reinterpret_cast<const uint32_t*>(xp + 8);
+                v0 = f2_to_h2(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u));
+                v1 = f2_to_h2(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u));
+              }
+              bx[ks][0] = v0;
+              bx[ks][1] = v1;
+            }
+          }
+        } else {
+          const int aa = assignment(grp + (g >> 1));
+          const float* hrow = aa >= 0 ? a.hin + (size_t)aa * a.I + 512 * c + 2 * t4 : nullptr;
+          // pass 1: largest |h| of the token's chunk (the four lanes t4 = 0..3
+          // of a row g hold it all between them)
+          float m = 0.f;
+          if (hrow) {
+            for (int ks = 0; ks < 4 * nv; ++ks) {
+              const float2 p0 = *reinterpret_cast<const float2*>(hrow + 16 * ks);
+              const float2 p1 = *reinterpret_cast<const float2*>(hrow + 16 * ks + 8);
+              m = fmaxf(m, fmaxf(fmaxf(fabsf(p0.x), fabsf(p0.y)),
+                                 fmaxf(fabsf(p1.x), fabsf(p1.y))));
+            }
+          }
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+          int sh = 0;
+          if (m > 0.f) {
+            const int e = (int)((__float_as_uint(m) >> 23) & 0xFF) - 127;
+            sh = min(max(e - 14, -100), 100);
+          }
+          const float dn = pow2i(-sh);
+          const bool lo = (g & 1) != 0;
+          // pass 2: scaled f16 hi (even g) or lo (odd g) parts
+#pragma unroll
+          for (int ks = 0; ks < 32; ++ks) {
+            uint32_t r[2] = {0u, 0u};
+            if (hrow && ks < 4 * nv) {
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const float2 p = *reinterpret_cast<const float2*>(hrow + 16 * ks + 8 * hh);
+                const float v0 = p.x * dn, v1 = p.y * dn;
+                const __half2 hi = __floats2half2_rn(v0, v1);
+                if (!lo) {
+                  r[hh] = *reinterpret_cast<const uint32_t*>(&hi);
+                } else {
+                  const float2 f = __half22float2(hi);
+                  r[hh] = f2_to_h2(v0 - f.x, v1 - f.y);
+                }
+              }
+            }
+            bx[ks][0] = r[0];
+            bx[ks][1] = r[1];
+          }
+          // this lane's D columns 2t4, 2t4+1 belong to token t4 (rows g = 2 t4)
+          csc = __shfl_sync(0xffffffffu, pow2i(sh), 4 * (2 * t4));
+        }
+        loaded_grp = (item << 16) | grp;
+      }
+
+      // ---- the tile (16 rows x this chunk) against the group
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const float zero[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int v = 0; v < 8; ++v) {
-        float4 f = hp[v];
-        xr[t][4 * v] = f.x; xr[t][4 * v + 1] = f.y;
-        xr[t][4 * v + 2] = f.z; xr[t][4 * v + 3] = f.w;
+        if (v < nv) {
+          const uint4 q = lds128(tile + 512 * (8 * c + v) + 16 * lane);
+          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+          const uint32_t sw = lds_u16(sp + 2 * v), sw8 = lds_u16(sp + nbc + 2 * v);
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {  // the two 32-column blocks of v
+            uint32_t a0[4], a1[4];
+            decode_word(w[2 * hb], a0);
+            decode_word(w[2 * hb + 1], a1);
+            float d[4];
+            mma16816(d, a0, bx[4 * v + 2 * hb][0], bx[4 * v + 2 * hb][1], zero);
+            mma16816(d, a1, bx[4 * v + 2 * hb + 1][0], bx[4 * v + 2 * hb + 1][1], d);
+            const float sg = __uint_as_float(((sw >> (8 * hb)) & 0xFFu) << 23);
+            const float sg8 = __uint_as_float(((sw8 >> (8 * hb)) & 0xFFu) << 23);
+            acc[0] = fmaf(d[0], sg, acc[0]);
+            acc[1] = fmaf(d[1], sg, acc[1]);
+            acc[2] = fmaf(d[2], sg8, acc[2]);
+            acc[3] = fmaf(d[3], sg8, acc[3]);
+          }
+        }
       }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) xr[t][j] = 0.f;
-    }
-  }
-  float acc[TG][16];
-  mx_group_chunk<TG>(span + L.dn_codes, span + L.dn_scales, I, G, c, lane, xr, acc);
+      if (grp + GT >= it.cnt) {  // last use of this tile: release the stage
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+      }
+      if (MODE == 1) {
+        // y rows g, g+8 of token t4 = (hi + lo) * 2^s
+        acc[0] = (acc[0] + acc[1]) * csc;
+        acc[2] = (acc[2] + acc[3]) * csc;
+      }
 
-  __shared__ float red[kMaxChunkWarps][kMaxTG][32];
-#pragma unroll
-  for (int t = 0; t < TG; ++t) {
-    float s = halfwarp_transpose_reduce(acc[t], lane & 15);
-    red[warp][t][lane] = s;
-  }
-  __syncthreads();
-  const int nw = blockDim.x >> 5;
-  for (int o = threadIdx.x; o < TG * 32; o += blockDim.x) {
-    const int t = o >> 5, l = o & 31;  // l = 16 r + p
-    const int a = t < it.cnt ? sorted[it.pos + t] : -1;
-    if (a >= 0) {
-      float s = 0.f;
-      for (int w = 0; w < nw; ++w) s += red[w][t][l];
-      const int row = 32 * G + 2 * (l & 15) + (l >> 4);
-      part[(size_t)a * H + row] = s;
+      // ---- cross-chunk reduction through a ring of shared-memory entries;
+      // the finalizer role rotates over the chunk warps
+      const int r = n_epi % kRedRing, u = n_epi / kRedRing;
+      if (u >= 1 && !mbar_wait(&rempty[r], (u - 1) & 1)) { ok = false; break; }
+      float4* rb = reinterpret_cast<float4*>(red) + (size_t)r * NCH * 32;
+      rb[c * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rfull[r]);
+      if (c == n_epi % NCH) {
+        if (!mbar_wait(&rfull[r], u & 1)) { ok = false; break; }
+        float4 sum = rb[lane];
+        for (int cc = 1; cc < NCH; ++cc) {
+          const float4 v4 = rb[cc * 32 + lane];
+          sum.x += v4.x; sum.y += v4.y; sum.z += v4.z; sum.w += v4.w;
+        }
+        if (MODE == 0) {
+          // columns 2t4, 2t4+1 = tokens grp+2t4, grp+2t4+1; rows g (gate) and
+          // g+8 (up) of intermediate index 8j + g
+          const int a0i = assignment(grp + 2 * t4), a1i = assignment(grp + 2 * t4 + 1);
+          if (a0i >= 0) a.out[(size_t)a0i * a.I + 8 * j + g] = silu_f(sum.x) * sum.z;
+          if (a1i >= 0) a.out[(size_t)a1i * a.I + 8 * j + g] = silu_f(sum.y) * sum.w;
+        } else {
+          const int ai = assignment(grp + t4);
+          if (ai >= 0) {
+            a.out[(size_t)ai * a.H + 16 * j + g] = sum.x;
+            a.out[(size_t)ai * a.H + 16 * j + g + 8] = sum.z;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rempty[r]);
+      }
+      ++n_epi;
     }
+    if (++stage == (uint32_t)S) { stage = 0; phase ^= 1; }
   }
+  // A failed (timed-out) wait: record it and leave; every other wait of the
+  // CTA is bounded too, so the rest of the slot ends on its own.
+  if (!ok) atomicOr(a.err, DEV_ERR_TIMEOUT);
 }
 
 // out[t][j] = residual + sum_i w[t][i] part[t k + i][j] + ysh[t][j]
@@ -262,6 +388,7 @@ __global__ void combine_kernel(const float* __restrict__ part,
                                const uint16_t* __restrict__ residual,
                                float* __restrict__ out_f32,
                                uint16_t* __restrict__ out_bf16) {
+  pdl_wait();
   const int t = blockIdx.y;
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= H) return;
@@ -271,9 +398,43 @@ __global__ void combine_kernel(const float* __restrict__ part,
   if (ysh) y += ysh[(size_t)t * H + j];
   if (residual) y += __uint_as_float((uint32_t)residual[(size_t)t * H + j] << 16);
   if (out_f32) out_f32[(size_t)t * H + j] = y;
-  if (out_bf16) {
-    out_bf16[(size_t)t * H + j] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+  if (out_bf16) out_bf16[(size_t)t * H + j] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
   }
+  return n;
+}
+
+template <int MODE>
+cudaError_t launch_mxv(const MxvArgs& a, int max_items, cudaStream_t s) {
+  const int K = MODE == 0 ? a.H : a.I;
+  const int NCH = mx_nchunks(K);
+  const int NS = slots_per_cta(K);
+  const int threads = NS * (NCH + 1) * 32;
+  const SlotGeom geo = slot_geom(K, NS);
+  const size_t smem = (size_t)NS * geo.bytes;
+  static int configured_smem[2] = {0, 0};
+  if (configured_smem[MODE] < (int)smem) {
+    cudaError_t e = cudaFuncSetAttribute(mxv_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    configured_smem[MODE] = (int)smem;
+  }
+  const int tpi = MODE == 0 ? (2 * a.I) / 16 : a.H / 16;
+  const long long max_tiles = (long long)max_items * tpi;
+  int grid = (int)((max_tiles + NS - 1) / NS);
+  if (grid > num_sms()) grid = num_sms();
+  if (grid < 1) grid = 1;
+  mxv_kernel<MODE><<<grid, threads, smem, s>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -281,31 +442,19 @@ __global__ void combine_kernel(const float* __restrict__ part,
 cudaError_t launch_gateup(const uint8_t* arena, size_t span_bytes, int H,
                           int I, int k, const uint16_t* x, const Item* items,
                           const int32_t* n_items, int max_items,
-                          const int32_t* sorted, float* hbuf, int tg,
-                          cudaStream_t s) {
-  dim3 grid(I / 16, max_items), block(mx_nchunks(H) * 32);
-  if (tg == 1)
-    gateup_kernel<1><<<grid, block, 0, s>>>(arena, span_bytes, H, I, k, x,
-                                            items, n_items, sorted, hbuf);
-  else
-    gateup_kernel<2><<<grid, block, 0, s>>>(arena, span_bytes, H, I, k, x,
-                                            items, n_items, sorted, hbuf);
-  return cudaGetLastError();
+                          const int32_t* sorted, float* hbuf, int /*tg*/,
+                          uint32_t* err, cudaStream_t s) {
+  MxvArgs a{arena, span_bytes, H, I, k, x, nullptr, items, n_items, sorted, hbuf, err};
+  return launch_mxv<0>(a, max_items, s);
 }
 
 cudaError_t launch_down(const uint8_t* arena, size_t span_bytes, int H, int I,
                         const Item* items, const int32_t* n_items,
                         int max_items, const int32_t* sorted,
-                        const float* hbuf, float* part, int tg,
+                        const float* hbuf, float* part, int /*tg*/, uint32_t* err,
                         cudaStream_t s) {
-  dim3 grid(H / 32, max_items), block(mx_nchunks(I) * 32);
-  if (tg == 1)
-    down_kernel<1><<<grid, block, 0, s>>>(arena, span_bytes, H, I, items,
-                                          n_items, sorted, hbuf, part);
-  else
-    down_kernel<2><<<grid, block, 0, s>>>(arena, span_bytes, H, I, items,
-                                          n_items, sorted, hbuf, part);
-  return cudaGetLastError();
+  MxvArgs a{arena, span_bytes, H, I, 0, nullptr, hbuf, items, n_items, sorted, part, err};
+  return launch_mxv<1>(a, max_items, s);
 }
 
 cudaError_t launch_combine(const float* part, const float* w, int T, int k,

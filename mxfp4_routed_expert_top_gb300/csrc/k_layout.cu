@@ -1,4 +1,4 @@
-// k_layout.cu — repacking canonical expert spans into the HBM layout the
+// k_layout.cu — repacking canonical expert spans into the fragment layout the
 // expert kernels stream (see internal.h), and back.
 #include "internal.h"
 
@@ -14,28 +14,49 @@ __device__ inline Canon canon_offsets(int H, int I) {
   return Canon{0, q, q + s, 2 * q + s, 2 * q + 2 * s, 3 * q + 2 * s};
 }
 
-// Decompose an offset inside a codes section into (pair, chunk, r, b).
-__device__ inline void codes_coord(size_t o, int K, size_t& P, int& c, int& r,
-                                   int& b) {
-  P = o / (size_t)K;
-  int rem = (int)(o - P * (size_t)K);
-  c = rem >> 9;
-  int nbc = mx_nbc(K, c);
-  int w = (rem - (c << 9)) >> 4;
-  r = w / nbc;
-  b = w - r * nbc;
+// Canonical byte offset of byte `o` of a codes section of a matrix with K
+// columns. Tile row rho of tile j maps to (tensor offset, row) by `gu`:
+// gate/up tiles interleave 8 gate and 8 up rows; down tiles are 16 rows.
+__device__ inline size_t codes_src(size_t o, int K, bool gu, const Canon& C) {
+  const size_t tile = (size_t)8 * K;
+  const size_t j = o / tile;
+  const int rem = (int)(o - j * tile);
+  const int grp = rem >> 9;            // 64-column group (8c + v)
+  const int w = rem & 511;
+  const int l = w >> 4, g = l >> 2, t = l & 3;
+  const int s = (w >> 2) & 3, q = w & 3;
+  const int rho = g + 8 * (q & 1);
+  const int col = 64 * grp + 16 * s + 2 * t + 8 * (q >> 1);
+  size_t base, row;
+  if (gu) {
+    base = rho < 8 ? C.gq : C.uq;
+    row = 8 * j + (rho & 7);
+  } else {
+    base = C.dq;
+    row = 16 * j + rho;
+  }
+  return base + row * (size_t)(K / 2) + (size_t)(col >> 1);
 }
 
-__device__ inline void scales_coord(size_t o, int K, size_t& G, int& c, int& r,
-                                    int& b) {
-  size_t gsz = (size_t)32 * mx_nb(K);
-  G = o / gsz;
-  int rem = (int)(o - G * gsz);
-  c = rem >> 9;
-  int nbc = mx_nbc(K, c);
-  int w = (rem - (c << 9)) >> 4;
-  r = w / nbc;
-  b = w - r * nbc;
+__device__ inline size_t scales_src(size_t o, int K, bool gu, const Canon& C) {
+  const size_t tile = (size_t)K / 2;
+  const size_t j = o / tile;
+  const int rem = (int)(o - j * tile);
+  const int c = rem >> 8;
+  const int w = rem & 255;
+  const int nbc = mx_nbc(K, c);
+  const int g = w / (2 * nbc), i = w - g * 2 * nbc;
+  const int rho = g + 8 * (i >= nbc ? 1 : 0);
+  const int block = 16 * c + (i >= nbc ? i - nbc : i);
+  size_t base, row;
+  if (gu) {
+    base = rho < 8 ? C.gs : C.us;
+    row = 8 * j + (rho & 7);
+  } else {
+    base = C.ds;
+    row = 16 * j + rho;
+  }
+  return base + row * (size_t)(K / 32) + (size_t)block;
 }
 
 // One thread per 16-byte unit of the device span. inverse = 0: canonical ->
@@ -47,51 +68,21 @@ __global__ void repack_kernel(const uint8_t* __restrict__ src,
   const Canon C = canon_offsets(H, I);
   const size_t units = D.bytes / 16;
   const size_t total = units * (size_t)n_spans;
-  for (size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
-       g += (size_t)gridDim.x * blockDim.x) {
-    const size_t span = g / units;
-    const size_t o = (g - span * units) * 16;  // offset in the device span
+  for (size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x; u < total;
+       u += (size_t)gridDim.x * blockDim.x) {
+    const size_t span = u / units;
+    const size_t o0 = (u - span * units) * 16;  // offset in the device span
     const uint8_t* sbase = src + span * D.bytes;
     uint8_t* dbase = dst + span * D.bytes;
-    size_t coff[16];
-    bool contiguous;
-    if (o < D.gu_scales) {  // gate/up codes, K = H
-      size_t P; int c, r, b;
-      codes_coord(o - D.gu_codes, H, P, c, r, b);
-      coff[0] = (r ? C.uq : C.gq) + P * (size_t)(H / 2) + (size_t)(16 * c + b) * 16;
-      contiguous = true;
-    } else if (o < D.dn_codes) {  // gate/up scales
-      size_t G; int c, r, b;
-      scales_coord(o - D.gu_scales, H, G, c, r, b);
-      const int NB = mx_nb(H);
-      for (int i = 0; i < 16; ++i)
-        coff[i] = (r ? C.us : C.gs) + (16 * G + i) * (size_t)NB + 16 * c + b;
-      contiguous = false;
-    } else if (o < D.dn_scales) {  // down codes, K = I
-      size_t P; int c, r, b;
-      codes_coord(o - D.dn_codes, I, P, c, r, b);
-      coff[0] = C.dq + (2 * P + r) * (size_t)(I / 2) + (size_t)(16 * c + b) * 16;
-      contiguous = true;
-    } else {  // down scales
-      size_t G; int c, r, b;
-      scales_coord(o - D.dn_scales, I, G, c, r, b);
-      const int NB = mx_nb(I);
-      for (int i = 0; i < 16; ++i)
-        coff[i] = C.ds + (2 * (16 * G + i) + r) * (size_t)NB + 16 * c + b;
-      contiguous = false;
-    }
-    if (contiguous) {
-      if (!inverse)
-        *reinterpret_cast<uint4*>(dbase + o) =
-            *reinterpret_cast<const uint4*>(sbase + coff[0]);
-      else
-        *reinterpret_cast<uint4*>(dbase + coff[0]) =
-            *reinterpret_cast<const uint4*>(sbase + o);
-    } else {
-      for (int i = 0; i < 16; ++i) {
-        if (!inverse) dbase[o + i] = sbase[coff[i]];
-        else dbase[coff[i]] = sbase[o + i];
-      }
+    for (int i = 0; i < 16; ++i) {
+      const size_t o = o0 + i;
+      size_t c;
+      if (o < D.gu_scales) c = codes_src(o - D.gu_codes, H, true, C);
+      else if (o < D.dn_codes) c = scales_src(o - D.gu_scales, H, true, C);
+      else if (o < D.dn_scales) c = codes_src(o - D.dn_codes, I, false, C);
+      else c = scales_src(o - D.dn_scales, I, false, C);
+      if (!inverse) dbase[o] = sbase[c];
+      else dbase[c] = sbase[o];
     }
   }
 }

@@ -11,101 +11,87 @@
 namespace dfm {
 namespace {
 
-constexpr int kRouterRowsPerBlock = 8;  // one warp per row
-constexpr int kRouterTT = 8;            // tokens per smem tile
-
-// part[split][t][e] = sum over the split's K range of Wr[e][j] x[t][j]
-__global__ void __launch_bounds__(256)
-router_kernel(const float* __restrict__ Wr, int E, int H,
-              const uint16_t* __restrict__ x, int T, float* __restrict__ part,
-              int split_len) {
-  extern __shared__ float xs[];  // [kRouterTT][split_len]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * kRouterRowsPerBlock + warp;
-  const int split = blockIdx.y;
-  const int k0 = split * split_len;
-  const int len = min(split_len, H - k0);
-  for (int t0 = 0; t0 < T; t0 += kRouterTT) {
-    const int tt = min(kRouterTT, T - t0);
-    __syncthreads();
-    for (int i = threadIdx.x; i < tt * len; i += blockDim.x) {
-      const int t = i / len, j = i - t * len;
-      xs[t * split_len + j] =
-          __uint_as_float((uint32_t)x[(size_t)(t0 + t) * H + k0 + j] << 16);
-    }
-    __syncthreads();
-    if (e < E) {
-      float acc[kRouterTT];
-#pragma unroll
-      for (int t = 0; t < kRouterTT; ++t) acc[t] = 0.f;
-      const float* wr = Wr + (size_t)e * H + k0;
-      for (int j = 4 * lane; j < len; j += 128) {
-        const float4 w4 = __ldg(reinterpret_cast<const float4*>(wr + j));
-#pragma unroll
-        for (int t = 0; t < kRouterTT; ++t) {
-          if (t < tt) {
-            const float4 x4 = *reinterpret_cast<const float4*>(xs + t * split_len + j);
-            acc[t] = fmaf(w4.x, x4.x, acc[t]);
-            acc[t] = fmaf(w4.y, x4.y, acc[t]);
-            acc[t] = fmaf(w4.z, x4.z, acc[t]);
-            acc[t] = fmaf(w4.w, x4.w, acc[t]);
-          }
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < kRouterTT; ++t) {
-        float v = acc[t];
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0 && t < tt)
-          part[((size_t)split * T + t0 + t) * E + e] = v;
-      }
-    }
-  }
-}
+constexpr int kRouterRowsPerBlock = 8;  // one warp per (row, column split)
+constexpr int kRouterMaxV = 16;         // float4 loads per lane: split <= 2048
 
 __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
   return v > bv || (v == bv && e < be);
 }
 
-// One block of 128 threads per token: sum the split partials (fixed order),
-// then warp 0 selects the top k and the softmax weights.
-__global__ void __launch_bounds__(128)
-topk_kernel(const float* __restrict__ part, int nsplit, int T, int E, int k,
-            float* __restrict__ logits_out, int32_t* __restrict__ ids,
-            float* __restrict__ w, Item* items, int32_t* n_items,
-            int32_t* sorted) {
-  __shared__ float lg[1024];
-  const int t = blockIdx.x;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    float v = 0.f;
-    for (int s = 0; s < nsplit; ++s) v += part[((size_t)s * T + t) * E + e];
-    lg[e] = v;
-    if (logits_out) logits_out[(size_t)t * E + e] = v;
+// Top-k of lg[0..E) (shared memory) by the first 128 threads of the block:
+// four warps select the top k of their quarter, warp 0 merges the 4k
+// candidates. On return lanes 0..k-1 of warp 0 hold (value, id) of rank
+// `lane`, descending. cand_v / cand_e: shared scratch of 4 * 32 entries.
+__device__ void block_topk(const float* lg, int E, int k, float* cand_v,
+                           int* cand_e, float& out_v, int& out_e) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp < 4) {
+    float v[8];
+    int id[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = warp * 256 + lane + 32 * i;
+      v[i] = e < E ? lg[e] : -INFINITY;
+      id[i] = e < E ? e : 0x7fffffff;
+    }
+    for (int r = 0; r < k; ++r) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (better(v[i], id[i], bv, be)) { bv = v[i]; be = id[i]; }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (id[i] == be) v[i] = -INFINITY;  // taken
+      if (lane == 0) {
+        cand_v[warp * 32 + r] = bv;
+        cand_e[warp * 32 + r] = be;
+      }
+    }
   }
   __syncthreads();
-  if (threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
-  float sel_v = 0.f;
-  int sel_e = 0;
-  for (int i = 0; i < k; ++i) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-    for (int e = lane; e < E; e += 32) {
-      const float v = lg[e];
-      if (better(v, e, bv, be)) { bv = v; be = e; }
-    }
+  if (warp == 0) {
+    float v[4];
+    int id[4];
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
+    for (int i = 0; i < 4; ++i) {
+      const int c = lane + 32 * i;  // candidate slot: warp c/32, rank c%32
+      const bool valid = (c & 31) < k;
+      v[i] = valid ? cand_v[c] : -INFINITY;
+      id[i] = valid ? cand_e[c] : 0x7fffffff;
     }
-    if (lane == i) { sel_v = bv; sel_e = be; }
-    __syncwarp();
-    if (lane == 0) lg[be] = -INFINITY;
-    __syncwarp();
+    for (int r = 0; r < k; ++r) {
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (better(v[i], id[i], bv, be)) { bv = v[i]; be = id[i]; }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (id[i] == be) v[i] = -INFINITY;
+      if (lane == r) { out_v = bv; out_e = be; }
+    }
   }
+}
+
+// Softmax over the k selected logits (warp 0, lanes 0..k-1 hold them) and
+// the writes of ids / weights (and, for a single token, the work items).
+__device__ void write_selection(int t, int k, float sel_v, int sel_e,
+                                int32_t* ids, float* w, Item* items,
+                                int32_t* n_items, int32_t* sorted) {
+  const int lane = threadIdx.x & 31;
   const float vmax = __shfl_sync(0xffffffffu, sel_v, 0);
   const float ex = lane < k ? expf(sel_v - vmax) : 0.f;
   float z = ex;
@@ -114,12 +100,117 @@ topk_kernel(const float* __restrict__ part, int nsplit, int T, int E, int k,
   if (lane < k) {
     ids[(size_t)t * k + lane] = sel_e;
     w[(size_t)t * k + lane] = ex / z;
-    if (items && T == 1) {
+    if (items) {
       items[lane] = Item{sel_e, lane, 1, 0};
       sorted[lane] = lane;
     }
   }
-  if (items && T == 1 && lane == 0) *n_items = k;
+  if (items && lane == 0) *n_items = k;
+}
+
+struct TopkFuse {  // fused top-k of a single token by the router's last block
+  unsigned int* counter;  // zero between calls; reset by the last block
+  int k;
+  int32_t* ids;
+  float* w;
+  Item* items;
+  int32_t* n_items;
+  int32_t* sorted;
+};
+
+// part[split][t][e] = sum over the split's columns of Wr[e][j] x[t][j].
+// One warp per (row, split); every weight load of the warp is issued before
+// the first FMA, and the weights stay in registers across tokens.
+__global__ void __launch_bounds__(256)
+router_kernel(const float* __restrict__ Wr, int E, int H,
+              const uint16_t* __restrict__ x, int T, float* __restrict__ part,
+              int split_len, TopkFuse fz) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kRouterRowsPerBlock + warp;
+  const int split = blockIdx.y;
+  const int k0 = split * split_len;
+  const int len = min(split_len, H - k0);
+  if (e < E) {
+    float4 w4[kRouterMaxV];
+    const float* wr = Wr + (size_t)e * H + k0 + 4 * lane;
+#pragma unroll
+    for (int i = 0; i < kRouterMaxV; ++i)
+      w4[i] = (4 * lane + 128 * i < len) ? __ldg(reinterpret_cast<const float4*>(wr + 128 * i))
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int t = 0; t < T; ++t) {
+      const uint16_t* xp = x + (size_t)t * H + k0 + 4 * lane;
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < kRouterMaxV; ++i) {
+        if (4 * lane + 128 * i < len) {
+          const uint2 xv = __ldg(reinterpret_cast<const uint2*>(xp + 128 * i));
+          acc = fmaf(w4[i].x, __uint_as_float(xv.x << 16), acc);
+          acc = fmaf(w4[i].y, __uint_as_float(xv.x & 0xFFFF0000u), acc);
+          acc = fmaf(w4[i].z, __uint_as_float(xv.y << 16), acc);
+          acc = fmaf(w4[i].w, __uint_as_float(xv.y & 0xFFFF0000u), acc);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) part[((size_t)split * T + t) * E + e] = acc;
+    }
+  }
+  if (!fz.counter) return;
+
+  // ---- single token: the last block to finish selects the experts ----
+  __shared__ unsigned int ticket;
+  __shared__ float lg[1024];
+  __shared__ float cand_v[128];
+  __shared__ int cand_e[128];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    ticket = atomicAdd(fz.counter, 1u);
+  }
+  __syncthreads();
+  if (ticket != gridDim.x * gridDim.y - 1) return;
+  __threadfence();
+  const int nsplit = gridDim.y;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) {
+    float v = 0.f;
+    for (int s = 0; s < nsplit; ++s) v += __ldcg(part + (size_t)s * E + i);
+    lg[i] = v;
+  }
+  __syncthreads();
+  float sel_v = 0.f;
+  int sel_e = 0;
+  block_topk(lg, E, fz.k, cand_v, cand_e, sel_v, sel_e);
+  if (warp == 0) {
+    write_selection(0, fz.k, sel_v, sel_e, fz.ids, fz.w, fz.items, fz.n_items,
+                    fz.sorted);
+    if (lane == 0) *fz.counter = 0u;
+  }
+}
+
+// One block of 128 threads per token: sum the split partials (fixed order),
+// select the top k and the softmax weights.
+__global__ void __launch_bounds__(128)
+topk_kernel(const float* __restrict__ part, int nsplit, int T, int E, int k,
+            float* __restrict__ logits_out, int32_t* __restrict__ ids,
+            float* __restrict__ w, Item* items, int32_t* n_items,
+            int32_t* sorted) {
+  __shared__ float lg[1024];
+  __shared__ float cand_v[128];
+  __shared__ int cand_e[128];
+  const int t = blockIdx.x;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float v = 0.f;
+    for (int s = 0; s < nsplit; ++s) v += part[((size_t)s * T + t) * E + e];
+    lg[e] = v;
+    if (logits_out) logits_out[(size_t)t * E + e] = v;
+  }
+  __syncthreads();
+  float sel_v = 0.f;
+  int sel_e = 0;
+  block_topk(lg, E, k, cand_v, cand_e, sel_v, sel_e);
+  if (threadIdx.x < 32)
+    write_selection(t, k, sel_v, sel_e, ids, w, (items && T == 1) ? items : nullptr,
+                    n_items, sorted);
 }
 
 // Block-wide exclusive scan of one value per thread (blockDim.x <= 1024).
@@ -213,17 +304,14 @@ group_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
 }  // namespace
 
 cudaError_t launch_router(const float* Wr, int E, int H, const uint16_t* x,
-                          int T, float* part, RouterSplit sp, cudaStream_t s) {
-  const int split_len = sp.split_len;
-  const size_t smem = (size_t)kRouterTT * split_len * sizeof(float);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(router_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+                          int T, float* part, RouterSplit sp, cudaStream_t s,
+                          const RouterFuse* fuse) {
+  TopkFuse fz{nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr};
+  if (fuse && T == 1)
+    fz = TopkFuse{fuse->counter, fuse->k, fuse->ids, fuse->w, fuse->items,
+                  fuse->n_items, fuse->sorted};
   dim3 grid((E + kRouterRowsPerBlock - 1) / kRouterRowsPerBlock, sp.nsplit);
-  router_kernel<<<grid, 256, smem, s>>>(Wr, E, H, x, T, part, split_len);
+  router_kernel<<<grid, 256, 0, s>>>(Wr, E, H, x, T, part, sp.split_len, fz);
   return cudaGetLastError();
 }
 

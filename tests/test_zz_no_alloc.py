@@ -55,7 +55,7 @@ def test_route_noalloc_matches_handle_path(torch):
 
 def test_route_noalloc_rejects_oversized_calls(torch):
     import mxfp4_routed_expert_top_gb300 as dfm
-    E, H, k, T = 896, 7168, 16, 98    # needs 3 * 98 * 896 > 262,144 floats
+    E, H, k, T = 896, 7168, 16, 98    # needs 4 * 98 * 896 > 262,144 floats
     router = torch.zeros((E, H), dtype=torch.float32, device="cuda")
     x = torch.zeros((T, H), dtype=torch.int16, device="cuda")
     ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
