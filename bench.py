@@ -49,6 +49,9 @@ def parse():
     p.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--tokens", type=int, default=0,
+                   help="override the tokens per step of the workload (the stack "
+                        "workload decodes at batch 1 and batch 4)")
     p.add_argument("--experts", type=int, default=0,
                    help="profiling aid: override the routed-expert count (same "
                         "per-token work, smaller resident set); not a bench line")
@@ -255,9 +258,11 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dist = init_dist(ws, "nccl")
     wl = synth.WORKLOADS[args.config]
+    import dataclasses
     if args.experts:
-        import dataclasses
         wl = dataclasses.replace(wl, E=args.experts, name=wl.name + "-e%d" % args.experts)
+    if args.tokens:
+        wl = dataclasses.replace(wl, T=args.tokens, name=wl.name + "-t%d" % args.tokens)
     T = wl.T
     m = dfm.MoE(wl.H, wl.E, wl.k, wl.I, wl.n_shared, wl.Is, n_layers=wl.L,
                 max_tokens=max(T, 4), rms_eps=wl.eps,
