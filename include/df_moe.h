@@ -66,12 +66,12 @@ extern "C" {
 typedef struct df_moe df_moe; /* opaque, library-owned */
 
 typedef struct {
-  int32_t hidden;       /* H: multiple of 32                                   */
+  int32_t hidden;       /* H: multiple of 64                                   */
   int32_t n_experts;    /* E: routed experts per layer, 1..1024                */
   int32_t top_k;        /* k: experts per token, 1..min(E, 32)                 */
-  int32_t inter;        /* I: routed-expert intermediate, multiple of 32       */
+  int32_t inter;        /* I: routed-expert intermediate, multiple of 64       */
   int32_t n_shared;     /* shared experts per layer (0..8)                     */
-  int32_t shared_inter; /* Is: shared intermediate, multiple of 32             */
+  int32_t shared_inter; /* Is: shared intermediate, multiple of 64             */
   int32_t n_layers;     /* L >= 1                                              */
   int32_t max_tokens;   /* largest T a forward call may use (1..4096)          */
   float rms_eps;        /* stack mode only                                     */
@@ -141,6 +141,18 @@ DF_MOE_API int df_moe_forward(df_moe* h, const void* x_bf16, int32_t T,
                    const void* residual_bf16, void* out_bf16, float* out_f32,
                    int32_t* ids, float* weights, void* stream);
 
+/* Stack mode: the same forward pass, also recording every layer's inputs as
+ * the device computed them, for checking a layer against a reference on
+ * exactly those inputs.
+ *   trace_x   device [L][T][H] bf16 or NULL: x entering layer l (the residual)
+ *   trace_xn  device [L][T][H] bf16 or NULL: its RMS-normalised form, the
+ *             input of layer l's router and experts
+ * Errors as df_moe_forward; EINVAL outside stack mode. */
+DF_MOE_API int df_moe_forward_trace(df_moe* h, const void* x_bf16, int32_t T,
+                         void* out_bf16, float* out_f32, int32_t* ids,
+                         float* weights, void* trace_x, void* trace_xn,
+                         void* stream);
+
 /* Same, with HOST buffers: copies x (and residual) to the device, runs the
  * forward, copies the results back and synchronises `stream` before
  * returning. out_f32, residual, ids and weights may be NULL. */
@@ -192,7 +204,7 @@ DF_MOE_API int df_moe_read_expert_span(df_moe* h, int32_t layer, int32_t expert,
  * With timing on, every kernel launch of forward is bracketed by CUDA events
  * on its stream; df_moe_timing_get returns, per kernel kind, the launches and
  * the summed device time since the last reset. */
-#define DF_MOE_KERNEL_KINDS 12
+#define DF_MOE_KERNEL_KINDS 13
 DF_MOE_API int df_moe_timing_enable(df_moe* h, int on);
 DF_MOE_API int df_moe_timing_reset(df_moe* h);
 DF_MOE_API int df_moe_timing_get(df_moe* h, int kind, const char** name,

@@ -13,13 +13,13 @@ LIB_PATH = os.path.join(PKG, "libdfmoe.so")
 
 OK, EINVAL, ENOMEM, ECUDA, ESTATE, ERANGE, ETIMEOUT, EDEVICE = 0, -1, -2, -3, -4, -5, -6, -7
 STACK_RMSNORM_RESIDUAL = 1
-KERNEL_KINDS = 12
+KERNEL_KINDS = 13
 
 # every symbol the header declares (checked by the CPU tests)
 SYMBOLS = [
     "df_moe_create", "df_moe_destroy", "df_moe_last_error",
     "df_moe_expert_span_bytes", "df_moe_span_bytes_for", "df_moe_load_experts",
-    "df_moe_forward", "df_moe_forward_host", "df_moe_sync",
+    "df_moe_forward", "df_moe_forward_trace", "df_moe_forward_host", "df_moe_sync",
     "df_moe_step_router", "df_moe_step_topk", "df_moe_step_group",
     "df_moe_step_expert_gateup", "df_moe_step_expert_down",
     "df_moe_step_shared", "df_moe_step_rmsnorm", "df_moe_read_expert_span",
@@ -71,6 +71,7 @@ def lib():
         L.df_moe_span_bytes_for.restype = ctypes.c_size_t
         L.df_moe_load_experts.argtypes = [vp, i32, ctypes.POINTER(LayerWeights), vp]
         L.df_moe_forward.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp]
+        L.df_moe_forward_trace.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp]
         L.df_moe_forward_host.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp]
         L.df_moe_sync.argtypes = [vp, vp]
         L.df_moe_step_router.argtypes = [vp, i32, vp, i32, vp, vp]
@@ -193,6 +194,14 @@ class MoE:
         self._check(lib().df_moe_forward(self.h, _ptr(x), T, _ptr(residual), _ptr(out),
                                          _ptr(out_f32), _ptr(ids), _ptr(weights),
                                          _stream(stream)))
+
+    def forward_trace(self, x, T, out, ids, weights, trace_x=None, trace_xn=None,
+                      out_f32=None, stream=None):
+        """Stack mode: forward that also records each layer's input x and its
+        normalised form xn ([L][T][H] bf16 device buffers)."""
+        self._check(lib().df_moe_forward_trace(self.h, _ptr(x), T, _ptr(out), _ptr(out_f32),
+                                               _ptr(ids), _ptr(weights), _ptr(trace_x),
+                                               _ptr(trace_xn), _stream(stream)))
 
     def forward_host(self, x, T, out, ids=None, weights=None, residual=None,
                      out_f32=None, stream=None):

@@ -24,6 +24,11 @@ struct LayerBufs {
   uint16_t* sh_gate = nullptr;  // [n_s*Is][H]
   uint16_t* sh_up = nullptr;    // [n_s*Is][H]
   uint16_t* sh_down = nullptr;  // [H][n_s*Is]
+  // shared experts as f16 fragment tiles with row scales (layer kernel)
+  uint4* sh_gu16 = nullptr;     // [n_s][Is/8][H/16][32]
+  float* sh_gu_rs = nullptr;    // [n_s][Is/8][16]
+  uint4* sh_dn16 = nullptr;     // [n_s][H/16][Is/16][32]
+  float* sh_dn_rs = nullptr;    // [n_s][H]
   bool router_loaded = false;
   std::vector<uint8_t> shared_loaded;
   std::vector<uint8_t> expert_loaded;
@@ -38,7 +43,7 @@ struct Pending {
 const char* kKindNames[K_NKINDS] = {"router", "topk", "group", "expert_gateup",
                                     "expert_down", "combine", "shared_gateup",
                                     "shared_down", "rmsnorm", "residual",
-                                    "repack", "other"};
+                                    "repack", "other", "layer"};
 
 }  // namespace
 
@@ -65,6 +70,20 @@ struct df_moe {
   uint16_t* xn = nullptr;        // [Tmax][H]
   uint32_t* err = nullptr;       // device error word
   unsigned int* counter = nullptr;  // router blocks done (zero between calls)
+  // layer kernel (decode batches, T <= kLayerMaxT)
+  int lk_T = 0;                  // largest T it serves (0: not available)
+  int lk_max_items = 0;
+  int lk_ks_rt = 1, lk_ks_gu = 1, lk_ks_sg = 1, lk_ks_dn = 1, lk_hf_groups = 0;
+  float* lk_logit_part = nullptr;
+  float2* lk_cand = nullptr;
+  float4* lk_gu_part = nullptr;
+  float4* lk_sg_part = nullptr;
+  float* lk_hsh32 = nullptr;
+  uint4* lk_hf = nullptr;
+  float* lk_hsc = nullptr;
+  uint32_t* lk_sync = nullptr;
+  SyncLayout lk_sl{};
+  uint32_t epoch = 0;
   // host-API device buffers
   uint16_t* hx = nullptr;
   uint16_t* hres = nullptr;
@@ -212,11 +231,67 @@ int shared_part(df_moe* h, int l, const uint16_t* x, int T, float* ysh,
 }
 
 // One MoE layer: out = residual + routed + shared.
+// The whole layer as one cooperative launch (T <= lk_T).
+int layer_kernel_forward(df_moe* h, int l, const uint16_t* x, int T,
+                         const uint16_t* residual, uint16_t* out_bf16, float* out_f32,
+                         int32_t* ids, float* w, cudaStream_t s) {
+  const df_moe_config& c = h->cfg;
+  const LayerBufs& L = h->layers[l];
+  LayerKernelArgs a{};
+  a.H = c.hidden;
+  a.E = c.n_experts;
+  a.k = c.top_k;
+  a.I = c.inter;
+  a.Is = c.n_shared > 0 ? c.shared_inter : 0;
+  a.n_shared = c.n_shared;
+  a.T = T;
+  a.max_items = std::min(T * c.top_k, c.n_experts);
+  a.ks_rt = h->lk_ks_rt;
+  a.ks_gu = h->lk_ks_gu;
+  a.ks_sg = h->lk_ks_sg;
+  a.ks_dn = h->lk_ks_dn;
+  a.Wr = L.router;
+  a.arena = L.arena;
+  a.span_bytes = h->span_bytes;
+  a.sh_gu = L.sh_gu16;
+  a.sh_gu_rs = L.sh_gu_rs;
+  a.sh_dn = L.sh_dn16;
+  a.sh_dn_rs = L.sh_dn_rs;
+  a.x = x;
+  a.residual = residual;
+  a.out_f32 = out_f32;
+  a.out_bf16 = out_bf16;
+  a.ids = ids;
+  a.w = w;
+  a.logit_part = h->lk_logit_part;
+  a.cand = h->lk_cand;
+  a.items = h->items;
+  a.n_items = h->n_items;
+  a.sorted = h->sorted;
+  a.gu_part = h->lk_gu_part;
+  a.sg_part = h->lk_sg_part;
+  a.h32 = h->hbuf;
+  a.hsh32 = h->lk_hsh32;
+  a.hf = h->lk_hf;
+  a.hf_groups = h->lk_hf_groups;
+  a.hsc = h->lk_hsc;
+  a.part = h->part;
+  a.sync = h->lk_sync;
+  a.sl = h->lk_sl;
+  if (++h->epoch == 0) h->epoch = 1;  // flags hold the epoch; 0 is "never set"
+  a.epoch = h->epoch;
+  a.err = h->err;
+  RUN(h, K_LAYER, s, launch_layer(a, s));
+  return DF_MOE_OK;
+}
+
 int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
                   const uint16_t* residual, uint16_t* out_bf16, float* out_f32,
                   int32_t* ids, float* w, cudaStream_t s) {
   const df_moe_config& c = h->cfg;
   const LayerBufs& L = h->layers[l];
+  if (T <= h->lk_T && layer_kernel_supports(c.hidden, T, c.top_k, c.n_experts))
+    return layer_kernel_forward(h, l, x, T, residual, out_bf16, out_f32, ids, w, s);
   const int tg = T == 1 ? 1 : kOneItemPerExpert;
   int rc = route(h, l, x, T, ids, w, s, nullptr, tg);
   if (rc) return rc;
@@ -273,20 +348,20 @@ int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
   if (!cfg || !out) return fail(nullptr, DF_MOE_EINVAL, "null argument");
   *out = nullptr;
   const df_moe_config c = *cfg;
-  if (c.hidden <= 0 || c.hidden % 32 || c.hidden > 8192)
-    return fail(nullptr, DF_MOE_EINVAL, "hidden must be a multiple of 32 in [32, 8192]");
-  if (c.inter <= 0 || c.inter % 32 || c.inter > 8192)
-    return fail(nullptr, DF_MOE_EINVAL, "inter must be a multiple of 32 in [32, 8192]");
+  if (c.hidden <= 0 || c.hidden % 64 || c.hidden > 8192)
+    return fail(nullptr, DF_MOE_EINVAL, "hidden must be a multiple of 64 in [64, 8192]");
+  if (c.inter <= 0 || c.inter % 64 || c.inter > 8192)
+    return fail(nullptr, DF_MOE_EINVAL, "inter must be a multiple of 64 in [64, 8192]");
   if (c.n_experts < 1 || c.n_experts > 1024)
     return fail(nullptr, DF_MOE_EINVAL, "n_experts must be in [1, 1024]");
   if (c.top_k < 1 || c.top_k > c.n_experts || c.top_k > 32)
     return fail(nullptr, DF_MOE_EINVAL, "top_k must be in [1, min(n_experts, 32)]");
   if (c.n_shared < 0 || c.n_shared > 8)
     return fail(nullptr, DF_MOE_EINVAL, "n_shared must be in [0, 8]");
-  if (c.n_shared > 0 && (c.shared_inter <= 0 || c.shared_inter % 32 ||
+  if (c.n_shared > 0 && (c.shared_inter <= 0 || c.shared_inter % 64 ||
                          c.n_shared * c.shared_inter > 6144))
     return fail(nullptr, DF_MOE_EINVAL,
-                "shared_inter must be a multiple of 32 with n_shared*shared_inter <= 6144");
+                "shared_inter must be a multiple of 64 with n_shared*shared_inter <= 6144");
   if (c.n_layers < 1 || c.n_layers > 64)
     return fail(nullptr, DF_MOE_EINVAL, "n_layers must be in [1, 64]");
   if (c.max_tokens < 1 || c.max_tokens > 4096 || c.max_tokens * c.top_k > 65535)
@@ -328,6 +403,10 @@ int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
     if (!rc && R) rc = dalloc(h, &L.sh_gate, R * H);
     if (!rc && R) rc = dalloc(h, &L.sh_up, R * H);
     if (!rc && R) rc = dalloc(h, &L.sh_down, H * R);
+    if (!rc && R) rc = dalloc(h, &L.sh_gu16, (size_t)c.n_shared * (c.shared_inter / 8) * (H / 16) * 32);
+    if (!rc && R) rc = dalloc(h, &L.sh_gu_rs, (size_t)c.n_shared * (c.shared_inter / 8) * 16);
+    if (!rc && R) rc = dalloc(h, &L.sh_dn16, (size_t)c.n_shared * (H / 16) * (c.shared_inter / 16) * 32);
+    if (!rc && R) rc = dalloc(h, &L.sh_dn_rs, (size_t)c.n_shared * H);
   }
   if (!rc) rc = dalloc(h, &h->router_part, (size_t)h->rsplit.nsplit * Tm * E);
   if (!rc) rc = dalloc(h, &h->logits, Tm * E);
@@ -336,8 +415,34 @@ int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
   if (!rc) rc = dalloc(h, &h->items, Tm * k);
   if (!rc) rc = dalloc(h, &h->n_items, 1);
   if (!rc) rc = dalloc(h, &h->sorted, Tm * k);
+  // layer kernel: used for T <= min(max_tokens, kLayerMaxT) when the device
+  // can hold its cooperative grid
+  const size_t T8 = std::min<size_t>(Tm, kLayerMaxT);
+  const size_t Is = c.n_shared > 0 ? (size_t)c.shared_inter : 0;
+  if (!rc && layer_kernel_grid() > 0) {
+    h->lk_T = (int)T8;
+    h->lk_max_items = (int)std::min<size_t>(T8 * k, E);
+    h->lk_ks_rt = std::max(1, std::min(8, (int)(H / 896)));
+    h->lk_ks_gu = std::min(8, std::max(1, (int)(H / 64) / 14));
+    h->lk_ks_dn = (I / 64) % 2 == 0 && I / 64 >= 8 ? 2 : 1;
+    h->lk_ks_sg = std::min(8, std::max(1, (int)(H / 64) / 14));
+    h->lk_hf_groups = (int)std::max<size_t>(I, Is) / 64;
+    const size_t nd = (size_t)h->lk_max_items + c.n_shared;
+    h->lk_sl = sync_layout(h->lk_max_items, c.n_shared, (int)H, (int)I, (int)Is);
+    rc = dalloc(h, &h->lk_logit_part, (size_t)h->lk_ks_rt * T8 * E);
+    if (!rc) rc = dalloc(h, &h->lk_cand, T8 * ((E + kRouterBlock - 1) / kRouterBlock) * kRouterBlock);
+    if (!rc) rc = dalloc(h, &h->lk_gu_part, (size_t)h->lk_max_items * (I / 8) * h->lk_ks_gu * 32);
+    if (!rc && Is) rc = dalloc(h, &h->lk_sg_part, (size_t)c.n_shared * (Is / 8) * h->lk_ks_sg * 32);
+    if (!rc && Is) rc = dalloc(h, &h->lk_hsh32, (size_t)c.n_shared * T8 * Is);
+    if (!rc) rc = dalloc(h, &h->lk_hf, nd * 2 * h->lk_hf_groups * 2 * 32);
+    if (!rc) rc = dalloc(h, &h->lk_hsc, nd * kLayerMaxT);
+    if (!rc) rc = dalloc(h, &h->lk_sync, h->lk_sl.total);
+    if (!rc && cudaMemset(h->lk_sync, 0, h->lk_sl.total * sizeof(uint32_t)) != cudaSuccess)
+      rc = fail(h, DF_MOE_ECUDA, "cudaMemset failed");
+  }
   if (!rc) rc = dalloc(h, &h->hbuf, Tm * k * I);
-  if (!rc) rc = dalloc(h, &h->part, Tm * k * H);
+  if (!rc) rc = dalloc(h, &h->part, std::max(Tm * k, (size_t)h->lk_ks_dn * T8 * k +
+                                                          (size_t)c.n_shared * T8) * H);
   if (!rc && R) rc = dalloc(h, &h->hsh, Tm * R);
   if (!rc) rc = dalloc(h, &h->ysh, Tm * H);
   if (!rc) rc = dalloc(h, &h->xbuf[0], Tm * H);
@@ -399,6 +504,12 @@ int df_moe_load_experts(df_moe* h, int32_t layer, const df_moe_layer_weights* w,
     CUDA_OR_FAIL(h, cudaMemcpy2DAsync(L.sh_down + sidx * Is, h->R * sizeof(uint16_t),
                                       d, Is * sizeof(uint16_t), Is * sizeof(uint16_t),
                                       H, kind, s));
+    RUN(h, K_REPACK, s, launch_pack_shared(L.sh_gate + sidx * Is * H, L.sh_up + sidx * Is * H,
+                                           L.sh_down + sidx * Is, h->R, (int)H, (int)Is,
+                                           L.sh_gu16 + (size_t)sidx * (Is / 8) * (H / 16) * 32,
+                                           L.sh_gu_rs + (size_t)sidx * (Is / 8) * 16,
+                                           L.sh_dn16 + (size_t)sidx * (H / 16) * (Is / 16) * 32,
+                                           L.sh_dn_rs + (size_t)sidx * H, s));
     L.shared_loaded[sidx] = 1;
   }
   if (w->expert_count > 0) {
@@ -441,9 +552,32 @@ int df_moe_load_experts(df_moe* h, int32_t layer, const df_moe_layer_weights* w,
   return DF_MOE_OK;
 }
 
+static int forward_impl(df_moe* h, const void* x_bf16, int32_t T,
+                        const void* residual_bf16, void* out_bf16, float* out_f32,
+                        int32_t* ids, float* weights, uint16_t* trace_x,
+                        uint16_t* trace_xn, void* stream);
+
 int df_moe_forward(df_moe* h, const void* x_bf16, int32_t T,
                    const void* residual_bf16, void* out_bf16, float* out_f32,
                    int32_t* ids, float* weights, void* stream) {
+  return forward_impl(h, x_bf16, T, residual_bf16, out_bf16, out_f32, ids, weights,
+                      nullptr, nullptr, stream);
+}
+
+int df_moe_forward_trace(df_moe* h, const void* x_bf16, int32_t T, void* out_bf16,
+                         float* out_f32, int32_t* ids, float* weights, void* trace_x,
+                         void* trace_xn, void* stream) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  if (!(h->cfg.flags & DF_MOE_STACK_RMSNORM_RESIDUAL))
+    return fail(h, DF_MOE_EINVAL, "forward_trace needs stack mode");
+  return forward_impl(h, x_bf16, T, nullptr, out_bf16, out_f32, ids, weights,
+                      (uint16_t*)trace_x, (uint16_t*)trace_xn, stream);
+}
+
+static int forward_impl(df_moe* h, const void* x_bf16, int32_t T,
+                        const void* residual_bf16, void* out_bf16, float* out_f32,
+                        int32_t* ids, float* weights, uint16_t* trace_x,
+                        uint16_t* trace_xn, void* stream) {
   if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
   const df_moe_config& c = h->cfg;
   h->launches = 0;
@@ -470,8 +604,14 @@ int df_moe_forward(df_moe* h, const void* x_bf16, int32_t T,
                          out_f32, ids, weights, s);
   }
   const uint16_t* cur = (const uint16_t*)x_bf16;
+  const size_t TH = (size_t)T * c.hidden;
   for (int l = 0; l < c.n_layers; ++l) {
     RUN(h, K_RMSNORM, s, launch_rmsnorm(cur, T, c.hidden, c.rms_eps, h->xn, s));
+    if (trace_x)
+      CUDA_OR_FAIL(h, cudaMemcpyAsync(trace_x + l * TH, cur, TH * 2, cudaMemcpyDeviceToDevice, s));
+    if (trace_xn)
+      CUDA_OR_FAIL(h, cudaMemcpyAsync(trace_xn + l * TH, h->xn, TH * 2,
+                                      cudaMemcpyDeviceToDevice, s));
     const bool last = l == c.n_layers - 1;
     uint16_t* nxt = last ? (uint16_t*)out_bf16 : h->xbuf[l & 1];
     int rc = layer_forward(h, l, h->xn, T, cur, nxt, last ? out_f32 : nullptr,
@@ -522,6 +662,9 @@ int df_moe_sync(df_moe* h, void* stream) {
   CUDA_OR_FAIL(h, cudaMemcpy(&e, h->err, 4, cudaMemcpyDeviceToHost));
   if (e) {
     CUDA_OR_FAIL(h, cudaMemset(h->err, 0, 4));
+    // a layer-kernel call that gave up leaves its tickets mid-count
+    if (h->lk_sync)
+      CUDA_OR_FAIL(h, cudaMemset(h->lk_sync, 0, h->lk_sl.total * sizeof(uint32_t)));
     if (e & DEV_ERR_TIMEOUT)
       return fail(h, DF_MOE_ETIMEOUT, "a bounded device wait gave up");
     return fail(h, DF_MOE_EDEVICE, "device-side check failed (0x%x)", e);

@@ -10,45 +10,44 @@ namespace dfm {
 // HBM layout of an MXFP4 matrix ("fragment layout")
 //
 // A matrix of R rows x K columns (R % 16 == 0, K % 64 == 0) is stored as
-// tiles of 16 rows x K. Inside a tile, columns go in chunks of up to 512
-// (chunk c holds 64-column groups v = 0 .. nv(c)-1), and every 64-column
-// group is 512 bytes: 32 lanes x 16 bytes, lane l = 4 g + t holding, for the
-// four 16-column k-steps s = 0..3 of the group (k0 = 512c + 64v + 16s), the
-// four bytes of an m16n8k16 A fragment:
-//   byte 0: (row g,   cols k0+2t, k0+2t+1)   byte 1: (row g+8, same cols)
-//   byte 2: (row g,   cols k0+2t+8, +9)      byte 3: (row g+8, same cols)
-// Each byte is the canonical byte of that row (low nibble = even column).
-//   codes  offset = j*8K + 512*(8c + v) + 16 l + 4 s + byte
-//   scales offset = j*K/2 + 256 c + g*2*nbc(c) + i,  i < nbc(c): row g,
-//                   block 16c+i; i >= nbc(c): row g+8, block 16c+i-nbc(c)
-// A tile's codes (8K bytes) and scales (K/2 bytes) are each contiguous. The
-// total size equals the canonical one (K/2 + K/32 bytes a row).
+// tiles of 16 rows x K. A tile is K/64 groups of 544 bytes, one per 64
+// columns, so one 16-byte load per lane streams a tile front to back:
+//   bytes [0, 512): codes, 32 lanes x 16 bytes. Lane l = 4g + t holds, for
+//     the four 16-column k-steps s of group G (k0 = 64G + 16s), the four bytes
+//     of an m16n8k16 A fragment:
+//       byte 0: (row g,   cols k0+2t, k0+2t+1)   byte 1: (row g+8, same cols)
+//       byte 2: (row g,   cols k0+2t+8, +9)      byte 3: (row g+8, same cols)
+//     each the canonical byte of that row (low nibble = even column);
+//   bytes [512, 544): E8M0 scales, 8 x 4 bytes; entry g holds
+//       (row g, block 2G), (row g, block 2G+1), (row g+8, block 2G),
+//       (row g+8, block 2G+1).
+//   codes  offset = (j*K/64 + G)*544 + 16 l + 4 s + byte
+//   scales offset = (j*K/64 + G)*544 + 512 + 4 g + i
+// The total size equals the canonical one (K/2 + K/32 bytes a row).
 // ---------------------------------------------------------------------------
-__host__ __device__ inline int mx_nb(int K) { return K >> 5; }
+constexpr int kGroupBytes = 544;
+__host__ __device__ inline int mx_ngroups(int K) { return K >> 6; }
+__host__ __device__ inline size_t mx_tile_bytes(int K) {
+  return (size_t)mx_ngroups(K) * kGroupBytes;
+}
 __host__ __device__ inline int mx_nchunks(int K) { return (K + 511) >> 9; }
 __host__ __device__ inline int mx_nv(int K, int c) {  // 64-column groups of chunk c
   int r = (K >> 6) - 8 * c;
   return r < 8 ? r : 8;
 }
-__host__ __device__ inline int mx_nbc(int K, int c) { return 2 * mx_nv(K, c); }
 
 // Expert span in device layout:
-//   [gate/up codes: 2I/16 tiles, K = H; tile j rows 0-7 = gate rows 8j..8j+7,
+//   [gate/up: 2I/16 tiles, K = H; tile j rows 0-7 = gate rows 8j..8j+7,
 //    rows 8-15 = up rows 8j..8j+7]
-//   [gate/up scales]
-//   [down codes: H/16 tiles, K = I; tile j = rows 16j..16j+15]
-//   [down scales]
+//   [down: H/16 tiles, K = I; tile j = rows 16j..16j+15]
 struct SpanLayout {
-  size_t gu_codes, gu_scales, dn_codes, dn_scales, bytes;
+  size_t gu, dn, bytes;
 };
 __host__ __device__ inline SpanLayout span_layout(int H, int I) {
   SpanLayout L;
-  size_t hi = (size_t)H * (size_t)I;
-  L.gu_codes = 0;
-  L.gu_scales = hi;              // 2I rows * H/2
-  L.dn_codes = hi + hi / 16;     // + 2I rows * H/32
-  L.dn_scales = L.dn_codes + hi / 2;
-  L.bytes = L.dn_scales + hi / 32;
+  L.gu = 0;
+  L.dn = (size_t)(2 * I / 16) * mx_tile_bytes(H);
+  L.bytes = L.dn + (size_t)(H / 16) * mx_tile_bytes(I);
   return L;
 }
 
@@ -64,7 +63,7 @@ constexpr int kOneItemPerExpert = 1 << 20;
 
 enum KernelKind {
   K_ROUTER = 0, K_TOPK, K_GROUP, K_GATEUP, K_DOWN, K_COMBINE, K_SHARED_GU,
-  K_SHARED_DN, K_RMSNORM, K_RESIDUAL, K_REPACK, K_OTHER, K_NKINDS
+  K_SHARED_DN, K_RMSNORM, K_RESIDUAL, K_REPACK, K_OTHER, K_LAYER, K_NKINDS
 };
 
 // Error word bits written by device-side checks.
@@ -135,5 +134,91 @@ cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps,
                            uint16_t* xn, cudaStream_t s);
 cudaError_t launch_repack_span(const uint8_t* src, uint8_t* dst, int n_spans,
                                int H, int I, int inverse, cudaStream_t s);
+
+// ---- the decode-batch layer kernel (k_layer.cu) -----------------------------
+// One persistent cooperative launch computes a whole MoE layer for T <= 8
+// tokens: every warp takes work units from a global queue in dependency order
+// (router, shared gate/up, routed gate/up, shared down, routed down),
+// and the units that finish a result hand it on by a ticket or an
+// epoch-valued flag.
+constexpr int kLayerMaxT = 8;
+
+// Word offsets of the synchronisation block. Tickets are zero between calls
+// (each is reset by the unit that takes its last value); flags hold the epoch
+// of the call that last set them.
+struct SyncLayout {
+  size_t queue, exit, t_rt, t_rtb, f_items, f_hp, t_item, t_rows, t_gu, t_sg, hmax, total;
+};
+constexpr int kRouterBlock = 32;  // experts per router block (one per lane)
+inline SyncLayout sync_layout(int max_items, int n_shared, int H, int I, int Is) {
+  SyncLayout L;
+  size_t o = 0;
+  L.queue = o++;
+  L.exit = o++;
+  L.t_rt = o++;                      // router blocks done
+  L.t_rtb = o; o += 1024 / kRouterBlock;  // router units done, per block
+  L.f_items = o++;
+  const size_t nd = (size_t)max_items + n_shared;  // down items
+  L.f_hp = o; o += nd;
+  L.t_item = o; o += nd;
+  L.t_rows = o; o += (size_t)H / 16;
+  L.t_gu = o; o += (size_t)max_items * (I / 8);
+  L.t_sg = o; o += (size_t)n_shared * (Is > 0 ? Is / 8 : 0);
+  L.hmax = o; o += nd * kLayerMaxT;
+  L.total = o;
+  return L;
+}
+
+struct LayerKernelArgs {
+  int H, E, k, I, Is, n_shared, T, max_items;
+  int ks_rt, ks_gu, ks_sg;   // K slices of router, routed and shared gate/up units
+  int ks_dn;                 // K parts of routed down units (1 or 2)
+  const float* Wr;           // [E][H]
+  const uint8_t* arena;      // E expert spans, fragment layout
+  size_t span_bytes;
+  const uint4* sh_gu;        // [n_shared][Is/8 tiles][H/16 k-steps][32 lanes]
+  const float* sh_gu_rs;     // [n_shared][Is/8][16] row scales
+  const uint4* sh_dn;        // [n_shared][H/16 tiles][Is/16 k-steps][32 lanes]
+  const float* sh_dn_rs;     // [n_shared][H]
+  const uint16_t* x;         // bf16 [T][H]
+  const uint16_t* residual;  // bf16 [T][H] or null
+  float* out_f32;            // [T][H] or null
+  uint16_t* out_bf16;        // [T][H] or null
+  int32_t* ids;              // [T][k]
+  float* w;                  // [T][k]
+  float* logit_part;         // [ks_rt][T][E]
+  float2* cand;              // [T][E/32 blocks][32]: (logit, id bits) of a block's best
+  Item* items;               // [max_items]
+  int32_t* n_items;
+  int32_t* sorted;           // [T*k]
+  float4* gu_part;           // [max_items * I/8][ks_gu][32]
+  float4* sg_part;           // [n_shared * Is/8][ks_sg][32]
+  float* h32;                // [T*k][I]
+  float* hsh32;              // [n_shared][T][Is]
+  uint4* hf;                 // [max_items + n_shared][2][hf_groups][2][32]
+  int hf_groups;             // max(I, Is) / 64
+  float* hsc;                // [max_items + n_shared][8]
+  float* part;               // [ks_dn*T*k + n_shared*T][H]
+  uint32_t* sync;
+  SyncLayout sl;
+  uint32_t epoch;
+  uint32_t* err;
+};
+size_t layer_kernel_smem(int H, int T);
+// Whether the layer kernel can run this shape (shared memory for its rings
+// and the routing merge).
+bool layer_kernel_supports(int H, int T, int k, int E);
+// Blocks per SM and grid of the cooperative launch (0 if it cannot run).
+int layer_kernel_grid();
+cudaError_t launch_layer(const LayerKernelArgs& a, cudaStream_t s);
+
+// Shared experts as f16 fragment tiles with a power-of-two scale per row
+// (k_layout.cu). gate/up/down: bf16 row-major of one shared expert;
+// down rows have `down_ld` elements (the row stride of the concatenated
+// down matrix).
+cudaError_t launch_pack_shared(const uint16_t* gate, const uint16_t* up,
+                               const uint16_t* down, int down_ld, int H, int Is,
+                               uint4* gu_out, float* gu_rs, uint4* dn_out,
+                               float* dn_rs, cudaStream_t s);
 
 }  // namespace dfm

@@ -16,8 +16,9 @@
 //   * Persistent CTAs; a CTA holds NS "slots" = one producer warp + one
 //     consumer warp per 512-column chunk. A slot owns a contiguous range of
 //     tiles (16 rows x K of one expert).
-//   * The producer streams each tile's codes (8K bytes) and scales (K/2)
-//     with cp.async.bulk into a shared-memory ring (mbarriers, bounded waits).
+//   * The producer streams each tile (K/64 groups of codes + scales, one
+//     contiguous block) with cp.async.bulk into a shared-memory ring
+//     (mbarriers, bounded waits).
 //   * Consumers: one 16-byte lds per lane = its A fragments for 4 k-steps;
 //     every 32-column MX block is accumulated by two MMAs into a temporary
 //     that is scaled by 2^(s-127) (per row) in fp32 and added to the result.
@@ -32,6 +33,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "mxfrag.cuh"
 #include "pipeline.cuh"
 
 namespace dfm {
@@ -41,41 +43,6 @@ constexpr int kMaxWarps = 16;
 constexpr int kMaxStages = 8;
 constexpr int kRedRing = 4;  // epilogue reduction ring depth
 constexpr size_t kSmemBudget = 200 * 1024;
-
-__device__ __forceinline__ float pow2i(int s) {  // 2^s for s in [-126, 127]
-  return __uint_as_float((uint32_t)(127 + s) << 23);
-}
-
-// Four bytes = eight E2M1 codes -> four f16x2 (low nibble in the low half).
-__device__ __forceinline__ void decode_word(uint32_t w, uint32_t (&h)[4]) {
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
-      : "r"(w));
-}
-
-// d = A * B (+ c): m16n8k16, f16 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4],
-                                         uint32_t b0, uint32_t b1,
-                                         const float (&c)[4]) {
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1),
-        "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
-}
-
-__device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
 struct MxvArgs {
   const uint8_t* arena;
@@ -100,7 +67,7 @@ struct SlotGeom {
 __host__ __device__ inline SlotGeom slot_geom(int K, int NS) {
   SlotGeom g;
   const int NCH = mx_nchunks(K);
-  g.stage_bytes = (size_t)8 * K + K / 2;
+  g.stage_bytes = mx_tile_bytes(K);
   g.red_bytes = (size_t)kRedRing * NCH * 32 * 16;
   const size_t fixed = g.red_bytes + (2 * kMaxStages + 2 * kRedRing) * 8;
   const size_t per_slot = kSmemBudget / NS;
@@ -160,9 +127,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) mxv_kernel(const MxvArgs a)
   const long long gs = (long long)blockIdx.x * NS + s;
   const int t_begin = (int)(ntiles * gs / nslots);
   const int t_end = (int)(ntiles * (gs + 1) / nslots);
-  const size_t codes_off = MODE == 0 ? L.gu_codes : L.dn_codes;
-  const size_t scales_off = MODE == 0 ? L.gu_scales : L.dn_scales;
-  const uint32_t codes_bytes = 8u * K, scale_bytes = (uint32_t)K / 2;
+  const size_t sec_off = MODE == 0 ? L.gu : L.dn;
+  const uint32_t tile_bytes = (uint32_t)mx_tile_bytes(K);
 
   if (role == NCH) {
     // ---------------- producer: one elected lane ----------------
@@ -181,11 +147,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) mxv_kernel(const MxvArgs a)
         }
         if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
         uint8_t* dst = ring + (size_t)stage * geo.stage_bytes;
-        mbar_arrive_expect_tx(&full[stage], codes_bytes + scale_bytes);
-        bulk_g2s(dst, span + codes_off + (size_t)j * codes_bytes, codes_bytes,
+        mbar_arrive_expect_tx(&full[stage], tile_bytes);
+        bulk_g2s(dst, span + sec_off + (size_t)j * tile_bytes, tile_bytes,
                  &full[stage], pol);
-        bulk_g2s(dst + codes_bytes, span + scales_off + (size_t)j * scale_bytes,
-                 scale_bytes, &full[stage], pol);
         ++issued;
         if (++stage == (uint32_t)S) { stage = 0; phase ^= 1; }
       }
@@ -203,7 +167,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) mxv_kernel(const MxvArgs a)
   // ---------------- consumers: warp `role` = chunk c ----------------
   const int c = role;
   const int g = lane >> 2, t4 = lane & 3;
-  const int nv = mx_nv(K, c), nbc = 2 * nv;
+  const int nv = mx_nv(K, c);
   uint32_t stage = 0, phase = 0;
   int cur_item = -1, loaded_grp = -1, loaded_tok = -2;
   Item it{0, 0, 0, 0};
@@ -230,8 +194,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) mxv_kernel(const MxvArgs a)
     ok = mbar_wait(&full[stage], phase);
     if (!ok) break;
     const uint8_t* tile = ring + (size_t)stage * geo.stage_bytes;
-    // scales of rows g and g+8: 2 bytes a row per 64-column group
-    const uint8_t* sp = tile + codes_bytes + 256 * c + g * 2 * nbc;
 
     for (int grp = 0; grp < it.cnt && ok; grp += GT) {
       // ---- B fragments of this token group (reloaded only when they change)
@@ -311,9 +273,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) mxv_kernel(const MxvArgs a)
 #pragma unroll
       for (int v = 0; v < 8; ++v) {
         if (v < nv) {
-          const uint4 q = lds128(tile + 512 * (8 * c + v) + 16 * lane);
+          const uint8_t* grp_p = tile + kGroupBytes * (8 * c + v);
+          const uint4 q = lds128(grp_p + 16 * lane);
           const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-          const uint32_t sw = lds_u16(sp + 2 * v), sw8 = lds_u16(sp + nbc + 2 * v);
+          // scales: (row g, block 0), (row g, block 1), (row g+8, 0), (row g+8, 1)
+          const uint32_t sc = lds_u32(grp_p + 512 + 4 * g);
 #pragma unroll
           for (int hb = 0; hb < 2; ++hb) {  // the two 32-column blocks of v
             uint32_t a0[4], a1[4];
@@ -322,8 +286,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) mxv_kernel(const MxvArgs a)
             float d[4];
             mma16816(d, a0, bx[4 * v + 2 * hb][0], bx[4 * v + 2 * hb][1], zero);
             mma16816(d, a1, bx[4 * v + 2 * hb + 1][0], bx[4 * v + 2 * hb + 1][1], d);
-            const float sg = __uint_as_float(((sw >> (8 * hb)) & 0xFFu) << 23);
-            const float sg8 = __uint_as_float(((sw8 >> (8 * hb)) & 0xFFu) << 23);
+            const float sg = __uint_as_float(((sc >> (8 * hb)) & 0xFFu) << 23);
+            const float sg8 = __uint_as_float(((sc >> (16 + 8 * hb)) & 0xFFu) << 23);
             acc[0] = fmaf(d[0], sg, acc[0]);
             acc[1] = fmaf(d[1], sg, acc[1]);
             acc[2] = fmaf(d[2], sg8, acc[2]);

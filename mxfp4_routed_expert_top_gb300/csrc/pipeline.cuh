@@ -86,6 +86,12 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t lds_u32(const void* p) {
+  uint32_t v;
+  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)));
+  return v;
+}
+
 __device__ __forceinline__ uint32_t lds_u16(const void* p) {
   uint16_t v;
   asm("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(smem_u32(p)));

@@ -124,6 +124,8 @@ def test_decode_batch1(k3, torch):
     x = _tokens(k3, WL1, 3)
     for t in range(3):
         out, out32, ids, w = _forward(k3.m, x[t:t + 1], 1, torch)
+        # decode batches run as the one fused layer launch
+        assert k3.m.last_launch_count() == 1
         ref = orc.moe_layer(k3.layers[0], x[t:t + 1])
         check_ids_weights(ids, w, ref["ids"], ref["w"])
         check_out(out32, ref["out"])
@@ -132,6 +134,7 @@ def test_decode_batch1(k3, torch):
 def test_decode_batch8(k3, torch):
     x = _tokens(k3, WL2, 8)
     out, out32, ids, w = _forward(k3.m, x, 8, torch)
+    assert k3.m.last_launch_count() == 1
     ref = orc.moe_layer(k3.layers[0], x)
     check_ids_weights(ids, w, ref["ids"], ref["w"])
     check_out(out32, ref["out"])

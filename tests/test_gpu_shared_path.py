@@ -1,0 +1,67 @@
+"""The shared-expert path of the fused layer kernel, on its own.
+
+K3 shape (hidden 7168, two bf16 shared experts of intermediate 1536) with 16
+routed experts whose E2M1 codes are all zero: code 0 is +0, so every routed
+expert contributes exactly 0 whatever the routing, and with top-16 of 16 the
+layer output is the shared experts' sum (plus the residual). In the full
+layer that sum is ~1e-5 of the routed part, so this is where its parity is
+visible. Batch sizes 1, 5 and 8 cover both the one- and two-column-group
+forms of the shared down GEMV.
+
+Bar: relative L2 <= 1e-5 against the oracle's double sum. The kernel's f16
+form of each bf16 weight row (a power-of-two row scale) is exact, products
+of f16 values are exact in fp32, and only fp32 accumulation rounding remains.
+"""
+import numpy as np
+import pytest
+
+import oracle as orc
+import synth
+from moe_setup import bits_to_f64, check_ids_weights, rel_l2, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+WL = synth.WORKLOADS[1]
+E = 16
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as t
+    if not t.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return t
+
+
+@pytest.fixture(scope="module")
+def zero_routed(torch):
+    import mxfp4_routed_expert_top_gb300 as dfm
+    m = dfm.MoE(WL.H, E, E, WL.I, WL.n_shared, WL.Is, max_tokens=8)
+    router = synth.router(WL.seed, WL.wcfg, 0, E, WL.H)
+    shared = [synth.shared(WL.seed, WL.wcfg, 0, s, WL.H, WL.Is) for s in range(WL.n_shared)]
+    zeros = torch.zeros(E * m.span_bytes, dtype=torch.uint8, device="cuda")
+    m.load_experts(0, router=router, shared=shared)
+    m.load_experts(0, experts=zeros, expert_begin=0, expert_count=E, src_is_device=True)
+    torch.cuda.synchronize()
+    yield m, router, shared
+    m.close()
+
+
+@pytest.mark.parametrize("T", [1, 5, 8])
+def test_shared_only_layer(zero_routed, torch, T):
+    m, router, shared = zero_routed
+    x = np.stack([synth.token(WL.seed, 2, 4000 + t, WL.H) for t in range(T)])
+    res = np.stack([synth.token(WL.seed, 2, 4100 + t, WL.H) for t in range(T)])
+    out = torch.empty((T, WL.H), dtype=torch.int16, device="cuda")
+    out32 = torch.empty((T, WL.H), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, E), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    m.forward(to_dev_bf16(x), T, out, ids, w, residual=to_dev_bf16(res), out_f32=out32)
+    m.sync()
+    got = out32.cpu().double().numpy() - bits_to_f64(res)
+    for t in range(T):
+        ref = sum(orc.shared_ffn(*s, bits_to_f64(x[t])) for s in shared)
+        assert rel_l2(got[t], ref) <= 1e-5, "token %d" % t
+    # routing over all 16 experts: the set is all of them, weights a softmax
+    rid, rw = orc.topk_softmax(orc.router_logits(router, x), E)
+    check_ids_weights(ids.cpu().numpy(), w.cpu().double().numpy(), rid, rw)

@@ -1,24 +1,23 @@
 """GPU parity of the stack workload: 8 Kimi-K3-shaped MoE layers resident in
 HBM (~127 GB), each preceded by RMSNorm (eps 1e-6, unit gain) and followed by
-a residual add, decoded at batch 1 and batch 4. Every token is drawn so that
-its routing gap is >= 1e-3 at every layer (oracle logits).
+a residual add, decoded at batch 1 and batch 4.
 
-Tolerances: ids bit-exact at every layer. Where both sides see the same
-layer input — layer 0 of the stack, and every layer of the replay below,
-which feeds the oracle the GPU's own layer inputs — the single-layer bars
-hold: weights within 1e-5, layer output within relative L2 2e-3 and max-abs
-1e-2 x RMS. The end-to-end output of L = 8 layers is the residual sum of the
-layers' outputs, each allowed its own 2e-3 share, so it is held to L x the
-single-layer bars (relative L2 1.6e-2, max-abs 8e-2 x RMS).
+Every layer is checked against the oracle on that layer's inputs as the
+device computed them (forward_trace records them): ids bit-exact (tokens
+whose 16th/17th logit gap on those inputs is below 1e-3 are redrawn), weights
+within 1e-5, and the layer's result within the single-layer bars. The next
+layer's input is the bf16 rounding of residual + layer output: it must equal
+the rounding of the oracle's sum except where the two sums straddle a bf16
+rounding boundary (at most one ulp, and rarely).
 
-Through the whole stack the layer inputs themselves drift apart: the
-residual stream is rounded to bf16 after every layer (|x| ~ 1e4, one bf16
-ulp = 64), and where the GPU's fp32 sum and the oracle's double fall on
-different sides of a rounding boundary (relative gap ~1e-6..1e-5 against an
-ulp of 2^-8, i.e. ~0.1% of the elements) that element of the next
-normalised input differs by one ulp (2^-8 relative). Each layer adds such
-flips and propagates the earlier ones, so after several layers a logit can
-move by ~1e-3, and the end-to-end weights of layers >= 1 are held to 1e-3.
+Why not one oracle chain end to end: the synthetic stack is chaotic. Layer
+outputs (~1e5) dwarf the normalised inputs, the residual stream is rounded
+to bf16 after every layer (one ulp = 2^-8 relative), and an fp32-vs-double
+difference that flips one rounding changes the next layer's normalised input
+by 2^-8 on that element. Measured on this stack, the weight difference
+between two correct implementations grows 5-20x per layer (4e-8 at layer 0,
+~1e-3 by layer 7) until a routing choice flips. Only layer 0, whose inputs
+agree exactly, is compared with the oracle's own chain.
 """
 import numpy as np
 import pytest
@@ -26,7 +25,7 @@ import pytest
 import oracle as orc
 import synth
 from moe_setup import (Setup, bits_to_f64, check_ids_weights, check_out,
-                       draw_stack_token, to_dev_bf16)
+                       draw_stack_token, gap_ok, to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -50,15 +49,19 @@ def stack(torch):
     torch.cuda.empty_cache()
 
 
-def _forward(m, x, T, torch):
-    out = torch.empty((T, WL.H), dtype=torch.int16, device="cuda")
-    out32 = torch.empty((T, WL.H), dtype=torch.float32, device="cuda")
-    ids = torch.empty((WL.L, T, WL.k), dtype=torch.int32, device="cuda")
-    w = torch.empty((WL.L, T, WL.k), dtype=torch.float32, device="cuda")
-    m.forward(to_dev_bf16(x), T, out, ids, w, out_f32=out32)
+def _forward_trace(m, x, T, torch):
+    L, H, k = WL.L, WL.H, WL.k
+    out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    out32 = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    ids = torch.empty((L, T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((L, T, k), dtype=torch.float32, device="cuda")
+    tx = torch.empty((L, T, H), dtype=torch.int16, device="cuda")
+    txn = torch.empty((L, T, H), dtype=torch.int16, device="cuda")
+    m.forward_trace(to_dev_bf16(x), T, out, ids, w, trace_x=tx, trace_xn=txn, out_f32=out32)
     m.sync()
-    return (out.cpu().numpy().view(np.uint16), out32.cpu().double().numpy(),
-            ids.cpu().numpy(), w.cpu().double().numpy())
+    u16 = lambda a: a.cpu().numpy().view(np.uint16)
+    return (u16(out), out32.cpu().double().numpy(), ids.cpu().numpy(),
+            w.cpu().double().numpy(), u16(tx), u16(txn))
 
 
 def test_rmsnorm_step(stack, torch):
@@ -76,19 +79,45 @@ def test_rmsnorm_step(stack, torch):
 
 @pytest.mark.parametrize("T", [1, 4])
 def test_stack_decode(stack, torch, T):
-    xs, refs = [], []
-    for t in range(T):
-        x, ref = draw_stack_token(stack, 1000 + 10 * T + t)
-        xs.append(x)
-        refs.append(ref)
-    x = np.stack(xs)
-    out, out32, ids, w = _forward(stack.m, x, T, torch)
-    for t in range(T):
-        for l in range(WL.L):
-            check_ids_weights(ids[l, t:t + 1], w[l, t:t + 1], refs[t]["ids"][l],
-                              refs[t]["w"][l], wtol=1e-5 if l == 0 else 1e-3)
-    last = np.concatenate([r["last"] for r in refs])
-    check_out(out32, last, rel_l2=WL.L * 2e-3, max_abs_rms=WL.L * 1e-2)
+    first = 1000 + 10 * T
+    redraw = [0] * T
+    for _ in range(synth.gen.REDRAWS_PER_TOKEN):
+        x = np.stack([synth.token(WL.seed, WL.cfg_id, first + t, WL.H, redraw=redraw[t])
+                      for t in range(T)])
+        out, out32, ids, w, tx, txn = _forward_trace(stack.m, x, T, torch)
+        # the gap rule, on the device's own layer inputs
+        bad = {t for l in range(WL.L) for t in range(T)
+               if not gap_ok(orc.router_logits(stack.routers[l], txn[l, t:t + 1]), WL.k)}
+        if not bad:
+            break
+        for t in bad:
+            redraw[t] += 1
+    else:
+        pytest.fail("no token set passed the gap rule")
+    assert np.array_equal(tx[0], x)
+    # layer 0 sees the same input on both sides: the oracle's own chain agrees
+    chain = orc.moe_stack(stack.layers, x, WL.eps)
+    check_ids_weights(ids[0], w[0], chain["ids"][0], chain["w"][0])
+    for l in range(WL.L):
+        ref = orc.moe_layer(stack.layers[l], txn[l], residual=tx[l])
+        check_ids_weights(ids[l], w[l], ref["ids"], ref["w"])
+        if l + 1 < WL.L:
+            want = np.array([[orc.f64_to_bf16(v) for v in row] for row in ref["out"]],
+                            dtype=np.uint16)
+            got = tx[l + 1]
+            # one ulp of the rounded sum, plus a slack of 1e-3 x RMS(layer
+            # output) for elements where residual and output nearly cancel
+            # (there a tiny difference in the output is many ulps of the sum)
+            y_ref = ref["out"] - bits_to_f64(tx[l])
+            slack = 1e-3 * np.sqrt(np.mean(y_ref ** 2, axis=-1, keepdims=True))
+            ulp = np.abs(bits_to_f64(want)) * 2.0 ** -7
+            diff = np.abs(bits_to_f64(got) - bits_to_f64(want))
+            assert np.all(diff <= ulp + slack), "layer %d: next input off by > 1 ulp" % l
+            assert np.mean(got == want) >= 0.99, "layer %d: next input" % l
+        else:
+            # the last layer's fp32 result, as the layer output plus residual
+            y = out32 - bits_to_f64(tx[l])
+            check_out(y, ref["out"] - bits_to_f64(tx[l]))
     # the bf16 output is the RNE rounding of the fp32 output
     rne = torch.from_numpy(out32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(out, rne)

@@ -34,7 +34,7 @@ def test_route_noalloc_matches_handle_path(torch):
     router = synth.router(wl.seed, wl.wcfg, 0, E, H)
     router_dev = torch.from_numpy(router).cuda()
     # a handle with the same router, for the existing entry points
-    with dfm.MoE(H, E, k, 32, 0, 0, max_tokens=8) as m:
+    with dfm.MoE(H, E, k, 64, 0, 0, max_tokens=8) as m:
         m.load_experts(0, router=router)
         for call, T in enumerate((8, 3)):   # two calls in a row
             x = np.stack([synth.token(wl.seed, wl.cfg_id, 40000 + 10 * call + t, H)
