@@ -52,6 +52,8 @@ def parse():
     p.add_argument("--tokens", type=int, default=0,
                    help="override the tokens per step of the workload (the stack "
                         "workload decodes at batch 1 and batch 4)")
+    p.add_argument("--fused", action="store_true",
+                   help="decode batches as one fused layer launch (DF_MOE_FUSED_DECODE)")
     p.add_argument("--experts", type=int, default=0,
                    help="profiling aid: override the routed-expert count (same "
                         "per-token work, smaller resident set); not a bench line")
@@ -264,9 +266,9 @@ def run_ours(args):
     if args.tokens:
         wl = dataclasses.replace(wl, T=args.tokens, name=wl.name + "-t%d" % args.tokens)
     T = wl.T
+    flags = (dfm.STACK_RMSNORM_RESIDUAL if wl.stack else 0) | (dfm.FUSED_DECODE if args.fused else 0)
     m = dfm.MoE(wl.H, wl.E, wl.k, wl.I, wl.n_shared, wl.Is, n_layers=wl.L,
-                max_tokens=max(T, 4), rms_eps=wl.eps,
-                flags=dfm.STACK_RMSNORM_RESIDUAL if wl.stack else 0, device=local)
+                max_tokens=max(T, 4), rms_eps=wl.eps, flags=flags, device=local)
     stream = torch.cuda.current_stream()
     load_workload(m, wl, torch, stream)
 
@@ -370,6 +372,7 @@ def run_ours(args):
                    "inter": wl.I, "shared": wl.n_shared, "tokens_per_step": T,
                    "layers": wl.L, "weights": "mxfp4 e2m1+e8m0/32, shared bf16",
                    "l2": "flushed (256 MiB write) before every timed step",
+                   "decode_path": "fused" if args.fused else "chain",
                    "parallelism": "replicas" if ws > 1 else "single-gpu"},
         "layer_hbm": {"achieved_gbs": round(layer_gbs, 1), "bytes_per_step": int(lb),
                       "frac_of_measured": round(layer_gbs / peak, 4),

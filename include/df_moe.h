@@ -62,6 +62,11 @@ extern "C" {
  * rounded to bf16; after it the layer output is added to x and rounded to
  * bf16. `out` is the final x. */
 #define DF_MOE_STACK_RMSNORM_RESIDUAL 1u
+/* Decode batches (T <= 8) run as one persistent cooperative launch per layer
+ * (router, selection, routed and shared experts and the combine in a single
+ * kernel) instead of the default chain of kernels on two streams. Same
+ * results within the stated tolerances. */
+#define DF_MOE_FUSED_DECODE 2u
 
 typedef struct df_moe df_moe; /* opaque, library-owned */
 
@@ -75,7 +80,7 @@ typedef struct {
   int32_t n_layers;     /* L >= 1                                              */
   int32_t max_tokens;   /* largest T a forward call may use (1..4096)          */
   float rms_eps;        /* stack mode only                                     */
-  uint32_t flags;       /* DF_MOE_STACK_RMSNORM_RESIDUAL or 0                  */
+  uint32_t flags;       /* DF_MOE_STACK_RMSNORM_RESIDUAL | DF_MOE_FUSED_DECODE */
 } df_moe_config;
 
 /* Weights of one layer, any subset per call (NULL / 0 = leave unchanged). */

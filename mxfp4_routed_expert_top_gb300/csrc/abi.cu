@@ -84,6 +84,10 @@ struct df_moe {
   uint32_t* lk_sync = nullptr;
   SyncLayout lk_sl{};
   uint32_t epoch = 0;
+  // the shared experts' chain runs on a second stream, on sh_ctas SMs
+  cudaStream_t s2 = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  int sms = 0;
   // host-API device buffers
   uint16_t* hx = nullptr;
   uint16_t* hres = nullptr;
@@ -220,13 +224,13 @@ int route(df_moe* h, int l, const uint16_t* x, int T, int32_t* ids, float* w,
 }
 
 int shared_part(df_moe* h, int l, const uint16_t* x, int T, float* ysh,
-                cudaStream_t s) {
+                cudaStream_t s, int max_ctas = 0) {
   const df_moe_config& c = h->cfg;
   const LayerBufs& L = h->layers[l];
   RUN(h, K_SHARED_GU, s, launch_shared_gateup(L.sh_gate, L.sh_up, h->R,
-                                              c.hidden, x, T, h->hsh, h->err, s));
+                                              c.hidden, x, T, h->hsh, h->err, s, max_ctas));
   RUN(h, K_SHARED_DN, s, launch_shared_down(L.sh_down, c.hidden, h->R, h->hsh,
-                                            T, ysh, h->err, s));
+                                            T, ysh, h->err, s, max_ctas));
   return DF_MOE_OK;
 }
 
@@ -293,19 +297,44 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
   if (T <= h->lk_T && layer_kernel_supports(c.hidden, T, c.top_k, c.n_experts))
     return layer_kernel_forward(h, l, x, T, residual, out_bf16, out_f32, ids, w, s);
   const int tg = T == 1 ? 1 : kOneItemPerExpert;
-  int rc = route(h, l, x, T, ids, w, s, nullptr, tg);
+  const int max_items = (T == 1 && tg == 1) ? c.top_k : std::min(T * c.top_k, c.n_experts);
+  // At T = 1 the shared experts, which do not depend on the routing, run on
+  // a second stream and a share of the SMs, beside the router -> gate/up ->
+  // down chain: each chain's ramp and tail, and the router's latency, are
+  // then covered by the other chain's streaming. The share is the shared
+  // bytes' part of the bytes with the routed chain's counted twice (per SM it
+  // streams at about half the rate once the router's latency is included;
+  // measured at K3 shape the optimum lies at 22-30 of 152 SMs). For T > 1 the
+  // shared GEMVs (fp32 FMA per token) become compute-bound on few SMs, so the
+  // chains run one after the other.
+  const double sh_bytes = (double)c.n_shared * 3.0 * c.shared_inter * c.hidden * 2.0;
+  const double rt_bytes = (double)c.n_experts * c.hidden * 4.0 + (double)max_items * h->span_bytes;
+  const int sh_ctas = (int)(h->sms * sh_bytes / (sh_bytes + 2.0 * rt_bytes) + 0.5);
+  const bool split = T == 1 && c.n_shared > 0 && h->s2 && sh_ctas >= 8 && sh_ctas <= h->sms / 2;
+  int rc = 0;
+  if (split) CUDA_OR_FAIL(h, cudaEventRecord(h->ev_fork, s));
+  // the router first: its latency is on the critical path, so its CTAs are
+  // dispatched before the shared chain's
+  rc = route(h, l, x, T, ids, w, s, nullptr, tg);
   if (rc) return rc;
-  if (c.n_shared > 0) {
+  if (split) {
+    CUDA_OR_FAIL(h, cudaStreamWaitEvent(h->s2, h->ev_fork, 0));
+    rc = shared_part(h, l, x, T, h->ysh, h->s2, sh_ctas);
+    if (rc) return rc;
+    CUDA_OR_FAIL(h, cudaEventRecord(h->ev_join, h->s2));
+  }
+  if (c.n_shared > 0 && !split) {
     rc = shared_part(h, l, x, T, h->ysh, s);
     if (rc) return rc;
   }
-  const int max_items = (T == 1 && tg == 1) ? c.top_k : std::min(T * c.top_k, c.n_experts);
+  const int rt_ctas = split ? h->sms - sh_ctas : 0;
   RUN(h, K_GATEUP, s, launch_gateup(L.arena, h->span_bytes, c.hidden, c.inter,
                                     c.top_k, x, h->items, h->n_items, max_items,
-                                    h->sorted, h->hbuf, tg, h->err, s));
+                                    h->sorted, h->hbuf, tg, h->err, s, rt_ctas));
   RUN(h, K_DOWN, s, launch_down(L.arena, h->span_bytes, c.hidden, c.inter,
                                 h->items, h->n_items, max_items, h->sorted,
-                                h->hbuf, h->part, tg, h->err, s));
+                                h->hbuf, h->part, tg, h->err, s, rt_ctas));
+  if (split) CUDA_OR_FAIL(h, cudaStreamWaitEvent(s, h->ev_join, 0));
   RUN(h, K_COMBINE, s, launch_combine(h->part, w, T, c.top_k, c.hidden,
                                       c.n_shared > 0 ? h->ysh : nullptr,
                                       residual, out_f32, out_bf16, s));
@@ -339,6 +368,9 @@ void df_moe_destroy(df_moe* h) {
     cudaEventDestroy(p.b);
   }
   for (auto e : h->event_pool) cudaEventDestroy(e);
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->s2) cudaStreamDestroy(h->s2);
   for (void* p : h->allocs) cudaFree(p);
   cudaSetDevice(prev);
   delete h;
@@ -369,7 +401,7 @@ int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
                 "max_tokens must be in [1, 4096] with max_tokens*top_k <= 65535");
   if (c.n_layers > 1 && !(c.flags & DF_MOE_STACK_RMSNORM_RESIDUAL))
     return fail(nullptr, DF_MOE_EINVAL, "n_layers > 1 needs DF_MOE_STACK_RMSNORM_RESIDUAL");
-  if ((c.flags & ~DF_MOE_STACK_RMSNORM_RESIDUAL) != 0)
+  if ((c.flags & ~(DF_MOE_STACK_RMSNORM_RESIDUAL | DF_MOE_FUSED_DECODE)) != 0)
     return fail(nullptr, DF_MOE_EINVAL, "unknown flags");
   if ((c.flags & DF_MOE_STACK_RMSNORM_RESIDUAL) && !(c.rms_eps >= 0.0f))
     return fail(nullptr, DF_MOE_EINVAL, "rms_eps must be >= 0");
@@ -419,7 +451,7 @@ int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
   // can hold its cooperative grid
   const size_t T8 = std::min<size_t>(Tm, kLayerMaxT);
   const size_t Is = c.n_shared > 0 ? (size_t)c.shared_inter : 0;
-  if (!rc && layer_kernel_grid() > 0) {
+  if (!rc && (c.flags & DF_MOE_FUSED_DECODE) && layer_kernel_grid() > 0) {
     h->lk_T = (int)T8;
     h->lk_max_items = (int)std::min<size_t>(T8 * k, E);
     h->lk_ks_rt = std::max(1, std::min(8, (int)(H / 896)));
@@ -456,6 +488,13 @@ int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
   if (!rc) rc = dalloc(h, &h->hout32, Tm * H);
   if (!rc) rc = dalloc(h, &h->hids, (size_t)c.n_layers * Tm * k);
   if (!rc) rc = dalloc(h, &h->hw, (size_t)c.n_layers * Tm * k);
+  if (!rc) {
+    cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, cuda_device);
+    if (cudaStreamCreateWithFlags(&h->s2, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess)
+      rc = fail(h, DF_MOE_ECUDA, "stream or event creation failed");
+  }
   if (!rc && (cudaMemset(h->err, 0, sizeof(uint32_t)) != cudaSuccess ||
               cudaMemset(h->counter, 0, sizeof(unsigned int)) != cudaSuccess))
     rc = fail(h, DF_MOE_ECUDA, "cudaMemset failed");

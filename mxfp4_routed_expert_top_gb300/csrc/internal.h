@@ -73,6 +73,8 @@ enum : uint32_t { DEV_ERR_RANGE = 1u, DEV_ERR_TIMEOUT = 2u };
 void set_thread_error(const char* msg);
 
 // ---- launchers (each returns cudaGetLastError()) ---------------------------
+// max_ctas (persistent kernels): at most this many CTAs, one per SM (0: all
+// SMs), so that two chains of kernels can run side by side on split SMs.
 // Router column split: `nsplit` column ranges of `split_len` (a multiple of
 // 128, at most 2048) so that E * nsplit warps keep HBM busy.
 struct RouterSplit { int split_len, nsplit; };
@@ -115,21 +117,22 @@ cudaError_t launch_gateup(const uint8_t* arena, size_t span_bytes, int H,
                           int I, int k, const uint16_t* x, const Item* items,
                           const int32_t* n_items, int max_items,
                           const int32_t* sorted, float* hbuf, int tg,
-                          uint32_t* err, cudaStream_t s);
+                          uint32_t* err, cudaStream_t s, int max_ctas = 0);
 cudaError_t launch_down(const uint8_t* arena, size_t span_bytes, int H, int I,
                         const Item* items, const int32_t* n_items,
                         int max_items, const int32_t* sorted,
                         const float* hbuf, float* part, int tg, uint32_t* err,
-                        cudaStream_t s);
+                        cudaStream_t s, int max_ctas = 0);
 cudaError_t launch_combine(const float* part, const float* w, int T, int k,
                            int H, const float* ysh, const uint16_t* residual,
                            float* out_f32, uint16_t* out_bf16, cudaStream_t s);
 cudaError_t launch_shared_gateup(const uint16_t* gate, const uint16_t* up,
                                  int R, int H, const uint16_t* x, int T,
-                                 float* hsh, uint32_t* err, cudaStream_t s);
+                                 float* hsh, uint32_t* err, cudaStream_t s,
+                                 int max_ctas = 0);
 cudaError_t launch_shared_down(const uint16_t* down, int H, int K,
                                const float* hsh, int T, float* ysh,
-                               uint32_t* err, cudaStream_t s);
+                               uint32_t* err, cudaStream_t s, int max_ctas = 0);
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps,
                            uint16_t* xn, cudaStream_t s);
 cudaError_t launch_repack_span(const uint8_t* src, uint8_t* dst, int n_spans,

@@ -377,7 +377,7 @@ int num_sms() {
 }
 
 template <int MODE>
-cudaError_t launch_mxv(const MxvArgs& a, int max_items, cudaStream_t s) {
+cudaError_t launch_mxv(const MxvArgs& a, int max_items, cudaStream_t s, int max_ctas) {
   const int K = MODE == 0 ? a.H : a.I;
   const int NCH = mx_nchunks(K);
   const int NS = slots_per_cta(K);
@@ -396,6 +396,7 @@ cudaError_t launch_mxv(const MxvArgs& a, int max_items, cudaStream_t s) {
   const long long max_tiles = (long long)max_items * tpi;
   int grid = (int)((max_tiles + NS - 1) / NS);
   if (grid > num_sms()) grid = num_sms();
+  if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
   if (grid < 1) grid = 1;
   mxv_kernel<MODE><<<grid, threads, smem, s>>>(a);
   return cudaGetLastError();
@@ -407,18 +408,18 @@ cudaError_t launch_gateup(const uint8_t* arena, size_t span_bytes, int H,
                           int I, int k, const uint16_t* x, const Item* items,
                           const int32_t* n_items, int max_items,
                           const int32_t* sorted, float* hbuf, int /*tg*/,
-                          uint32_t* err, cudaStream_t s) {
+                          uint32_t* err, cudaStream_t s, int max_ctas) {
   MxvArgs a{arena, span_bytes, H, I, k, x, nullptr, items, n_items, sorted, hbuf, err};
-  return launch_mxv<0>(a, max_items, s);
+  return launch_mxv<0>(a, max_items, s, max_ctas);
 }
 
 cudaError_t launch_down(const uint8_t* arena, size_t span_bytes, int H, int I,
                         const Item* items, const int32_t* n_items,
                         int max_items, const int32_t* sorted,
                         const float* hbuf, float* part, int /*tg*/, uint32_t* err,
-                        cudaStream_t s) {
+                        cudaStream_t s, int max_ctas) {
   MxvArgs a{arena, span_bytes, H, I, 0, nullptr, hbuf, items, n_items, sorted, part, err};
-  return launch_mxv<1>(a, max_items, s);
+  return launch_mxv<1>(a, max_items, s, max_ctas);
 }
 
 cudaError_t launch_combine(const float* part, const float* w, int T, int k,

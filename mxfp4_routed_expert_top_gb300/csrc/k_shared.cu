@@ -289,7 +289,7 @@ int num_sms_b() {
 }
 
 template <int MODE, bool ONE>
-cudaError_t launch_bfv_t(const BfvArgs& a, cudaStream_t s) {
+cudaError_t launch_bfv_t(const BfvArgs& a, cudaStream_t s, int max_ctas) {
   const int NW = bfv_warps(a.K);
   const int NS = bfv_slots(a.K);
   const BfvGeom geo = bfv_geom(a.K, NS);
@@ -304,13 +304,15 @@ cudaError_t launch_bfv_t(const BfvArgs& a, cudaStream_t s) {
   const int ntiles = MODE == 0 ? a.rows / 2 : a.rows / kRows;
   int grid = (ntiles + NS - 1) / NS;
   if (grid > num_sms_b()) grid = num_sms_b();
+  if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
   bfv_kernel<MODE, ONE><<<grid, NS * (NW + 1) * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
 template <int MODE>
-cudaError_t launch_bfv(const BfvArgs& a, cudaStream_t s) {
-  return a.T == 1 ? launch_bfv_t<MODE, true>(a, s) : launch_bfv_t<MODE, false>(a, s);
+cudaError_t launch_bfv(const BfvArgs& a, cudaStream_t s, int max_ctas) {
+  return a.T == 1 ? launch_bfv_t<MODE, true>(a, s, max_ctas)
+                  : launch_bfv_t<MODE, false>(a, s, max_ctas);
 }
 
 // xn = RNE_bf16(x / sqrt(mean(x^2) + eps)); one block per token.
@@ -341,14 +343,14 @@ rmsnorm_kernel(const uint16_t* __restrict__ x, int H, float eps,
 
 cudaError_t launch_shared_gateup(const uint16_t* gate, const uint16_t* up,
                                  int R, int H, const uint16_t* x, int T,
-                                 float* hsh, uint32_t* err, cudaStream_t s) {
-  return launch_bfv<0>(BfvArgs{gate, up, R, H, x, T, hsh, err}, s);
+                                 float* hsh, uint32_t* err, cudaStream_t s, int max_ctas) {
+  return launch_bfv<0>(BfvArgs{gate, up, R, H, x, T, hsh, err}, s, max_ctas);
 }
 
 cudaError_t launch_shared_down(const uint16_t* down, int H, int K,
                                const float* hsh, int T, float* ysh,
-                               uint32_t* err, cudaStream_t s) {
-  return launch_bfv<1>(BfvArgs{down, nullptr, H, K, hsh, T, ysh, err}, s);
+                               uint32_t* err, cudaStream_t s, int max_ctas) {
+  return launch_bfv<1>(BfvArgs{down, nullptr, H, K, hsh, T, ysh, err}, s, max_ctas);
 }
 
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps,

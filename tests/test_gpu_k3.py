@@ -1,7 +1,8 @@
 """GPU parity at full Kimi-K3 layer size: hidden 7168, 896 MXFP4 experts
 (17,547,264 B each, 15.7 GB resident), top-16, two bf16 shared experts.
 
-Batch 1, batch 8 and batch 512 run on the same layer. The oracle computes
+Batch 1, batch 8 and batch 512 run on the same layer, on both decode paths
+(the chain of kernels and the fused layer kernel). The oracle computes
 sampled tokens in full; routing (ids, weights) is checked for every token.
 Tolerances as stated for the layer: ids bit-exact, weights 1e-5, output
 relative L2 <= 2e-3 and max-abs <= 1e-2 x RMS. Steps: relative L2 <= 1e-5
@@ -28,9 +29,11 @@ def torch():
     return t
 
 
-@pytest.fixture(scope="module")
-def k3(torch):
-    s = Setup(WL1, max_tokens=512)
+# every test runs on both decode paths: the default chain of kernels (shared
+# experts on a second stream) and the fused single-launch layer kernel
+@pytest.fixture(scope="module", params=["chain", "fused"])
+def k3(torch, request):
+    s = Setup(WL1, max_tokens=512, fused=request.param == "fused")
     yield s
     s.close()
     torch.cuda.empty_cache()
@@ -124,8 +127,8 @@ def test_decode_batch1(k3, torch):
     x = _tokens(k3, WL1, 3)
     for t in range(3):
         out, out32, ids, w = _forward(k3.m, x[t:t + 1], 1, torch)
-        # decode batches run as the one fused layer launch
-        assert k3.m.last_launch_count() == 1
+        # with the fused flag, decode batches run as the one layer launch
+        assert (k3.m.last_launch_count() == 1) == k3.fused
         ref = orc.moe_layer(k3.layers[0], x[t:t + 1])
         check_ids_weights(ids, w, ref["ids"], ref["w"])
         check_out(out32, ref["out"])
@@ -134,7 +137,7 @@ def test_decode_batch1(k3, torch):
 def test_decode_batch8(k3, torch):
     x = _tokens(k3, WL2, 8)
     out, out32, ids, w = _forward(k3.m, x, 8, torch)
-    assert k3.m.last_launch_count() == 1
+    assert (k3.m.last_launch_count() == 1) == k3.fused
     ref = orc.moe_layer(k3.layers[0], x)
     check_ids_weights(ids, w, ref["ids"], ref["w"])
     check_out(out32, ref["out"])

@@ -1,4 +1,4 @@
-"""The shared-expert path of the fused layer kernel, on its own.
+"""The shared-expert path of the layer, on its own (both decode paths).
 
 K3 shape (hidden 7168, two bf16 shared experts of intermediate 1536) with 16
 routed experts whose E2M1 codes are all zero: code 0 is +0, so every routed
@@ -33,10 +33,11 @@ def torch():
     return t
 
 
-@pytest.fixture(scope="module")
-def zero_routed(torch):
+@pytest.fixture(scope="module", params=["chain", "fused"])
+def zero_routed(torch, request):
     import mxfp4_routed_expert_top_gb300 as dfm
-    m = dfm.MoE(WL.H, E, E, WL.I, WL.n_shared, WL.Is, max_tokens=8)
+    flags = dfm.FUSED_DECODE if request.param == "fused" else 0
+    m = dfm.MoE(WL.H, E, E, WL.I, WL.n_shared, WL.Is, max_tokens=8, flags=flags)
     router = synth.router(WL.seed, WL.wcfg, 0, E, WL.H)
     shared = [synth.shared(WL.seed, WL.wcfg, 0, s, WL.H, WL.Is) for s in range(WL.n_shared)]
     zeros = torch.zeros(E * m.span_bytes, dtype=torch.uint8, device="cuda")

@@ -40,10 +40,10 @@ def torch():
     return t
 
 
-@pytest.fixture(scope="module")
-def stack(torch):
+@pytest.fixture(scope="module", params=["chain", "fused"])
+def stack(torch, request):
     torch.cuda.empty_cache()
-    s = Setup(WL, max_tokens=4)
+    s = Setup(WL, max_tokens=4, fused=request.param == "fused")
     yield s
     s.close()
     torch.cuda.empty_cache()
