@@ -54,6 +54,9 @@ def parse():
                         "workload decodes at batch 1 and batch 4)")
     p.add_argument("--fused", action="store_true",
                    help="decode batches as one fused layer launch (DF_MOE_FUSED_DECODE)")
+    p.add_argument("--mma-sync-prefill", action="store_true",
+                   help="batches above 8 tokens on the register-fragment expert kernels "
+                        "instead of the tcgen05 GEMMs (DF_MOE_PREFILL_MMA_SYNC)")
     p.add_argument("--experts", type=int, default=0,
                    help="profiling aid: override the routed-expert count (same "
                         "per-token work, smaller resident set); not a bench line")
@@ -78,6 +81,12 @@ def gateup_bytes(wl, n_union, T):
     return n_union * per_expert + T * wl.H * 2 + T * wl.k * wl.I * 4
 
 
+def gateup_flops(wl, T):
+    """Useful flops of the routed gate/up contraction: 2 per multiply-add of
+    each of the T*k assignments' 2I x H products."""
+    return 2.0 * T * wl.k * 2 * wl.I * wl.H
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -85,6 +94,14 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def measured_bf16_tflops():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        return float(json.load(open(path))["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 def csrc_hash():
@@ -266,7 +283,8 @@ def run_ours(args):
     if args.tokens:
         wl = dataclasses.replace(wl, T=args.tokens, name=wl.name + "-t%d" % args.tokens)
     T = wl.T
-    flags = (dfm.STACK_RMSNORM_RESIDUAL if wl.stack else 0) | (dfm.FUSED_DECODE if args.fused else 0)
+    flags = ((dfm.STACK_RMSNORM_RESIDUAL if wl.stack else 0) | (dfm.FUSED_DECODE if args.fused else 0)
+             | (dfm.PREFILL_MMA_SYNC if args.mma_sync_prefill else 0))
     m = dfm.MoE(wl.H, wl.E, wl.k, wl.I, wl.n_shared, wl.Is, n_layers=wl.L,
                 max_tokens=max(T, 4), rms_eps=wl.eps, flags=flags, device=local)
     stream = torch.cuda.current_stream()
@@ -350,10 +368,12 @@ def run_ours(args):
     peak, peak_kind = measured_peaks()
     ms = dev_s_max / args.steps * 1e3
     lb = layer_bytes(wl, u_mean, T) * wl.L
-    # dominant kernel: the fused layer kernel (decode batches), else the
-    # routed gate/up GEMV of the multi-kernel path
+    # dominant kernel: the fused layer kernel (decode batches), the routed
+    # gate/up GEMM (tcgen05, larger batches), else the routed gate/up GEMV
     if kt.get("layer", (0, 0.0))[0]:
         dom, dom_bytes = "layer", layer_bytes(wl, u_mean, T)
+    elif kt.get("gemm_gateup", (0, 0.0))[0]:
+        dom, dom_bytes = "gemm_gateup", gateup_bytes(wl, u_mean, T)
     else:
         dom, dom_bytes = "expert_gateup", gateup_bytes(wl, u_mean, T)
     dom_n, dom_ms = kt[dom]
@@ -373,6 +393,7 @@ def run_ours(args):
                    "layers": wl.L, "weights": "mxfp4 e2m1+e8m0/32, shared bf16",
                    "l2": "flushed (256 MiB write) before every timed step",
                    "decode_path": "fused" if args.fused else "chain",
+                   "prefill_path": "mma_sync" if args.mma_sync_prefill else "tcgen05",
                    "parallelism": "replicas" if ws > 1 else "single-gpu"},
         "layer_hbm": {"achieved_gbs": round(layer_gbs, 1), "bytes_per_step": int(lb),
                       "frac_of_measured": round(layer_gbs / peak, 4),
@@ -384,6 +405,7 @@ def run_ours(args):
                      "bytes_per_launch": int(dom_bytes),
                      "traffic": recorded_traffic(dom)},
         "kernels": kernels,
+        "tensor": tensor_use(kt, wl, T),
         "e2e": {"value": round(e2e_tokens / e2e_max, 2), "unit": UNIT,
                 "h2d_bytes_per_step": T * wl.H * 2,
                 "d2h_bytes_per_step": T * wl.H * 2 + wl.L * T * wl.k * 8},
@@ -393,6 +415,20 @@ def run_ours(args):
     }
     m.close()
     return res
+
+
+def tensor_use(kt, wl, T):
+    """Useful bf16 tensor throughput of the gate/up GEMM (tcgen05 path only):
+    the assignments' flops over its average launch time, against the
+    measured dense bf16 peak. At a few tokens per expert the GEMM is HBM
+    bound, so this fraction is small by construction."""
+    n, t = kt.get("gemm_gateup", (0, 0.0))
+    if not n:
+        return None
+    peak, src = measured_bf16_tflops()
+    tf = gateup_flops(wl, T) / (t / n / 1e3) / 1e12
+    return {"kernel": "gemm_gateup", "achieved": round(tf, 2), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(tf / peak, 4), "peak_source": src}
 
 
 def run_reference(args):

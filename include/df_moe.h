@@ -67,6 +67,12 @@ extern "C" {
  * kernel) instead of the default chain of kernels on two streams. Same
  * results within the stated tolerances. */
 #define DF_MOE_FUSED_DECODE 2u
+/* Batches above the decode range (T > 8) run the routed experts on the
+ * register-fragment (mma.sync) kernels of the decode chain instead of the
+ * default grouped GEMMs on the 5th-generation tensor cores (tcgen05, fp32
+ * accumulators in tensor memory). For comparison; same results within the
+ * stated tolerances. */
+#define DF_MOE_PREFILL_MMA_SYNC 4u
 
 typedef struct df_moe df_moe; /* opaque, library-owned */
 
@@ -80,7 +86,8 @@ typedef struct {
   int32_t n_layers;     /* L >= 1                                              */
   int32_t max_tokens;   /* largest T a forward call may use (1..4096)          */
   float rms_eps;        /* stack mode only                                     */
-  uint32_t flags;       /* DF_MOE_STACK_RMSNORM_RESIDUAL | DF_MOE_FUSED_DECODE */
+  uint32_t flags;       /* DF_MOE_STACK_RMSNORM_RESIDUAL | DF_MOE_FUSED_DECODE |
+                           DF_MOE_PREFILL_MMA_SYNC                              */
 } df_moe_config;
 
 /* Weights of one layer, any subset per call (NULL / 0 = leave unchanged). */
@@ -209,7 +216,7 @@ DF_MOE_API int df_moe_read_expert_span(df_moe* h, int32_t layer, int32_t expert,
  * With timing on, every kernel launch of forward is bracketed by CUDA events
  * on its stream; df_moe_timing_get returns, per kernel kind, the launches and
  * the summed device time since the last reset. */
-#define DF_MOE_KERNEL_KINDS 13
+#define DF_MOE_KERNEL_KINDS 15
 DF_MOE_API int df_moe_timing_enable(df_moe* h, int on);
 DF_MOE_API int df_moe_timing_reset(df_moe* h);
 DF_MOE_API int df_moe_timing_get(df_moe* h, int kind, const char** name,

@@ -29,6 +29,8 @@ struct LayerBufs {
   float* sh_gu_rs = nullptr;    // [n_s][Is/8][16]
   uint4* sh_dn16 = nullptr;     // [n_s][H/16][Is/16][32]
   float* sh_dn_rs = nullptr;    // [n_s][H]
+  uint8_t* eref = nullptr;      // [E][2I + H] row reference exponents (tcgen05 GEMMs)
+  ChunkMap map_gu{}, map_dn{};  // tensor maps of the arena's tiles (tcgen05 GEMMs)
   bool router_loaded = false;
   std::vector<uint8_t> shared_loaded;
   std::vector<uint8_t> expert_loaded;
@@ -43,7 +45,8 @@ struct Pending {
 const char* kKindNames[K_NKINDS] = {"router", "topk", "group", "expert_gateup",
                                     "expert_down", "combine", "shared_gateup",
                                     "shared_down", "rmsnorm", "residual",
-                                    "repack", "other", "layer"};
+                                    "repack", "other", "layer", "gemm_gateup",
+                                    "gemm_down"};
 
 }  // namespace
 
@@ -84,6 +87,12 @@ struct df_moe {
   uint32_t* lk_sync = nullptr;
   SyncLayout lk_sl{};
   uint32_t epoch = 0;
+  // tcgen05 GEMMs for batches above the decode range
+  bool gemm = false;
+  uint16_t* g_xg = nullptr;      // [Tmax*k][H] f16: gate/up B rows in expert order
+  uint16_t* g_hh = nullptr;      // [Tmax*k][2][I] f16: down B rows in expert order
+  float* g_bsc = nullptr;        // [Tmax*k] their power-of-two row scales
+  ChunkMap bmap_gu{}, bmap_dn{};
   // the shared experts' chain runs on a second stream, on sh_ctas SMs
   cudaStream_t s2 = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
@@ -223,6 +232,51 @@ int route(df_moe* h, int l, const uint16_t* x, int T, int32_t* ids, float* w,
   return DF_MOE_OK;
 }
 
+// Routed experts of a batch grouped one item per expert (or per token at
+// T = 1). Above the decode range the grouped tcgen05 GEMMs run them, unless
+// the handle asks for the register-fragment kernels.
+bool use_gemm(const df_moe* h, int T, int tg) {
+  return h->gemm && T > kLayerMaxT && tg == kOneItemPerExpert;
+}
+
+int expert_gateup(df_moe* h, int l, const uint16_t* x, int T, int max_items, int tg,
+                  float* hbuf, cudaStream_t s, int max_ctas = 0) {
+  const df_moe_config& c = h->cfg;
+  const uint8_t* arena = h->layers[l].arena;
+  if (use_gemm(h, T, tg)) {
+    RUN(h, K_OTHER, s, launch_prep_x(x, T * c.top_k, c.hidden, c.top_k, h->sorted, h->g_xg,
+                                     h->g_bsc, s));
+    RUN(h, K_GEMM_GU, s, launch_gemm_gateup(h->layers[l].map_gu, h->bmap_gu, arena,
+                                            h->span_bytes, h->layers[l].eref, c.hidden, c.inter,
+                                            c.top_k, h->g_bsc, h->items, h->n_items, max_items,
+                                            h->sorted, hbuf, h->err, s));
+  } else {
+    RUN(h, K_GATEUP, s, launch_gateup(arena, h->span_bytes, c.hidden, c.inter, c.top_k, x,
+                                      h->items, h->n_items, max_items, h->sorted, hbuf, tg,
+                                      h->err, s, max_ctas));
+  }
+  return DF_MOE_OK;
+}
+
+int expert_down(df_moe* h, int l, const float* hbuf, int T, int max_items, int tg,
+                cudaStream_t s, int max_ctas = 0) {
+  const df_moe_config& c = h->cfg;
+  const uint8_t* arena = h->layers[l].arena;
+  if (use_gemm(h, T, tg)) {
+    RUN(h, K_OTHER, s, launch_split_h(hbuf, T * c.top_k, c.inter, h->sorted, h->g_hh, h->g_bsc,
+                                      s));
+    RUN(h, K_GEMM_DN, s, launch_gemm_down(h->layers[l].map_dn, h->bmap_dn, arena,
+                                          h->span_bytes, h->layers[l].eref, c.hidden, c.inter,
+                                          c.top_k, h->g_bsc, h->items, h->n_items, max_items,
+                                          h->sorted, h->part, h->err, s));
+  } else {
+    RUN(h, K_DOWN, s, launch_down(arena, h->span_bytes, c.hidden, c.inter, h->items,
+                                  h->n_items, max_items, h->sorted, hbuf, h->part, tg, h->err,
+                                  s, max_ctas));
+  }
+  return DF_MOE_OK;
+}
+
 int shared_part(df_moe* h, int l, const uint16_t* x, int T, float* ysh,
                 cudaStream_t s, int max_ctas = 0) {
   const df_moe_config& c = h->cfg;
@@ -328,12 +382,10 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
     if (rc) return rc;
   }
   const int rt_ctas = split ? h->sms - sh_ctas : 0;
-  RUN(h, K_GATEUP, s, launch_gateup(L.arena, h->span_bytes, c.hidden, c.inter,
-                                    c.top_k, x, h->items, h->n_items, max_items,
-                                    h->sorted, h->hbuf, tg, h->err, s, rt_ctas));
-  RUN(h, K_DOWN, s, launch_down(L.arena, h->span_bytes, c.hidden, c.inter,
-                                h->items, h->n_items, max_items, h->sorted,
-                                h->hbuf, h->part, tg, h->err, s, rt_ctas));
+  rc = expert_gateup(h, l, x, T, max_items, tg, h->hbuf, s, rt_ctas);
+  if (rc) return rc;
+  rc = expert_down(h, l, h->hbuf, T, max_items, tg, s, rt_ctas);
+  if (rc) return rc;
   if (split) CUDA_OR_FAIL(h, cudaStreamWaitEvent(s, h->ev_join, 0));
   RUN(h, K_COMBINE, s, launch_combine(h->part, w, T, c.top_k, c.hidden,
                                       c.n_shared > 0 ? h->ysh : nullptr,
@@ -401,7 +453,8 @@ int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
                 "max_tokens must be in [1, 4096] with max_tokens*top_k <= 65535");
   if (c.n_layers > 1 && !(c.flags & DF_MOE_STACK_RMSNORM_RESIDUAL))
     return fail(nullptr, DF_MOE_EINVAL, "n_layers > 1 needs DF_MOE_STACK_RMSNORM_RESIDUAL");
-  if ((c.flags & ~(DF_MOE_STACK_RMSNORM_RESIDUAL | DF_MOE_FUSED_DECODE)) != 0)
+  if ((c.flags & ~(DF_MOE_STACK_RMSNORM_RESIDUAL | DF_MOE_FUSED_DECODE |
+                   DF_MOE_PREFILL_MMA_SYNC)) != 0)
     return fail(nullptr, DF_MOE_EINVAL, "unknown flags");
   if ((c.flags & DF_MOE_STACK_RMSNORM_RESIDUAL) && !(c.rms_eps >= 0.0f))
     return fail(nullptr, DF_MOE_EINVAL, "rms_eps must be >= 0");
@@ -439,6 +492,24 @@ int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
     if (!rc && R) rc = dalloc(h, &L.sh_gu_rs, (size_t)c.n_shared * (c.shared_inter / 8) * 16);
     if (!rc && R) rc = dalloc(h, &L.sh_dn16, (size_t)c.n_shared * (H / 16) * (c.shared_inter / 16) * 32);
     if (!rc && R) rc = dalloc(h, &L.sh_dn_rs, (size_t)c.n_shared * H);
+  }
+  // tcgen05 GEMMs: batches above the decode range, unless asked otherwise
+  h->gemm = Tm > (size_t)kLayerMaxT && !(c.flags & DF_MOE_PREFILL_MMA_SYNC) &&
+            gemm_supported(c.hidden, c.inter);
+  if (h->gemm) {
+    for (int l = 0; l < c.n_layers && !rc; ++l) {
+      LayerBufs& L = h->layers[l];
+      rc = dalloc(h, &L.eref, gemm_eref_bytes(c.n_experts, c.hidden, c.inter));
+      if (!rc && !make_chunk_maps(L.arena, h->span_bytes, c.hidden, c.inter, c.n_experts,
+                                  &L.map_gu, &L.map_dn))
+        rc = fail(h, DF_MOE_ECUDA, "tensor map encoding failed");
+    }
+    if (!rc) rc = dalloc(h, &h->g_xg, Tm * k * H);
+    if (!rc) rc = dalloc(h, &h->g_hh, Tm * k * 2 * I);
+    if (!rc) rc = dalloc(h, &h->g_bsc, Tm * k);
+    if (!rc && !make_b_maps(h->g_xg, h->g_hh, (int)(Tm * k), c.hidden, c.inter, &h->bmap_gu,
+                            &h->bmap_dn))
+      rc = fail(h, DF_MOE_ECUDA, "tensor map encoding failed");
   }
   if (!rc) rc = dalloc(h, &h->router_part, (size_t)h->rsplit.nsplit * Tm * E);
   if (!rc) rc = dalloc(h, &h->logits, Tm * E);
@@ -581,6 +652,11 @@ int df_moe_load_experts(df_moe* h, int32_t layer, const df_moe_layer_weights* w,
       }
       CUDA_OR_FAIL(h, cudaStreamSynchronize(s));
     }
+    if (h->gemm)
+      RUN(h, K_REPACK, s, launch_row_ref(dst, h->span_bytes, c.hidden, c.inter, w->expert_count,
+                                         L.eref + (size_t)w->expert_begin *
+                                                      (2 * (size_t)c.inter + c.hidden),
+                                         s));
     for (int e = w->expert_begin; e < w->expert_begin + w->expert_count; ++e) {
       if (!L.expert_loaded[e]) {
         L.expert_loaded[e] = 1;
@@ -773,11 +849,8 @@ int df_moe_step_expert_gateup(df_moe* h, int32_t layer, const void* x_bf16,
   RUN(h, K_GROUP, s, launch_group(ids, T, c.top_k, c.n_experts, nullptr, nullptr,
                                   nullptr, nullptr, h->items, h->n_items,
                                   h->sorted, tg, s));
-  RUN(h, K_GATEUP, s, launch_gateup(h->layers[layer].arena, h->span_bytes,
-                                    c.hidden, c.inter, c.top_k,
-                                    (const uint16_t*)x_bf16, h->items, h->n_items,
-                                    std::min(T * c.top_k, c.n_experts), h->sorted, hbuf, tg, h->err, s));
-  return DF_MOE_OK;
+  return expert_gateup(h, layer, (const uint16_t*)x_bf16, T,
+                       std::min(T * c.top_k, c.n_experts), tg, hbuf, s);
 }
 
 int df_moe_step_expert_down(df_moe* h, int32_t layer, const float* hbuf,
@@ -796,10 +869,8 @@ int df_moe_step_expert_down(df_moe* h, int32_t layer, const float* hbuf,
   RUN(h, K_GROUP, s, launch_group(ids, T, c.top_k, c.n_experts, nullptr, nullptr,
                                   nullptr, nullptr, h->items, h->n_items,
                                   h->sorted, tg, s));
-  RUN(h, K_DOWN, s, launch_down(h->layers[layer].arena, h->span_bytes, c.hidden,
-                                c.inter, h->items, h->n_items,
-                                std::min(T * c.top_k, c.n_experts), h->sorted,
-                                hbuf, h->part, tg, h->err, s));
+  const int rc = expert_down(h, layer, hbuf, T, std::min(T * c.top_k, c.n_experts), tg, s);
+  if (rc) return rc;
   RUN(h, K_COMBINE, s, launch_combine(h->part, weights, T, c.top_k, c.hidden,
                                       nullptr, nullptr, y, nullptr, s));
   return DF_MOE_OK;

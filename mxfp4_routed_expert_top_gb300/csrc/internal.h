@@ -63,7 +63,8 @@ constexpr int kOneItemPerExpert = 1 << 20;
 
 enum KernelKind {
   K_ROUTER = 0, K_TOPK, K_GROUP, K_GATEUP, K_DOWN, K_COMBINE, K_SHARED_GU,
-  K_SHARED_DN, K_RMSNORM, K_RESIDUAL, K_REPACK, K_OTHER, K_LAYER, K_NKINDS
+  K_SHARED_DN, K_RMSNORM, K_RESIDUAL, K_REPACK, K_OTHER, K_LAYER, K_GEMM_GU,
+  K_GEMM_DN, K_NKINDS
 };
 
 // Error word bits written by device-side checks.
@@ -137,6 +138,47 @@ cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps,
                            uint16_t* xn, cudaStream_t s);
 cudaError_t launch_repack_span(const uint8_t* src, uint8_t* dst, int n_spans,
                                int H, int I, int inverse, cudaStream_t s);
+
+// ---- routed experts of large batches on tcgen05 (k_gemm.cu) ----------------
+// Grouped GEMMs over the items (one per expert, all of its tokens): the MXFP4
+// weights decoded to f16 (times 2^(e - r), r a per-row reference exponent)
+// straight into tensor memory, multiplied by f16 token columns on the tensor
+// cores with fp32 accumulators in tensor memory. Same outputs as
+// launch_gateup / launch_down with one item per expert.
+bool gemm_supported(int H, int I);
+// A TMA tensor map (CUtensorMap), opaque here.
+struct alignas(64) ChunkMap {
+  uint64_t w[16];
+};
+// Tensor maps of the gate/up and down tiles of an arena of E spans; false if
+// the driver's encoder is unavailable or refuses the shape.
+bool make_chunk_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E,
+                     ChunkMap* gu, ChunkMap* dn);
+// Row reference exponents: [E][2I + H] bytes, fragment row order (gate/up
+// tile rows, then down rows), written by launch_row_ref for `n` spans.
+size_t gemm_eref_bytes(int n_experts, int H, int I);
+cudaError_t launch_row_ref(const uint8_t* spans, size_t span_bytes, int H, int I, int n,
+                           uint8_t* eref, cudaStream_t s);
+// B rows in expert order (R = T*k assignments, row p for sorted[p]):
+// gate/up xg [R][H] f16 = x[sorted[p] / k] * 2^-s_p (exact), bsc[p] = 2^s_p;
+cudaError_t launch_prep_x(const uint16_t* x, int R, int H, int k, const int32_t* sorted,
+                          uint16_t* xg, float* bsc, cudaStream_t s);
+// down hh [R][2][I] f16 = high and low parts of h[sorted[p]] * 2^-s_p.
+cudaError_t launch_split_h(const float* h, int R, int I, const int32_t* sorted, uint16_t* hh,
+                           float* bsc, cudaStream_t s);
+// Tensor maps of xg ([R][H]) and hh ([2R][I]) for rows allocated for R.
+bool make_b_maps(const uint16_t* xg, const uint16_t* hh, int R, int H, int I, ChunkMap* gu,
+                 ChunkMap* dn);
+cudaError_t launch_gemm_gateup(const ChunkMap& map, const ChunkMap& bmap, const uint8_t* arena,
+                               size_t span_bytes, const uint8_t* eref, int H, int I, int k,
+                               const float* bsc, const Item* items, const int32_t* n_items,
+                               int max_items, const int32_t* sorted, float* hbuf, uint32_t* err,
+                               cudaStream_t s);
+cudaError_t launch_gemm_down(const ChunkMap& map, const ChunkMap& bmap, const uint8_t* arena,
+                             size_t span_bytes, const uint8_t* eref, int H, int I, int k,
+                             const float* bsc, const Item* items, const int32_t* n_items,
+                             int max_items, const int32_t* sorted, float* part, uint32_t* err,
+                             cudaStream_t s);
 
 // ---- the decode-batch layer kernel (k_layer.cu) -----------------------------
 // One persistent cooperative launch computes a whole MoE layer for T <= 8
