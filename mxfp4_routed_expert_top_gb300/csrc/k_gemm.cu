@@ -19,33 +19,36 @@
 // items list them), so that a block's columns are consecutive rows: one
 // TMA tile per chunk.
 //
-// One persistent CTA per SM, 736 threads in roles; a unit is one expert x one
+// One persistent CTA per SM, 832 threads in roles; a unit is one expert x one
 // M tile of 128 weight rows (8 of the 16-row fragment tiles: 64 gate + 64 up
 // rows, or 128 down rows) x all of the expert's tokens, in blocks of at most
 // 32 columns (32 tokens for gate/up, 16 for down: hi and lo columns):
 //   warp 20     streams each 64-column chunk of the unit's 8 tiles
 //               (8 x 544 B, one 4-d TMA tensor copy) into a ring of raw
 //               stages;
-//   warps 4-19  decode: four groups of four warps take every fourth chunk,
-//               each warp two tiles (the 32 tensor memory lanes it may
-//               write): E2M1 -> f16 (cvt), times the block's 2^(e - r)
-//               (mul.f16x2), stored straight into tensor memory
-//               (tcgen05.st .16x128b: the register fragment of the 16-row
-//               tile lands in its 16 lanes, K along the columns) — the A
-//               operand never touches shared memory;
 //   warp 21     loads the B tile of the chunk (32 rows x 64 f16, one 2-d TMA
 //               copy in the 128-byte swizzle layout) into a ring of
 //               shared-memory stages;
-//   warp 22     issues tcgen05.mma (A from tensor memory, B from shared
-//               memory, M = 128, N = 16 or 32, K = 16) into one of two fp32
-//               accumulators in tensor memory, and commits each chunk to the
-//               mbarrier that frees its A and B stages;
-// The copy and MMA warps run their loops on all 32 lanes with warp-uniform
-// values, one lane issuing: a single thread's chain of asynchronous
-// instructions costs far more per instruction than the work it starts.
-//   warps 0-3   read a finished accumulator (tcgen05.ld, one row per thread)
-//               and write h = silu(gate) * up, or the down rows per token,
-//               while the MMAs of the next block run on the other one.
+//   warps 4-19  four groups of four warps; group g takes the chunks n with
+//               n % 4 == g. Each warp decodes two tiles (the 32 tensor
+//               memory lanes it may write): E2M1 -> f16 (cvt), times the
+//               block's 2^(e - r) (mul.f16x2), stored straight into tensor
+//               memory (tcgen05.st .16x128b: the register fragment of the
+//               16-row tile lands in its 16 lanes, K along the columns), so
+//               the A operand never touches shared memory;
+//   warps 22-25 one per decoder group: issues the group's tcgen05.mma (A from
+//               tensor memory, B from shared memory, M = 128, N = 16 or 32,
+//               K = 16) into the group's own fp32 accumulator, one of two in
+//               tensor memory per group (one issuing thread per accumulator
+//               keeps its MMAs in order);
+//   warps 0-3   read a finished block (tcgen05.ld, one row per thread), sum
+//               the groups' accumulators and write h = silu(gate) * up, or the
+//               down rows per token, while the next block accumulates in the
+//               other buffers.
+// Barrier waits and fences cost a few hundred cycles of latency each; four
+// MMA warps overlap them, where a single one would serialise them.
+// Asynchronous instructions are issued by one elected lane of a converged
+// warp.
 // Every wait is bounded; on a timeout the CTA records it, lets its copies
 // and MMAs land, frees its tensor memory and leaves.
 #include <cuda.h>
@@ -66,8 +69,8 @@ constexpr int kEpiWarps = 4;                   // warps 0-3
 constexpr int kDecWarp0 = 4, kDecWarps = 16;   // warps 4-19
 constexpr int kDecGroups = 4;                  // groups of 4 warps, every fourth chunk
 constexpr int kGroupWarps = kDecWarps / kDecGroups;
-constexpr int kRawWarp = 20, kBWarp = 21, kMmaWarp = 22;
-constexpr int kThr = 23 * 32;
+constexpr int kRawWarp = 20, kBWarp = 21, kMmaWarp0 = 22;  // MMA warps 22-25
+constexpr int kThr = 26 * 32;
 constexpr int kM = 128;                        // weight rows per unit
 constexpr int kTilesPerM = kM / 16;
 constexpr int kCodeBytes = kTilesPerM * kGroupBytes;  // 4352: one 64-column chunk
@@ -79,11 +82,10 @@ constexpr int kSB = 16;                        // B stages (shared memory)
 constexpr int kNMax = 32;                      // MMA N at most (B rows of a block)
 constexpr int kBBytes = kNMax * 64 * 2;        // B stage: 32 rows x 64 f16 (the TMA box)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCol = 0;                // two accumulators of kNMax columns
-constexpr uint32_t kACol = 2 * kNMax;          // kA A stages of 32 columns
+constexpr uint32_t kAccCol = 0;                // per group two accumulators of kNMax columns
+constexpr uint32_t kACol = 2 * kDecGroups * kNMax;  // kA A stages of 32 columns
 
 static_assert(kACol + 32 * kA <= kTmemCols, "tensor memory");
-static_assert(kA <= kSB, "A stage reuse waits on the commit of chunk n - kA");
 static_assert(kRawBytes % 16 == 0, "bulk copies need 16-byte aligned stages");
 
 struct GemmArgs {
@@ -104,11 +106,14 @@ struct GemmArgs {
 
 struct Smem {
   uint64_t raw_full[kRaw], raw_empty[kRaw];
-  uint64_t a_full[kA];    // A stage decoded
-  uint64_t b_full[kSB];   // B stage gathered
-  uint64_t done[kSB];     // MMAs of chunk n (n mod kSB) complete: frees B stage
-                          // n mod kSB and A stage n mod kA
-  uint64_t acc_full[2], acc_empty[2];
+  uint64_t a_full[kA], a_free[kA];    // A stage decoded / read by its MMAs
+  uint64_t b_full[kSB], b_free[kSB];  // B stage loaded / read by its MMAs
+  uint64_t acc_full[2];   // every chunk of a block committed (one arrival per chunk)
+  // Epilogue warps that have finished reading a block, summed over blocks.
+  // A counter, not a barrier: the four MMA warps run at their own pace, and a
+  // warp that is two blocks ahead of the epilogue would read a barrier's
+  // parity as the phase before last.
+  uint32_t epi_done;
   uint32_t tmem;
   int err;
 };
@@ -192,6 +197,35 @@ __device__ __forceinline__ int block_rows(const Item& it, int tb) {
 }
 __device__ __forceinline__ int mma_n(int rows) { return (rows + 15) & ~15; }
 
+// Bounded wait that sleeps between polls: for the warps off the critical
+// path, whose polling would otherwise crowd the shared-memory pipe that the
+// MMA warp's own barrier operations go through.
+constexpr uint32_t kSleepWaitLimit = 1u << 22;
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  for (uint32_t i = 0; i < kSleepWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    __nanosleep(ns);
+  }
+  return false;
+}
+
+// Bounded wait until a shared counter reaches `target` (acquire).
+__device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t target) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(ctr)) : "memory");
+    if (v >= target) return true;
+  }
+  return false;
+}
+
+// A value the compiler can treat as warp-uniform (lane 0's), for the
+// operands of instructions that take uniform registers.
+__device__ __forceinline__ uint32_t uni(uint32_t v) { return __shfl_sync(0xffffffffu, v, 0); }
+__device__ __forceinline__ uint64_t uni64(uint64_t v) {
+  return ((uint64_t)uni((uint32_t)(v >> 32)) << 32) | uni((uint32_t)v);
+}
+
 __device__ __forceinline__ void set_err(Smem* sm) { *(volatile int*)&sm->err = 1; }
 __device__ __forceinline__ bool has_err(Smem* sm) { return *(volatile int*)&sm->err != 0; }
 
@@ -211,19 +245,20 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
 // follow them, issued by one elected lane of a converged warp in one
 // straight-line block: A at tensor memory column a (+8 per step), B from the
 // descriptor bd (+bstep per step), accumulating into d unless `fresh`;
-// commits to `done` and, if `acc` is nonzero, to `acc` as well.
+// commits to the A stage, the B stage and the block barriers. A commit
+// tracks the issuing thread's own MMAs, so every chunk commits to the block
+// barrier (one arrival per chunk).
 __device__ __forceinline__ void mma_chunk(uint32_t d, uint32_t a, uint64_t bd, uint64_t bstep,
-                                          uint32_t idesc, uint32_t fresh, uint32_t done,
-                                          uint32_t acc) {
+                                          uint32_t idesc, uint32_t fresh, uint32_t a_free,
+                                          uint32_t b_free, uint32_t acc) {
   asm volatile(
       "{\n\t"
-      ".reg .pred e, p0, pt, pa;\n\t"
+      ".reg .pred e, p0, pt;\n\t"
       ".reg .b32 r, a1, a2, a3;\n\t"
       ".reg .b64 b1, b2, b3;\n\t"
       "elect.sync r|e, 0xffffffff;\n\t"
       "setp.eq.u32 p0, %5, 0;\n\t"
       "setp.eq.u32 pt, %5, %5;\n\t"
-      "setp.ne.and.u32 pa, %7, 0, e;\n\t"
       "add.u32 a1, %1, 8;\n\t"
       "add.u32 a2, %1, 16;\n\t"
       "add.u32 a3, %1, 24;\n\t"
@@ -235,9 +270,10 @@ __device__ __forceinline__ void mma_chunk(uint32_t d, uint32_t a, uint64_t bd, u
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %4, pt;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %4, pt;\n\t"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
-      "@pa tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t"
       "}" ::"r"(d),
-      "r"(a), "l"(bd), "l"(bstep), "r"(idesc), "r"(fresh), "r"(done), "r"(acc)
+      "r"(a), "l"(bd), "l"(bstep), "r"(idesc), "r"(fresh), "r"(a_free), "r"(b_free), "r"(acc)
       : "memory");
 }
 
@@ -273,7 +309,7 @@ __device__ void role_raw(const GemmArgs& a, int n_items, Smem* sm, uint8_t* raw,
   int e = 0, e_item = -1;
   while (!w.done) {
     const uint32_t rs = n % kRaw;
-    bool ok = n < (uint32_t)kRaw || mbar_wait(&sm->raw_empty[rs], ((n / kRaw) - 1) & 1);
+    bool ok = n < (uint32_t)kRaw || mbar_wait_sleep(&sm->raw_empty[rs], ((n / kRaw) - 1) & 1, 128);
     ok = __all_sync(0xffffffffu, ok) && !has_err(sm);
     if (!ok) {
       set_err(sm);
@@ -305,10 +341,11 @@ __device__ void role_raw(const GemmArgs& a, int n_items, Smem* sm, uint8_t* raw,
           ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;\n\t"
           "@pr cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
           " [%12], [%9], %13, [%6], %7;\n\t"
-          "}" ::"r"(dst),
-          "l"(&a.map), "r"(0), "r"(w.c), "r"(kTilesPerM * w.mt), "r"(e), "r"(bar), "l"(pol),
-          "r"(ref), "l"(rsrc), "r"((uint32_t)(kCodeBytes + kRefBytes)), "r"((uint32_t)kCodeBytes),
-          "r"(dst + (uint32_t)kCodeBytes), "r"((uint32_t)kRefBytes)
+          "}" ::"r"(uni(dst)),
+          "l"(&a.map), "r"(0), "r"(uni(w.c)), "r"(uni(kTilesPerM * w.mt)), "r"(uni(e)),
+          "r"(uni(bar)), "l"(pol), "r"(uni(ref)), "l"(uni64((uint64_t)rsrc)),
+          "r"((uint32_t)(kCodeBytes + kRefBytes)), "r"((uint32_t)kCodeBytes),
+          "r"(uni(dst + (uint32_t)kCodeBytes)), "r"((uint32_t)kRefBytes)
           : "memory");
     }
     ++n;
@@ -335,8 +372,22 @@ __device__ __forceinline__ void load_tile(uint32_t tile_s, int lane, uint32_t (&
 __device__ __forceinline__ void decode_tile(const uint32_t (&cw)[4], uint32_t sc, uint32_t rg,
                                             uint32_t rg8, uint32_t (&v)[16]) {
   // scale entry g: (row g, block 2G), (row g, 2G+1), (row g+8, 2G), (row g+8, 2G+1)
-  const uint32_t f0 = pow2_h2(sc & 0xFF, rg), f1 = pow2_h2((sc >> 8) & 0xFF, rg);
-  const uint32_t f80 = pow2_h2((sc >> 16) & 0xFF, rg8), f81 = pow2_h2(sc >> 24, rg8);
+  uint32_t f0, f1, f80, f81;
+  const int d0 = (int)(sc & 0xFF) - (int)rg, d1 = (int)((sc >> 8) & 0xFF) - (int)rg;
+  const int d2 = (int)((sc >> 16) & 0xFF) - (int)rg8, d3 = (int)(sc >> 24) - (int)rg8;
+  if (min(min(d0, d1), min(d2, d3)) >= -14 && __vcmpeq4(sc, 0xFFFFFFFFu) == 0) {
+    // 2^d as a normal f16, both halves: exponent field d + 15 (d <= 13 by
+    // the choice of r)
+    f0 = (uint32_t)(d0 + 15) * 0x04000400u;
+    f1 = (uint32_t)(d1 + 15) * 0x04000400u;
+    f80 = (uint32_t)(d2 + 15) * 0x04000400u;
+    f81 = (uint32_t)(d3 + 15) * 0x04000400u;
+  } else {  // NaN scales, or blocks far below the row's largest
+    f0 = pow2_h2(sc & 0xFF, rg);
+    f1 = pow2_h2((sc >> 8) & 0xFF, rg);
+    f80 = pow2_h2((sc >> 16) & 0xFF, rg8);
+    f81 = pow2_h2(sc >> 24, rg8);
+  }
 #pragma unroll
   for (int ks = 0; ks < 4; ++ks) {
     uint32_t hv[4];
@@ -362,28 +413,26 @@ __device__ __forceinline__ void tmem_st_16x128b_x8(uint32_t ta, const uint32_t (
 template <int MODE>
 __device__ void role_decode(const GemmArgs& a, int n_items, Smem* sm, const uint8_t* raw,
                             uint32_t tmem, int warp, int lane) {
-  const int q = warp & 3;                       // tensor memory lanes 32q..32q+31
+  const int q = warp & 3;                            // tensor memory lanes 32q..32q+31
   const int grp = (warp - kDecWarp0) / kGroupWarps;  // chunks n with n % kDecGroups == grp
   const int g = lane >> 2;
+  const int NC = walk_nc<MODE>(a);
   Walk w;
   walk_start<MODE>(a, n_items, w);
-  uint32_t n = 0;
+  uint32_t nb0 = 0;               // global index of the block's chunk 0
   uint32_t rf[4] = {0, 0, 0, 0};  // reference exponents: rows g, g+8 of tiles 2q, 2q+1
-  while (!w.done) {
-    if ((int)(n % kDecGroups) == grp) {
+  bool ok = true;
+  while (!w.done && ok) {
+    // this group's chunks of the block: n = nb0 + c with n % kDecGroups == grp
+    for (int c = (grp - (int)(nb0 % kDecGroups) + kDecGroups) % kDecGroups; c < NC; c += kDecGroups) {
+      const uint32_t n = nb0 + c;
       const uint32_t rs = n % kRaw, s = n % kA;
-      bool ok = mbar_wait(&sm->raw_full[rs], (n / kRaw) & 1);
-      if (ok && n >= (uint32_t)kA) {
-        const uint32_t m = n - kA;  // the chunk that used this A stage last
-        ok = mbar_wait(&sm->done[m % kSB], (m / kSB) & 1);
-      }
+      ok = mbar_wait(&sm->raw_full[rs], (n / kRaw) & 1);
+      if (ok && n >= (uint32_t)kA) ok = mbar_wait(&sm->a_free[s], ((n / kA) - 1) & 1);
       ok = __all_sync(0xffffffffu, ok) && !has_err(sm);
-      if (!ok) {
-        set_err(sm);
-        break;
-      }
+      if (!ok) break;
       const uint8_t* base = raw + (size_t)rs * kRawBytes;
-      if (w.c < kDecGroups) {
+      if (c < kDecGroups) {
         rf[0] = base[kCodeBytes + 32 * q + g];
         rf[1] = base[kCodeBytes + 32 * q + g + 8];
         rf[2] = base[kCodeBytes + 32 * q + 16 + g];
@@ -406,9 +455,50 @@ __device__ void role_decode(const GemmArgs& a, int n_items, Smem* sm, const uint
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->a_full[s]);
     }
-    ++n;
-    walk_next<MODE>(a, n_items, w);
+    nb0 += NC;
+    walk_next_block<MODE>(a, n_items, w);
   }
+  if (!ok) set_err(sm);
+}
+
+// The MMA warp of decoder group grp: the group's chunks in order, into the
+// group's accumulators.
+template <int MODE>
+__device__ void role_mma(const GemmArgs& a, int n_items, Smem* sm, const uint8_t* bring,
+                         uint32_t tmem, int grp) {
+  const int NC = walk_nc<MODE>(a);
+  Walk w;
+  walk_start<MODE>(a, n_items, w);
+  uint32_t nb0 = 0, blk = 0;
+  int last = -1;  // the last chunk whose MMAs this warp issued
+  bool ok = true;
+  while (!w.done && ok) {
+    const uint32_t idesc = umma::idesc_f16_f32(kM, mma_n(block_rows<MODE>(a.items[w.item], w.tb)));
+    for (int c = (grp - (int)(nb0 % kDecGroups) + kDecGroups) % kDecGroups; c < NC; c += kDecGroups) {
+      const uint32_t n = nb0 + c;
+      const uint32_t s = n % kA, sbi = n % kSB, ab = blk & 1;
+      const uint32_t fresh = c < kDecGroups ? 1u : 0u;  // the group's first chunk of the block
+      ok = mbar_wait(&sm->a_full[s], (n / kA) & 1) && mbar_wait(&sm->b_full[sbi], (n / kSB) & 1);
+      if (ok && fresh && blk >= 2) ok = wait_count(&sm->epi_done, kEpiWarps * (blk - 1));
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      mma_chunk(uni(tmem + kAccCol + (uint32_t)kNMax * (2 * grp + ab)), uni(tmem + kACol + 32u * s),
+                uni64(umma::smem_desc_sw128(smem_u32(bring + (size_t)sbi * kBBytes))), 32 >> 4,
+                uni(idesc), uni(fresh), uni(smem_u32(&sm->a_free[s])),
+                uni(smem_u32(&sm->b_free[sbi])), uni(smem_u32(&sm->acc_full[ab])));
+      last = (int)n;
+    }
+    nb0 += NC;
+    ++blk;
+    walk_next_block<MODE>(a, n_items, w);
+  }
+  if (!ok) set_err(sm);
+  // the MMAs must land before the tensor memory is released (a commit tracks
+  // all of the issuing thread's earlier MMAs)
+  if (last >= 0) (void)mbar_wait(&sm->a_free[last % kA], ((uint32_t)last / kA) & 1);
 }
 
 // The B warp: one tensor copy per chunk, the block's 32 consecutive rows in
@@ -427,7 +517,8 @@ __device__ void role_b(const GemmArgs& a, int n_items, Smem* sm, uint8_t* bring,
     for (int c = 0; c < NC; ++c) {
       const uint32_t s = n % kSB;
       if (n >= (uint32_t)kSB) {
-        const bool got = __all_sync(0xffffffffu, mbar_wait(&sm->done[s], ((n / kSB) - 1) & 1));
+        const bool got =
+            __all_sync(0xffffffffu, mbar_wait_sleep(&sm->b_free[s], ((n / kSB) - 1) & 1, 128));
         if (!got || has_err(sm)) {
           set_err(sm);
           ok = false;
@@ -442,8 +533,8 @@ __device__ void role_b(const GemmArgs& a, int n_items, Smem* sm, uint8_t* bring,
           "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%4], %5;\n\t"
           "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
           " [%0], [%1, {%2, %3}], [%4];\n\t"
-          "}" ::"r"(smem_u32(bring + (size_t)s * kBBytes)),
-          "l"(&a.bmap), "r"(64 * c), "r"(row0), "r"(smem_u32(&sm->b_full[s])),
+          "}" ::"r"(uni(smem_u32(bring + (size_t)s * kBBytes))),
+          "l"(&a.bmap), "r"(uni(64 * c)), "r"(uni(row0)), "r"(uni(smem_u32(&sm->b_full[s]))),
           "r"((uint32_t)kBBytes)
           : "memory");
       ++n;
@@ -457,44 +548,15 @@ __device__ void role_b(const GemmArgs& a, int n_items, Smem* sm, uint8_t* bring,
   }
 }
 
-template <int MODE>
-__device__ void role_mma(const GemmArgs& a, int n_items, Smem* sm, const uint8_t* bring,
-                         uint32_t tmem, int lane) {
-  // the whole warp walks and waits; lane 0 issues the MMAs and commits
-  const int NC = walk_nc<MODE>(a);
-  Walk w;
-  walk_start<MODE>(a, n_items, w);
-  uint32_t n = 0, blk = 0;
-  bool ok = true;
-  while (!w.done && ok) {
-    const Item it = a.items[w.item];
-    const int N = mma_n(block_rows<MODE>(it, w.tb));
-    const uint32_t idesc = umma::idesc_f16_f32(kM, N);
-    const uint32_t ab = blk & 1;
-    const uint32_t d = tmem + kAccCol + (uint32_t)kNMax * ab;
-    if (blk >= 2)
-      ok = __all_sync(0xffffffffu, mbar_wait(&sm->acc_empty[ab], ((blk / 2) - 1) & 1));
-    for (int c = 0; c < NC && ok; ++c) {
-      const uint32_t s = n % kA, sbi = n % kSB;
-      bool got = mbar_wait(&sm->a_full[s], (n / kA) & 1) && mbar_wait(&sm->b_full[sbi], (n / kSB) & 1);
-      if (!__all_sync(0xffffffffu, got) || has_err(sm)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t sb = smem_u32(bring + (size_t)sbi * kBBytes);
-      mma_chunk(d, tmem + kACol + 32u * s, umma::smem_desc_sw128(sb), (uint64_t)(32 >> 4), idesc,
-                c == 0 ? 1u : 0u, smem_u32(&sm->done[sbi]),
-                c == NC - 1 ? smem_u32(&sm->acc_full[ab]) : 0u);
-      ++n;
-    }
-    if (!ok) break;
-    ++blk;
-    walk_next_block<MODE>(a, n_items, w);
-  }
-  if (!ok) set_err(sm);
-  // the last commit covers every MMA issued before it
-  if (lane == 0 && n > 0) (void)mbar_wait(&sm->done[(n - 1) % kSB], ((n - 1) / kSB) & 1);
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t ta, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(ta));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 template <int MODE>
@@ -502,6 +564,7 @@ __device__ void role_epilogue(const GemmArgs& a, int n_items, Smem* sm, uint32_t
                               int lane) {
   const int m = 32 * warp + lane;  // accumulator row = tensor memory lane
   const size_t eref_row = (size_t)2 * a.I + a.H;
+  const int NC = walk_nc<MODE>(a);
   Walk w;
   walk_start<MODE>(a, n_items, w);
   uint32_t blk = 0;
@@ -522,23 +585,28 @@ __device__ void role_epilogue(const GemmArgs& a, int n_items, Smem* sm, uint32_t
                                   (size_t)kM * w.mt + m];
     const float rowfac = __uint_as_float(e_ref ? (e_ref << 23) : 0x00400000u);  // 2^(r - 127)
     const uint32_t ab = blk & 1;
-    const bool got = __all_sync(0xffffffffu, mbar_wait(&sm->acc_full[ab], (blk / 2) & 1));
+    const bool got = __all_sync(0xffffffffu, mbar_wait_sleep(&sm->acc_full[ab], (blk / 2) & 1, 256));
     if (!got || has_err(sm)) {
       set_err(sm);
       break;
     }
     tc_fence_after();
+    // the groups that hold chunks of this block (all four unless K < 256):
+    // chunk c of block blk went to group (blk * NC + c) % 4
+    uint32_t gmask = 0;
+    for (int c = 0; c < NC && c < kDecGroups; ++c) gmask |= 1u << ((blk * NC + c) % kDecGroups);
     const uint32_t d = tmem + ((uint32_t)(32 * warp) << 16) + kAccCol + (uint32_t)kNMax * ab;
     for (int c0 = 0; c0 < N; c0 += 16) {
       uint32_t r[16];
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-          "%13,%14,%15}, [%16];"
-          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-            "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-            "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-          : "r"(d + (uint32_t)c0));
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      float acc[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+      for (int gg = 0; gg < kDecGroups; ++gg) {
+        if (!(gmask >> gg & 1)) continue;
+        tmem_ld_32x32b_x16(d + (uint32_t)(2 * kNMax * gg + c0), r);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(r[i]);
+      }
       if (MODE == 0) {
         // rows 16t + rho: gate row rho < 8 pairs with up row rho + 8 (lane ^ 8)
         const int rho = m & 15;
@@ -548,7 +616,7 @@ __device__ void role_epilogue(const GemmArgs& a, int n_items, Smem* sm, uint32_t
           const int col = c0 + i;
           const int asg = __shfl_sync(0xffffffffu, asg0, col);
           const float xs = __shfl_sync(0xffffffffu, sc0, col);
-          const float v = __uint_as_float(r[i]) * rowfac * xs;
+          const float v = acc[i] * rowfac * xs;
           const float up = __shfl_xor_sync(0xffffffffu, v, 8);
           if (rho < 8 && col < rows) a.out[(size_t)asg * a.I + irow] = silu_f(v) * up;
         }
@@ -560,13 +628,15 @@ __device__ void role_epilogue(const GemmArgs& a, int n_items, Smem* sm, uint32_t
           const float hs = __shfl_sync(0xffffffffu, sc0, tok);
           if (tok < nt)
             a.out[(size_t)asg * a.H + (size_t)kM * w.mt + m] =
-                (__uint_as_float(r[i]) + __uint_as_float(r[i + 1])) * rowfac * hs;
+                (acc[i] + acc[i + 1]) * rowfac * hs;
         }
       }
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm->acc_empty[ab]);
+    if (lane == 0)  // this warp's reads of the block are done
+      asm volatile("red.release.cta.shared::cta.add.u32 [%0], 1;" ::"r"(smem_u32(&sm->epi_done))
+                   : "memory");
     ++blk;
     walk_next_block<MODE>(a, n_items, w);
   }
@@ -592,15 +662,17 @@ __global__ void __launch_bounds__(kThr, 1) gemm_kernel(const __grid_constant__ G
       mbar_init(&sm->raw_full[i], 1);
       mbar_init(&sm->raw_empty[i], kGroupWarps);
     }
-    for (int i = 0; i < kA; ++i) mbar_init(&sm->a_full[i], kGroupWarps);
+    for (int i = 0; i < kA; ++i) {
+      mbar_init(&sm->a_full[i], kGroupWarps);
+      mbar_init(&sm->a_free[i], 1);
+    }
     for (int i = 0; i < kSB; ++i) {
       mbar_init(&sm->b_full[i], 1);
-      mbar_init(&sm->done[i], 1);
+      mbar_init(&sm->b_free[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm->acc_full[i], 1);
-      mbar_init(&sm->acc_empty[i], kEpiWarps);
-    }
+    for (int i = 0; i < 2; ++i)
+      mbar_init(&sm->acc_full[i], (uint32_t)walk_nc<MODE>(a));  // one commit per chunk
+    sm->epi_done = 0;
     sm->err = 0;
     fence_barrier_init();
   }
@@ -619,8 +691,8 @@ __global__ void __launch_bounds__(kThr, 1) gemm_kernel(const __grid_constant__ G
     role_raw<MODE>(a, n_items, sm, raw, lane);
   } else if (warp == kBWarp) {
     role_b<MODE>(a, n_items, sm, bring, lane);
-  } else if (warp == kMmaWarp) {
-    role_mma<MODE>(a, n_items, sm, bring, tmem, lane);
+  } else {
+    role_mma<MODE>(a, n_items, sm, bring, tmem, warp - kMmaWarp0);
   }
   tc_fence_before();
   __syncthreads();
