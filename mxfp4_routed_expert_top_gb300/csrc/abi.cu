@@ -31,6 +31,8 @@ struct LayerBufs {
   float* sh_dn_rs = nullptr;    // [n_s][H]
   uint8_t* eref = nullptr;      // [E][2I + H] row reference exponents (tcgen05 GEMMs)
   ChunkMap map_gu{}, map_dn{};  // tensor maps of the arena's tiles (tcgen05 GEMMs)
+  SharedMaps sh_maps{};         // shared experts as dense tcgen05 GEMMs (batches)
+  bool sh_maps_ok = false;
   bool router_loaded = false;
   std::vector<uint8_t> shared_loaded;
   std::vector<uint8_t> expert_loaded;
@@ -91,6 +93,7 @@ struct df_moe {
   bool gemm = false;
   uint16_t* g_xg = nullptr;      // [Tmax*k][H] f16: gate/up B rows in expert order
   uint16_t* g_hh = nullptr;      // [Tmax*k][2][I] f16: down B rows in expert order
+  uint16_t* s_hh = nullptr;      // [Tmax][3][R] bf16: shared h rows (3 parts), batches
   float* g_bsc = nullptr;        // [Tmax*k] their power-of-two row scales
   ChunkMap bmap_gu{}, bmap_dn{};
   // the shared experts' chain runs on a second stream, on sh_ctas SMs
@@ -219,9 +222,20 @@ int route(df_moe* h, int l, const uint16_t* x, int T, int32_t* ids, float* w,
                                       h->router_part, h->rsplit, s, &fz));
     return DF_MOE_OK;
   }
-  RUN(h, K_ROUTER, s, launch_router(L.router, c.n_experts, c.hidden, x, T,
-                                    h->router_part, h->rsplit, s));
-  RUN(h, K_TOPK, s, launch_topk(h->router_part, h->rsplit.nsplit, T,
+  int nsplit = h->rsplit.nsplit;
+  if (T > kLayerMaxT) {
+    // a batch: the logits as one tiled GEMM (weights read once for all tokens)
+    int used = -1;
+    RUN(h, K_ROUTER, s, (used = launch_router_gemm(L.router, c.n_experts, c.hidden, x, T,
+                                                   h->router_part, nsplit, h->sms, s)) < 0
+                            ? cudaErrorLaunchFailure
+                            : cudaSuccess);
+    nsplit = used;
+  } else {
+    RUN(h, K_ROUTER, s, launch_router(L.router, c.n_experts, c.hidden, x, T,
+                                      h->router_part, h->rsplit, s));
+  }
+  RUN(h, K_TOPK, s, launch_topk(h->router_part, nsplit, T,
                                 c.n_experts, c.top_k, logits_out, ids, w,
                                 direct ? h->items : nullptr, h->n_items,
                                 h->sorted, s));
@@ -281,6 +295,13 @@ int shared_part(df_moe* h, int l, const uint16_t* x, int T, float* ysh,
                 cudaStream_t s, int max_ctas = 0) {
   const df_moe_config& c = h->cfg;
   const LayerBufs& L = h->layers[l];
+  if (T > kLayerMaxT && L.sh_maps_ok && ((uintptr_t)x & 15) == 0) {
+    // a batch: two dense GEMMs on the tensor cores
+    RUN(h, K_SHARED_GU, s, launch_shared_gemm_gateup(L.sh_maps, x, T, c.hidden, h->R, h->s_hh,
+                                                     h->err, s));
+    RUN(h, K_SHARED_DN, s, launch_shared_gemm_down(L.sh_maps, T, c.hidden, h->R, ysh, h->err, s));
+    return DF_MOE_OK;
+  }
   RUN(h, K_SHARED_GU, s, launch_shared_gateup(L.sh_gate, L.sh_up, h->R,
                                               c.hidden, x, T, h->hsh, h->err, s, max_ctas));
   RUN(h, K_SHARED_DN, s, launch_shared_down(L.sh_down, c.hidden, h->R, h->hsh,
@@ -507,6 +528,14 @@ int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
     if (!rc) rc = dalloc(h, &h->g_xg, Tm * k * H);
     if (!rc) rc = dalloc(h, &h->g_hh, Tm * k * 2 * I);
     if (!rc) rc = dalloc(h, &h->g_bsc, Tm * k);
+    if (!rc && R && dense_supported(c.hidden, (int)R)) {
+      rc = dalloc(h, &h->s_hh, Tm * 3 * R);
+      for (int l = 0; l < c.n_layers && !rc; ++l) {
+        LayerBufs& L = h->layers[l];
+        L.sh_maps_ok = make_shared_maps(L.sh_gate, L.sh_up, L.sh_down, c.hidden, (int)R, h->s_hh,
+                                        (int)(3 * Tm), &L.sh_maps);
+      }
+    }
     if (!rc && !make_b_maps(h->g_xg, h->g_hh, (int)(Tm * k), c.hidden, c.inter, &h->bmap_gu,
                             &h->bmap_dn))
       rc = fail(h, DF_MOE_ECUDA, "tensor map encoding failed");

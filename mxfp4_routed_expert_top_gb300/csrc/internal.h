@@ -106,6 +106,11 @@ struct RouterFuse {
 cudaError_t launch_router(const float* Wr, int E, int H, const uint16_t* x,
                           int T, float* part, RouterSplit sp, cudaStream_t s,
                           const RouterFuse* fuse = nullptr);
+// Router logits of a batch (T > 1) as a tiled fp32 GEMM into at most
+// max_splits column splits of part; returns the split count used (-1 on a
+// launch error).
+int launch_router_gemm(const float* Wr, int E, int H, const uint16_t* x, int T, float* part,
+                       int max_splits, int sms, cudaStream_t s);
 cudaError_t launch_topk(const float* part, int nsplit, int T, int E, int k,
                         float* logits_out, int32_t* ids, float* w,
                         Item* items, int32_t* n_items, int32_t* sorted,
@@ -179,6 +184,23 @@ cudaError_t launch_gemm_down(const ChunkMap& map, const ChunkMap& bmap, const ui
                              const float* bsc, const Item* items, const int32_t* n_items,
                              int max_items, const int32_t* sorted, float* part, uint32_t* err,
                              cudaStream_t s);
+
+// ---- shared experts of large batches on tcgen05 (k_dense.cu) ----------------
+// Tensor maps of one layer's shared-expert weights (gate, up [R][H]; down
+// [H][R]; bf16) and of the h rows handed from GEMM 1 to GEMM 2 ([3 max_T][R]).
+struct SharedMaps {
+  ChunkMap gate, up, down, hh;
+};
+bool dense_supported(int H, int R);
+bool make_shared_maps(const uint16_t* gate, const uint16_t* up, const uint16_t* down, int H,
+                      int R, const uint16_t* hh, int max_rows, SharedMaps* out);
+// h = silu(gate x) * (up x) as three bf16 parts, rows hh [T][3][R] (x: bf16
+// [T][H], 16-byte aligned).
+cudaError_t launch_shared_gemm_gateup(const SharedMaps& m, const uint16_t* x, int T, int H,
+                                      int R, uint16_t* hh, uint32_t* err, cudaStream_t s);
+// y [T][H] = down (high + middle + low).
+cudaError_t launch_shared_gemm_down(const SharedMaps& m, int T, int H, int R, float* y,
+                                    uint32_t* err, cudaStream_t s);
 
 // ---- the decode-batch layer kernel (k_layer.cu) -----------------------------
 // One persistent cooperative launch computes a whole MoE layer for T <= 8

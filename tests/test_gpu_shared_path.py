@@ -6,11 +6,18 @@ expert contributes exactly 0 whatever the routing, and with top-16 of 16 the
 layer output is the shared experts' sum (plus the residual). In the full
 layer that sum is ~1e-5 of the routed part, so this is where its parity is
 visible. Batch sizes 1, 5 and 8 cover both the one- and two-column-group
-forms of the shared down GEMV.
+forms of the shared down GEMV; 9, 100 and 200 the dense tcgen05 GEMMs that
+take over above the decode range (ragged token tiles of 128, and for the
+down GEMM two columns per token).
 
-Bar: relative L2 <= 1e-5 against the oracle's double sum. The kernel's f16
-form of each bf16 weight row (a power-of-two row scale) is exact, products
-of f16 values are exact in fp32, and only fp32 accumulation rounding remains.
+Bar: relative L2 <= 1e-5 against the oracle's double sum on the decode
+path (T <= 8): the kernel's f16 form of each bf16 weight row (a power-of-two
+row scale) is exact, products of f16 values are exact in fp32, and only fp32
+accumulation rounding remains. Above the decode range the contractions
+(K = 7168, then 3072) run on tcgen05, whose accumulation of the exact bf16
+products follows the tensor core's own summation rather than sequential
+fp32 adds; measured 1.9e-5, bar 5e-5. (The shared part is ~1e-5 of a
+layer's output, so either bar sits far inside the layer tolerance.)
 """
 import numpy as np
 import pytest
@@ -37,7 +44,7 @@ def torch():
 def zero_routed(torch, request):
     import mxfp4_routed_expert_top_gb300 as dfm
     flags = dfm.FUSED_DECODE if request.param == "fused" else 0
-    m = dfm.MoE(WL.H, E, E, WL.I, WL.n_shared, WL.Is, max_tokens=8, flags=flags)
+    m = dfm.MoE(WL.H, E, E, WL.I, WL.n_shared, WL.Is, max_tokens=200, flags=flags)
     router = synth.router(WL.seed, WL.wcfg, 0, E, WL.H)
     shared = [synth.shared(WL.seed, WL.wcfg, 0, s, WL.H, WL.Is) for s in range(WL.n_shared)]
     zeros = torch.zeros(E * m.span_bytes, dtype=torch.uint8, device="cuda")
@@ -48,7 +55,7 @@ def zero_routed(torch, request):
     m.close()
 
 
-@pytest.mark.parametrize("T", [1, 5, 8])
+@pytest.mark.parametrize("T", [1, 5, 8, 9, 100, 200])
 def test_shared_only_layer(zero_routed, torch, T):
     m, router, shared = zero_routed
     x = np.stack([synth.token(WL.seed, 2, 4000 + t, WL.H) for t in range(T)])
@@ -60,9 +67,10 @@ def test_shared_only_layer(zero_routed, torch, T):
     m.forward(to_dev_bf16(x), T, out, ids, w, residual=to_dev_bf16(res), out_f32=out32)
     m.sync()
     got = out32.cpu().double().numpy() - bits_to_f64(res)
+    bar = 1e-5 if T <= 8 else 5e-5
     for t in range(T):
         ref = sum(orc.shared_ffn(*s, bits_to_f64(x[t])) for s in shared)
-        assert rel_l2(got[t], ref) <= 1e-5, "token %d" % t
+        assert rel_l2(got[t], ref) <= bar, "token %d" % t
     # routing over all 16 experts: the set is all of them, weights a softmax
     rid, rw = orc.topk_softmax(orc.router_logits(router, x), E)
     check_ids_weights(ids.cpu().numpy(), w.cpu().double().numpy(), rid, rw)
