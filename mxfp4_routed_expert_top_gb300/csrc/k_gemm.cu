@@ -73,19 +73,22 @@ constexpr int kRawWarp = 20, kBWarp = 21, kMmaWarp0 = 22;  // MMA warps 22-25
 constexpr int kThr = 26 * 32;
 constexpr int kM = 128;                        // weight rows per unit
 constexpr int kTilesPerM = kM / 16;
-constexpr int kCodeBytes = kTilesPerM * kGroupBytes;  // 4352: one 64-column chunk
+constexpr int kCG = 2;                         // 64-column groups per chunk
+constexpr int kCodeBytes = kTilesPerM * kCG * kGroupBytes;  // 8704: one 128-column chunk
 constexpr int kRefBytes = kM;                  // reference exponents of the rows
 constexpr int kRawBytes = kCodeBytes + kRefBytes;
-constexpr int kRaw = 28;                       // raw chunks in flight
-constexpr int kA = 8;                          // A stages (tensor memory)
-constexpr int kSB = 16;                        // B stages (shared memory)
+constexpr int kRaw = 16;                       // raw chunks in flight
+constexpr int kA = 4;                          // A stages (tensor memory)
+constexpr int kSB = 8;                         // B stages (shared memory)
 constexpr int kNMax = 32;                      // MMA N at most (B rows of a block)
-constexpr int kBBytes = kNMax * 64 * 2;        // B stage: 32 rows x 64 f16 (the TMA box)
+constexpr int kBHalf = kNMax * 64 * 2;         // one TMA box: 32 rows x 64 f16
+constexpr int kBBytes = kCG * kBHalf;          // B stage: 32 rows x 128 f16
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;                // per group two accumulators of kNMax columns
-constexpr uint32_t kACol = 2 * kDecGroups * kNMax;  // kA A stages of 32 columns
+constexpr uint32_t kACol = 2 * kDecGroups * kNMax;  // kA A stages of 32 kCG columns
+constexpr uint32_t kAStageCols = 32 * kCG;
 
-static_assert(kACol + 32 * kA <= kTmemCols, "tensor memory");
+static_assert(kACol + kAStageCols * kA <= kTmemCols, "tensor memory");
 static_assert(kRawBytes % 16 == 0, "bulk copies need 16-byte aligned stages");
 
 struct GemmArgs {
@@ -135,7 +138,9 @@ struct Walk {
 };
 
 template <int MODE>
-__device__ __forceinline__ int walk_nc(const GemmArgs& a) { return (MODE == 0 ? a.H : a.I) / 64; }
+__device__ __forceinline__ int walk_nc(const GemmArgs& a) {
+  return (MODE == 0 ? a.H : a.I) / (64 * kCG);
+}
 template <int MODE>
 __device__ __forceinline__ int walk_mt(const GemmArgs& a) { return MODE == 0 ? a.I / 64 : a.H / kM; }
 template <int MODE>
@@ -245,15 +250,15 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
 // follow them, issued by one elected lane of a converged warp in one
 // straight-line block: A at tensor memory column a (+8 per step), B from the
 // descriptor bd (+bstep per step), accumulating into d unless `fresh`;
-// commits to the A stage, the B stage and the block barriers. A commit
-// tracks the issuing thread's own MMAs, so every chunk commits to the block
-// barrier (one arrival per chunk).
+// commits to the A stage, the B stage and the block barriers (none when
+// a_free is 0). A commit tracks the issuing thread's own MMAs, so every
+// chunk commits to the block barrier (one arrival per chunk).
 __device__ __forceinline__ void mma_chunk(uint32_t d, uint32_t a, uint64_t bd, uint64_t bstep,
                                           uint32_t idesc, uint32_t fresh, uint32_t a_free,
                                           uint32_t b_free, uint32_t acc) {
   asm volatile(
       "{\n\t"
-      ".reg .pred e, p0, pt;\n\t"
+      ".reg .pred e, p0, pt, pc;\n\t"
       ".reg .b32 r, a1, a2, a3;\n\t"
       ".reg .b64 b1, b2, b3;\n\t"
       "elect.sync r|e, 0xffffffff;\n\t"
@@ -269,9 +274,10 @@ __device__ __forceinline__ void mma_chunk(uint32_t d, uint32_t a, uint64_t bd, u
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, pt;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %4, pt;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %4, pt;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t"
+      "setp.ne.and.u32 pc, %6, 0, e;\n\t"
+      "@pc tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
+      "@pc tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t"
+      "@pc tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t"
       "}" ::"r"(d),
       "r"(a), "l"(bd), "l"(bstep), "r"(idesc), "r"(fresh), "r"(a_free), "r"(b_free), "r"(acc)
       : "memory");
@@ -342,7 +348,7 @@ __device__ void role_raw(const GemmArgs& a, int n_items, Smem* sm, uint8_t* raw,
           "@pr cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
           " [%12], [%9], %13, [%6], %7;\n\t"
           "}" ::"r"(uni(dst)),
-          "l"(&a.map), "r"(0), "r"(uni(w.c)), "r"(uni(kTilesPerM * w.mt)), "r"(uni(e)),
+          "l"(&a.map), "r"(0), "r"(uni(kCG * w.c)), "r"(uni(kTilesPerM * w.mt)), "r"(uni(e)),
           "r"(uni(bar)), "l"(pol), "r"(uni(ref)), "l"(uni64((uint64_t)rsrc)),
           "r"((uint32_t)(kCodeBytes + kRefBytes)), "r"((uint32_t)kCodeBytes),
           "r"(uni(dst + (uint32_t)kCodeBytes)), "r"((uint32_t)kRefBytes)
@@ -438,18 +444,26 @@ __device__ void role_decode(const GemmArgs& a, int n_items, Smem* sm, const uint
         rf[2] = base[kCodeBytes + 32 * q + 16 + g];
         rf[3] = base[kCodeBytes + 32 * q + 16 + g + 8];
       }
-      const uint32_t t0 = smem_u32(base) + (uint32_t)(2 * q * kGroupBytes);
-      uint32_t cw0[4], cw1[4], sc0, sc1;
-      load_tile(t0, lane, cw0, sc0);
-      load_tile(t0 + kGroupBytes, lane, cw1, sc1);
-      uint32_t v0[16], v1[16];
-      decode_tile(cw0, sc0, rf[0], rf[1], v0);
-      decode_tile(cw1, sc1, rf[2], rf[3], v1);
+      // stage layout [tile][group][544 B]; tile 2q -> lanes 32q.., 2q+1 -> 32q+16..
+      const uint32_t t0 = smem_u32(base) + (uint32_t)(2 * q * kCG * kGroupBytes);
+      const uint32_t t1 = t0 + (uint32_t)(kCG * kGroupBytes);
+      uint32_t cw[kCG][2][4], sc[kCG][2];
+#pragma unroll
+      for (int j = 0; j < kCG; ++j) {
+        load_tile(t0 + (uint32_t)(j * kGroupBytes), lane, cw[j][0], sc[j][0]);
+        load_tile(t1 + (uint32_t)(j * kGroupBytes), lane, cw[j][1], sc[j][1]);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->raw_empty[rs]);
-      const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kACol + 32u * s;
-      tmem_st_16x128b_x8(ta, v0);
-      tmem_st_16x128b_x8(ta + (16u << 16), v1);
+      const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + kACol + kAStageCols * s;
+#pragma unroll
+      for (int j = 0; j < kCG; ++j) {
+        uint32_t v0[16], v1[16];
+        decode_tile(cw[j][0], sc[j][0], rf[0], rf[1], v0);
+        decode_tile(cw[j][1], sc[j][1], rf[2], rf[3], v1);
+        tmem_st_16x128b_x8(ta + 32u * j, v0);
+        tmem_st_16x128b_x8(ta + (16u << 16) + 32u * j, v1);
+      }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
@@ -485,10 +499,14 @@ __device__ void role_mma(const GemmArgs& a, int n_items, Smem* sm, const uint8_t
         break;
       }
       tc_fence_after();
-      mma_chunk(uni(tmem + kAccCol + (uint32_t)kNMax * (2 * grp + ab)), uni(tmem + kACol + 32u * s),
-                uni64(umma::smem_desc_sw128(smem_u32(bring + (size_t)sbi * kBBytes))), 32 >> 4,
-                uni(idesc), uni(fresh), uni(smem_u32(&sm->a_free[s])),
-                uni(smem_u32(&sm->b_free[sbi])), uni(smem_u32(&sm->acc_full[ab])));
+      const uint32_t d = uni(tmem + kAccCol + (uint32_t)kNMax * (2 * grp + ab));
+      const uint32_t at = uni(tmem + kACol + kAStageCols * s);
+      const uint64_t bd = uni64(umma::smem_desc_sw128(smem_u32(bring + (size_t)sbi * kBBytes)));
+      // group 0: fresh on the group's first chunk; group 1 always accumulates
+      mma_chunk(d, at, bd, 32 >> 4, uni(idesc), uni(fresh), 0u, 0u, 0u);
+      mma_chunk(d, at + 32u, bd + (uint64_t)(kBHalf >> 4), 32 >> 4, uni(idesc), 0u,
+                uni(smem_u32(&sm->a_free[s])), uni(smem_u32(&sm->b_free[sbi])),
+                uni(smem_u32(&sm->acc_full[ab])));
       last = (int)n;
     }
     nb0 += NC;
@@ -533,9 +551,12 @@ __device__ void role_b(const GemmArgs& a, int n_items, Smem* sm, uint8_t* bring,
           "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%4], %5;\n\t"
           "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
           " [%0], [%1, {%2, %3}], [%4];\n\t"
+          "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+          " [%6], [%1, {%7, %3}], [%4];\n\t"
           "}" ::"r"(uni(smem_u32(bring + (size_t)s * kBBytes))),
-          "l"(&a.bmap), "r"(uni(64 * c)), "r"(uni(row0)), "r"(uni(smem_u32(&sm->b_full[s]))),
-          "r"((uint32_t)kBBytes)
+          "l"(&a.bmap), "r"(uni(128 * c)), "r"(uni(row0)), "r"(uni(smem_u32(&sm->b_full[s]))),
+          "r"((uint32_t)kBBytes), "r"(uni(smem_u32(bring + (size_t)s * kBBytes + kBHalf))),
+          "r"(uni(128 * c + 64))
           : "memory");
       ++n;
     }
@@ -834,7 +855,9 @@ cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-bool gemm_supported(int H, int I) { return H % kM == 0 && I % 64 == 0 && H >= kM; }
+bool gemm_supported(int H, int I) {
+  return H % kM == 0 && H % (64 * kCG) == 0 && I % (64 * kCG) == 0 && I % 64 == 0 && H >= kM;
+}
 
 // The tiles of one matrix kind of every expert as a 4-d tensor of u32:
 // (136 words of a 544-byte group, K/64 groups, tiles of the expert, expert),
@@ -866,7 +889,7 @@ bool make_chunk_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int 
     const cuuint64_t dims[4] = {kGroupBytes / 4, (cuuint64_t)(K / 64), (cuuint64_t)tiles,
                                 (cuuint64_t)E};
     const cuuint64_t strides[3] = {kGroupBytes, mx_tile_bytes(K), span_bytes};
-    const cuuint32_t box[4] = {kGroupBytes / 4, 1, kTilesPerM, 1};
+    const cuuint32_t box[4] = {kGroupBytes / 4, kCG, kTilesPerM, 1};
     const cuuint32_t es[4] = {1, 1, 1, 1};
     void* base = const_cast<uint8_t*>(arena + (mode == 0 ? L.gu : L.dn));
     CUtensorMap* m = reinterpret_cast<CUtensorMap*>(mode == 0 ? gu : dn);

@@ -2,7 +2,8 @@
 grouped tcgen05 GEMMs (default) and the register-fragment kernels they
 replace (PREFILL_MMA_SYNC), through the C ABI against the oracle.
 
-Tiny workload shape (H=256, I=64, 8 experts, top-2) so that the oracle can
+Tiny workload shape with a wider intermediate (H=256, I=128, 8 experts,
+top-2; the GEMMs take K in chunks of 128 columns) so that the oracle can
 check every assignment: with 512 tokens each expert holds ~128 of them,
 several token blocks of both GEMMs (32 tokens of gate/up, 16 tokens of
 down), and a ragged last block. A hot expert that every token picks covers
@@ -14,6 +15,8 @@ the weights as E2M1 values times 2^(e - r), r a per-row reference exponent
 power of two per token), and the down input h as a high and a low f16 part
 (|h - hi - lo| <= 2^-22 |h|); accumulation is fp32.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -24,7 +27,7 @@ from moe_setup import (Setup, bits_to_f64, check_ids_weights, check_out,
 
 pytestmark = pytest.mark.gpu
 
-WL = synth.WORKLOADS[0]
+WL = dataclasses.replace(synth.WORKLOADS[0], I=128, name="tiny-h256-i128-e8-top2")
 
 
 @pytest.fixture(scope="module")
