@@ -67,6 +67,27 @@ enum KernelKind {
   K_GEMM_DN, K_NKINDS
 };
 
+// Launches `kernel` as a programmatic dependent of the previous kernel in
+// the stream: its grid may be set up, and its CTAs may start, while the
+// previous kernel's last CTAs finish; the kernel itself waits for the
+// previous grid's completion (griddepcontrol.wait) before reading its
+// results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after_previous(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                  cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, (KArgs)args...);
+}
+
 // Error word bits written by device-side checks.
 enum : uint32_t { DEV_ERR_RANGE = 1u, DEV_ERR_TIMEOUT = 2u };
 

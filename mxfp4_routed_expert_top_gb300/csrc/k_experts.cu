@@ -120,6 +120,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) mxv_kernel(const MxvArgs a)
   __syncthreads();
 
   pdl_wait();  // items, x and h come from the preceding kernels
+  // every CTA is resident (one wave): the next kernel may be set up now and
+  // start on each SM as this one's CTA leaves
+  pdl_launch_dependents();
   const SpanLayout L = span_layout(a.H, a.I);
   const int tpi = MODE == 0 ? (2 * a.I) / 16 : a.H / 16;  // tiles per item
   const int ntiles = *a.n_items * tpi;
@@ -398,8 +401,7 @@ cudaError_t launch_mxv(const MxvArgs& a, int max_items, cudaStream_t s, int max_
   if (grid > num_sms()) grid = num_sms();
   if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
   if (grid < 1) grid = 1;
-  mxv_kernel<MODE><<<grid, threads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_after_previous(mxv_kernel<MODE>, dim3(grid), dim3(threads), smem, s, a);
 }
 
 }  // namespace
@@ -426,9 +428,8 @@ cudaError_t launch_combine(const float* part, const float* w, int T, int k,
                            int H, const float* ysh, const uint16_t* residual,
                            float* out_f32, uint16_t* out_bf16, cudaStream_t s) {
   dim3 grid((H + 255) / 256, T);
-  combine_kernel<<<grid, 256, 0, s>>>(part, w, k, H, ysh, residual, out_f32,
-                                      out_bf16);
-  return cudaGetLastError();
+  return launch_after_previous(combine_kernel, grid, dim3(256), 0, s, part, w, k, H, ysh,
+                               residual, out_f32, out_bf16);
 }
 
 }  // namespace dfm

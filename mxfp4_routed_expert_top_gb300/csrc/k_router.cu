@@ -9,6 +9,7 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "pipeline.cuh"
 
 namespace dfm {
 namespace {
@@ -130,6 +131,8 @@ router_kernel(const float* __restrict__ Wr, int E, int H,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * kRouterRowsPerBlock + warp;
   const int split = blockIdx.y;
+  // the expert kernels may be set up once every router CTA has started
+  pdl_launch_dependents();
   const int k0 = split * split_len;
   const int len = min(split_len, H - k0);
   if (e < E) {
