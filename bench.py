@@ -74,11 +74,16 @@ def layer_bytes(wl, n_union, T):
     return router + shared + n_union * span + T * wl.H * 2 * 2
 
 
-def gateup_bytes(wl, n_union, T):
+def gateup_bytes(wl, n_union, T, with_shared=False):
     """Algorithmic bytes of the gate/up kernel: the gate and up halves of every
-    distinct selected expert (codes + scales), x in, h out (fp32)."""
+    distinct selected expert (codes + scales), x in, h out (fp32); with_shared:
+    also the shared experts' gate and up rows (bf16) and their h (the decode
+    phase kernel runs both)."""
     per_expert = 2 * wl.I * wl.H * 17 // 32
-    return n_union * per_expert + T * wl.H * 2 + T * wl.k * wl.I * 4
+    b = n_union * per_expert + T * wl.H * 2 + T * wl.k * wl.I * 4
+    if with_shared:
+        b += wl.n_shared * 2 * wl.Is * wl.H * 2 + T * wl.n_shared * wl.Is * 4
+    return b
 
 
 def gateup_flops(wl, T):
@@ -375,7 +380,9 @@ def run_ours(args):
     elif kt.get("gemm_gateup", (0, 0.0))[0]:
         dom, dom_bytes = "gemm_gateup", gateup_bytes(wl, u_mean, T)
     else:
-        dom, dom_bytes = "expert_gateup", gateup_bytes(wl, u_mean, T)
+        # decode batches: the gate/up phase kernel streams the routed and the
+        # shared experts' gate/up rows
+        dom, dom_bytes = "expert_gateup", gateup_bytes(wl, u_mean, T, with_shared=T <= 8)
     dom_n, dom_ms = kt[dom]
     dom_avg_ms = dom_ms / max(dom_n, 1)
     dom_gbs = dom_bytes / (dom_avg_ms / 1e3) / 1e9

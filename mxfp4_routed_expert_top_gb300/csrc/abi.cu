@@ -96,9 +96,7 @@ struct df_moe {
   uint16_t* s_hh = nullptr;      // [Tmax][3][R] bf16: shared h rows (3 parts), batches
   float* g_bsc = nullptr;        // [Tmax*k] their power-of-two row scales
   ChunkMap bmap_gu{}, bmap_dn{};
-  // the shared experts' chain runs on a second stream, on sh_ctas SMs
-  cudaStream_t s2 = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  bool phase = false;  // decode batches run the two phase kernels
   int sms = 0;
   // host-API device buffers
   uint16_t* hx = nullptr;
@@ -209,11 +207,18 @@ int check_layer_ready(df_moe* h, int l) {
 }
 
 // Router + top-k (+ grouping) of one layer. ids/w: [T][k] device.
+// planes_only (one token): only the partial-logit planes; the gate/up phase
+// kernel selects.
 int route(df_moe* h, int l, const uint16_t* x, int T, int32_t* ids, float* w,
-          cudaStream_t s, float* logits_out, int tg) {
+          cudaStream_t s, float* logits_out, int tg, bool planes_only = false) {
   const df_moe_config& c = h->cfg;
   const LayerBufs& L = h->layers[l];
   const bool direct = (T == 1 && tg == 1);
+  if (direct && planes_only && !logits_out) {
+    RUN(h, K_ROUTER, s, launch_router(L.router, c.n_experts, c.hidden, x, T,
+                                      h->router_part, h->rsplit, s));
+    return DF_MOE_OK;
+  }
   if (direct && !logits_out) {
     // one token: the router's last block selects the experts and writes the
     // work items (no separate top-k launch)
@@ -273,7 +278,7 @@ int expert_gateup(df_moe* h, int l, const uint16_t* x, int T, int max_items, int
 }
 
 int expert_down(df_moe* h, int l, const float* hbuf, int T, int max_items, int tg,
-                cudaStream_t s, int max_ctas = 0) {
+                cudaStream_t s, int max_ctas = 0, bool after_gateup = false) {
   const df_moe_config& c = h->cfg;
   const uint8_t* arena = h->layers[l].arena;
   if (use_gemm(h, T, tg)) {
@@ -286,7 +291,7 @@ int expert_down(df_moe* h, int l, const float* hbuf, int T, int max_items, int t
   } else {
     RUN(h, K_DOWN, s, launch_down(arena, h->span_bytes, c.hidden, c.inter, h->items,
                                   h->n_items, max_items, h->sorted, hbuf, h->part, tg, h->err,
-                                  s, max_ctas));
+                                  s, max_ctas, after_gateup));
   }
   return DF_MOE_OK;
 }
@@ -373,41 +378,57 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
     return layer_kernel_forward(h, l, x, T, residual, out_bf16, out_f32, ids, w, s);
   const int tg = T == 1 ? 1 : kOneItemPerExpert;
   const int max_items = (T == 1 && tg == 1) ? c.top_k : std::min(T * c.top_k, c.n_experts);
-  // At T = 1 the shared experts, which do not depend on the routing, run on
-  // a second stream and a share of the SMs, beside the router -> gate/up ->
-  // down chain: each chain's ramp and tail, and the router's latency, are
-  // then covered by the other chain's streaming. The share is the shared
-  // bytes' part of the bytes with the routed chain's counted twice (per SM it
-  // streams at about half the rate once the router's latency is included;
-  // measured at K3 shape the optimum lies at 22-30 of 152 SMs). For T > 1 the
-  // shared GEMVs (fp32 FMA per token) become compute-bound on few SMs, so the
-  // chains run one after the other.
-  const double sh_bytes = (double)c.n_shared * 3.0 * c.shared_inter * c.hidden * 2.0;
-  const double rt_bytes = (double)c.n_experts * c.hidden * 4.0 + (double)max_items * h->span_bytes;
-  const int sh_ctas = (int)(h->sms * sh_bytes / (sh_bytes + 2.0 * rt_bytes) + 0.5);
-  const bool split = T == 1 && c.n_shared > 0 && h->s2 && sh_ctas >= 8 && sh_ctas <= h->sms / 2;
-  int rc = 0;
-  if (split) CUDA_OR_FAIL(h, cudaEventRecord(h->ev_fork, s));
-  // the router first: its latency is on the critical path, so its CTAs are
-  // dispatched before the shared chain's
-  rc = route(h, l, x, T, ids, w, s, nullptr, tg);
-  if (rc) return rc;
-  if (split) {
-    CUDA_OR_FAIL(h, cudaStreamWaitEvent(h->s2, h->ev_fork, 0));
-    rc = shared_part(h, l, x, T, h->ysh, h->s2, sh_ctas);
-    if (rc) return rc;
-    CUDA_OR_FAIL(h, cudaEventRecord(h->ev_join, h->s2));
+  const int R = c.n_shared > 0 ? h->R : 0;
+  const bool phase = T <= kLayerMaxT && h->phase;
+  int sh_gu = 0, sh_dn = 0;
+  if (phase && R > 0) {
+    // CTAs for the shared experts in each phase: the split that ends both
+    // sides together at the per-SM streaming rates measured on GB300 at K3
+    // shape (GB/s an SM): routed MXFP4 gate/up ~31, down ~24; shared bf16
+    // gate/up ~57 and down ~61 at one token, falling as the fp32 FMAs per
+    // byte grow with T (~11.6 and ~10.7 at T = 8). At T = 1 the routed CTAs
+    // first spend ~7 us selecting the experts.
+    const double n_rt = std::min(T * c.top_k, c.n_experts);
+    const double gu_rt = n_rt * 2.0 * c.inter * c.hidden * 17 / 32 / 31e3;  // us x SMs
+    const double dn_rt = n_rt * (double)c.hidden * c.inter * 17 / 32 / 24e3;
+    const double gu_sh = 2.0 * R * c.hidden * 2 / (57e3 / (1.0 + 0.566 * (T - 1)));
+    const double dn_sh = (double)R * c.hidden * 2 / (61e3 / (1.0 + 0.671 * (T - 1)));
+    auto split = [&](double sh, double rt, double rt_delay) {
+      int best = 1;
+      double best_t = 1e30;
+      for (int n = 1; n < h->sms; ++n) {
+        const double t = std::max(sh / n, rt / (h->sms - n) + rt_delay);
+        if (t < best_t) { best_t = t; best = n; }
+      }
+      return best;
+    };
+    sh_gu = split(gu_sh, gu_rt, T == 1 ? 7.0 : 0.0);
+    sh_dn = split(dn_sh, dn_rt, 0.0);
   }
-  if (c.n_shared > 0 && !split) {
-    rc = shared_part(h, l, x, T, h->ysh, s);
+  int rc = route(h, l, x, T, ids, w, s, nullptr, tg, /*planes_only=*/phase);
+  if (rc) return rc;
+  if (phase) {
+    // decode batches: routed and shared experts together on every SM, each
+    // kernel a programmatic dependent of the one before
+    RUN(h, K_GATEUP, s, launch_phase_gateup(L.sh_gate, L.sh_up, R, L.arena, h->span_bytes,
+                                            c.hidden, c.inter, c.top_k, x, T, h->items,
+                                            h->n_items, h->sorted, h->router_part,
+                                            h->rsplit.nsplit, c.n_experts, ids, w, h->hsh,
+                                            h->hbuf, h->err, sh_gu, s));
+    RUN(h, K_DOWN, s, launch_phase_down(L.arena, h->span_bytes, c.hidden, c.inter, h->items,
+                                        h->n_items, h->sorted, h->hbuf, h->part, L.sh_down, R,
+                                        h->hsh, T, h->ysh, h->err, sh_dn, s));
+  } else {
+    // batches: the shared experts, then the routed ones
+    if (c.n_shared > 0) {
+      rc = shared_part(h, l, x, T, h->ysh, s);
+      if (rc) return rc;
+    }
+    rc = expert_gateup(h, l, x, T, max_items, tg, h->hbuf, s);
+    if (rc) return rc;
+    rc = expert_down(h, l, h->hbuf, T, max_items, tg, s, 0, /*after_gateup=*/true);
     if (rc) return rc;
   }
-  const int rt_ctas = split ? h->sms - sh_ctas : 0;
-  rc = expert_gateup(h, l, x, T, max_items, tg, h->hbuf, s, rt_ctas);
-  if (rc) return rc;
-  rc = expert_down(h, l, h->hbuf, T, max_items, tg, s, rt_ctas);
-  if (rc) return rc;
-  if (split) CUDA_OR_FAIL(h, cudaStreamWaitEvent(s, h->ev_join, 0));
   RUN(h, K_COMBINE, s, launch_combine(h->part, w, T, c.top_k, c.hidden,
                                       c.n_shared > 0 ? h->ysh : nullptr,
                                       residual, out_f32, out_bf16, s));
@@ -441,9 +462,6 @@ void df_moe_destroy(df_moe* h) {
     cudaEventDestroy(p.b);
   }
   for (auto e : h->event_pool) cudaEventDestroy(e);
-  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
-  if (h->ev_join) cudaEventDestroy(h->ev_join);
-  if (h->s2) cudaStreamDestroy(h->s2);
   for (void* p : h->allocs) cudaFree(p);
   cudaSetDevice(prev);
   delete h;
@@ -590,10 +608,7 @@ int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
   if (!rc) rc = dalloc(h, &h->hw, (size_t)c.n_layers * Tm * k);
   if (!rc) {
     cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, cuda_device);
-    if (cudaStreamCreateWithFlags(&h->s2, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess)
-      rc = fail(h, DF_MOE_ECUDA, "stream or event creation failed");
+    h->phase = phase_supported(H, c.inter, c.n_shared > 0 ? h->R : 0, c.n_experts, c.top_k);
   }
   if (!rc && (cudaMemset(h->err, 0, sizeof(uint32_t)) != cudaSuccess ||
               cudaMemset(h->counter, 0, sizeof(unsigned int)) != cudaSuccess))

@@ -145,11 +145,14 @@ cudaError_t launch_gateup(const uint8_t* arena, size_t span_bytes, int H,
                           const int32_t* n_items, int max_items,
                           const int32_t* sorted, float* hbuf, int tg,
                           uint32_t* err, cudaStream_t s, int max_ctas = 0);
+// after_gateup: the preceding kernel on `s` is the gate/up kernel of the same
+// selection (so the selection is complete when this grid starts, and the
+// weight stream may begin before h is).
 cudaError_t launch_down(const uint8_t* arena, size_t span_bytes, int H, int I,
                         const Item* items, const int32_t* n_items,
                         int max_items, const int32_t* sorted,
                         const float* hbuf, float* part, int tg, uint32_t* err,
-                        cudaStream_t s, int max_ctas = 0);
+                        cudaStream_t s, int max_ctas = 0, bool after_gateup = false);
 cudaError_t launch_combine(const float* part, const float* w, int T, int k,
                            int H, const float* ysh, const uint16_t* residual,
                            float* out_f32, uint16_t* out_bf16, cudaStream_t s);
@@ -162,6 +165,26 @@ cudaError_t launch_shared_down(const uint16_t* down, int H, int K,
                                uint32_t* err, cudaStream_t s, int max_ctas = 0);
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps,
                            uint16_t* xn, cudaStream_t s);
+// Decode batches (T <= kLayerMaxT): routed and shared experts in two phase
+// kernels on every SM (k_phase.cu). The gate/up phase follows the router
+// (T = 1: it selects the experts itself from the partial logits
+// router_part [nsplit][E], writing ids, w, items, n_items and sorted) or the
+// grouping kernel (T > 1: items, n_items, sorted are its inputs) directly on
+// `s`; the down phase follows the gate/up phase directly. R = n_shared * Is
+// (0: no shared experts). n_sh: CTAs (of one per SM) that run the shared
+// experts, in [1, SMs - 1] (0 when R = 0); the others run the routed ones.
+bool phase_supported(int H, int I, int R, int E, int k);
+cudaError_t launch_phase_gateup(const uint16_t* sh_gate, const uint16_t* sh_up, int R,
+                                const uint8_t* arena, size_t span_bytes, int H, int I, int k,
+                                const uint16_t* x, int T, Item* items, int32_t* n_items,
+                                int32_t* sorted, const float* router_part, int nsplit, int E,
+                                int32_t* ids, float* w, float* hsh, float* hbuf, uint32_t* err,
+                                int n_sh, cudaStream_t s);
+cudaError_t launch_phase_down(const uint8_t* arena, size_t span_bytes, int H, int I,
+                              const Item* items, const int32_t* n_items, const int32_t* sorted,
+                              const float* hbuf, float* part, const uint16_t* sh_down, int R,
+                              const float* hsh, int T, float* ysh, uint32_t* err, int n_sh,
+                              cudaStream_t s);
 cudaError_t launch_repack_span(const uint8_t* src, uint8_t* dst, int n_spans,
                                int H, int I, int inverse, cudaStream_t s);
 

@@ -10,84 +10,15 @@
 
 #include "internal.h"
 #include "pipeline.cuh"
+#include "select.cuh"
 
 namespace dfm {
 namespace {
 
 constexpr int kRouterRowsPerBlock = 8;  // one warp per (row, column split)
 constexpr int kRouterMaxV = 16;         // float4 loads per lane: split <= 2048
-
-__device__ __forceinline__ bool better(float v, int e, float bv, int be) {
-  return v > bv || (v == bv && e < be);
-}
-
-// Top-k of lg[0..E) (shared memory) by the first 128 threads of the block:
-// four warps select the top k of their quarter, warp 0 merges the 4k
-// candidates. On return lanes 0..k-1 of warp 0 hold (value, id) of rank
-// `lane`, descending. cand_v / cand_e: shared scratch of 4 * 32 entries.
-__device__ void block_topk(const float* lg, int E, int k, float* cand_v,
-                           int* cand_e, float& out_v, int& out_e) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp < 4) {
-    float v[8];
-    int id[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = warp * 256 + lane + 32 * i;
-      v[i] = e < E ? lg[e] : -INFINITY;
-      id[i] = e < E ? e : 0x7fffffff;
-    }
-    for (int r = 0; r < k; ++r) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (better(v[i], id[i], bv, be)) { bv = v[i]; be = id[i]; }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (id[i] == be) v[i] = -INFINITY;  // taken
-      if (lane == 0) {
-        cand_v[warp * 32 + r] = bv;
-        cand_e[warp * 32 + r] = be;
-      }
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    float v[4];
-    int id[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int c = lane + 32 * i;  // candidate slot: warp c/32, rank c%32
-      const bool valid = (c & 31) < k;
-      v[i] = valid ? cand_v[c] : -INFINITY;
-      id[i] = valid ? cand_e[c] : 0x7fffffff;
-    }
-    for (int r = 0; r < k; ++r) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (better(v[i], id[i], bv, be)) { bv = v[i]; be = id[i]; }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (better(ov, oe, bv, be)) { bv = ov; be = oe; }
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (id[i] == be) v[i] = -INFINITY;
-      if (lane == r) { out_v = bv; out_e = be; }
-    }
-  }
-}
+constexpr int kRouterThreads = 32 * kRouterRowsPerBlock;
+constexpr int kTopkThreads = 256;       // top-k blocks of the batch path
 
 // Softmax over the k selected logits (warp 0, lanes 0..k-1 hold them) and
 // the writes of ids / weights (and, for a single token, the work items).
@@ -95,14 +26,10 @@ __device__ void write_selection(int t, int k, float sel_v, int sel_e,
                                 int32_t* ids, float* w, Item* items,
                                 int32_t* n_items, int32_t* sorted) {
   const int lane = threadIdx.x & 31;
-  const float vmax = __shfl_sync(0xffffffffu, sel_v, 0);
-  const float ex = lane < k ? expf(sel_v - vmax) : 0.f;
-  float z = ex;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  const float wt = selected_softmax(k, sel_v);
   if (lane < k) {
     ids[(size_t)t * k + lane] = sel_e;
-    w[(size_t)t * k + lane] = ex / z;
+    w[(size_t)t * k + lane] = wt;
     if (items) {
       items[lane] = Item{sel_e, lane, 1, 0};
       sorted[lane] = lane;
@@ -123,8 +50,12 @@ struct TopkFuse {  // fused top-k of a single token by the router's last block
 
 // part[split][t][e] = sum over the split's columns of Wr[e][j] x[t][j].
 // One warp per (row, split); every weight load of the warp is issued before
-// the first FMA, and the weights stay in registers across tokens.
-__global__ void __launch_bounds__(256)
+// the first FMA. Tokens go in passes of NT, each weight register feeding the
+// NT accumulators of a pass, so the weights are read once per call. For one
+// token at most 80 registers a thread (three blocks an SM, so that the K3
+// router's 448 blocks run as a single wave on 152 SMs), else at most 128 (two).
+template <int NT>
+__global__ void __launch_bounds__(kRouterThreads, NT == 1 ? 3 : 2)
 router_kernel(const float* __restrict__ Wr, int E, int H,
               const uint16_t* __restrict__ x, int T, float* __restrict__ part,
               int split_len, TopkFuse fz) {
@@ -142,31 +73,40 @@ router_kernel(const float* __restrict__ Wr, int E, int H,
     for (int i = 0; i < kRouterMaxV; ++i)
       w4[i] = (4 * lane + 128 * i < len) ? __ldg(reinterpret_cast<const float4*>(wr + 128 * i))
                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int t = 0; t < T; ++t) {
-      const uint16_t* xp = x + (size_t)t * H + k0 + 4 * lane;
-      float acc = 0.f;
+    for (int t0 = 0; t0 < T; t0 += NT) {
+      float acc[NT];
+#pragma unroll
+      for (int u = 0; u < NT; ++u) acc[u] = 0.f;
 #pragma unroll
       for (int i = 0; i < kRouterMaxV; ++i) {
         if (4 * lane + 128 * i < len) {
-          const uint2 xv = __ldg(reinterpret_cast<const uint2*>(xp + 128 * i));
-          acc = fmaf(w4[i].x, __uint_as_float(xv.x << 16), acc);
-          acc = fmaf(w4[i].y, __uint_as_float(xv.x & 0xFFFF0000u), acc);
-          acc = fmaf(w4[i].z, __uint_as_float(xv.y << 16), acc);
-          acc = fmaf(w4[i].w, __uint_as_float(xv.y & 0xFFFF0000u), acc);
+#pragma unroll
+          for (int u = 0; u < NT; ++u) {
+            if (t0 + u < T) {
+              const uint2 xv = __ldg(reinterpret_cast<const uint2*>(
+                  x + (size_t)(t0 + u) * H + k0 + 4 * lane + 128 * i));
+              acc[u] = fmaf(w4[i].x, __uint_as_float(xv.x << 16), acc[u]);
+              acc[u] = fmaf(w4[i].y, __uint_as_float(xv.x & 0xFFFF0000u), acc[u]);
+              acc[u] = fmaf(w4[i].z, __uint_as_float(xv.y << 16), acc[u]);
+              acc[u] = fmaf(w4[i].w, __uint_as_float(xv.y & 0xFFFF0000u), acc[u]);
+            }
+          }
         }
       }
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (lane == 0) part[((size_t)split * T + t) * E + e] = acc;
+      for (int u = 0; u < NT; ++u) {
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], o);
+        if (lane == 0 && t0 + u < T) part[((size_t)split * T + t0 + u) * E + e] = acc[u];
+      }
     }
   }
   if (!fz.counter) return;
 
   // ---- single token: the last block to finish selects the experts ----
   __shared__ unsigned int ticket;
-  __shared__ float lg[1024];
-  __shared__ float cand_v[128];
-  __shared__ int cand_e[128];
+  __shared__ float cand_v[kRouterThreads];
+  __shared__ int cand_e[kRouterThreads];
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -176,15 +116,11 @@ router_kernel(const float* __restrict__ Wr, int E, int H,
   if (ticket != gridDim.x * gridDim.y - 1) return;
   __threadfence();
   const int nsplit = gridDim.y;
-  for (int i = threadIdx.x; i < E; i += blockDim.x) {
-    float v = 0.f;
-    for (int s = 0; s < nsplit; ++s) v += __ldcg(part + (size_t)s * E + i);
-    lg[i] = v;
-  }
-  __syncthreads();
   float sel_v = 0.f;
   int sel_e = 0;
-  block_topk(lg, E, fz.k, cand_v, cand_e, sel_v, sel_e);
+  block_topk<kRouterThreads / 32>(
+      [&](int i) { return sum_planes<true>(part + i, E, nsplit); },
+      E, cand_v, cand_e, sel_v, sel_e);
   if (warp == 0) {
     write_selection(0, fz.k, sel_v, sel_e, fz.ids, fz.w, fz.items, fz.n_items,
                     fz.sorted);
@@ -192,27 +128,25 @@ router_kernel(const float* __restrict__ Wr, int E, int H,
   }
 }
 
-// One block of 128 threads per token: sum the split partials (fixed order),
+// One block of kTopkThreads per token: sum the split partials (fixed order),
 // select the top k and the softmax weights.
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kTopkThreads)
 topk_kernel(const float* __restrict__ part, int nsplit, int T, int E, int k,
             float* __restrict__ logits_out, int32_t* __restrict__ ids,
             float* __restrict__ w, Item* items, int32_t* n_items,
             int32_t* sorted) {
-  __shared__ float lg[1024];
-  __shared__ float cand_v[128];
-  __shared__ int cand_e[128];
+  __shared__ float cand_v[kTopkThreads];
+  __shared__ int cand_e[kTopkThreads];
   const int t = blockIdx.x;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    float v = 0.f;
-    for (int s = 0; s < nsplit; ++s) v += part[((size_t)s * T + t) * E + e];
-    lg[e] = v;
-    if (logits_out) logits_out[(size_t)t * E + e] = v;
-  }
-  __syncthreads();
   float sel_v = 0.f;
   int sel_e = 0;
-  block_topk(lg, E, k, cand_v, cand_e, sel_v, sel_e);
+  block_topk<kTopkThreads / 32>(
+      [&](int e) {
+        const float v = sum_planes<false>(part + (size_t)t * E + e, (size_t)T * E, nsplit);
+        if (logits_out) logits_out[(size_t)t * E + e] = v;
+        return v;
+      },
+      E, cand_v, cand_e, sel_v, sel_e);
   if (threadIdx.x < 32)
     write_selection(t, k, sel_v, sel_e, ids, w, (items && T == 1) ? items : nullptr,
                     n_items, sorted);
@@ -416,14 +350,21 @@ cudaError_t launch_router(const float* Wr, int E, int H, const uint16_t* x,
     fz = TopkFuse{fuse->counter, fuse->k, fuse->ids, fuse->w, fuse->items,
                   fuse->n_items, fuse->sorted};
   dim3 grid((E + kRouterRowsPerBlock - 1) / kRouterRowsPerBlock, sp.nsplit);
-  router_kernel<<<grid, 256, 0, s>>>(Wr, E, H, x, T, part, sp.split_len, fz);
+  if (T == 1)
+    router_kernel<1><<<grid, kRouterThreads, 0, s>>>(Wr, E, H, x, T, part, sp.split_len, fz);
+  else if (T <= 2)
+    router_kernel<2><<<grid, kRouterThreads, 0, s>>>(Wr, E, H, x, T, part, sp.split_len, fz);
+  else if (T <= 4)
+    router_kernel<4><<<grid, kRouterThreads, 0, s>>>(Wr, E, H, x, T, part, sp.split_len, fz);
+  else
+    router_kernel<8><<<grid, kRouterThreads, 0, s>>>(Wr, E, H, x, T, part, sp.split_len, fz);
   return cudaGetLastError();
 }
 
 cudaError_t launch_topk(const float* part, int nsplit, int T, int E, int k,
                         float* logits_out, int32_t* ids, float* w, Item* items,
                         int32_t* n_items, int32_t* sorted, cudaStream_t s) {
-  topk_kernel<<<T, 128, 0, s>>>(part, nsplit, T, E, k, logits_out, ids, w,
+  topk_kernel<<<T, kTopkThreads, 0, s>>>(part, nsplit, T, E, k, logits_out, ids, w,
                                 items, n_items, sorted);
   return cudaGetLastError();
 }

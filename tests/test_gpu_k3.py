@@ -88,6 +88,28 @@ def test_router_and_topk_steps(k3, torch):
     assert np.max(np.abs(w.cpu().double().numpy() - rw)) <= 1e-6
 
 
+def test_topk_step_ties(k3, torch):
+    """Selection at full width (896 logits, top 16) with ties everywhere:
+    equal logits go to the lower id, ids come out best first."""
+    rng = np.random.default_rng(5)
+    T = 9
+    lg = rng.standard_normal((T, WL1.E)).astype(np.float32)
+    lg[0, :] = 0.25                                   # all tied
+    top = np.sort(lg[1])[::-1]
+    lg[1, rng.permutation(WL1.E)[:40]] = top[15]      # 40 ties across the cut
+    lg[2] = rng.integers(0, 5, WL1.E).astype(np.float32)  # five distinct values
+    lg[3, WL1.E - 16:] = 9.0                          # the best are the last ids
+    lg[4, :] = -np.inf
+    lg[4, [895, 3, 500]] = [1.0, 1.0, 2.0]            # -inf fills the rest
+    ids = torch.empty((T, WL1.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, WL1.k), dtype=torch.float32, device="cuda")
+    k3.m.step_topk(torch.from_numpy(lg).cuda(), T, ids, w)
+    torch.cuda.synchronize()
+    rid, rw = orc.topk_softmax(lg.astype(np.float64), WL1.k)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert np.max(np.abs(w.cpu().double().numpy() - rw)) <= 1e-6
+
+
 def test_expert_steps(k3, torch):
     T = 2
     x = _tokens(k3, WL2, T, first_id=60)
@@ -159,5 +181,33 @@ def test_ragged_batch(k3, torch):
     x = _tokens(k3, WL2, T, first_id=500)
     out, out32, ids, w = _forward(k3.m, x, T, torch)
     ref = orc.moe_layer(k3.layers[0], x)
+    check_ids_weights(ids, w, ref["ids"], ref["w"])
+    check_out(out32, ref["out"])
+
+
+def _bf16_rne(v):
+    """float64 array -> bf16 bits, round to nearest even through fp32."""
+    u = np.asarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def test_verify_pass_t2(k3, torch):
+    """A two-position verify call (n-gram speculation checks a drafted token
+    in the same pass as the current one [Deltafin README, "N-gram
+    speculation"]). The drafted position's hidden state is correlated with
+    the first (0.8 x1 + 0.6 z), so the two top-16 sets overlap and the
+    shared experts are read once for both positions."""
+    from moe_setup import gap_ok
+    x1 = _tokens(k3, WL1, 1, first_id=900)[0]
+    for r in range(synth.gen.REDRAWS_PER_TOKEN):
+        z = synth.token(WL1.seed, WL1.cfg_id, 901, WL1.H, redraw=r)
+        x2 = _bf16_rne(0.8 * bits_to_f64(x1) + 0.6 * bits_to_f64(z))
+        if gap_ok(orc.router_logits(k3.routers[0], x2[None]), WL1.k):
+            break
+    x = np.stack([x1, x2])
+    out, out32, ids, w = _forward(k3.m, x, 2, torch)
+    ref = orc.moe_layer(k3.layers[0], x)
+    shared = len(set(ref["ids"][0]) & set(ref["ids"][1]))
+    assert shared >= 2, "the drafted position shares %d experts" % shared
     check_ids_weights(ids, w, ref["ids"], ref["w"])
     check_out(out32, ref["out"])
