@@ -237,7 +237,7 @@ DF_MOE_API int df_moe_last_launch_count(const df_moe* h);
  * is part of the library: every GPU that loads the library holds it until the
  * process exits. The call allocates nothing (no cudaMalloc/cudaFree, no
  * allocating library routine).
- *   router  device [E][H] fp32      x_bf16  device [T][H] bf16
+ *   router  device [E][H] fp32      x_bf16  device [T][H] bf16, 16-byte aligned
  *   ids     device [T][k] int32     weights device [T][k] fp32
  * Limits: H a multiple of 32 up to 8192, 1 <= E <= 1024, 1 <= k <=
  * min(E, 32), and the scratch must hold nsplit*T*E floats (262,144 floats;

@@ -384,15 +384,16 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
   if (phase && R > 0) {
     // CTAs for the shared experts in each phase: the split that ends both
     // sides together at the per-SM streaming rates measured on GB300 at K3
-    // shape (GB/s an SM): routed MXFP4 gate/up ~31, down ~24; shared bf16
-    // gate/up ~57 and down ~61 at one token, falling as the fp32 FMAs per
-    // byte grow with T (~11.6 and ~10.7 at T = 8). At T = 1 the routed CTAs
-    // first spend ~7 us selecting the experts.
+    // shape (GB/s an SM): routed MXFP4 gate/up ~32, down ~27; shared bf16
+    // gate/up ~60 and down ~68 at one token, falling as the fp32 FMAs per
+    // byte grow with the tokens a pass (~9 and ~11 at 8). At T = 1 the routed
+    // CTAs first spend ~6 us selecting the experts.
     const double n_rt = std::min(T * c.top_k, c.n_experts);
-    const double gu_rt = n_rt * 2.0 * c.inter * c.hidden * 17 / 32 / 31e3;  // us x SMs
-    const double dn_rt = n_rt * (double)c.hidden * c.inter * 17 / 32 / 24e3;
-    const double gu_sh = 2.0 * R * c.hidden * 2 / (57e3 / (1.0 + 0.566 * (T - 1)));
-    const double dn_sh = (double)R * c.hidden * 2 / (61e3 / (1.0 + 0.671 * (T - 1)));
+    const double gu_rt = n_rt * 2.0 * c.inter * c.hidden * 17 / 32 / 32e3;  // us x SMs
+    const double dn_rt = n_rt * (double)c.hidden * c.inter * 17 / 32 / 27e3;
+    const int TT = T == 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;  // shared tokens a pass
+    const double gu_sh = 2.0 * R * c.hidden * 2 / (60e3 / (1.0 + 0.81 * (TT - 1)));
+    const double dn_sh = (double)R * c.hidden * 2 / (68e3 / (1.0 + 0.74 * (TT - 1)));
     auto split = [&](double sh, double rt, double rt_delay) {
       int best = 1;
       double best_t = 1e30;
@@ -402,7 +403,7 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
       }
       return best;
     };
-    sh_gu = split(gu_sh, gu_rt, T == 1 ? 7.0 : 0.0);
+    sh_gu = split(gu_sh, gu_rt, T == 1 ? 6.0 : 0.0);
     sh_dn = split(dn_sh, dn_rt, 0.0);
   }
   int rc = route(h, l, x, T, ids, w, s, nullptr, tg, /*planes_only=*/phase);

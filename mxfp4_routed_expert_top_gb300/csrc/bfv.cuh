@@ -116,7 +116,9 @@ __host__ __device__ inline size_t bfv_smem_bytes(int K) {
 // come from the preceding grid (programmatic dependent launch); without it
 // they must have been complete when the grid started. Inputs are read
 // through L2 only.
-template <int MODE, bool ONE>
+// TT: tokens a pass (1, 2, 4 or 8); with TT = 1 the one token's x stays in
+// registers across tiles.
+template <int MODE, int TT>
 __device__ __forceinline__ void bfv_cta(const BfvArgs& a, uint8_t* smem, uint64_t* bars,
                                         int cta, int ncta, bool wait) {
   const int NW = bfv_warps(a.K);
@@ -190,6 +192,7 @@ __device__ __forceinline__ void bfv_cta(const BfvArgs& a, uint8_t* smem, uint64_
   const bool reducer = role == NW + 1;
   const int w = role;
   const int c0 = w * kColsPerWarp + 8 * lane;
+  constexpr bool ONE = TT == 1;
   float xr[kIt][8];  // x of the single token (ONE), kept across tiles
 #pragma unroll
   for (int i = 0; i < kIt; ++i) {
@@ -208,7 +211,6 @@ __device__ __forceinline__ void bfv_cta(const BfvArgs& a, uint8_t* smem, uint64_
       }
     }
   }
-  constexpr int TT = ONE ? 1 : kTT;
   uint32_t stage = 0, phase = 0;
   int n_epi = 0;
   bool ok = true;
@@ -218,10 +220,10 @@ __device__ __forceinline__ void bfv_cta(const BfvArgs& a, uint8_t* smem, uint64_
       if (!ok) break;
     }
     const uint16_t* tile = reinterpret_cast<const uint16_t*>(base + (size_t)stage * geo.stage_bytes);
-    const int groups = ONE ? 1 : (a.T + kTT - 1) / kTT;
+    const int groups = ONE ? 1 : (a.T + TT - 1) / TT;
     for (int gi = 0; gi < groups && ok; ++gi) {
-      const int t0 = gi * kTT;
-      const int tt = ONE ? 1 : min(kTT, a.T - t0);
+      const int t0 = gi * TT;
+      const int tt = ONE ? 1 : min(TT, a.T - t0);
       const int ri = n_epi % kRing, u = n_epi / kRing;
       float* rb = red + (size_t)ri * NW * kRows * kTT;
       if (!reducer) {

@@ -60,7 +60,7 @@ cudaError_t launch_mxv(const MxvArgs& a, int max_items, cudaStream_t s, int max_
   constexpr int CG = mxv_cg(MODE);
   const int NS = slots_per_cta(K, CG);
   const int threads = NS * mxv_wps(K, CG) * 32;
-  const size_t smem = mxv_smem_bytes(K, CG);
+  const size_t smem = mxv_smem_bytes(K, CG, mxv_unit(MODE));
   static int configured_smem[2] = {0, 0};
   if (configured_smem[MODE] < (int)smem) {
     cudaError_t e = cudaFuncSetAttribute(mxv_kernel<MODE>,

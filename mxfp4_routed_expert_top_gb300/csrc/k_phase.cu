@@ -31,7 +31,8 @@ struct SelArgs {       // one token's selection inside the gate/up phase
   float* w;
 };
 
-template <bool ONE>
+// TT: the shared experts' tokens a pass (1, 2, 4 or 8); TT = 1 is one token.
+template <int TT>
 __global__ void __launch_bounds__(kPhaseThreads, 1)
 phase_gateup_kernel(const BfvArgs sh, const MxvArgs rt_in, const SelArgs sel, int n_sh) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -40,7 +41,7 @@ phase_gateup_kernel(const BfvArgs sh, const MxvArgs rt_in, const SelArgs sel, in
   __shared__ int32_t sel_sorted[32];
   __shared__ int32_t sel_n;
   if ((int)blockIdx.x < n_sh) {
-    bfv_cta<0, ONE>(sh, smem, bars, blockIdx.x, n_sh, /*wait=*/false);
+    bfv_cta<0, TT>(sh, smem, bars, blockIdx.x, n_sh, /*wait=*/false);
     return;
   }
   const int cta = blockIdx.x - n_sh, ncta = gridDim.x - n_sh;
@@ -48,7 +49,7 @@ phase_gateup_kernel(const BfvArgs sh, const MxvArgs rt_in, const SelArgs sel, in
   // the routed pipeline's barriers are set up while the router finishes
   mxv_set_up_barriers<0>(rt, bars);
   pdl_wait();  // the router (one token) or the grouping kernel
-  if (ONE && sel.part) {
+  if (TT == 1 && sel.part) {
     float sel_v = 0.f;
     int sel_e = 0;
     block_topk<kPhaseThreads / 32>(
@@ -86,7 +87,7 @@ phase_gateup_kernel(const BfvArgs sh, const MxvArgs rt_in, const SelArgs sel, in
   mxv_cta<0>(rt, smem, bars, cta, ncta, /*set_up=*/false);
 }
 
-template <bool ONE>
+template <int TT>
 __global__ void __launch_bounds__(kPhaseThreads, 1)
 phase_down_kernel(const MxvArgs rt, const BfvArgs sh, int n_rt) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -94,7 +95,7 @@ phase_down_kernel(const MxvArgs rt, const BfvArgs sh, int n_rt) {
   if ((int)blockIdx.x < n_rt)
     mxv_cta<1>(rt, smem, bars, blockIdx.x, n_rt);  // rt.early: streams before h
   else
-    bfv_cta<1, ONE>(sh, smem, bars, blockIdx.x - n_rt, gridDim.x - n_rt, /*wait=*/true);
+    bfv_cta<1, TT>(sh, smem, bars, blockIdx.x - n_rt, gridDim.x - n_rt, /*wait=*/true);
 }
 
 int phase_sms() {
@@ -120,8 +121,8 @@ cudaError_t set_smem(Kern kernel, size_t smem, size_t& configured) {
 }  // namespace
 
 bool phase_supported(int H, int I, int R, int E, int k) {
-  const size_t gu = std::max(bfv_smem_bytes(H), mxv_smem_bytes(H, mxv_cg(0)));
-  const size_t dn = std::max(mxv_smem_bytes(I, mxv_cg(1)), bfv_smem_bytes(R > 0 ? R : I));
+  const size_t gu = std::max(bfv_smem_bytes(H), mxv_smem_bytes(H, mxv_cg(0), mxv_unit(0)));
+  const size_t dn = std::max(mxv_smem_bytes(I, mxv_cg(1), mxv_unit(1)), bfv_smem_bytes(R > 0 ? R : I));
   const size_t stat = (kBfvBars > kMxvBars ? kBfvBars : kMxvBars) * 8 + 1024;
   return H % 64 == 0 && I % 64 == 0 && E <= 1024 && k <= 32 && gu + stat <= 227 * 1024 &&
          dn + stat <= 227 * 1024 && gu >= kPhaseThreads * 8;
@@ -136,15 +137,18 @@ cudaError_t launch_phase_gateup(const uint16_t* sh_gate, const uint16_t* sh_up, 
   const BfvArgs sh{sh_gate, sh_up, R, H, x, T, hsh, err};
   const MxvArgs rt{arena, span_bytes, H, I, k, x, nullptr, items, n_items, sorted, hbuf, err, 0};
   const SelArgs sel{T == 1 ? router_part : nullptr, nsplit, E, k, ids, w};
-  const size_t smem = std::max(bfv_smem_bytes(H), mxv_smem_bytes(H, mxv_cg(0)));
-  static size_t conf[2] = {0, 0};
-  cudaError_t e = T == 1 ? set_smem(phase_gateup_kernel<true>, smem, conf[1])
-                         : set_smem(phase_gateup_kernel<false>, smem, conf[0]);
-  if (e != cudaSuccess) return e;
-  return T == 1 ? launch_after_previous(phase_gateup_kernel<true>, dim3(phase_sms()),
-                                        dim3(kPhaseThreads), smem, s, sh, rt, sel, n_sh)
-                : launch_after_previous(phase_gateup_kernel<false>, dim3(phase_sms()),
-                                        dim3(kPhaseThreads), smem, s, sh, rt, sel, n_sh);
+  const size_t smem = std::max(bfv_smem_bytes(H), mxv_smem_bytes(H, mxv_cg(0), mxv_unit(0)));
+  auto go = [&](auto kernel, size_t& conf) {
+    const cudaError_t e = set_smem(kernel, smem, conf);
+    if (e != cudaSuccess) return e;
+    return launch_after_previous(kernel, dim3(phase_sms()), dim3(kPhaseThreads), smem, s, sh, rt,
+                                 sel, n_sh);
+  };
+  static size_t conf[4] = {0, 0, 0, 0};
+  return T == 1   ? go(phase_gateup_kernel<1>, conf[0])
+         : T <= 2 ? go(phase_gateup_kernel<2>, conf[1])
+         : T <= 4 ? go(phase_gateup_kernel<4>, conf[2])
+                  : go(phase_gateup_kernel<8>, conf[3]);
 }
 
 cudaError_t launch_phase_down(const uint8_t* arena, size_t span_bytes, int H, int I,
@@ -156,15 +160,19 @@ cudaError_t launch_phase_down(const uint8_t* arena, size_t span_bytes, int H, in
                    1};
   // no shared experts: no rows to stream (K only sizes the geometry)
   const BfvArgs sh{sh_down, nullptr, R > 0 ? H : 0, R > 0 ? R : I, hsh, T, ysh, err};
-  const size_t smem = std::max(mxv_smem_bytes(I, mxv_cg(1)), bfv_smem_bytes(sh.K));
-  static size_t conf[2] = {0, 0};
-  cudaError_t e = T == 1 ? set_smem(phase_down_kernel<true>, smem, conf[1])
-                         : set_smem(phase_down_kernel<false>, smem, conf[0]);
-  if (e != cudaSuccess) return e;
-  return T == 1 ? launch_after_previous(phase_down_kernel<true>, dim3(phase_sms()),
-                                        dim3(kPhaseThreads), smem, s, rt, sh, phase_sms() - n_sh)
-                : launch_after_previous(phase_down_kernel<false>, dim3(phase_sms()),
-                                        dim3(kPhaseThreads), smem, s, rt, sh, phase_sms() - n_sh);
+  const size_t smem = std::max(mxv_smem_bytes(I, mxv_cg(1), mxv_unit(1)), bfv_smem_bytes(sh.K));
+  const int n_rt = phase_sms() - n_sh;
+  auto go = [&](auto kernel, size_t& conf) {
+    const cudaError_t e = set_smem(kernel, smem, conf);
+    if (e != cudaSuccess) return e;
+    return launch_after_previous(kernel, dim3(phase_sms()), dim3(kPhaseThreads), smem, s, rt, sh,
+                                 n_rt);
+  };
+  static size_t conf[4] = {0, 0, 0, 0};
+  return T == 1   ? go(phase_down_kernel<1>, conf[0])
+         : T <= 2 ? go(phase_down_kernel<2>, conf[1])
+         : T <= 4 ? go(phase_down_kernel<4>, conf[2])
+                  : go(phase_down_kernel<8>, conf[3]);
 }
 
 }  // namespace dfm

@@ -66,14 +66,33 @@ router_kernel(const float* __restrict__ Wr, int E, int H,
   pdl_launch_dependents();
   const int k0 = split * split_len;
   const int len = min(split_len, H - k0);
+  // each pass's slice of x, [NT][split_len] bf16, is staged in shared
+  // memory (all its loads issued at once; the first pass while the weight
+  // loads are in flight)
+  extern __shared__ __align__(16) uint16_t xs[];
+  float4 w4[kRouterMaxV];
   if (e < E) {
-    float4 w4[kRouterMaxV];
     const float* wr = Wr + (size_t)e * H + k0 + 4 * lane;
 #pragma unroll
     for (int i = 0; i < kRouterMaxV; ++i)
       w4[i] = (4 * lane + 128 * i < len) ? __ldg(reinterpret_cast<const float4*>(wr + 128 * i))
                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int t0 = 0; t0 < T; t0 += NT) {
+  }
+  // x and the outputs' readers come from the preceding kernels; the weights
+  // (read above) do not
+  pdl_wait();
+  const int q8 = len >> 3;  // 8 bf16 a copy (len is a multiple of 32)
+  for (int t0 = 0; t0 < T; t0 += NT) {
+    const int nt = min(NT, T - t0);
+    if (t0 > 0) __syncthreads();  // the previous pass has read its slice
+    for (int q = threadIdx.x; q < nt * q8; q += blockDim.x) {
+      const int t = q / q8, c = q - t * q8;
+      reinterpret_cast<uint4*>(xs + (size_t)t * split_len)[c] =
+          __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * H + k0) + c);
+    }
+    __syncthreads();
+    if (e >= E) continue;
+    {
       float acc[NT];
 #pragma unroll
       for (int u = 0; u < NT; ++u) acc[u] = 0.f;
@@ -83,8 +102,8 @@ router_kernel(const float* __restrict__ Wr, int E, int H,
 #pragma unroll
           for (int u = 0; u < NT; ++u) {
             if (t0 + u < T) {
-              const uint2 xv = __ldg(reinterpret_cast<const uint2*>(
-                  x + (size_t)(t0 + u) * H + k0 + 4 * lane + 128 * i));
+              const uint2 xv = *reinterpret_cast<const uint2*>(
+                  xs + (size_t)u * split_len + 4 * lane + 128 * i);
               acc[u] = fmaf(w4[i].x, __uint_as_float(xv.x << 16), acc[u]);
               acc[u] = fmaf(w4[i].y, __uint_as_float(xv.x & 0xFFFF0000u), acc[u]);
               acc[u] = fmaf(w4[i].z, __uint_as_float(xv.y << 16), acc[u]);
@@ -137,6 +156,9 @@ topk_kernel(const float* __restrict__ part, int nsplit, int T, int E, int k,
             int32_t* sorted) {
   __shared__ float cand_v[kTopkThreads];
   __shared__ int cand_e[kTopkThreads];
+  // the next kernel may start now: it waits for this grid before it reads
+  pdl_launch_dependents();
+  pdl_wait();  // the router's partial logits
   const int t = blockIdx.x;
   float sel_v = 0.f;
   int sel_e = 0;
@@ -194,6 +216,8 @@ group_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
   const int tid = threadIdx.x;
   const int A = T * k;
   cnt[tid] = 0;
+  pdl_launch_dependents();  // the next kernel waits for this grid itself
+  pdl_wait();  // the selected ids
   __syncthreads();
   for (int a = tid; a < A; a += blockDim.x) atomicAdd(&cnt[ids[a]], 1);
   __syncthreads();
@@ -350,32 +374,35 @@ cudaError_t launch_router(const float* Wr, int E, int H, const uint16_t* x,
     fz = TopkFuse{fuse->counter, fuse->k, fuse->ids, fuse->w, fuse->items,
                   fuse->n_items, fuse->sorted};
   dim3 grid((E + kRouterRowsPerBlock - 1) / kRouterRowsPerBlock, sp.nsplit);
+  const int nt = T == 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
+  const size_t xs = (size_t)nt * sp.split_len * sizeof(uint16_t);  // <= 8 * 2048 * 2
+  const dim3 block(kRouterThreads);
   if (T == 1)
-    router_kernel<1><<<grid, kRouterThreads, 0, s>>>(Wr, E, H, x, T, part, sp.split_len, fz);
-  else if (T <= 2)
-    router_kernel<2><<<grid, kRouterThreads, 0, s>>>(Wr, E, H, x, T, part, sp.split_len, fz);
-  else if (T <= 4)
-    router_kernel<4><<<grid, kRouterThreads, 0, s>>>(Wr, E, H, x, T, part, sp.split_len, fz);
-  else
-    router_kernel<8><<<grid, kRouterThreads, 0, s>>>(Wr, E, H, x, T, part, sp.split_len, fz);
-  return cudaGetLastError();
+    return launch_after_previous(router_kernel<1>, grid, block, xs, s, Wr, E, H, x, T, part,
+                                 sp.split_len, fz);
+  if (T <= 2)
+    return launch_after_previous(router_kernel<2>, grid, block, xs, s, Wr, E, H, x, T, part,
+                                 sp.split_len, fz);
+  if (T <= 4)
+    return launch_after_previous(router_kernel<4>, grid, block, xs, s, Wr, E, H, x, T, part,
+                                 sp.split_len, fz);
+  return launch_after_previous(router_kernel<8>, grid, block, xs, s, Wr, E, H, x, T, part,
+                               sp.split_len, fz);
 }
 
 cudaError_t launch_topk(const float* part, int nsplit, int T, int E, int k,
                         float* logits_out, int32_t* ids, float* w, Item* items,
                         int32_t* n_items, int32_t* sorted, cudaStream_t s) {
-  topk_kernel<<<T, kTopkThreads, 0, s>>>(part, nsplit, T, E, k, logits_out, ids, w,
-                                items, n_items, sorted);
-  return cudaGetLastError();
+  return launch_after_previous(topk_kernel, dim3(T), dim3(kTopkThreads), 0, s, part, nsplit, T, E,
+                               k, logits_out, ids, w, items, n_items, sorted);
 }
 
 cudaError_t launch_group(const int32_t* ids, int T, int k, int E,
                          int32_t* offs, int32_t* tok, int32_t* slot,
                          int32_t* n_union, Item* items, int32_t* n_items,
                          int32_t* sorted, int tg, cudaStream_t s) {
-  group_kernel<<<1, 1024, 0, s>>>(ids, T, k, E, offs, tok, slot, n_union,
-                                  items, n_items, sorted, tg);
-  return cudaGetLastError();
+  return launch_after_previous(group_kernel, dim3(1), dim3(1024), 0, s, ids, T, k, E, offs, tok,
+                               slot, n_union, items, n_items, sorted, tg);
 }
 
 }  // namespace dfm

@@ -5,11 +5,11 @@
 namespace dfm {
 namespace {
 
-template <int MODE, bool ONE>
+template <int MODE, int TT>
 __global__ void __launch_bounds__(512, 1) bfv_kernel(const BfvArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t bars[kBfvBars];
-  bfv_cta<MODE, ONE>(a, smem, bars, blockIdx.x, gridDim.x, true);
+  bfv_cta<MODE, TT>(a, smem, bars, blockIdx.x, gridDim.x, true);
 }
 
 int num_sms_b() {
@@ -23,13 +23,13 @@ int num_sms_b() {
   return n;
 }
 
-template <int MODE, bool ONE>
+template <int MODE, int TT>
 cudaError_t launch_bfv_t(const BfvArgs& a, cudaStream_t s, int max_ctas) {
   const int NS = bfv_slots(a.K);
   const size_t smem = bfv_smem_bytes(a.K);
   static size_t configured = 0;
   if (configured < smem) {
-    cudaError_t e = cudaFuncSetAttribute(bfv_kernel<MODE, ONE>,
+    cudaError_t e = cudaFuncSetAttribute(bfv_kernel<MODE, TT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured = smem;
@@ -38,14 +38,16 @@ cudaError_t launch_bfv_t(const BfvArgs& a, cudaStream_t s, int max_ctas) {
   int grid = (ntiles + NS - 1) / NS;
   if (grid > num_sms_b()) grid = num_sms_b();
   if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
-  bfv_kernel<MODE, ONE><<<grid, NS * bfv_wps(a.K) * 32, smem, s>>>(a);
+  bfv_kernel<MODE, TT><<<grid, NS * bfv_wps(a.K) * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
 template <int MODE>
 cudaError_t launch_bfv(const BfvArgs& a, cudaStream_t s, int max_ctas) {
-  return a.T == 1 ? launch_bfv_t<MODE, true>(a, s, max_ctas)
-                  : launch_bfv_t<MODE, false>(a, s, max_ctas);
+  return a.T == 1   ? launch_bfv_t<MODE, 1>(a, s, max_ctas)
+         : a.T <= 2 ? launch_bfv_t<MODE, 2>(a, s, max_ctas)
+         : a.T <= 4 ? launch_bfv_t<MODE, 4>(a, s, max_ctas)
+                    : launch_bfv_t<MODE, 8>(a, s, max_ctas);
 }
 
 // xn = RNE_bf16(x / sqrt(mean(x^2) + eps)); one block per token.
@@ -53,6 +55,8 @@ __global__ void __launch_bounds__(256)
 rmsnorm_kernel(const uint16_t* __restrict__ x, int H, float eps,
                uint16_t* __restrict__ xn) {
   __shared__ float ws[8];
+  pdl_wait();  // x comes from the preceding kernel
+  pdl_launch_dependents();
   const int t = blockIdx.x;
   const uint16_t* xr = x + (size_t)t * H;
   float ss = 0.f;
@@ -88,8 +92,7 @@ cudaError_t launch_shared_down(const uint16_t* down, int H, int K,
 
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps,
                            uint16_t* xn, cudaStream_t s) {
-  rmsnorm_kernel<<<T, 256, 0, s>>>(x, H, eps, xn);
-  return cudaGetLastError();
+  return launch_after_previous(rmsnorm_kernel, dim3(T), dim3(256), 0, s, x, H, eps, xn);
 }
 
 }  // namespace dfm

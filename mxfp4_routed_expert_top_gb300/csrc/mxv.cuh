@@ -48,6 +48,9 @@ constexpr int kMaxWarps = 16;
 // tile still spreads over several warps and a slot keeps a deep ring.
 constexpr int kCGGateUp = 8, kCGDown = 4;
 __host__ __device__ constexpr int mxv_cg(int mode) { return mode == 0 ? kCGGateUp : kCGDown; }
+// 16-row tiles per pipeline unit (one copy, one reduction): down's tiles are a
+// quarter to a fifth of gate/up's, so it takes them in pairs.
+__host__ __device__ constexpr int mxv_unit(int mode) { return mode == 0 ? 1 : 2; }
 
 // Consumer chunks of a K-long row and the groups of chunk c.
 __host__ __device__ inline int mxv_nchunks(int K, int cg) { return (K + 64 * cg - 1) / (64 * cg); }
@@ -57,7 +60,7 @@ __host__ __device__ inline int mxv_nv(int K, int c, int cg) {
 }
 constexpr int kMaxStages = 8;
 constexpr int kRedRing = 4;  // epilogue reduction ring depth
-constexpr size_t kSmemBudget = 200 * 1024;
+constexpr size_t kSmemBudget = 214 * 1024;
 
 struct MxvArgs {
   const uint8_t* arena;
@@ -80,11 +83,11 @@ struct SlotGeom {
   size_t stage_bytes, red_bytes, bytes;
 };
 
-__host__ __device__ inline SlotGeom slot_geom(int K, int NS, int cg) {
+__host__ __device__ inline SlotGeom slot_geom(int K, int NS, int cg, int u) {
   SlotGeom g;
   const int NCH = mxv_nchunks(K, cg);
-  g.stage_bytes = mx_tile_bytes(K);
-  g.red_bytes = (size_t)kRedRing * NCH * 32 * 16;
+  g.stage_bytes = (size_t)u * mx_tile_bytes(K);
+  g.red_bytes = (size_t)kRedRing * NCH * u * 32 * 16;
   const size_t fixed = g.red_bytes;
   const size_t per_slot = kSmemBudget / NS;
   int st = (int)((per_slot > fixed ? per_slot - fixed : 0) / g.stage_bytes);
@@ -111,9 +114,9 @@ constexpr int kMxvBarsPerSlot = 2 * kMaxStages + 2 * kRedRing;
 constexpr int kMxvBars = kMaxWarps / 2 * kMxvBarsPerSlot;  // at most 8 slots
 
 // Dynamic shared memory of one CTA for contraction length K.
-__host__ __device__ inline size_t mxv_smem_bytes(int K, int cg) {
+__host__ __device__ inline size_t mxv_smem_bytes(int K, int cg, int u) {
   const int NS = slots_per_cta(K, cg);
-  return (size_t)NS * slot_geom(K, NS, cg).bytes;
+  return (size_t)NS * slot_geom(K, NS, cg, u).bytes;
 }
 
 // MODE 0: gate/up (K = H, 8 tokens per group), MODE 1: down (K = I, 4 tokens
@@ -129,7 +132,7 @@ __device__ __forceinline__ void mxv_set_up_barriers(const MxvArgs& a, uint64_t* 
   const int NS = slots_per_cta(K, CG);
   const int s = warp / wps, role = warp - s * wps;
   if (s < NS && role == NCH && lane == 0) {
-    const int S = slot_geom(K, NS, CG).stages;
+    const int S = slot_geom(K, NS, CG, mxv_unit(MODE)).stages;
     uint64_t* full = bars + (size_t)s * kMxvBarsPerSlot;
     uint64_t* empty = full + kMaxStages;
     uint64_t* rfull = empty + kMaxStages;
@@ -157,6 +160,7 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
                                         int cta, int ncta, bool set_up = true) {
   constexpr int GT = MODE == 0 ? 8 : 4;  // tokens per group
   constexpr int CG = mxv_cg(MODE);
+  constexpr int U = mxv_unit(MODE);
   const int K = MODE == 0 ? a.H : a.I;
   const int NCH = mxv_nchunks(K, CG);
   const bool own_reducer = mxv_own_reducer(K, CG);
@@ -164,7 +168,7 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = slots_per_cta(K, CG);
   const int s = warp / wps, role = warp - s * wps;
-  const SlotGeom geo = slot_geom(K, NS, CG);
+  const SlotGeom geo = slot_geom(K, NS, CG, U);
   const int S = geo.stages;
   uint8_t* base = smem + (size_t)s * geo.bytes;
   uint8_t* ring = base;
@@ -194,7 +198,7 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
   pdl_launch_dependents();
   if (s >= NS) return;
   const SpanLayout L = span_layout(a.H, a.I);
-  const int tpi = MODE == 0 ? (2 * a.I) / 16 : a.H / 16;  // tiles per item
+  const int tpi = (MODE == 0 ? (2 * a.I) / 16 : a.H / 16) / U;  // units per item
   const int ntiles = (early ? __ldcg(a.n_items) : *a.n_items) * tpi;
   const long long nslots = (long long)ncta * NS;
   const long long gs = (long long)cta * NS + s;
@@ -202,6 +206,7 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
   const int t_end = (int)(ntiles * (gs + 1) / nslots);
   const size_t sec_off = MODE == 0 ? L.gu : L.dn;
   const uint32_t tile_bytes = (uint32_t)mx_tile_bytes(K);
+  const uint32_t unit_bytes = U * tile_bytes;
 
   if (role == NCH) {
     // ---------------- producer: one elected lane ----------------
@@ -221,8 +226,8 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
         }
         if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
         uint8_t* dst = ring + (size_t)stage * geo.stage_bytes;
-        mbar_arrive_expect_tx(&full[stage], tile_bytes);
-        bulk_g2s(dst, span + sec_off + (size_t)j * tile_bytes, tile_bytes,
+        mbar_arrive_expect_tx(&full[stage], unit_bytes);
+        bulk_g2s(dst, span + sec_off + (size_t)j * unit_bytes, unit_bytes,
                  &full[stage], pol);
         ++issued;
         if (++stage == (uint32_t)S) { stage = 0; phase ^= 1; }
@@ -274,7 +279,9 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
     const uint8_t* tile = ring + (size_t)stage * geo.stage_bytes;
 
     for (int grp = 0; grp < it.cnt && ok; grp += GT) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc[U][4];
+#pragma unroll
+      for (int st = 0; st < U; ++st) acc[st][0] = acc[st][1] = acc[st][2] = acc[st][3] = 0.f;
       if (!reducer) {
         // ---- B fragments of this token group (reloaded only when they change)
         if (item != loaded_grp >> 16 || grp != (loaded_grp & 0xFFFF)) {
@@ -347,41 +354,47 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
           loaded_grp = (item << 16) | grp;
         }
 
-        // ---- the tile (16 rows x this chunk) against the group
+        // ---- the unit's tiles (16 rows x this chunk each) against the group
         const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-  #pragma unroll
-        for (int v = 0; v < CG; ++v) {
-          if (v < nv) {
-            const uint8_t* grp_p = tile + kGroupBytes * (CG * c + v);
-            const uint4 q = lds128(grp_p + 16 * lane);
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-            // scales: (row g, block 0), (row g, block 1), (row g+8, 0), (row g+8, 1)
-            const uint32_t sc = lds_u32(grp_p + 512 + 4 * g);
-  #pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {  // the two 32-column blocks of v
-              uint32_t a0[4], a1[4];
-              decode_word(w[2 * hb], a0);
-              decode_word(w[2 * hb + 1], a1);
-              float d[4];
-              mma16816(d, a0, bx[4 * v + 2 * hb][0], bx[4 * v + 2 * hb][1], zero);
-              mma16816(d, a1, bx[4 * v + 2 * hb + 1][0], bx[4 * v + 2 * hb + 1][1], d);
-              const float sg = __uint_as_float(((sc >> (8 * hb)) & 0xFFu) << 23);
-              const float sg8 = __uint_as_float(((sc >> (16 + 8 * hb)) & 0xFFu) << 23);
-              acc[0] = fmaf(d[0], sg, acc[0]);
-              acc[1] = fmaf(d[1], sg, acc[1]);
-              acc[2] = fmaf(d[2], sg8, acc[2]);
-              acc[3] = fmaf(d[3], sg8, acc[3]);
+#pragma unroll
+        for (int st = 0; st < U; ++st) {
+#pragma unroll
+          for (int v = 0; v < CG; ++v) {
+            if (v < nv) {
+              const uint8_t* grp_p = tile + st * tile_bytes + kGroupBytes * (CG * c + v);
+              const uint4 q = lds128(grp_p + 16 * lane);
+              const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+              // scales: (row g, block 0), (row g, block 1), (row g+8, 0), (row g+8, 1)
+              const uint32_t sc = lds_u32(grp_p + 512 + 4 * g);
+#pragma unroll
+              for (int hb = 0; hb < 2; ++hb) {  // the two 32-column blocks of v
+                uint32_t a0[4], a1[4];
+                decode_word(w[2 * hb], a0);
+                decode_word(w[2 * hb + 1], a1);
+                float d[4];
+                mma16816(d, a0, bx[4 * v + 2 * hb][0], bx[4 * v + 2 * hb][1], zero);
+                mma16816(d, a1, bx[4 * v + 2 * hb + 1][0], bx[4 * v + 2 * hb + 1][1], d);
+                const float sg = __uint_as_float(((sc >> (8 * hb)) & 0xFFu) << 23);
+                const float sg8 = __uint_as_float(((sc >> (16 + 8 * hb)) & 0xFFu) << 23);
+                acc[st][0] = fmaf(d[0], sg, acc[st][0]);
+                acc[st][1] = fmaf(d[1], sg, acc[st][1]);
+                acc[st][2] = fmaf(d[2], sg8, acc[st][2]);
+                acc[st][3] = fmaf(d[3], sg8, acc[st][3]);
+              }
             }
           }
         }
-        if (grp + GT >= it.cnt) {  // last use of this tile: release the stage
+        if (grp + GT >= it.cnt) {  // last use of this unit: release the stage
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[stage]);
         }
         if (MODE == 1) {
           // y rows g, g+8 of token t4 = (hi + lo) * 2^s
-          acc[0] = (acc[0] + acc[1]) * csc;
-          acc[2] = (acc[2] + acc[3]) * csc;
+#pragma unroll
+          for (int st = 0; st < U; ++st) {
+            acc[st][0] = (acc[st][0] + acc[st][1]) * csc;
+            acc[st][2] = (acc[st][2] + acc[st][3]) * csc;
+          }
         }
       }
 
@@ -390,31 +403,37 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
       // where the CTA has one to spare, else the chunk warps in turn) sums
       // the entry in chunk order, writes the rows and frees the entry
       const int r = n_epi % kRedRing, u = n_epi / kRedRing;
-      float4* rb = reinterpret_cast<float4*>(red) + (size_t)r * NCH * 32;
+      float4* rb = reinterpret_cast<float4*>(red) + (size_t)r * NCH * U * 32;  // [c][st][lane]
       if (!reducer) {
         if (u >= 1 && !mbar_wait(&rempty[r], (u - 1) & 1)) { ok = false; break; }
-        rb[c * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+#pragma unroll
+        for (int st = 0; st < U; ++st)
+          rb[(c * U + st) * 32 + lane] = make_float4(acc[st][0], acc[st][1], acc[st][2], acc[st][3]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&rfull[r]);
       }
       if (reducer || (!own_reducer && c == n_epi % NCH)) {
         if (!mbar_wait(&rfull[r], u & 1)) { ok = false; break; }
-        float4 sum = rb[lane];
-        for (int cc = 1; cc < NCH; ++cc) {
-          const float4 v4 = rb[cc * 32 + lane];
-          sum.x += v4.x; sum.y += v4.y; sum.z += v4.z; sum.w += v4.w;
-        }
-        if (MODE == 0) {
-          // columns 2t4, 2t4+1 = tokens grp+2t4, grp+2t4+1; rows g (gate) and
-          // g+8 (up) of intermediate index 8j + g
-          const int a0i = assignment(grp + 2 * t4), a1i = assignment(grp + 2 * t4 + 1);
-          if (a0i >= 0) a.out[(size_t)a0i * a.I + 8 * j + g] = silu_f(sum.x) * sum.z;
-          if (a1i >= 0) a.out[(size_t)a1i * a.I + 8 * j + g] = silu_f(sum.y) * sum.w;
-        } else {
-          const int ai = assignment(grp + t4);
-          if (ai >= 0) {
-            a.out[(size_t)ai * a.H + 16 * j + g] = sum.x;
-            a.out[(size_t)ai * a.H + 16 * j + g + 8] = sum.z;
+#pragma unroll
+        for (int st = 0; st < U; ++st) {
+          float4 sum = rb[st * 32 + lane];
+          for (int cc = 1; cc < NCH; ++cc) {
+            const float4 v4 = rb[(cc * U + st) * 32 + lane];
+            sum.x += v4.x; sum.y += v4.y; sum.z += v4.z; sum.w += v4.w;
+          }
+          const int tl = U * j + st;  // tile of the item
+          if (MODE == 0) {
+            // columns 2t4, 2t4+1 = tokens grp+2t4, grp+2t4+1; rows g (gate)
+            // and g+8 (up) of intermediate index 8 tl + g
+            const int a0i = assignment(grp + 2 * t4), a1i = assignment(grp + 2 * t4 + 1);
+            if (a0i >= 0) a.out[(size_t)a0i * a.I + 8 * tl + g] = silu_f(sum.x) * sum.z;
+            if (a1i >= 0) a.out[(size_t)a1i * a.I + 8 * tl + g] = silu_f(sum.y) * sum.w;
+          } else {
+            const int ai = assignment(grp + t4);
+            if (ai >= 0) {
+              a.out[(size_t)ai * a.H + 16 * tl + g] = sum.x;
+              a.out[(size_t)ai * a.H + 16 * tl + g + 8] = sum.z;
+            }
           }
         }
         __syncwarp();

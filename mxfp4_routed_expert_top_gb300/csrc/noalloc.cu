@@ -62,6 +62,7 @@ extern "C" DF_MOE_API int df_moe_route_noalloc(const float* router, int32_t E,
                                                float* weights, void* stream) {
   if (!router || !x_bf16 || !ids || !weights)
     return fail(DF_MOE_EINVAL, "router, x, ids and weights are required");
+  if ((uintptr_t)x_bf16 & 15) return fail(DF_MOE_EINVAL, "x must be 16-byte aligned");
   if (H <= 0 || H % 32 || H > 8192)
     return fail(DF_MOE_EINVAL, "H must be a multiple of 32 in [32, 8192]");
   if (E < 1 || E > 1024) return fail(DF_MOE_EINVAL, "E must be in [1, 1024]");
