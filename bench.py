@@ -54,6 +54,10 @@ def parse():
                         "workload decodes at batch 1 and batch 4)")
     p.add_argument("--fused", action="store_true",
                    help="decode batches as one fused layer launch (DF_MOE_FUSED_DECODE)")
+    p.add_argument("--graph", action="store_true",
+                   help="replay the forward pass as one CUDA graph (df_moe_graph_*); each "
+                        "step's token is copied into the graph's input buffer before the "
+                        "step's timed region, with the L2 flush")
     p.add_argument("--mma-sync-prefill", action="store_true",
                    help="batches above 8 tokens on the register-fragment expert kernels "
                         "instead of the tcgen05 GEMMs (DF_MOE_PREFILL_MMA_SYNC)")
@@ -304,10 +308,28 @@ def run_ours(args):
     w = torch.empty((wl.L, T, wl.k), dtype=torch.float32, device="cuda")
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
 
-    def step(i):
-        m.forward(xs[i % TOKEN_POOL], T, out, ids, w, stream=stream)
+    graph = None
+    if args.graph:
+        x_cur = xs[0].clone()
+        graph = m.graph(x_cur, T, out, ids, w)
+
+        def stage(i):  # outside the timed region, beside the flush
+            x_cur.copy_(xs[i % TOKEN_POOL])
+
+        def step(i):
+            graph.launch(stream=stream)
+    else:
+        def stage(i):
+            pass
+
+        def step(i):
+            m.forward(xs[i % TOKEN_POOL], T, out, ids, w, stream=stream)
+
+    def launches_of_step():
+        return graph.launch_count() if graph is not None else m.last_launch_count()
 
     for i in range(args.warmup):
+        stage(i)
         flush.fill_(float(i))
         step(i)
     m.sync(stream)
@@ -322,11 +344,12 @@ def run_ours(args):
         torch.cuda.synchronize()
         wall0 = time.perf_counter()
         for i in range(args.steps):
+            stage(i)
             flush.fill_(float(i))
             starts[i].record(stream)
             step(i)
             ends[i].record(stream)
-            launches += m.last_launch_count()
+            launches += launches_of_step()
         torch.cuda.synchronize()
         barrier(dist)
         wall = time.perf_counter() - wall0
@@ -344,9 +367,25 @@ def run_ours(args):
     m.timing_enable(True)
     for i in range(min(args.steps, 50)):
         flush.fill_(float(i))
-        step(i)
+        m.forward(xs[i % TOKEN_POOL], T, out, ids, w, stream=stream)
     kt = m.timing()
     m.timing_enable(False)
+
+    # the read-only streaming rate of this GPU (our probe kernel over 1 GiB)
+    probe = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+    sink = torch.empty(8 * torch.cuda.get_device_properties(local).multi_processor_count * 256,
+                       dtype=torch.int32, device="cuda")
+    probe_ms = []
+    for i in range(8):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dfm.stream_read(probe, probe.numel(), sink, stream=stream)
+        b.record(stream)
+        b.synchronize()
+        if i >= 3:
+            probe_ms.append(a.elapsed_time(b))
+    stream_read_gbs = probe.numel() / (float(np.median(probe_ms)) / 1e3) / 1e9
+    del probe, sink
 
     # end to end through the public API with host buffers (pinned)
     hx = torch.from_numpy(pool.view(np.int16)).pin_memory()
@@ -367,6 +406,8 @@ def run_ours(args):
     dev_s_max, tokens = aggregate_over_ranks(dist, dev_s, T * args.steps, device="cuda")
     e2e_max, e2e_tokens = aggregate_over_ranks(dist, e2e_s, T * e2e_steps, device="cuda")
     if rank != 0:
+        if graph is not None:
+            graph.close()
         m.close()
         return None
 
@@ -400,10 +441,16 @@ def run_ours(args):
                    "layers": wl.L, "weights": "mxfp4 e2m1+e8m0/32, shared bf16",
                    "l2": "flushed (256 MiB write) before every timed step",
                    "decode_path": "fused" if args.fused else "chain",
+                   "launch": "cuda graph" if args.graph else "stream",
                    "prefill_path": "mma_sync" if args.mma_sync_prefill else "tcgen05",
                    "parallelism": "replicas" if ws > 1 else "single-gpu"},
+        "step_us": {"median": round(float(np.median(step_ms)) * 1e3, 2),
+                    "p10": round(float(np.percentile(step_ms, 10)) * 1e3, 2),
+                    "p90": round(float(np.percentile(step_ms, 90)) * 1e3, 2)},
         "layer_hbm": {"achieved_gbs": round(layer_gbs, 1), "bytes_per_step": int(lb),
                       "frac_of_measured": round(layer_gbs / peak, 4),
+                      "stream_read_gbs": round(stream_read_gbs, 1),
+                      "frac_of_stream_read": round(layer_gbs / stream_read_gbs, 4),
                       "frac_of_nominal_8tbs": round(layer_gbs / 8000.0, 4),
                       "distinct_experts_per_step": u_mean},
         "roofline": {"bound": "hbm", "kernel": dom,
@@ -420,6 +467,8 @@ def run_ours(args):
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 4),
     }
+    if graph is not None:
+        graph.close()
     m.close()
     return res
 

@@ -176,6 +176,35 @@ DF_MOE_API int df_moe_forward_host(df_moe* h, const uint16_t* x_bf16, int32_t T,
 /* Synchronises `stream` and reports any device-side error word. */
 DF_MOE_API int df_moe_sync(df_moe* h, void* stream);
 
+/* ---- CUDA graphs -----------------------------------------------------------
+ * A forward pass captured once into a CUDA graph and replayed: one launch a
+ * step instead of one per kernel, the programmatic dependencies between the
+ * kernels kept as graph edges. The graph is bound to the buffers given here;
+ * between launches the caller changes the CONTENTS of x (and residual), not
+ * the pointers. Arguments as df_moe_forward; the capture runs on a stream of
+ * the handle's own, so `stream` may be any stream (the legacy default one
+ * included) and nothing is enqueued on it.
+ * Not with DF_MOE_FUSED_DECODE (the layer kernel's flags need a fresh epoch
+ * each call: EINVAL) nor with timing on (EINVAL). The graph holds no
+ * reference to the handle's host state: destroy it before the handle. */
+typedef struct df_moe_graph df_moe_graph; /* opaque */
+DF_MOE_API int df_moe_graph_create(df_moe* h, const void* x_bf16, int32_t T,
+                                   const void* residual_bf16, void* out_bf16, float* out_f32,
+                                   int32_t* ids, float* weights, df_moe_graph** out);
+/* Enqueues one replay on `stream`. Errors: EINVAL (null graph), ECUDA. */
+DF_MOE_API int df_moe_graph_launch(df_moe_graph* g, void* stream);
+/* Kernel launches in one replay. */
+DF_MOE_API int df_moe_graph_launch_count(const df_moe_graph* g);
+/* NULL-safe. */
+DF_MOE_API void df_moe_graph_destroy(df_moe_graph* g);
+
+/* ---- read bandwidth probe --------------------------------------------------
+ * Streams `bytes` (a multiple of 16, buf 16-byte aligned) of device memory
+ * with 16-byte loads into one word per thread of `sink` (device, at least
+ * 152 * 8 * 256 words): the read-only streaming rate the layer's kernels are
+ * measured against beside the copy peak. Errors: EINVAL, ECUDA. */
+DF_MOE_API int df_moe_stream_read(const void* buf, size_t bytes, uint32_t* sink, void* stream);
+
 /* ---- single steps (the rows of the hot path, for per-step checks) ---------
  * Each runs one step of the forward on its own, with the same kernels. */
 

@@ -2,4 +2,4 @@
 (libdfmoe.so, include/df_moe.h) and its thin Python binding."""
 from .binding import (MoE, DfMoeError, Config, LayerWeights, lib, span_bytes_for,  # noqa: F401
                       STACK_RMSNORM_RESIDUAL, FUSED_DECODE, PREFILL_MMA_SYNC, SYMBOLS,
-                      route_noalloc)
+                      route_noalloc, Graph, stream_read)

@@ -27,6 +27,8 @@ SYMBOLS = [
     "df_moe_step_shared", "df_moe_step_rmsnorm", "df_moe_read_expert_span",
     "df_moe_timing_enable", "df_moe_timing_reset", "df_moe_timing_get",
     "df_moe_last_launch_count", "df_moe_route_noalloc",
+    "df_moe_graph_create", "df_moe_graph_launch", "df_moe_graph_launch_count",
+    "df_moe_graph_destroy", "df_moe_stream_read",
 ]
 
 
@@ -90,6 +92,12 @@ def lib():
                                         ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]
         L.df_moe_last_launch_count.argtypes = [vp]
         L.df_moe_route_noalloc.argtypes = [vp, i32, i32, vp, i32, i32, vp, vp, vp]
+        L.df_moe_graph_create.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp,
+                                          ctypes.POINTER(ctypes.c_void_p)]
+        L.df_moe_graph_launch.argtypes = [vp, vp]
+        L.df_moe_graph_launch_count.argtypes = [vp]
+        L.df_moe_graph_destroy.argtypes = [vp]; L.df_moe_graph_destroy.restype = None
+        L.df_moe_stream_read.argtypes = [vp, ctypes.c_size_t, vp, vp]
         for name in SYMBOLS:
             f = getattr(L, name)
             if f.restype is ctypes.c_int:  # default
@@ -265,3 +273,43 @@ class MoE:
 
     def last_launch_count(self):
         return lib().df_moe_last_launch_count(self.h)
+
+    def graph(self, x, T, out, ids, weights, residual=None, out_f32=None):
+        """A forward pass captured into a CUDA graph (df_moe_graph_create),
+        bound to these buffers: replay with Graph.launch after changing the
+        contents of x."""
+        g = ctypes.c_void_p()
+        self._check(lib().df_moe_graph_create(self.h, _ptr(x), T, _ptr(residual), _ptr(out),
+                                              _ptr(out_f32), _ptr(ids), _ptr(weights),
+                                              ctypes.byref(g)))
+        return Graph(g)
+
+
+class Graph:
+    """Owns one df_moe_graph."""
+
+    def __init__(self, g):
+        self.g = g
+
+    def launch(self, stream=None):
+        rc = lib().df_moe_graph_launch(self.g, _stream(stream))
+        if rc != OK:
+            raise DfMoeError(rc, lib().df_moe_last_error(None).decode())
+
+    def launch_count(self):
+        return lib().df_moe_graph_launch_count(self.g)
+
+    def close(self):
+        if self.g:
+            lib().df_moe_graph_destroy(self.g)
+            self.g = None
+
+    def __del__(self):
+        self.close()
+
+
+def stream_read(buf, nbytes, sink, stream=None):
+    """Read-only streaming probe over nbytes of device memory (df_moe_stream_read)."""
+    rc = lib().df_moe_stream_read(_ptr(buf), nbytes, _ptr(sink), _stream(stream))
+    if rc != OK:
+        raise DfMoeError(rc, lib().df_moe_last_error(None).decode())

@@ -98,6 +98,7 @@ struct df_moe {
   ChunkMap bmap_gu{}, bmap_dn{};
   bool phase = false;  // decode batches run the two phase kernels
   int sms = 0;
+  cudaStream_t cap_stream = nullptr;  // CUDA-graph captures run on it
   // host-API device buffers
   uint16_t* hx = nullptr;
   uint16_t* hres = nullptr;
@@ -458,6 +459,7 @@ void df_moe_destroy(df_moe* h) {
   int prev = 0;
   cudaGetDevice(&prev);
   cudaSetDevice(h->device);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   for (auto& p : h->pending) {
     cudaEventDestroy(p.a);
     cudaEventDestroy(p.b);
@@ -1015,6 +1017,83 @@ int df_moe_timing_get(df_moe* h, int kind, const char** name, int64_t* launches,
 }
 
 int df_moe_last_launch_count(const df_moe* h) { return h ? h->launches : 0; }
+
+// ---- CUDA graphs ----------------------------------------------------------
+
+struct df_moe_graph {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int device = 0;
+  int launches = 0;
+};
+
+int df_moe_graph_create(df_moe* h, const void* x_bf16, int32_t T, const void* residual_bf16,
+                        void* out_bf16, float* out_f32, int32_t* ids, float* weights,
+                        df_moe_graph** out) {
+  if (!h || !out) return fail(h, DF_MOE_EINVAL, "null handle or output");
+  *out = nullptr;
+  if (h->cfg.flags & DF_MOE_FUSED_DECODE)
+    return fail(h, DF_MOE_EINVAL, "graphs need the kernel chain (no DF_MOE_FUSED_DECODE)");
+  if (h->timing) return fail(h, DF_MOE_EINVAL, "turn timing off before capturing a graph");
+  CUDA_OR_FAIL(h, cudaSetDevice(h->device));
+  if (!h->cap_stream)
+    CUDA_OR_FAIL(h, cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
+  CUDA_OR_FAIL(h, cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
+  const int rc = forward_impl(h, x_bf16, T, residual_bf16, out_bf16, out_f32, ids, weights,
+                              nullptr, nullptr, h->cap_stream);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(h->cap_stream, &graph);
+  if (rc) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  if (ec != cudaSuccess)
+    return fail(h, DF_MOE_ECUDA, "graph capture failed: %s", cudaGetErrorString(ec));
+  cudaGraphExec_t exec = nullptr;
+  const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
+  if (ei != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    return fail(h, DF_MOE_ECUDA, "graph instantiation failed: %s", cudaGetErrorString(ei));
+  }
+  df_moe_graph* g = new df_moe_graph;
+  g->graph = graph;
+  g->exec = exec;
+  g->device = h->device;
+  g->launches = h->launches;
+  *out = g;
+  return DF_MOE_OK;
+}
+
+int df_moe_graph_launch(df_moe_graph* g, void* stream) {
+  if (!g) return fail(nullptr, DF_MOE_EINVAL, "null graph");
+  cudaError_t e = cudaSetDevice(g->device);
+  if (e == cudaSuccess) e = cudaGraphLaunch(g->exec, (cudaStream_t)stream);
+  if (e != cudaSuccess)
+    return fail(nullptr, DF_MOE_ECUDA, "graph launch failed: %s", cudaGetErrorString(e));
+  return DF_MOE_OK;
+}
+
+int df_moe_graph_launch_count(const df_moe_graph* g) { return g ? g->launches : 0; }
+
+void df_moe_graph_destroy(df_moe_graph* g) {
+  if (!g) return;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(g->device);
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  cudaSetDevice(prev);
+  delete g;
+}
+
+int df_moe_stream_read(const void* buf, size_t bytes, uint32_t* sink, void* stream) {
+  if (!buf || !sink || (bytes & 15) || ((uintptr_t)buf & 15))
+    return fail(nullptr, DF_MOE_EINVAL, "buf must be 16-byte aligned, bytes a multiple of 16");
+  const cudaError_t e = launch_stream_read(buf, bytes, sink, (cudaStream_t)stream);
+  if (e != cudaSuccess)
+    return fail(nullptr, DF_MOE_ECUDA, "read probe launch failed: %s", cudaGetErrorString(e));
+  return DF_MOE_OK;
+}
 
 }  // extern "C"
 

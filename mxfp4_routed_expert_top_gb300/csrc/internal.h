@@ -174,6 +174,9 @@ cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps,
 // (0: no shared experts). n_sh: CTAs (of one per SM) that run the shared
 // experts, in [1, SMs - 1] (0 when R = 0); the others run the routed ones.
 bool phase_supported(int H, int I, int R, int E, int k);
+// Read-only streaming probe: 16-byte loads over `bytes`, one word a thread
+// into sink (at least 8 * SMs * 256 words).
+cudaError_t launch_stream_read(const void* buf, size_t bytes, uint32_t* sink, cudaStream_t s);
 cudaError_t launch_phase_gateup(const uint16_t* sh_gate, const uint16_t* sh_up, int R,
                                 const uint8_t* arena, size_t span_bytes, int H, int I, int k,
                                 const uint16_t* x, int T, Item* items, int32_t* n_items,

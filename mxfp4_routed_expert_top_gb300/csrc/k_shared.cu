@@ -76,7 +76,38 @@ rmsnorm_kernel(const uint16_t* __restrict__ x, int H, float eps,
   }
 }
 
+// Read-only streaming probe: each thread keeps 16 loads of 16 bytes in flight
+// (non-coherent path, no L1 allocation) and folds them into one word.
+__global__ void __launch_bounds__(256) stream_read_kernel(const uint4* __restrict__ p, size_t n16,
+                                                          uint32_t* __restrict__ sink) {
+  constexpr int U = 16;
+  uint32_t acc = 0;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + (U - 1) * stride < n16; i += U * stride) {
+    uint32_t v[U][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(v[u][0]), "=r"(v[u][1]), "=r"(v[u][2]), "=r"(v[u][3])
+                   : "l"(p + i + u * stride));
+#pragma unroll
+    for (int u = 0; u < U; ++u) acc ^= v[u][0] ^ v[u][1] ^ v[u][2] ^ v[u][3];
+  }
+  for (; i < n16; i += stride) {
+    const uint4 v = p[i];
+    acc ^= v.x ^ v.y ^ v.z ^ v.w;
+  }
+  sink[(size_t)blockIdx.x * blockDim.x + threadIdx.x] = acc;
+}
+
 }  // namespace
+
+cudaError_t launch_stream_read(const void* buf, size_t bytes, uint32_t* sink, cudaStream_t s) {
+  stream_read_kernel<<<4 * num_sms_b(), 256, 0, s>>>(static_cast<const uint4*>(buf), bytes / 16,
+                                                      sink);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_shared_gateup(const uint16_t* gate, const uint16_t* up,
                                  int R, int H, const uint16_t* x, int T,

@@ -211,3 +211,58 @@ def test_verify_pass_t2(k3, torch):
     assert shared >= 2, "the drafted position shares %d experts" % shared
     check_ids_weights(ids, w, ref["ids"], ref["w"])
     check_out(out32, ref["out"])
+
+
+def test_graph_replay_matches_eager(k3, torch):
+    """df_moe_graph_*: a forward pass captured once and replayed on new
+    contents of its input buffer gives, bit for bit, the eager call's
+    results (the same kernels), and the oracle's routing."""
+    import mxfp4_routed_expert_top_gb300 as dfm
+    x = _tokens(k3, WL1, 3, first_id=1300)
+    x_buf = torch.empty((1, WL1.H), dtype=torch.int16, device="cuda")
+    out = torch.empty((1, WL1.H), dtype=torch.int16, device="cuda")
+    out32 = torch.empty((1, WL1.H), dtype=torch.float32, device="cuda")
+    ids = torch.empty((1, WL1.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((1, WL1.k), dtype=torch.float32, device="cuda")
+    if k3.fused:
+        with pytest.raises(dfm.DfMoeError):
+            k3.m.graph(x_buf, 1, out, ids, w, out_f32=out32)
+        return
+    g = k3.m.graph(x_buf, 1, out, ids, w, out_f32=out32)
+    try:
+        assert g.launch_count() >= 3
+        for t in range(3):
+            x_buf.copy_(to_dev_bf16(x[t:t + 1]))
+            g.launch()
+            torch.cuda.synchronize()
+            got = (out.cpu().numpy().copy(), out32.cpu().numpy().copy(), ids.cpu().numpy().copy(),
+                   w.cpu().numpy().copy())
+            e_out, e_out32, e_ids, e_w = _forward(k3.m, x[t:t + 1], 1, torch)
+            assert np.array_equal(got[0].view(np.uint16), e_out)
+            assert np.array_equal(got[1], e_out32.astype(np.float32))
+            assert np.array_equal(got[2], e_ids)
+            assert np.array_equal(got[3], e_w.astype(np.float32))
+            rid, rw = orc.topk_softmax(orc.router_logits(k3.routers[0], x[t:t + 1]), WL1.k)
+            check_ids_weights(got[2], got[3].astype(np.float64), rid, rw)
+    finally:
+        g.close()
+
+
+def test_stream_read_probe(torch):
+    """df_moe_stream_read reads every 16-byte word exactly once: the XOR of
+    its per-thread words is the XOR of the buffer's words."""
+    import mxfp4_routed_expert_top_gb300 as dfm
+    n = (64 << 20) + 48  # not a multiple of the grid's stride
+    buf = torch.zeros(n // 4, dtype=torch.int32, device="cuda")
+    buf[12345] = 0x1234567
+    buf[n // 4 - 1] = 0x70000001
+    sink = torch.empty(8 * torch.cuda.get_device_properties(0).multi_processor_count * 256,
+                       dtype=torch.int32, device="cuda")
+    dfm.stream_read(buf, n, sink)
+    torch.cuda.synchronize()
+    # the probe writes 4 * SMs * 256 words; the rest of sink is never read
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    folded = np.bitwise_xor.reduce(sink.cpu().numpy().view(np.uint32)[:4 * nsm * 256])
+    assert folded == (0x1234567 ^ 0x70000001)
+    with pytest.raises(dfm.DfMoeError):
+        dfm.stream_read(buf, n - 4, sink)
