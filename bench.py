@@ -61,6 +61,13 @@ def parse():
     p.add_argument("--mma-sync-prefill", action="store_true",
                    help="batches above 8 tokens on the register-fragment expert kernels "
                         "instead of the tcgen05 GEMMs (DF_MOE_PREFILL_MMA_SYNC)")
+    p.add_argument("--cache-slots", type=int, default=0,
+                   help="experts in pinned host memory, this many a layer cached in HBM "
+                        "(df_moe_create_cached); decode batches only")
+    p.add_argument("--token-corr", type=float, default=0.0,
+                   help="consecutive steps take consecutive tokens of a stream whose "
+                        "neighbours have this correlation (0.7: ~31%% of the experts "
+                        "reused from the previous token); 0: independent tokens")
     p.add_argument("--experts", type=int, default=0,
                    help="profiling aid: override the routed-expert count (same "
                         "per-token work, smaller resident set); not a bench line")
@@ -294,14 +301,25 @@ def run_ours(args):
     T = wl.T
     flags = ((dfm.STACK_RMSNORM_RESIDUAL if wl.stack else 0) | (dfm.FUSED_DECODE if args.fused else 0)
              | (dfm.PREFILL_MMA_SYNC if args.mma_sync_prefill else 0))
+    if args.cache_slots and T > 8:
+        raise SystemExit("--cache-slots serves decode batches (<= 8 tokens)")
     m = dfm.MoE(wl.H, wl.E, wl.k, wl.I, wl.n_shared, wl.Is, n_layers=wl.L,
-                max_tokens=max(T, 4), rms_eps=wl.eps, flags=flags, device=local)
+                max_tokens=T if args.cache_slots else max(T, 4), rms_eps=wl.eps, flags=flags,
+                device=local, cache_slots=args.cache_slots)
     stream = torch.cuda.current_stream()
     load_workload(m, wl, torch, stream)
 
-    # a pool of distinct synthetic tokens (fresh x each step), resident in HBM
-    pool = np.stack([synth.token(wl.seed, wl.cfg_id, 200000 + rank * 100000 + i, wl.H)
-                     for i in range(TOKEN_POOL * T)]).reshape(TOKEN_POOL, T, wl.H)
+    # a pool of distinct synthetic tokens (fresh x each step), resident in HBM;
+    # a correlated stream runs through the warm-up and the timed steps
+    # without wrapping
+    n_pool = TOKEN_POOL
+    if args.token_corr:
+        n_pool = max(TOKEN_POOL, args.warmup + args.steps)
+        pool = synth.token_stream(wl.seed, wl.cfg_id, 0, n_pool * T, wl.H, args.token_corr,
+                                  stream=1 + rank).reshape(n_pool, T, wl.H)
+    else:
+        pool = np.stack([synth.token(wl.seed, wl.cfg_id, 200000 + rank * 100000 + i, wl.H)
+                         for i in range(n_pool * T)]).reshape(n_pool, T, wl.H)
     xs = torch.from_numpy(pool.view(np.int16)).cuda()
     out = torch.empty((T, wl.H), dtype=torch.int16, device="cuda")
     ids = torch.empty((wl.L, T, wl.k), dtype=torch.int32, device="cuda")
@@ -314,7 +332,7 @@ def run_ours(args):
         graph = m.graph(x_cur, T, out, ids, w)
 
         def stage(i):  # outside the timed region, beside the flush
-            x_cur.copy_(xs[i % TOKEN_POOL])
+            x_cur.copy_(xs[i % n_pool])
 
         def step(i):
             graph.launch(stream=stream)
@@ -323,7 +341,7 @@ def run_ours(args):
             pass
 
         def step(i):
-            m.forward(xs[i % TOKEN_POOL], T, out, ids, w, stream=stream)
+            m.forward(xs[i % n_pool], T, out, ids, w, stream=stream)
 
     def launches_of_step():
         return graph.launch_count() if graph is not None else m.last_launch_count()
@@ -339,6 +357,7 @@ def run_ours(args):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     n_union = []
     launches = 0
+    cache0 = m.cache_stats()
     with ClockSampler(local) as clk:
         barrier(dist)
         torch.cuda.synchronize()
@@ -354,12 +373,19 @@ def run_ours(args):
         barrier(dist)
         wall = time.perf_counter() - wall0
     m.sync(stream)
+    cache1 = m.cache_stats()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     dev_s = sum(step_ms) / 1e3
-    # distinct experts per step (for the byte count), from the ids of the pool
-    for i in range(min(args.steps, TOKEN_POOL)):
+    # distinct experts per step (for the byte count), from the ids of the
+    # pool; and the share of a step's experts that the step before selected
+    prev, reuse = None, []
+    for i in range(min(args.steps, n_pool)):
         m.forward(xs[i], T, out, ids, w, stream=stream)
-        n_union.append(len(np.unique(ids[0].cpu().numpy())))
+        sel = set(np.unique(ids[0].cpu().numpy()).tolist())
+        n_union.append(len(sel))
+        if prev is not None:
+            reuse.append(len(sel & prev) / len(sel))
+        prev = sel
     u_mean = float(np.mean(n_union))
 
     # per-kernel device time (same steps, library events on the same stream)
@@ -367,7 +393,7 @@ def run_ours(args):
     m.timing_enable(True)
     for i in range(min(args.steps, 50)):
         flush.fill_(float(i))
-        m.forward(xs[i % TOKEN_POOL], T, out, ids, w, stream=stream)
+        m.forward(xs[i % n_pool], T, out, ids, w, stream=stream)
     kt = m.timing()
     m.timing_enable(False)
 
@@ -387,6 +413,41 @@ def run_ours(args):
     stream_read_gbs = probe.numel() / (float(np.median(probe_ms)) / 1e3) / 1e9
     del probe, sink
 
+    cache = None
+    if args.cache_slots:
+        # the ceiling of the cache's copies: pinned host -> HBM copy rate, as
+        # one 1 GiB copy and as 16 expert-span copies (one token's misses)
+        span = m.span_bytes
+        hsrc = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+        ddst = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+
+        def h2d_gbs(nbytes, pieces):
+            t = []
+            for i in range(6):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for j in range(pieces):
+                    ddst[j * nbytes:(j + 1) * nbytes].copy_(hsrc[j * nbytes:(j + 1) * nbytes],
+                                                           non_blocking=True)
+                b.record(stream)
+                b.synchronize()
+                if i >= 2:
+                    t.append(a.elapsed_time(b))
+            return nbytes * pieces / (float(np.median(t)) / 1e3) / 1e9
+
+        copy_gbs, burst_gbs = h2d_gbs(1 << 30, 1), h2d_gbs(span, 16)
+        del hsrc, ddst
+        dh, dm, db = (cache1[i] - cache0[i] for i in range(3))
+        ntok = T * args.steps
+        cache = {"slots_per_layer": args.cache_slots, "hits": dh, "misses": dm,
+                 "hit_rate": round(dh / max(dh + dm, 1), 4),
+                 "bytes_in_per_token": int(round(db / ntok)),
+                 "bytes_in_gbs": round(db / dev_s / 1e9, 1),
+                 "h2d_copy_gbs": round(copy_gbs, 1),
+                 "h2d_16_span_copies_gbs": round(burst_gbs, 1),
+                 "frac_of_h2d_copy": round(db / dev_s / 1e9 / copy_gbs, 4),
+                 "reuse_of_previous_step": round(float(np.mean(reuse)), 4) if reuse else None}
+
     # end to end through the public API with host buffers (pinned)
     hx = torch.from_numpy(pool.view(np.int16)).pin_memory()
     hout = torch.empty((T, wl.H), dtype=torch.int16).pin_memory()
@@ -398,7 +459,7 @@ def run_ours(args):
         flush.fill_(float(i))
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        m.forward_host(hx[i % TOKEN_POOL], T, hout, ids=hids, weights=hw, stream=stream)
+        m.forward_host(hx[i % n_pool], T, hout, ids=hids, weights=hw, stream=stream)
         if i >= 3:
             e2e_t.append(time.perf_counter() - t0)
     e2e_s = sum(e2e_t)
@@ -443,6 +504,10 @@ def run_ours(args):
                    "decode_path": "fused" if args.fused else "chain",
                    "launch": "cuda graph" if args.graph else "stream",
                    "prefill_path": "mma_sync" if args.mma_sync_prefill else "tcgen05",
+                   "experts_home": ("pinned host memory, %d a layer cached in HBM"
+                                    % args.cache_slots) if args.cache_slots else "HBM",
+                   "tokens": ("AR(1) stream, neighbour correlation %g" % args.token_corr)
+                             if args.token_corr else "independent N(0,1)",
                    "parallelism": "replicas" if ws > 1 else "single-gpu"},
         "step_us": {"median": round(float(np.median(step_ms)) * 1e3, 2),
                     "p10": round(float(np.percentile(step_ms, 10)) * 1e3, 2),
@@ -464,6 +529,7 @@ def run_ours(args):
                 "h2d_bytes_per_step": T * wl.H * 2,
                 "d2h_bytes_per_step": T * wl.H * 2 + wl.L * T * wl.k * 8},
         "gpu_launches": launches,
+        **({"cache": cache} if cache else {}),
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 4),
     }

@@ -120,6 +120,25 @@ typedef struct {
  * Errors: EINVAL (bad config), ENOMEM, ECUDA. */
 DF_MOE_API int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out);
 
+/* Expert cache (models larger than HBM): as df_moe_create, but every
+ * layer's experts live in pinned host memory (the Grace side, reached over
+ * NVLink-C2C) and only `cache_slots` of them a layer in HBM. Each forward
+ * layer brings its selection to the host (one synchronisation: forward is
+ * synchronous on its stream), copies the selected experts that are not
+ * cached into free or least recently used slots (one cudaMemcpyAsync each)
+ * and runs the decode kernels on the slots. Consecutive tokens that reuse
+ * experts find them cached (the Deltafin README, "Techniques", and the
+ * kimi-k3-in-c blog's expert LRU cache stream experts from SSD with the same
+ * reuse). Limits: max_tokens <= 8, no DF_MOE_FUSED_DECODE,
+ * min(max_tokens*top_k, n_experts) <= cache_slots <= n_experts; no graphs
+ * and no single expert steps on such a handle. Errors as df_moe_create. */
+DF_MOE_API int df_moe_create_cached(const df_moe_config* cfg, int cuda_device,
+                                    int32_t cache_slots, df_moe** out);
+/* Since creation: selected experts found cached, experts copied in, and the
+ * bytes copied from host to HBM. Zeros for a handle without a cache. */
+DF_MOE_API int df_moe_cache_stats(const df_moe* h, int64_t* hits, int64_t* misses,
+                                  int64_t* bytes_in);
+
 /* Frees everything. NULL-safe. The caller must not have work in flight. */
 DF_MOE_API void df_moe_destroy(df_moe* h);
 
@@ -245,7 +264,7 @@ DF_MOE_API int df_moe_read_expert_span(df_moe* h, int32_t layer, int32_t expert,
  * With timing on, every kernel launch of forward is bracketed by CUDA events
  * on its stream; df_moe_timing_get returns, per kernel kind, the launches and
  * the summed device time since the last reset. */
-#define DF_MOE_KERNEL_KINDS 15
+#define DF_MOE_KERNEL_KINDS 16
 DF_MOE_API int df_moe_timing_enable(df_moe* h, int on);
 DF_MOE_API int df_moe_timing_reset(df_moe* h);
 DF_MOE_API int df_moe_timing_get(df_moe* h, int kind, const char** name,

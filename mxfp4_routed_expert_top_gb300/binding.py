@@ -15,7 +15,7 @@ OK, EINVAL, ENOMEM, ECUDA, ESTATE, ERANGE, ETIMEOUT, EDEVICE = 0, -1, -2, -3, -4
 STACK_RMSNORM_RESIDUAL = 1
 FUSED_DECODE = 2
 PREFILL_MMA_SYNC = 4
-KERNEL_KINDS = 15
+KERNEL_KINDS = 16
 
 # every symbol the header declares (checked by the CPU tests)
 SYMBOLS = [
@@ -28,7 +28,8 @@ SYMBOLS = [
     "df_moe_timing_enable", "df_moe_timing_reset", "df_moe_timing_get",
     "df_moe_last_launch_count", "df_moe_route_noalloc",
     "df_moe_graph_create", "df_moe_graph_launch", "df_moe_graph_launch_count",
-    "df_moe_graph_destroy", "df_moe_stream_read",
+    "df_moe_graph_destroy", "df_moe_stream_read", "df_moe_create_cached",
+    "df_moe_cache_stats",
 ]
 
 
@@ -98,6 +99,10 @@ def lib():
         L.df_moe_graph_launch_count.argtypes = [vp]
         L.df_moe_graph_destroy.argtypes = [vp]; L.df_moe_graph_destroy.restype = None
         L.df_moe_stream_read.argtypes = [vp, ctypes.c_size_t, vp, vp]
+        L.df_moe_create_cached.argtypes = [ctypes.POINTER(Config), ctypes.c_int, i32,
+                                           ctypes.POINTER(ctypes.c_void_p)]
+        L.df_moe_cache_stats.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                         ctypes.POINTER(i64)]
         for name in SYMBOLS:
             f = getattr(L, name)
             if f.restype is ctypes.c_int:  # default
@@ -146,11 +151,17 @@ class MoE:
     dropped) and raise DfMoeError on failure."""
 
     def __init__(self, hidden, n_experts, top_k, inter, n_shared, shared_inter,
-                 n_layers=1, max_tokens=1, rms_eps=1e-6, flags=0, device=0):
+                 n_layers=1, max_tokens=1, rms_eps=1e-6, flags=0, device=0, cache_slots=0):
+        """cache_slots > 0: experts in pinned host memory, that many a layer
+        in HBM (df_moe_create_cached)."""
         self.cfg = Config(hidden, n_experts, top_k, inter, n_shared, shared_inter,
                           n_layers, max_tokens, rms_eps, flags)
         h = ctypes.c_void_p()
-        rc = lib().df_moe_create(ctypes.byref(self.cfg), device, ctypes.byref(h))
+        if cache_slots:
+            rc = lib().df_moe_create_cached(ctypes.byref(self.cfg), device, cache_slots,
+                                            ctypes.byref(h))
+        else:
+            rc = lib().df_moe_create(ctypes.byref(self.cfg), device, ctypes.byref(h))
         if rc != OK:
             raise DfMoeError(rc, lib().df_moe_last_error(None).decode())
         self.h = h
@@ -273,6 +284,13 @@ class MoE:
 
     def last_launch_count(self):
         return lib().df_moe_last_launch_count(self.h)
+
+    def cache_stats(self):
+        """(hits, misses, bytes copied host -> HBM) of the expert cache."""
+        hits, misses, nbytes = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        self._check(lib().df_moe_cache_stats(self.h, ctypes.byref(hits), ctypes.byref(misses),
+                                             ctypes.byref(nbytes)))
+        return hits.value, misses.value, nbytes.value
 
     def graph(self, x, T, out, ids, weights, residual=None, out_f32=None):
         """A forward pass captured into a CUDA graph (df_moe_graph_create),

@@ -37,6 +37,13 @@ struct LayerBufs {
   std::vector<uint8_t> shared_loaded;
   std::vector<uint8_t> expert_loaded;
   int n_experts_loaded = 0;
+  // expert cache (df_moe_create_cached): every span in pinned host memory,
+  // `cache_slots` of them in HBM (the arena), found through span_tab
+  uint8_t* host_pool = nullptr;              // [E] spans, kernel layout (pinned, mapped)
+  const uint8_t* host_pool_dev = nullptr;    // the same pages as the device sees them
+  unsigned long long* span_tab = nullptr;    // device [E] span addresses (of cached experts)
+  std::vector<int> slot_of, expert_of;       // expert -> slot (-1), slot -> expert (-1)
+  std::vector<uint64_t> used;                // slot -> last use
 };
 
 struct Pending {
@@ -48,7 +55,7 @@ const char* kKindNames[K_NKINDS] = {"router", "topk", "group", "expert_gateup",
                                     "expert_down", "combine", "shared_gateup",
                                     "shared_down", "rmsnorm", "residual",
                                     "repack", "other", "layer", "gemm_gateup",
-                                    "gemm_down"};
+                                    "gemm_down", "cache_fill"};
 
 }  // namespace
 
@@ -99,6 +106,14 @@ struct df_moe {
   bool phase = false;  // decode batches run the two phase kernels
   int sms = 0;
   cudaStream_t cap_stream = nullptr;  // CUDA-graph captures run on it
+  // expert cache: HBM slots a layer (0: every expert resident in HBM)
+  int cache_slots = 0;
+  uint64_t cache_clock = 0;
+  int64_t cache_hits = 0, cache_misses = 0, cache_bytes = 0;
+  int32_t* ids_h = nullptr;  // pinned [Tmax * k]: a layer's selection on the host
+  CacheCopy* fill_h = nullptr;        // pinned, mapped [Tmax * k]: a layer's fill plan
+  const CacheCopy* fill_d = nullptr;  // the same as the device sees it
+  std::vector<void*> host_allocs;
   // host-API device buffers
   uint16_t* hx = nullptr;
   uint16_t* hres = nullptr;
@@ -370,6 +385,68 @@ int layer_kernel_forward(df_moe* h, int l, const uint16_t* x, int T,
   return DF_MOE_OK;
 }
 
+// Expert cache: brings layer l's selection (ids, on the device) into HBM
+// slots. The selection comes to the host (one synchronisation); every
+// selected expert not cached gets an empty slot, else the least recently
+// used slot not needed now, and one fill kernel copies those experts from
+// the pinned host pool into their slots and points their span-table entries
+// at them (a cached expert's entry already points at its slot). Consecutive
+// tokens that share experts find them cached: the last token's experts are
+// the most recently used ones. This is the previous-token reuse of the Deltafin README
+// ("Techniques", "I/O and streaming") and the expert LRU cache of the
+// kimi-k3-in-c blog, moved from SSD -> RAM to Grace memory -> HBM. The
+// blog's first trap counts a prefetched expert as a hit although its bytes
+// moved, so the statistics count the bytes copied in.
+int cache_plan(df_moe* h, int l, int T, const int32_t* ids, cudaStream_t s) {
+  const df_moe_config& c = h->cfg;
+  LayerBufs& L = h->layers[l];
+  const int n = T * c.top_k;
+  CUDA_OR_FAIL(h, cudaMemcpyAsync(h->ids_h, ids, n * sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  CUDA_OR_FAIL(h, cudaStreamSynchronize(s));
+  const uint64_t now = ++h->cache_clock;
+  std::vector<int> miss;
+  int nfill = 0;
+  for (int i = 0; i < n; ++i) {
+    const int e = h->ids_h[i];
+    if (e < 0 || e >= c.n_experts)
+      return fail(h, DF_MOE_ECUDA, "layer %d: selected expert %d out of range", l, e);
+    const int sl = L.slot_of[e];
+    if (sl >= 0) {
+      if (L.used[sl] != now) {
+        L.used[sl] = now;
+        ++h->cache_hits;
+      }
+    } else if (std::find(miss.begin(), miss.end(), e) == miss.end()) {
+      miss.push_back(e);
+    }
+  }
+  for (const int e : miss) {
+    int v = -1;
+    for (int sl = 0; sl < h->cache_slots; ++sl) {
+      if (L.used[sl] == now) continue;
+      if (L.expert_of[sl] < 0) {
+        v = sl;
+        break;
+      }
+      if (v < 0 || L.used[sl] < L.used[v]) v = sl;
+    }
+    if (v < 0) return fail(h, DF_MOE_ESTATE, "layer %d: no free cache slot", l);
+    if (L.expert_of[v] >= 0) L.slot_of[L.expert_of[v]] = -1;
+    L.expert_of[v] = e;
+    L.slot_of[e] = v;
+    L.used[v] = now;
+    // the plan buffer is free: the synchronisation above came after the
+    // previous fill kernel
+    h->fill_h[nfill++] = CacheCopy{L.host_pool_dev + (size_t)e * h->span_bytes,
+                                   L.arena + (size_t)v * h->span_bytes, e};
+    ++h->cache_misses;
+    h->cache_bytes += (int64_t)h->span_bytes;
+  }
+  if (nfill)
+    RUN(h, K_CACHE_FILL, s, launch_cache_fill(h->fill_d, nfill, h->span_bytes, L.span_tab, s));
+  return DF_MOE_OK;
+}
+
 int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
                   const uint16_t* residual, uint16_t* out_bf16, float* out_f32,
                   int32_t* ids, float* w, cudaStream_t s) {
@@ -381,6 +458,7 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
   const int max_items = (T == 1 && tg == 1) ? c.top_k : std::min(T * c.top_k, c.n_experts);
   const int R = c.n_shared > 0 ? h->R : 0;
   const bool phase = T <= kLayerMaxT && h->phase;
+  const bool cached = h->cache_slots > 0;
   int sh_gu = 0, sh_dn = 0;
   if (phase && R > 0) {
     // CTAs for the shared experts in each phase: the split that ends both
@@ -407,19 +485,28 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
     sh_gu = split(gu_sh, gu_rt, T == 1 ? 6.0 : 0.0);
     sh_dn = split(dn_sh, dn_rt, 0.0);
   }
-  int rc = route(h, l, x, T, ids, w, s, nullptr, tg, /*planes_only=*/phase);
+  int rc = route(h, l, x, T, ids, w, s, nullptr, tg, /*planes_only=*/phase && !cached);
   if (rc) return rc;
+  if (cached) {
+    rc = cache_plan(h, l, T, ids, s);
+    if (rc) return rc;
+  }
   if (phase) {
     // decode batches: routed and shared experts together on every SM, each
     // kernel a programmatic dependent of the one before
     RUN(h, K_GATEUP, s, launch_phase_gateup(L.sh_gate, L.sh_up, R, L.arena, h->span_bytes,
                                             c.hidden, c.inter, c.top_k, x, T, h->items,
-                                            h->n_items, h->sorted, h->router_part,
+                                            h->n_items, h->sorted,
+                                            cached ? nullptr : h->router_part,
                                             h->rsplit.nsplit, c.n_experts, ids, w, h->hsh,
-                                            h->hbuf, h->err, sh_gu, s));
+                                            h->hbuf, h->err, sh_gu,
+                                            cached ? (const uint8_t* const*)L.span_tab : nullptr,
+                                            s));
     RUN(h, K_DOWN, s, launch_phase_down(L.arena, h->span_bytes, c.hidden, c.inter, h->items,
                                         h->n_items, h->sorted, h->hbuf, h->part, L.sh_down, R,
-                                        h->hsh, T, h->ysh, h->err, sh_dn, s));
+                                        h->hsh, T, h->ysh, h->err, sh_dn,
+                                        cached ? (const uint8_t* const*)L.span_tab : nullptr,
+                                        s));
   } else {
     // batches: the shared experts, then the routed ones
     if (c.n_shared > 0) {
@@ -466,11 +553,12 @@ void df_moe_destroy(df_moe* h) {
   }
   for (auto e : h->event_pool) cudaEventDestroy(e);
   for (void* p : h->allocs) cudaFree(p);
+  for (void* p : h->host_allocs) cudaFreeHost(p);
   cudaSetDevice(prev);
   delete h;
 }
 
-int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
+static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_moe** out) {
   if (!cfg || !out) return fail(nullptr, DF_MOE_EINVAL, "null argument");
   *out = nullptr;
   const df_moe_config c = *cfg;
@@ -500,6 +588,15 @@ int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
     return fail(nullptr, DF_MOE_EINVAL, "unknown flags");
   if ((c.flags & DF_MOE_STACK_RMSNORM_RESIDUAL) && !(c.rms_eps >= 0.0f))
     return fail(nullptr, DF_MOE_EINVAL, "rms_eps must be >= 0");
+  if (slots) {
+    if (c.max_tokens > kLayerMaxT || (c.flags & DF_MOE_FUSED_DECODE))
+      return fail(nullptr, DF_MOE_EINVAL,
+                  "an expert cache serves decode batches (max_tokens <= %d, no fused layer)",
+                  kLayerMaxT);
+    if (slots < std::min(c.max_tokens * c.top_k, c.n_experts) || slots > c.n_experts)
+      return fail(nullptr, DF_MOE_EINVAL,
+                  "cache_slots must be in [min(max_tokens*top_k, n_experts), n_experts]");
+  }
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || cuda_device < 0 ||
       cuda_device >= ndev) {
@@ -514,6 +611,7 @@ int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
   df_moe* h = new df_moe;
   h->cfg = c;
   h->device = cuda_device;
+  h->cache_slots = slots;
   h->span_bytes = span_layout(c.hidden, c.inter).bytes;
   h->R = c.n_shared * c.shared_inter;
   h->rsplit = router_split(c.n_experts, c.hidden);
@@ -525,7 +623,27 @@ int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
     LayerBufs& L = h->layers[l];
     L.shared_loaded.assign(c.n_shared, 0);
     L.expert_loaded.assign(c.n_experts, 0);
-    rc = dalloc(h, &L.arena, E * h->span_bytes);
+    rc = dalloc(h, &L.arena, (slots ? (size_t)slots : E) * h->span_bytes);
+    if (!rc && slots) {
+      L.slot_of.assign(E, -1);
+      L.expert_of.assign(slots, -1);
+      L.used.assign(slots, 0);
+      rc = dalloc(h, &L.span_tab, E);
+      if (!rc && cudaMemset(L.span_tab, 0, E * sizeof(unsigned long long)) != cudaSuccess)
+        rc = fail(h, DF_MOE_ECUDA, "cudaMemset failed");
+      void* hp = nullptr;
+      if (!rc && cudaHostAlloc(&hp, E * h->span_bytes,
+                               cudaHostAllocPortable | cudaHostAllocMapped) != cudaSuccess)
+        rc = fail(h, DF_MOE_ENOMEM, "pinned host pool of %zu bytes failed", E * h->span_bytes);
+      if (!rc) {
+        h->host_allocs.push_back(hp);
+        L.host_pool = static_cast<uint8_t*>(hp);
+        void* dp = nullptr;
+        if (cudaHostGetDevicePointer(&dp, hp, 0) != cudaSuccess)
+          rc = fail(h, DF_MOE_ECUDA, "host pool not mapped into the device");
+        L.host_pool_dev = static_cast<const uint8_t*>(dp);
+      }
+    }
     if (!rc) rc = dalloc(h, &L.router, E * H);
     if (!rc && R) rc = dalloc(h, &L.sh_gate, R * H);
     if (!rc && R) rc = dalloc(h, &L.sh_up, R * H);
@@ -536,7 +654,7 @@ int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
     if (!rc && R) rc = dalloc(h, &L.sh_dn_rs, (size_t)c.n_shared * H);
   }
   // tcgen05 GEMMs: batches above the decode range, unless asked otherwise
-  h->gemm = Tm > (size_t)kLayerMaxT && !(c.flags & DF_MOE_PREFILL_MMA_SYNC) &&
+  h->gemm = !slots && Tm > (size_t)kLayerMaxT && !(c.flags & DF_MOE_PREFILL_MMA_SYNC) &&
             gemm_supported(c.hidden, c.inter);
   if (h->gemm) {
     for (int l = 0; l < c.n_layers && !rc; ++l) {
@@ -609,9 +727,32 @@ int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
   if (!rc) rc = dalloc(h, &h->hout32, Tm * H);
   if (!rc) rc = dalloc(h, &h->hids, (size_t)c.n_layers * Tm * k);
   if (!rc) rc = dalloc(h, &h->hw, (size_t)c.n_layers * Tm * k);
+  if (!rc && slots) {
+    void* hp = nullptr;
+    if (cudaHostAlloc(&hp, Tm * k * sizeof(int32_t), cudaHostAllocPortable) != cudaSuccess)
+      rc = fail(h, DF_MOE_ENOMEM, "pinned id buffer failed");
+    else {
+      h->host_allocs.push_back(hp);
+      h->ids_h = static_cast<int32_t*>(hp);
+    }
+    hp = nullptr;
+    if (!rc && cudaHostAlloc(&hp, Tm * k * sizeof(CacheCopy),
+                             cudaHostAllocPortable | cudaHostAllocMapped) != cudaSuccess)
+      rc = fail(h, DF_MOE_ENOMEM, "pinned fill plan failed");
+    if (!rc) {
+      h->host_allocs.push_back(hp);
+      h->fill_h = static_cast<CacheCopy*>(hp);
+      void* dp = nullptr;
+      if (cudaHostGetDevicePointer(&dp, hp, 0) != cudaSuccess)
+        rc = fail(h, DF_MOE_ECUDA, "fill plan not mapped into the device");
+      h->fill_d = static_cast<const CacheCopy*>(dp);
+    }
+  }
   if (!rc) {
     cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, cuda_device);
     h->phase = phase_supported(H, c.inter, c.n_shared > 0 ? h->R : 0, c.n_experts, c.top_k);
+    if (slots && !h->phase)
+      rc = fail(h, DF_MOE_EINVAL, "an expert cache needs the decode phase kernels' shapes");
   }
   if (!rc && (cudaMemset(h->err, 0, sizeof(uint32_t)) != cudaSuccess ||
               cudaMemset(h->counter, 0, sizeof(unsigned int)) != cudaSuccess))
@@ -624,6 +765,24 @@ int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
   }
   cudaSetDevice(prev);
   *out = h;
+  return DF_MOE_OK;
+}
+
+int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe** out) {
+  return create_impl(cfg, cuda_device, 0, out);
+}
+
+int df_moe_create_cached(const df_moe_config* cfg, int cuda_device, int32_t cache_slots,
+                         df_moe** out) {
+  if (cache_slots < 1) return fail(nullptr, DF_MOE_EINVAL, "cache_slots must be >= 1");
+  return create_impl(cfg, cuda_device, cache_slots, out);
+}
+
+int df_moe_cache_stats(const df_moe* h, int64_t* hits, int64_t* misses, int64_t* bytes_in) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  if (hits) *hits = h->cache_hits;
+  if (misses) *misses = h->cache_misses;
+  if (bytes_in) *bytes_in = h->cache_bytes;
   return DF_MOE_OK;
 }
 
@@ -675,7 +834,42 @@ int df_moe_load_experts(df_moe* h, int32_t layer, const df_moe_layer_weights* w,
       return fail(h, DF_MOE_ERANGE, "experts [%d, %d) out of range", w->expert_begin,
                   w->expert_begin + w->expert_count);
     uint8_t* dst = L.arena + (size_t)w->expert_begin * h->span_bytes;
-    if (w->src_is_device) {
+    if (h->cache_slots) {
+      // repacked on the device in chunks of 8 spans, then kept in the pinned
+      // host pool; the HBM slots fill on demand
+      const size_t chunk = 8;
+      if (!h->staging) {
+        h->staging_spans = chunk;
+        int rc = dalloc(h, &h->staging, 2 * chunk * h->span_bytes);
+        if (rc) return rc;
+      }
+      uint8_t* packed = h->staging + chunk * h->span_bytes;
+      if (w->src_is_device && !aligned16(w->experts))
+        return fail(h, DF_MOE_EINVAL, "device expert spans must be 16-byte aligned");
+      for (int e0 = 0; e0 < w->expert_count; e0 += (int)chunk) {
+        const int n = (int)std::min<size_t>(chunk, (size_t)(w->expert_count - e0));
+        const uint8_t* src = w->experts + (size_t)e0 * h->span_bytes;
+        if (!w->src_is_device) {
+          CUDA_OR_FAIL(h, cudaMemcpyAsync(h->staging, src, (size_t)n * h->span_bytes,
+                                          cudaMemcpyHostToDevice, s));
+          src = h->staging;
+        }
+        RUN(h, K_REPACK, s, launch_repack_span(src, packed, n, c.hidden, c.inter, 0, s));
+        CUDA_OR_FAIL(h, cudaMemcpyAsync(L.host_pool + (size_t)(w->expert_begin + e0) *
+                                                          h->span_bytes,
+                                        packed, (size_t)n * h->span_bytes,
+                                        cudaMemcpyDeviceToHost, s));
+      }
+      CUDA_OR_FAIL(h, cudaStreamSynchronize(s));
+      for (int e = w->expert_begin; e < w->expert_begin + w->expert_count; ++e) {
+        // a reloaded expert leaves the cache
+        const int sl = L.slot_of[e];
+        if (sl >= 0) {
+          L.expert_of[sl] = -1;
+          L.slot_of[e] = -1;
+        }
+      }
+    } else if (w->src_is_device) {
       if (!aligned16(w->experts))
         return fail(h, DF_MOE_EINVAL, "device expert spans must be 16-byte aligned");
       RUN(h, K_REPACK, s, launch_repack_span(w->experts, dst, w->expert_count,
@@ -890,6 +1084,8 @@ int df_moe_step_expert_gateup(df_moe* h, int32_t layer, const void* x_bf16,
   if (!x_bf16 || !ids || !hbuf) return fail(h, DF_MOE_EINVAL, "null pointer");
   if (h->layers[layer].n_experts_loaded != c.n_experts)
     return fail(h, DF_MOE_ESTATE, "experts not loaded");
+  if (h->cache_slots)
+    return fail(h, DF_MOE_EINVAL, "single expert steps read the resident arena: not with a cache");
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
   cudaStream_t s = (cudaStream_t)stream;
   const int tg = kOneItemPerExpert;
@@ -910,6 +1106,8 @@ int df_moe_step_expert_down(df_moe* h, int32_t layer, const float* hbuf,
   if (!hbuf || !ids || !weights || !y) return fail(h, DF_MOE_EINVAL, "null pointer");
   if (h->layers[layer].n_experts_loaded != c.n_experts)
     return fail(h, DF_MOE_ESTATE, "experts not loaded");
+  if (h->cache_slots)
+    return fail(h, DF_MOE_EINVAL, "single expert steps read the resident arena: not with a cache");
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
   cudaStream_t s = (cudaStream_t)stream;
   const int tg = kOneItemPerExpert;
@@ -964,10 +1162,16 @@ int df_moe_read_expert_span(df_moe* h, int32_t layer, int32_t expert,
   if (!dst) return fail(h, DF_MOE_EINVAL, "null dst");
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
   uint8_t* tmp = nullptr;
-  CUDA_OR_FAIL(h, cudaMalloc(&tmp, h->span_bytes));
-  cudaError_t e = launch_repack_span(h->layers[layer].arena +
-                                         (size_t)expert * h->span_bytes,
-                                     tmp, 1, c.hidden, c.inter, 1, nullptr);
+  CUDA_OR_FAIL(h, cudaMalloc(&tmp, 2 * h->span_bytes));
+  const uint8_t* src = h->layers[layer].arena + (size_t)expert * h->span_bytes;
+  cudaError_t e = cudaSuccess;
+  if (h->cache_slots) {  // the expert's home is the pinned host pool
+    e = cudaMemcpy(tmp + h->span_bytes, h->layers[layer].host_pool +
+                                            (size_t)expert * h->span_bytes,
+                   h->span_bytes, cudaMemcpyHostToDevice);
+    src = tmp + h->span_bytes;
+  }
+  if (e == cudaSuccess) e = launch_repack_span(src, tmp, 1, c.hidden, c.inter, 1, nullptr);
   if (e == cudaSuccess) e = cudaMemcpy(dst, tmp, h->span_bytes, cudaMemcpyDeviceToHost);
   cudaFree(tmp);
   if (e != cudaSuccess)
@@ -1035,6 +1239,8 @@ int df_moe_graph_create(df_moe* h, const void* x_bf16, int32_t T, const void* re
   if (h->cfg.flags & DF_MOE_FUSED_DECODE)
     return fail(h, DF_MOE_EINVAL, "graphs need the kernel chain (no DF_MOE_FUSED_DECODE)");
   if (h->timing) return fail(h, DF_MOE_EINVAL, "turn timing off before capturing a graph");
+  if (h->cache_slots)
+    return fail(h, DF_MOE_EINVAL, "an expert cache plans each layer on the host: no graphs");
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
   if (!h->cap_stream)
     CUDA_OR_FAIL(h, cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));

@@ -64,7 +64,7 @@ constexpr int kOneItemPerExpert = 1 << 20;
 enum KernelKind {
   K_ROUTER = 0, K_TOPK, K_GROUP, K_GATEUP, K_DOWN, K_COMBINE, K_SHARED_GU,
   K_SHARED_DN, K_RMSNORM, K_RESIDUAL, K_REPACK, K_OTHER, K_LAYER, K_GEMM_GU,
-  K_GEMM_DN, K_NKINDS
+  K_GEMM_DN, K_CACHE_FILL, K_NKINDS
 };
 
 // Launches `kernel` as a programmatic dependent of the previous kernel in
@@ -173,21 +173,33 @@ cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps,
 // `s`; the down phase follows the gate/up phase directly. R = n_shared * Is
 // (0: no shared experts). n_sh: CTAs (of one per SM) that run the shared
 // experts, in [1, SMs - 1] (0 when R = 0); the others run the routed ones.
+// spans: device [E] of span addresses (expert cache), or null for arena + e
+// * span_bytes.
 bool phase_supported(int H, int I, int R, int E, int k);
 // Read-only streaming probe: 16-byte loads over `bytes`, one word a thread
 // into sink (at least 8 * SMs * 256 words).
 cudaError_t launch_stream_read(const void* buf, size_t bytes, uint32_t* sink, cudaStream_t s);
+// Expert cache fill: one span copy of the plan (device-visible memory, n
+// entries): `span_bytes` (a multiple of 16) from src (pinned host memory,
+// mapped) to dst (an HBM slot), then span_tab[e] = dst.
+struct CacheCopy {
+  const void* src;
+  void* dst;
+  long long e;
+};
+cudaError_t launch_cache_fill(const CacheCopy* plan, int n, size_t span_bytes,
+                              unsigned long long* span_tab, cudaStream_t s);
 cudaError_t launch_phase_gateup(const uint16_t* sh_gate, const uint16_t* sh_up, int R,
                                 const uint8_t* arena, size_t span_bytes, int H, int I, int k,
                                 const uint16_t* x, int T, Item* items, int32_t* n_items,
                                 int32_t* sorted, const float* router_part, int nsplit, int E,
                                 int32_t* ids, float* w, float* hsh, float* hbuf, uint32_t* err,
-                                int n_sh, cudaStream_t s);
+                                int n_sh, const uint8_t* const* spans, cudaStream_t s);
 cudaError_t launch_phase_down(const uint8_t* arena, size_t span_bytes, int H, int I,
                               const Item* items, const int32_t* n_items, const int32_t* sorted,
                               const float* hbuf, float* part, const uint16_t* sh_down, int R,
                               const float* hsh, int T, float* ysh, uint32_t* err, int n_sh,
-                              cudaStream_t s);
+                              const uint8_t* const* spans, cudaStream_t s);
 cudaError_t launch_repack_span(const uint8_t* src, uint8_t* dst, int n_spans,
                                int H, int I, int inverse, cudaStream_t s);
 

@@ -85,7 +85,8 @@ cudaError_t launch_gateup(const uint8_t* arena, size_t span_bytes, int H,
                           const int32_t* n_items, int max_items,
                           const int32_t* sorted, float* hbuf, int /*tg*/,
                           uint32_t* err, cudaStream_t s, int max_ctas) {
-  MxvArgs a{arena, span_bytes, H, I, k, x, nullptr, items, n_items, sorted, hbuf, err, 0};
+  MxvArgs a{arena, span_bytes, H, I, k, x, nullptr, items, n_items, sorted, hbuf, err, 0,
+            nullptr};
   return launch_mxv<0>(a, max_items, s, max_ctas);
 }
 
@@ -95,7 +96,7 @@ cudaError_t launch_down(const uint8_t* arena, size_t span_bytes, int H, int I,
                         const float* hbuf, float* part, int /*tg*/, uint32_t* err,
                         cudaStream_t s, int max_ctas, bool after_gateup) {
   MxvArgs a{arena, span_bytes, H, I, 0, nullptr, hbuf, items, n_items, sorted, part, err,
-            after_gateup ? 1 : 0};
+            after_gateup ? 1 : 0, nullptr};
   return launch_mxv<1>(a, max_items, s, max_ctas);
 }
 

@@ -133,9 +133,10 @@ cudaError_t launch_phase_gateup(const uint16_t* sh_gate, const uint16_t* sh_up, 
                                 const uint16_t* x, int T, Item* items, int32_t* n_items,
                                 int32_t* sorted, const float* router_part, int nsplit, int E,
                                 int32_t* ids, float* w, float* hsh, float* hbuf, uint32_t* err,
-                                int n_sh, cudaStream_t s) {
+                                int n_sh, const uint8_t* const* spans, cudaStream_t s) {
   const BfvArgs sh{sh_gate, sh_up, R, H, x, T, hsh, err};
-  const MxvArgs rt{arena, span_bytes, H, I, k, x, nullptr, items, n_items, sorted, hbuf, err, 0};
+  const MxvArgs rt{arena, span_bytes, H, I, k, x, nullptr, items, n_items, sorted, hbuf, err, 0,
+                   spans};
   const SelArgs sel{T == 1 ? router_part : nullptr, nsplit, E, k, ids, w};
   const size_t smem = std::max(bfv_smem_bytes(H), mxv_smem_bytes(H, mxv_cg(0), mxv_unit(0)));
   auto go = [&](auto kernel, size_t& conf) {
@@ -155,9 +156,9 @@ cudaError_t launch_phase_down(const uint8_t* arena, size_t span_bytes, int H, in
                               const Item* items, const int32_t* n_items, const int32_t* sorted,
                               const float* hbuf, float* part, const uint16_t* sh_down, int R,
                               const float* hsh, int T, float* ysh, uint32_t* err, int n_sh,
-                              cudaStream_t s) {
+                              const uint8_t* const* spans, cudaStream_t s) {
   const MxvArgs rt{arena, span_bytes, H, I, 0, nullptr, hbuf, items, n_items, sorted, part, err,
-                   1};
+                   1, spans};
   // no shared experts: no rows to stream (K only sizes the geometry)
   const BfvArgs sh{sh_down, nullptr, R > 0 ? H : 0, R > 0 ? R : I, hsh, T, ysh, err};
   const size_t smem = std::max(mxv_smem_bytes(I, mxv_cg(1), mxv_unit(1)), bfv_smem_bytes(sh.K));

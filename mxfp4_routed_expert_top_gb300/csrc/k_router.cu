@@ -1,9 +1,10 @@
 // k_router.cu — router GEMV, top-k selection with softmax over the selected
 // logits, and grouping of token->expert assignments by expert.
 //
-// "The router picks 16 of the 896 experts; only those are read" (Deltafin
-// README, "How it works"; Deltafin analysis §5.1). Selection ties go to the
-// lower expert id; ids come out in descending logit order.
+// Each token's router chooses 16 of the 896 experts, and only the chosen
+// experts' weights are touched (Deltafin README, "How it works"; Deltafin
+// analysis §5.1). Selection ties go to the lower expert id; ids come out in
+// descending logit order.
 #include <math.h>
 
 #include <algorithm>

@@ -101,7 +101,46 @@ __global__ void __launch_bounds__(256) stream_read_kernel(const uint4* __restric
   sink[(size_t)blockIdx.x * blockDim.x + threadIdx.x] = acc;
 }
 
+// Expert cache fill: block (x, y) copies its share of span y from pinned host
+// memory over NVLink-C2C (plain loads of the mapped pages, eight 16-byte
+// loads in flight a thread) into its HBM slot; block (0, y) also points the
+// span table at the slot. SM loads keep the whole copy near the link's rate
+// where copy-engine copies of single spans showed a slow tail.
+__global__ void __launch_bounds__(512) cache_fill_kernel(const CacheCopy* __restrict__ plan,
+                                                         size_t n16,
+                                                         unsigned long long* __restrict__ span_tab) {
+  constexpr int U = 8;
+  __shared__ CacheCopy c;
+  if (threadIdx.x == 0) {
+    c = plan[blockIdx.y];
+    if (blockIdx.x == 0) span_tab[c.e] = (unsigned long long)(uintptr_t)c.dst;
+  }
+  __syncthreads();
+  const uint4* __restrict__ src = static_cast<const uint4*>(c.src);
+  uint4* __restrict__ dst = static_cast<uint4*>(c.dst);
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + (U - 1) * stride < n16; i += U * stride) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) v[u] = src[i + u * stride];
+#pragma unroll
+    for (int u = 0; u < U; ++u) dst[i + u * stride] = v[u];
+  }
+  for (; i < n16; i += stride) dst[i] = src[i];
+}
+
 }  // namespace
+
+cudaError_t launch_cache_fill(const CacheCopy* plan, int n, size_t span_bytes,
+                              unsigned long long* span_tab, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  if (span_bytes % 16 || n > 65535) return cudaErrorInvalidValue;
+  // about four blocks an SM over all spans
+  const int bx = std::max(1, (4 * num_sms_b() + n - 1) / n);
+  cache_fill_kernel<<<dim3(bx, n), 512, 0, s>>>(plan, span_bytes / 16, span_tab);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_stream_read(const void* buf, size_t bytes, uint32_t* sink, cudaStream_t s) {
   stream_read_kernel<<<4 * num_sms_b(), 256, 0, s>>>(static_cast<const uint4*>(buf), bytes / 16,

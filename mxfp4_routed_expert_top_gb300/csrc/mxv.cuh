@@ -74,6 +74,7 @@ struct MxvArgs {
   float* out;             // gate/up: h [T*k][I]; down: part [T*k][H]
   uint32_t* err;
   int early;              // down only: the selection is complete at grid start
+  const uint8_t* const* spans;  // [E] span addresses (expert cache), or null: arena
 };
 
 __host__ __device__ inline size_t align128(size_t v) { return (v + 127) & ~(size_t)127; }
@@ -221,8 +222,10 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
         const int item = t / tpi, j = t - item * tpi;
         if (item != cur_item) {
           cur_item = item;
-          span = a.arena + (size_t)(early ? __ldcg(&a.items[item].e) : a.items[item].e) *
-                           a.span_bytes;
+          const int e = early ? __ldcg(&a.items[item].e) : a.items[item].e;
+          span = a.spans ? reinterpret_cast<const uint8_t*>(
+                               __ldcg(reinterpret_cast<const unsigned long long*>(a.spans) + e))
+                         : a.arena + (size_t)e * a.span_bytes;
         }
         if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
         uint8_t* dst = ring + (size_t)stage * geo.stage_bytes;

@@ -1,9 +1,10 @@
 // select.cuh — top-k selection of one token's logits by a thread block:
 // bitonic sorting networks on warp shuffles.
 //
-// "The router picks 16 of the 896 experts; only those are read" (Deltafin
-// README, "How it works"). Order: larger logit first, equal logits by lower
-// expert id, so the selection equals a full sort of the logits.
+// Each token's router chooses 16 of the 896 experts, and only the chosen
+// experts' weights are touched (Deltafin README, "How it works"). Order:
+// larger logit first, equal logits by lower expert id, so the selection
+// equals a full sort of the logits.
 #pragma once
 
 #include <math.h>

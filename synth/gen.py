@@ -17,6 +17,7 @@ KIND_SHARED_UP = 3
 KIND_SHARED_DOWN = 4
 KIND_X = 5
 KIND_RESIDUAL = 6
+KIND_X_STREAM = 7
 KIND_EXPERT_BASE = 16
 
 # redraw sub-seeds per token (tokens whose routing gap is too small are redrawn)
@@ -175,6 +176,34 @@ def token(seed, cfg, token_id, H, redraw=0, kind=KIND_X):
         raise ValueError("redraw out of range")
     k = key(seed, cfg, 0, kind, token_id * REDRAWS_PER_TOKEN + redraw)
     return normal_bf16(k, H, 1.0)
+
+
+def f64_to_bf16_bits(a):
+    """Round fp64 values to bf16 (through fp32, nearest-even); uint16 bits."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def token_stream(seed, cfg, first, n, H, rho, stream=0):
+    """bf16 bits [n, H]: consecutive tokens of a stream with temporal
+    correlation, x_0 = z_0 and x_i = rho x_(i-1) + sqrt(1 - rho^2) z_i with
+    z_i ~ N(0, 1) i.i.d. (a stationary AR(1) process per coordinate, so each
+    token is N(0, 1) and neighbours have correlation rho). Token i of the
+    stream starting at `first` is the same whatever n is. rho = 0 gives
+    independent tokens. `stream` selects one of independent streams (it takes
+    the layer field of the key)."""
+    if not 0.0 <= rho < 1.0:
+        raise ValueError("rho must be in [0, 1)")
+    c = math.sqrt(1.0 - rho * rho)
+    x = normal_f64(key(seed, cfg, stream, KIND_X_STREAM, 0), H, 1.0)
+    out = np.empty((n, H), dtype=np.uint16)
+    for i in range(first + n):
+        if i:
+            x = rho * x + c * normal_f64(key(seed, cfg, stream, KIND_X_STREAM, i), H, 1.0)
+        if i >= first:
+            out[i - first] = f64_to_bf16_bits(x)
+    return out
 
 
 def dev_expert_spans(seed, cfg, layer, e0, n, H, I, dst_ptr, stream_ptr=0):

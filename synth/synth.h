@@ -43,6 +43,7 @@ enum {
   SYNTH_KIND_SHARED_DOWN = 4,  /* bf16 [H][Is]                         */
   SYNTH_KIND_X = 5,            /* bf16 [H] per token ~ N(0, 1)         */
   SYNTH_KIND_RESIDUAL = 6,     /* bf16 [H] per token ~ N(0, 1)         */
+  SYNTH_KIND_X_STREAM = 7,     /* fp64 innovations of a token stream   */
   SYNTH_KIND_EXPERT_BASE = 16  /* + tensor id 0..5 of an expert span   */
 };
 

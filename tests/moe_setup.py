@@ -41,7 +41,8 @@ class Setup:
     oracle's view of the same weights (spans generated on demand on the
     host)."""
 
-    def __init__(self, wl, max_tokens=None, chunk=64, fused=False, mma_sync_prefill=False):
+    def __init__(self, wl, max_tokens=None, chunk=64, fused=False, mma_sync_prefill=False,
+                 cache_slots=0):
         import mxfp4_routed_expert_top_gb300 as dfm
         torch = torch_mod()
         self.wl = wl
@@ -50,7 +51,7 @@ class Setup:
                  | (dfm.PREFILL_MMA_SYNC if mma_sync_prefill else 0))
         self.m = dfm.MoE(wl.H, wl.E, wl.k, wl.I, wl.n_shared, wl.Is,
                          n_layers=wl.L, max_tokens=max_tokens or wl.T,
-                         rms_eps=wl.eps, flags=flags)
+                         rms_eps=wl.eps, flags=flags, cache_slots=cache_slots)
         self.routers, self.shared, self.layers = [], [], []
         span = synth.span_bytes(wl.H, wl.I)
         stream = torch.cuda.current_stream()

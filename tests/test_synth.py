@@ -60,3 +60,27 @@ def test_token_redraws_are_independent():
     a = synth.token(0, 1, 5, 256, redraw=0)
     b = synth.token(0, 1, 5, 256, redraw=1)
     assert not np.array_equal(a, b)
+
+
+def test_f64_to_bf16_bits_matches_torch():
+    import torch
+    a = np.concatenate([synth.normal_f64(synth.key(1, 2, 0, 5, 3), 4000, 3.0),
+                        [0.0, -0.0, 1.0, 1.00390625, 1.005859375, 65504.0, -2.5e-3]])
+    ref = (torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)
+           .view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(synth.f64_to_bf16_bits(a), ref)
+
+
+def test_token_stream_window_moments_and_correlation():
+    H, rho = 7168, 0.7
+    full = synth.token_stream(4, 3, 0, 12, H, rho)
+    assert np.array_equal(synth.token_stream(4, 3, 5, 4, H, rho), full[5:9])
+    x = (full.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    # every token N(0, 1); neighbours correlated rho, two apart rho^2
+    assert np.all(np.abs(x.var(axis=1) - 1.0) < 0.06)
+    c1 = np.mean([np.corrcoef(x[i], x[i + 1])[0, 1] for i in range(11)])
+    c2 = np.mean([np.corrcoef(x[i], x[i + 2])[0, 1] for i in range(10)])
+    assert abs(c1 - rho) < 0.02 and abs(c2 - rho * rho) < 0.02
+    ind = synth.token_stream(4, 3, 0, 6, H, 0.0)
+    y = (ind.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert abs(np.corrcoef(y[0], y[1])[0, 1]) < 0.05
