@@ -15,7 +15,8 @@ import pytest
 
 import oracle as orc
 import synth
-from moe_setup import Setup, check_ids_weights, check_out, draw_tokens, to_dev_bf16
+from moe_setup import (Setup, bits_to_f64, check_ids_weights, check_out, draw_tokens,
+                       to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -201,3 +202,87 @@ def test_k3_cached_matches_oracle(k3_cached, torch):
         assert nbytes == misses * span
     # the repeated token moved no bytes
     assert model.hits >= wl.k
+
+
+@pytest.fixture(scope="module")
+def k3_cached8(torch):
+    s = Setup(K3, max_tokens=8, cache_slots=128)
+    yield s
+    s.close()
+    torch.cuda.empty_cache()
+
+
+def test_k3_cached_batch8(k3_cached8, torch):
+    """Batches of 8 tokens (up to 128 distinct experts a call) through 128
+    slots: the second batch evicts most of the first; the third repeats
+    the first and must find only what the second left."""
+    s, wl = k3_cached8, K3
+    span = s.m.span_bytes
+    model = LruModel(128)
+    x = draw_tokens(s, 16, first_id=300)
+    for i, xc in enumerate([x[0:8], x[8:16], x[0:8], x[4:8]]):
+        T = xc.shape[0]
+        out32, ids, w = _forward(s.m, xc, T, torch, wl.H, wl.k)
+        ref = orc.moe_layer(s.layers[0], xc)
+        check_ids_weights(ids, w, ref["ids"], ref["w"])
+        check_out(out32, ref["out"])
+        model.call(ref["ids"].reshape(-1).tolist())
+        hits, misses, nbytes = s.m.cache_stats()
+        assert (hits, misses) == (model.hits, model.misses), "call %d" % i
+        assert nbytes == misses * span
+
+
+def test_tiny_stack_cached(torch):
+    """Three tiny layers with RMSNorm and residual, each with its own 3 HBM
+    slots: bit-identical to the resident handle (same kernels on the same
+    span bytes), and every layer against the oracle on the inputs the device
+    gave it."""
+    import dataclasses
+    from moe_setup import gap_ok
+    wl = dataclasses.replace(TINY, name="tiny-stack3", L=3, stack=True)
+    cached = Setup(wl, max_tokens=2, cache_slots=4)
+    resident = Setup(wl, max_tokens=2)
+    try:
+        L, H, k = wl.L, wl.H, wl.k
+        for T, first in ((1, 40), (2, 60), (1, 40)):
+            res = {}
+            for name, s in (("cached", cached), ("resident", resident)):
+                out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+                out32 = torch.empty((T, H), dtype=torch.float32, device="cuda")
+                ids = torch.empty((L, T, k), dtype=torch.int32, device="cuda")
+                w = torch.empty((L, T, k), dtype=torch.float32, device="cuda")
+                tx = torch.empty((L, T, H), dtype=torch.int16, device="cuda")
+                txn = torch.empty((L, T, H), dtype=torch.int16, device="cuda")
+                x = np.stack([synth.token(wl.seed, wl.cfg_id, first + t, H) for t in range(T)])
+                s.m.forward_trace(to_dev_bf16(x), T, out, ids, w, trace_x=tx, trace_xn=txn,
+                                  out_f32=out32)
+                s.m.sync()
+                res[name] = [a.cpu().numpy() for a in (out, out32, ids, w, tx, txn)]
+            for a, b in zip(res["cached"], res["resident"]):
+                assert np.array_equal(a, b)
+            out, out32, ids, w, tx, txn = res["cached"]
+            tx, txn = tx.view(np.uint16), txn.view(np.uint16)
+            for l in range(L):
+                if not all(gap_ok(orc.router_logits(cached.routers[l], txn[l, t:t + 1]), k)
+                           for t in range(T)):
+                    continue  # ids of a near-tie are not unique
+                ref = orc.moe_layer(cached.layers[l], txn[l], residual=tx[l])
+                check_ids_weights(ids[l], w[l], ref["ids"], ref["w"])
+                y_ref = ref["out"] - bits_to_f64(tx[l])
+                if l == L - 1:
+                    check_out(out32 - bits_to_f64(tx[l]), y_ref)
+                else:
+                    # the next input is the bf16 rounding of residual + output:
+                    # within one ulp of the oracle sum's rounding (plus 1e-3 x
+                    # RMS of the output where the two nearly cancel)
+                    want = np.array([[orc.f64_to_bf16(v) for v in row] for row in ref["out"]],
+                                    dtype=np.uint16)
+                    slack = 1e-3 * np.sqrt(np.mean(y_ref ** 2, axis=-1, keepdims=True))
+                    ulp = np.abs(bits_to_f64(want)) * 2.0 ** -7
+                    diff = np.abs(bits_to_f64(tx[l + 1]) - bits_to_f64(want))
+                    assert np.all(diff <= ulp + slack), "layer %d" % l
+        hits, misses, _ = cached.m.cache_stats()
+        assert misses >= k * L and hits + misses >= 3 * k * L
+    finally:
+        cached.close()
+        resident.close()
