@@ -8,7 +8,8 @@ token. L2 is flushed (a 256 MiB write) before every timed step, outside the
 timed events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--config 1|2|3|4] [--no-cpu-baseline]
+                  [--config 1|2|3|4] [--tokens T] [--graph | --fused]
+                  [--cache-slots N [--token-corr RHO]] [--no-cpu-baseline]
 
 Prints one JSON line on rank 0. Under torchrun (N > 1) every rank runs an
 independent replica on its own GPU (the layer does not shard: replicas only);
@@ -43,7 +44,7 @@ TOKEN_POOL = 64
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4])
@@ -594,6 +595,16 @@ def main():
                 "cores": threads, "kind": "oracle",
                 "sample": "%d tokens of %s through the CPU oracle (%.1f s)" % (
                     n, wl.name, n / rate)}
+            # the same oracle on one core (a third of the time budget)
+            import oracle as orc
+            orc.set_num_threads(1)
+            try:
+                r1, n1, _ = cpu_oracle_rate(wl, args.cpu_seconds / 3)
+            finally:
+                orc.set_num_threads(threads)
+            res["cpu_baseline"]["single_thread"] = {
+                "value": round(r1, 4), "unit": UNIT, "cores": 1,
+                "sample": "%d tokens, %.1f s" % (n1, n1 / r1)}
     if res is not None:
         print(json.dumps(res), flush=True)
 
