@@ -39,6 +39,7 @@ METRIC = "K3-shape MoE-layer decode tokens/s; achieved HBM GB/s vs GB300 peak"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
 TOKEN_POOL = 64
+REF_TIMED_SECONDS = 120  # cap on the reference arm's timed oracle tokens
 
 
 def parse():
@@ -239,7 +240,8 @@ def aggregate_over_ranks(dist, seconds, units, device="cpu"):
 
 def cpu_oracle_rate(wl, seconds, max_tokens=None):
     """Tokens/s of the CPU oracle on the workload's tokens, timed until
-    `seconds` of work (at least one token). Returns (rate, tokens, threads)."""
+    `seconds` of work (0: no time limit) or `max_tokens` tokens, whichever
+    comes first (at least one token). Returns (rate, tokens, threads)."""
     import oracle as orc
     layers = []
     for l in range(wl.L):
@@ -261,7 +263,7 @@ def cpu_oracle_rate(wl, seconds, max_tokens=None):
             L.clear_cache()
         n += 1
         el = time.perf_counter() - t0
-        if el >= seconds or (max_tokens and n >= max_tokens):
+        if (seconds > 0 and el >= seconds) or (max_tokens and n >= max_tokens):
             break
     return n / el, n, orc.num_threads()
 
@@ -498,9 +500,7 @@ def run_ours(args):
         "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "impl": "ours",
-        "config": {"workload": wl.name, "hidden": wl.H, "experts": wl.E, "top_k": wl.k,
-                   "inter": wl.I, "shared": wl.n_shared, "tokens_per_step": T,
-                   "layers": wl.L, "weights": "mxfp4 e2m1+e8m0/32, shared bf16",
+        "config": {**workload_config(wl, ws),
                    "l2": "flushed (256 MiB write) before every timed step",
                    "decode_path": "fused" if args.fused else "chain",
                    "launch": "cuda graph" if args.graph else "stream",
@@ -508,8 +508,7 @@ def run_ours(args):
                    "experts_home": ("pinned host memory, %d a layer cached in HBM"
                                     % args.cache_slots) if args.cache_slots else "HBM",
                    "tokens": ("AR(1) stream, neighbour correlation %g" % args.token_corr)
-                             if args.token_corr else "independent N(0,1)",
-                   "parallelism": "replicas" if ws > 1 else "single-gpu"},
+                             if args.token_corr else "independent N(0,1)"},
         "step_us": {"median": round(float(np.median(step_ms)) * 1e3, 2),
                     "p10": round(float(np.percentile(step_ms, 10)) * 1e3, 2),
                     "p90": round(float(np.percentile(step_ms, 90)) * 1e3, 2)},
@@ -554,16 +553,29 @@ def tensor_use(kt, wl, T):
             "frac": round(tf / peak, 4), "peak_source": src}
 
 
+def workload_config(wl, ws):
+    """The workload keys of the JSON line's config, shared by both arms."""
+    return {"workload": wl.name, "hidden": wl.H, "experts": wl.E, "top_k": wl.k,
+            "inter": wl.I, "shared": wl.n_shared, "tokens_per_step": wl.T,
+            "layers": wl.L, "weights": "mxfp4 e2m1+e8m0/32, shared bf16",
+            "parallelism": "replicas" if ws > 1 else "single-gpu"}
+
+
 def run_reference(args):
     ws, rank, local = dist_env()
     if rank != 0:
         return None
     wl = synth.WORKLOADS[args.config]
+    if args.tokens:
+        import dataclasses
+        wl = dataclasses.replace(wl, T=args.tokens, name=wl.name + "-t%d" % args.tokens)
     # each step: one token of the workload through the oracle (a bounded
     # sample of the workload: the oracle is per-token, so tokens/s carries over)
-    cpu_oracle_rate(wl, 0.0, max_tokens=max(args.warmup, 1))
+    # at most a minute of warm-up and two of timed tokens, so that the whole
+    # run ends within minutes at every workload
+    cpu_oracle_rate(wl, 60.0, max_tokens=max(args.warmup, 1))
     t0 = time.perf_counter()
-    rate, n, threads = cpu_oracle_rate(wl, 0.0, max_tokens=args.steps)
+    rate, n, threads = cpu_oracle_rate(wl, REF_TIMED_SECONDS, max_tokens=args.steps)
     el = time.perf_counter() - t0
     value = n / el
     return {
@@ -572,10 +584,12 @@ def run_reference(args):
         "ms_per_step": round(el / n * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
-        "config": {"workload": wl.name, "tokens_per_step": 1, "layers": wl.L},
+        "config": workload_config(wl, ws),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads,
                          "kind": "oracle",
-                         "sample": "%d tokens of %s, one per step" % (n, wl.name)},
+                         "sample": "%d tokens of %s (%d of %d steps within the %d s cap), one "
+                                   "token through the oracle per step (its cost is per token)"
+                                   % (n, wl.name, n, args.steps, REF_TIMED_SECONDS)},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
