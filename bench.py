@@ -132,13 +132,16 @@ def csrc_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel):
+def recorded_traffic(kernel, wl):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
-    kernel sources have not changed since it was captured; else None."""
+    kernel sources have not changed since it was captured and a launch of
+    workload `wl` does the captured launch's work (same tokens a layer and
+    experts); else None."""
     try:
         d = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
         rec = d.get(kernel)
-        if rec and rec.get("csrc_hash") == csrc_hash():
+        if (rec and rec.get("csrc_hash") == csrc_hash() and rec.get("tokens") == wl.T
+                and rec.get("experts") == wl.E and rec.get("hidden") == wl.H):
             return rec["dram_bytes_per_launch"]
     except Exception:
         pass
@@ -522,7 +525,7 @@ def run_ours(args):
                      "achieved": round(dom_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(dom_gbs / peak, 4), "peak_source": peak_kind,
                      "bytes_per_launch": int(dom_bytes),
-                     "traffic": recorded_traffic(dom)},
+                     "traffic": recorded_traffic(dom, wl)},
         "kernels": kernels,
         "tensor": tensor_use(kt, wl, T),
         "e2e": {"value": round(e2e_tokens / e2e_max, 2), "unit": UNIT,
