@@ -124,14 +124,18 @@ DF_MOE_API int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe**
  * layer's experts live in pinned host memory (the Grace side, reached over
  * NVLink-C2C) and only `cache_slots` of them a layer in HBM. Each forward
  * layer brings its selection to the host (one synchronisation: forward is
- * synchronous on its stream), copies the selected experts that are not
- * cached into free or least recently used slots (one cudaMemcpyAsync each)
- * and runs the decode kernels on the slots. Consecutive tokens that reuse
- * experts find them cached (the Deltafin README, "Techniques", and the
- * kimi-k3-in-c blog's expert LRU cache stream experts from SSD with the same
- * reuse). Limits: max_tokens <= 8, no DF_MOE_FUSED_DECODE,
+ * synchronous on its stream), gives the selected experts that are not
+ * cached free or least recently used slots, copies them in with one fill
+ * kernel (SM loads of the mapped host pool) and runs the decode kernels on
+ * the slots. A call whose experts are all cached copies nothing.
+ * Consecutive tokens that reuse experts find them cached (the Deltafin
+ * README, "Techniques", and the kimi-k3-in-c blog's expert LRU cache stream
+ * experts from SSD with the same reuse). The library owns the pinned pool
+ * (n_layers * n_experts spans) and frees it in df_moe_destroy; load_experts
+ * fills it. Limits: max_tokens <= 8, no DF_MOE_FUSED_DECODE,
  * min(max_tokens*top_k, n_experts) <= cache_slots <= n_experts; no graphs
- * and no single expert steps on such a handle. Errors as df_moe_create. */
+ * and no single expert steps on such a handle. Errors as df_moe_create
+ * (ENOMEM also when the pinned pool cannot be allocated). */
 DF_MOE_API int df_moe_create_cached(const df_moe_config* cfg, int cuda_device,
                                     int32_t cache_slots, df_moe** out);
 /* Since creation: selected experts found cached, experts copied in, and the
