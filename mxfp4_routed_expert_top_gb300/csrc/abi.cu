@@ -833,7 +833,9 @@ int df_moe_load_experts(df_moe* h, int32_t layer, const df_moe_layer_weights* w,
     if (w->expert_begin < 0 || w->expert_begin + w->expert_count > c.n_experts)
       return fail(h, DF_MOE_ERANGE, "experts [%d, %d) out of range", w->expert_begin,
                   w->expert_begin + w->expert_count);
-    uint8_t* dst = L.arena + (size_t)w->expert_begin * h->span_bytes;
+    // without a cache the spans go to their home in the arena (with one, the
+    // arena holds only slots)
+    uint8_t* dst = h->cache_slots ? nullptr : L.arena + (size_t)w->expert_begin * h->span_bytes;
     if (h->cache_slots) {
       // repacked on the device in chunks of 8 spans, then kept in the pinned
       // host pool; the HBM slots fill on demand

@@ -41,6 +41,9 @@ phase_gateup_kernel(const BfvArgs sh, const MxvArgs rt_in, const SelArgs sel, in
   __shared__ int32_t sel_sorted[32];
   __shared__ int32_t sel_n;
   if ((int)blockIdx.x < n_sh) {
+    // x is complete without a wait: the router triggers its dependents only
+    // after its own wait, and each later kernel starts only after the one
+    // before it has triggered
     bfv_cta<0, TT>(sh, smem, bars, blockIdx.x, n_sh, /*wait=*/false);
     return;
   }

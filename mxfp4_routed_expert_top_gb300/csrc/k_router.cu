@@ -63,8 +63,6 @@ router_kernel(const float* __restrict__ Wr, int E, int H,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * kRouterRowsPerBlock + warp;
   const int split = blockIdx.y;
-  // the expert kernels may be set up once every router CTA has started
-  pdl_launch_dependents();
   const int k0 = split * split_len;
   const int len = min(split_len, H - k0);
   // each pass's slice of x, [NT][split_len] bf16, is staged in shared
@@ -82,6 +80,12 @@ router_kernel(const float* __restrict__ Wr, int E, int H,
   // x and the outputs' readers come from the preceding kernels; the weights
   // (read above) do not
   pdl_wait();
+  // The next kernel may start now. Triggering only after the wait makes the
+  // start of any later kernel of the chain (each starts only after the one
+  // before it has triggered) imply that x is complete: the decode phase
+  // kernels' shared-expert CTAs read x without waiting, and x may come from
+  // the kernel before this one (the stack's RMSNorm, which triggers early).
+  pdl_launch_dependents();
   const int q8 = len >> 3;  // 8 bf16 a copy (len is a multiple of 32)
   for (int t0 = 0; t0 < T; t0 += NT) {
     const int nt = min(NT, T - t0);
@@ -158,6 +162,7 @@ topk_kernel(const float* __restrict__ part, int nsplit, int T, int E, int k,
   __shared__ float cand_v[kTopkThreads];
   __shared__ int cand_e[kTopkThreads];
   // the next kernel may start now: it waits for this grid before it reads
+  // (and this grid started only after the router had passed its own wait)
   pdl_launch_dependents();
   pdl_wait();  // the router's partial logits
   const int t = blockIdx.x;
