@@ -79,7 +79,8 @@ phase_gateup_kernel(const BfvArgs sh, const MxvArgs rt_in, const SelArgs sel, in
         if (pub) *const_cast<int32_t*>(rt_in.n_items) = sel.k;
       }
       // the down phase reads the published selection as soon as it starts,
-      // which is after every CTA of this grid has passed mxv_cta's trigger
+      // which is after every CTA of this grid has exited (the gate/up phase
+      // triggers its dependent only implicitly)
       if (pub) __threadfence();
     }
     rt.items = sel_items;
