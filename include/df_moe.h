@@ -64,8 +64,9 @@ extern "C" {
 #define DF_MOE_STACK_RMSNORM_RESIDUAL 1u
 /* Decode batches (T <= 8) run as one persistent cooperative launch per layer
  * (router, selection, routed and shared experts and the combine in a single
- * kernel) instead of the default chain of kernels on two streams. Same
- * results within the stated tolerances. */
+ * kernel) instead of the default chain of kernels on the caller's stream
+ * (router, gate/up phase, down phase, combine). Same results within the
+ * stated tolerances. */
 #define DF_MOE_FUSED_DECODE 2u
 /* Batches above the decode range (T > 8) run the routed experts on the
  * register-fragment (mma.sync) kernels of the decode chain instead of the

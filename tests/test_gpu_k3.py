@@ -29,8 +29,9 @@ def torch():
     return t
 
 
-# every test runs on both decode paths: the default chain of kernels (shared
-# experts on a second stream) and the fused single-launch layer kernel
+# every test runs on both decode paths: the default chain of kernels (routed
+# and shared experts side by side in two phase kernels) and the fused
+# single-launch layer kernel
 @pytest.fixture(scope="module", params=["chain", "fused"])
 def k3(torch, request):
     s = Setup(WL1, max_tokens=512, fused=request.param == "fused")
