@@ -272,3 +272,28 @@ def test_k_equals_e_and_no_shared(tiny, torch):
     ref = orc.moe_layer(L, x)
     check_ids_weights(ids[0], w[0], ref["ids"], ref["w"])
     check_out(out32, ref["out"])
+
+
+@pytest.mark.parametrize("T", [1, 2])
+def test_one_token_selects_in_the_gateup_phase(tiny, torch, T):
+    """One token: the gate/up phase kernel selects the experts itself (no
+    top-k or grouping launch); two and more take the top-k and grouping
+    kernels. Both against the oracle, with the ids and weights the
+    selection publishes."""
+    x = draw_tokens(tiny, T, first_id=12000 + 10 * T)
+    out32 = torch.empty((T, WL.H), dtype=torch.float32, device="cuda")
+    out = torch.empty((T, WL.H), dtype=torch.int16, device="cuda")
+    ids = torch.empty((T, WL.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, WL.k), dtype=torch.float32, device="cuda")
+    tiny.m.timing_enable(True)
+    tiny.m.timing_reset()
+    tiny.m.forward(to_dev_bf16(x), T, out, ids, w, out_f32=out32)
+    tiny.m.sync()
+    kinds = tiny.m.timing()
+    tiny.m.timing_enable(False)
+    separate = 0 if T == 1 else 1
+    assert kinds["topk"][0] == separate and kinds["group"][0] == separate
+    assert kinds["expert_gateup"][0] == 1
+    ref = orc.moe_layer(tiny.layers[0], x)
+    check_ids_weights(ids.cpu().numpy(), w.cpu().double().numpy(), ref["ids"], ref["w"])
+    check_out(out32.cpu().double().numpy(), ref["out"])
