@@ -442,8 +442,20 @@ int cache_plan(df_moe* h, int l, int T, const int32_t* ids, cudaStream_t s) {
     ++h->cache_misses;
     h->cache_bytes += (int64_t)h->span_bytes;
   }
-  if (nfill)
-    RUN(h, K_CACHE_FILL, s, launch_cache_fill(h->fill_d, nfill, h->span_bytes, L.span_tab, s));
+  if (nfill) {
+    const int rc = run(h, K_CACHE_FILL, s, [&]() {
+      return launch_cache_fill(h->fill_d, nfill, h->span_bytes, L.span_tab, s);
+    });
+    if (rc) {
+      // nothing was copied: this call's experts leave their slots again
+      for (int i = 0; i < nfill; ++i) {
+        const int e = (int)h->fill_h[i].e;
+        if (L.slot_of[e] >= 0) L.expert_of[L.slot_of[e]] = -1;
+        L.slot_of[e] = -1;
+      }
+      return rc;
+    }
+  }
   return DF_MOE_OK;
 }
 
