@@ -67,3 +67,24 @@ def test_two_gloo_ranks():
     assert ref0["config"]["parallelism"] == "replicas"
     assert ref0["cpu_baseline"]["kind"] == "oracle" and ref0["value"] > 0
     assert ref0["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_line_keys(monkeypatch):
+    """The reference arm's JSON line carries every key of the bench contract
+    (single process: rank 0 runs it)."""
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    ref = bench.run_reference(argparse.Namespace(config=0, steps=3, warmup=1, tokens=0))
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "impl", "cpu_baseline", "e2e"):
+        assert key in ref, key
+    assert ref["impl"] == "reference" and ref["n_gpus"] == 1 and ref["steps"] == 3
+    assert ref["metric"] == bench.METRIC and ref["unit"] == bench.UNIT
+    assert ref["config"]["workload"] == "tiny-h256-e8-top2"
+    assert ref["config"]["parallelism"] == "single-gpu"
+    assert ref["e2e"]["unit"] == bench.UNIT and ref["e2e"]["value"] == ref["value"]
+    assert "3 tokens" in ref["cpu_baseline"]["sample"]  # every requested step timed
