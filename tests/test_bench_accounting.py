@@ -1,8 +1,8 @@
 """The roofline numerators: the bench's algorithmic byte counts against the
 closed forms of the K3 layer. MXFP4 costs 17/32 B a weight (4 bits plus one
 8-bit scale per 32 weights; kimi-k3-in-c blog, section 先把账算明白), so a
-SwiGLU expert of 3 x 7168 x 1536 weights is
-17,547,264 B, two thirds of it gate and up. The router is fp32 [896][7168];
+SwiGLU expert of 3 x 7168 x 1536 weights is 17,547,264 B, two thirds of it
+gate and up. The router is fp32 [896][7168];
 the two shared experts are bf16 SwiGLU FFNs of intermediate 1536.
 """
 import os
