@@ -8,7 +8,7 @@ token. L2 is flushed (a 256 MiB write) before every timed step, outside the
 timed events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--config 1|2|3|4] [--tokens T] [--graph | --fused]
+                  [--config 1|2|3|4] [--tokens T] [--graph]
                   [--cache-slots N [--token-corr RHO]] [--no-cpu-baseline]
 
 Prints one JSON line on rank 0. Under torchrun (N > 1) every rank runs an
@@ -54,8 +54,6 @@ def parse():
     p.add_argument("--tokens", type=int, default=0,
                    help="override the tokens per step of the workload (the stack "
                         "workload decodes at batch 1 and batch 4)")
-    p.add_argument("--fused", action="store_true",
-                   help="decode batches as one fused layer launch (DF_MOE_FUSED_DECODE)")
     p.add_argument("--graph", action="store_true",
                    help="replay the forward pass as one CUDA graph (df_moe_graph_*); each "
                         "step's token is copied into the graph's input buffer before the "
@@ -305,7 +303,7 @@ def run_ours(args):
     if args.tokens:
         wl = dataclasses.replace(wl, T=args.tokens, name=wl.name + "-t%d" % args.tokens)
     T = wl.T
-    flags = ((dfm.STACK_RMSNORM_RESIDUAL if wl.stack else 0) | (dfm.FUSED_DECODE if args.fused else 0)
+    flags = ((dfm.STACK_RMSNORM_RESIDUAL if wl.stack else 0)
              | (dfm.PREFILL_MMA_SYNC if args.mma_sync_prefill else 0))
     if args.cache_slots and T > 8:
         raise SystemExit("--cache-slots serves decode batches (<= 8 tokens)")
@@ -481,11 +479,9 @@ def run_ours(args):
     peak, peak_kind = measured_peaks()
     ms = dev_s_max / args.steps * 1e3
     lb = layer_bytes(wl, u_mean, T) * wl.L
-    # dominant kernel: the fused layer kernel (decode batches), the routed
-    # gate/up GEMM (tcgen05, larger batches), else the routed gate/up GEMV
-    if kt.get("layer", (0, 0.0))[0]:
-        dom, dom_bytes = "layer", layer_bytes(wl, u_mean, T)
-    elif kt.get("gemm_gateup", (0, 0.0))[0]:
+    # dominant kernel: the routed gate/up GEMM (tcgen05, larger batches),
+    # else the gate/up phase of decode batches
+    if kt.get("gemm_gateup", (0, 0.0))[0]:
         dom, dom_bytes = "gemm_gateup", gateup_bytes(wl, u_mean, T)
     else:
         # decode batches: the gate/up phase kernel streams the routed and the
@@ -505,7 +501,6 @@ def run_ours(args):
         "impl": "ours",
         "config": {**workload_config(wl, ws),
                    "l2": "flushed (256 MiB write) before every timed step",
-                   "decode_path": "fused" if args.fused else "chain",
                    "launch": "cuda graph" if args.graph else "stream",
                    "prefill_path": "mma_sync" if args.mma_sync_prefill else "tcgen05",
                    "experts_home": ("pinned host memory, %d a layer cached in HBM"

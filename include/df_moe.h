@@ -62,12 +62,7 @@ extern "C" {
  * rounded to bf16; after it the layer output is added to x and rounded to
  * bf16. `out` is the final x. */
 #define DF_MOE_STACK_RMSNORM_RESIDUAL 1u
-/* Decode batches (T <= 8) run as one persistent cooperative launch per layer
- * (router, selection, routed and shared experts and the combine in a single
- * kernel) instead of the default chain of kernels on the caller's stream
- * (router, gate/up phase, down phase, combine). Same results within the
- * stated tolerances. */
-#define DF_MOE_FUSED_DECODE 2u
+/* Flag bit 2u is reserved: create rejects it as an unknown flag. */
 /* Batches above the decode range (T > 8) run the routed experts on the
  * register-fragment (mma.sync) kernels of the decode chain instead of the
  * default grouped GEMMs on the 5th-generation tensor cores (tcgen05, fp32
@@ -87,8 +82,7 @@ typedef struct {
   int32_t n_layers;     /* L >= 1                                              */
   int32_t max_tokens;   /* largest T a forward call may use (1..4096)          */
   float rms_eps;        /* stack mode only                                     */
-  uint32_t flags;       /* DF_MOE_STACK_RMSNORM_RESIDUAL | DF_MOE_FUSED_DECODE |
-                           DF_MOE_PREFILL_MMA_SYNC                              */
+  uint32_t flags;       /* DF_MOE_STACK_RMSNORM_RESIDUAL | DF_MOE_PREFILL_MMA_SYNC */
 } df_moe_config;
 
 /* Weights of one layer, any subset per call (NULL / 0 = leave unchanged). */
@@ -133,7 +127,7 @@ DF_MOE_API int df_moe_create(const df_moe_config* cfg, int cuda_device, df_moe**
  * README, "Techniques", and the kimi-k3-in-c blog's expert LRU cache stream
  * experts from SSD with the same reuse). The library owns the pinned pool
  * (n_layers * n_experts spans) and frees it in df_moe_destroy; load_experts
- * fills it. Limits: max_tokens <= 8, no DF_MOE_FUSED_DECODE,
+ * fills it. Limits: max_tokens <= 8,
  * min(max_tokens*top_k, n_experts) <= cache_slots <= n_experts; no graphs
  * and no single expert steps on such a handle. Errors as df_moe_create
  * (ENOMEM also when the pinned pool cannot be allocated). */
@@ -208,8 +202,7 @@ DF_MOE_API int df_moe_sync(df_moe* h, void* stream);
  * the pointers. Arguments as df_moe_forward; the capture runs on a stream of
  * the handle's own, so `stream` may be any stream (the legacy default one
  * included) and nothing is enqueued on it.
- * Not with DF_MOE_FUSED_DECODE (the layer kernel's flags need a fresh epoch
- * each call: EINVAL) nor with timing on (EINVAL). The graph holds no
+ * Not with timing on (EINVAL). The graph holds no
  * reference to the handle's host state: destroy it before the handle. */
 typedef struct df_moe_graph df_moe_graph; /* opaque */
 DF_MOE_API int df_moe_graph_create(df_moe* h, const void* x_bf16, int32_t T,

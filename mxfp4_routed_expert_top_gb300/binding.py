@@ -13,7 +13,6 @@ LIB_PATH = os.path.join(PKG, "libdfmoe.so")
 
 OK, EINVAL, ENOMEM, ECUDA, ESTATE, ERANGE, ETIMEOUT, EDEVICE = 0, -1, -2, -3, -4, -5, -6, -7
 STACK_RMSNORM_RESIDUAL = 1
-FUSED_DECODE = 2
 PREFILL_MMA_SYNC = 4
 KERNEL_KINDS = 16
 

@@ -24,11 +24,6 @@ struct LayerBufs {
   uint16_t* sh_gate = nullptr;  // [n_s*Is][H]
   uint16_t* sh_up = nullptr;    // [n_s*Is][H]
   uint16_t* sh_down = nullptr;  // [H][n_s*Is]
-  // shared experts as f16 fragment tiles with row scales (layer kernel)
-  uint4* sh_gu16 = nullptr;     // [n_s][Is/8][H/16][32]
-  float* sh_gu_rs = nullptr;    // [n_s][Is/8][16]
-  uint4* sh_dn16 = nullptr;     // [n_s][H/16][Is/16][32]
-  float* sh_dn_rs = nullptr;    // [n_s][H]
   uint8_t* eref = nullptr;      // [E][2I + H] row reference exponents (tcgen05 GEMMs)
   ChunkMap map_gu{}, map_dn{};  // tensor maps of the arena's tiles (tcgen05 GEMMs)
   SharedMaps sh_maps{};         // shared experts as dense tcgen05 GEMMs (batches)
@@ -54,7 +49,7 @@ struct Pending {
 const char* kKindNames[K_NKINDS] = {"router", "topk", "group", "expert_gateup",
                                     "expert_down", "combine", "shared_gateup",
                                     "shared_down", "rmsnorm", "residual",
-                                    "repack", "other", "layer", "gemm_gateup",
+                                    "repack", "other", "reserved", "gemm_gateup",
                                     "gemm_down", "cache_fill"};
 
 }  // namespace
@@ -82,20 +77,6 @@ struct df_moe {
   uint16_t* xn = nullptr;        // [Tmax][H]
   uint32_t* err = nullptr;       // device error word
   unsigned int* counter = nullptr;  // router blocks done (zero between calls)
-  // layer kernel (decode batches, T <= kLayerMaxT)
-  int lk_T = 0;                  // largest T it serves (0: not available)
-  int lk_max_items = 0;
-  int lk_ks_rt = 1, lk_ks_gu = 1, lk_ks_sg = 1, lk_ks_dn = 1, lk_hf_groups = 0;
-  float* lk_logit_part = nullptr;
-  float2* lk_cand = nullptr;
-  float4* lk_gu_part = nullptr;
-  float4* lk_sg_part = nullptr;
-  float* lk_hsh32 = nullptr;
-  uint4* lk_hf = nullptr;
-  float* lk_hsc = nullptr;
-  uint32_t* lk_sync = nullptr;
-  SyncLayout lk_sl{};
-  uint32_t epoch = 0;
   // tcgen05 GEMMs for batches above the decode range
   bool gemm = false;
   uint16_t* g_xg = nullptr;      // [Tmax*k][H] f16: gate/up B rows in expert order
@@ -244,7 +225,7 @@ int route(df_moe* h, int l, const uint16_t* x, int T, int32_t* ids, float* w,
     return DF_MOE_OK;
   }
   int nsplit = h->rsplit.nsplit;
-  if (T > kLayerMaxT) {
+  if (T > kDecodeMaxT) {
     // a batch: the logits as one tiled GEMM (weights read once for all tokens)
     int used = -1;
     RUN(h, K_ROUTER, s, (used = launch_router_gemm(L.router, c.n_experts, c.hidden, x, T,
@@ -271,7 +252,7 @@ int route(df_moe* h, int l, const uint16_t* x, int T, int32_t* ids, float* w,
 // T = 1). Above the decode range the grouped tcgen05 GEMMs run them, unless
 // the handle asks for the register-fragment kernels.
 bool use_gemm(const df_moe* h, int T, int tg) {
-  return h->gemm && T > kLayerMaxT && tg == kOneItemPerExpert;
+  return h->gemm && T > kDecodeMaxT && tg == kOneItemPerExpert;
 }
 
 int expert_gateup(df_moe* h, int l, const uint16_t* x, int T, int max_items, int tg,
@@ -316,7 +297,7 @@ int shared_part(df_moe* h, int l, const uint16_t* x, int T, float* ysh,
                 cudaStream_t s, int max_ctas = 0) {
   const df_moe_config& c = h->cfg;
   const LayerBufs& L = h->layers[l];
-  if (T > kLayerMaxT && L.sh_maps_ok && ((uintptr_t)x & 15) == 0) {
+  if (T > kDecodeMaxT && L.sh_maps_ok && ((uintptr_t)x & 15) == 0) {
     // a batch: two dense GEMMs on the tensor cores
     RUN(h, K_SHARED_GU, s, launch_shared_gemm_gateup(L.sh_maps, x, T, c.hidden, h->R, h->s_hh,
                                                      h->err, s));
@@ -327,61 +308,6 @@ int shared_part(df_moe* h, int l, const uint16_t* x, int T, float* ysh,
                                               c.hidden, x, T, h->hsh, h->err, s, max_ctas));
   RUN(h, K_SHARED_DN, s, launch_shared_down(L.sh_down, c.hidden, h->R, h->hsh,
                                             T, ysh, h->err, s, max_ctas));
-  return DF_MOE_OK;
-}
-
-// One MoE layer: out = residual + routed + shared.
-// The whole layer as one cooperative launch (T <= lk_T).
-int layer_kernel_forward(df_moe* h, int l, const uint16_t* x, int T,
-                         const uint16_t* residual, uint16_t* out_bf16, float* out_f32,
-                         int32_t* ids, float* w, cudaStream_t s) {
-  const df_moe_config& c = h->cfg;
-  const LayerBufs& L = h->layers[l];
-  LayerKernelArgs a{};
-  a.H = c.hidden;
-  a.E = c.n_experts;
-  a.k = c.top_k;
-  a.I = c.inter;
-  a.Is = c.n_shared > 0 ? c.shared_inter : 0;
-  a.n_shared = c.n_shared;
-  a.T = T;
-  a.max_items = std::min(T * c.top_k, c.n_experts);
-  a.ks_rt = h->lk_ks_rt;
-  a.ks_gu = h->lk_ks_gu;
-  a.ks_sg = h->lk_ks_sg;
-  a.ks_dn = h->lk_ks_dn;
-  a.Wr = L.router;
-  a.arena = L.arena;
-  a.span_bytes = h->span_bytes;
-  a.sh_gu = L.sh_gu16;
-  a.sh_gu_rs = L.sh_gu_rs;
-  a.sh_dn = L.sh_dn16;
-  a.sh_dn_rs = L.sh_dn_rs;
-  a.x = x;
-  a.residual = residual;
-  a.out_f32 = out_f32;
-  a.out_bf16 = out_bf16;
-  a.ids = ids;
-  a.w = w;
-  a.logit_part = h->lk_logit_part;
-  a.cand = h->lk_cand;
-  a.items = h->items;
-  a.n_items = h->n_items;
-  a.sorted = h->sorted;
-  a.gu_part = h->lk_gu_part;
-  a.sg_part = h->lk_sg_part;
-  a.h32 = h->hbuf;
-  a.hsh32 = h->lk_hsh32;
-  a.hf = h->lk_hf;
-  a.hf_groups = h->lk_hf_groups;
-  a.hsc = h->lk_hsc;
-  a.part = h->part;
-  a.sync = h->lk_sync;
-  a.sl = h->lk_sl;
-  if (++h->epoch == 0) h->epoch = 1;  // flags hold the epoch; 0 is "never set"
-  a.epoch = h->epoch;
-  a.err = h->err;
-  RUN(h, K_LAYER, s, launch_layer(a, s));
   return DF_MOE_OK;
 }
 
@@ -464,12 +390,10 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
                   int32_t* ids, float* w, cudaStream_t s) {
   const df_moe_config& c = h->cfg;
   const LayerBufs& L = h->layers[l];
-  if (T <= h->lk_T && layer_kernel_supports(c.hidden, T, c.top_k, c.n_experts))
-    return layer_kernel_forward(h, l, x, T, residual, out_bf16, out_f32, ids, w, s);
   const int tg = T == 1 ? 1 : kOneItemPerExpert;
   const int max_items = (T == 1 && tg == 1) ? c.top_k : std::min(T * c.top_k, c.n_experts);
   const int R = c.n_shared > 0 ? h->R : 0;
-  const bool phase = T <= kLayerMaxT && h->phase;
+  const bool phase = T <= kDecodeMaxT && h->phase;
   const bool cached = h->cache_slots > 0;
   int sh_gu = 0, sh_dn = 0;
   if (phase && R > 0) {
@@ -595,16 +519,14 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
                 "max_tokens must be in [1, 4096] with max_tokens*top_k <= 65535");
   if (c.n_layers > 1 && !(c.flags & DF_MOE_STACK_RMSNORM_RESIDUAL))
     return fail(nullptr, DF_MOE_EINVAL, "n_layers > 1 needs DF_MOE_STACK_RMSNORM_RESIDUAL");
-  if ((c.flags & ~(DF_MOE_STACK_RMSNORM_RESIDUAL | DF_MOE_FUSED_DECODE |
-                   DF_MOE_PREFILL_MMA_SYNC)) != 0)
+  if ((c.flags & ~(DF_MOE_STACK_RMSNORM_RESIDUAL | DF_MOE_PREFILL_MMA_SYNC)) != 0)
     return fail(nullptr, DF_MOE_EINVAL, "unknown flags");
   if ((c.flags & DF_MOE_STACK_RMSNORM_RESIDUAL) && !(c.rms_eps >= 0.0f))
     return fail(nullptr, DF_MOE_EINVAL, "rms_eps must be >= 0");
   if (slots) {
-    if (c.max_tokens > kLayerMaxT || (c.flags & DF_MOE_FUSED_DECODE))
+    if (c.max_tokens > kDecodeMaxT)
       return fail(nullptr, DF_MOE_EINVAL,
-                  "an expert cache serves decode batches (max_tokens <= %d, no fused layer)",
-                  kLayerMaxT);
+                  "an expert cache serves decode batches (max_tokens <= %d)", kDecodeMaxT);
     if (slots < std::min(c.max_tokens * c.top_k, c.n_experts) || slots > c.n_experts)
       return fail(nullptr, DF_MOE_EINVAL,
                   "cache_slots must be in [min(max_tokens*top_k, n_experts), n_experts]");
@@ -660,13 +582,9 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
     if (!rc && R) rc = dalloc(h, &L.sh_gate, R * H);
     if (!rc && R) rc = dalloc(h, &L.sh_up, R * H);
     if (!rc && R) rc = dalloc(h, &L.sh_down, H * R);
-    if (!rc && R) rc = dalloc(h, &L.sh_gu16, (size_t)c.n_shared * (c.shared_inter / 8) * (H / 16) * 32);
-    if (!rc && R) rc = dalloc(h, &L.sh_gu_rs, (size_t)c.n_shared * (c.shared_inter / 8) * 16);
-    if (!rc && R) rc = dalloc(h, &L.sh_dn16, (size_t)c.n_shared * (H / 16) * (c.shared_inter / 16) * 32);
-    if (!rc && R) rc = dalloc(h, &L.sh_dn_rs, (size_t)c.n_shared * H);
   }
   // tcgen05 GEMMs: batches above the decode range, unless asked otherwise
-  h->gemm = !slots && Tm > (size_t)kLayerMaxT && !(c.flags & DF_MOE_PREFILL_MMA_SYNC) &&
+  h->gemm = !slots && Tm > (size_t)kDecodeMaxT && !(c.flags & DF_MOE_PREFILL_MMA_SYNC) &&
             gemm_supported(c.hidden, c.inter);
   if (h->gemm) {
     for (int l = 0; l < c.n_layers && !rc; ++l) {
@@ -698,34 +616,8 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
   if (!rc) rc = dalloc(h, &h->items, Tm * k);
   if (!rc) rc = dalloc(h, &h->n_items, 1);
   if (!rc) rc = dalloc(h, &h->sorted, Tm * k);
-  // layer kernel: used for T <= min(max_tokens, kLayerMaxT) when the device
-  // can hold its cooperative grid
-  const size_t T8 = std::min<size_t>(Tm, kLayerMaxT);
-  const size_t Is = c.n_shared > 0 ? (size_t)c.shared_inter : 0;
-  if (!rc && (c.flags & DF_MOE_FUSED_DECODE) && layer_kernel_grid() > 0) {
-    h->lk_T = (int)T8;
-    h->lk_max_items = (int)std::min<size_t>(T8 * k, E);
-    h->lk_ks_rt = std::max(1, std::min(8, (int)(H / 896)));
-    h->lk_ks_gu = std::min(8, std::max(1, (int)(H / 64) / 14));
-    h->lk_ks_dn = (I / 64) % 2 == 0 && I / 64 >= 8 ? 2 : 1;
-    h->lk_ks_sg = std::min(8, std::max(1, (int)(H / 64) / 14));
-    h->lk_hf_groups = (int)std::max<size_t>(I, Is) / 64;
-    const size_t nd = (size_t)h->lk_max_items + c.n_shared;
-    h->lk_sl = sync_layout(h->lk_max_items, c.n_shared, (int)H, (int)I, (int)Is);
-    rc = dalloc(h, &h->lk_logit_part, (size_t)h->lk_ks_rt * T8 * E);
-    if (!rc) rc = dalloc(h, &h->lk_cand, T8 * ((E + kRouterBlock - 1) / kRouterBlock) * kRouterBlock);
-    if (!rc) rc = dalloc(h, &h->lk_gu_part, (size_t)h->lk_max_items * (I / 8) * h->lk_ks_gu * 32);
-    if (!rc && Is) rc = dalloc(h, &h->lk_sg_part, (size_t)c.n_shared * (Is / 8) * h->lk_ks_sg * 32);
-    if (!rc && Is) rc = dalloc(h, &h->lk_hsh32, (size_t)c.n_shared * T8 * Is);
-    if (!rc) rc = dalloc(h, &h->lk_hf, nd * 2 * h->lk_hf_groups * 2 * 32);
-    if (!rc) rc = dalloc(h, &h->lk_hsc, nd * kLayerMaxT);
-    if (!rc) rc = dalloc(h, &h->lk_sync, h->lk_sl.total);
-    if (!rc && cudaMemset(h->lk_sync, 0, h->lk_sl.total * sizeof(uint32_t)) != cudaSuccess)
-      rc = fail(h, DF_MOE_ECUDA, "cudaMemset failed");
-  }
   if (!rc) rc = dalloc(h, &h->hbuf, Tm * k * I);
-  if (!rc) rc = dalloc(h, &h->part, std::max(Tm * k, (size_t)h->lk_ks_dn * T8 * k +
-                                                          (size_t)c.n_shared * T8) * H);
+  if (!rc) rc = dalloc(h, &h->part, Tm * k * H);
   if (!rc && R) rc = dalloc(h, &h->hsh, Tm * R);
   if (!rc) rc = dalloc(h, &h->ysh, Tm * H);
   if (!rc) rc = dalloc(h, &h->xbuf[0], Tm * H);
@@ -832,12 +724,6 @@ int df_moe_load_experts(df_moe* h, int32_t layer, const df_moe_layer_weights* w,
     CUDA_OR_FAIL(h, cudaMemcpy2DAsync(L.sh_down + sidx * Is, h->R * sizeof(uint16_t),
                                       d, Is * sizeof(uint16_t), Is * sizeof(uint16_t),
                                       H, kind, s));
-    RUN(h, K_REPACK, s, launch_pack_shared(L.sh_gate + sidx * Is * H, L.sh_up + sidx * Is * H,
-                                           L.sh_down + sidx * Is, h->R, (int)H, (int)Is,
-                                           L.sh_gu16 + (size_t)sidx * (Is / 8) * (H / 16) * 32,
-                                           L.sh_gu_rs + (size_t)sidx * (Is / 8) * 16,
-                                           L.sh_dn16 + (size_t)sidx * (H / 16) * (Is / 16) * 32,
-                                           L.sh_dn_rs + (size_t)sidx * H, s));
     L.shared_loaded[sidx] = 1;
   }
   if (w->expert_count > 0) {
@@ -1032,9 +918,6 @@ int df_moe_sync(df_moe* h, void* stream) {
   CUDA_OR_FAIL(h, cudaMemcpy(&e, h->err, 4, cudaMemcpyDeviceToHost));
   if (e) {
     CUDA_OR_FAIL(h, cudaMemset(h->err, 0, 4));
-    // a layer-kernel call that gave up leaves its tickets mid-count
-    if (h->lk_sync)
-      CUDA_OR_FAIL(h, cudaMemset(h->lk_sync, 0, h->lk_sl.total * sizeof(uint32_t)));
     if (e & DEV_ERR_TIMEOUT)
       return fail(h, DF_MOE_ETIMEOUT, "a bounded device wait gave up");
     return fail(h, DF_MOE_EDEVICE, "device-side check failed (0x%x)", e);
@@ -1250,8 +1133,6 @@ int df_moe_graph_create(df_moe* h, const void* x_bf16, int32_t T, const void* re
                         df_moe_graph** out) {
   if (!h || !out) return fail(h, DF_MOE_EINVAL, "null handle or output");
   *out = nullptr;
-  if (h->cfg.flags & DF_MOE_FUSED_DECODE)
-    return fail(h, DF_MOE_EINVAL, "graphs need the kernel chain (no DF_MOE_FUSED_DECODE)");
   if (h->timing) return fail(h, DF_MOE_EINVAL, "turn timing off before capturing a graph");
   if (h->cache_slots)
     return fail(h, DF_MOE_EINVAL, "an expert cache plans each layer on the host: no graphs");

@@ -63,7 +63,7 @@ constexpr int kOneItemPerExpert = 1 << 20;
 
 enum KernelKind {
   K_ROUTER = 0, K_TOPK, K_GROUP, K_GATEUP, K_DOWN, K_COMBINE, K_SHARED_GU,
-  K_SHARED_DN, K_RMSNORM, K_RESIDUAL, K_REPACK, K_OTHER, K_LAYER, K_GEMM_GU,
+  K_SHARED_DN, K_RMSNORM, K_RESIDUAL, K_REPACK, K_OTHER, K_LAYER_UNUSED, K_GEMM_GU,
   K_GEMM_DN, K_CACHE_FILL, K_NKINDS
 };
 
@@ -165,7 +165,11 @@ cudaError_t launch_shared_down(const uint16_t* down, int H, int K,
                                uint32_t* err, cudaStream_t s, int max_ctas = 0);
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps,
                            uint16_t* xn, cudaStream_t s);
-// Decode batches (T <= kLayerMaxT): routed and shared experts in two phase
+// Largest decode batch: up to this many tokens a call run as decode batches
+// (the phase kernels below); larger calls are batches (tcgen05 GEMMs).
+constexpr int kDecodeMaxT = 8;
+
+// Decode batches (T <= kDecodeMaxT): routed and shared experts in two phase
 // kernels on every SM (k_phase.cu). The gate/up phase follows the router
 // (T = 1: it selects the experts itself from the partial logits
 // router_part [nsplit][E], writing ids, w, items, n_items and sorted) or the
@@ -260,91 +264,5 @@ cudaError_t launch_shared_gemm_gateup(const SharedMaps& m, const uint16_t* x, in
 // y [T][H] = down (high + middle + low).
 cudaError_t launch_shared_gemm_down(const SharedMaps& m, int T, int H, int R, float* y,
                                     uint32_t* err, cudaStream_t s);
-
-// ---- the decode-batch layer kernel (k_layer.cu) -----------------------------
-// One persistent cooperative launch computes a whole MoE layer for T <= 8
-// tokens: every warp takes work units from a global queue in dependency order
-// (router, shared gate/up, routed gate/up, shared down, routed down),
-// and the units that finish a result hand it on by a ticket or an
-// epoch-valued flag.
-constexpr int kLayerMaxT = 8;
-
-// Word offsets of the synchronisation block. Tickets are zero between calls
-// (each is reset by the unit that takes its last value); flags hold the epoch
-// of the call that last set them.
-struct SyncLayout {
-  size_t queue, exit, t_rt, t_rtb, f_items, f_hp, t_item, t_rows, t_gu, t_sg, hmax, total;
-};
-constexpr int kRouterBlock = 32;  // experts per router block (one per lane)
-inline SyncLayout sync_layout(int max_items, int n_shared, int H, int I, int Is) {
-  SyncLayout L;
-  size_t o = 0;
-  L.queue = o++;
-  L.exit = o++;
-  L.t_rt = o++;                      // router blocks done
-  L.t_rtb = o; o += 1024 / kRouterBlock;  // router units done, per block
-  L.f_items = o++;
-  const size_t nd = (size_t)max_items + n_shared;  // down items
-  L.f_hp = o; o += nd;
-  L.t_item = o; o += nd;
-  L.t_rows = o; o += (size_t)H / 16;
-  L.t_gu = o; o += (size_t)max_items * (I / 8);
-  L.t_sg = o; o += (size_t)n_shared * (Is > 0 ? Is / 8 : 0);
-  L.hmax = o; o += nd * kLayerMaxT;
-  L.total = o;
-  return L;
-}
-
-struct LayerKernelArgs {
-  int H, E, k, I, Is, n_shared, T, max_items;
-  int ks_rt, ks_gu, ks_sg;   // K slices of router, routed and shared gate/up units
-  int ks_dn;                 // K parts of routed down units (1 or 2)
-  const float* Wr;           // [E][H]
-  const uint8_t* arena;      // E expert spans, fragment layout
-  size_t span_bytes;
-  const uint4* sh_gu;        // [n_shared][Is/8 tiles][H/16 k-steps][32 lanes]
-  const float* sh_gu_rs;     // [n_shared][Is/8][16] row scales
-  const uint4* sh_dn;        // [n_shared][H/16 tiles][Is/16 k-steps][32 lanes]
-  const float* sh_dn_rs;     // [n_shared][H]
-  const uint16_t* x;         // bf16 [T][H]
-  const uint16_t* residual;  // bf16 [T][H] or null
-  float* out_f32;            // [T][H] or null
-  uint16_t* out_bf16;        // [T][H] or null
-  int32_t* ids;              // [T][k]
-  float* w;                  // [T][k]
-  float* logit_part;         // [ks_rt][T][E]
-  float2* cand;              // [T][E/32 blocks][32]: (logit, id bits) of a block's best
-  Item* items;               // [max_items]
-  int32_t* n_items;
-  int32_t* sorted;           // [T*k]
-  float4* gu_part;           // [max_items * I/8][ks_gu][32]
-  float4* sg_part;           // [n_shared * Is/8][ks_sg][32]
-  float* h32;                // [T*k][I]
-  float* hsh32;              // [n_shared][T][Is]
-  uint4* hf;                 // [max_items + n_shared][2][hf_groups][2][32]
-  int hf_groups;             // max(I, Is) / 64
-  float* hsc;                // [max_items + n_shared][8]
-  float* part;               // [ks_dn*T*k + n_shared*T][H]
-  uint32_t* sync;
-  SyncLayout sl;
-  uint32_t epoch;
-  uint32_t* err;
-};
-size_t layer_kernel_smem(int H, int T);
-// Whether the layer kernel can run this shape (shared memory for its rings
-// and the routing merge).
-bool layer_kernel_supports(int H, int T, int k, int E);
-// Blocks per SM and grid of the cooperative launch (0 if it cannot run).
-int layer_kernel_grid();
-cudaError_t launch_layer(const LayerKernelArgs& a, cudaStream_t s);
-
-// Shared experts as f16 fragment tiles with a power-of-two scale per row
-// (k_layout.cu). gate/up/down: bf16 row-major of one shared expert;
-// down rows have `down_ld` elements (the row stride of the concatenated
-// down matrix).
-cudaError_t launch_pack_shared(const uint16_t* gate, const uint16_t* up,
-                               const uint16_t* down, int down_ld, int H, int Is,
-                               uint4* gu_out, float* gu_rs, uint4* dn_out,
-                               float* dn_rs, cudaStream_t s);
 
 }  // namespace dfm

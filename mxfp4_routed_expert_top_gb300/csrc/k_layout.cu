@@ -90,128 +90,4 @@ cudaError_t launch_repack_span(const uint8_t* src, uint8_t* dst, int n_spans,
   return cudaGetLastError();
 }
 
-
-
-// ---------------------------------------------------------------------------
-// Shared experts as f16 m16n8k16 A fragments.
-//
-// The shared-expert weights are bf16. The layer kernel multiplies them on the
-// tensor cores in f16, which holds every bf16 value exactly once the row is
-// scaled by a power of two that puts its largest magnitude in [2^14, 2^15):
-// f16 normals then cover 2^28 below the row maximum (with bf16's 8-bit
-// significand inside f16's 11), and smaller values keep an absolute error
-// below 2^-39 of the row maximum. The scale is applied back in fp32 after
-// the contraction.
-//
-// Tiles are 16 rows x K; k-step s of tile j is 32 lanes x 16 bytes, lane
-// l = 4g + t holding {(g, 16s+2t), (g, +1)}, {(g+8, 16s+2t), +1},
-// {(g, 16s+2t+8), +1}, {(g+8, 16s+2t+8), +1} as f16x2 (first column low).
-// gate/up tile j: rows 0-7 = gate rows 8j..8j+7, rows 8-15 = up rows
-// 8j..8j+7; down tile j: rows 16j..16j+15.
-// ---------------------------------------------------------------------------
-namespace {
-
-__device__ inline float bf16_val(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
-
-// Exponent sc of the power-of-two row scale (largest |w| in [2^14, 2^15) after
-// multiplying by 2^-sc); 0 for an all-zero row.
-__device__ inline int row_scale_exp(float m) {
-  if (!(m > 0.f)) return 0;
-  const int e = (int)((__float_as_uint(m) >> 23) & 0xFF) - 127;
-  int sc = e - 14;
-  return sc < -126 ? -126 : (sc > 127 ? 127 : sc);
-}
-
-// One warp per row. rows [0, Is): gate, [Is, 2Is): up, [2Is, 2Is+H): down.
-__global__ void shared_row_scales(const uint16_t* __restrict__ gate,
-                                  const uint16_t* __restrict__ up,
-                                  const uint16_t* __restrict__ down, int down_ld,
-                                  int H, int Is, float* __restrict__ gu_rs,
-                                  float* __restrict__ dn_rs) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int nrows = 2 * Is + H;
-  if (warp >= nrows) return;
-  const uint16_t* row;
-  int len;
-  if (warp < Is) { row = gate + (size_t)warp * H; len = H; }
-  else if (warp < 2 * Is) { row = up + (size_t)(warp - Is) * H; len = H; }
-  else { row = down + (size_t)(warp - 2 * Is) * down_ld; len = Is; }
-  float m = 0.f;
-  for (int c = lane; c < len; c += 32) m = fmaxf(m, fabsf(bf16_val(row[c])));
-  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0) {
-    const float rs = ldexpf(1.0f, row_scale_exp(m));
-    if (warp < 2 * Is) {
-      const int r = warp < Is ? warp : warp - Is;
-      gu_rs[(size_t)(r >> 3) * 16 + (warp < Is ? 0 : 8) + (r & 7)] = rs;
-    } else {
-      dn_rs[warp - 2 * Is] = rs;
-    }
-  }
-}
-
-__device__ inline uint32_t pack_pair(const uint16_t* p, int sc) {
-  const __half2 h = __floats2half2_rn(ldexpf(bf16_val(p[0]), -sc), ldexpf(bf16_val(p[1]), -sc));
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// One thread per 16-byte fragment: gate/up units first, then down units.
-__global__ void shared_pack(const uint16_t* __restrict__ gate,
-                            const uint16_t* __restrict__ up,
-                            const uint16_t* __restrict__ down, int down_ld, int H,
-                            int Is, const float* __restrict__ gu_rs,
-                            const float* __restrict__ dn_rs, uint4* __restrict__ gu_out,
-                            uint4* __restrict__ dn_out) {
-  const size_t n_gu = (size_t)(Is / 8) * (H / 16) * 32;
-  const size_t n_dn = (size_t)(H / 16) * (Is / 16) * 32;
-  for (size_t u = (size_t)blockIdx.x * blockDim.x + threadIdx.x; u < n_gu + n_dn;
-       u += (size_t)gridDim.x * blockDim.x) {
-    const bool gu = u < n_gu;
-    const size_t v = gu ? u : u - n_gu;
-    const int lane = (int)(v & 31);
-    const size_t tk = v >> 5;
-    const int nks = gu ? H / 16 : Is / 16;
-    const int j = (int)(tk / nks), ks = (int)(tk % nks);
-    const int g = lane >> 2, t = lane & 3;
-    const int c0 = 16 * ks + 2 * t;
-    const uint16_t *r0, *r1;
-    int s0, s1;
-    if (gu) {
-      r0 = gate + (size_t)(8 * j + g) * H;
-      r1 = up + (size_t)(8 * j + g) * H;
-      s0 = (int)(__float_as_uint(gu_rs[(size_t)j * 16 + g]) >> 23) - 127;
-      s1 = (int)(__float_as_uint(gu_rs[(size_t)j * 16 + 8 + g]) >> 23) - 127;
-    } else {
-      r0 = down + (size_t)(16 * j + g) * down_ld;
-      r1 = down + (size_t)(16 * j + g + 8) * down_ld;
-      s0 = (int)(__float_as_uint(dn_rs[16 * j + g]) >> 23) - 127;
-      s1 = (int)(__float_as_uint(dn_rs[16 * j + g + 8]) >> 23) - 127;
-    }
-    const uint4 o = make_uint4(pack_pair(r0 + c0, s0), pack_pair(r1 + c0, s1),
-                               pack_pair(r0 + c0 + 8, s0), pack_pair(r1 + c0 + 8, s1));
-    if (gu) gu_out[v] = o;
-    else dn_out[v] = o;
-  }
-}
-
-}  // namespace
-
-cudaError_t launch_pack_shared(const uint16_t* gate, const uint16_t* up,
-                               const uint16_t* down, int down_ld, int H, int Is,
-                               uint4* gu_out, float* gu_rs, uint4* dn_out,
-                               float* dn_rs, cudaStream_t s) {
-  const int rows = 2 * Is + H;
-  shared_row_scales<<<(rows * 32 + 255) / 256, 256, 0, s>>>(gate, up, down, down_ld, H, Is,
-                                                            gu_rs, dn_rs);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const size_t n = (size_t)(Is / 8) * (H / 16) * 32 + (size_t)(H / 16) * (Is / 16) * 32;
-  size_t grid = (n + 255) / 256;
-  if (grid > 152 * 32) grid = 152 * 32;
-  shared_pack<<<(unsigned)grid, 256, 0, s>>>(gate, up, down, down_ld, H, Is, gu_rs, dn_rs,
-                                            gu_out, dn_out);
-  return cudaGetLastError();
-}
-
 }  // namespace dfm

@@ -41,13 +41,12 @@ class Setup:
     oracle's view of the same weights (spans generated on demand on the
     host)."""
 
-    def __init__(self, wl, max_tokens=None, chunk=64, fused=False, mma_sync_prefill=False,
+    def __init__(self, wl, max_tokens=None, chunk=64, mma_sync_prefill=False,
                  cache_slots=0):
         import mxfp4_routed_expert_top_gb300 as dfm
         torch = torch_mod()
         self.wl = wl
-        self.fused = fused
-        flags = ((dfm.STACK_RMSNORM_RESIDUAL if wl.stack else 0) | (dfm.FUSED_DECODE if fused else 0)
+        flags = ((dfm.STACK_RMSNORM_RESIDUAL if wl.stack else 0)
                  | (dfm.PREFILL_MMA_SYNC if mma_sync_prefill else 0))
         self.m = dfm.MoE(wl.H, wl.E, wl.k, wl.I, wl.n_shared, wl.Is,
                          n_layers=wl.L, max_tokens=max_tokens or wl.T,

@@ -154,7 +154,7 @@ def test_cache_guards(tiny_cached, torch):
     for kw in (dict(max_tokens=2, cache_slots=3),      # < max_tokens * top_k
                dict(max_tokens=1, cache_slots=9),      # > n_experts
                dict(max_tokens=16, cache_slots=8),     # beyond decode batches
-               dict(max_tokens=1, cache_slots=4, flags=dfm.FUSED_DECODE)):
+               dict(max_tokens=1, cache_slots=4, flags=2)):  # a reserved flag bit
         with pytest.raises(dfm.DfMoeError) as ei:
             dfm.MoE(wl.H, wl.E, wl.k, wl.I, wl.n_shared, wl.Is, **kw)
         assert ei.value.code == -1

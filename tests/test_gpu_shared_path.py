@@ -40,11 +40,10 @@ def torch():
     return t
 
 
-@pytest.fixture(scope="module", params=["chain", "fused"])
-def zero_routed(torch, request):
+@pytest.fixture(scope="module")
+def zero_routed(torch):
     import mxfp4_routed_expert_top_gb300 as dfm
-    flags = dfm.FUSED_DECODE if request.param == "fused" else 0
-    m = dfm.MoE(WL.H, E, E, WL.I, WL.n_shared, WL.Is, max_tokens=200, flags=flags)
+    m = dfm.MoE(WL.H, E, E, WL.I, WL.n_shared, WL.Is, max_tokens=200)
     router = synth.router(WL.seed, WL.wcfg, 0, E, WL.H)
     shared = [synth.shared(WL.seed, WL.wcfg, 0, s, WL.H, WL.Is) for s in range(WL.n_shared)]
     zeros = torch.zeros(E * m.span_bytes, dtype=torch.uint8, device="cuda")

@@ -40,10 +40,10 @@ def torch():
     return t
 
 
-@pytest.fixture(scope="module", params=["chain", "fused"])
-def stack(torch, request):
+@pytest.fixture(scope="module")
+def stack(torch):
     torch.cuda.empty_cache()
-    s = Setup(WL, max_tokens=4, fused=request.param == "fused")
+    s = Setup(WL, max_tokens=4)
     yield s
     s.close()
     torch.cuda.empty_cache()
