@@ -166,7 +166,13 @@ DF_MOE_API int df_moe_load_experts(df_moe* h, int32_t layer,
  *   ids           device [L][T][k] int32, descending logit order
  *   weights       device [L][T][k] fp32, softmax over the selected logits
  * Errors: EINVAL, ERANGE (T), ESTATE (weights not loaded), ECUDA, and the
- * error recorded by an earlier device-side check (EDEVICE / ETIMEOUT). */
+ * error recorded by the device-side checks of an earlier call: ETIMEOUT (a
+ * bounded wait gave up) or EDEVICE (an index out of range was skipped). The
+ * last kernel of every call copies the device error word to a host-visible
+ * word when it is nonzero; a call that finds that word set synchronises
+ * `stream`, clears the error, returns it and launches nothing (results of
+ * the call that recorded it are not to be trusted). A call after that runs
+ * normally. */
 DF_MOE_API int df_moe_forward(df_moe* h, const void* x_bf16, int32_t T,
                    const void* residual_bf16, void* out_bf16, float* out_f32,
                    int32_t* ids, float* weights, void* stream);
@@ -185,14 +191,28 @@ DF_MOE_API int df_moe_forward_trace(df_moe* h, const void* x_bf16, int32_t T,
 
 /* Same, with HOST buffers: copies x (and residual) to the device, runs the
  * forward, copies the results back and synchronises `stream` before
- * returning. out_f32, residual, ids and weights may be NULL. */
+ * returning. out_f32, residual, ids and weights may be NULL. Errors as
+ * df_moe_forward, and also ETIMEOUT / EDEVICE recorded by this call's own
+ * kernels (checked after the synchronisation; the error is then cleared). */
 DF_MOE_API int df_moe_forward_host(df_moe* h, const uint16_t* x_bf16, int32_t T,
                         const uint16_t* residual_bf16, uint16_t* out_bf16,
                         float* out_f32, int32_t* ids, float* weights,
                         void* stream);
 
-/* Synchronises `stream` and reports any device-side error word. */
+/* Synchronises `stream` and reports (and clears) any device-side error
+ * word: ETIMEOUT if a bounded wait gave up, EDEVICE if a range check failed,
+ * DF_MOE_OK otherwise. */
 DF_MOE_API int df_moe_sync(df_moe* h, void* stream);
+
+/* Test hook for the failure path (no GPU fault involved): the next forward
+ * call's gate/up phase (decode batches, T <= 8) leaves one stage of one
+ * routed-expert pipeline unfilled and unannounced, and its bounded waits use
+ * a short limit (2^12 polls). The waiting warps give up, record a timeout in
+ * the device error word and leave; every other wait of the call is bounded
+ * too, so the call ends. That call's results are wrong and the error is
+ * reported as ETIMEOUT by df_moe_sync, by df_moe_forward_host after its
+ * synchronisation, or by the next forward. One-shot. Errors: EINVAL (null). */
+DF_MOE_API int df_moe_test_drop_arrival(df_moe* h);
 
 /* ---- CUDA graphs -----------------------------------------------------------
  * A forward pass captured once into a CUDA graph and replayed: one launch a
@@ -283,7 +303,8 @@ DF_MOE_API int df_moe_last_launch_count(const df_moe* h);
  * is part of the library: every GPU that loads the library holds it until the
  * process exits. The call allocates nothing (no cudaMalloc/cudaFree, no
  * allocating library routine).
- *   router  device [E][H] fp32      x_bf16  device [T][H] bf16, 16-byte aligned
+ *   router  device [E][H] fp32      x_bf16  device [T][H] bf16; both 16-byte aligned
+ *           (EINVAL otherwise, checked before anything is launched)
  *   ids     device [T][k] int32     weights device [T][k] fp32
  * Limits: H a multiple of 32 up to 8192, 1 <= E <= 1024, 1 <= k <=
  * min(E, 32), and the scratch must hold nsplit*T*E floats (262,144 floats;
@@ -291,8 +312,11 @@ DF_MOE_API int df_moe_last_launch_count(const df_moe* h);
  * there). Larger calls fail with DF_MOE_ERANGE and a message from
  * df_moe_last_error(NULL); nothing is launched then.
  * The first call on each device looks up the array's device address (with
- * that device current) and caches it; make that first call before any stream
- * capture. All calls share the one array: calls that overlap on the GPU (on
+ * that device current) and caches it for the life of the process; make that
+ * first call before any stream capture. A device reset (cudaDeviceReset)
+ * would leave the cached address stale: this entry point does not support
+ * calls after one. The router kernel is an ordinary launch on `stream`, so
+ * inputs written by the caller's kernels earlier on that stream are seen. All calls share the one array: calls that overlap on the GPU (on
  * different streams, or from different threads) race and must be ordered by
  * the caller. Nothing in it needs clearing between calls: each call writes
  * every scratch element it later reads. */

@@ -28,7 +28,7 @@ SYMBOLS = [
     "df_moe_last_launch_count", "df_moe_route_noalloc",
     "df_moe_graph_create", "df_moe_graph_launch", "df_moe_graph_launch_count",
     "df_moe_graph_destroy", "df_moe_stream_read", "df_moe_create_cached",
-    "df_moe_cache_stats",
+    "df_moe_cache_stats", "df_moe_test_drop_arrival",
 ]
 
 
@@ -231,6 +231,11 @@ class MoE:
 
     def sync(self, stream=None):
         self._check(lib().df_moe_sync(self.h, _stream(stream)))
+
+    def test_drop_arrival(self):
+        """Test hook: the next forward's gate/up phase leaves one pipeline
+        stage unfilled, so a bounded device wait runs out (ETIMEOUT)."""
+        self._check(lib().df_moe_test_drop_arrival(self.h))
 
     def step_router(self, layer, x, T, logits, stream=None):
         self._check(lib().df_moe_step_router(self.h, layer, _ptr(x), T, _ptr(logits),

@@ -76,6 +76,11 @@ struct df_moe {
   uint16_t* xbuf[2] = {nullptr, nullptr};  // [Tmax][H] stack ping-pong
   uint16_t* xn = nullptr;        // [Tmax][H]
   uint32_t* err = nullptr;       // device error word
+  // host-visible copy of the error word (pinned, mapped): the last kernel of
+  // every forward writes the word there when it is nonzero
+  uint32_t* err_mirror_h = nullptr;
+  uint32_t* err_mirror_d = nullptr;  // the same word as the device sees it
+  bool drop_next = false;            // test hook: the next forward's gate/up drops a stage
   unsigned int* counter = nullptr;  // router blocks done (zero between calls)
   // tcgen05 GEMMs for batches above the decode range
   bool gemm = false;
@@ -244,7 +249,7 @@ int route(df_moe* h, int l, const uint16_t* x, int T, int32_t* ids, float* w,
   if (!direct)
     RUN(h, K_GROUP, s, launch_group(ids, T, c.top_k, c.n_experts, nullptr,
                                     nullptr, nullptr, nullptr, h->items,
-                                    h->n_items, h->sorted, tg, s));
+                                    h->n_items, h->sorted, tg, h->err, s));
   return DF_MOE_OK;
 }
 
@@ -261,15 +266,16 @@ int expert_gateup(df_moe* h, int l, const uint16_t* x, int T, int max_items, int
   const uint8_t* arena = h->layers[l].arena;
   if (use_gemm(h, T, tg)) {
     RUN(h, K_OTHER, s, launch_prep_x(x, T * c.top_k, c.hidden, c.top_k, h->sorted, h->g_xg,
-                                     h->g_bsc, s));
+                                     h->g_bsc, h->err, s));
     RUN(h, K_GEMM_GU, s, launch_gemm_gateup(h->layers[l].map_gu, h->bmap_gu, arena,
                                             h->span_bytes, h->layers[l].eref, c.hidden, c.inter,
                                             c.top_k, h->g_bsc, h->items, h->n_items, max_items,
-                                            h->sorted, hbuf, h->err, s));
+                                            h->sorted, hbuf, c.n_experts, T * c.top_k, h->err,
+                                            s));
   } else {
     RUN(h, K_GATEUP, s, launch_gateup(arena, h->span_bytes, c.hidden, c.inter, c.top_k, x,
                                       h->items, h->n_items, max_items, h->sorted, hbuf, tg,
-                                      h->err, s, max_ctas));
+                                      c.n_experts, T * c.top_k, h->err, s, max_ctas));
   }
   return DF_MOE_OK;
 }
@@ -280,15 +286,16 @@ int expert_down(df_moe* h, int l, const float* hbuf, int T, int max_items, int t
   const uint8_t* arena = h->layers[l].arena;
   if (use_gemm(h, T, tg)) {
     RUN(h, K_OTHER, s, launch_split_h(hbuf, T * c.top_k, c.inter, h->sorted, h->g_hh, h->g_bsc,
-                                      s));
+                                      h->err, s));
     RUN(h, K_GEMM_DN, s, launch_gemm_down(h->layers[l].map_dn, h->bmap_dn, arena,
                                           h->span_bytes, h->layers[l].eref, c.hidden, c.inter,
                                           c.top_k, h->g_bsc, h->items, h->n_items, max_items,
-                                          h->sorted, h->part, h->err, s));
+                                          h->sorted, h->part, c.n_experts, T * c.top_k, h->err,
+                                          s));
   } else {
     RUN(h, K_DOWN, s, launch_down(arena, h->span_bytes, c.hidden, c.inter, h->items,
-                                  h->n_items, max_items, h->sorted, hbuf, h->part, tg, h->err,
-                                  s, max_ctas, after_gateup));
+                                  h->n_items, max_items, h->sorted, hbuf, h->part, tg,
+                                  c.n_experts, T * c.top_k, h->err, s, max_ctas, after_gateup));
   }
   return DF_MOE_OK;
 }
@@ -335,7 +342,8 @@ int cache_plan(df_moe* h, int l, int T, const int32_t* ids, cudaStream_t s) {
   for (int i = 0; i < n; ++i) {
     const int e = h->ids_h[i];
     if (e < 0 || e >= c.n_experts)
-      return fail(h, DF_MOE_ECUDA, "layer %d: selected expert %d out of range", l, e);
+      return fail(h, DF_MOE_EDEVICE, "layer %d: the device selected expert %d, out of range", l,
+                  e);
     const int sl = L.slot_of[e];
     if (sl >= 0) {
       if (L.used[sl] != now) {
@@ -365,8 +373,6 @@ int cache_plan(df_moe* h, int l, int T, const int32_t* ids, cudaStream_t s) {
     // previous fill kernel
     h->fill_h[nfill++] = CacheCopy{L.host_pool_dev + (size_t)e * h->span_bytes,
                                    L.arena + (size_t)v * h->span_bytes, e};
-    ++h->cache_misses;
-    h->cache_bytes += (int64_t)h->span_bytes;
   }
   if (nfill) {
     const int rc = run(h, K_CACHE_FILL, s, [&]() {
@@ -381,6 +387,9 @@ int cache_plan(df_moe* h, int l, int T, const int32_t* ids, cudaStream_t s) {
       }
       return rc;
     }
+    // counted once the copies are on their way: the bytes actually moved
+    h->cache_misses += nfill;
+    h->cache_bytes += (int64_t)nfill * (int64_t)h->span_bytes;
   }
   return DF_MOE_OK;
 }
@@ -437,10 +446,11 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
                                             h->rsplit.nsplit, c.n_experts, ids, w, h->hsh,
                                             h->hbuf, h->err, sh_gu,
                                             cached ? (const uint8_t* const*)L.span_tab : nullptr,
-                                            s));
-    RUN(h, K_DOWN, s, launch_phase_down(L.arena, h->span_bytes, c.hidden, c.inter, h->items,
-                                        h->n_items, h->sorted, h->hbuf, h->part, L.sh_down, R,
-                                        h->hsh, T, h->ysh, h->err, sh_dn,
+                                            h->drop_next, s));
+    h->drop_next = false;
+    RUN(h, K_DOWN, s, launch_phase_down(L.arena, h->span_bytes, c.hidden, c.inter, c.n_experts,
+                                        c.top_k, h->items, h->n_items, h->sorted, h->hbuf,
+                                        h->part, L.sh_down, R, h->hsh, T, h->ysh, h->err, sh_dn,
                                         cached ? (const uint8_t* const*)L.span_tab : nullptr,
                                         s));
   } else {
@@ -456,7 +466,7 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
   }
   RUN(h, K_COMBINE, s, launch_combine(h->part, w, T, c.top_k, c.hidden,
                                       c.n_shared > 0 ? h->ysh : nullptr,
-                                      residual, out_f32, out_bf16, s));
+                                      residual, out_f32, out_bf16, h->err, h->err_mirror_d, s));
   return DF_MOE_OK;
 }
 
@@ -625,6 +635,20 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
   if (!rc) rc = dalloc(h, &h->xn, Tm * H);
   if (!rc) rc = dalloc(h, &h->err, 1);
   if (!rc) rc = dalloc(h, &h->counter, 1);
+  if (!rc) {
+    void* hp = nullptr;
+    if (cudaHostAlloc(&hp, 64, cudaHostAllocPortable | cudaHostAllocMapped) != cudaSuccess)
+      rc = fail(h, DF_MOE_ENOMEM, "pinned error mirror failed");
+    if (!rc) {
+      h->host_allocs.push_back(hp);
+      h->err_mirror_h = static_cast<uint32_t*>(hp);
+      *h->err_mirror_h = 0u;
+      void* dp = nullptr;
+      if (cudaHostGetDevicePointer(&dp, hp, 0) != cudaSuccess)
+        rc = fail(h, DF_MOE_ECUDA, "error mirror not mapped into the device");
+      h->err_mirror_d = static_cast<uint32_t*>(dp);
+    }
+  }
   if (!rc) rc = dalloc(h, &h->hx, Tm * H);
   if (!rc) rc = dalloc(h, &h->hres, Tm * H);
   if (!rc) rc = dalloc(h, &h->hout, Tm * H);
@@ -808,6 +832,30 @@ int df_moe_load_experts(df_moe* h, int32_t layer, const df_moe_layer_weights* w,
   return DF_MOE_OK;
 }
 
+// A device-side error recorded by earlier work on `stream`: synchronises the
+// stream, reads and clears the device error word and its host mirror, puts
+// the router's block counter (which a call that gave up may have left
+// mid-count) back to zero, and returns ETIMEOUT (a bounded wait gave up) or
+// EDEVICE (a range check failed). DF_MOE_OK when the word is clear.
+static int report_device_error(df_moe* h, cudaStream_t s) {
+  CUDA_OR_FAIL(h, cudaStreamSynchronize(s));
+  uint32_t e = 0;
+  CUDA_OR_FAIL(h, cudaMemcpy(&e, h->err, 4, cudaMemcpyDeviceToHost));
+  e |= *reinterpret_cast<volatile uint32_t*>(h->err_mirror_h);
+  if (!e) return DF_MOE_OK;
+  CUDA_OR_FAIL(h, cudaMemset(h->err, 0, 4));
+  CUDA_OR_FAIL(h, cudaMemset(h->counter, 0, sizeof(unsigned int)));
+  *reinterpret_cast<volatile uint32_t*>(h->err_mirror_h) = 0u;
+  if (e & DEV_ERR_TIMEOUT)
+    return fail(h, DF_MOE_ETIMEOUT, "a bounded device wait gave up (error word 0x%x)", e);
+  return fail(h, DF_MOE_EDEVICE, "a device-side range check failed (error word 0x%x)", e);
+}
+
+// The host mirror of the error word is set: report the error (as above).
+static bool mirror_set(const df_moe* h) {
+  return *reinterpret_cast<volatile const uint32_t*>(h->err_mirror_h) != 0u;
+}
+
 static int forward_impl(df_moe* h, const void* x_bf16, int32_t T,
                         const void* residual_bf16, void* out_bf16, float* out_f32,
                         int32_t* ids, float* weights, uint16_t* trace_x,
@@ -853,6 +901,9 @@ static int forward_impl(df_moe* h, const void* x_bf16, int32_t T,
   }
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
   cudaStream_t s = (cudaStream_t)stream;
+  // an error that an earlier call's kernels recorded is reported now, before
+  // anything is launched
+  if (mirror_set(h)) return report_device_error(h, s);
   const size_t Tk = (size_t)T * c.top_k;
   if (!stack) {
     return layer_forward(h, 0, (const uint16_t*)x_bf16, T,
@@ -907,21 +958,20 @@ int df_moe_forward_host(df_moe* h, const uint16_t* x_bf16, int32_t T,
   if (weights)
     CUDA_OR_FAIL(h, cudaMemcpyAsync(weights, h->hw, nk * 4, cudaMemcpyDeviceToHost, s));
   CUDA_OR_FAIL(h, cudaStreamSynchronize(s));
+  // this call's own device-side errors (published by its last kernel)
+  if (mirror_set(h)) return report_device_error(h, s);
   return DF_MOE_OK;
 }
 
 int df_moe_sync(df_moe* h, void* stream) {
   if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
-  CUDA_OR_FAIL(h, cudaStreamSynchronize((cudaStream_t)stream));
-  uint32_t e = 0;
-  CUDA_OR_FAIL(h, cudaMemcpy(&e, h->err, 4, cudaMemcpyDeviceToHost));
-  if (e) {
-    CUDA_OR_FAIL(h, cudaMemset(h->err, 0, 4));
-    if (e & DEV_ERR_TIMEOUT)
-      return fail(h, DF_MOE_ETIMEOUT, "a bounded device wait gave up");
-    return fail(h, DF_MOE_EDEVICE, "device-side check failed (0x%x)", e);
-  }
+  return report_device_error(h, (cudaStream_t)stream);
+}
+
+int df_moe_test_drop_arrival(df_moe* h) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  h->drop_next = true;
   return DF_MOE_OK;
 }
 
@@ -967,7 +1017,7 @@ int df_moe_step_group(df_moe* h, const int32_t* ids, int32_t T, int32_t* offs,
   cudaStream_t s = (cudaStream_t)stream;
   RUN(h, K_GROUP, s, launch_group(ids, T, c.top_k, c.n_experts, offs, tok, slot,
                                   n_union, h->items, h->n_items, h->sorted,
-                                  kOneItemPerExpert, s));
+                                  kOneItemPerExpert, h->err, s));
   return DF_MOE_OK;
 }
 
@@ -988,7 +1038,7 @@ int df_moe_step_expert_gateup(df_moe* h, int32_t layer, const void* x_bf16,
   const int tg = kOneItemPerExpert;
   RUN(h, K_GROUP, s, launch_group(ids, T, c.top_k, c.n_experts, nullptr, nullptr,
                                   nullptr, nullptr, h->items, h->n_items,
-                                  h->sorted, tg, s));
+                                  h->sorted, tg, h->err, s));
   return expert_gateup(h, layer, (const uint16_t*)x_bf16, T,
                        std::min(T * c.top_k, c.n_experts), tg, hbuf, s);
 }
@@ -1010,11 +1060,11 @@ int df_moe_step_expert_down(df_moe* h, int32_t layer, const float* hbuf,
   const int tg = kOneItemPerExpert;
   RUN(h, K_GROUP, s, launch_group(ids, T, c.top_k, c.n_experts, nullptr, nullptr,
                                   nullptr, nullptr, h->items, h->n_items,
-                                  h->sorted, tg, s));
+                                  h->sorted, tg, h->err, s));
   const int rc = expert_down(h, layer, hbuf, T, std::min(T * c.top_k, c.n_experts), tg, s);
   if (rc) return rc;
   RUN(h, K_COMBINE, s, launch_combine(h->part, weights, T, c.top_k, c.hidden,
-                                      nullptr, nullptr, y, nullptr, s));
+                                      nullptr, nullptr, y, nullptr, h->err, h->err_mirror_d, s));
   return DF_MOE_OK;
 }
 

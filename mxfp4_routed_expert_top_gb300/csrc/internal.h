@@ -124,9 +124,12 @@ struct RouterFuse {
   int32_t* n_items;
   int32_t* sorted;
 };
+// after_previous: launched as a programmatic dependent of the kernel before it
+// (its weights are then read before it waits for that kernel, so they must
+// not be written by it); false: an ordinary launch.
 cudaError_t launch_router(const float* Wr, int E, int H, const uint16_t* x,
                           int T, float* part, RouterSplit sp, cudaStream_t s,
-                          const RouterFuse* fuse = nullptr);
+                          const RouterFuse* fuse = nullptr, bool after_previous = true);
 // Router logits of a batch (T > 1) as a tiled fp32 GEMM into at most
 // max_splits column splits of part; returns the split count used (-1 on a
 // launch error).
@@ -136,14 +139,16 @@ cudaError_t launch_topk(const float* part, int nsplit, int T, int E, int k,
                         float* logits_out, int32_t* ids, float* w,
                         Item* items, int32_t* n_items, int32_t* sorted,
                         cudaStream_t s);
+// ids outside [0, E) are left out and recorded in *err (DEV_ERR_RANGE).
 cudaError_t launch_group(const int32_t* ids, int T, int k, int E,
                          int32_t* offs, int32_t* tok, int32_t* slot,
                          int32_t* n_union, Item* items, int32_t* n_items,
-                         int32_t* sorted, int tg, cudaStream_t s);
+                         int32_t* sorted, int tg, uint32_t* err, cudaStream_t s);
+// E: experts of the layer, nassign: T * k (range checks of the items).
 cudaError_t launch_gateup(const uint8_t* arena, size_t span_bytes, int H,
                           int I, int k, const uint16_t* x, const Item* items,
                           const int32_t* n_items, int max_items,
-                          const int32_t* sorted, float* hbuf, int tg,
+                          const int32_t* sorted, float* hbuf, int tg, int E, int nassign,
                           uint32_t* err, cudaStream_t s, int max_ctas = 0);
 // after_gateup: the preceding kernel on `s` is the gate/up kernel of the same
 // selection (so the selection is complete when this grid starts, and the
@@ -151,11 +156,15 @@ cudaError_t launch_gateup(const uint8_t* arena, size_t span_bytes, int H,
 cudaError_t launch_down(const uint8_t* arena, size_t span_bytes, int H, int I,
                         const Item* items, const int32_t* n_items,
                         int max_items, const int32_t* sorted,
-                        const float* hbuf, float* part, int tg, uint32_t* err,
-                        cudaStream_t s, int max_ctas = 0, bool after_gateup = false);
+                        const float* hbuf, float* part, int tg, int E, int nassign,
+                        uint32_t* err, cudaStream_t s, int max_ctas = 0,
+                        bool after_gateup = false);
+// err_mirror (or null): the host-visible copy of the error word, written when
+// the word is nonzero.
 cudaError_t launch_combine(const float* part, const float* w, int T, int k,
                            int H, const float* ysh, const uint16_t* residual,
-                           float* out_f32, uint16_t* out_bf16, cudaStream_t s);
+                           float* out_f32, uint16_t* out_bf16, uint32_t* err,
+                           uint32_t* err_mirror, cudaStream_t s);
 cudaError_t launch_shared_gateup(const uint16_t* gate, const uint16_t* up,
                                  int R, int H, const uint16_t* x, int T,
                                  float* hsh, uint32_t* err, cudaStream_t s,
@@ -180,6 +189,7 @@ constexpr int kDecodeMaxT = 8;
 // spans: device [E] of span addresses (expert cache), or null for arena + e
 // * span_bytes.
 bool phase_supported(int H, int I, int R, int E, int k);
+
 // Read-only streaming probe: 16-byte loads over `bytes`, one word a thread
 // into sink (at least 8 * SMs * 256 words).
 cudaError_t launch_stream_read(const void* buf, size_t bytes, uint32_t* sink, cudaStream_t s);
@@ -193,17 +203,21 @@ struct CacheCopy {
 };
 cudaError_t launch_cache_fill(const CacheCopy* plan, int n, size_t span_bytes,
                               unsigned long long* span_tab, cudaStream_t s);
+// drop: the test hook (one stage of the routed gate/up never filled, short
+// waits), so that a bounded wait runs out.
 cudaError_t launch_phase_gateup(const uint16_t* sh_gate, const uint16_t* sh_up, int R,
                                 const uint8_t* arena, size_t span_bytes, int H, int I, int k,
                                 const uint16_t* x, int T, Item* items, int32_t* n_items,
                                 int32_t* sorted, const float* router_part, int nsplit, int E,
                                 int32_t* ids, float* w, float* hsh, float* hbuf, uint32_t* err,
-                                int n_sh, const uint8_t* const* spans, cudaStream_t s);
-cudaError_t launch_phase_down(const uint8_t* arena, size_t span_bytes, int H, int I,
-                              const Item* items, const int32_t* n_items, const int32_t* sorted,
-                              const float* hbuf, float* part, const uint16_t* sh_down, int R,
-                              const float* hsh, int T, float* ysh, uint32_t* err, int n_sh,
-                              const uint8_t* const* spans, cudaStream_t s);
+                                int n_sh, const uint8_t* const* spans, bool drop,
+                                cudaStream_t s);
+cudaError_t launch_phase_down(const uint8_t* arena, size_t span_bytes, int H, int I, int E,
+                              int k, const Item* items, const int32_t* n_items,
+                              const int32_t* sorted, const float* hbuf, float* part,
+                              const uint16_t* sh_down, int R, const float* hsh, int T, float* ysh,
+                              uint32_t* err, int n_sh, const uint8_t* const* spans,
+                              cudaStream_t s);
 cudaError_t launch_repack_span(const uint8_t* src, uint8_t* dst, int n_spans,
                                int H, int I, int inverse, cudaStream_t s);
 
@@ -230,23 +244,23 @@ cudaError_t launch_row_ref(const uint8_t* spans, size_t span_bytes, int H, int I
 // B rows in expert order (R = T*k assignments, row p for sorted[p]):
 // gate/up xg [R][H] f16 = x[sorted[p] / k] * 2^-s_p (exact), bsc[p] = 2^s_p;
 cudaError_t launch_prep_x(const uint16_t* x, int R, int H, int k, const int32_t* sorted,
-                          uint16_t* xg, float* bsc, cudaStream_t s);
+                          uint16_t* xg, float* bsc, uint32_t* err, cudaStream_t s);
 // down hh [R][2][I] f16 = high and low parts of h[sorted[p]] * 2^-s_p.
 cudaError_t launch_split_h(const float* h, int R, int I, const int32_t* sorted, uint16_t* hh,
-                           float* bsc, cudaStream_t s);
+                           float* bsc, uint32_t* err, cudaStream_t s);
 // Tensor maps of xg ([R][H]) and hh ([2R][I]) for rows allocated for R.
 bool make_b_maps(const uint16_t* xg, const uint16_t* hh, int R, int H, int I, ChunkMap* gu,
                  ChunkMap* dn);
 cudaError_t launch_gemm_gateup(const ChunkMap& map, const ChunkMap& bmap, const uint8_t* arena,
                                size_t span_bytes, const uint8_t* eref, int H, int I, int k,
                                const float* bsc, const Item* items, const int32_t* n_items,
-                               int max_items, const int32_t* sorted, float* hbuf, uint32_t* err,
-                               cudaStream_t s);
+                               int max_items, const int32_t* sorted, float* hbuf, int E,
+                               int nassign, uint32_t* err, cudaStream_t s);
 cudaError_t launch_gemm_down(const ChunkMap& map, const ChunkMap& bmap, const uint8_t* arena,
                              size_t span_bytes, const uint8_t* eref, int H, int I, int k,
                              const float* bsc, const Item* items, const int32_t* n_items,
-                             int max_items, const int32_t* sorted, float* part, uint32_t* err,
-                             cudaStream_t s);
+                             int max_items, const int32_t* sorted, float* part, int E,
+                             int nassign, uint32_t* err, cudaStream_t s);
 
 // ---- shared experts of large batches on tcgen05 (k_dense.cu) ----------------
 // Tensor maps of one layer's shared-expert weights (gate, up [R][H]; down

@@ -15,13 +15,20 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) mxv_kernel(const MxvArgs a)
 
 // out[t][j] = residual + sum_i w[t][i] part[t k + i][j] + ysh[t][j], k <= 32.
 // Every load of a thread is issued before the first FMA (one L2 round trip);
-// the sum runs in slot order.
+// the sum runs in slot order. The last kernel of a batch forward: its first
+// thread copies the device error word, complete once the kernels before it
+// are, to the host-visible mirror.
 constexpr int kCombineThreads = 128;
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const float* __restrict__ part, const float* __restrict__ w, int k, int H,
                const float* __restrict__ ysh, const uint16_t* __restrict__ residual,
-               float* __restrict__ out_f32, uint16_t* __restrict__ out_bf16) {
+               float* __restrict__ out_f32, uint16_t* __restrict__ out_bf16, uint32_t* err,
+               uint32_t* err_mirror) {
   pdl_wait();
+  if (err_mirror && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    const uint32_t e = atomicOr(err, 0u);
+    if (e) *reinterpret_cast<volatile uint32_t*>(err_mirror) = e;
+  }
   const int t = blockIdx.y;
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= H) return;
@@ -83,29 +90,36 @@ cudaError_t launch_mxv(const MxvArgs& a, int max_items, cudaStream_t s, int max_
 cudaError_t launch_gateup(const uint8_t* arena, size_t span_bytes, int H,
                           int I, int k, const uint16_t* x, const Item* items,
                           const int32_t* n_items, int max_items,
-                          const int32_t* sorted, float* hbuf, int /*tg*/,
+                          const int32_t* sorted, float* hbuf, int /*tg*/, int E, int nassign,
                           uint32_t* err, cudaStream_t s, int max_ctas) {
   MxvArgs a{arena, span_bytes, H, I, k, x, nullptr, items, n_items, sorted, hbuf, err, 0,
             nullptr};
+  a.E = E;
+  a.nassign = nassign;
+  a.max_items = max_items;
   return launch_mxv<0>(a, max_items, s, max_ctas);
 }
 
 cudaError_t launch_down(const uint8_t* arena, size_t span_bytes, int H, int I,
                         const Item* items, const int32_t* n_items,
                         int max_items, const int32_t* sorted,
-                        const float* hbuf, float* part, int /*tg*/, uint32_t* err,
-                        cudaStream_t s, int max_ctas, bool after_gateup) {
+                        const float* hbuf, float* part, int /*tg*/, int E, int nassign,
+                        uint32_t* err, cudaStream_t s, int max_ctas, bool after_gateup) {
   MxvArgs a{arena, span_bytes, H, I, 0, nullptr, hbuf, items, n_items, sorted, part, err,
             after_gateup ? 1 : 0, nullptr};
+  a.E = E;
+  a.nassign = nassign;
+  a.max_items = max_items;
   return launch_mxv<1>(a, max_items, s, max_ctas);
 }
 
 cudaError_t launch_combine(const float* part, const float* w, int T, int k,
                            int H, const float* ysh, const uint16_t* residual,
-                           float* out_f32, uint16_t* out_bf16, cudaStream_t s) {
+                           float* out_f32, uint16_t* out_bf16, uint32_t* err,
+                           uint32_t* err_mirror, cudaStream_t s) {
   dim3 grid((H + kCombineThreads - 1) / kCombineThreads, T);
   return launch_after_previous(combine_kernel, grid, dim3(kCombineThreads), 0, s, part, w, k, H, ysh,
-                               residual, out_f32, out_bf16);
+                               residual, out_f32, out_bf16, err, err_mirror);
 }
 
 }  // namespace dfm

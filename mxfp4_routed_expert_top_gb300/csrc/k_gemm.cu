@@ -105,6 +105,11 @@ struct GemmArgs {
   int max_items;
   float* out;           // gate/up: h [T*k][I]; down: part [T*k][H]
   uint32_t* err;
+  // range checks: an item whose expert is outside [0, E) or whose
+  // assignments leave [0, nassign) is skipped by every role alike, an
+  // assignment index outside [0, nassign) is not written, and either is
+  // recorded in *err (DEV_ERR_RANGE)
+  int E, nassign;
 };
 
 struct Smem {
@@ -162,7 +167,13 @@ __device__ void walk_seek(const GemmArgs& a, int n_items, Walk& w) {
       w.done = true;  // items are dense: none beyond n_items
       return;
     }
-    const int cnt = a.items[w.item].cnt;
+    const Item it = a.items[w.item];
+    if ((unsigned)it.e >= (unsigned)a.E || it.pos < 0 || it.cnt < 0 ||
+        it.pos + it.cnt > a.nassign) {
+      if ((threadIdx.x & 31) == 0) atomicOr(a.err, DEV_ERR_RANGE);
+      continue;
+    }
+    const int cnt = it.cnt;
     if (cnt <= 0) continue;
     w.ntb = (cnt + block_tokens<MODE>() - 1) / block_tokens<MODE>();
     w.tb = 0;
@@ -601,6 +612,10 @@ __device__ void role_epilogue(const GemmArgs& a, int n_items, Smem* sm, uint32_t
     if (lane < nt) {
       asg0 = a.sorted[it.pos + n0 + lane];
       sc0 = a.bsc[it.pos + n0 + lane];
+      if ((unsigned)asg0 >= (unsigned)a.nassign) {
+        atomicOr(a.err, DEV_ERR_RANGE);
+        asg0 = -1;
+      }
     }
     const uint32_t e_ref = a.eref[(size_t)it.e * eref_row + (MODE == 0 ? 0 : 2 * (size_t)a.I) +
                                   (size_t)kM * w.mt + m];
@@ -639,7 +654,7 @@ __device__ void role_epilogue(const GemmArgs& a, int n_items, Smem* sm, uint32_t
           const float xs = __shfl_sync(0xffffffffu, sc0, col);
           const float v = acc[i] * rowfac * xs;
           const float up = __shfl_xor_sync(0xffffffffu, v, 8);
-          if (rho < 8 && col < rows) a.out[(size_t)asg * a.I + irow] = silu_f(v) * up;
+          if (rho < 8 && col < rows && asg >= 0) a.out[(size_t)asg * a.I + irow] = silu_f(v) * up;
         }
       } else {
 #pragma unroll
@@ -647,7 +662,7 @@ __device__ void role_epilogue(const GemmArgs& a, int n_items, Smem* sm, uint32_t
           const int tok = (c0 + i) >> 1;  // columns 2 tok (hi), 2 tok + 1 (lo)
           const int asg = __shfl_sync(0xffffffffu, asg0, tok);
           const float hs = __shfl_sync(0xffffffffu, sc0, tok);
-          if (tok < nt)
+          if (tok < nt && asg >= 0)
             a.out[(size_t)asg * a.H + (size_t)kM * w.mt + m] =
                 (acc[i] + acc[i + 1]) * rowfac * hs;
         }
@@ -703,7 +718,11 @@ __global__ void __launch_bounds__(kThr, 1) gemm_kernel(const __grid_constant__ G
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(&sm->tmem);
 
   pdl_wait();  // items and the B sources come from the preceding kernels
-  const int n_items = *a.n_items;
+  int n_items = *a.n_items;
+  if (n_items < 0 || n_items > a.max_items) {
+    if (threadIdx.x == 0) atomicOr(a.err, DEV_ERR_RANGE);
+    n_items = n_items < 0 ? 0 : a.max_items;
+  }
   if (warp < kEpiWarps) {
     role_epilogue<MODE>(a, n_items, sm, tmem, warp, lane);
   } else if (warp < kDecWarp0 + kDecWarps) {
@@ -758,10 +777,15 @@ __device__ float block_max_abs(float v, float* red) {
 // exact for bf16 x), bsc[p] = 2^s, s from the token's largest |x|.
 __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t* x, int H, int k,
                                                      const int32_t* sorted, __half* xg,
-                                                     float* bsc) {
+                                                     float* bsc, uint32_t* err) {
   __shared__ float red[32];
   const int p = blockIdx.x;
-  const uint16_t* xr = x + (size_t)(sorted[p] / k) * H;
+  int a = sorted[p];
+  if ((unsigned)a >= gridDim.x) {  // R = T * k assignments
+    if (threadIdx.x == 0) atomicOr(err, DEV_ERR_RANGE);
+    a = 0;
+  }
+  const uint16_t* xr = x + (size_t)(a / k) * H;
   float mx = 0.f;
   for (int i = threadIdx.x; i < H; i += blockDim.x)
     mx = fmaxf(mx, fabsf(__uint_as_float((uint32_t)xr[i] << 16)));
@@ -777,10 +801,15 @@ __global__ void __launch_bounds__(256) prep_x_kernel(const uint16_t* x, int H, i
 // h[sorted[p]] * 2^-s, bsc[p] = 2^s.
 __global__ void __launch_bounds__(256) split_h_kernel(const float* h, int I,
                                                       const int32_t* sorted, __half* hh,
-                                                      float* bsc) {
+                                                      float* bsc, uint32_t* err) {
   __shared__ float red[32];
   const int p = blockIdx.x;
-  const float* hr = h + (size_t)sorted[p] * I;
+  int a = sorted[p];
+  if ((unsigned)a >= gridDim.x) {  // R = T * k assignments
+    if (threadIdx.x == 0) atomicOr(err, DEV_ERR_RANGE);
+    a = 0;
+  }
+  const float* hr = h + (size_t)a * I;
   float mx = 0.f;
   for (int i = threadIdx.x; i < I; i += blockDim.x) mx = fmaxf(mx, fabsf(hr[i]));
   mx = block_max_abs(mx, red);
@@ -915,14 +944,14 @@ cudaError_t launch_row_ref(const uint8_t* arena, size_t span_bytes, int H, int I
 }
 
 cudaError_t launch_prep_x(const uint16_t* x, int R, int H, int k, const int32_t* sorted,
-                          uint16_t* xg, float* bsc, cudaStream_t s) {
-  prep_x_kernel<<<R, 256, 0, s>>>(x, H, k, sorted, reinterpret_cast<__half*>(xg), bsc);
+                          uint16_t* xg, float* bsc, uint32_t* err, cudaStream_t s) {
+  prep_x_kernel<<<R, 256, 0, s>>>(x, H, k, sorted, reinterpret_cast<__half*>(xg), bsc, err);
   return cudaGetLastError();
 }
 
 cudaError_t launch_split_h(const float* h, int R, int I, const int32_t* sorted, uint16_t* hh,
-                           float* bsc, cudaStream_t s) {
-  split_h_kernel<<<R, 256, 0, s>>>(h, I, sorted, reinterpret_cast<__half*>(hh), bsc);
+                           float* bsc, uint32_t* err, cudaStream_t s) {
+  split_h_kernel<<<R, 256, 0, s>>>(h, I, sorted, reinterpret_cast<__half*>(hh), bsc, err);
   return cudaGetLastError();
 }
 
@@ -951,20 +980,20 @@ bool make_b_maps(const uint16_t* xg, const uint16_t* hh, int R, int H, int I, Ch
 cudaError_t launch_gemm_gateup(const ChunkMap& map, const ChunkMap& bmap, const uint8_t* arena,
                                size_t span_bytes, const uint8_t* eref, int H, int I, int k,
                                const float* bsc, const Item* items, const int32_t* n_items,
-                               int max_items, const int32_t* sorted, float* hbuf, uint32_t* err,
-                               cudaStream_t s) {
+                               int max_items, const int32_t* sorted, float* hbuf, int E,
+                               int nassign, uint32_t* err, cudaStream_t s) {
   GemmArgs a{map, bmap, arena, span_bytes, eref, H, I, k, bsc,
-             items, n_items, sorted, max_items, hbuf, err};
+             items, n_items, sorted, max_items, hbuf, err, E, nassign};
   return launch_gemm<0>(a, s);
 }
 
 cudaError_t launch_gemm_down(const ChunkMap& map, const ChunkMap& bmap, const uint8_t* arena,
                              size_t span_bytes, const uint8_t* eref, int H, int I, int k,
                              const float* bsc, const Item* items, const int32_t* n_items,
-                             int max_items, const int32_t* sorted, float* part, uint32_t* err,
-                             cudaStream_t s) {
+                             int max_items, const int32_t* sorted, float* part, int E,
+                             int nassign, uint32_t* err, cudaStream_t s) {
   GemmArgs a{map, bmap, arena, span_bytes, eref, H, I, k, bsc,
-             items, n_items, sorted, max_items, part, err};
+             items, n_items, sorted, max_items, part, err, E, nassign};
   return launch_gemm<1>(a, s);
 }
 

@@ -88,7 +88,8 @@ phase_gateup_kernel(const BfvArgs sh, const MxvArgs rt_in, const SelArgs sel, in
     rt.sorted = sel_sorted;
   }
   __syncthreads();  // barriers set up; the selection in shared memory
-  mxv_cta<0>(rt, smem, bars, cta, ncta, /*set_up=*/false);
+  // one token: every item is its own (the library's own selection)
+  mxv_cta<0, TT == 1>(rt, smem, bars, cta, ncta, /*set_up=*/false);
 }
 
 template <int TT>
@@ -125,7 +126,8 @@ cudaError_t set_smem(Kern kernel, size_t smem, size_t& configured) {
 }  // namespace
 
 bool phase_supported(int H, int I, int R, int E, int k) {
-  const size_t gu = std::max(bfv_smem_bytes(H), mxv_smem_bytes(H, mxv_cg(0), mxv_unit(0)));
+  const size_t gu = std::max(bfv_smem_bytes(H), mxv_smem_bytes(H, mxv_cg(0), mxv_unit(0)) +
+                                                    mxv_x_bytes(H, mxv_cg(0)));
   const size_t dn = std::max(mxv_smem_bytes(I, mxv_cg(1), mxv_unit(1)), bfv_smem_bytes(R > 0 ? R : I));
   const size_t stat = (kBfvBars > kMxvBars ? kBfvBars : kMxvBars) * 8 + 1024;
   return H % 64 == 0 && I % 64 == 0 && E <= 1024 && k <= 32 && gu + stat <= 227 * 1024 &&
@@ -137,12 +139,22 @@ cudaError_t launch_phase_gateup(const uint16_t* sh_gate, const uint16_t* sh_up, 
                                 const uint16_t* x, int T, Item* items, int32_t* n_items,
                                 int32_t* sorted, const float* router_part, int nsplit, int E,
                                 int32_t* ids, float* w, float* hsh, float* hbuf, uint32_t* err,
-                                int n_sh, const uint8_t* const* spans, cudaStream_t s) {
+                                int n_sh, const uint8_t* const* spans, bool drop,
+                                cudaStream_t s) {
   const BfvArgs sh{sh_gate, sh_up, R, H, x, T, hsh, err};
-  const MxvArgs rt{arena, span_bytes, H, I, k, x, nullptr, items, n_items, sorted, hbuf, err, 0,
-                   spans};
+  MxvArgs rt{arena, span_bytes, H, I, k, x, nullptr, items, n_items, sorted, hbuf, err, 0,
+             spans};
+  rt.E = E;
+  rt.nassign = T * k;
+  rt.max_items = std::min(T * k, E);
+  if (drop) {
+    rt.drop = 1;
+    rt.wait_limit = kTestWaitLimit;
+  }
   const SelArgs sel{T == 1 ? router_part : nullptr, nsplit, E, k, ids, w};
-  const size_t smem = std::max(bfv_smem_bytes(H), mxv_smem_bytes(H, mxv_cg(0), mxv_unit(0)));
+  // one token: the routed CTAs also keep its B fragments (mxv_x_bytes)
+  const size_t smem = std::max(bfv_smem_bytes(H), mxv_smem_bytes(H, mxv_cg(0), mxv_unit(0)) +
+                                                      (T == 1 ? mxv_x_bytes(H, mxv_cg(0)) : 0));
   auto go = [&](auto kernel, size_t& conf) {
     const cudaError_t e = set_smem(kernel, smem, conf);
     if (e != cudaSuccess) return e;
@@ -156,13 +168,17 @@ cudaError_t launch_phase_gateup(const uint16_t* sh_gate, const uint16_t* sh_up, 
                   : go(phase_gateup_kernel<8>, conf[3]);
 }
 
-cudaError_t launch_phase_down(const uint8_t* arena, size_t span_bytes, int H, int I,
-                              const Item* items, const int32_t* n_items, const int32_t* sorted,
-                              const float* hbuf, float* part, const uint16_t* sh_down, int R,
-                              const float* hsh, int T, float* ysh, uint32_t* err, int n_sh,
-                              const uint8_t* const* spans, cudaStream_t s) {
-  const MxvArgs rt{arena, span_bytes, H, I, 0, nullptr, hbuf, items, n_items, sorted, part, err,
-                   1, spans};
+cudaError_t launch_phase_down(const uint8_t* arena, size_t span_bytes, int H, int I, int E,
+                              int k, const Item* items, const int32_t* n_items,
+                              const int32_t* sorted, const float* hbuf, float* part,
+                              const uint16_t* sh_down, int R, const float* hsh, int T, float* ysh,
+                              uint32_t* err, int n_sh, const uint8_t* const* spans,
+                              cudaStream_t s) {
+  MxvArgs rt{arena, span_bytes, H, I, 0, nullptr, hbuf, items, n_items, sorted, part, err,
+             1, spans};
+  rt.E = E;
+  rt.nassign = T * k;
+  rt.max_items = std::min(T * k, E);
   // no shared experts: no rows to stream (K only sizes the geometry)
   const BfvArgs sh{sh_down, nullptr, R > 0 ? H : 0, R > 0 ? R : I, hsh, T, ysh, err};
   const size_t smem = std::max(mxv_smem_bytes(I, mxv_cg(1), mxv_unit(1)), bfv_smem_bytes(sh.K));

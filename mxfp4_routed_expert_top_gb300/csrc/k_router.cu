@@ -214,7 +214,7 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 __global__ void __launch_bounds__(1024)
 group_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
              int32_t* offs, int32_t* tok, int32_t* slot, int32_t* n_union,
-             Item* items, int32_t* n_items, int32_t* sorted, int tg) {
+             Item* items, int32_t* n_items, int32_t* sorted, int tg, uint32_t* err) {
   __shared__ int cnt[1024];
   __shared__ int fill[1024];
   __shared__ int warp_sums[32];
@@ -225,18 +225,28 @@ group_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
   pdl_launch_dependents();  // the next kernel waits for this grid itself
   pdl_wait();  // the selected ids
   __syncthreads();
-  for (int a = tid; a < A; a += blockDim.x) atomicAdd(&cnt[ids[a]], 1);
+  // an id outside [0, E) (the single-step entry points take the caller's
+  // ids) is left out of every segment and recorded in the error word
+  bool bad = false;
+  for (int a = tid; a < A; a += blockDim.x) {
+    const int e = ids[a];
+    if ((unsigned)e < (unsigned)E) atomicAdd(&cnt[e], 1);
+    else bad = true;
+  }
+  if (bad && err) atomicOr(err, DEV_ERR_RANGE);
   __syncthreads();
   const int c = tid < E ? cnt[tid] : 0;
-  const int start = block_exclusive_scan(c, warp_sums, nullptr);
+  const int start = block_exclusive_scan(c, warp_sums, &tot);
   if (tid < E) {
     fill[tid] = start;
     if (offs) offs[tid] = start;
   }
-  if (tid == 0 && offs) offs[E] = A;
   __syncthreads();
+  if (tid == 0 && offs) offs[E] = tot;  // A when every id is in range
   for (int a = tid; a < A; a += blockDim.x) {
-    const int p = atomicAdd(&fill[ids[a]], 1);
+    const int e = ids[a];
+    if ((unsigned)e >= (unsigned)E) continue;
+    const int p = atomicAdd(&fill[e], 1);
     sorted[p] = a;
   }
   __syncthreads();
@@ -374,7 +384,7 @@ int launch_router_gemm(const float* Wr, int E, int H, const uint16_t* x, int T, 
 
 cudaError_t launch_router(const float* Wr, int E, int H, const uint16_t* x,
                           int T, float* part, RouterSplit sp, cudaStream_t s,
-                          const RouterFuse* fuse) {
+                          const RouterFuse* fuse, bool after_previous) {
   TopkFuse fz{nullptr, 0, nullptr, nullptr, nullptr, nullptr, nullptr};
   if (fuse && T == 1)
     fz = TopkFuse{fuse->counter, fuse->k, fuse->ids, fuse->w, fuse->items,
@@ -383,17 +393,20 @@ cudaError_t launch_router(const float* Wr, int E, int H, const uint16_t* x,
   const int nt = T == 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
   const size_t xs = (size_t)nt * sp.split_len * sizeof(uint16_t);  // <= 8 * 2048 * 2
   const dim3 block(kRouterThreads);
-  if (T == 1)
-    return launch_after_previous(router_kernel<1>, grid, block, xs, s, Wr, E, H, x, T, part,
-                                 sp.split_len, fz);
-  if (T <= 2)
-    return launch_after_previous(router_kernel<2>, grid, block, xs, s, Wr, E, H, x, T, part,
-                                 sp.split_len, fz);
-  if (T <= 4)
-    return launch_after_previous(router_kernel<4>, grid, block, xs, s, Wr, E, H, x, T, part,
-                                 sp.split_len, fz);
-  return launch_after_previous(router_kernel<8>, grid, block, xs, s, Wr, E, H, x, T, part,
-                               sp.split_len, fz);
+  auto go = [&](auto kernel) {
+    if (after_previous)
+      return launch_after_previous(kernel, grid, block, xs, s, Wr, E, H, x, T, part,
+                                   sp.split_len, fz);
+    // an ordinary launch: it starts after everything before it on the stream
+    // has completed (its griddepcontrol.wait then returns at once), so even
+    // the weights, read before that wait, may come from the kernel before it
+    kernel<<<grid, block, xs, s>>>(Wr, E, H, x, T, part, sp.split_len, fz);
+    return cudaGetLastError();
+  };
+  if (T == 1) return go(router_kernel<1>);
+  if (T <= 2) return go(router_kernel<2>);
+  if (T <= 4) return go(router_kernel<4>);
+  return go(router_kernel<8>);
 }
 
 cudaError_t launch_topk(const float* part, int nsplit, int T, int E, int k,
@@ -406,9 +419,9 @@ cudaError_t launch_topk(const float* part, int nsplit, int T, int E, int k,
 cudaError_t launch_group(const int32_t* ids, int T, int k, int E,
                          int32_t* offs, int32_t* tok, int32_t* slot,
                          int32_t* n_union, Item* items, int32_t* n_items,
-                         int32_t* sorted, int tg, cudaStream_t s) {
+                         int32_t* sorted, int tg, uint32_t* err, cudaStream_t s) {
   return launch_after_previous(group_kernel, dim3(1), dim3(1024), 0, s, ids, T, k, E, offs, tok,
-                               slot, n_union, items, n_items, sorted, tg);
+                               slot, n_union, items, n_items, sorted, tg, err);
 }
 
 }  // namespace dfm

@@ -23,10 +23,13 @@
 //   * Consumers: one 16-byte lds per lane = its A fragments for 4 k-steps;
 //     every 32-column MX block is accumulated by two MMAs into a temporary
 //     that is scaled by 2^(s-127) (per row) in fp32 and added to the result.
-//   * B (x) fragments live in registers as f16: the gate/up input is bf16,
-//     exact in f16 except |x| < 2^-17 (error <= 2^-25). The down input h
-//     (fp32, |h| up to ~1e5) is scaled per (token, chunk) by a power of two
-//     into f16 range and split into hi and lo columns (~22 bits).
+//   * B (x) fragments live in registers as f16. The gate/up input (bf16) is
+//     scaled per (token, chunk) by a power of two that puts its largest
+//     magnitude at exponent 15, so every entry within 2^32 of that maximum
+//     is exact in f16 whatever the token's range. The down input h (fp32,
+//     |h| up to ~1e5) is scaled the same way per (token, chunk) and split
+//     into hi and lo columns (~22 bits). The scales are undone on the fp32
+//     partial sums.
 //   * An item (one expert and all its tokens) is processed in token groups of
 //     8 (gate/up) or 4 (down) against the tile already in shared memory, so
 //     each expert's weights cross HBM once per call.
@@ -59,7 +62,7 @@ __host__ __device__ inline int mxv_nv(int K, int c, int cg) {
   return n < cg ? n : cg;
 }
 constexpr int kMaxStages = 8;
-constexpr int kRedRing = 4;  // epilogue reduction ring depth
+constexpr int kRedRing = 2;  // epilogue reduction ring depth
 constexpr size_t kSmemBudget = 214 * 1024;
 
 struct MxvArgs {
@@ -75,6 +78,16 @@ struct MxvArgs {
   uint32_t* err;
   int early;              // down only: the selection is complete at grid start
   const uint8_t* const* spans;  // [E] span addresses (expert cache), or null: arena
+  // Range checks: an item whose expert is outside [0, E) or whose
+  // assignments leave [0, nassign), an assignment index outside [0,
+  // nassign), or more than max_items items is skipped and recorded in *err
+  // (DEV_ERR_RANGE).
+  int E = 0, nassign = 0, max_items = 0;
+  uint32_t wait_limit = kWaitLimit;  // polls of every bounded wait
+  // Test hook: the call's first unit (of whichever slot owns it) is neither
+  // copied nor announced on its barrier, so its consumers' bounded wait runs
+  // out.
+  int drop = 0;
 };
 
 __host__ __device__ inline size_t align128(size_t v) { return (v + 127) & ~(size_t)127; }
@@ -119,6 +132,12 @@ __host__ __device__ inline size_t mxv_smem_bytes(int K, int cg, int u) {
   const int NS = slots_per_cta(K, cg);
   return (size_t)NS * slot_geom(K, NS, cg, u).bytes;
 }
+// The one-token gate/up path also keeps the token's B fragments in shared
+// memory (after the slots): per chunk, per pair of k-steps, per lane t4 of
+// B row 0, 16 bytes; then 16 zero bytes that the other rows read.
+__host__ __device__ inline size_t mxv_x_bytes(int K, int cg) {
+  return (size_t)mxv_nchunks(K, cg) * (2 * cg) * 4 * 16 + 16;
+}
 
 // MODE 0: gate/up (K = H, 8 tokens per group), MODE 1: down (K = I, 4 tokens
 // per group, columns 2t / 2t+1 = hi / lo part of token t).
@@ -156,9 +175,13 @@ __device__ __forceinline__ void mxv_set_up_barriers(const MxvArgs& a, uint64_t* 
 // mbarriers (kMxvBars). Warps beyond the CTA's NS slots only take part in the
 // barrier set-up. With `set_up` false the caller has already run
 // mxv_set_up_barriers, a __syncthreads and the wait for the preceding grid.
-template <int MODE>
+// ONE (gate/up of a single token whose selection the CTA made itself): every
+// item is that token's, so its B fragments are loaded once before the loop,
+// the items need no range check, and only the token's D column is summed.
+template <int MODE, bool ONE = false>
 __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_t* bars,
                                         int cta, int ncta, bool set_up = true) {
+  static_assert(!ONE || MODE == 0, "the one-token path is gate/up only");
   constexpr int GT = MODE == 0 ? 8 : 4;  // tokens per group
   constexpr int CG = mxv_cg(MODE);
   constexpr int U = mxv_unit(MODE);
@@ -205,7 +228,18 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
   if (s >= NS) return;
   const SpanLayout L = span_layout(a.H, a.I);
   const int tpi = (MODE == 0 ? (2 * a.I) / 16 : a.H / 16) / U;  // units per item
-  const int ntiles = (early ? __ldcg(a.n_items) : *a.n_items) * tpi;
+  int n_items = early ? __ldcg(a.n_items) : *a.n_items;
+  if (n_items < 0 || n_items > a.max_items) {
+    if (threadIdx.x == 0) atomicOr(a.err, DEV_ERR_RANGE);
+    n_items = n_items < 0 ? 0 : a.max_items;
+  }
+  const int ntiles = n_items * tpi;
+  // an item the kernels can run: its expert exists and its assignments lie
+  // in the sorted list (the producer and the consumers skip the others alike)
+  auto item_ok = [&](const Item& it) {
+    return ONE || ((unsigned)it.e < (unsigned)a.E && it.cnt >= 1 && it.pos >= 0 &&
+                   it.pos + it.cnt <= a.nassign);
+  };
   const long long nslots = (long long)ncta * NS;
   const long long gs = (long long)cta * NS + s;
   const int t_begin = (int)(ntiles * gs / nslots);
@@ -222,31 +256,50 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
       int issued = 0;
       bool ok = true;
       int cur_item = -1;
+      bool cur_ok = false;
       const uint8_t* span = nullptr;
+      // per stage: armed at least once (bit) and the parity of its last
+      // armed phase (bit), for the final wait on the copies in flight
+      uint32_t armed = 0u, last_par = 0u;
       for (int t = t_begin; t < t_end; ++t) {
         const int item = t / tpi, j = t - item * tpi;
         if (item != cur_item) {
           cur_item = item;
-          const int e = early ? __ldcg(&a.items[item].e) : a.items[item].e;
-          span = a.spans ? reinterpret_cast<const uint8_t*>(
-                               __ldcg(reinterpret_cast<const unsigned long long*>(a.spans) + e))
-                         : a.arena + (size_t)e * a.span_bytes;
+          Item it;
+          if (early) {
+            const int4 v = __ldcg(reinterpret_cast<const int4*>(a.items + item));
+            it = Item{v.x, v.y, v.z, v.w};
+          } else {
+            it = a.items[item];
+          }
+          cur_ok = item_ok(it);
+          if (!cur_ok) {
+            atomicOr(a.err, DEV_ERR_RANGE);
+          } else {
+            span = a.spans ? reinterpret_cast<const uint8_t*>(__ldcg(
+                                 reinterpret_cast<const unsigned long long*>(a.spans) + it.e))
+                           : a.arena + (size_t)it.e * a.span_bytes;
+          }
         }
-        if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
-        uint8_t* dst = ring + (size_t)stage * geo.stage_bytes;
-        mbar_arrive_expect_tx(&full[stage], unit_bytes);
-        bulk_g2s(dst, span + sec_off + (size_t)j * unit_bytes, unit_bytes,
-                 &full[stage], pol);
-        ++issued;
+        if (!cur_ok) continue;
+        if (!mbar_wait(&empty[stage], phase ^ 1, a.wait_limit)) { ok = false; break; }
+        if (a.drop && t == 0) {
+          // test hook: this stage is never filled
+        } else {
+          uint8_t* dst = ring + (size_t)stage * geo.stage_bytes;
+          mbar_arrive_expect_tx(&full[stage], unit_bytes);
+          bulk_g2s(dst, span + sec_off + (size_t)j * unit_bytes, unit_bytes,
+                   &full[stage], pol);
+          armed |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (phase << stage);
+        }
         if (++stage == (uint32_t)S) { stage = 0; phase ^= 1; }
       }
       if (!ok) atomicOr(a.err, DEV_ERR_TIMEOUT);
       // Every copy this lane issued must land before the CTA may exit: wait
       // (bounded) for the last armed phase of each stage.
-      for (int i = 0; i < S && i < issued; ++i) {
-        const int n = (issued - i + S - 1) / S;
-        (void)mbar_wait(&full[i], (uint32_t)((n - 1) & 1));
-      }
+      for (int i = 0; i < S; ++i)
+        if (armed >> i & 1u) (void)mbar_wait(&full[i], last_par >> i & 1u, a.wait_limit);
     }
     return;
   }
@@ -263,6 +316,8 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
   int a_lane = -1;     // sorted[pos + lane] of the current item (cnt <= 32)
   uint32_t bx[4 * CG][2];  // B fragments, 2 registers per k-step of the chunk
   float csc = 1.f;     // down: 2^s of this lane's token (column pair)
+  // gate/up: 2^s of the group's eight tokens (B rows g), one row per warp
+  __shared__ float xsc[kMaxWarps][8];
   int n_epi = 0;
   bool ok = true;
 
@@ -270,18 +325,90 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
   auto assignment = [&](int ti) -> int {
     const int v = __shfl_sync(0xffffffffu, a_lane, ti & 31);
     if (ti >= it.cnt) return -1;
-    return it.cnt <= 32 ? v : a.sorted[it.pos + ti];
+    if (it.cnt <= 32) return v;
+    const int w = a.sorted[it.pos + ti];
+    if ((unsigned)w >= (unsigned)a.nassign) {
+      atomicOr(a.err, DEV_ERR_RANGE);
+      return -1;
+    }
+    return w;
   };
+
+  bool cur_ok = false;
+  // gate/up B fragments of token `tok` (-1: none) for this warp's chunk, as
+  // f16 of x * 2^-s, s putting the largest magnitude of the token's chunk at
+  // exponent 15: bf16's 8-bit significands are then exact in f16 down to
+  // 2^32 below the maximum, and smaller entries keep an absolute error below
+  // 2^-40 of it. A NaN or inf maximum (exponent field 255) keeps s = 112, so
+  // non-finite stays non-finite. Every lane must call; 2^s goes to xsc.
+  auto load_x = [&](int tok) {
+    // pass 1: the raw bf16 pairs and the largest |x| of the chunk (the four
+    // lanes t4 = 0..3 of row g hold it all)
+    uint32_t mbits = 0u;
+#pragma unroll
+    for (int ks = 0; ks < 4 * CG; ++ks) {
+      uint32_t v0 = 0u, v1 = 0u;
+      if (tok >= 0 && ks < 4 * nv) {
+        const uint16_t* xp = a.x + (size_t)tok * a.H + 64 * CG * c + 16 * ks + 2 * t4;
+        v0 = *reinterpret_cast<const uint32_t*>(xp);
+        v1 = *reinterpret_cast<const uint32_t*>(xp + 8);
+      }
+      bx[ks][0] = v0;
+      bx[ks][1] = v1;
+      mbits = max(mbits, max(max(v0 & 0x7FFFu, (v0 >> 16) & 0x7FFFu),
+                             max(v1 & 0x7FFFu, (v1 >> 16) & 0x7FFFu)));
+    }
+    mbits = max(mbits, __shfl_xor_sync(0xffffffffu, mbits, 1));
+    mbits = max(mbits, __shfl_xor_sync(0xffffffffu, mbits, 2));
+    // pass 2: scale and convert in place
+    int sh = 0;
+    if (mbits != 0u) sh = min(max((int)(mbits >> 7) - 127 - 15, -120), 112);
+    const float dn = pow2i(-sh);
+#pragma unroll
+    for (int ks = 0; ks < 4 * CG; ++ks) {
+      const uint32_t w0 = bx[ks][0], w1 = bx[ks][1];
+      bx[ks][0] = f2_to_h2(__uint_as_float(w0 << 16) * dn, __uint_as_float(w0 & 0xFFFF0000u) * dn);
+      bx[ks][1] = f2_to_h2(__uint_as_float(w1 << 16) * dn, __uint_as_float(w1 & 0xFFFF0000u) * dn);
+    }
+    // 2^s of token g, kept in shared memory (not in registers across the
+    // loop, where the B fragments fill the register file)
+    if (t4 == 0) xsc[warp][g] = pow2i(sh);
+    __syncwarp();
+  };
+  // one token: its B fragments for this chunk go to shared memory once
+  // (B row 0 only; the other rows read zeros), and the loop reads them back
+  // per k-step pair, which leaves the register file to the decode pipeline
+  uint4* const xs = reinterpret_cast<uint4*>(smem + (size_t)NS * geo.bytes);
+  const uint4* xsl = xs + (g == 0 ? (size_t)c * (2 * CG) * 4 + t4
+                                  : (size_t)mxv_nchunks(K, CG) * (2 * CG) * 4);
+  const int xstride = g == 0 ? 4 : 0;
+  if (ONE && !reducer) {
+    load_x(g == 0 ? 0 : -1);  // every item is token 0's
+    if (g == 0) {
+#pragma unroll
+      for (int pp = 0; pp < 2 * CG; ++pp)
+        xs[(size_t)(c * (2 * CG) + pp) * 4 + t4] =
+            make_uint4(bx[2 * pp][0], bx[2 * pp][1], bx[2 * pp + 1][0], bx[2 * pp + 1][1]);
+    }
+    if (c == 0 && lane == 0) xs[(size_t)mxv_nchunks(K, CG) * (2 * CG) * 4] = make_uint4(0, 0, 0, 0);
+    __syncwarp();
+  }
 
   for (int t = t_begin; t < t_end && ok; ++t) {
     const int item = t / tpi, j = t - item * tpi;
     if (item != cur_item) {
       cur_item = item;
       it = a.items[item];
-      a_lane = lane < it.cnt ? a.sorted[it.pos + lane] : -1;
+      cur_ok = item_ok(it);
+      a_lane = cur_ok && lane < it.cnt ? a.sorted[it.pos + lane] : -1;
+      if ((unsigned)a_lane >= (unsigned)a.nassign && a_lane != -1) {
+        atomicOr(a.err, DEV_ERR_RANGE);
+        a_lane = -1;
+      }
     }
+    if (!cur_ok) continue;  // skipped by the producer too
     if (!reducer) {
-      ok = mbar_wait(&full[stage], phase);
+      ok = mbar_wait(&full[stage], phase, a.wait_limit);
       if (!ok) break;
     }
     const uint8_t* tile = ring + (size_t)stage * geo.stage_bytes;
@@ -294,22 +421,12 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
         // ---- B fragments of this token group (reloaded only when they change)
         if (item != loaded_grp >> 16 || grp != (loaded_grp & 0xFFFF)) {
           if (MODE == 0) {
-            const int aa = assignment(grp + g);
-            const int tok = aa >= 0 ? aa / a.k : -1;
-            if (tok != loaded_tok) {
-              loaded_tok = tok;
-  #pragma unroll
-              for (int ks = 0; ks < 4 * CG; ++ks) {
-                uint32_t v0 = 0u, v1 = 0u;
-                if (tok >= 0 && ks < 4 * nv) {
-                  const uint16_t* xp = a.x + (size_t)tok * a.H + 64 * CG * c + 16 * ks + 2 * t4;
-                  const uint32_t w0 = *reinterpret_cast<const uint32_t*>(xp);
-                  const uint32_t w1 = *reinterpret_cast<const uint32_t*>(xp + 8);
-                  v0 = f2_to_h2(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xFFFF0000u));
-                  v1 = f2_to_h2(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xFFFF0000u));
-                }
-                bx[ks][0] = v0;
-                bx[ks][1] = v1;
+            if (!ONE) {
+              const int aa = assignment(grp + g);
+              const int tok = aa >= 0 ? aa / a.k : -1;
+              if (__any_sync(0xffffffffu, tok != loaded_tok)) {
+                loaded_tok = tok;
+                load_x(tok);
               }
             }
           } else {
@@ -331,7 +448,7 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
             int sh = 0;
             if (m > 0.f) {
               const int e = (int)((__float_as_uint(m) >> 23) & 0xFF) - 127;
-              sh = min(max(e - 14, -100), 100);
+              sh = min(max(e - 14, -112), 112);
             }
             const float dn = pow2i(-sh);
             const bool lo = (g & 1) != 0;
@@ -380,14 +497,20 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
                 decode_word(w[2 * hb], a0);
                 decode_word(w[2 * hb + 1], a1);
                 float d[4];
-                mma16816(d, a0, bx[4 * v + 2 * hb][0], bx[4 * v + 2 * hb][1], zero);
-                mma16816(d, a1, bx[4 * v + 2 * hb + 1][0], bx[4 * v + 2 * hb + 1][1], d);
+                if (ONE) {
+                  const uint4 bb = lds128(xsl + (size_t)(2 * v + hb) * xstride);
+                  mma16816(d, a0, bb.x, bb.y, zero);
+                  mma16816(d, a1, bb.z, bb.w, d);
+                } else {
+                  mma16816(d, a0, bx[4 * v + 2 * hb][0], bx[4 * v + 2 * hb][1], zero);
+                  mma16816(d, a1, bx[4 * v + 2 * hb + 1][0], bx[4 * v + 2 * hb + 1][1], d);
+                }
                 const float sg = __uint_as_float(((sc >> (8 * hb)) & 0xFFu) << 23);
                 const float sg8 = __uint_as_float(((sc >> (16 + 8 * hb)) & 0xFFu) << 23);
                 acc[st][0] = fmaf(d[0], sg, acc[st][0]);
-                acc[st][1] = fmaf(d[1], sg, acc[st][1]);
+                if (!ONE) acc[st][1] = fmaf(d[1], sg, acc[st][1]);
                 acc[st][2] = fmaf(d[2], sg8, acc[st][2]);
-                acc[st][3] = fmaf(d[3], sg8, acc[st][3]);
+                if (!ONE) acc[st][3] = fmaf(d[3], sg8, acc[st][3]);
               }
             }
           }
@@ -403,6 +526,17 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
             acc[st][0] = (acc[st][0] + acc[st][1]) * csc;
             acc[st][2] = (acc[st][2] + acc[st][3]) * csc;
           }
+        } else {
+          // undo the scales of this lane's D columns 2t4, 2t4+1 (tokens
+          // 2t4, 2t4+1 of the group)
+          const float2 cs = lds_f2(&xsc[warp][2 * t4]);
+#pragma unroll
+          for (int st = 0; st < U; ++st) {
+            acc[st][0] *= cs.x;
+            acc[st][1] *= cs.y;
+            acc[st][2] *= cs.x;
+            acc[st][3] *= cs.y;
+          }
         }
       }
 
@@ -413,7 +547,7 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
       const int r = n_epi % kRedRing, u = n_epi / kRedRing;
       float4* rb = reinterpret_cast<float4*>(red) + (size_t)r * NCH * U * 32;  // [c][st][lane]
       if (!reducer) {
-        if (u >= 1 && !mbar_wait(&rempty[r], (u - 1) & 1)) { ok = false; break; }
+        if (u >= 1 && !mbar_wait(&rempty[r], (u - 1) & 1, a.wait_limit)) { ok = false; break; }
 #pragma unroll
         for (int st = 0; st < U; ++st)
           rb[(c * U + st) * 32 + lane] = make_float4(acc[st][0], acc[st][1], acc[st][2], acc[st][3]);
@@ -421,7 +555,7 @@ __device__ __forceinline__ void mxv_cta(const MxvArgs& a, uint8_t* smem, uint64_
         if (lane == 0) mbar_arrive(&rfull[r]);
       }
       if (reducer || (!own_reducer && c == n_epi % NCH)) {
-        if (!mbar_wait(&rfull[r], u & 1)) { ok = false; break; }
+        if (!mbar_wait(&rfull[r], u & 1, a.wait_limit)) { ok = false; break; }
 #pragma unroll
         for (int st = 0; st < U; ++st) {
           float4 sum = rb[st * 32 + lane];

@@ -63,6 +63,8 @@ extern "C" DF_MOE_API int df_moe_route_noalloc(const float* router, int32_t E,
   if (!router || !x_bf16 || !ids || !weights)
     return fail(DF_MOE_EINVAL, "router, x, ids and weights are required");
   if ((uintptr_t)x_bf16 & 15) return fail(DF_MOE_EINVAL, "x must be 16-byte aligned");
+  // the router kernel reads the weights with 16-byte loads
+  if ((uintptr_t)router & 15) return fail(DF_MOE_EINVAL, "router must be 16-byte aligned");
   if (H <= 0 || H % 32 || H > 8192)
     return fail(DF_MOE_EINVAL, "H must be a multiple of 32 in [32, 8192]");
   if (E < 1 || E > 1024) return fail(DF_MOE_EINVAL, "E must be in [1, 1024]");
@@ -79,8 +81,11 @@ extern "C" DF_MOE_API int df_moe_route_noalloc(const float* router, int32_t E,
   int rc = scratch_address(&scratch);
   if (rc) return rc;
   cudaStream_t s = (cudaStream_t)stream;
+  // an ordinary launch, not a programmatic dependent: here the router
+  // weights are the caller's, and the caller's kernel just before this call
+  // may have written them
   cudaError_t e = dfm::launch_router(router, E, H, (const uint16_t*)x_bf16, T,
-                                     scratch, sp, s);
+                                     scratch, sp, s, nullptr, /*after_previous=*/false);
   if (e != cudaSuccess)
     return fail(DF_MOE_ECUDA, "router launch: %s", cudaGetErrorString(e));
   e = dfm::launch_topk(scratch, sp.nsplit, T, E, k, nullptr, ids, weights,

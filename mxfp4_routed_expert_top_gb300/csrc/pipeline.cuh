@@ -8,6 +8,8 @@
 namespace dfm {
 
 constexpr uint32_t kWaitLimit = 1u << 24;
+// The test hook's short limit: a wait that nothing will end gives up quickly.
+constexpr uint32_t kTestWaitLimit = 1u << 12;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -49,9 +51,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+// Bounded wait for the phase with the given parity to complete: at most
+// `limit` polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint32_t limit = kWaitLimit) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
@@ -89,6 +93,14 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
 __device__ __forceinline__ uint32_t lds_u32(const void* p) {
   uint32_t v;
   asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)));
+  return v;
+}
+
+// A float pair from shared memory, read again at every call (volatile: the
+// compiler keeps no copy of it in registers).
+__device__ __forceinline__ float2 lds_f2(const void* p) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(smem_u32(p)));
   return v;
 }
 

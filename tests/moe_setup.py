@@ -106,6 +106,34 @@ def draw_tokens(setup, T, first_id=0):
     return np.stack(out)
 
 
+def scaled_bits(x, p):
+    """bf16 bits of x * 2^p (exact: a power of two, no overflow or underflow)."""
+    f = (np.asarray(x, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+    y = f * np.float32(2.0 ** p)
+    assert np.all(np.isfinite(y)) and np.all((y == 0) == (f == 0))
+    return (y.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def range_tokens(setup, first_id, chunk=512):
+    """Three tokens at the edges of the hidden state's range: one scaled by
+    2^20 (~1e6), one by 2^-60 (~1e-18), and one whose first 512-column chunk
+    is scaled by 2^20 and second by 2^-40 (the rest N(0,1)). Scaling a token
+    by a power of two scales its logits exactly, so tokens that passed the
+    gap rule still pass it; the mixed token is checked on its own."""
+    wl = setup.wl
+    base = draw_tokens(setup, 2, first_id=first_id)
+    big, small = scaled_bits(base[0], 20), scaled_bits(base[1], -60)
+    for r in range(synth.gen.REDRAWS_PER_TOKEN):
+        x = synth.token(wl.seed, wl.cfg_id, first_id + 2, wl.H, redraw=r)
+        mixed = x.copy()
+        c1 = min(chunk, wl.H // 2)
+        mixed[:c1] = scaled_bits(x[:c1], 20)
+        mixed[c1:2 * c1] = scaled_bits(x[c1:2 * c1], -40)
+        if gap_ok(orc.router_logits(setup.routers[0], mixed), wl.k):
+            return np.stack([big, small, mixed])
+    raise RuntimeError("no mixed token passed the gap rule")
+
+
 def draw_stack_token(setup, token_id):
     """One token for a stack workload that passes the gap rule at every
     layer; returns (x, oracle result of the stack for it)."""

@@ -13,7 +13,7 @@ import pytest
 import oracle as orc
 import synth
 from moe_setup import (Setup, bits_to_f64, check_ids_weights, check_out,
-                       draw_tokens, rel_l2, to_dev_bf16)
+                       draw_tokens, range_tokens, rel_l2, to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -167,9 +167,33 @@ def test_prefill_batch512(k3, torch):
     out, out32, ids, w = _forward(k3.m, x, T, torch)
     rid, rw = orc.topk_softmax(orc.router_logits(k3.routers[0], x), WL1.k)
     check_ids_weights(ids, w, rid, rw)          # every token's routing
-    sample = [0, 1, 77, 255, 300, 511]          # full outputs on a sample
+    # full outputs on every eighth token and the last one (65 of 512)
+    sample = list(range(0, T, 8)) + [T - 1]
     ref = orc.moe_layer(k3.layers[0], x[sample])
     check_out(out32[sample], ref["out"])
+    # and every token's output is finite with the bf16 output its rounding
+    assert np.all(np.isfinite(out32))
+    rne = torch.from_numpy(out32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(out, rne)
+
+
+@pytest.mark.parametrize("T", [1, 8, 16])
+def test_input_range(k3, torch, T):
+    """Hidden states at the edges of the range: a token scaled by 2^20, one
+    by 2^-60, one with a 2^20 chunk and a 2^-40 chunk. T = 1 runs each on
+    its own (the decode chain), T = 8 and T = 16 mix them with N(0,1)
+    tokens (decode batch and the tcgen05 batch path)."""
+    xs = range_tokens(k3, first_id=60000)
+    if T > 1:
+        xs = np.concatenate([xs, _tokens(k3, WL2, T - 3, first_id=60100)])
+    batches = [xs[i:i + 1] for i in range(3)] if T == 1 else [xs]
+    for x in batches:
+        n = x.shape[0]
+        out, out32, ids, w = _forward(k3.m, x, n, torch)
+        assert np.all(np.isfinite(out32))
+        ref = orc.moe_layer(k3.layers[0], x)
+        check_ids_weights(ids, w, ref["ids"], ref["w"])
+        check_out(out32, ref["out"])
 
 
 def test_ragged_batch(k3, torch):

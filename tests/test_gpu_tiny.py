@@ -14,7 +14,7 @@ import pytest
 import oracle as orc
 import synth
 from moe_setup import (Setup, bits_to_f64, check_ids_weights, check_out,
-                       draw_tokens, rel_l2, to_dev_bf16)
+                       draw_tokens, range_tokens, rel_l2, to_dev_bf16)
 
 pytestmark = pytest.mark.gpu
 
@@ -297,3 +297,84 @@ def test_one_token_selects_in_the_gateup_phase(tiny, torch, T):
     ref = orc.moe_layer(tiny.layers[0], x)
     check_ids_weights(ids.cpu().numpy(), w.cpu().double().numpy(), ref["ids"], ref["w"])
     check_out(out32.cpu().double().numpy(), ref["out"])
+
+
+# ---- the input range of the decode paths ----------------------------------
+# A hidden state may hold any bf16 value. The decode GEMVs multiply x as f16
+# after scaling each (token, 512-column chunk) by a power of two, so large
+# (2^20 ~ 1e6) and small (2^-60 ~ 1e-18) tokens are exact as well. Scaling a
+# token by a power of two scales its logits exactly, so tokens that pass the
+# gap rule still do; the mixed token is checked on its own.
+
+@pytest.mark.parametrize("T", [1, 3, 9])
+def test_forward_input_range(tiny, torch, T):
+    """Decode batches (T = 1 for each token, T = 3 for all three) and the
+    batch path (T = 9: the three tokens and six N(0,1) ones)."""
+    xs = range_tokens(tiny, first_id=30000)
+    if T == 9:
+        xs = np.concatenate([xs, draw_tokens(tiny, 6, first_id=30100)])
+    batches = [xs[i:i + 1] for i in range(3)] if T == 1 else [xs]
+    for x in batches:
+        n = x.shape[0]
+        out, out32, ids, w = _forward(tiny.m, x, n, torch)
+        assert np.all(np.isfinite(out32))
+        ref = orc.moe_layer(tiny.layers[0], x)
+        check_ids_weights(ids[0], w[0], ref["ids"], ref["w"])
+        check_out(out32, ref["out"])
+
+
+def test_gateup_step_input_range(tiny, torch):
+    """The gate/up step on its own at the single-step bar (1e-5)."""
+    x = range_tokens(tiny, first_id=30200)
+    rid, _ = _oracle_route(tiny, x)
+    hbuf = torch.empty((3 * WL.k, WL.I), dtype=torch.float32, device="cuda")
+    tiny.m.step_expert_gateup(0, to_dev_bf16(x), 3, torch.from_numpy(rid).cuda(), hbuf)
+    torch.cuda.synchronize()
+    got = hbuf.cpu().double().numpy()
+    for t in range(3):
+        for j in range(WL.k):
+            ref = orc.expert_gateup(tiny._span(0, rid[t, j]), WL.H, WL.I, bits_to_f64(x[t]))
+            assert rel_l2(got[t * WL.k + j], ref) <= 1e-5
+
+
+# ---- E8M0 codes 0 and 255 -------------------------------------------------
+# The generator never draws them (scales are 2^-8 .. 2^0). The oracle decodes
+# them as the format defines them, 2^-127 and NaN. The decode GEMVs read code
+# 0 as 0 (a block of 2^-127 weights adds below 1e-37 here, invisible at the
+# stated bars) and code 255 as +inf: every output that the oracle makes NaN
+# comes out non-finite.
+
+def _gate_scale_offset(row, block):
+    q = WL.H * WL.I // 2
+    return q + row * (WL.H // 32) + block
+
+
+def test_e8m0_code_zero(tiny, torch):
+    spans = synth.expert_spans(WL.seed, WL.wcfg, 0, 0, WL.E, WL.H, WL.I)
+    for e in range(WL.E):
+        for row in (0, 7, 33):
+            spans[e, _gate_scale_offset(row, 2)] = 0
+    x = draw_tokens(tiny, 2, first_id=30300)
+    with _host_handle(torch, spans, tiny.routers[0], tiny.shared[0]) as m:
+        out, out32, ids, w = _forward(m, x, 2, torch)
+    L = orc.Layer(WL.H, WL.E, WL.k, WL.I, WL.Is, tiny.routers[0], tiny.shared[0],
+                  lambda l, e: spans[e])
+    ref = orc.moe_layer(L, x)
+    check_ids_weights(ids[0], w[0], ref["ids"], ref["w"])
+    check_out(out32, ref["out"])
+
+
+def test_e8m0_code_255(tiny, torch):
+    spans = synth.expert_spans(WL.seed, WL.wcfg, 0, 0, WL.E, WL.H, WL.I)
+    for e in range(WL.E):
+        spans[e, _gate_scale_offset(3, 1)] = 255
+    x = draw_tokens(tiny, 1, first_id=30400)
+    with _host_handle(torch, spans, tiny.routers[0], tiny.shared[0]) as m:
+        out, out32, ids, w = _forward(m, x, 1, torch)
+    L = orc.Layer(WL.H, WL.E, WL.k, WL.I, WL.Is, tiny.routers[0], tiny.shared[0],
+                  lambda l, e: spans[e])
+    ref = orc.moe_layer(L, x)
+    nan = np.isnan(ref["out"])
+    assert nan.any()
+    assert not np.any(np.isfinite(out32[nan]))
+    assert np.array_equal(np.isfinite(out32), ~nan)
