@@ -230,6 +230,77 @@ void orc_rmsnorm_bf16(const uint16_t* x, int T, int H, double eps,
   }
 }
 
+// ---- MXFP8 (OCP microscaling, E4M3 elements) ----------------------------
+// The element type is FP8 E4M3 as the OCP 8-bit floating point format
+// defines it: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits, subnormals
+// at exponent field 0, no infinities, and S.1111.111 the only NaN; the largest
+// finite magnitude is 1.75 * 2^8 = 448. The block scale is E8M0 (2^(e-127)).
+// The conversion of a block follows the OCP MX specification's recipe: the
+// shared exponent is floor(log2(max|v|)) minus the element type's largest
+// exponent (8 for E4M3), and each element is v / 2^shared rounded to the
+// element type.
+
+double orc_e4m3_value(uint8_t code) {
+  const int sgn = code >> 7, ex = (code >> 3) & 15, man = code & 7;
+  if (ex == 15 && man == 7) return NAN;
+  const double mag = ex == 0 ? std::ldexp((double)man, -9)              // 2^-6 * m/8
+                             : std::ldexp(1.0 + man / 8.0, ex - 7);
+  return sgn ? -mag : mag;
+}
+
+uint8_t orc_e4m3_from_f64(double v) {
+  const uint8_t sgn = std::signbit(v) ? 0x80 : 0x00;
+  double a = std::fabs(v);
+  if (a >= 448.0) return (uint8_t)(sgn | 0x7E);  // saturate: 1.110 * 2^8
+  // spacing of E4M3 values near a: 2^(e - 3) for a in [2^e, 2^(e+1)),
+  // e >= -6; the subnormal spacing 2^-9 below 2^-6
+  int e = -7;
+  if (a >= std::ldexp(1.0, -6)) {
+    std::frexp(a, &e);  // a in [2^(e-1), 2^e)
+    e -= 1;
+  }
+  const int q = e >= -6 ? e - 3 : -9;
+  const double r = std::nearbyint(std::ldexp(a, -q));  // ties to even
+  const double rv = std::ldexp(r, q);
+  if (rv > 448.0) return (uint8_t)(sgn | 0x7E);
+  // encode rv exactly
+  if (rv < std::ldexp(1.0, -6)) return (uint8_t)(sgn | (uint8_t)std::ldexp(rv, 9));
+  int re;
+  const double fr = std::frexp(rv, &re);  // rv = fr * 2^re, fr in [0.5, 1)
+  const int ex = re - 1 + 7;
+  const int man = (int)std::ldexp(fr * 2.0 - 1.0, 3);
+  return (uint8_t)(sgn | (ex << 3) | man);
+}
+
+uint8_t orc_mxfp8_block(const double* v, uint8_t* codes) {
+  double amax = 0.0;
+  for (int i = 0; i < 32; ++i) amax = std::max(amax, std::fabs(v[i]));
+  int shared = -127;
+  if (amax > 0.0) {
+    int e;
+    std::frexp(amax, &e);  // amax in [2^(e-1), 2^e): floor(log2) = e - 1
+    shared = std::min(127, std::max(-127, e - 1 - 8));
+  }
+  for (int i = 0; i < 32; ++i) codes[i] = orc_e4m3_from_f64(std::ldexp(v[i], -shared));
+  return (uint8_t)(shared + 127);
+}
+
+void orc_mxfp8_quantize(const double* v, int rows, int n, uint8_t* codes,
+                        uint8_t* scales) {
+  for (int r = 0; r < rows; ++r)
+    for (int b = 0; b < n / 32; ++b)
+      scales[(size_t)r * (n / 32) + b] =
+          orc_mxfp8_block(v + (size_t)r * n + 32 * b, codes + (size_t)r * n + 32 * b);
+}
+
+void orc_mxfp8_dequant(const uint8_t* codes, const uint8_t* scales, int rows,
+                       int n, double* v) {
+  for (int r = 0; r < rows; ++r)
+    for (int i = 0; i < n; ++i)
+      v[(size_t)r * n + i] = orc_e4m3_value(codes[(size_t)r * n + i]) *
+                             orc_e8m0_value(scales[(size_t)r * (n / 32) + i / 32]);
+}
+
 int orc_moe_layer(const orc_layer* L, const uint16_t* x, int T,
                   const uint16_t* residual, double* out, int32_t* ids,
                   double* w, double* logits_out, double* routed_out,

@@ -85,6 +85,26 @@ int orc_group(const int32_t* ids, int T, int k, int E, int32_t* offs,
 void orc_rmsnorm_bf16(const uint16_t* x, int T, int H, double eps,
                       uint16_t* xn);
 
+/* ---- MXFP8 activations (the lossy variant) ------------------------------
+ * Kimi K3 is trained quantisation-aware with MXFP4 weights and MXFP8
+ * activations (Deltafin analysis, section 2.1). The activation format is the
+ * OCP microscaling one: blocks of 32 elements along the contraction, each an
+ * FP8 E4M3 value, sharing one E8M0 exponent. */
+double orc_e4m3_value(uint8_t code);   /* bias 7, no inf; 0x7F / 0xFF NaN  */
+/* Nearest E4M3 code of v, ties to even, |v| above 448 saturating to 448
+ * (E4M3 has no inf); v finite. */
+uint8_t orc_e4m3_from_f64(double v);
+/* One block: X = 2^(floor(log2(max|v|)) - 8), exponent clamped to
+ * [-127, 127] (an all-zero block takes 2^-127); codes[i] =
+ * e4m3(v[i] / X), scale = the E8M0 code of X. v finite. Returns the scale. */
+uint8_t orc_mxfp8_block(const double* v, uint8_t* codes);
+/* Rows of n elements (n % 32 == 0): codes [rows][n], scales [rows][n/32]. */
+void orc_mxfp8_quantize(const double* v, int rows, int n, uint8_t* codes,
+                        uint8_t* scales);
+/* The dequantised values: codes[i] * 2^(scale - 127). */
+void orc_mxfp8_dequant(const uint8_t* codes, const uint8_t* scales, int rows,
+                       int n, double* v);
+
 /* ---- whole layer / stack ------------------------------------------------ */
 /* Expert spans are fetched on demand, once per needed expert, from the
  * calling thread: get_span(ctx, layer, expert) returns a canonical span. */

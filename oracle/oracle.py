@@ -75,6 +75,10 @@ def lib():
         L.orc_moe_stack.argtypes = [ctypes.POINTER(_Layer), i32, vp, i32, dbl, vp,
                                     vp, vp, vp, vp]
         L.orc_moe_stack.restype = i32
+        L.orc_e4m3_value.argtypes = [ctypes.c_uint8]; L.orc_e4m3_value.restype = dbl
+        L.orc_e4m3_from_f64.argtypes = [dbl]; L.orc_e4m3_from_f64.restype = ctypes.c_uint8
+        L.orc_mxfp8_quantize.argtypes = [vp, i32, i32, vp, vp]
+        L.orc_mxfp8_dequant.argtypes = [vp, vp, i32, i32, vp]
         L.orc_num_threads.restype = i32
         L.orc_set_num_threads.argtypes = [i32]
         _lib = L
@@ -211,6 +215,73 @@ def rmsnorm_bf16(x, eps):
     out = np.empty_like(x)
     lib().orc_rmsnorm_bf16(_p(x), T, H, eps, _p(out))
     return out
+
+
+# ---- MXFP8 activations (the lossy variant) ----------------------------------
+
+def e4m3_value(code):
+    return lib().orc_e4m3_value(code)
+
+
+def e4m3_from_f64(v):
+    return lib().orc_e4m3_from_f64(float(v))
+
+
+def mxfp8_quantize(v):
+    """Rows of v (last dimension a multiple of 32) -> (codes u8, scales u8)."""
+    v = _c(v, np.float64)
+    shp = v.shape
+    n = shp[-1]
+    rows = v.size // n
+    codes = np.empty(shp, dtype=np.uint8)
+    scales = np.empty(shp[:-1] + (n // 32,), dtype=np.uint8)
+    lib().orc_mxfp8_quantize(_p(v), rows, n, _p(codes), _p(scales))
+    return codes, scales
+
+
+def mxfp8_dequant(codes, scales):
+    codes = _c(codes, np.uint8); scales = _c(scales, np.uint8)
+    n = codes.shape[-1]
+    rows = codes.size // n
+    v = np.empty(codes.shape, dtype=np.float64)
+    lib().orc_mxfp8_dequant(_p(codes), _p(scales), rows, n, _p(v))
+    return v
+
+
+def mxfp8_round(v):
+    """The values the MXFP8 format holds for v (quantise, then dequantise)."""
+    return mxfp8_dequant(*mxfp8_quantize(v))
+
+
+def moe_layer_mxfp8(layer, x_bf16, residual=None, h_in=None):
+    """The layer with MXFP8 activations into the routed experts: every routed
+    expert takes x rounded to MXFP8, and its down projection takes h rounded
+    to MXFP8; router and shared experts are exact. h_in (optional, [T*k][I]
+    in the order t*k + j) replaces the oracle's own h before its rounding, so
+    that a caller can feed the h of the device (the rounding then decides on
+    the same values). Returns dict(out, ids, w, routed, shared, h)."""
+    L = layer.s
+    H, I, k = L.H, L.I, L.k
+    x = _c(x_bf16, np.uint16).reshape(-1, H)
+    T = x.shape[0]
+    ref = moe_layer(layer, x, residual)
+    ids, w = ref["ids"], ref["w"]
+    xd = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    xq = mxfp8_round(xd)
+    routed = np.zeros((T, H))
+    hs = np.empty((T * k, I))
+    for t in range(T):
+        for j in range(k):
+            span = layer._spans(L.layer, int(ids[t, j]))
+            h = expert_gateup(span, H, I, xq[t])
+            hs[t * k + j] = h
+            hh = h if h_in is None else np.asarray(h_in[t * k + j], dtype=np.float64)
+            routed[t] += w[t, j] * expert_down(span, H, I, mxfp8_round(hh[None, :])[0])
+    res = 0.0 if residual is None else (
+        (_c(residual, np.uint16).reshape(T, H).astype(np.uint32) << 16)
+        .view(np.float32).astype(np.float64))
+    out = res + (routed + ref["shared"])
+    return dict(out=out, ids=ids, w=w, routed=routed, shared=ref["shared"], h=hs)
 
 
 # ---- layer / stack ----------------------------------------------------------
