@@ -68,6 +68,9 @@ def parse():
                    help="consecutive steps take consecutive tokens of a stream whose "
                         "neighbours have this correlation (0.7: ~31%% of the experts "
                         "reused from the previous token); 0: independent tokens")
+    p.add_argument("--mxfp8", action="store_true",
+                   help="the lossy MXFP8-activation variant (DF_MOE_MXFP8_ACT): routed "
+                        "experts on block-scaled MXFP4 x MXFP8 tcgen05 GEMMs")
     p.add_argument("--experts", type=int, default=0,
                    help="profiling aid: override the routed-expert count (same "
                         "per-token work, smaller resident set); not a bench line")
@@ -95,6 +98,16 @@ def gateup_bytes(wl, n_union, T, with_shared=False):
     if with_shared:
         b += wl.n_shared * 2 * wl.Is * wl.H * 2 + T * wl.n_shared * wl.Is * 4
     return b
+
+
+def mx8_gateup_bytes(wl, n_union, T):
+    """Algorithmic bytes of the MXFP8 variant's gate/up GEMM: the gate and up
+    halves of every distinct selected expert (codes + scales), the E4M3 x rows
+    of the T*k assignments with their scales in, and the E4M3 h rows with
+    their scales out."""
+    per_expert = 2 * wl.I * wl.H * 17 // 32
+    rows = T * wl.k
+    return n_union * per_expert + rows * (wl.H + wl.H // 32) + rows * (wl.I + wl.I // 32)
 
 
 def gateup_flops(wl, T):
@@ -304,7 +317,8 @@ def run_ours(args):
         wl = dataclasses.replace(wl, T=args.tokens, name=wl.name + "-t%d" % args.tokens)
     T = wl.T
     flags = ((dfm.STACK_RMSNORM_RESIDUAL if wl.stack else 0)
-             | (dfm.PREFILL_MMA_SYNC if args.mma_sync_prefill else 0))
+             | (dfm.PREFILL_MMA_SYNC if args.mma_sync_prefill else 0)
+             | (dfm.MXFP8_ACT if args.mxfp8 else 0))
     if args.cache_slots and T > 8:
         raise SystemExit("--cache-slots serves decode batches (<= 8 tokens)")
     m = dfm.MoE(wl.H, wl.E, wl.k, wl.I, wl.n_shared, wl.Is, n_layers=wl.L,
@@ -481,7 +495,9 @@ def run_ours(args):
     lb = layer_bytes(wl, u_mean, T) * wl.L
     # dominant kernel: the routed gate/up GEMM (tcgen05, larger batches),
     # else the gate/up phase of decode batches
-    if kt.get("gemm_gateup", (0, 0.0))[0]:
+    if kt.get("mx8_gateup", (0, 0.0))[0]:
+        dom, dom_bytes = "mx8_gateup", mx8_gateup_bytes(wl, u_mean, T)
+    elif kt.get("gemm_gateup", (0, 0.0))[0]:
         dom, dom_bytes = "gemm_gateup", gateup_bytes(wl, u_mean, T)
     else:
         # decode batches: the gate/up phase kernel streams the routed and the
@@ -497,19 +513,26 @@ def run_ours(args):
         "metric": METRIC, "value": round(tokens / dev_s_max, 2), "unit": UNIT,
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None,
+        "dtype": "e2m1 x e4m3, f32 accumulate" if args.mxfp8 else "f32",
+        "data": "synthetic",
         "impl": "ours",
         "config": {**workload_config(wl, ws),
                    "l2": "flushed (256 MiB write) before every timed step",
                    "launch": "cuda graph" if args.graph else "stream",
                    "prefill_path": "mma_sync" if args.mma_sync_prefill else "tcgen05",
+                   "activations": ("MXFP8 (E4M3, E8M0 per 32) into the routed experts: "
+                                   "the lossy variant") if args.mxfp8 else "exact",
                    "experts_home": ("pinned host memory, %d a layer cached in HBM"
                                     % args.cache_slots) if args.cache_slots else "HBM",
                    "tokens": ("AR(1) stream, neighbour correlation %g" % args.token_corr)
                              if args.token_corr else "independent N(0,1)"},
         "step_us": {"median": round(float(np.median(step_ms)) * 1e3, 2),
+                    "mean": round(float(np.mean(step_ms)) * 1e3, 2),
                     "p10": round(float(np.percentile(step_ms, 10)) * 1e3, 2),
-                    "p90": round(float(np.percentile(step_ms, 90)) * 1e3, 2)},
+                    "p90": round(float(np.percentile(step_ms, 90)) * 1e3, 2),
+                    "max": round(float(np.max(step_ms)) * 1e3, 2),
+                    "max_step": int(np.argmax(step_ms))},
         "layer_hbm": {"achieved_gbs": round(layer_gbs, 1), "bytes_per_step": int(lb),
                       "frac_of_measured": round(layer_gbs / peak, 4),
                       "stream_read_gbs": round(stream_read_gbs, 1),
@@ -542,12 +565,20 @@ def tensor_use(kt, wl, T):
     the assignments' flops over its average launch time, against the
     measured dense bf16 peak. At a few tokens per expert the GEMM is HBM
     bound, so this fraction is small by construction."""
-    n, t = kt.get("gemm_gateup", (0, 0.0))
+    kern, ratio = "gemm_gateup", 1.0
+    n, t = kt.get(kern, (0, 0.0))
+    if not n:
+        # the MXFP8 variant: E4M3 x E2M1 on the fp8 pipe, nominally twice bf16
+        kern, ratio = "mx8_gateup", 2.0
+        n, t = kt.get(kern, (0, 0.0))
     if not n:
         return None
     peak, src = measured_bf16_tflops()
+    peak *= ratio
+    if ratio != 1.0:
+        src += " bf16 x 2 (nominal fp8/bf16 ratio)"
     tf = gateup_flops(wl, T) / (t / n / 1e3) / 1e12
-    return {"kernel": "gemm_gateup", "achieved": round(tf, 2), "peak": peak, "unit": "TFLOP/s",
+    return {"kernel": kern, "achieved": round(tf, 2), "peak": peak, "unit": "TFLOP/s",
             "frac": round(tf / peak, 4), "peak_source": src}
 
 

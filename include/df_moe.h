@@ -69,6 +69,17 @@ extern "C" {
  * accumulators in tensor memory). For comparison; same results within the
  * stated tolerances. */
 #define DF_MOE_PREFILL_MMA_SYNC 4u
+/* The lossy MXFP8-activation variant: the inputs of the routed experts (x
+ * into gate/up, h into down) are rounded to MXFP8 — blocks of 32 along the
+ * contraction, E4M3 elements sharing an E8M0 exponent, the exponent
+ * floor(log2 max|v|) - 8, elements rounded to nearest even and saturated at
+ * 448 — and the experts run as grouped GEMMs on the 5th-generation tensor
+ * cores' block-scaled MXFP4 x MXFP8 MMA. Kimi K3 is trained with MXFP8
+ * activations (Deltafin analysis, section 2.1); the pages' reference runs
+ * keep activations exact, and so does every handle without this flag. The
+ * router and the shared experts stay exact. Needs hidden and inter multiples
+ * of 128; not with an expert cache or DF_MOE_PREFILL_MMA_SYNC. */
+#define DF_MOE_MXFP8_ACT 8u
 
 typedef struct df_moe df_moe; /* opaque, library-owned */
 
@@ -82,7 +93,8 @@ typedef struct {
   int32_t n_layers;     /* L >= 1                                              */
   int32_t max_tokens;   /* largest T a forward call may use (1..4096)          */
   float rms_eps;        /* stack mode only                                     */
-  uint32_t flags;       /* DF_MOE_STACK_RMSNORM_RESIDUAL | DF_MOE_PREFILL_MMA_SYNC */
+  uint32_t flags;       /* DF_MOE_STACK_RMSNORM_RESIDUAL | DF_MOE_PREFILL_MMA_SYNC |
+                           DF_MOE_MXFP8_ACT */
 } df_moe_config;
 
 /* Weights of one layer, any subset per call (NULL / 0 = leave unchanged). */
@@ -266,6 +278,13 @@ DF_MOE_API int df_moe_step_expert_gateup(df_moe* h, int32_t layer, const void* x
 DF_MOE_API int df_moe_step_expert_down(df_moe* h, int32_t layer, const float* hbuf,
                             int32_t T, const int32_t* ids,
                             const float* weights, float* y, void* stream);
+/* With DF_MOE_MXFP8_ACT the two expert steps take MXFP8 activations: gate/up
+ * rounds x first (hbuf is h before its own rounding), down rounds hbuf first.
+ * The rounding alone, with the same kernels' routine: v device [rows][n] fp32
+ * (n a multiple of 32, 16-byte aligned) -> codes device [rows][n] E4M3 bytes,
+ * scales device [rows][n/32] E8M0 bytes. Any handle. Errors: EINVAL. */
+DF_MOE_API int df_moe_step_mxfp8(df_moe* h, const float* v, int32_t rows, int32_t n,
+                                 uint8_t* codes, uint8_t* scales, void* stream);
 /* y device [T][H] fp32 = sum over shared experts. */
 DF_MOE_API int df_moe_step_shared(df_moe* h, int32_t layer, const void* x_bf16, int32_t T,
                        float* y, void* stream);
@@ -282,7 +301,7 @@ DF_MOE_API int df_moe_read_expert_span(df_moe* h, int32_t layer, int32_t expert,
  * With timing on, every kernel launch of forward is bracketed by CUDA events
  * on its stream; df_moe_timing_get returns, per kernel kind, the launches and
  * the summed device time since the last reset. */
-#define DF_MOE_KERNEL_KINDS 16
+#define DF_MOE_KERNEL_KINDS 18
 DF_MOE_API int df_moe_timing_enable(df_moe* h, int on);
 DF_MOE_API int df_moe_timing_reset(df_moe* h);
 DF_MOE_API int df_moe_timing_get(df_moe* h, int kind, const char** name,

@@ -14,7 +14,8 @@ LIB_PATH = os.path.join(PKG, "libdfmoe.so")
 OK, EINVAL, ENOMEM, ECUDA, ESTATE, ERANGE, ETIMEOUT, EDEVICE = 0, -1, -2, -3, -4, -5, -6, -7
 STACK_RMSNORM_RESIDUAL = 1
 PREFILL_MMA_SYNC = 4
-KERNEL_KINDS = 16
+MXFP8_ACT = 8
+KERNEL_KINDS = 18
 
 # every symbol the header declares (checked by the CPU tests)
 SYMBOLS = [
@@ -28,7 +29,7 @@ SYMBOLS = [
     "df_moe_last_launch_count", "df_moe_route_noalloc",
     "df_moe_graph_create", "df_moe_graph_launch", "df_moe_graph_launch_count",
     "df_moe_graph_destroy", "df_moe_stream_read", "df_moe_create_cached",
-    "df_moe_cache_stats", "df_moe_test_drop_arrival",
+    "df_moe_cache_stats", "df_moe_test_drop_arrival", "df_moe_step_mxfp8",
 ]
 
 
@@ -85,6 +86,7 @@ def lib():
         L.df_moe_step_expert_down.argtypes = [vp, i32, vp, i32, vp, vp, vp, vp]
         L.df_moe_step_shared.argtypes = [vp, i32, vp, i32, vp, vp]
         L.df_moe_step_rmsnorm.argtypes = [vp, vp, i32, vp, vp]
+        L.df_moe_step_mxfp8.argtypes = [vp, vp, i32, i32, vp, vp, vp]
         L.df_moe_read_expert_span.argtypes = [vp, i32, i32, vp]
         L.df_moe_timing_enable.argtypes = [vp, ctypes.c_int]
         L.df_moe_timing_reset.argtypes = [vp]
@@ -264,6 +266,12 @@ class MoE:
     def step_rmsnorm(self, x, T, xn, stream=None):
         self._check(lib().df_moe_step_rmsnorm(self.h, _ptr(x), T, _ptr(xn),
                                               _stream(stream)))
+
+    def step_mxfp8(self, v, rows, n, codes, scales, stream=None):
+        """The library's MXFP8 rounding of fp32 rows v [rows][n]: E4M3 codes
+        [rows][n] and E8M0 scales [rows][n/32]."""
+        self._check(lib().df_moe_step_mxfp8(self.h, _ptr(v), rows, n, _ptr(codes), _ptr(scales),
+                                            _stream(stream)))
 
     def read_expert_span(self, layer, expert, dst):
         self._check(lib().df_moe_read_expert_span(self.h, layer, expert, _ptr(dst)))

@@ -26,6 +26,7 @@ struct LayerBufs {
   uint16_t* sh_down = nullptr;  // [H][n_s*Is]
   uint8_t* eref = nullptr;      // [E][2I + H] row reference exponents (tcgen05 GEMMs)
   ChunkMap map_gu{}, map_dn{};  // tensor maps of the arena's tiles (tcgen05 GEMMs)
+  ChunkMap mx_gate{}, mx_up{}, mx_down{};  // code tensor maps (MXFP8-activation variant)
   SharedMaps sh_maps{};         // shared experts as dense tcgen05 GEMMs (batches)
   bool sh_maps_ok = false;
   bool router_loaded = false;
@@ -49,8 +50,8 @@ struct Pending {
 const char* kKindNames[K_NKINDS] = {"router", "topk", "group", "expert_gateup",
                                     "expert_down", "combine", "shared_gateup",
                                     "shared_down", "rmsnorm", "residual",
-                                    "repack", "other", "reserved", "gemm_gateup",
-                                    "gemm_down", "cache_fill"};
+                                    "repack", "other", "mx8_quant", "gemm_gateup",
+                                    "gemm_down", "cache_fill", "mx8_gateup", "mx8_down"};
 
 }  // namespace
 
@@ -89,6 +90,15 @@ struct df_moe {
   uint16_t* s_hh = nullptr;      // [Tmax][3][R] bf16: shared h rows (3 parts), batches
   float* g_bsc = nullptr;        // [Tmax*k] their power-of-two row scales
   ChunkMap bmap_gu{}, bmap_dn{};
+  // the MXFP8-activation variant (DF_MOE_MXFP8_ACT): E4M3 rows of x and h in
+  // expert order and their scales, stage-major
+  bool mx8 = false;
+  int mx_rows = 0;
+  uint8_t* mx_xq = nullptr;   // [mx_rows][H]
+  uint8_t* mx_xsf = nullptr;  // [H/128][mx_rows][4]
+  uint8_t* mx_hq = nullptr;   // [mx_rows][I]
+  uint8_t* mx_hsf = nullptr;  // [I/128][mx_rows][4]
+  ChunkMap mx_xmap{}, mx_hmap{};
   bool phase = false;  // decode batches run the two phase kernels
   int sms = 0;
   cudaStream_t cap_stream = nullptr;  // CUDA-graph captures run on it
@@ -155,6 +165,16 @@ int dalloc(df_moe* h, T** p, size_t n) {
   }
   h->allocs.push_back(*p);
   return DF_MOE_OK;
+}
+
+// Canonical spans -> the handle's device layout (inverse: back): the
+// fragment layout, or for the MXFP8-activation variant the canonical codes
+// with stage-major scales.
+cudaError_t span_layout_copy(const df_moe* h, const uint8_t* src, uint8_t* dst, int n,
+                             int inverse, cudaStream_t s) {
+  const df_moe_config& c = h->cfg;
+  return h->mx8 ? launch_mx8_layout(src, dst, n, c.hidden, c.inter, h->span_bytes, inverse, s)
+                : launch_repack_span(src, dst, n, c.hidden, c.inter, inverse, s);
 }
 
 cudaEvent_t get_event(df_moe* h) {
@@ -264,6 +284,19 @@ int expert_gateup(df_moe* h, int l, const uint16_t* x, int T, int max_items, int
                   float* hbuf, cudaStream_t s, int max_ctas = 0) {
   const df_moe_config& c = h->cfg;
   const uint8_t* arena = h->layers[l].arena;
+  if (h->mx8) {
+    // MXFP8 activations: x rounded per assignment row, then the block-scaled
+    // GEMM (h rounded again in its epilogue for the down GEMM)
+    const LayerBufs& L = h->layers[l];
+    RUN(h, K_MX8_QUANT, s, launch_mx8_rows(x, true, c.hidden, c.top_k, h->items, h->n_items,
+                                           max_items, h->sorted, T * c.top_k, c.n_experts,
+                                           h->mx_xq, h->mx_xsf, h->mx_rows, h->err, s));
+    RUN(h, K_MX8_GU, s, launch_mx8_gateup(L.mx_gate, L.mx_up, h->mx_xmap, arena, h->span_bytes,
+                                          c.hidden, c.inter, h->mx_xsf, h->mx_rows, h->items,
+                                          h->n_items, max_items, h->sorted, c.n_experts,
+                                          T * c.top_k, hbuf, h->mx_hq, h->mx_hsf, h->err, s));
+    return DF_MOE_OK;
+  }
   if (use_gemm(h, T, tg)) {
     RUN(h, K_OTHER, s, launch_prep_x(x, T * c.top_k, c.hidden, c.top_k, h->sorted, h->g_xg,
                                      h->g_bsc, h->err, s));
@@ -284,6 +317,19 @@ int expert_down(df_moe* h, int l, const float* hbuf, int T, int max_items, int t
                 cudaStream_t s, int max_ctas = 0, bool after_gateup = false) {
   const df_moe_config& c = h->cfg;
   const uint8_t* arena = h->layers[l].arena;
+  if (h->mx8) {
+    // MXFP8 activations: h (when given) rounded first; else the gate/up
+    // GEMM's rounded h
+    if (hbuf)
+      RUN(h, K_MX8_QUANT, s, launch_mx8_rows(hbuf, false, c.inter, 1, h->items, h->n_items,
+                                             max_items, h->sorted, T * c.top_k, c.n_experts,
+                                             h->mx_hq, h->mx_hsf, h->mx_rows, h->err, s));
+    RUN(h, K_MX8_DN, s, launch_mx8_down(h->layers[l].mx_down, h->mx_hmap, arena, h->span_bytes,
+                                        c.hidden, c.inter, h->mx_hsf, h->mx_rows, h->items,
+                                        h->n_items, max_items, h->sorted, c.n_experts,
+                                        T * c.top_k, h->part, h->err, s));
+    return DF_MOE_OK;
+  }
   if (use_gemm(h, T, tg)) {
     RUN(h, K_OTHER, s, launch_split_h(hbuf, T * c.top_k, c.inter, h->sorted, h->g_hh, h->g_bsc,
                                       h->err, s));
@@ -459,9 +505,11 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
       rc = shared_part(h, l, x, T, h->ysh, s);
       if (rc) return rc;
     }
-    rc = expert_gateup(h, l, x, T, max_items, tg, h->hbuf, s);
+    // (the MXFP8 variant hands h from GEMM to GEMM already rounded)
+    rc = expert_gateup(h, l, x, T, max_items, tg, h->mx8 ? nullptr : h->hbuf, s);
     if (rc) return rc;
-    rc = expert_down(h, l, h->hbuf, T, max_items, tg, s, 0, /*after_gateup=*/true);
+    rc = expert_down(h, l, h->mx8 ? nullptr : h->hbuf, T, max_items, tg, s, 0,
+                     /*after_gateup=*/true);
     if (rc) return rc;
   }
   RUN(h, K_COMBINE, s, launch_combine(h->part, w, T, c.top_k, c.hidden,
@@ -529,8 +577,19 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
                 "max_tokens must be in [1, 4096] with max_tokens*top_k <= 65535");
   if (c.n_layers > 1 && !(c.flags & DF_MOE_STACK_RMSNORM_RESIDUAL))
     return fail(nullptr, DF_MOE_EINVAL, "n_layers > 1 needs DF_MOE_STACK_RMSNORM_RESIDUAL");
-  if ((c.flags & ~(DF_MOE_STACK_RMSNORM_RESIDUAL | DF_MOE_PREFILL_MMA_SYNC)) != 0)
+  if ((c.flags & ~(DF_MOE_STACK_RMSNORM_RESIDUAL | DF_MOE_PREFILL_MMA_SYNC |
+                   DF_MOE_MXFP8_ACT)) != 0)
     return fail(nullptr, DF_MOE_EINVAL, "unknown flags");
+  if (c.flags & DF_MOE_MXFP8_ACT) {
+    if (slots)
+      return fail(nullptr, DF_MOE_EINVAL, "DF_MOE_MXFP8_ACT does not combine with an expert cache");
+    if (c.flags & DF_MOE_PREFILL_MMA_SYNC)
+      return fail(nullptr, DF_MOE_EINVAL,
+                  "DF_MOE_MXFP8_ACT does not combine with DF_MOE_PREFILL_MMA_SYNC");
+    if (!mx8_supported(c.hidden, c.inter))
+      return fail(nullptr, DF_MOE_EINVAL,
+                  "DF_MOE_MXFP8_ACT needs hidden and inter multiples of 128 (hidden >= 128)");
+  }
   if ((c.flags & DF_MOE_STACK_RMSNORM_RESIDUAL) && !(c.rms_eps >= 0.0f))
     return fail(nullptr, DF_MOE_EINVAL, "rms_eps must be >= 0");
   if (slots) {
@@ -594,8 +653,26 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
     if (!rc && R) rc = dalloc(h, &L.sh_down, H * R);
   }
   // tcgen05 GEMMs: batches above the decode range, unless asked otherwise
-  h->gemm = !slots && Tm > (size_t)kDecodeMaxT && !(c.flags & DF_MOE_PREFILL_MMA_SYNC) &&
-            gemm_supported(c.hidden, c.inter);
+  h->mx8 = (c.flags & DF_MOE_MXFP8_ACT) != 0;
+  h->gemm = !slots && !h->mx8 && Tm > (size_t)kDecodeMaxT &&
+            !(c.flags & DF_MOE_PREFILL_MMA_SYNC) && gemm_supported(c.hidden, c.inter);
+  if (h->mx8) {
+    h->mx_rows = mx8_rows_cap((int)(Tm * k), (int)std::min(Tm * k, E));
+    const size_t rows = (size_t)h->mx_rows;
+    for (int l = 0; l < c.n_layers && !rc; ++l) {
+      LayerBufs& L = h->layers[l];
+      if (!make_mx8_maps(L.arena, h->span_bytes, c.hidden, c.inter, c.n_experts, &L.mx_gate,
+                         &L.mx_up, &L.mx_down))
+        rc = fail(h, DF_MOE_ECUDA, "tensor map encoding failed");
+    }
+    if (!rc) rc = dalloc(h, &h->mx_xq, rows * H);
+    if (!rc) rc = dalloc(h, &h->mx_xsf, H / 128 * rows * 4);
+    if (!rc) rc = dalloc(h, &h->mx_hq, rows * I);
+    if (!rc) rc = dalloc(h, &h->mx_hsf, I / 128 * rows * 4);
+    if (!rc && (!make_mx8_row_map(h->mx_xq, h->mx_rows, c.hidden, &h->mx_xmap) ||
+                !make_mx8_row_map(h->mx_hq, h->mx_rows, c.inter, &h->mx_hmap)))
+      rc = fail(h, DF_MOE_ECUDA, "tensor map encoding failed");
+  }
   if (h->gemm) {
     for (int l = 0; l < c.n_layers && !rc; ++l) {
       LayerBufs& L = h->layers[l];
@@ -607,17 +684,20 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
     if (!rc) rc = dalloc(h, &h->g_xg, Tm * k * H);
     if (!rc) rc = dalloc(h, &h->g_hh, Tm * k * 2 * I);
     if (!rc) rc = dalloc(h, &h->g_bsc, Tm * k);
-    if (!rc && R && dense_supported(c.hidden, (int)R)) {
-      rc = dalloc(h, &h->s_hh, Tm * 3 * R);
-      for (int l = 0; l < c.n_layers && !rc; ++l) {
-        LayerBufs& L = h->layers[l];
-        L.sh_maps_ok = make_shared_maps(L.sh_gate, L.sh_up, L.sh_down, c.hidden, (int)R, h->s_hh,
-                                        (int)(3 * Tm), &L.sh_maps);
-      }
-    }
     if (!rc && !make_b_maps(h->g_xg, h->g_hh, (int)(Tm * k), c.hidden, c.inter, &h->bmap_gu,
                             &h->bmap_dn))
       rc = fail(h, DF_MOE_ECUDA, "tensor map encoding failed");
+  }
+  // the shared experts of batches as dense tcgen05 GEMMs (the routed
+  // experts' path aside: exact GEMMs, the MXFP8 variant, or none)
+  if (!rc && (h->gemm || h->mx8) && Tm > (size_t)kDecodeMaxT && R &&
+      dense_supported(c.hidden, (int)R)) {
+    rc = dalloc(h, &h->s_hh, Tm * 3 * R);
+    for (int l = 0; l < c.n_layers && !rc; ++l) {
+      LayerBufs& L = h->layers[l];
+      L.sh_maps_ok = make_shared_maps(L.sh_gate, L.sh_up, L.sh_down, c.hidden, (int)R, h->s_hh,
+                                      (int)(3 * Tm), &L.sh_maps);
+    }
   }
   if (!rc) rc = dalloc(h, &h->router_part, (size_t)h->rsplit.nsplit * Tm * E);
   if (!rc) rc = dalloc(h, &h->logits, Tm * E);
@@ -678,7 +758,9 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
   }
   if (!rc) {
     cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, cuda_device);
-    h->phase = phase_supported(H, c.inter, c.n_shared > 0 ? h->R : 0, c.n_experts, c.top_k);
+    // (the MXFP8 variant runs every batch through its GEMMs)
+    h->phase = !h->mx8 &&
+               phase_supported(H, c.inter, c.n_shared > 0 ? h->R : 0, c.n_experts, c.top_k);
     if (slots && !h->phase)
       rc = fail(h, DF_MOE_EINVAL, "an expert cache needs the decode phase kernels' shapes");
   }
@@ -778,7 +860,7 @@ int df_moe_load_experts(df_moe* h, int32_t layer, const df_moe_layer_weights* w,
                                           cudaMemcpyHostToDevice, s));
           src = h->staging;
         }
-        RUN(h, K_REPACK, s, launch_repack_span(src, packed, n, c.hidden, c.inter, 0, s));
+        RUN(h, K_REPACK, s, span_layout_copy(h, src, packed, n, 0, s));
         CUDA_OR_FAIL(h, cudaMemcpyAsync(L.host_pool + (size_t)(w->expert_begin + e0) *
                                                           h->span_bytes,
                                         packed, (size_t)n * h->span_bytes,
@@ -796,8 +878,7 @@ int df_moe_load_experts(df_moe* h, int32_t layer, const df_moe_layer_weights* w,
     } else if (w->src_is_device) {
       if (!aligned16(w->experts))
         return fail(h, DF_MOE_EINVAL, "device expert spans must be 16-byte aligned");
-      RUN(h, K_REPACK, s, launch_repack_span(w->experts, dst, w->expert_count,
-                                             c.hidden, c.inter, 0, s));
+      RUN(h, K_REPACK, s, span_layout_copy(h, w->experts, dst, w->expert_count, 0, s));
     } else {
       const size_t chunk = 8;
       if (!h->staging) {
@@ -811,9 +892,8 @@ int df_moe_load_experts(df_moe* h, int32_t layer, const df_moe_layer_weights* w,
                                         w->experts + (size_t)e0 * h->span_bytes,
                                         (size_t)n * h->span_bytes,
                                         cudaMemcpyHostToDevice, s));
-        RUN(h, K_REPACK, s, launch_repack_span(h->staging,
-                                               dst + (size_t)e0 * h->span_bytes,
-                                               n, c.hidden, c.inter, 0, s));
+        RUN(h, K_REPACK, s, span_layout_copy(h, h->staging, dst + (size_t)e0 * h->span_bytes,
+                                             n, 0, s));
       }
       CUDA_OR_FAIL(h, cudaStreamSynchronize(s));
     }
@@ -1033,6 +1113,8 @@ int df_moe_step_expert_gateup(df_moe* h, int32_t layer, const void* x_bf16,
     return fail(h, DF_MOE_ESTATE, "experts not loaded");
   if (h->cache_slots)
     return fail(h, DF_MOE_EINVAL, "single expert steps read the resident arena: not with a cache");
+  if (h->mx8 && !aligned16(x_bf16))
+    return fail(h, DF_MOE_EINVAL, "x must be 16-byte aligned");
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
   cudaStream_t s = (cudaStream_t)stream;
   const int tg = kOneItemPerExpert;
@@ -1055,6 +1137,8 @@ int df_moe_step_expert_down(df_moe* h, int32_t layer, const float* hbuf,
     return fail(h, DF_MOE_ESTATE, "experts not loaded");
   if (h->cache_slots)
     return fail(h, DF_MOE_EINVAL, "single expert steps read the resident arena: not with a cache");
+  if (h->mx8 && !aligned16(hbuf))
+    return fail(h, DF_MOE_EINVAL, "hbuf must be 16-byte aligned");
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
   cudaStream_t s = (cudaStream_t)stream;
   const int tg = kOneItemPerExpert;
@@ -1065,6 +1149,18 @@ int df_moe_step_expert_down(df_moe* h, int32_t layer, const float* hbuf,
   if (rc) return rc;
   RUN(h, K_COMBINE, s, launch_combine(h->part, weights, T, c.top_k, c.hidden,
                                       nullptr, nullptr, y, nullptr, h->err, h->err_mirror_d, s));
+  return DF_MOE_OK;
+}
+
+int df_moe_step_mxfp8(df_moe* h, const float* v, int32_t rows, int32_t n, uint8_t* codes,
+                      uint8_t* scales, void* stream) {
+  if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
+  if (!v || !codes || !scales) return fail(h, DF_MOE_EINVAL, "null pointer");
+  if (rows < 0 || n < 0 || n % 32) return fail(h, DF_MOE_EINVAL, "n must be a multiple of 32");
+  if (!aligned16(v)) return fail(h, DF_MOE_EINVAL, "v must be 16-byte aligned");
+  CUDA_OR_FAIL(h, cudaSetDevice(h->device));
+  cudaStream_t s = (cudaStream_t)stream;
+  RUN(h, K_MX8_QUANT, s, launch_mx8_plain(v, rows, n, codes, scales, s));
   return DF_MOE_OK;
 }
 
@@ -1118,7 +1214,7 @@ int df_moe_read_expert_span(df_moe* h, int32_t layer, int32_t expert,
                    h->span_bytes, cudaMemcpyHostToDevice);
     src = tmp + h->span_bytes;
   }
-  if (e == cudaSuccess) e = launch_repack_span(src, tmp, 1, c.hidden, c.inter, 1, nullptr);
+  if (e == cudaSuccess) e = span_layout_copy(h, src, tmp, 1, 1, nullptr);
   if (e == cudaSuccess) e = cudaMemcpy(dst, tmp, h->span_bytes, cudaMemcpyDeviceToHost);
   cudaFree(tmp);
   if (e != cudaSuccess)

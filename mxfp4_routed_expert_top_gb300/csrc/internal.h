@@ -63,8 +63,8 @@ constexpr int kOneItemPerExpert = 1 << 20;
 
 enum KernelKind {
   K_ROUTER = 0, K_TOPK, K_GROUP, K_GATEUP, K_DOWN, K_COMBINE, K_SHARED_GU,
-  K_SHARED_DN, K_RMSNORM, K_RESIDUAL, K_REPACK, K_OTHER, K_LAYER_UNUSED, K_GEMM_GU,
-  K_GEMM_DN, K_CACHE_FILL, K_NKINDS
+  K_SHARED_DN, K_RMSNORM, K_RESIDUAL, K_REPACK, K_OTHER, K_MX8_QUANT, K_GEMM_GU,
+  K_GEMM_DN, K_CACHE_FILL, K_MX8_GU, K_MX8_DN, K_NKINDS
 };
 
 // Launches `kernel` as a programmatic dependent of the previous kernel in
@@ -278,5 +278,47 @@ cudaError_t launch_shared_gemm_gateup(const SharedMaps& m, const uint16_t* x, in
 // y [T][H] = down (high + middle + low).
 cudaError_t launch_shared_gemm_down(const SharedMaps& m, int T, int H, int R, float* y,
                                     uint32_t* err, cudaStream_t s);
+
+// ---- routed experts with MXFP8 activations (k_mx8.cu) ----------------------
+// The lossy variant: activations rounded to MXFP8 (E4M3 elements, E8M0 per
+// 32), experts as grouped GEMMs on tcgen05.mma kind::mxf8f6f4 with the MXFP4
+// weights in the canonical code layout and their scales stage-major.
+bool mx8_supported(int H, int I);
+// Rows of the expert-ordered activation buffers for nassign assignments in
+// at most max_items items (each item's rows start at a multiple of 4).
+int mx8_rows_cap(int nassign, int max_items);
+// Tensor maps of the gate, up and down codes of an arena of E spans.
+bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E, ChunkMap* gate,
+                   ChunkMap* up, ChunkMap* down);
+// Tensor map of E4M3 activation rows [rows_cap][K].
+bool make_mx8_row_map(const uint8_t* rows, int rows_cap, int K, ChunkMap* map);
+// Rounds the rows of the items' assignments: row n of item i is source row
+// sorted[pos + n] / div of src (bf16 or fp32, [.][K], 16-byte aligned),
+// written to q row row_base(i) + n ([rows_cap][K]) with its scales in sf
+// ([K/128][rows_cap][4]).
+cudaError_t launch_mx8_rows(const void* src, bool bf16, int K, int div, const Item* items,
+                            const int32_t* n_items, int max_items, const int32_t* sorted,
+                            int nassign, int E, uint8_t* q, uint8_t* sf, int rows_cap,
+                            uint32_t* err, cudaStream_t s);
+// The rounding on plain rows: codes [rows][n], scales [rows][n/32].
+cudaError_t launch_mx8_plain(const float* v, int rows, int n, uint8_t* codes, uint8_t* scales,
+                             cudaStream_t s);
+// Canonical spans -> the variant's span layout (inverse: back).
+cudaError_t launch_mx8_layout(const uint8_t* src, uint8_t* dst, int n_spans, int H, int I,
+                              size_t span_bytes, int inverse, cudaStream_t s);
+// gate/up: h rounded to MXFP8 into hq/hsf (and, optionally, h before the
+// rounding into hbuf [nassign][I]).
+cudaError_t launch_mx8_gateup(const ChunkMap& gate, const ChunkMap& up, const ChunkMap& xmap,
+                              const uint8_t* arena, size_t span_bytes, int H, int I,
+                              const uint8_t* xsf, int rows_cap, const Item* items,
+                              const int32_t* n_items, int max_items, const int32_t* sorted,
+                              int E, int nassign, float* hbuf, uint8_t* hq, uint8_t* hsf,
+                              uint32_t* err, cudaStream_t s);
+// down: part [nassign][H].
+cudaError_t launch_mx8_down(const ChunkMap& down, const ChunkMap& hmap, const uint8_t* arena,
+                            size_t span_bytes, int H, int I, const uint8_t* hsf, int rows_cap,
+                            const Item* items, const int32_t* n_items, int max_items,
+                            const int32_t* sorted, int E, int nassign, float* part,
+                            uint32_t* err, cudaStream_t s);
 
 }  // namespace dfm

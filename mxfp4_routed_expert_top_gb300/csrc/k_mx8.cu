@@ -1,0 +1,828 @@
+// k_mx8.cu — the routed experts with MXFP8 activations (the lossy variant):
+// grouped GEMMs on tcgen05.mma kind::mxf8f6f4 with hardware block scales.
+//
+// Kimi K3 is trained quantisation-aware with MXFP4 weights and MXFP8
+// activations (Deltafin analysis, section 2.1); the pages' reference runs
+// keep the numerics exact and list the lossy switches apart (section 9.2).
+// Here the activations entering the routed experts (x for gate/up, h for
+// down) are rounded to MXFP8 — OCP microscaling blocks of 32 along the
+// contraction, E4M3 elements sharing one E8M0 exponent — and the tensor core
+// multiplies the E2M1 weights by the E4M3 activations, applying both blocks'
+// exponents itself. Products are exact and the sums are fp32, so the only
+// loss is the rounding of the activations to the format.
+//
+// Weights: the canonical MXFP4 codes (row-major, low nibble first) are read
+// by TMA as 16U4_ALIGN16B, which puts every 16 codes in the first 8 bytes of
+// a 16-byte group of shared memory: the operand layout of kind::mxf8f6f4 for
+// a 4-bit type (a byte of space per element, so a K = 32 step is 32 bytes,
+// as for the 8-bit B). The scale bytes are kept stage-major (arranged at load
+// time): for each 64-row block of a matrix and each 128-column stage, the 64
+// rows' four E8M0 bytes, 256 contiguous bytes, one bulk copy.
+// Activations: E4M3 rows in expert order, each item's rows starting at a
+// multiple of 4 (row_base(i) = 4 ceil((pos_i + 3 i) / 4)), their scales
+// stage-major ([K/128][rows][4 bytes]), so that a stage's token scales are
+// one 16-byte aligned bulk copy.
+//
+// One persistent CTA per SM, 320 threads in roles; a unit is one item x one
+// M tile of 128 rows (gate/up: 128 gate and the same 128 up rows, two MMAs a
+// K step into two accumulators, so that each thread of the epilogue holds
+// both values of its h row; down: 128 rows) x the item's tokens in passes of
+// at most 64 (the MMA's N, a multiple of 16), the contraction in stages of
+// 128 columns:
+//   warp 8     TMA: a stage's A operands (64-row boxes), its B rows (boxes of
+//              16 rows) and the scale blocks (bulk copies), on a ring of
+//              shared-memory stages;
+//   warps 4-7  move a stage's scales to tensor memory in the layout the MMA
+//              reads (A: row r at lane r, column base + r/32; B: token n at
+//              lane n mod 32 of every lane quarter, column base + n/32; the
+//              byte of the word is the K step);
+//   warp 9     issues the stage's MMAs (M = 128, K = 32) into one of two
+//              accumulator sets in tensor memory, and the commits;
+//   warps 0-3  the epilogue of a finished pass, one TMEM lane (one row) a
+//              thread: gate/up: h = silu(gate) * up, rounded to MXFP8 per 32
+//              rows (one warp a block) for the down GEMM; down: the rows of
+//              each assignment's output.
+// Every wait is bounded; after a timeout every role leaves its loop, the
+// copies and MMAs in flight land, and the CTA frees its tensor memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "pipeline.cuh"
+#include "umma.cuh"
+
+namespace dfm {
+namespace {
+
+constexpr int kThr = 320;
+constexpr int kSfWarp0 = 4, kTmaWarp = 8, kMmaWarp = 9;
+constexpr int kM = 128, kHalfRows = 64;
+constexpr int kKS = 128;                  // contraction columns a stage
+constexpr int kN = 64;                    // tokens a pass at most
+constexpr int kBoxRows = 16;              // B rows a TMA box
+constexpr int kABytes = kM * kKS;         // 16384: one A operand (a byte a code)
+constexpr int kAHalfTx = kHalfRows * kKS / 2;  // 4096: a 64-row box's codes as copied
+constexpr int kBBytes = kN * kKS;         // 8192
+constexpr int kSfaBytes = kM * 4;         // 512 a 128-row operand
+constexpr int kSfbBytes = kN * 4;         // 256
+constexpr uint32_t kTmemCols = 512;
+
+// Per GEMM: A operands a stage (gate/up: gate and up), stages, and the
+// layout of one stage in shared memory and of the tensor memory columns.
+template <int MODE>
+struct Geo {
+  static constexpr int NA = MODE == 0 ? 2 : 1;
+  static constexpr int S = MODE == 0 ? 5 : 8;
+  static constexpr size_t offA = 0;
+  static constexpr size_t offB = offA + (size_t)S * NA * kABytes;
+  static constexpr size_t offSfa = offB + (size_t)S * kBBytes;
+  static constexpr size_t offSfb = offSfa + (size_t)S * NA * kSfaBytes;
+  static constexpr size_t offBars = offSfb + (size_t)S * kSfbBytes;
+  static constexpr uint32_t accCols = NA * kN;      // one accumulator set
+  static constexpr uint32_t sfCol = 2 * accCols;    // then per stage NA x 4 A, 4 B
+  static constexpr uint32_t sfStride = NA * 4 + 4;
+};
+
+template <int S>
+struct Bars {
+  uint64_t full[S], sfull[S], empty[S];
+  uint64_t accf[2], acce[2], fin;
+  uint32_t tmem;
+  int err;
+};
+template <int MODE>
+constexpr size_t smem_bytes() {
+  return Geo<MODE>::offBars + sizeof(Bars<Geo<MODE>::S>);
+}
+static_assert(smem_bytes<0>() <= 227 * 1024 && smem_bytes<1>() <= 227 * 1024, "shared memory");
+static_assert(Geo<0>::sfCol + Geo<0>::sfStride * Geo<0>::S <= kTmemCols, "tensor memory");
+static_assert(Geo<1>::sfCol + Geo<1>::sfStride * Geo<1>::S <= kTmemCols, "tensor memory");
+static_assert(Geo<0>::offB % 1024 == 0 && Geo<1>::offB % 1024 == 0, "128-byte swizzle atoms");
+
+struct Mx8Args {
+  ChunkMap amap0, amap1;  // gate/up: gate and up codes; down: down codes
+  ChunkMap bmap;          // activation rows [rows_cap][K] E4M3
+  const uint8_t* arena;
+  size_t span_bytes;
+  size_t sfa0, sfa1;      // span offsets of the A operands' scale sections
+  int K, MT;              // contraction; M tiles an item
+  int I, H;
+  const uint8_t* bsf;     // activation scales [K/128][rows_cap][4]
+  int rows_cap;
+  const Item* items;
+  const int32_t* n_items;
+  const int32_t* sorted;
+  int max_items, E, nassign;
+  float* hbuf;            // gate/up: optional [nassign][I] h before rounding
+  uint8_t* hq;            // gate/up: [rows_cap][I] E4M3 rows of h (expert order)
+  uint8_t* hsf;           // gate/up: [I/128][rows_cap][4] their scales
+  float* part;            // down: [nassign][H]
+  uint32_t* err;
+};
+
+// ---------------------------------------------------------------------------
+// MXFP8 rounding (OCP microscaling, E4M3 elements, E8M0 per 32)
+// ---------------------------------------------------------------------------
+
+// 2^e for e in [-127, 127] (2^-127 is a subnormal float).
+__device__ __forceinline__ float pow2f(int e) {
+  return e >= -126 ? __int_as_float((e + 127) << 23) : __int_as_float(0x00400000);
+}
+
+// The block's shared exponent: floor(log2(amax)) - 8 (8 is E4M3's largest
+// exponent), clamped to E8M0's [-127, 127]; -127 for an all-zero block.
+__device__ __forceinline__ int mx8_shared_exp(float amax) {
+  if (amax == 0.f) return -127;
+  return max(-127, min(127, ilogbf(amax) - 8));
+}
+
+// E4M3 code of v, nearest with ties to even, |v| beyond 448 saturating.
+__device__ __forceinline__ uint32_t e4m3_rn_sat(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(r) : "f"(v));
+  return r & 0xFFu;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// First activation row of item i (rows of earlier items end before it): a
+// multiple of 4 from pos_i and i alone.
+__device__ __forceinline__ int row_base(int i, int pos) { return (pos + 3 * i + 3) & ~3; }
+
+// ---------------------------------------------------------------------------
+// tensor memory, MMA and copy helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void mma_mx(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc,
+                                       uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n\t}" ::"r"(d),
+      "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void tma3d(void* dst, const ChunkMap* m, int x, int y, int z,
+                                      uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma2d(void* dst, const ChunkMap* m, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_plain(void* dst, const void* src, uint32_t bytes,
+                                           uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: gives up after ~200 ms (and records it in *err), or soon
+// after another role of the CTA has given up.
+constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;
+__device__ __forceinline__ bool wait_or_give_up(uint64_t* bar, uint32_t parity, int* err) {
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 63u) {
+      if (*(volatile int*)err) return false;
+      if (global_ns() - t0 > kWaitNs) {
+        *(volatile int*)err = 1;
+        return false;
+      }
+    }
+  }
+}
+// The same for all lanes of a warp, which then agree.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* err) {
+  const bool ok = wait_or_give_up(bar, parity, err);
+  return __all_sync(0xffffffffu, ok);
+}
+// Bounded wait that records nothing (teardown).
+__device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity) && global_ns() - t0 < kWaitNs) {
+  }
+}
+
+// The sequence every role walks: the CTA's units (u = blockIdx.x + j *
+// gridDim.x), each one's passes of at most kN tokens, each pass's stages.
+struct Unit {
+  bool ok;
+  int e, mt, pos, cnt, base;
+};
+__device__ __forceinline__ Unit unit_at(const Mx8Args& a, int u) {
+  Unit w;
+  const int item = u / a.MT;
+  w.mt = u - item * a.MT;
+  const Item it = a.items[item];
+  w.e = it.e;
+  w.pos = it.pos;
+  w.cnt = it.cnt;
+  w.base = row_base(item, it.pos);
+  w.ok = (unsigned)it.e < (unsigned)a.E && it.cnt >= 1 && it.pos >= 0 &&
+         it.pos + it.cnt <= a.nassign && w.base + ((it.cnt + 3) & ~3) <= a.rows_cap;
+  return w;
+}
+
+// ---------------------------------------------------------------------------
+// roles
+// ---------------------------------------------------------------------------
+
+template <int MODE>
+__device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE>::S>* b) {
+  using G = Geo<MODE>;
+  const int nks = a.K / kKS;
+  uint32_t g = 0;
+  uint32_t armed = 0u, last_par = 0u;
+  bool ok = true;
+  for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    const Unit w = unit_at(a, u);
+    if (!w.ok) continue;
+    const uint8_t* span = a.arena + (size_t)w.e * a.span_bytes;
+    for (int tb = 0; tb < w.cnt && ok; tb += kN) {
+      const int nv = min(kN, w.cnt - tb);
+      const int nb = (nv + kBoxRows - 1) / kBoxRows;
+      const uint32_t sfb_bytes = (uint32_t)((nv + 3) & ~3) * 4u;
+      const int row = w.base + tb;
+      for (int ks = 0; ks < nks; ++ks, ++g) {
+        const uint32_t s = g % G::S, ph = (g / G::S) & 1u;
+        if (!wait_or_give_up(&b->empty[s], ph ^ 1u, &b->err)) { ok = false; break; }
+        uint64_t* full = &b->full[s];
+        mbar_arrive_expect_tx(full, G::NA * (2 * kAHalfTx + kSfaBytes) + nb * kBoxRows * kKS +
+                                        sfb_bytes);
+        for (int o = 0; o < G::NA; ++o) {
+          uint8_t* as = smem + G::offA + ((size_t)s * G::NA + o) * kABytes;
+          uint8_t* sa = smem + G::offSfa + ((size_t)s * G::NA + o) * kSfaBytes;
+          const ChunkMap* m = o == 0 ? &a.amap0 : &a.amap1;
+          const size_t sec = o == 0 ? a.sfa0 : a.sfa1;
+          for (int h = 0; h < 2; ++h) {
+            tma3d(as + h * (kABytes / 2), m, ks * kKS, kM * w.mt + kHalfRows * h, w.e, full);
+            bulk_plain(sa + h * (kSfaBytes / 2),
+                       span + sec + ((size_t)(2 * w.mt + h) * nks + ks) * (kHalfRows * 4),
+                       kSfaBytes / 2, full);
+          }
+        }
+        uint8_t* bs = smem + G::offB + (size_t)s * kBBytes;
+        for (int i = 0; i < nb; ++i)
+          tma2d(bs + i * kBoxRows * kKS, &a.bmap, ks * kKS, row + kBoxRows * i, full);
+        bulk_plain(smem + G::offSfb + (size_t)s * kSfbBytes,
+                   a.bsf + ((size_t)ks * a.rows_cap + row) * 4, sfb_bytes, full);
+        armed |= 1u << s;
+        last_par = (last_par & ~(1u << s)) | (ph << s);
+      }
+    }
+  }
+  // the copies in flight land before the CTA may leave
+  for (int s = 0; s < G::S; ++s)
+    if (armed >> s & 1u) drain(&b->full[s], last_par >> s & 1u);
+}
+
+template <int MODE>
+__device__ void role_sf(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE>::S>* b,
+                        uint32_t tmem, int q, int lane) {
+  using G = Geo<MODE>;
+  const int nks = a.K / kKS;
+  const int L = 32 * q + lane;
+  const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
+  uint32_t g = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    const Unit w = unit_at(a, u);
+    if (!w.ok) continue;
+    for (int tb = 0; tb < w.cnt && ok; tb += kN) {
+      const int nv4 = (min(kN, w.cnt - tb) + 3) & ~3;
+      for (int ks = 0; ks < nks; ++ks, ++g) {
+        const uint32_t s = g % G::S, ph = (g / G::S) & 1u;
+        if (!warp_wait(&b->full[s], ph, &b->err)) { ok = false; break; }
+        const uint32_t col = G::sfCol + G::sfStride * s;
+#pragma unroll
+        for (int o = 0; o < G::NA; ++o) {
+          const uint32_t va =
+              lds_u32(smem + G::offSfa + ((size_t)s * G::NA + o) * kSfaBytes + 4 * L);
+          asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(
+                           lane_addr + col + 4 * o + q),
+                       "r"(va)
+                       : "memory");
+        }
+        const uint8_t* sb = smem + G::offSfb + (size_t)s * kSfbBytes;
+        const uint32_t vb0 = lane < nv4 ? lds_u32(sb + 4 * lane) : 0x7F7F7F7Fu;
+        const uint32_t vb1 = lane + 32 < nv4 ? lds_u32(sb + 4 * (lane + 32)) : 0x7F7F7F7Fu;
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(
+                         lane_addr + col + 4 * G::NA),
+                     "r"(vb0), "r"(vb1)
+                     : "memory");
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&b->sfull[s]);
+      }
+    }
+  }
+}
+
+template <int MODE>
+__device__ void role_mma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE>::S>* b,
+                         uint32_t tmem) {
+  using G = Geo<MODE>;
+  const int nks = a.K / kKS;
+  uint32_t g = 0, pc = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    const Unit w = unit_at(a, u);
+    if (!w.ok) continue;
+    for (int tb = 0; tb < w.cnt && ok; tb += kN, ++pc) {
+      const int nv = min(kN, w.cnt - tb);
+      const int N = (nv + 15) & ~15;
+      const uint32_t acc = pc & 1u;
+      if (!wait_or_give_up(&b->acce[acc], ((pc >> 1) & 1u) ^ 1u, &b->err)) { ok = false; break; }
+      tc_fence_after();
+      for (int ks = 0; ks < nks; ++ks, ++g) {
+        const uint32_t s = g % G::S, ph = (g / G::S) & 1u;
+        if (!wait_or_give_up(&b->sfull[s], ph, &b->err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t bs = smem_u32(smem + G::offB + (size_t)s * kBBytes);
+        const uint32_t col = tmem + G::sfCol + G::sfStride * s;
+#pragma unroll
+        for (int kk = 0; kk < kKS / 32; ++kk) {
+          const uint32_t idesc = umma::idesc_mxf8f6f4_e2m1_e4m3(kM, N, kk, kk);
+          const uint64_t bd = umma::smem_desc_sw128(bs + 32 * kk);
+#pragma unroll
+          for (int o = 0; o < G::NA; ++o) {
+            const uint32_t as = smem_u32(smem + G::offA + ((size_t)s * G::NA + o) * kABytes);
+            mma_mx(tmem + acc * G::accCols + o * kN, umma::smem_desc_sw128(as + 32 * kk), bd,
+                   idesc, col + 4 * o, col + 4 * G::NA, (ks | kk) != 0);
+          }
+        }
+        tc_commit(&b->empty[s]);
+      }
+      if (ok) tc_commit(&b->accf[acc]);
+    }
+  }
+  // every MMA issued completes before the tensor memory is freed
+  tc_commit(&b->fin);
+  drain(&b->fin, 0);
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t addr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"
+      "%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, "
+      "[%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(addr));
+}
+
+template <int MODE>
+__device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE>::S>* b,
+                              uint32_t tmem, int warp, int lane) {
+  using G = Geo<MODE>;
+  const int L = 32 * warp + lane;
+  const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+  uint32_t pc = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    const Unit w = unit_at(a, u);
+    if (!w.ok) {
+      if (L == 0) atomicOr(a.err, DEV_ERR_RANGE);
+      continue;
+    }
+    const int r = kM * w.mt + L;  // this thread's row (h row or output row)
+    for (int tb = 0; tb < w.cnt && ok; tb += kN, ++pc) {
+      const int nv = min(kN, w.cnt - tb);
+      const uint32_t acc = pc & 1u;
+      if (!warp_wait(&b->accf[acc], (pc >> 1) & 1u, &b->err)) { ok = false; break; }
+      tc_fence_after();
+      for (int c0 = 0; c0 < nv; c0 += 32) {
+        const int nc = min(32, nv - c0);
+        uint32_t v[32];
+        tmem_ld32(lane_addr + acc * G::accCols + c0, v);
+        if (MODE == 1) {
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+          for (int n = 0; n < 32; ++n) {
+            if (n >= nc) break;
+            const int aa = a.sorted[w.pos + tb + c0 + n];
+            if ((unsigned)aa < (unsigned)a.nassign)
+              a.part[(size_t)aa * a.H + r] = __uint_as_float(v[n]);
+            else if (lane == 0)
+              atomicOr(a.err, DEV_ERR_RANGE);
+          }
+        } else {
+          uint32_t vu[32];
+          tmem_ld32(lane_addr + acc * G::accCols + kN + c0, vu);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          const int blk = 4 * w.mt + warp;  // MXFP8 block of h along I
+#pragma unroll
+          for (int n = 0; n < 32; ++n) {
+            if (n >= nc) break;
+            const float gt = __uint_as_float(v[n]);
+            const float hv = gt / (1.f + expf(-gt)) * __uint_as_float(vu[n]);
+            const int aa = a.sorted[w.pos + tb + c0 + n];
+            if (a.hbuf && (unsigned)aa < (unsigned)a.nassign)
+              a.hbuf[(size_t)aa * a.I + r] = hv;
+            const int sh = mx8_shared_exp(warp_max(fabsf(hv)));
+            const int row = w.base + tb + c0 + n;
+            a.hq[(size_t)row * a.I + r] = (uint8_t)e4m3_rn_sat(hv * pow2f(-sh));
+            if (lane == 0)
+              a.hsf[((size_t)(blk >> 2) * a.rows_cap + row) * 4 + (blk & 3)] = (uint8_t)(sh + 127);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&b->acce[acc]);
+    }
+  }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThr, 1) mx8_gemm_kernel(const __grid_constant__ Mx8Args a) {
+  using G = Geo<MODE>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Bars<G::S>* b = reinterpret_cast<Bars<G::S>*>(smem + G::offBars);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&b->tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (threadIdx.x == 32) {
+    for (int i = 0; i < G::S; ++i) {
+      mbar_init(&b->full[i], 1);
+      mbar_init(&b->sfull[i], 4);
+      mbar_init(&b->empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&b->accf[i], 1);
+      mbar_init(&b->acce[i], 4);
+    }
+    mbar_init(&b->fin, 1);
+    b->err = 0;
+    fence_barrier_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(&b->tmem);
+  int n_items = *a.n_items;
+  if (n_items < 0 || n_items > a.max_items) {
+    if (threadIdx.x == 0) atomicOr(a.err, DEV_ERR_RANGE);
+    n_items = n_items < 0 ? 0 : a.max_items;
+  }
+  const int n_units = n_items * a.MT;
+  if (warp < 4) {
+    role_epilogue<MODE>(a, n_units, b, tmem, warp, lane);
+  } else if (warp < kTmaWarp) {
+    role_sf<MODE>(a, n_units, smem, b, tmem, warp - kSfWarp0, lane);
+  } else if (warp == kTmaWarp) {
+    if (lane == 0) role_tma<MODE>(a, n_units, smem, b);
+  } else if (warp == kMmaWarp && lane == 0) {
+    role_mma<MODE>(a, n_units, smem, b, tmem);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0 && b->err) atomicOr(a.err, DEV_ERR_TIMEOUT);
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+}
+
+// Rounds activation rows to MXFP8 into the expert-ordered buffers: block =
+// item, thread j = 32-column block j of each of the item's rows. Row n of
+// item i is source row sorted[pos + n] / div (x: the token; h: the
+// assignment), written to q row row_base(i) + n.
+template <bool BF16>
+__global__ void __launch_bounds__(256) mx8_rows_kernel(const void* src, int K, int div,
+                                                       const Item* items, const int32_t* n_items,
+                                                       int max_items, const int32_t* sorted,
+                                                       int nassign, int E, uint8_t* q,
+                                                       uint8_t* sf, int rows_cap, uint32_t* err) {
+  const int i = blockIdx.x;
+  int ni = *n_items;
+  if (ni > max_items) ni = max_items;
+  if (i >= ni) return;
+  const Item it = items[i];
+  const int base = row_base(i, it.pos);
+  if ((unsigned)it.e >= (unsigned)E || it.cnt < 1 || it.pos < 0 || it.pos + it.cnt > nassign ||
+      base + it.cnt > rows_cap) {
+    if (threadIdx.x == 0) atomicOr(err, DEV_ERR_RANGE);
+    return;
+  }
+  const int nblk = K / 32;
+  for (int n = 0; n < it.cnt; ++n) {
+    const int aa = sorted[it.pos + n];
+    if ((unsigned)aa >= (unsigned)nassign) {
+      if (threadIdx.x == 0) atomicOr(err, DEV_ERR_RANGE);
+      continue;
+    }
+    const int srow = aa / div;
+    for (int j = threadIdx.x; j < nblk; j += blockDim.x) {
+      float v[32];
+      if (BF16) {
+        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) +
+                                                        (size_t)srow * K + 32 * j);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 t = p[c];
+          const uint32_t wd[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            v[8 * c + 2 * m] = __uint_as_float(wd[m] << 16);
+            v[8 * c + 2 * m + 1] = __uint_as_float(wd[m] & 0xFFFF0000u);
+          }
+        }
+      } else {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) +
+                                                          (size_t)srow * K + 32 * j);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 t = p[c];
+          v[4 * c] = t.x;
+          v[4 * c + 1] = t.y;
+          v[4 * c + 2] = t.z;
+          v[4 * c + 3] = t.w;
+        }
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int m = 0; m < 32; ++m) amax = fmaxf(amax, fabsf(v[m]));
+      const int sh = mx8_shared_exp(amax);
+      const float sc = pow2f(-sh);
+      uint32_t wq[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+        wq[m] = e4m3_rn_sat(v[4 * m] * sc) | e4m3_rn_sat(v[4 * m + 1] * sc) << 8 |
+                e4m3_rn_sat(v[4 * m + 2] * sc) << 16 | e4m3_rn_sat(v[4 * m + 3] * sc) << 24;
+      uint4* d = reinterpret_cast<uint4*>(q + (size_t)(base + n) * K + 32 * j);
+      d[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+      d[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
+      sf[((size_t)(j >> 2) * rows_cap + base + n) * 4 + (j & 3)] = (uint8_t)(sh + 127);
+    }
+  }
+}
+
+// The same rounding on plain rows (the format's own layout): codes [rows][n],
+// scales [rows][n/32]; one thread a block.
+__global__ void mx8_plain_kernel(const float* v, int rows, int n, uint8_t* codes,
+                                 uint8_t* scales) {
+  const int nb = n / 32;
+  const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= (long long)rows * nb) return;
+  const float* p = v + t * 32;
+  float amax = 0.f;
+  for (int m = 0; m < 32; ++m) amax = fmaxf(amax, fabsf(p[m]));
+  const int sh = mx8_shared_exp(amax);
+  const float sc = pow2f(-sh);
+  for (int m = 0; m < 32; ++m) codes[t * 32 + m] = (uint8_t)e4m3_rn_sat(p[m] * sc);
+  scales[t] = (uint8_t)(sh + 127);
+}
+
+// Canonical span <-> MXFP8-path span: the code sections stay, the three
+// scale sections go stage-major (or back, `inverse`). One thread a byte.
+__global__ void mx8_layout_kernel(const uint8_t* src, uint8_t* dst, int n_spans, int H, int I,
+                                  size_t span, int inverse) {
+  const size_t q = (size_t)H * I / 2, sb = (size_t)H * I / 32;
+  const size_t off_s[3] = {q, 2 * q + sb, 3 * q + 2 * sb};
+  const int Ks[3] = {H, H, I};
+  const size_t total = (size_t)n_spans * span;
+  for (size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x; t < total;
+       t += (size_t)gridDim.x * blockDim.x) {
+    const size_t sp = t / span, o = t - sp * span;
+    size_t canon = o, dev = o;
+    for (int m = 0; m < 3; ++m) {
+      if (o >= off_s[m] && o < off_s[m] + sb) {
+        const size_t r0 = o - off_s[m];
+        const int K = Ks[m], nb = K / 32, nks = K / kKS;
+        const int r = (int)(r0 / nb), kb = (int)(r0 - (size_t)r * nb);
+        dev = off_s[m] + (((size_t)(r / 64) * nks + kb / 4) * 64 + (r % 64)) * 4 + (kb & 3);
+        canon = o;
+        break;
+      }
+    }
+    if (!inverse)
+      dst[sp * span + dev] = src[sp * span + canon];
+    else
+      dst[sp * span + canon] = src[sp * span + dev];
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  if (!enc) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &qr) != cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess || !fn)
+      return nullptr;
+    enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return enc;
+}
+
+int sms_mx8() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+template <int MODE>
+cudaError_t launch_mx8(const Mx8Args& a, cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        mx8_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<MODE>());
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const long long units = (long long)a.max_items * a.MT;
+  int grid = sms_mx8();
+  if (units < grid) grid = (int)(units > 0 ? units : 1);
+  mx8_gemm_kernel<MODE><<<grid, kThr, smem_bytes<MODE>(), s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool mx8_supported(int H, int I) { return H % kKS == 0 && I % kKS == 0 && H >= kM; }
+
+int mx8_rows_cap(int nassign, int max_items) { return (nassign + 3 * max_items + 7) & ~3; }
+
+bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E, ChunkMap* gate,
+                   ChunkMap* up, ChunkMap* down) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return false;
+  const size_t q = (size_t)H * I / 2, sb = (size_t)H * I / 32;
+  const size_t offs[3] = {0, q + sb, 2 * (q + sb)};
+  ChunkMap* maps[3] = {gate, up, down};
+  for (int m = 0; m < 3; ++m) {
+    const int K = m < 2 ? H : I, rows = m < 2 ? I : H;
+    const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)E};
+    const cuuint64_t strides[2] = {(cuuint64_t)K / 2, (cuuint64_t)span_bytes};
+    const cuuint32_t box[3] = {kKS, kHalfRows, 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    if (enc(reinterpret_cast<CUtensorMap*>(maps[m]), CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3,
+            const_cast<uint8_t*>(arena + offs[m]), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
+}
+
+bool make_mx8_row_map(const uint8_t* rows_buf, int rows_cap, int K, ChunkMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows_cap};
+  const cuuint64_t strides[1] = {(cuuint64_t)K};
+  const cuuint32_t box[2] = {kKS, kBoxRows};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(reinterpret_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+             const_cast<uint8_t*>(rows_buf), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_mx8_rows(const void* src, bool bf16, int K, int div, const Item* items,
+                            const int32_t* n_items, int max_items, const int32_t* sorted,
+                            int nassign, int E, uint8_t* q, uint8_t* sf, int rows_cap,
+                            uint32_t* err, cudaStream_t s) {
+  if (max_items <= 0) return cudaSuccess;
+  if (bf16)
+    mx8_rows_kernel<true><<<max_items, 256, 0, s>>>(src, K, div, items, n_items, max_items, sorted,
+                                                    nassign, E, q, sf, rows_cap, err);
+  else
+    mx8_rows_kernel<false><<<max_items, 256, 0, s>>>(src, K, div, items, n_items, max_items,
+                                                     sorted, nassign, E, q, sf, rows_cap, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx8_plain(const float* v, int rows, int n, uint8_t* codes, uint8_t* scales,
+                             cudaStream_t s) {
+  const long long blocks = (long long)rows * (n / 32);
+  if (blocks <= 0) return cudaSuccess;
+  mx8_plain_kernel<<<(unsigned)((blocks + 255) / 256), 256, 0, s>>>(v, rows, n, codes, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx8_layout(const uint8_t* src, uint8_t* dst, int n_spans, int H, int I,
+                              size_t span_bytes, int inverse, cudaStream_t s) {
+  if (n_spans <= 0) return cudaSuccess;
+  const size_t total = (size_t)n_spans * span_bytes;
+  const int grid = (int)std::min<size_t>((total + 255) / 256, 8192);
+  mx8_layout_kernel<<<grid, 256, 0, s>>>(src, dst, n_spans, H, I, span_bytes, inverse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx8_gateup(const ChunkMap& gate, const ChunkMap& up, const ChunkMap& xmap,
+                              const uint8_t* arena, size_t span_bytes, int H, int I,
+                              const uint8_t* xsf, int rows_cap, const Item* items,
+                              const int32_t* n_items, int max_items, const int32_t* sorted,
+                              int E, int nassign, float* hbuf, uint8_t* hq, uint8_t* hsf,
+                              uint32_t* err, cudaStream_t s) {
+  const size_t q = (size_t)H * I / 2, sb = (size_t)H * I / 32;
+  Mx8Args a{};
+  a.amap0 = gate;
+  a.amap1 = up;
+  a.bmap = xmap;
+  a.arena = arena;
+  a.span_bytes = span_bytes;
+  a.sfa0 = q;
+  a.sfa1 = 2 * q + sb;
+  a.K = H;
+  a.MT = I / kM;
+  a.I = I;
+  a.H = H;
+  a.bsf = xsf;
+  a.rows_cap = rows_cap;
+  a.items = items;
+  a.n_items = n_items;
+  a.sorted = sorted;
+  a.max_items = max_items;
+  a.E = E;
+  a.nassign = nassign;
+  a.hbuf = hbuf;
+  a.hq = hq;
+  a.hsf = hsf;
+  a.err = err;
+  return launch_mx8<0>(a, s);
+}
+
+cudaError_t launch_mx8_down(const ChunkMap& down, const ChunkMap& hmap, const uint8_t* arena,
+                            size_t span_bytes, int H, int I, const uint8_t* hsf, int rows_cap,
+                            const Item* items, const int32_t* n_items, int max_items,
+                            const int32_t* sorted, int E, int nassign, float* part,
+                            uint32_t* err, cudaStream_t s) {
+  const size_t q = (size_t)H * I / 2, sb = (size_t)H * I / 32;
+  Mx8Args a{};
+  a.amap0 = down;
+  a.amap1 = down;
+  a.bmap = hmap;
+  a.arena = arena;
+  a.span_bytes = span_bytes;
+  a.sfa0 = 3 * q + 2 * sb;
+  a.sfa1 = a.sfa0;
+  a.K = I;
+  a.MT = H / kM;
+  a.I = I;
+  a.H = H;
+  a.bsf = hsf;
+  a.rows_cap = rows_cap;
+  a.items = items;
+  a.n_items = n_items;
+  a.sorted = sorted;
+  a.max_items = max_items;
+  a.E = E;
+  a.nassign = nassign;
+  a.part = part;
+  a.err = err;
+  return launch_mx8<1>(a, s);
+}
+
+}  // namespace dfm

@@ -1,7 +1,7 @@
 // umma.cuh — encodings for the 5th-generation tensor core MMA (tcgen05.mma)
 // of sm_100-family GPUs: shared-memory matrix descriptors and the
-// instruction descriptor of kind::f16. Host and device, so that the host
-// tests can check them field by field.
+// instruction descriptors of kind::f16 and kind::mxf8f6f4.block_scale. Host
+// and device, so that the host tests can check them field by field.
 //
 // Operands here are K-major and unswizzled ("interleaved"): a matrix of R
 // rows x 16 K-columns of 16-bit elements is made of core matrices of
@@ -47,6 +47,18 @@ __host__ __device__ inline uint32_t idesc_bf16_f32(int M, int N) {
 // The same with f16 A and B (A and B formats 0).
 __host__ __device__ inline uint32_t idesc_f16_f32(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor of tcgen05.mma kind::mxf8f6f4.block_scale (32
+// bits), dense, fp32 D, E2M1 A (the weights) and E4M3 B (the activations),
+// both K-major, E8M0 scale factors:
+//   [4,6) B scale factor id (the byte of the 32-bit scale word in tensor
+//   memory)  [7,10) A format (5 = E2M1)  [10,13) B format (0 = E4M3)
+//   [15] A major  [16] B major  [17,23) N >> 3  [23] scale type (1 = E8M0)
+//   [27,29) M >> 7  [29,31) A scale factor id
+__host__ __device__ inline uint32_t idesc_mxf8f6f4_e2m1_e4m3(int M, int N, int a_sf, int b_sf) {
+  return ((uint32_t)(b_sf & 3) << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) |
+         (1u << 23) | ((uint32_t)(M >> 7) << 27) | ((uint32_t)(a_sf & 3) << 29);
 }
 
 // Byte offset of element (r, k) (16-bit elements) in a K-major tile of `rows`

@@ -34,6 +34,10 @@ int main() {
   const int ns[5] = {16, 32, 48, 64, 256};
   for (int n : ns) printf("I %d %d %u\n", 128, n, idesc_bf16_f32(128, n));
   for (int n : ns) printf("F %d %d %u\n", 128, n, idesc_f16_f32(128, n));
+  for (int n : ns)
+    for (int a = 0; a < 4; ++a)
+      for (int b = 0; b < 4; ++b)
+        printf("X %d %d %d %d %u\n", 128, n, a, b, idesc_mxf8f6f4_e2m1_e4m3(128, n, a, b));
   const int rows[4] = {16, 32, 64, 128};
   for (int R : rows)
     for (int r = 0; r < R; ++r)
@@ -53,7 +57,7 @@ def enc(tmp_path_factory):
     src.write_text(DRIVER)
     subprocess.run([gxx, "-std=c++17", "-O0", "-I" + CSRC, str(src), "-o", str(exe)], check=True)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
-    res = {"D": {}, "S": {}, "I": {}, "F": {}, "K": {}}
+    res = {"D": {}, "S": {}, "I": {}, "F": {}, "K": {}, "X": {}}
     for line in out.splitlines():
         f = line.split()
         if f[0] == "LBO":
@@ -62,6 +66,8 @@ def enc(tmp_path_factory):
             res[f[0]][int(f[1])] = int(f[2])
         elif f[0] in ("I", "F"):
             res[f[0]][(int(f[1]), int(f[2]))] = int(f[3])
+        elif f[0] == "X":
+            res["X"][tuple(int(v) for v in f[1:5])] = int(f[5])
         else:
             res["K"].setdefault(int(f[1]), {})[(int(f[2]), int(f[3]))] = int(f[4])
     return res
@@ -114,6 +120,28 @@ def test_instruction_descriptor_f16(enc):
         assert bits(v, 7, 13) == 0       # A and B: f16 (the same type)
         assert bits(v, 17, 23) == N >> 3 and bits(v, 24, 29) == M >> 4
         assert v & ~((0x3 << 4) | (0x3F << 17) | (0x1F << 24)) == 0
+
+
+def test_instruction_descriptor_block_scaled(enc):
+    """kind::mxf8f6f4.block_scale with E2M1 A (the weights) and E4M3 B (the
+    activations): the block-scaled descriptor moves M to bits 27-28 (M >> 7)
+    and puts the two scale-factor ids (which byte of each 32-bit scale word
+    in tensor memory the MMA takes) at bits 4-5 (B) and 29-30 (A)."""
+    assert len(enc["X"]) == 5 * 16
+    for (M, N, a, b), v in enc["X"].items():
+        assert bits(v, 0, 4) == 0        # dense
+        assert bits(v, 4, 6) == b        # B scale factor id
+        assert bits(v, 6, 7) == 0
+        assert bits(v, 7, 10) == 5       # A: E2M1
+        assert bits(v, 10, 13) == 0      # B: E4M3
+        assert bits(v, 13, 15) == 0      # no negation
+        assert bits(v, 15, 17) == 0      # A and B K-major (the only form for E2M1)
+        assert bits(v, 17, 23) == N >> 3
+        assert bits(v, 23, 24) == 1      # scale type E8M0
+        assert bits(v, 24, 27) == 0
+        assert bits(v, 27, 29) == M >> 7
+        assert bits(v, 29, 31) == a      # A scale factor id
+        assert bits(v, 31, 32) == 0      # K = 32 a step (dense)
 
 
 def test_kmajor_layout(enc):
