@@ -95,9 +95,9 @@ struct df_moe {
   bool mx8 = false;
   int mx_rows = 0;
   uint8_t* mx_xq = nullptr;   // [mx_rows][H]
-  uint8_t* mx_xsf = nullptr;  // [H/128][mx_rows][4]
+  uint8_t* mx_xsf = nullptr;  // [H/128][mx_rows][16]
   uint8_t* mx_hq = nullptr;   // [mx_rows][I]
-  uint8_t* mx_hsf = nullptr;  // [I/128][mx_rows][4]
+  uint8_t* mx_hsf = nullptr;  // [I/128][mx_rows][16]
   ChunkMap mx_xmap{}, mx_hmap{};
   bool phase = false;  // decode batches run the two phase kernels
   int sms = 0;
@@ -666,9 +666,9 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
         rc = fail(h, DF_MOE_ECUDA, "tensor map encoding failed");
     }
     if (!rc) rc = dalloc(h, &h->mx_xq, rows * H);
-    if (!rc) rc = dalloc(h, &h->mx_xsf, H / 128 * rows * 4);
+    if (!rc) rc = dalloc(h, &h->mx_xsf, H / 128 * rows * 16);
     if (!rc) rc = dalloc(h, &h->mx_hq, rows * I);
-    if (!rc) rc = dalloc(h, &h->mx_hsf, I / 128 * rows * 4);
+    if (!rc) rc = dalloc(h, &h->mx_hsf, I / 128 * rows * 16);
     if (!rc && (!make_mx8_row_map(h->mx_xq, h->mx_rows, c.hidden, &h->mx_xmap) ||
                 !make_mx8_row_map(h->mx_hq, h->mx_rows, c.inter, &h->mx_hmap)))
       rc = fail(h, DF_MOE_ECUDA, "tensor map encoding failed");

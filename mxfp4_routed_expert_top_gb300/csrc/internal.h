@@ -285,7 +285,8 @@ cudaError_t launch_shared_gemm_down(const SharedMaps& m, int T, int H, int R, fl
 // weights in the canonical code layout and their scales stage-major.
 bool mx8_supported(int H, int I);
 // Rows of the expert-ordered activation buffers for nassign assignments in
-// at most max_items items (each item's rows start at a multiple of 4).
+// at most max_items items (the assignments' rows and 32 more, read past the
+// last row by a stage's 32-row scale chunk).
 int mx8_rows_cap(int nassign, int max_items);
 // Tensor maps of the gate, up and down codes of an arena of E spans.
 bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E, ChunkMap* gate,
@@ -294,8 +295,8 @@ bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E,
 bool make_mx8_row_map(const uint8_t* rows, int rows_cap, int K, ChunkMap* map);
 // Rounds the rows of the items' assignments: row n of item i is source row
 // sorted[pos + n] / div of src (bf16 or fp32, [.][K], 16-byte aligned),
-// written to q row row_base(i) + n ([rows_cap][K]) with its scales in sf
-// ([K/128][rows_cap][4]).
+// written to q row pos + n ([rows_cap][K]) with its scales in sf
+// ([K/128][rows_cap][16], word q of a row the scales of the row 32 q later).
 cudaError_t launch_mx8_rows(const void* src, bool bf16, int K, int div, const Item* items,
                             const int32_t* n_items, int max_items, const int32_t* sorted,
                             int nassign, int E, uint8_t* q, uint8_t* sf, int rows_cap,

@@ -15,29 +15,31 @@
 // by TMA as 16U4_ALIGN16B, which puts every 16 codes in the first 8 bytes of
 // a 16-byte group of shared memory: the operand layout of kind::mxf8f6f4 for
 // a 4-bit type (a byte of space per element, so a K = 32 step is 32 bytes,
-// as for the 8-bit B). The scale bytes are kept stage-major (arranged at load
-// time): for each 64-row block of a matrix and each 128-column stage, the 64
-// rows' four E8M0 bytes, 256 contiguous bytes, one bulk copy.
-// Activations: E4M3 rows in expert order, each item's rows starting at a
-// multiple of 4 (row_base(i) = 4 ceil((pos_i + 3 i) / 4)), their scales
-// stage-major ([K/128][rows][4 bytes]), so that a stage's token scales are
-// one 16-byte aligned bulk copy.
+// as for the 8-bit B).
+// Scales reach tensor memory by tcgen05.cp .32x128b.warpx4, issued by the MMA
+// thread just before the stage's MMAs (the tensor pipe keeps them in order):
+// it copies 32 rows of 16 bytes to the 32 lanes of every lane quarter, and
+// the MMA reads row r (A) or token n (B) at lane r mod 32 of its quarter,
+// column base + r/32 (n/32), byte = the K step. So a stage's scales are a
+// 512-byte chunk holding the word of row r at 16 (r mod 32) + 4 (r / 32):
+//   weights: arranged so at load time, per 128-row tile and 128-column stage
+//            (one bulk copy per operand and stage);
+//   activations: rows of 16 bytes whose word j is the scale word of row
+//            + 32 j, so that the 32 rows from any first row are that chunk
+//            (stage-major: [K/128][rows][16 bytes]).
+// Activation rows: E4M3, in expert order (row p for sorted position p).
 //
-// One persistent CTA per SM, 320 threads in roles; a unit is one item x one
+// One persistent CTA per SM, 192 threads in roles; a unit is one item x one
 // M tile of 128 rows (gate/up: 128 gate and the same 128 up rows, two MMAs a
 // K step into two accumulators, so that each thread of the epilogue holds
 // both values of its h row; down: 128 rows) x the item's tokens in passes of
 // at most 64 (the MMA's N, a multiple of 16), the contraction in stages of
 // 128 columns:
-//   warp 8     TMA: a stage's A operands (64-row boxes), its B rows (boxes of
-//              16 rows) and the scale blocks (bulk copies), on a ring of
+//   warp 4     TMA: a stage's A operands (64-row boxes), its B rows (boxes of
+//              16 rows) and its scale chunks (bulk copies), on a ring of
 //              shared-memory stages;
-//   warps 4-7  move a stage's scales to tensor memory in the layout the MMA
-//              reads (A: row r at lane r, column base + r/32; B: token n at
-//              lane n mod 32 of every lane quarter, column base + n/32; the
-//              byte of the word is the K step);
-//   warp 9     issues the stage's MMAs (M = 128, K = 32) into one of two
-//              accumulator sets in tensor memory, and the commits;
+//   warp 5     per stage: the scale copies to tensor memory, the MMAs (M =
+//              128, K = 32) into one of two accumulator sets, the commits;
 //   warps 0-3  the epilogue of a finished pass, one TMEM lane (one row) a
 //              thread: gate/up: h = silu(gate) * up, rounded to MXFP8 per 32
 //              rows (one warp a block) for the down GEMM; down: the rows of
@@ -56,8 +58,8 @@
 namespace dfm {
 namespace {
 
-constexpr int kThr = 320;
-constexpr int kSfWarp0 = 4, kTmaWarp = 8, kMmaWarp = 9;
+constexpr int kThr = 192;
+constexpr int kTmaWarp = 4, kMmaWarp = 5;
 constexpr int kM = 128, kHalfRows = 64;
 constexpr int kKS = 128;                  // contraction columns a stage
 constexpr int kN = 64;                    // tokens a pass at most
@@ -65,8 +67,8 @@ constexpr int kBoxRows = 16;              // B rows a TMA box
 constexpr int kABytes = kM * kKS;         // 16384: one A operand (a byte a code)
 constexpr int kAHalfTx = kHalfRows * kKS / 2;  // 4096: a 64-row box's codes as copied
 constexpr int kBBytes = kN * kKS;         // 8192
-constexpr int kSfaBytes = kM * 4;         // 512 a 128-row operand
-constexpr int kSfbBytes = kN * 4;         // 256
+constexpr int kSfBytes = 512;            // a stage's scale chunk (an operand's, or the tokens')
+constexpr int kSfRowBytes = 16;           // an activation row's scale words
 constexpr uint32_t kTmemCols = 512;
 
 // Per GEMM: A operands a stage (gate/up: gate and up), stages, and the
@@ -78,8 +80,8 @@ struct Geo {
   static constexpr size_t offA = 0;
   static constexpr size_t offB = offA + (size_t)S * NA * kABytes;
   static constexpr size_t offSfa = offB + (size_t)S * kBBytes;
-  static constexpr size_t offSfb = offSfa + (size_t)S * NA * kSfaBytes;
-  static constexpr size_t offBars = offSfb + (size_t)S * kSfbBytes;
+  static constexpr size_t offSfb = offSfa + (size_t)S * NA * kSfBytes;
+  static constexpr size_t offBars = offSfb + (size_t)S * kSfBytes;
   static constexpr uint32_t accCols = NA * kN;      // one accumulator set
   static constexpr uint32_t sfCol = 2 * accCols;    // then per stage NA x 4 A, 4 B
   static constexpr uint32_t sfStride = NA * 4 + 4;
@@ -87,7 +89,7 @@ struct Geo {
 
 template <int S>
 struct Bars {
-  uint64_t full[S], sfull[S], empty[S];
+  uint64_t full[S], empty[S];
   uint64_t accf[2], acce[2], fin;
   uint32_t tmem;
   int err;
@@ -109,7 +111,7 @@ struct Mx8Args {
   size_t sfa0, sfa1;      // span offsets of the A operands' scale sections
   int K, MT;              // contraction; M tiles an item
   int I, H;
-  const uint8_t* bsf;     // activation scales [K/128][rows_cap][4]
+  const uint8_t* bsf;     // activation scales [K/128][rows_cap][16]
   int rows_cap;
   const Item* items;
   const int32_t* n_items;
@@ -117,7 +119,7 @@ struct Mx8Args {
   int max_items, E, nassign;
   float* hbuf;            // gate/up: optional [nassign][I] h before rounding
   uint8_t* hq;            // gate/up: [rows_cap][I] E4M3 rows of h (expert order)
-  uint8_t* hsf;           // gate/up: [I/128][rows_cap][4] their scales
+  uint8_t* hsf;           // gate/up: [I/128][rows_cap][16] their scales
   float* part;            // down: [nassign][H]
   uint32_t* err;
 };
@@ -151,9 +153,15 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// First activation row of item i (rows of earlier items end before it): a
-// multiple of 4 from pos_i and i alone.
-__device__ __forceinline__ int row_base(int i, int pos) { return (pos + 3 * i + 3) & ~3; }
+// Writes the scale byte of block j (along K) of activation row `row` into
+// the stage-major, row-interleaved layout: stage j/4, byte j mod 4 of word q
+// of row row - 32 q, q = 0..3.
+__device__ __forceinline__ void put_scale(uint8_t* sf, int rows_cap, int row, int j, uint8_t v) {
+  const size_t ks = (size_t)(j >> 2);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (row - 32 * q >= 0) sf[((ks * rows_cap + row - 32 * q) * 4 + q) * 4 + (j & 3)] = v;
+}
 
 // ---------------------------------------------------------------------------
 // tensor memory, MMA and copy helpers
@@ -186,6 +194,10 @@ __device__ __forceinline__ void tma3d(void* dst, const ChunkMap* m, int x, int y
       "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
       "l"(m), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
+}
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, const void* src) {
+  const uint64_t d = umma::smem_desc(smem_u32(src), 128, 128);
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(d) : "memory");
 }
 __device__ __forceinline__ void tma2d(void* dst, const ChunkMap* m, int x, int y, uint64_t* bar) {
   asm volatile(
@@ -241,7 +253,7 @@ __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
 // gridDim.x), each one's passes of at most kN tokens, each pass's stages.
 struct Unit {
   bool ok;
-  int e, mt, pos, cnt, base;
+  int e, mt, pos, cnt;
 };
 __device__ __forceinline__ Unit unit_at(const Mx8Args& a, int u) {
   Unit w;
@@ -251,9 +263,8 @@ __device__ __forceinline__ Unit unit_at(const Mx8Args& a, int u) {
   w.e = it.e;
   w.pos = it.pos;
   w.cnt = it.cnt;
-  w.base = row_base(item, it.pos);
   w.ok = (unsigned)it.e < (unsigned)a.E && it.cnt >= 1 && it.pos >= 0 &&
-         it.pos + it.cnt <= a.nassign && w.base + ((it.cnt + 3) & ~3) <= a.rows_cap;
+         it.pos + it.cnt <= a.nassign && it.pos + it.cnt + 32 <= a.rows_cap;
   return w;
 }
 
@@ -275,31 +286,27 @@ __device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<
     for (int tb = 0; tb < w.cnt && ok; tb += kN) {
       const int nv = min(kN, w.cnt - tb);
       const int nb = (nv + kBoxRows - 1) / kBoxRows;
-      const uint32_t sfb_bytes = (uint32_t)((nv + 3) & ~3) * 4u;
-      const int row = w.base + tb;
+      const int row = w.pos + tb;
       for (int ks = 0; ks < nks; ++ks, ++g) {
         const uint32_t s = g % G::S, ph = (g / G::S) & 1u;
         if (!wait_or_give_up(&b->empty[s], ph ^ 1u, &b->err)) { ok = false; break; }
         uint64_t* full = &b->full[s];
-        mbar_arrive_expect_tx(full, G::NA * (2 * kAHalfTx + kSfaBytes) + nb * kBoxRows * kKS +
-                                        sfb_bytes);
+        mbar_arrive_expect_tx(full, G::NA * (2 * kAHalfTx + kSfBytes) + nb * kBoxRows * kKS +
+                                        kSfBytes);
         for (int o = 0; o < G::NA; ++o) {
           uint8_t* as = smem + G::offA + ((size_t)s * G::NA + o) * kABytes;
-          uint8_t* sa = smem + G::offSfa + ((size_t)s * G::NA + o) * kSfaBytes;
           const ChunkMap* m = o == 0 ? &a.amap0 : &a.amap1;
-          const size_t sec = o == 0 ? a.sfa0 : a.sfa1;
-          for (int h = 0; h < 2; ++h) {
+          for (int h = 0; h < 2; ++h)
             tma3d(as + h * (kABytes / 2), m, ks * kKS, kM * w.mt + kHalfRows * h, w.e, full);
-            bulk_plain(sa + h * (kSfaBytes / 2),
-                       span + sec + ((size_t)(2 * w.mt + h) * nks + ks) * (kHalfRows * 4),
-                       kSfaBytes / 2, full);
-          }
+          bulk_plain(smem + G::offSfa + ((size_t)s * G::NA + o) * kSfBytes,
+                     span + (o == 0 ? a.sfa0 : a.sfa1) + ((size_t)w.mt * nks + ks) * kSfBytes,
+                     kSfBytes, full);
         }
         uint8_t* bs = smem + G::offB + (size_t)s * kBBytes;
         for (int i = 0; i < nb; ++i)
           tma2d(bs + i * kBoxRows * kKS, &a.bmap, ks * kKS, row + kBoxRows * i, full);
-        bulk_plain(smem + G::offSfb + (size_t)s * kSfbBytes,
-                   a.bsf + ((size_t)ks * a.rows_cap + row) * 4, sfb_bytes, full);
+        bulk_plain(smem + G::offSfb + (size_t)s * kSfBytes,
+                   a.bsf + ((size_t)ks * a.rows_cap + row) * kSfRowBytes, kSfBytes, full);
         armed |= 1u << s;
         last_par = (last_par & ~(1u << s)) | (ph << s);
       }
@@ -308,49 +315,6 @@ __device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<
   // the copies in flight land before the CTA may leave
   for (int s = 0; s < G::S; ++s)
     if (armed >> s & 1u) drain(&b->full[s], last_par >> s & 1u);
-}
-
-template <int MODE>
-__device__ void role_sf(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE>::S>* b,
-                        uint32_t tmem, int q, int lane) {
-  using G = Geo<MODE>;
-  const int nks = a.K / kKS;
-  const int L = 32 * q + lane;
-  const uint32_t lane_addr = tmem + ((uint32_t)(32 * q) << 16);
-  uint32_t g = 0;
-  bool ok = true;
-  for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-    const Unit w = unit_at(a, u);
-    if (!w.ok) continue;
-    for (int tb = 0; tb < w.cnt && ok; tb += kN) {
-      const int nv4 = (min(kN, w.cnt - tb) + 3) & ~3;
-      for (int ks = 0; ks < nks; ++ks, ++g) {
-        const uint32_t s = g % G::S, ph = (g / G::S) & 1u;
-        if (!warp_wait(&b->full[s], ph, &b->err)) { ok = false; break; }
-        const uint32_t col = G::sfCol + G::sfStride * s;
-#pragma unroll
-        for (int o = 0; o < G::NA; ++o) {
-          const uint32_t va =
-              lds_u32(smem + G::offSfa + ((size_t)s * G::NA + o) * kSfaBytes + 4 * L);
-          asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(
-                           lane_addr + col + 4 * o + q),
-                       "r"(va)
-                       : "memory");
-        }
-        const uint8_t* sb = smem + G::offSfb + (size_t)s * kSfbBytes;
-        const uint32_t vb0 = lane < nv4 ? lds_u32(sb + 4 * lane) : 0x7F7F7F7Fu;
-        const uint32_t vb1 = lane + 32 < nv4 ? lds_u32(sb + 4 * (lane + 32)) : 0x7F7F7F7Fu;
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(
-                         lane_addr + col + 4 * G::NA),
-                     "r"(vb0), "r"(vb1)
-                     : "memory");
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&b->sfull[s]);
-      }
-    }
-  }
 }
 
 template <int MODE>
@@ -371,10 +335,15 @@ __device__ void role_mma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<
       tc_fence_after();
       for (int ks = 0; ks < nks; ++ks, ++g) {
         const uint32_t s = g % G::S, ph = (g / G::S) & 1u;
-        if (!wait_or_give_up(&b->sfull[s], ph, &b->err)) { ok = false; break; }
+        if (!wait_or_give_up(&b->full[s], ph, &b->err)) { ok = false; break; }
         tc_fence_after();
         const uint32_t bs = smem_u32(smem + G::offB + (size_t)s * kBBytes);
         const uint32_t col = tmem + G::sfCol + G::sfStride * s;
+        // the stage's scales into tensor memory, ahead of its MMAs
+#pragma unroll
+        for (int o = 0; o < G::NA; ++o)
+          tc_cp_sf(col + 4 * o, smem + G::offSfa + ((size_t)s * G::NA + o) * kSfBytes);
+        tc_cp_sf(col + 4 * G::NA, smem + G::offSfb + (size_t)s * kSfBytes);
 #pragma unroll
         for (int kk = 0; kk < kKS / 32; ++kk) {
           const uint32_t idesc = umma::idesc_mxf8f6f4_e2m1_e4m3(kM, N, kk, kk);
@@ -458,10 +427,9 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE>::S>*
             if (a.hbuf && (unsigned)aa < (unsigned)a.nassign)
               a.hbuf[(size_t)aa * a.I + r] = hv;
             const int sh = mx8_shared_exp(warp_max(fabsf(hv)));
-            const int row = w.base + tb + c0 + n;
+            const int row = w.pos + tb + c0 + n;
             a.hq[(size_t)row * a.I + r] = (uint8_t)e4m3_rn_sat(hv * pow2f(-sh));
-            if (lane == 0)
-              a.hsf[((size_t)(blk >> 2) * a.rows_cap + row) * 4 + (blk & 3)] = (uint8_t)(sh + 127);
+            if (lane == 0) put_scale(a.hsf, a.rows_cap, row, blk, (uint8_t)(sh + 127));
           }
         }
       }
@@ -488,7 +456,6 @@ __global__ void __launch_bounds__(kThr, 1) mx8_gemm_kernel(const __grid_constant
   if (threadIdx.x == 32) {
     for (int i = 0; i < G::S; ++i) {
       mbar_init(&b->full[i], 1);
-      mbar_init(&b->sfull[i], 4);
       mbar_init(&b->empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -511,8 +478,6 @@ __global__ void __launch_bounds__(kThr, 1) mx8_gemm_kernel(const __grid_constant
   const int n_units = n_items * a.MT;
   if (warp < 4) {
     role_epilogue<MODE>(a, n_units, b, tmem, warp, lane);
-  } else if (warp < kTmaWarp) {
-    role_sf<MODE>(a, n_units, smem, b, tmem, warp - kSfWarp0, lane);
   } else if (warp == kTmaWarp) {
     if (lane == 0) role_tma<MODE>(a, n_units, smem, b);
   } else if (warp == kMmaWarp && lane == 0) {
@@ -531,7 +496,7 @@ __global__ void __launch_bounds__(kThr, 1) mx8_gemm_kernel(const __grid_constant
 // Rounds activation rows to MXFP8 into the expert-ordered buffers: block =
 // item, thread j = 32-column block j of each of the item's rows. Row n of
 // item i is source row sorted[pos + n] / div (x: the token; h: the
-// assignment), written to q row row_base(i) + n.
+// assignment), written to q row pos + n.
 template <bool BF16>
 __global__ void __launch_bounds__(256) mx8_rows_kernel(const void* src, int K, int div,
                                                        const Item* items, const int32_t* n_items,
@@ -543,7 +508,7 @@ __global__ void __launch_bounds__(256) mx8_rows_kernel(const void* src, int K, i
   if (ni > max_items) ni = max_items;
   if (i >= ni) return;
   const Item it = items[i];
-  const int base = row_base(i, it.pos);
+  const int base = it.pos;
   if ((unsigned)it.e >= (unsigned)E || it.cnt < 1 || it.pos < 0 || it.pos + it.cnt > nassign ||
       base + it.cnt > rows_cap) {
     if (threadIdx.x == 0) atomicOr(err, DEV_ERR_RANGE);
@@ -597,7 +562,7 @@ __global__ void __launch_bounds__(256) mx8_rows_kernel(const void* src, int K, i
       uint4* d = reinterpret_cast<uint4*>(q + (size_t)(base + n) * K + 32 * j);
       d[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
       d[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
-      sf[((size_t)(j >> 2) * rows_cap + base + n) * 4 + (j & 3)] = (uint8_t)(sh + 127);
+      put_scale(sf, rows_cap, base + n, j, (uint8_t)(sh + 127));
     }
   }
 }
@@ -635,7 +600,9 @@ __global__ void mx8_layout_kernel(const uint8_t* src, uint8_t* dst, int n_spans,
         const size_t r0 = o - off_s[m];
         const int K = Ks[m], nb = K / 32, nks = K / kKS;
         const int r = (int)(r0 / nb), kb = (int)(r0 - (size_t)r * nb);
-        dev = off_s[m] + (((size_t)(r / 64) * nks + kb / 4) * 64 + (r % 64)) * 4 + (kb & 3);
+        const int rr = r % kM;  // row in its 128-row tile: word at 16 (rr mod 32) + 4 (rr / 32)
+        dev = off_s[m] + ((size_t)(r / kM) * nks + kb / 4) * kSfBytes + 16 * (rr % 32) +
+              4 * (rr / 32) + (kb & 3);
         canon = o;
         break;
       }
@@ -692,7 +659,10 @@ cudaError_t launch_mx8(const Mx8Args& a, cudaStream_t s) {
 
 bool mx8_supported(int H, int I) { return H % kKS == 0 && I % kKS == 0 && H >= kM; }
 
-int mx8_rows_cap(int nassign, int max_items) { return (nassign + 3 * max_items + 7) & ~3; }
+int mx8_rows_cap(int nassign, int max_items) {
+  (void)max_items;
+  return nassign + 32;  // a stage's token scales are read as 32 rows from the pass's first
+}
 
 bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E, ChunkMap* gate,
                    ChunkMap* up, ChunkMap* down) {
