@@ -282,7 +282,7 @@ cudaError_t launch_shared_gemm_down(const SharedMaps& m, int T, int H, int R, fl
 // ---- routed experts with MXFP8 activations (k_mx8.cu) ----------------------
 // The lossy variant: activations rounded to MXFP8 (E4M3 elements, E8M0 per
 // 32), experts as grouped GEMMs on tcgen05.mma kind::mxf8f6f4 with the MXFP4
-// weights in the canonical code layout and their scales stage-major.
+// codes and scales of each 128-row tile arranged stage by stage.
 bool mx8_supported(int H, int I);
 // Rows of the expert-ordered activation buffers for nassign assignments in
 // at most max_items items (the assignments' rows and 32 more, read past the

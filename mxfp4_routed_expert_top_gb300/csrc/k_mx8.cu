@@ -11,11 +11,13 @@
 // exponents itself. Products are exact and the sums are fp32, so the only
 // loss is the rounding of the activations to the format.
 //
-// Weights: the canonical MXFP4 codes (row-major, low nibble first) are read
-// by TMA as 16U4_ALIGN16B, which puts every 16 codes in the first 8 bytes of
-// a 16-byte group of shared memory: the operand layout of kind::mxf8f6f4 for
-// a 4-bit type (a byte of space per element, so a K = 32 step is 32 bytes,
-// as for the 8-bit B).
+// Weights: MXFP4 codes (low nibble first), arranged at load time so that
+// each 128-row tile's 128-column stage is 8 KB of contiguous rows of 64
+// bytes ([tile][stage][row][64 bytes]: the stream of a unit is sequential),
+// read by TMA as 16U4_ALIGN16B, which puts every 16 codes in the first 8
+// bytes of a 16-byte group of shared memory: the operand layout of
+// kind::mxf8f6f4 for a 4-bit type (a byte of space per element, so a K = 32
+// step is 32 bytes, as for the 8-bit B).
 // Scales reach tensor memory by tcgen05.cp .32x128b.warpx4, issued by the MMA
 // thread just before the stage's MMAs (the tensor pipe keeps them in order):
 // it copies 32 rows of 16 bytes to the 32 lanes of every lane quarter, and
@@ -39,7 +41,8 @@
 //              16 rows) and its scale chunks (bulk copies), on a ring of
 //              shared-memory stages;
 //   warp 5     per stage: the scale copies to tensor memory, the MMAs (M =
-//              128, K = 32) into one of two accumulator sets, the commits;
+//              128, K = 32) into one of 3 (gate/up) or 4 (down) accumulator
+//              sets in turn, the commits;
 //   warps 0-3  the epilogue of a finished pass, one TMEM lane (one row) a
 //              thread: gate/up: h = silu(gate) * up, rounded to MXFP8 per 32
 //              rows (one warp a block) for the down GEMM; down: the rows of
@@ -62,46 +65,57 @@ constexpr int kThr = 192;
 constexpr int kTmaWarp = 4, kMmaWarp = 5;
 constexpr int kM = 128, kHalfRows = 64;
 constexpr int kKS = 128;                  // contraction columns a stage
-constexpr int kN = 64;                    // tokens a pass at most
 constexpr int kBoxRows = 16;              // B rows a TMA box
 constexpr int kABytes = kM * kKS;         // 16384: one A operand (a byte a code)
 constexpr int kAHalfTx = kHalfRows * kKS / 2;  // 4096: a 64-row box's codes as copied
-constexpr int kBBytes = kN * kKS;         // 8192
 constexpr int kSfBytes = 512;            // a stage's scale chunk (an operand's, or the tokens')
 constexpr int kSfRowBytes = 16;           // an activation row's scale words
 constexpr uint32_t kTmemCols = 512;
 
-// Per GEMM: A operands a stage (gate/up: gate and up), stages, and the
-// layout of one stage in shared memory and of the tensor memory columns.
-template <int MODE>
+// Per GEMM and token tile KN (tokens a pass at most, 32 or 64): A operands
+// a stage (gate/up: gate and up), the stages that fit in shared memory, the
+// accumulator sets that fit in tensor memory beside the stages' scales, and
+// the layout of one stage in shared memory and of the tensor memory columns.
+template <int MODE, int KN>
 struct Geo {
   static constexpr int NA = MODE == 0 ? 2 : 1;
-  static constexpr int S = MODE == 0 ? 5 : 8;
+  static constexpr int BBytes = KN * kKS;
+  static constexpr int StageBytes = NA * kABytes + BBytes + NA * kSfBytes + kSfBytes;
+  static constexpr int S0 = (226 * 1024) / StageBytes;
+  static constexpr int S = S0 > 12 ? 12 : S0;
   static constexpr size_t offA = 0;
   static constexpr size_t offB = offA + (size_t)S * NA * kABytes;
-  static constexpr size_t offSfa = offB + (size_t)S * kBBytes;
+  static constexpr size_t offSfa = offB + (size_t)S * BBytes;
   static constexpr size_t offSfb = offSfa + (size_t)S * NA * kSfBytes;
   static constexpr size_t offBars = offSfb + (size_t)S * kSfBytes;
-  static constexpr uint32_t accCols = NA * kN;      // one accumulator set
-  static constexpr uint32_t sfCol = 2 * accCols;    // then per stage NA x 4 A, 4 B
-  static constexpr uint32_t sfStride = NA * 4 + 4;
+  static constexpr uint32_t accCols = NA * KN;      // one accumulator set
+  static constexpr uint32_t sfStride = NA * 4 + 4;  // per stage NA x 4 A, 4 B scale columns
+  static constexpr int NACC0 = (int)((kTmemCols - S * sfStride) / accCols);
+  static constexpr int NACC = NACC0 > 4 ? 4 : NACC0;  // accumulator sets (MMA runs ahead)
+  static constexpr uint32_t sfCol = NACC * accCols;
 };
 
-template <int S>
+template <int S, int NACC>
 struct Bars {
   uint64_t full[S], empty[S];
-  uint64_t accf[2], acce[2], fin;
+  uint64_t accf[NACC], acce[NACC], fin;
   uint32_t tmem;
   int err;
 };
-template <int MODE>
+template <int MODE, int KN>
 constexpr size_t smem_bytes() {
-  return Geo<MODE>::offBars + sizeof(Bars<Geo<MODE>::S>);
+  using G = Geo<MODE, KN>;
+  return G::offBars + sizeof(Bars<G::S, G::NACC>);
 }
-static_assert(smem_bytes<0>() <= 227 * 1024 && smem_bytes<1>() <= 227 * 1024, "shared memory");
-static_assert(Geo<0>::sfCol + Geo<0>::sfStride * Geo<0>::S <= kTmemCols, "tensor memory");
-static_assert(Geo<1>::sfCol + Geo<1>::sfStride * Geo<1>::S <= kTmemCols, "tensor memory");
-static_assert(Geo<0>::offB % 1024 == 0 && Geo<1>::offB % 1024 == 0, "128-byte swizzle atoms");
+template <int MODE, int KN>
+constexpr bool geo_ok() {
+  using G = Geo<MODE, KN>;
+  return smem_bytes<MODE, KN>() <= 227 * 1024 && G::NACC >= 2 &&
+         G::sfCol + G::sfStride * G::S <= kTmemCols && G::offB % 1024 == 0 &&
+         G::BBytes % 1024 == 0;
+}
+static_assert(geo_ok<0, 32>() && geo_ok<0, 64>() && geo_ok<1, 32>() && geo_ok<1, 64>(),
+              "shared or tensor memory");
 
 struct Mx8Args {
   ChunkMap amap0, amap1;  // gate/up: gate and up codes; down: down codes
@@ -187,12 +201,15 @@ __device__ __forceinline__ void mma_mx(uint32_t d, uint64_t ad, uint64_t bd, uin
       "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
       : "memory");
 }
-__device__ __forceinline__ void tma3d(void* dst, const ChunkMap* m, int x, int y, int z,
-                                      uint64_t* bar) {
+// Weight tiles (read once a call): evict-first in L2, so that the streamed
+// weights do not push out the activation rows every M tile re-reads.
+// Coordinates (element, row in the tile, stage, tile, expert).
+__device__ __forceinline__ void tma5d_stream(void* dst, const ChunkMap* m, int r, int ks, int tile,
+                                             int e, uint64_t* bar, uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-      "l"(m), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+      "l"(m), "r"(0), "r"(r), "r"(ks), "r"(tile), "r"(e), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, const void* src) {
@@ -250,7 +267,7 @@ __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
 }
 
 // The sequence every role walks: the CTA's units (u = blockIdx.x + j *
-// gridDim.x), each one's passes of at most kN tokens, each pass's stages.
+// gridDim.x), each one's passes of at most KN tokens, each pass's stages.
 struct Unit {
   bool ok;
   int e, mt, pos, cnt;
@@ -272,19 +289,20 @@ __device__ __forceinline__ Unit unit_at(const Mx8Args& a, int u) {
 // roles
 // ---------------------------------------------------------------------------
 
-template <int MODE>
-__device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE>::S>* b) {
-  using G = Geo<MODE>;
+template <int MODE, int KN>
+__device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE, KN>::S, Geo<MODE, KN>::NACC>* b) {
+  using G = Geo<MODE, KN>;
   const int nks = a.K / kKS;
   uint32_t g = 0;
   uint32_t armed = 0u, last_par = 0u;
   bool ok = true;
+  const uint64_t pol = l2_evict_first_policy();
   for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
     const Unit w = unit_at(a, u);
     if (!w.ok) continue;
     const uint8_t* span = a.arena + (size_t)w.e * a.span_bytes;
-    for (int tb = 0; tb < w.cnt && ok; tb += kN) {
-      const int nv = min(kN, w.cnt - tb);
+    for (int tb = 0; tb < w.cnt && ok; tb += KN) {
+      const int nv = min(KN, w.cnt - tb);
       const int nb = (nv + kBoxRows - 1) / kBoxRows;
       const int row = w.pos + tb;
       for (int ks = 0; ks < nks; ++ks, ++g) {
@@ -297,12 +315,12 @@ __device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<
           uint8_t* as = smem + G::offA + ((size_t)s * G::NA + o) * kABytes;
           const ChunkMap* m = o == 0 ? &a.amap0 : &a.amap1;
           for (int h = 0; h < 2; ++h)
-            tma3d(as + h * (kABytes / 2), m, ks * kKS, kM * w.mt + kHalfRows * h, w.e, full);
-          bulk_plain(smem + G::offSfa + ((size_t)s * G::NA + o) * kSfBytes,
-                     span + (o == 0 ? a.sfa0 : a.sfa1) + ((size_t)w.mt * nks + ks) * kSfBytes,
-                     kSfBytes, full);
+            tma5d_stream(as + h * (kABytes / 2), m, kHalfRows * h, ks, w.mt, w.e, full, pol);
+          bulk_g2s(smem + G::offSfa + ((size_t)s * G::NA + o) * kSfBytes,
+                   span + (o == 0 ? a.sfa0 : a.sfa1) + ((size_t)w.mt * nks + ks) * kSfBytes,
+                   kSfBytes, full, pol);
         }
-        uint8_t* bs = smem + G::offB + (size_t)s * kBBytes;
+        uint8_t* bs = smem + G::offB + (size_t)s * G::BBytes;
         for (int i = 0; i < nb; ++i)
           tma2d(bs + i * kBoxRows * kKS, &a.bmap, ks * kKS, row + kBoxRows * i, full);
         bulk_plain(smem + G::offSfb + (size_t)s * kSfBytes,
@@ -317,27 +335,27 @@ __device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<
     if (armed >> s & 1u) drain(&b->full[s], last_par >> s & 1u);
 }
 
-template <int MODE>
-__device__ void role_mma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE>::S>* b,
+template <int MODE, int KN>
+__device__ void role_mma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE, KN>::S, Geo<MODE, KN>::NACC>* b,
                          uint32_t tmem) {
-  using G = Geo<MODE>;
+  using G = Geo<MODE, KN>;
   const int nks = a.K / kKS;
   uint32_t g = 0, pc = 0;
   bool ok = true;
   for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
     const Unit w = unit_at(a, u);
     if (!w.ok) continue;
-    for (int tb = 0; tb < w.cnt && ok; tb += kN, ++pc) {
-      const int nv = min(kN, w.cnt - tb);
+    for (int tb = 0; tb < w.cnt && ok; tb += KN, ++pc) {
+      const int nv = min(KN, w.cnt - tb);
       const int N = (nv + 15) & ~15;
-      const uint32_t acc = pc & 1u;
-      if (!wait_or_give_up(&b->acce[acc], ((pc >> 1) & 1u) ^ 1u, &b->err)) { ok = false; break; }
+      const uint32_t acc = pc % G::NACC;
+      if (!wait_or_give_up(&b->acce[acc], ((pc / G::NACC) & 1u) ^ 1u, &b->err)) { ok = false; break; }
       tc_fence_after();
       for (int ks = 0; ks < nks; ++ks, ++g) {
         const uint32_t s = g % G::S, ph = (g / G::S) & 1u;
         if (!wait_or_give_up(&b->full[s], ph, &b->err)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t bs = smem_u32(smem + G::offB + (size_t)s * kBBytes);
+        const uint32_t bs = smem_u32(smem + G::offB + (size_t)s * G::BBytes);
         const uint32_t col = tmem + G::sfCol + G::sfStride * s;
         // the stage's scales into tensor memory, ahead of its MMAs
 #pragma unroll
@@ -351,7 +369,7 @@ __device__ void role_mma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<
 #pragma unroll
           for (int o = 0; o < G::NA; ++o) {
             const uint32_t as = smem_u32(smem + G::offA + ((size_t)s * G::NA + o) * kABytes);
-            mma_mx(tmem + acc * G::accCols + o * kN, umma::smem_desc_sw128(as + 32 * kk), bd,
+            mma_mx(tmem + acc * G::accCols + o * KN, umma::smem_desc_sw128(as + 32 * kk), bd,
                    idesc, col + 4 * o, col + 4 * G::NA, (ks | kk) != 0);
           }
         }
@@ -378,10 +396,10 @@ __device__ __forceinline__ void tmem_ld32(uint32_t addr, uint32_t (&v)[32]) {
       : "r"(addr));
 }
 
-template <int MODE>
-__device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE>::S>* b,
+template <int MODE, int KN>
+__device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN>::S, Geo<MODE, KN>::NACC>* b,
                               uint32_t tmem, int warp, int lane) {
-  using G = Geo<MODE>;
+  using G = Geo<MODE, KN>;
   const int L = 32 * warp + lane;
   const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
   uint32_t pc = 0;
@@ -393,13 +411,15 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE>::S>*
       continue;
     }
     const int r = kM * w.mt + L;  // this thread's row (h row or output row)
-    for (int tb = 0; tb < w.cnt && ok; tb += kN, ++pc) {
-      const int nv = min(kN, w.cnt - tb);
-      const uint32_t acc = pc & 1u;
-      if (!warp_wait(&b->accf[acc], (pc >> 1) & 1u, &b->err)) { ok = false; break; }
+    for (int tb = 0; tb < w.cnt && ok; tb += KN, ++pc) {
+      const int nv = min(KN, w.cnt - tb);
+      const uint32_t acc = pc % G::NACC;
+      if (!warp_wait(&b->accf[acc], (pc / G::NACC) & 1u, &b->err)) { ok = false; break; }
       tc_fence_after();
       for (int c0 = 0; c0 < nv; c0 += 32) {
         const int nc = min(32, nv - c0);
+        // the chunk's assignment indices, one a lane, fetched together
+        const int my_a = lane < nc ? a.sorted[w.pos + tb + c0 + lane] : -1;
         uint32_t v[32];
         tmem_ld32(lane_addr + acc * G::accCols + c0, v);
         if (MODE == 1) {
@@ -407,7 +427,7 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE>::S>*
 #pragma unroll
           for (int n = 0; n < 32; ++n) {
             if (n >= nc) break;
-            const int aa = a.sorted[w.pos + tb + c0 + n];
+            const int aa = __shfl_sync(0xffffffffu, my_a, n);
             if ((unsigned)aa < (unsigned)a.nassign)
               a.part[(size_t)aa * a.H + r] = __uint_as_float(v[n]);
             else if (lane == 0)
@@ -415,7 +435,7 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE>::S>*
           }
         } else {
           uint32_t vu[32];
-          tmem_ld32(lane_addr + acc * G::accCols + kN + c0, vu);
+          tmem_ld32(lane_addr + acc * G::accCols + KN + c0, vu);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
           const int blk = 4 * w.mt + warp;  // MXFP8 block of h along I
 #pragma unroll
@@ -423,7 +443,7 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE>::S>*
             if (n >= nc) break;
             const float gt = __uint_as_float(v[n]);
             const float hv = gt / (1.f + expf(-gt)) * __uint_as_float(vu[n]);
-            const int aa = a.sorted[w.pos + tb + c0 + n];
+            const int aa = __shfl_sync(0xffffffffu, my_a, n);
             if (a.hbuf && (unsigned)aa < (unsigned)a.nassign)
               a.hbuf[(size_t)aa * a.I + r] = hv;
             const int sh = mx8_shared_exp(warp_max(fabsf(hv)));
@@ -440,11 +460,11 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE>::S>*
   }
 }
 
-template <int MODE>
+template <int MODE, int KN>
 __global__ void __launch_bounds__(kThr, 1) mx8_gemm_kernel(const __grid_constant__ Mx8Args a) {
-  using G = Geo<MODE>;
+  using G = Geo<MODE, KN>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  Bars<G::S>* b = reinterpret_cast<Bars<G::S>*>(smem + G::offBars);
+  Bars<G::S, G::NACC>* b = reinterpret_cast<Bars<G::S, G::NACC>*>(smem + G::offBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -458,7 +478,7 @@ __global__ void __launch_bounds__(kThr, 1) mx8_gemm_kernel(const __grid_constant
       mbar_init(&b->full[i], 1);
       mbar_init(&b->empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < G::NACC; ++i) {
       mbar_init(&b->accf[i], 1);
       mbar_init(&b->acce[i], 4);
     }
@@ -477,11 +497,11 @@ __global__ void __launch_bounds__(kThr, 1) mx8_gemm_kernel(const __grid_constant
   }
   const int n_units = n_items * a.MT;
   if (warp < 4) {
-    role_epilogue<MODE>(a, n_units, b, tmem, warp, lane);
+    role_epilogue<MODE, KN>(a, n_units, b, tmem, warp, lane);
   } else if (warp == kTmaWarp) {
-    if (lane == 0) role_tma<MODE>(a, n_units, smem, b);
+    if (lane == 0) role_tma<MODE, KN>(a, n_units, smem, b);
   } else if (warp == kMmaWarp && lane == 0) {
-    role_mma<MODE>(a, n_units, smem, b, tmem);
+    role_mma<MODE, KN>(a, n_units, smem, b, tmem);
   }
   tc_fence_before();
   __syncthreads();
@@ -583,11 +603,13 @@ __global__ void mx8_plain_kernel(const float* v, int rows, int n, uint8_t* codes
   scales[t] = (uint8_t)(sh + 127);
 }
 
-// Canonical span <-> MXFP8-path span: the code sections stay, the three
-// scale sections go stage-major (or back, `inverse`). One thread a byte.
+// Canonical span <-> MXFP8-path span: the three code sections go to
+// [tile][stage][row][64 bytes], the three scale sections to 512-byte chunks
+// per tile and stage (or back, `inverse`). One thread a byte.
 __global__ void mx8_layout_kernel(const uint8_t* src, uint8_t* dst, int n_spans, int H, int I,
                                   size_t span, int inverse) {
   const size_t q = (size_t)H * I / 2, sb = (size_t)H * I / 32;
+  const size_t off_q[3] = {0, q + sb, 2 * q + 2 * sb};
   const size_t off_s[3] = {q, 2 * q + sb, 3 * q + 2 * sb};
   const int Ks[3] = {H, H, I};
   const size_t total = (size_t)n_spans * span;
@@ -596,6 +618,15 @@ __global__ void mx8_layout_kernel(const uint8_t* src, uint8_t* dst, int n_spans,
     const size_t sp = t / span, o = t - sp * span;
     size_t canon = o, dev = o;
     for (int m = 0; m < 3; ++m) {
+      if (o >= off_q[m] && o < off_q[m] + q) {
+        // codes: [tile][stage][row][64 bytes]
+        const size_t r0 = o - off_q[m];
+        const int K = Ks[m], rb = K / 2, nks = K / kKS;
+        const int r = (int)(r0 / rb), c = (int)(r0 - (size_t)r * rb);
+        dev = off_q[m] + (((size_t)(r / kM) * nks + c / (kKS / 2)) * kM + r % kM) * (kKS / 2) +
+              c % (kKS / 2);
+        break;
+      }
       if (o >= off_s[m] && o < off_s[m] + sb) {
         const size_t r0 = o - off_s[m];
         const int K = Ks[m], nb = K / 32, nks = K / kKS;
@@ -639,20 +670,31 @@ int sms_mx8() {
   return n;
 }
 
-template <int MODE>
-cudaError_t launch_mx8(const Mx8Args& a, cudaStream_t s) {
+template <int MODE, int KN>
+cudaError_t launch_mx8_kn(const Mx8Args& a, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        mx8_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<MODE>());
+    const cudaError_t e =
+        cudaFuncSetAttribute(mx8_gemm_kernel<MODE, KN>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_bytes<MODE, KN>());
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const long long units = (long long)a.max_items * a.MT;
   int grid = sms_mx8();
   if (units < grid) grid = (int)(units > 0 ? units : 1);
-  mx8_gemm_kernel<MODE><<<grid, kThr, smem_bytes<MODE>(), s>>>(a);
+  mx8_gemm_kernel<MODE, KN><<<grid, kThr, smem_bytes<MODE, KN>(), s>>>(a);
   return cudaGetLastError();
+}
+
+// The token tile: 32 when the items average up to 24 tokens (a smaller B
+// slot leaves room for more stages, i.e. more weight bytes in flight), else
+// 64 (fewer passes over each expert's weights).
+template <int MODE>
+cudaError_t launch_mx8(const Mx8Args& a, cudaStream_t s) {
+  return a.nassign <= 24LL * a.max_items ? launch_mx8_kn<MODE, 32>(a, s)
+                                         : launch_mx8_kn<MODE, 64>(a, s);
 }
 
 }  // namespace
@@ -673,11 +715,14 @@ bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E,
   ChunkMap* maps[3] = {gate, up, down};
   for (int m = 0; m < 3; ++m) {
     const int K = m < 2 ? H : I, rows = m < 2 ? I : H;
-    const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)E};
-    const cuuint64_t strides[2] = {(cuuint64_t)K / 2, (cuuint64_t)span_bytes};
-    const cuuint32_t box[3] = {kKS, kHalfRows, 1};
-    const cuuint32_t es[3] = {1, 1, 1};
-    if (enc(reinterpret_cast<CUtensorMap*>(maps[m]), CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3,
+    // (128 codes = 64 bytes, 128 rows, K/128 stages, rows/128 tiles, E experts)
+    const cuuint64_t dims[5] = {(cuuint64_t)kKS, (cuuint64_t)kM, (cuuint64_t)(K / kKS),
+                                (cuuint64_t)(rows / kM), (cuuint64_t)E};
+    const cuuint64_t strides[4] = {(cuuint64_t)kKS / 2, (cuuint64_t)kM * kKS / 2,
+                                   (cuuint64_t)K / kKS * kM * kKS / 2, (cuuint64_t)span_bytes};
+    const cuuint32_t box[5] = {kKS, kHalfRows, 1, 1, 1};
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    if (enc(reinterpret_cast<CUtensorMap*>(maps[m]), CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 5,
             const_cast<uint8_t*>(arena + offs[m]), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
