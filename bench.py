@@ -71,6 +71,9 @@ def parse():
     p.add_argument("--mxfp8", action="store_true",
                    help="the lossy MXFP8-activation variant (DF_MOE_MXFP8_ACT): routed "
                         "experts on block-scaled MXFP4 x MXFP8 tcgen05 GEMMs")
+    p.add_argument("--planes", action="store_true",
+                   help="exact batches on the block-scaled MXFP4 x E4M3 tcgen05 GEMMs, "
+                        "activations as sums of E4M3 planes (DF_MOE_PLANES)")
     p.add_argument("--experts", type=int, default=0,
                    help="profiling aid: override the routed-expert count (same "
                         "per-token work, smaller resident set); not a bench line")
@@ -100,14 +103,15 @@ def gateup_bytes(wl, n_union, T, with_shared=False):
     return b
 
 
-def mx8_gateup_bytes(wl, n_union, T):
-    """Algorithmic bytes of the MXFP8 variant's gate/up GEMM: the gate and up
-    halves of every distinct selected expert (codes + scales), the E4M3 x rows
-    of the T*k assignments with their scales in, and the E4M3 h rows with
-    their scales out."""
+def mx8_gateup_bytes(wl, n_union, T, planes=1):
+    """Algorithmic bytes of the block-scaled gate/up GEMM: the gate and up
+    halves of every distinct selected expert (codes + scales) and the E4M3 x
+    rows of the T*k assignments (`planes` rows each) with their scales in;
+    out, the E4M3 h rows with their scales (MXFP8) or h in fp32 (planes)."""
     per_expert = 2 * wl.I * wl.H * 17 // 32
     rows = T * wl.k
-    return n_union * per_expert + rows * (wl.H + wl.H // 32) + rows * (wl.I + wl.I // 32)
+    h_out = rows * (wl.I + wl.I // 32) if planes == 1 else rows * wl.I * 4
+    return n_union * per_expert + rows * planes * (wl.H + wl.H // 32) + h_out
 
 
 def gateup_flops(wl, T):
@@ -318,7 +322,8 @@ def run_ours(args):
     T = wl.T
     flags = ((dfm.STACK_RMSNORM_RESIDUAL if wl.stack else 0)
              | (dfm.PREFILL_MMA_SYNC if args.mma_sync_prefill else 0)
-             | (dfm.MXFP8_ACT if args.mxfp8 else 0))
+             | (dfm.MXFP8_ACT if args.mxfp8 else 0)
+             | (dfm.PLANES if args.planes else 0))
     if args.cache_slots and T > 8:
         raise SystemExit("--cache-slots serves decode batches (<= 8 tokens)")
     m = dfm.MoE(wl.H, wl.E, wl.k, wl.I, wl.n_shared, wl.Is, n_layers=wl.L,
@@ -481,6 +486,38 @@ def run_ours(args):
         if i >= 3:
             e2e_t.append(time.perf_counter() - t0)
     e2e_s = sum(e2e_t)
+    # where the host-buffer call's time goes: its copies on their own (same
+    # sizes, pinned memory, each followed by a synchronisation), an empty
+    # synchronisation, and the device step; the rest is the library's host
+    # work and kernel launches
+    xdev = torch.empty((T, wl.H), dtype=torch.int16, device="cuda")
+
+    def host_us(fn, n=50):
+        fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            fn()
+        return (time.perf_counter() - t0) / n * 1e6
+
+    def h2d():
+        xdev.copy_(hx[0], non_blocking=True)
+        stream.synchronize()
+
+    def d2h():
+        hout.copy_(out, non_blocking=True)
+        hids.copy_(ids, non_blocking=True)
+        hw.copy_(w, non_blocking=True)
+        stream.synchronize()
+
+    call_us = e2e_s / max(len(e2e_t), 1) * 1e6
+    h2d_us, d2h_us, sync_us = host_us(h2d), host_us(d2h), host_us(stream.synchronize)
+    dev_us = float(np.median(step_ms)) * 1e3
+    e2e_breakdown = {"call_us": round(call_us, 1), "device_step_us": round(dev_us, 1),
+                     "h2d_copy_and_sync_us": round(h2d_us, 1),
+                     "d2h_copies_and_sync_us": round(d2h_us, 1),
+                     "empty_sync_us": round(sync_us, 1),
+                     "launch_and_host_us": round(call_us - dev_us - h2d_us - d2h_us + sync_us, 1)}
 
     dev_s_max, tokens = aggregate_over_ranks(dist, dev_s, T * args.steps, device="cuda")
     e2e_max, e2e_tokens = aggregate_over_ranks(dist, e2e_s, T * e2e_steps, device="cuda")
@@ -496,7 +533,7 @@ def run_ours(args):
     # dominant kernel: the routed gate/up GEMM (tcgen05, larger batches),
     # else the gate/up phase of decode batches
     if kt.get("mx8_gateup", (0, 0.0))[0]:
-        dom, dom_bytes = "mx8_gateup", mx8_gateup_bytes(wl, u_mean, T)
+        dom, dom_bytes = "mx8_gateup", mx8_gateup_bytes(wl, u_mean, T, 4 if args.planes else 1)
     elif kt.get("gemm_gateup", (0, 0.0))[0]:
         dom, dom_bytes = "gemm_gateup", gateup_bytes(wl, u_mean, T)
     else:
@@ -514,7 +551,8 @@ def run_ours(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e2m1 x e4m3, f32 accumulate" if args.mxfp8 else "f32",
+        "dtype": ("e2m1 x e4m3, f32 accumulate" if args.mxfp8 else
+                  "e2m1 x e4m3 planes, f32 accumulate" if args.planes else "f32"),
         "data": "synthetic",
         "impl": "ours",
         "config": {**workload_config(wl, ws),
@@ -522,7 +560,9 @@ def run_ours(args):
                    "launch": "cuda graph" if args.graph else "stream",
                    "prefill_path": "mma_sync" if args.mma_sync_prefill else "tcgen05",
                    "activations": ("MXFP8 (E4M3, E8M0 per 32) into the routed experts: "
-                                   "the lossy variant") if args.mxfp8 else "exact",
+                                   "the lossy variant") if args.mxfp8 else
+                                  ("exact, as sums of E4M3 planes (x 4, h 5) on the "
+                                   "block-scaled GEMMs") if args.planes else "exact",
                    "experts_home": ("pinned host memory, %d a layer cached in HBM"
                                     % args.cache_slots) if args.cache_slots else "HBM",
                    "tokens": ("AR(1) stream, neighbour correlation %g" % args.token_corr)
@@ -548,7 +588,8 @@ def run_ours(args):
         "tensor": tensor_use(kt, wl, T),
         "e2e": {"value": round(e2e_tokens / e2e_max, 2), "unit": UNIT,
                 "h2d_bytes_per_step": T * wl.H * 2,
-                "d2h_bytes_per_step": T * wl.H * 2 + wl.L * T * wl.k * 8},
+                "d2h_bytes_per_step": T * wl.H * 2 + wl.L * T * wl.k * 8,
+                "breakdown": e2e_breakdown},
         "gpu_launches": launches,
         **({"cache": cache} if cache else {}),
         "clocks": clk.summary(),

@@ -80,6 +80,14 @@ extern "C" {
  * router and the shared experts stay exact. Needs hidden and inter multiples
  * of 128; not with an expert cache or DF_MOE_PREFILL_MMA_SYNC. */
 #define DF_MOE_MXFP8_ACT 8u
+/* The same block-scaled tensor-core GEMMs on exact activations: x and h
+ * enter them as sums of E4M3 planes (x: 4, h: 5), each plane the MXFP8
+ * rounding of what the planes before it left, so that the sum reproduces the
+ * activation to fp32 precision; the results are the exact path's, within its
+ * tolerances. Meant for batches (prefill): on such a handle decode calls run
+ * these GEMMs too, slower than the default decode kernels. Same shape rules
+ * as DF_MOE_MXFP8_ACT, and not together with it. */
+#define DF_MOE_PLANES 16u
 
 typedef struct df_moe df_moe; /* opaque, library-owned */
 
@@ -94,7 +102,7 @@ typedef struct {
   int32_t max_tokens;   /* largest T a forward call may use (1..4096)          */
   float rms_eps;        /* stack mode only                                     */
   uint32_t flags;       /* DF_MOE_STACK_RMSNORM_RESIDUAL | DF_MOE_PREFILL_MMA_SYNC |
-                           DF_MOE_MXFP8_ACT */
+                           DF_MOE_MXFP8_ACT | DF_MOE_PLANES */
 } df_moe_config;
 
 /* Weights of one layer, any subset per call (NULL / 0 = leave unchanged). */

@@ -15,6 +15,7 @@ OK, EINVAL, ENOMEM, ECUDA, ESTATE, ERANGE, ETIMEOUT, EDEVICE = 0, -1, -2, -3, -4
 STACK_RMSNORM_RESIDUAL = 1
 PREFILL_MMA_SYNC = 4
 MXFP8_ACT = 8
+PLANES = 16
 KERNEL_KINDS = 18
 
 # every symbol the header declares (checked by the CPU tests)

@@ -90,14 +90,16 @@ struct df_moe {
   uint16_t* s_hh = nullptr;      // [Tmax][3][R] bf16: shared h rows (3 parts), batches
   float* g_bsc = nullptr;        // [Tmax*k] their power-of-two row scales
   ChunkMap bmap_gu{}, bmap_dn{};
-  // the MXFP8-activation variant (DF_MOE_MXFP8_ACT): E4M3 rows of x and h in
-  // expert order and their scales, stage-major
+  // block-scaled GEMMs on E4M3 activations: the MXFP8 variant
+  // (DF_MOE_MXFP8_ACT, one plane) or exact planes (DF_MOE_PLANES); E4M3 rows
+  // of x and h in expert order and their scales, stage-major
   bool mx8 = false;
-  int mx_rows = 0;
-  uint8_t* mx_xq = nullptr;   // [mx_rows][H]
-  uint8_t* mx_xsf = nullptr;  // [H/128][mx_rows][16]
-  uint8_t* mx_hq = nullptr;   // [mx_rows][I]
-  uint8_t* mx_hsf = nullptr;  // [I/128][mx_rows][16]
+  int px = 1, ph = 1;         // planes of x and of h
+  int mx_xrows = 0, mx_hrows = 0;
+  uint8_t* mx_xq = nullptr;   // [mx_xrows][H]
+  uint8_t* mx_xsf = nullptr;  // [H/128][mx_xrows][16]
+  uint8_t* mx_hq = nullptr;   // [mx_hrows][I]
+  uint8_t* mx_hsf = nullptr;  // [I/128][mx_hrows][16]
   ChunkMap mx_xmap{}, mx_hmap{};
   bool phase = false;  // decode batches run the two phase kernels
   int sms = 0;
@@ -285,16 +287,18 @@ int expert_gateup(df_moe* h, int l, const uint16_t* x, int T, int max_items, int
   const df_moe_config& c = h->cfg;
   const uint8_t* arena = h->layers[l].arena;
   if (h->mx8) {
-    // MXFP8 activations: x rounded per assignment row, then the block-scaled
-    // GEMM (h rounded again in its epilogue for the down GEMM)
+    // block-scaled GEMM on E4M3 x: MXFP8 (h rounded again in its epilogue
+    // for the down GEMM) or x's planes (h exact into hbuf)
     const LayerBufs& L = h->layers[l];
-    RUN(h, K_MX8_QUANT, s, launch_mx8_rows(x, true, c.hidden, c.top_k, h->items, h->n_items,
-                                           max_items, h->sorted, T * c.top_k, c.n_experts,
-                                           h->mx_xq, h->mx_xsf, h->mx_rows, h->err, s));
+    RUN(h, K_MX8_QUANT, s, launch_mx8_rows(x, true, c.hidden, c.top_k, h->px, h->items,
+                                           h->n_items, max_items, h->sorted, T * c.top_k,
+                                           c.n_experts, h->mx_xq, h->mx_xsf, h->mx_xrows, h->err,
+                                           s));
     RUN(h, K_MX8_GU, s, launch_mx8_gateup(L.mx_gate, L.mx_up, h->mx_xmap, arena, h->span_bytes,
-                                          c.hidden, c.inter, h->mx_xsf, h->mx_rows, h->items,
+                                          c.hidden, c.inter, h->mx_xsf, h->mx_xrows, h->items,
                                           h->n_items, max_items, h->sorted, c.n_experts,
-                                          T * c.top_k, hbuf, h->mx_hq, h->mx_hsf, h->err, s));
+                                          T * c.top_k, hbuf, h->mx_hq, h->mx_hsf, h->px, h->err,
+                                          s));
     return DF_MOE_OK;
   }
   if (use_gemm(h, T, tg)) {
@@ -318,16 +322,17 @@ int expert_down(df_moe* h, int l, const float* hbuf, int T, int max_items, int t
   const df_moe_config& c = h->cfg;
   const uint8_t* arena = h->layers[l].arena;
   if (h->mx8) {
-    // MXFP8 activations: h (when given) rounded first; else the gate/up
-    // GEMM's rounded h
+    // block-scaled GEMM on E4M3 h: h (when given) rounded to MXFP8 or split
+    // into its planes first; else (MXFP8) the gate/up GEMM's rounded h
     if (hbuf)
-      RUN(h, K_MX8_QUANT, s, launch_mx8_rows(hbuf, false, c.inter, 1, h->items, h->n_items,
-                                             max_items, h->sorted, T * c.top_k, c.n_experts,
-                                             h->mx_hq, h->mx_hsf, h->mx_rows, h->err, s));
+      RUN(h, K_MX8_QUANT, s, launch_mx8_rows(hbuf, false, c.inter, 1, h->ph, h->items,
+                                             h->n_items, max_items, h->sorted, T * c.top_k,
+                                             c.n_experts, h->mx_hq, h->mx_hsf, h->mx_hrows,
+                                             h->err, s));
     RUN(h, K_MX8_DN, s, launch_mx8_down(h->layers[l].mx_down, h->mx_hmap, arena, h->span_bytes,
-                                        c.hidden, c.inter, h->mx_hsf, h->mx_rows, h->items,
+                                        c.hidden, c.inter, h->mx_hsf, h->mx_hrows, h->items,
                                         h->n_items, max_items, h->sorted, c.n_experts,
-                                        T * c.top_k, h->part, h->err, s));
+                                        T * c.top_k, h->part, h->ph, h->err, s));
     return DF_MOE_OK;
   }
   if (use_gemm(h, T, tg)) {
@@ -506,9 +511,10 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
       if (rc) return rc;
     }
     // (the MXFP8 variant hands h from GEMM to GEMM already rounded)
-    rc = expert_gateup(h, l, x, T, max_items, tg, h->mx8 ? nullptr : h->hbuf, s);
+    const bool rounded_h = h->mx8 && h->ph == 1;
+    rc = expert_gateup(h, l, x, T, max_items, tg, rounded_h ? nullptr : h->hbuf, s);
     if (rc) return rc;
-    rc = expert_down(h, l, h->mx8 ? nullptr : h->hbuf, T, max_items, tg, s, 0,
+    rc = expert_down(h, l, rounded_h ? nullptr : h->hbuf, T, max_items, tg, s, 0,
                      /*after_gateup=*/true);
     if (rc) return rc;
   }
@@ -578,17 +584,18 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
   if (c.n_layers > 1 && !(c.flags & DF_MOE_STACK_RMSNORM_RESIDUAL))
     return fail(nullptr, DF_MOE_EINVAL, "n_layers > 1 needs DF_MOE_STACK_RMSNORM_RESIDUAL");
   if ((c.flags & ~(DF_MOE_STACK_RMSNORM_RESIDUAL | DF_MOE_PREFILL_MMA_SYNC |
-                   DF_MOE_MXFP8_ACT)) != 0)
+                   DF_MOE_MXFP8_ACT | DF_MOE_PLANES)) != 0)
     return fail(nullptr, DF_MOE_EINVAL, "unknown flags");
-  if (c.flags & DF_MOE_MXFP8_ACT) {
-    if (slots)
-      return fail(nullptr, DF_MOE_EINVAL, "DF_MOE_MXFP8_ACT does not combine with an expert cache");
+  if (c.flags & (DF_MOE_MXFP8_ACT | DF_MOE_PLANES)) {
+    const char* f = (c.flags & DF_MOE_MXFP8_ACT) ? "DF_MOE_MXFP8_ACT" : "DF_MOE_PLANES";
+    if ((c.flags & DF_MOE_MXFP8_ACT) && (c.flags & DF_MOE_PLANES))
+      return fail(nullptr, DF_MOE_EINVAL, "DF_MOE_MXFP8_ACT and DF_MOE_PLANES exclude each other");
+    if (slots) return fail(nullptr, DF_MOE_EINVAL, "%s does not combine with an expert cache", f);
     if (c.flags & DF_MOE_PREFILL_MMA_SYNC)
-      return fail(nullptr, DF_MOE_EINVAL,
-                  "DF_MOE_MXFP8_ACT does not combine with DF_MOE_PREFILL_MMA_SYNC");
+      return fail(nullptr, DF_MOE_EINVAL, "%s does not combine with DF_MOE_PREFILL_MMA_SYNC", f);
     if (!mx8_supported(c.hidden, c.inter))
       return fail(nullptr, DF_MOE_EINVAL,
-                  "DF_MOE_MXFP8_ACT needs hidden and inter multiples of 128 (hidden >= 128)");
+                  "%s needs hidden and inter multiples of 128 (hidden >= 128)", f);
   }
   if ((c.flags & DF_MOE_STACK_RMSNORM_RESIDUAL) && !(c.rms_eps >= 0.0f))
     return fail(nullptr, DF_MOE_EINVAL, "rms_eps must be >= 0");
@@ -653,24 +660,29 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
     if (!rc && R) rc = dalloc(h, &L.sh_down, H * R);
   }
   // tcgen05 GEMMs: batches above the decode range, unless asked otherwise
-  h->mx8 = (c.flags & DF_MOE_MXFP8_ACT) != 0;
+  h->mx8 = (c.flags & (DF_MOE_MXFP8_ACT | DF_MOE_PLANES)) != 0;
+  if (c.flags & DF_MOE_PLANES) {
+    h->px = kPlanesX;
+    h->ph = kPlanesH;
+  }
   h->gemm = !slots && !h->mx8 && Tm > (size_t)kDecodeMaxT &&
             !(c.flags & DF_MOE_PREFILL_MMA_SYNC) && gemm_supported(c.hidden, c.inter);
   if (h->mx8) {
-    h->mx_rows = mx8_rows_cap((int)(Tm * k), (int)std::min(Tm * k, E));
-    const size_t rows = (size_t)h->mx_rows;
+    h->mx_xrows = mx8_rows_cap((int)(Tm * k), h->px);
+    h->mx_hrows = mx8_rows_cap((int)(Tm * k), h->ph);
+    const size_t xrows = (size_t)h->mx_xrows, hrows = (size_t)h->mx_hrows;
     for (int l = 0; l < c.n_layers && !rc; ++l) {
       LayerBufs& L = h->layers[l];
       if (!make_mx8_maps(L.arena, h->span_bytes, c.hidden, c.inter, c.n_experts, &L.mx_gate,
                          &L.mx_up, &L.mx_down))
         rc = fail(h, DF_MOE_ECUDA, "tensor map encoding failed");
     }
-    if (!rc) rc = dalloc(h, &h->mx_xq, rows * H);
-    if (!rc) rc = dalloc(h, &h->mx_xsf, H / 128 * rows * 16);
-    if (!rc) rc = dalloc(h, &h->mx_hq, rows * I);
-    if (!rc) rc = dalloc(h, &h->mx_hsf, I / 128 * rows * 16);
-    if (!rc && (!make_mx8_row_map(h->mx_xq, h->mx_rows, c.hidden, &h->mx_xmap) ||
-                !make_mx8_row_map(h->mx_hq, h->mx_rows, c.inter, &h->mx_hmap)))
+    if (!rc) rc = dalloc(h, &h->mx_xq, xrows * H);
+    if (!rc) rc = dalloc(h, &h->mx_xsf, H / 128 * xrows * 16);
+    if (!rc) rc = dalloc(h, &h->mx_hq, hrows * I);
+    if (!rc) rc = dalloc(h, &h->mx_hsf, I / 128 * hrows * 16);
+    if (!rc && (!make_mx8_row_map(h->mx_xq, h->mx_xrows, c.hidden, &h->mx_xmap) ||
+                !make_mx8_row_map(h->mx_hq, h->mx_hrows, c.inter, &h->mx_hmap)))
       rc = fail(h, DF_MOE_ECUDA, "tensor map encoding failed");
   }
   if (h->gemm) {

@@ -279,15 +279,18 @@ cudaError_t launch_shared_gemm_gateup(const SharedMaps& m, const uint16_t* x, in
 cudaError_t launch_shared_gemm_down(const SharedMaps& m, int T, int H, int R, float* y,
                                     uint32_t* err, cudaStream_t s);
 
-// ---- routed experts with MXFP8 activations (k_mx8.cu) ----------------------
-// The lossy variant: activations rounded to MXFP8 (E4M3 elements, E8M0 per
-// 32), experts as grouped GEMMs on tcgen05.mma kind::mxf8f6f4 with the MXFP4
-// codes and scales of each 128-row tile arranged stage by stage.
+// ---- routed experts on block-scaled MXFP4 x E4M3 GEMMs (k_mx8.cu) ----------
+// Grouped GEMMs on tcgen05.mma kind::mxf8f6f4 with the MXFP4 codes and
+// scales of each 128-row tile arranged stage by stage, the activations in
+// E4M3 with an E8M0 exponent per 32: one plane (the lossy MXFP8 variant: the
+// activation rounded to the format) or several planes whose sum reproduces
+// the activation (x: kPlanesX, h: kPlanesH; the exact path for batches).
+constexpr int kPlanesX = 4, kPlanesH = 5;
 bool mx8_supported(int H, int I);
-// Rows of the expert-ordered activation buffers for nassign assignments in
-// at most max_items items (the assignments' rows and 32 more, read past the
-// last row by a stage's 32-row scale chunk).
-int mx8_rows_cap(int nassign, int max_items);
+// Rows of an expert-ordered activation buffer for nassign assignments of
+// `planes` rows each (and 32 more, read past the last row by a stage's
+// 32-row scale chunk).
+int mx8_rows_cap(int nassign, int planes);
 // Tensor maps of the gate, up and down codes of an arena of E spans.
 bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E, ChunkMap* gate,
                    ChunkMap* up, ChunkMap* down);
@@ -295,31 +298,33 @@ bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E,
 bool make_mx8_row_map(const uint8_t* rows, int rows_cap, int K, ChunkMap* map);
 // Rounds the rows of the items' assignments: row n of item i is source row
 // sorted[pos + n] / div of src (bf16 or fp32, [.][K], 16-byte aligned),
-// written to q row pos + n ([rows_cap][K]) with its scales in sf
-// ([K/128][rows_cap][16], word q of a row the scales of the row 32 q later).
-cudaError_t launch_mx8_rows(const void* src, bool bf16, int K, int div, const Item* items,
-                            const int32_t* n_items, int max_items, const int32_t* sorted,
-                            int nassign, int E, uint8_t* q, uint8_t* sf, int rows_cap,
-                            uint32_t* err, cudaStream_t s);
+// written as `planes` E4M3 rows (pos + n) planes + p of q ([rows_cap][K])
+// with their scales in sf ([K/128][rows_cap][16], word q of a row the scales
+// of the row 32 q later). planes: 1, kPlanesX (bf16) or kPlanesH (fp32).
+cudaError_t launch_mx8_rows(const void* src, bool bf16, int K, int div, int planes,
+                            const Item* items, const int32_t* n_items, int max_items,
+                            const int32_t* sorted, int nassign, int E, uint8_t* q, uint8_t* sf,
+                            int rows_cap, uint32_t* err, cudaStream_t s);
 // The rounding on plain rows: codes [rows][n], scales [rows][n/32].
 cudaError_t launch_mx8_plain(const float* v, int rows, int n, uint8_t* codes, uint8_t* scales,
                              cudaStream_t s);
 // Canonical spans -> the variant's span layout (inverse: back).
 cudaError_t launch_mx8_layout(const uint8_t* src, uint8_t* dst, int n_spans, int H, int I,
                               size_t span_bytes, int inverse, cudaStream_t s);
-// gate/up: h rounded to MXFP8 into hq/hsf (and, optionally, h before the
-// rounding into hbuf [nassign][I]).
+// gate/up on x's planes (1 or kPlanesX). One plane: h rounded to MXFP8
+// into hq/hsf (and, optionally, h before the rounding into hbuf
+// [nassign][I]); planes: h into hbuf.
 cudaError_t launch_mx8_gateup(const ChunkMap& gate, const ChunkMap& up, const ChunkMap& xmap,
                               const uint8_t* arena, size_t span_bytes, int H, int I,
                               const uint8_t* xsf, int rows_cap, const Item* items,
                               const int32_t* n_items, int max_items, const int32_t* sorted,
                               int E, int nassign, float* hbuf, uint8_t* hq, uint8_t* hsf,
-                              uint32_t* err, cudaStream_t s);
-// down: part [nassign][H].
+                              int planes, uint32_t* err, cudaStream_t s);
+// down on h's planes (1 or kPlanesH): part [nassign][H].
 cudaError_t launch_mx8_down(const ChunkMap& down, const ChunkMap& hmap, const uint8_t* arena,
                             size_t span_bytes, int H, int I, const uint8_t* hsf, int rows_cap,
                             const Item* items, const int32_t* n_items, int max_items,
                             const int32_t* sorted, int E, int nassign, float* part,
-                            uint32_t* err, cudaStream_t s);
+                            int planes, uint32_t* err, cudaStream_t s);
 
 }  // namespace dfm

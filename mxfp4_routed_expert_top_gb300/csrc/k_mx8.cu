@@ -51,6 +51,7 @@
 // copies and MMAs in flight land, and the CTA frees its tensor memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 
@@ -114,7 +115,8 @@ constexpr bool geo_ok() {
          G::sfCol + G::sfStride * G::S <= kTmemCols && G::offB % 1024 == 0 &&
          G::BBytes % 1024 == 0;
 }
-static_assert(geo_ok<0, 32>() && geo_ok<0, 64>() && geo_ok<1, 32>() && geo_ok<1, 64>(),
+static_assert(geo_ok<0, 32>() && geo_ok<0, 64>() && geo_ok<1, 32>() && geo_ok<1, 64>() &&
+                  geo_ok<1, 80>(),
               "shared or tensor memory");
 
 struct Mx8Args {
@@ -272,6 +274,7 @@ struct Unit {
   bool ok;
   int e, mt, pos, cnt;
 };
+template <int P>
 __device__ __forceinline__ Unit unit_at(const Mx8Args& a, int u) {
   Unit w;
   const int item = u / a.MT;
@@ -281,7 +284,7 @@ __device__ __forceinline__ Unit unit_at(const Mx8Args& a, int u) {
   w.pos = it.pos;
   w.cnt = it.cnt;
   w.ok = (unsigned)it.e < (unsigned)a.E && it.cnt >= 1 && it.pos >= 0 &&
-         it.pos + it.cnt <= a.nassign && it.pos + it.cnt + 32 <= a.rows_cap;
+         it.pos + it.cnt <= a.nassign && (it.pos + it.cnt) * P + 32 <= a.rows_cap;
   return w;
 }
 
@@ -289,7 +292,7 @@ __device__ __forceinline__ Unit unit_at(const Mx8Args& a, int u) {
 // roles
 // ---------------------------------------------------------------------------
 
-template <int MODE, int KN>
+template <int MODE, int KN, int P>
 __device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE, KN>::S, Geo<MODE, KN>::NACC>* b) {
   using G = Geo<MODE, KN>;
   const int nks = a.K / kKS;
@@ -298,13 +301,13 @@ __device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<
   bool ok = true;
   const uint64_t pol = l2_evict_first_policy();
   for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-    const Unit w = unit_at(a, u);
+    const Unit w = unit_at<P>(a, u);
     if (!w.ok) continue;
     const uint8_t* span = a.arena + (size_t)w.e * a.span_bytes;
-    for (int tb = 0; tb < w.cnt && ok; tb += KN) {
-      const int nv = min(KN, w.cnt - tb);
-      const int nb = (nv + kBoxRows - 1) / kBoxRows;
-      const int row = w.pos + tb;
+    for (int tb = 0; tb < w.cnt && ok; tb += KN / P) {
+      const int nr = min(KN / P, w.cnt - tb) * P;  // B rows of the pass (tokens x planes)
+      const int nb = (nr + kBoxRows - 1) / kBoxRows;
+      const int row = (w.pos + tb) * P;
       for (int ks = 0; ks < nks; ++ks, ++g) {
         const uint32_t s = g % G::S, ph = (g / G::S) & 1u;
         if (!wait_or_give_up(&b->empty[s], ph ^ 1u, &b->err)) { ok = false; break; }
@@ -335,7 +338,7 @@ __device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<
     if (armed >> s & 1u) drain(&b->full[s], last_par >> s & 1u);
 }
 
-template <int MODE, int KN>
+template <int MODE, int KN, int P>
 __device__ void role_mma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE, KN>::S, Geo<MODE, KN>::NACC>* b,
                          uint32_t tmem) {
   using G = Geo<MODE, KN>;
@@ -343,11 +346,10 @@ __device__ void role_mma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<
   uint32_t g = 0, pc = 0;
   bool ok = true;
   for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-    const Unit w = unit_at(a, u);
+    const Unit w = unit_at<P>(a, u);
     if (!w.ok) continue;
-    for (int tb = 0; tb < w.cnt && ok; tb += KN, ++pc) {
-      const int nv = min(KN, w.cnt - tb);
-      const int N = (nv + 15) & ~15;
+    for (int tb = 0; tb < w.cnt && ok; tb += KN / P, ++pc) {
+      const int N = (min(KN / P, w.cnt - tb) * P + 15) & ~15;
       const uint32_t acc = pc % G::NACC;
       if (!wait_or_give_up(&b->acce[acc], ((pc / G::NACC) & 1u) ^ 1u, &b->err)) { ok = false; break; }
       tc_fence_after();
@@ -396,60 +398,122 @@ __device__ __forceinline__ void tmem_ld32(uint32_t addr, uint32_t (&v)[32]) {
       : "r"(addr));
 }
 
-template <int MODE, int KN>
+__device__ __forceinline__ void tmem_ld16(uint32_t addr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(addr));
+}
+
+// KN consecutive accumulator columns of this warp's lanes (x32 loads, then
+// an x16 for a remainder of 16); the caller waits.
+template <int KN>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t addr, uint32_t (&v)[KN]) {
+#pragma unroll
+  for (int c = 0; c + 32 <= KN; c += 32)
+    tmem_ld32(addr + c, *reinterpret_cast<uint32_t(*)[32]>(v + c));
+  if constexpr (KN % 32 == 16) tmem_ld16(addr + KN - 16, v + KN - 16);
+}
+
+template <int MODE, int KN, int P>
 __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN>::S, Geo<MODE, KN>::NACC>* b,
                               uint32_t tmem, int warp, int lane) {
   using G = Geo<MODE, KN>;
+  constexpr int TPP = KN / P;  // tokens a pass
   const int L = 32 * warp + lane;
   const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
   uint32_t pc = 0;
   bool ok = true;
   for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-    const Unit w = unit_at(a, u);
+    const Unit w = unit_at<P>(a, u);
     if (!w.ok) {
       if (L == 0) atomicOr(a.err, DEV_ERR_RANGE);
       continue;
     }
     const int r = kM * w.mt + L;  // this thread's row (h row or output row)
-    for (int tb = 0; tb < w.cnt && ok; tb += KN, ++pc) {
-      const int nv = min(KN, w.cnt - tb);
+    for (int tb = 0; tb < w.cnt && ok; tb += TPP, ++pc) {
+      const int nv = min(TPP, w.cnt - tb);
       const uint32_t acc = pc % G::NACC;
       if (!warp_wait(&b->accf[acc], (pc / G::NACC) & 1u, &b->err)) { ok = false; break; }
       tc_fence_after();
-      for (int c0 = 0; c0 < nv; c0 += 32) {
-        const int nc = min(32, nv - c0);
-        // the chunk's assignment indices, one a lane, fetched together
-        const int my_a = lane < nc ? a.sorted[w.pos + tb + c0 + lane] : -1;
-        uint32_t v[32];
-        tmem_ld32(lane_addr + acc * G::accCols + c0, v);
-        if (MODE == 1) {
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      if constexpr (P == 1) {
+        for (int c0 = 0; c0 < nv; c0 += 32) {
+          const int nc = min(32, nv - c0);
+          // the chunk's assignment indices, one a lane, fetched together
+          const int my_a = lane < nc ? a.sorted[w.pos + tb + c0 + lane] : -1;
+          uint32_t v[32];
+          tmem_ld32(lane_addr + acc * G::accCols + c0, v);
+          if (MODE == 1) {
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-          for (int n = 0; n < 32; ++n) {
-            if (n >= nc) break;
-            const int aa = __shfl_sync(0xffffffffu, my_a, n);
-            if ((unsigned)aa < (unsigned)a.nassign)
-              a.part[(size_t)aa * a.H + r] = __uint_as_float(v[n]);
-            else if (lane == 0)
-              atomicOr(a.err, DEV_ERR_RANGE);
+            for (int n = 0; n < 32; ++n) {
+              if (n >= nc) break;
+              const int aa = __shfl_sync(0xffffffffu, my_a, n);
+              if ((unsigned)aa < (unsigned)a.nassign)
+                a.part[(size_t)aa * a.H + r] = __uint_as_float(v[n]);
+              else if (lane == 0)
+                atomicOr(a.err, DEV_ERR_RANGE);
+            }
+          } else {
+            uint32_t vu[32];
+            tmem_ld32(lane_addr + acc * G::accCols + KN + c0, vu);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            const int blk = 4 * w.mt + warp;  // MXFP8 block of h along I
+#pragma unroll
+            for (int n = 0; n < 32; ++n) {
+              if (n >= nc) break;
+              const float gt = __uint_as_float(v[n]);
+              const float hv = gt / (1.f + expf(-gt)) * __uint_as_float(vu[n]);
+              const int aa = __shfl_sync(0xffffffffu, my_a, n);
+              if (a.hbuf && (unsigned)aa < (unsigned)a.nassign)
+                a.hbuf[(size_t)aa * a.I + r] = hv;
+              const int sh = mx8_shared_exp(warp_max(fabsf(hv)));
+              const int row = w.pos + tb + c0 + n;
+              a.hq[(size_t)row * a.I + r] = (uint8_t)e4m3_rn_sat(hv * pow2f(-sh));
+              if (lane == 0) put_scale(a.hsf, a.rows_cap, row, blk, (uint8_t)(sh + 127));
+            }
           }
-        } else {
-          uint32_t vu[32];
-          tmem_ld32(lane_addr + acc * G::accCols + KN + c0, vu);
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          const int blk = 4 * w.mt + warp;  // MXFP8 block of h along I
+        }
+      } else {
+        // planes: token n's value is the sum of its P columns, in plane order
+        static_assert(KN % 16 == 0 && KN <= 96 && TPP <= 32, "plane pass columns");
+        const int my_a = lane < nv ? a.sorted[w.pos + tb + lane] : -1;
+        uint32_t v[KN];
+        float gs[TPP];
+        tmem_ld_cols<KN>(lane_addr + acc * G::accCols, v);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-          for (int n = 0; n < 32; ++n) {
-            if (n >= nc) break;
-            const float gt = __uint_as_float(v[n]);
-            const float hv = gt / (1.f + expf(-gt)) * __uint_as_float(vu[n]);
-            const int aa = __shfl_sync(0xffffffffu, my_a, n);
-            if (a.hbuf && (unsigned)aa < (unsigned)a.nassign)
-              a.hbuf[(size_t)aa * a.I + r] = hv;
-            const int sh = mx8_shared_exp(warp_max(fabsf(hv)));
-            const int row = w.pos + tb + c0 + n;
-            a.hq[(size_t)row * a.I + r] = (uint8_t)e4m3_rn_sat(hv * pow2f(-sh));
-            if (lane == 0) put_scale(a.hsf, a.rows_cap, row, blk, (uint8_t)(sh + 127));
+        for (int n = 0; n < TPP; ++n) {
+          float t = __uint_as_float(v[n * P]);
+#pragma unroll
+          for (int q = 1; q < P; ++q) t += __uint_as_float(v[n * P + q]);
+          gs[n] = t;
+        }
+        if (MODE == 0) {
+          tmem_ld_cols<KN>(lane_addr + acc * G::accCols + KN, v);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        }
+#pragma unroll
+        for (int n = 0; n < TPP; ++n) {
+          if (n >= nv) break;
+          float y = gs[n];
+          if (MODE == 0) {
+            float up = __uint_as_float(v[n * P]);
+#pragma unroll
+            for (int q = 1; q < P; ++q) up += __uint_as_float(v[n * P + q]);
+            y = y / (1.f + expf(-y)) * up;  // h = silu(gate) * up
+          }
+          const int aa = __shfl_sync(0xffffffffu, my_a, n);
+          if ((unsigned)aa < (unsigned)a.nassign) {
+            if (MODE == 0)
+              a.hbuf[(size_t)aa * a.I + r] = y;
+            else
+              a.part[(size_t)aa * a.H + r] = y;
+          } else if (lane == 0) {
+            atomicOr(a.err, DEV_ERR_RANGE);
           }
         }
       }
@@ -460,7 +524,7 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN>:
   }
 }
 
-template <int MODE, int KN>
+template <int MODE, int KN, int P>
 __global__ void __launch_bounds__(kThr, 1) mx8_gemm_kernel(const __grid_constant__ Mx8Args a) {
   using G = Geo<MODE, KN>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -497,11 +561,11 @@ __global__ void __launch_bounds__(kThr, 1) mx8_gemm_kernel(const __grid_constant
   }
   const int n_units = n_items * a.MT;
   if (warp < 4) {
-    role_epilogue<MODE, KN>(a, n_units, b, tmem, warp, lane);
+    role_epilogue<MODE, KN, P>(a, n_units, b, tmem, warp, lane);
   } else if (warp == kTmaWarp) {
-    if (lane == 0) role_tma<MODE, KN>(a, n_units, smem, b);
+    if (lane == 0) role_tma<MODE, KN, P>(a, n_units, smem, b);
   } else if (warp == kMmaWarp && lane == 0) {
-    role_mma<MODE, KN>(a, n_units, smem, b, tmem);
+    role_mma<MODE, KN, P>(a, n_units, smem, b, tmem);
   }
   tc_fence_before();
   __syncthreads();
@@ -513,11 +577,22 @@ __global__ void __launch_bounds__(kThr, 1) mx8_gemm_kernel(const __grid_constant
                  : "memory");
 }
 
+// E4M3 code -> its value (exact).
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)(code | code << 8)));
+  return __half2float(__ushort_as_half((uint16_t)(h2 & 0xFFFFu)));
+}
+
 // Rounds activation rows to MXFP8 into the expert-ordered buffers: block =
 // item, thread j = 32-column block j of each of the item's rows. Row n of
 // item i is source row sorted[pos + n] / div (x: the token; h: the
-// assignment), written to q row pos + n.
-template <bool BF16>
+// assignment). P = 1: the row rounded to MXFP8, written to q row pos + n.
+// P > 1: the row as P planes, q rows (pos + n) P + p: plane p is the MXFP8
+// rounding of what the planes before it left (each plane with its own block
+// exponent), the remainder exact in fp32 at every step, so the planes' sum
+// reproduces the row up to the last remainder.
+template <bool BF16, int P>
 __global__ void __launch_bounds__(256) mx8_rows_kernel(const void* src, int K, int div,
                                                        const Item* items, const int32_t* n_items,
                                                        int max_items, const int32_t* sorted,
@@ -528,9 +603,8 @@ __global__ void __launch_bounds__(256) mx8_rows_kernel(const void* src, int K, i
   if (ni > max_items) ni = max_items;
   if (i >= ni) return;
   const Item it = items[i];
-  const int base = it.pos;
   if ((unsigned)it.e >= (unsigned)E || it.cnt < 1 || it.pos < 0 || it.pos + it.cnt > nassign ||
-      base + it.cnt > rows_cap) {
+      (it.pos + it.cnt) * P + 32 > rows_cap) {
     if (threadIdx.x == 0) atomicOr(err, DEV_ERR_RANGE);
     return;
   }
@@ -569,20 +643,32 @@ __global__ void __launch_bounds__(256) mx8_rows_kernel(const void* src, int K, i
           v[4 * c + 3] = t.w;
         }
       }
-      float amax = 0.f;
+#pragma unroll 1
+      for (int pl = 0; pl < P; ++pl) {
+        float amax = 0.f;
 #pragma unroll
-      for (int m = 0; m < 32; ++m) amax = fmaxf(amax, fabsf(v[m]));
-      const int sh = mx8_shared_exp(amax);
-      const float sc = pow2f(-sh);
-      uint32_t wq[8];
+        for (int m = 0; m < 32; ++m) amax = fmaxf(amax, fabsf(v[m]));
+        const int sh = mx8_shared_exp(amax);
+        const float sc = pow2f(-sh), back = pow2f(sh);
+        uint32_t wq[8];
 #pragma unroll
-      for (int m = 0; m < 8; ++m)
-        wq[m] = e4m3_rn_sat(v[4 * m] * sc) | e4m3_rn_sat(v[4 * m + 1] * sc) << 8 |
-                e4m3_rn_sat(v[4 * m + 2] * sc) << 16 | e4m3_rn_sat(v[4 * m + 3] * sc) << 24;
-      uint4* d = reinterpret_cast<uint4*>(q + (size_t)(base + n) * K + 32 * j);
-      d[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-      d[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
-      put_scale(sf, rows_cap, base + n, j, (uint8_t)(sh + 127));
+        for (int m = 0; m < 8; ++m) {
+          uint32_t word = 0;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t code = e4m3_rn_sat(v[4 * m + c] * sc);
+            word |= code << (8 * c);
+            // the remainder for the next plane (exact: v minus its rounding)
+            if (P > 1) v[4 * m + c] -= e4m3_value(code) * back;
+          }
+          wq[m] = word;
+        }
+        const int row = (it.pos + n) * P + pl;
+        uint4* d = reinterpret_cast<uint4*>(q + (size_t)row * K + 32 * j);
+        d[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+        d[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
+        put_scale(sf, rows_cap, row, j, (uint8_t)(sh + 127));
+      }
     }
   }
 }
@@ -670,12 +756,12 @@ int sms_mx8() {
   return n;
 }
 
-template <int MODE, int KN>
+template <int MODE, int KN, int P>
 cudaError_t launch_mx8_kn(const Mx8Args& a, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
     const cudaError_t e =
-        cudaFuncSetAttribute(mx8_gemm_kernel<MODE, KN>,
+        cudaFuncSetAttribute(mx8_gemm_kernel<MODE, KN, P>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem_bytes<MODE, KN>());
     if (e != cudaSuccess) return e;
@@ -684,26 +770,32 @@ cudaError_t launch_mx8_kn(const Mx8Args& a, cudaStream_t s) {
   const long long units = (long long)a.max_items * a.MT;
   int grid = sms_mx8();
   if (units < grid) grid = (int)(units > 0 ? units : 1);
-  mx8_gemm_kernel<MODE, KN><<<grid, kThr, smem_bytes<MODE, KN>(), s>>>(a);
+  mx8_gemm_kernel<MODE, KN, P><<<grid, kThr, smem_bytes<MODE, KN>(), s>>>(a);
   return cudaGetLastError();
 }
 
-// The token tile: 32 when the items average up to 24 tokens (a smaller B
-// slot leaves room for more stages, i.e. more weight bytes in flight), else
-// 64 (fewer passes over each expert's weights).
+// MXFP8 (planes = 1): the token tile is 32 when the items average up to 24
+// tokens (a smaller B slot leaves room for more stages, i.e. more weight
+// bytes in flight), else 64 (fewer passes over each expert's weights).
+// Planes: 16 tokens a pass (64 B rows of x's 4 planes, 80 of h's 5).
 template <int MODE>
-cudaError_t launch_mx8(const Mx8Args& a, cudaStream_t s) {
-  return a.nassign <= 24LL * a.max_items ? launch_mx8_kn<MODE, 32>(a, s)
-                                         : launch_mx8_kn<MODE, 64>(a, s);
+cudaError_t launch_mx8(const Mx8Args& a, int planes, cudaStream_t s) {
+  if (planes > 1) {
+    constexpr int P = MODE == 0 ? kPlanesX : kPlanesH;
+    if (planes != P) return cudaErrorInvalidValue;
+    return launch_mx8_kn<MODE, 16 * P, P>(a, s);
+  }
+  return a.nassign <= 24LL * a.max_items ? launch_mx8_kn<MODE, 32, 1>(a, s)
+                                         : launch_mx8_kn<MODE, 64, 1>(a, s);
 }
 
 }  // namespace
 
 bool mx8_supported(int H, int I) { return H % kKS == 0 && I % kKS == 0 && H >= kM; }
 
-int mx8_rows_cap(int nassign, int max_items) {
-  (void)max_items;
-  return nassign + 32;  // a stage's token scales are read as 32 rows from the pass's first
+int mx8_rows_cap(int nassign, int planes) {
+  // a stage's token scales are read as 32 rows from the pass's first
+  return nassign * planes + 32;
 }
 
 bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E, ChunkMap* gate,
@@ -744,18 +836,20 @@ bool make_mx8_row_map(const uint8_t* rows_buf, int rows_cap, int K, ChunkMap* ma
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_mx8_rows(const void* src, bool bf16, int K, int div, const Item* items,
-                            const int32_t* n_items, int max_items, const int32_t* sorted,
-                            int nassign, int E, uint8_t* q, uint8_t* sf, int rows_cap,
-                            uint32_t* err, cudaStream_t s) {
+cudaError_t launch_mx8_rows(const void* src, bool bf16, int K, int div, int planes,
+                            const Item* items, const int32_t* n_items, int max_items,
+                            const int32_t* sorted, int nassign, int E, uint8_t* q, uint8_t* sf,
+                            int rows_cap, uint32_t* err, cudaStream_t s) {
   if (max_items <= 0) return cudaSuccess;
-  if (bf16)
-    mx8_rows_kernel<true><<<max_items, 256, 0, s>>>(src, K, div, items, n_items, max_items, sorted,
-                                                    nassign, E, q, sf, rows_cap, err);
-  else
-    mx8_rows_kernel<false><<<max_items, 256, 0, s>>>(src, K, div, items, n_items, max_items,
-                                                     sorted, nassign, E, q, sf, rows_cap, err);
-  return cudaGetLastError();
+  auto go = [&](auto kernel) {
+    kernel<<<max_items, 256, 0, s>>>(src, K, div, items, n_items, max_items, sorted, nassign, E,
+                                     q, sf, rows_cap, err);
+    return cudaGetLastError();
+  };
+  if (planes == 1) return bf16 ? go(mx8_rows_kernel<true, 1>) : go(mx8_rows_kernel<false, 1>);
+  if (planes == kPlanesX && bf16) return go(mx8_rows_kernel<true, kPlanesX>);
+  if (planes == kPlanesH && !bf16) return go(mx8_rows_kernel<false, kPlanesH>);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_mx8_plain(const float* v, int rows, int n, uint8_t* codes, uint8_t* scales,
@@ -780,7 +874,8 @@ cudaError_t launch_mx8_gateup(const ChunkMap& gate, const ChunkMap& up, const Ch
                               const uint8_t* xsf, int rows_cap, const Item* items,
                               const int32_t* n_items, int max_items, const int32_t* sorted,
                               int E, int nassign, float* hbuf, uint8_t* hq, uint8_t* hsf,
-                              uint32_t* err, cudaStream_t s) {
+                              int planes, uint32_t* err, cudaStream_t s) {
+  if (planes > 1 && !hbuf) return cudaErrorInvalidValue;  // planes: h goes to hbuf
   const size_t q = (size_t)H * I / 2, sb = (size_t)H * I / 32;
   Mx8Args a{};
   a.amap0 = gate;
@@ -806,14 +901,14 @@ cudaError_t launch_mx8_gateup(const ChunkMap& gate, const ChunkMap& up, const Ch
   a.hq = hq;
   a.hsf = hsf;
   a.err = err;
-  return launch_mx8<0>(a, s);
+  return launch_mx8<0>(a, planes, s);
 }
 
 cudaError_t launch_mx8_down(const ChunkMap& down, const ChunkMap& hmap, const uint8_t* arena,
                             size_t span_bytes, int H, int I, const uint8_t* hsf, int rows_cap,
                             const Item* items, const int32_t* n_items, int max_items,
                             const int32_t* sorted, int E, int nassign, float* part,
-                            uint32_t* err, cudaStream_t s) {
+                            int planes, uint32_t* err, cudaStream_t s) {
   const size_t q = (size_t)H * I / 2, sb = (size_t)H * I / 32;
   Mx8Args a{};
   a.amap0 = down;
@@ -837,7 +932,7 @@ cudaError_t launch_mx8_down(const ChunkMap& down, const ChunkMap& hmap, const ui
   a.nassign = nassign;
   a.part = part;
   a.err = err;
-  return launch_mx8<1>(a, s);
+  return launch_mx8<1>(a, planes, s);
 }
 
 }  // namespace dfm

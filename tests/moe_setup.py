@@ -42,13 +42,14 @@ class Setup:
     host)."""
 
     def __init__(self, wl, max_tokens=None, chunk=64, mma_sync_prefill=False,
-                 cache_slots=0, mxfp8=False):
+                 cache_slots=0, mxfp8=False, planes=False):
         import mxfp4_routed_expert_top_gb300 as dfm
         torch = torch_mod()
         self.wl = wl
         flags = ((dfm.STACK_RMSNORM_RESIDUAL if wl.stack else 0)
                  | (dfm.PREFILL_MMA_SYNC if mma_sync_prefill else 0)
-                 | (dfm.MXFP8_ACT if mxfp8 else 0))
+                 | (dfm.MXFP8_ACT if mxfp8 else 0)
+                 | (dfm.PLANES if planes else 0))
         self.m = dfm.MoE(wl.H, wl.E, wl.k, wl.I, wl.n_shared, wl.Is,
                          n_layers=wl.L, max_tokens=max_tokens or wl.T,
                          rms_eps=wl.eps, flags=flags, cache_slots=cache_slots)

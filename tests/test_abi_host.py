@@ -49,9 +49,11 @@ def test_create_rejects_bad_config(dfm):
                 shared_inter=64, max_tokens=1)
     bad = [dict(hidden=255), dict(inter=48), dict(top_k=9), dict(top_k=0),
            dict(n_experts=2000), dict(max_tokens=0), dict(n_shared=9),
-           dict(flags=16),                                   # unknown flag
+           dict(flags=32),                                   # unknown flag
            dict(flags=dfm.MXFP8_ACT),                        # inter 64: not a multiple of 128
-           dict(flags=dfm.MXFP8_ACT | dfm.PREFILL_MMA_SYNC, inter=128)]
+           dict(flags=dfm.MXFP8_ACT | dfm.PREFILL_MMA_SYNC, inter=128),
+           dict(flags=dfm.MXFP8_ACT | dfm.PLANES, inter=128),
+           dict(flags=dfm.PLANES)]                           # inter 64 again
     for b in bad:
         cfg = dict(base, **b)
         with pytest.raises(dfm.DfMoeError) as ei:
