@@ -50,6 +50,68 @@ combine_kernel(const float* __restrict__ part, const float* __restrict__ w, int 
   if (out_bf16) out_bf16[(size_t)t * H + j] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
 }
 
+// The same for batches: each thread takes four consecutive columns with
+// 16-byte loads and stores (H a multiple of 4, rows 16-byte aligned); the
+// sums run in the same slot order.
+__global__ void __launch_bounds__(kCombineThreads)
+combine4_kernel(const float* __restrict__ part, const float* __restrict__ w, int k, int H,
+                const float* __restrict__ ysh, const uint16_t* __restrict__ residual,
+                float* __restrict__ out_f32, uint16_t* __restrict__ out_bf16, uint32_t* err,
+                uint32_t* err_mirror) {
+  pdl_wait();
+  if (blockIdx.x == 0 && blockIdx.y == 0 && err_mirror && threadIdx.x == 0) {
+    const uint32_t e = atomicOr(err, 0u);
+    if (e) *reinterpret_cast<volatile uint32_t*>(err_mirror) = e;
+  }
+  const int t = blockIdx.y;
+  const int j = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (j >= H) return;
+  // slots in groups of eight: a group's loads are issued together, the sums
+  // run in slot order
+  float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i0 = 0; i0 < k; i0 += 8) {
+    float4 pv[8];
+    float wv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i0 + i < k) {
+        pv[i] = *reinterpret_cast<const float4*>(part + ((size_t)t * k + i0 + i) * H + j);
+        wv[i] = w[(size_t)t * k + i0 + i];
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (i0 + i < k) {
+        y.x = fmaf(wv[i], pv[i].x, y.x);
+        y.y = fmaf(wv[i], pv[i].y, y.y);
+        y.z = fmaf(wv[i], pv[i].z, y.z);
+        y.w = fmaf(wv[i], pv[i].w, y.w);
+      }
+  }
+  if (ysh) {
+    const float4 s = *reinterpret_cast<const float4*>(ysh + (size_t)t * H + j);
+    y.x += s.x;
+    y.y += s.y;
+    y.z += s.z;
+    y.w += s.w;
+  }
+  if (residual) {
+    const uint2 r = *reinterpret_cast<const uint2*>(residual + (size_t)t * H + j);
+    y.x += __uint_as_float(r.x << 16);
+    y.y += __uint_as_float(r.x & 0xFFFF0000u);
+    y.z += __uint_as_float(r.y << 16);
+    y.w += __uint_as_float(r.y & 0xFFFF0000u);
+  }
+  if (out_f32) *reinterpret_cast<float4*>(out_f32 + (size_t)t * H + j) = y;
+  if (out_bf16) {
+    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(y.x)) |
+                        (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.y)) << 16;
+    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(y.z)) |
+                        (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.w)) << 16;
+    *reinterpret_cast<uint2*>(out_bf16 + (size_t)t * H + j) = make_uint2(lo, hi);
+  }
+}
+
 int num_sms() {
   static int n = 0;
   if (!n) {
@@ -117,6 +179,14 @@ cudaError_t launch_combine(const float* part, const float* w, int T, int k,
                            int H, const float* ysh, const uint16_t* residual,
                            float* out_f32, uint16_t* out_bf16, uint32_t* err,
                            uint32_t* err_mirror, cudaStream_t s) {
+  const auto al16 = [](const void* p) { return ((uintptr_t)p & 15) == 0; };
+  if (T > 8 && H % 4 == 0 && al16(part) && (!ysh || al16(ysh)) && (!out_f32 || al16(out_f32)) &&
+      (!residual || ((uintptr_t)residual & 7) == 0) && (!out_bf16 || ((uintptr_t)out_bf16 & 7) == 0)) {
+    // batches: four columns a thread
+    dim3 grid((H / 4 + kCombineThreads - 1) / kCombineThreads, T);
+    return launch_after_previous(combine4_kernel, grid, dim3(kCombineThreads), 0, s, part, w, k,
+                                 H, ysh, residual, out_f32, out_bf16, err, err_mirror);
+  }
   dim3 grid((H + kCombineThreads - 1) / kCombineThreads, T);
   return launch_after_previous(combine_kernel, grid, dim3(kCombineThreads), 0, s, part, w, k, H, ysh,
                                residual, out_f32, out_bf16, err, err_mirror);

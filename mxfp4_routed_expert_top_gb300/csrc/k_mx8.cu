@@ -608,17 +608,26 @@ __global__ void __launch_bounds__(256) mx8_rows_kernel(const void* src, int K, i
     if (threadIdx.x == 0) atomicOr(err, DEV_ERR_RANGE);
     return;
   }
-  const int nblk = K / 32;
-  for (int n = 0; n < it.cnt; ++n) {
+  const int nblk = K / 32;  // a multiple of 4: the four blocks of a stage sit in 4 lanes
+  const int lane = threadIdx.x & 31;
+  // the item's (row, block) pairs, spread over the block's threads; every
+  // lane of a warp runs the same iterations (the scale words are gathered
+  // across lanes), lanes past the last pair only shuffle
+  const int total = it.cnt * nblk;
+  for (int t0 = threadIdx.x - lane; t0 < total; t0 += blockDim.x) {
+    const int t = t0 + lane;
+    const int n = (t < total ? t : 0) / nblk, j = (t < total ? t : 0) - n * nblk;
     const int aa = sorted[it.pos + n];
-    if ((unsigned)aa >= (unsigned)nassign) {
-      if (threadIdx.x == 0) atomicOr(err, DEV_ERR_RANGE);
-      continue;
-    }
-    const int srow = aa / div;
-    for (int j = threadIdx.x; j < nblk; j += blockDim.x) {
+    const bool bad = (unsigned)aa >= (unsigned)nassign;
+    if (bad && t < total && j == 0) atomicOr(err, DEV_ERR_RANGE);
+    const bool live = t < total && !bad;
+    const int srow = live ? aa / div : 0;
+    {
       float v[32];
-      if (BF16) {
+      if (!live) {
+#pragma unroll
+        for (int m = 0; m < 32; ++m) v[m] = 0.f;
+      } else if (BF16) {
         const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) +
                                                         (size_t)srow * K + 32 * j);
 #pragma unroll
@@ -664,10 +673,25 @@ __global__ void __launch_bounds__(256) mx8_rows_kernel(const void* src, int K, i
           wq[m] = word;
         }
         const int row = (it.pos + n) * P + pl;
-        uint4* d = reinterpret_cast<uint4*>(q + (size_t)row * K + 32 * j);
-        d[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-        d[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
-        put_scale(sf, rows_cap, row, j, (uint8_t)(sh + 127));
+        if (live) {
+          uint4* d = reinterpret_cast<uint4*>(q + (size_t)row * K + 32 * j);
+          d[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+          d[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
+        }
+        // the stage's four scale bytes (blocks 4 ks .. 4 ks + 3, lanes
+        // 4 g .. 4 g + 3) as one word, written by the group's first lane to
+        // its four places (word q of row - 32 q)
+        const uint32_t b0 = (uint32_t)(sh + 127);
+        const uint32_t word = b0 | __shfl_down_sync(0xffffffffu, b0, 1) << 8 |
+                              __shfl_down_sync(0xffffffffu, b0, 2) << 16 |
+                              __shfl_down_sync(0xffffffffu, b0, 3) << 24;
+        if (live && (lane & 3) == 0) {
+          const size_t ks = (size_t)(j >> 2);
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq)
+            if (row - 32 * qq >= 0)
+              reinterpret_cast<uint32_t*>(sf)[(ks * rows_cap + row - 32 * qq) * 4 + qq] = word;
+        }
       }
     }
   }
