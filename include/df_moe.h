@@ -77,8 +77,9 @@ extern "C" {
  * cores' block-scaled MXFP4 x MXFP8 MMA. Kimi K3 is trained with MXFP8
  * activations (Deltafin analysis, section 2.1); the pages' reference runs
  * keep activations exact, and so does every handle without this flag. The
- * router and the shared experts stay exact. Needs hidden and inter multiples
- * of 128; not with an expert cache or DF_MOE_PREFILL_MMA_SYNC. */
+ * router and the shared experts stay exact. Needs hidden a multiple of 256
+ * and inter a multiple of 128; not with an expert cache or
+ * DF_MOE_PREFILL_MMA_SYNC. */
 #define DF_MOE_MXFP8_ACT 8u
 /* The same block-scaled tensor-core GEMMs on exact activations: x and h
  * enter them as sums of E4M3 planes (x: 4, h: 5), each plane the MXFP8

@@ -595,7 +595,7 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
       return fail(nullptr, DF_MOE_EINVAL, "%s does not combine with DF_MOE_PREFILL_MMA_SYNC", f);
     if (!mx8_supported(c.hidden, c.inter))
       return fail(nullptr, DF_MOE_EINVAL,
-                  "%s needs hidden and inter multiples of 128 (hidden >= 128)", f);
+                  "%s needs hidden a multiple of 256 and inter a multiple of 128", f);
   }
   if ((c.flags & DF_MOE_STACK_RMSNORM_RESIDUAL) && !(c.rms_eps >= 0.0f))
     return fail(nullptr, DF_MOE_EINVAL, "rms_eps must be >= 0");

@@ -32,11 +32,11 @@
 // Activation rows: E4M3, in expert order (row p for sorted position p).
 //
 // One persistent CTA per SM, 192 threads in roles; a unit is one item x one
-// M tile of 128 rows (gate/up: 128 gate and the same 128 up rows, two MMAs a
-// K step into two accumulators, so that each thread of the epilogue holds
-// both values of its h row; down: 128 rows) x the item's tokens in passes of
-// at most 64 (the MMA's N, a multiple of 16), the contraction in stages of
-// 128 columns:
+// pair of 128-row operands (gate/up: 128 gate and the same 128 up rows, so
+// that each thread of the epilogue holds both values of its h row; down: two
+// consecutive 128-row tiles), two MMAs a K step into two accumulators, x the
+// item's tokens in passes (the MMA's N a multiple of 16), the contraction in
+// stages of 128 columns:
 //   warp 4     TMA: a stage's A operands (64-row boxes), its B rows (boxes of
 //              16 rows) and its scale chunks (bulk copies), on a ring of
 //              shared-memory stages;
@@ -79,7 +79,7 @@ constexpr uint32_t kTmemCols = 512;
 // the layout of one stage in shared memory and of the tensor memory columns.
 template <int MODE, int KN>
 struct Geo {
-  static constexpr int NA = MODE == 0 ? 2 : 1;
+  static constexpr int NA = 2;  // gate/up: gate and up; down: two 128-row tiles
   static constexpr int BBytes = KN * kKS;
   static constexpr int StageBytes = NA * kABytes + BBytes + NA * kSfBytes + kSfBytes;
   static constexpr int S0 = (226 * 1024) / StageBytes;
@@ -116,7 +116,7 @@ constexpr bool geo_ok() {
          G::BBytes % 1024 == 0;
 }
 static_assert(geo_ok<0, 32>() && geo_ok<0, 64>() && geo_ok<1, 32>() && geo_ok<1, 64>() &&
-                  geo_ok<1, 80>(),
+                  geo_ok<1, 80>() && geo_ok<0, 64>(),
               "shared or tensor memory");
 
 struct Mx8Args {
@@ -317,10 +317,11 @@ __device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<
         for (int o = 0; o < G::NA; ++o) {
           uint8_t* as = smem + G::offA + ((size_t)s * G::NA + o) * kABytes;
           const ChunkMap* m = o == 0 ? &a.amap0 : &a.amap1;
+          const int tile = MODE == 0 ? w.mt : 2 * w.mt + o;  // 128-row tile of the matrix
           for (int h = 0; h < 2; ++h)
-            tma5d_stream(as + h * (kABytes / 2), m, kHalfRows * h, ks, w.mt, w.e, full, pol);
+            tma5d_stream(as + h * (kABytes / 2), m, kHalfRows * h, ks, tile, w.e, full, pol);
           bulk_g2s(smem + G::offSfa + ((size_t)s * G::NA + o) * kSfBytes,
-                   span + (o == 0 ? a.sfa0 : a.sfa1) + ((size_t)w.mt * nks + ks) * kSfBytes,
+                   span + (o == 0 ? a.sfa0 : a.sfa1) + ((size_t)tile * nks + ks) * kSfBytes,
                    kSfBytes, full, pol);
         }
         uint8_t* bs = smem + G::offB + (size_t)s * G::BBytes;
@@ -433,7 +434,9 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN>:
       if (L == 0) atomicOr(a.err, DEV_ERR_RANGE);
       continue;
     }
-    const int r = kM * w.mt + L;  // this thread's row (h row or output row)
+    // this thread's row: the h row (gate/up), or the output rows of the
+    // unit's two tiles (down)
+    const int r = MODE == 0 ? kM * w.mt + L : 2 * kM * w.mt + L;
     for (int tb = 0; tb < w.cnt && ok; tb += TPP, ++pc) {
       const int nv = min(TPP, w.cnt - tb);
       const uint32_t acc = pc % G::NACC;
@@ -447,15 +450,19 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN>:
           uint32_t v[32];
           tmem_ld32(lane_addr + acc * G::accCols + c0, v);
           if (MODE == 1) {
+            uint32_t v1[32];
+            tmem_ld32(lane_addr + acc * G::accCols + KN + c0, v1);
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
             for (int n = 0; n < 32; ++n) {
               if (n >= nc) break;
               const int aa = __shfl_sync(0xffffffffu, my_a, n);
-              if ((unsigned)aa < (unsigned)a.nassign)
+              if ((unsigned)aa < (unsigned)a.nassign) {
                 a.part[(size_t)aa * a.H + r] = __uint_as_float(v[n]);
-              else if (lane == 0)
+                a.part[(size_t)aa * a.H + r + kM] = __uint_as_float(v1[n]);
+              } else if (lane == 0) {
                 atomicOr(a.err, DEV_ERR_RANGE);
+              }
             }
           } else {
             uint32_t vu[32];
@@ -492,26 +499,24 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN>:
           for (int q = 1; q < P; ++q) t += __uint_as_float(v[n * P + q]);
           gs[n] = t;
         }
-        if (MODE == 0) {
-          tmem_ld_cols<KN>(lane_addr + acc * G::accCols + KN, v);
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        }
+        // the second operand's columns: up (gate/up) or the second tile (down)
+        tmem_ld_cols<KN>(lane_addr + acc * G::accCols + KN, v);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
         for (int n = 0; n < TPP; ++n) {
           if (n >= nv) break;
-          float y = gs[n];
-          if (MODE == 0) {
-            float up = __uint_as_float(v[n * P]);
+          float y1 = __uint_as_float(v[n * P]);
 #pragma unroll
-            for (int q = 1; q < P; ++q) up += __uint_as_float(v[n * P + q]);
-            y = y / (1.f + expf(-y)) * up;  // h = silu(gate) * up
-          }
+          for (int q = 1; q < P; ++q) y1 += __uint_as_float(v[n * P + q]);
           const int aa = __shfl_sync(0xffffffffu, my_a, n);
           if ((unsigned)aa < (unsigned)a.nassign) {
-            if (MODE == 0)
-              a.hbuf[(size_t)aa * a.I + r] = y;
-            else
-              a.part[(size_t)aa * a.H + r] = y;
+            if (MODE == 0) {
+              const float gt = gs[n];
+              a.hbuf[(size_t)aa * a.I + r] = gt / (1.f + expf(-gt)) * y1;  // silu(gate) * up
+            } else {
+              a.part[(size_t)aa * a.H + r] = gs[n];
+              a.part[(size_t)aa * a.H + r + kM] = y1;
+            }
           } else if (lane == 0) {
             atomicOr(a.err, DEV_ERR_RANGE);
           }
@@ -815,7 +820,7 @@ cudaError_t launch_mx8(const Mx8Args& a, int planes, cudaStream_t s) {
 
 }  // namespace
 
-bool mx8_supported(int H, int I) { return H % kKS == 0 && I % kKS == 0 && H >= kM; }
+bool mx8_supported(int H, int I) { return H % (2 * kM) == 0 && I % kKS == 0; }
 
 int mx8_rows_cap(int nassign, int planes) {
   // a stage's token scales are read as 32 rows from the pass's first
@@ -943,7 +948,7 @@ cudaError_t launch_mx8_down(const ChunkMap& down, const ChunkMap& hmap, const ui
   a.sfa0 = 3 * q + 2 * sb;
   a.sfa1 = a.sfa0;
   a.K = I;
-  a.MT = H / kM;
+  a.MT = H / (2 * kM);  // units of two 128-row tiles
   a.I = I;
   a.H = H;
   a.bsf = hsf;
