@@ -73,7 +73,11 @@ def parse():
                         "experts on block-scaled MXFP4 x MXFP8 tcgen05 GEMMs")
     p.add_argument("--planes", action="store_true",
                    help="exact batches on the block-scaled MXFP4 x E4M3 tcgen05 GEMMs, "
-                        "activations as sums of E4M3 planes (DF_MOE_PLANES)")
+                        "activations as sums of E4M3 planes (DF_MOE_PLANES); the default "
+                        "for batch workloads (more than 8 tokens a step)")
+    p.add_argument("--no-planes", action="store_true",
+                   help="batches on the default handle's GEMMs (MXFP4 decoded into tensor "
+                        "memory) instead of the planes")
     p.add_argument("--experts", type=int, default=0,
                    help="profiling aid: override the routed-expert count (same "
                         "per-token work, smaller resident set); not a bench line")
@@ -337,6 +341,10 @@ def run_ours(args):
     if args.tokens:
         wl = dataclasses.replace(wl, T=args.tokens, name=wl.name + "-t%d" % args.tokens)
     T = wl.T
+    # batches run on the exact planes unless another batch path is asked for
+    if (T > 8 and not (args.no_planes or args.mxfp8 or args.mma_sync_prefill or args.cache_slots
+                       or wl.stack)):
+        args.planes = True
     flags = ((dfm.STACK_RMSNORM_RESIDUAL if wl.stack else 0)
              | (dfm.PREFILL_MMA_SYNC if args.mma_sync_prefill else 0)
              | (dfm.MXFP8_ACT if args.mxfp8 else 0)
@@ -585,7 +593,10 @@ def run_ours(args):
         "config": {**workload_config(wl, ws),
                    "l2": "flushed (256 MiB write) before every timed step",
                    "launch": "cuda graph" if args.graph else "stream",
-                   "prefill_path": "mma_sync" if args.mma_sync_prefill else "tcgen05",
+                   "prefill_path": ("mma_sync" if args.mma_sync_prefill else
+                                    "tcgen05 block-scaled (E4M3 planes)" if args.planes else
+                                    "tcgen05 block-scaled (MXFP8)" if args.mxfp8 else
+                                    "tcgen05 (MXFP4 decoded into tensor memory)"),
                    "activations": ("MXFP8 (E4M3, E8M0 per 32) into the routed experts: "
                                    "the lossy variant") if args.mxfp8 else
                                   ("exact, as sums of E4M3 planes (x 4, h 5) on the "
