@@ -264,7 +264,11 @@ DF_MOE_API void df_moe_graph_destroy(df_moe_graph* g);
 DF_MOE_API int df_moe_stream_read(const void* buf, size_t bytes, uint32_t* sink, void* stream);
 
 /* ---- single steps (the rows of the hot path, for per-step checks) ---------
- * Each runs one step of the forward on its own, with the same kernels. */
+ * Each runs one step of the forward on its own, with the same kernels. Every
+ * device array argument of the steps below (x, logits, ids, weights, hbuf,
+ * y, xn, and group's outputs) must be 16-byte aligned, as the kernels read
+ * and write them with vector accesses and tensor maps; a misaligned one is
+ * EINVAL before anything is launched. */
 
 /* logits device [T][E] fp32 of layer `layer`. */
 DF_MOE_API int df_moe_step_router(df_moe* h, int32_t layer, const void* x_bf16, int32_t T,

@@ -21,6 +21,8 @@ thread_local std::string g_thread_err;
 struct LayerBufs {
   uint8_t* arena = nullptr;   // E spans, device layout
   float* router = nullptr;    // [E][H]
+  uint16_t* router3 = nullptr;  // [E][3H] bf16 high | middle | low (batch router on tcgen05)
+  ChunkMap router_map{};        // its tensor map
   uint16_t* sh_gate = nullptr;  // [n_s*Is][H]
   uint16_t* sh_up = nullptr;    // [n_s*Is][H]
   uint16_t* sh_down = nullptr;  // [H][n_s*Is]
@@ -63,7 +65,9 @@ struct df_moe {
   RouterSplit rsplit{};
   std::vector<LayerBufs> layers;
   // workspace
-  float* router_part = nullptr;  // [nsplit][Tmax][E]
+  float* router_part = nullptr;  // [nsplit][Tmax][E] (batches on tcgen05: [splits][T][E])
+  size_t router_part_rows = 0;   // its rows (planes x tokens)
+  bool router_tc = false;        // batches' router logits on tcgen05
   float* logits = nullptr;       // [Tmax][E]
   int32_t* ids_ws = nullptr;     // [Tmax][k]
   float* w_ws = nullptr;         // [Tmax][k]
@@ -253,12 +257,14 @@ int route(df_moe* h, int l, const uint16_t* x, int T, int32_t* ids, float* w,
   }
   int nsplit = h->rsplit.nsplit;
   if (T > kDecodeMaxT) {
-    // a batch: the logits as one tiled GEMM (weights read once for all tokens)
+    // a batch: the logits as one GEMM on the tensor cores (the weights read
+    // once for all tokens)
     int used = -1;
-    RUN(h, K_ROUTER, s, (used = launch_router_gemm(L.router, c.n_experts, c.hidden, x, T,
-                                                   h->router_part, nsplit, h->sms, s)) < 0
-                            ? cudaErrorLaunchFailure
-                            : cudaSuccess);
+    RUN(h, K_ROUTER, s,
+        (used = launch_router_tc(L.router_map, x, T, c.n_experts, c.hidden, h->router_part,
+                                 h->router_part_rows, h->sms, h->err, s)) < 0
+            ? cudaErrorLaunchFailure
+            : cudaSuccess);
     nsplit = used;
   } else {
     RUN(h, K_ROUTER, s, launch_router(L.router, c.n_experts, c.hidden, x, T,
@@ -525,6 +531,11 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+bool all_aligned16(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (!aligned16(p)) return false;
+  return true;
+}
 
 }  // namespace
 
@@ -625,6 +636,7 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
   h->span_bytes = span_layout(c.hidden, c.inter).bytes;
   h->R = c.n_shared * c.shared_inter;
   h->rsplit = router_split(c.n_experts, c.hidden);
+  cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, cuda_device);
   const size_t H = c.hidden, E = c.n_experts, k = c.top_k, I = c.inter;
   const size_t Tm = c.max_tokens, R = h->R;
   int rc = DF_MOE_OK;
@@ -711,7 +723,19 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
                                       (int)(3 * Tm), &L.sh_maps);
     }
   }
-  if (!rc) rc = dalloc(h, &h->router_part, (size_t)h->rsplit.nsplit * Tm * E);
+  // batches' router on tcgen05: the weights' bf16 parts and their map
+  h->router_tc = Tm > (size_t)kDecodeMaxT;
+  for (int l = 0; l < c.n_layers && !rc && h->router_tc; ++l) {
+    LayerBufs& L = h->layers[l];
+    rc = dalloc(h, &L.router3, E * 3 * H);
+    if (!rc && !make_router_map(L.router3, c.n_experts, c.hidden, &L.router_map))
+      rc = fail(h, DF_MOE_ECUDA, "tensor map encoding failed");
+  }
+  h->router_part_rows = (size_t)h->rsplit.nsplit * Tm;
+  if (h->router_tc)
+    h->router_part_rows = std::max(h->router_part_rows,
+                                   router_tc_part_rows(c.n_experts, c.hidden, (int)Tm, h->sms));
+  if (!rc) rc = dalloc(h, &h->router_part, h->router_part_rows * E);
   if (!rc) rc = dalloc(h, &h->logits, Tm * E);
   if (!rc) rc = dalloc(h, &h->ids_ws, Tm * k);
   if (!rc) rc = dalloc(h, &h->w_ws, Tm * k);
@@ -769,7 +793,6 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
     }
   }
   if (!rc) {
-    cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, cuda_device);
     // (the MXFP8 variant runs every batch through its GEMMs)
     h->phase = !h->mx8 &&
                phase_supported(H, c.inter, c.n_shared > 0 ? h->R : 0, c.n_experts, c.top_k);
@@ -825,6 +848,8 @@ int df_moe_load_experts(df_moe* h, int32_t layer, const df_moe_layer_weights* w,
     CUDA_OR_FAIL(h, cudaMemcpyAsync(L.router, w->router,
                                     (size_t)c.n_experts * H * sizeof(float),
                                     kind, s));
+    if (L.router3)
+      CUDA_OR_FAIL(h, launch_router_parts(L.router, c.n_experts, c.hidden, L.router3, s));
     L.router_loaded = true;
   }
   for (int sidx = 0; sidx < c.n_shared; ++sidx) {
@@ -1076,6 +1101,8 @@ int df_moe_step_router(df_moe* h, int32_t layer, const void* x_bf16, int32_t T,
   if (layer < 0 || layer >= c.n_layers) return fail(h, DF_MOE_ERANGE, "bad layer");
   if (T < 1 || T > c.max_tokens) return fail(h, DF_MOE_ERANGE, "bad T");
   if (!x_bf16 || !logits) return fail(h, DF_MOE_EINVAL, "null pointer");
+  if (!all_aligned16({x_bf16, logits}))
+    return fail(h, DF_MOE_EINVAL, "device arrays must be 16-byte aligned");
   if (!h->layers[layer].router_loaded) return fail(h, DF_MOE_ESTATE, "router not loaded");
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
   cudaStream_t s = (cudaStream_t)stream;
@@ -1089,6 +1116,8 @@ int df_moe_step_topk(df_moe* h, const float* logits, int32_t T, int32_t* ids,
   const df_moe_config& c = h->cfg;
   if (T < 1 || T > c.max_tokens) return fail(h, DF_MOE_ERANGE, "bad T");
   if (!logits || !ids || !weights) return fail(h, DF_MOE_EINVAL, "null pointer");
+  if (!all_aligned16({logits, ids, weights}))
+    return fail(h, DF_MOE_EINVAL, "device arrays must be 16-byte aligned");
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
   cudaStream_t s = (cudaStream_t)stream;
   // the top-k kernel sums nsplit partial-logit planes; one plane = logits
@@ -1105,6 +1134,8 @@ int df_moe_step_group(df_moe* h, const int32_t* ids, int32_t T, int32_t* offs,
   if (T < 1 || T > c.max_tokens) return fail(h, DF_MOE_ERANGE, "bad T");
   if (!ids || !offs || !tok || !slot || !n_union)
     return fail(h, DF_MOE_EINVAL, "null pointer");
+  if (!all_aligned16({ids, offs, tok, slot, n_union}))
+    return fail(h, DF_MOE_EINVAL, "device arrays must be 16-byte aligned");
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
   cudaStream_t s = (cudaStream_t)stream;
   RUN(h, K_GROUP, s, launch_group(ids, T, c.top_k, c.n_experts, offs, tok, slot,
@@ -1121,12 +1152,12 @@ int df_moe_step_expert_gateup(df_moe* h, int32_t layer, const void* x_bf16,
   if (layer < 0 || layer >= c.n_layers) return fail(h, DF_MOE_ERANGE, "bad layer");
   if (T < 1 || T > c.max_tokens) return fail(h, DF_MOE_ERANGE, "bad T");
   if (!x_bf16 || !ids || !hbuf) return fail(h, DF_MOE_EINVAL, "null pointer");
+  if (!all_aligned16({x_bf16, ids, hbuf}))
+    return fail(h, DF_MOE_EINVAL, "device arrays must be 16-byte aligned");
   if (h->layers[layer].n_experts_loaded != c.n_experts)
     return fail(h, DF_MOE_ESTATE, "experts not loaded");
   if (h->cache_slots)
     return fail(h, DF_MOE_EINVAL, "single expert steps read the resident arena: not with a cache");
-  if (h->mx8 && !aligned16(x_bf16))
-    return fail(h, DF_MOE_EINVAL, "x must be 16-byte aligned");
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
   cudaStream_t s = (cudaStream_t)stream;
   const int tg = kOneItemPerExpert;
@@ -1145,12 +1176,12 @@ int df_moe_step_expert_down(df_moe* h, int32_t layer, const float* hbuf,
   if (layer < 0 || layer >= c.n_layers) return fail(h, DF_MOE_ERANGE, "bad layer");
   if (T < 1 || T > c.max_tokens) return fail(h, DF_MOE_ERANGE, "bad T");
   if (!hbuf || !ids || !weights || !y) return fail(h, DF_MOE_EINVAL, "null pointer");
+  if (!all_aligned16({hbuf, ids, weights, y}))
+    return fail(h, DF_MOE_EINVAL, "device arrays must be 16-byte aligned");
   if (h->layers[layer].n_experts_loaded != c.n_experts)
     return fail(h, DF_MOE_ESTATE, "experts not loaded");
   if (h->cache_slots)
     return fail(h, DF_MOE_EINVAL, "single expert steps read the resident arena: not with a cache");
-  if (h->mx8 && !aligned16(hbuf))
-    return fail(h, DF_MOE_EINVAL, "hbuf must be 16-byte aligned");
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
   cudaStream_t s = (cudaStream_t)stream;
   const int tg = kOneItemPerExpert;
@@ -1183,6 +1214,8 @@ int df_moe_step_shared(df_moe* h, int32_t layer, const void* x_bf16, int32_t T,
   if (layer < 0 || layer >= c.n_layers) return fail(h, DF_MOE_ERANGE, "bad layer");
   if (T < 1 || T > c.max_tokens) return fail(h, DF_MOE_ERANGE, "bad T");
   if (!x_bf16 || !y) return fail(h, DF_MOE_EINVAL, "null pointer");
+  if (!all_aligned16({x_bf16, y}))
+    return fail(h, DF_MOE_EINVAL, "device arrays must be 16-byte aligned");
   for (int sidx = 0; sidx < c.n_shared; ++sidx)
     if (!h->layers[layer].shared_loaded[sidx])
       return fail(h, DF_MOE_ESTATE, "shared expert %d not loaded", sidx);
@@ -1201,6 +1234,8 @@ int df_moe_step_rmsnorm(df_moe* h, const void* x_bf16, int32_t T, void* xn_bf16,
   const df_moe_config& c = h->cfg;
   if (T < 1 || T > c.max_tokens) return fail(h, DF_MOE_ERANGE, "bad T");
   if (!x_bf16 || !xn_bf16) return fail(h, DF_MOE_EINVAL, "null pointer");
+  if (!all_aligned16({x_bf16, xn_bf16}))
+    return fail(h, DF_MOE_EINVAL, "device arrays must be 16-byte aligned");
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
   cudaStream_t s = (cudaStream_t)stream;
   RUN(h, K_RMSNORM, s, launch_rmsnorm((const uint16_t*)x_bf16, T, c.hidden,

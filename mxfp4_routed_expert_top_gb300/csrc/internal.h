@@ -130,11 +130,6 @@ struct RouterFuse {
 cudaError_t launch_router(const float* Wr, int E, int H, const uint16_t* x,
                           int T, float* part, RouterSplit sp, cudaStream_t s,
                           const RouterFuse* fuse = nullptr, bool after_previous = true);
-// Router logits of a batch (T > 1) as a tiled fp32 GEMM into at most
-// max_splits column splits of part; returns the split count used (-1 on a
-// launch error).
-int launch_router_gemm(const float* Wr, int E, int H, const uint16_t* x, int T, float* part,
-                       int max_splits, int sms, cudaStream_t s);
 cudaError_t launch_topk(const float* part, int nsplit, int T, int E, int k,
                         float* logits_out, int32_t* ids, float* w,
                         Item* items, int32_t* n_items, int32_t* sorted,
@@ -278,6 +273,23 @@ cudaError_t launch_shared_gemm_gateup(const SharedMaps& m, const uint16_t* x, in
 // y [T][H] = down (high + middle + low).
 cudaError_t launch_shared_gemm_down(const SharedMaps& m, int T, int H, int R, float* y,
                                     uint32_t* err, cudaStream_t s);
+
+// ---- router logits of batches on tcgen05 (k_dense.cu) ------------------------
+// The fp32 router weights as three bf16 parts per row ([E][3H]: high,
+// middle, low, summing to the weight), written once at load; a dense bf16
+// GEMM of x against them gives fp32 logits with exact products. K is split
+// over CTAs to fill `sms` SMs: split s writes part[s][T][E] (summed by the
+// top-k kernel). max_rows bounds splits x T (the part buffer's rows; 0: no
+// bound). H: a multiple of 64.
+int router_tc_splits(int E, int H, int T, int sms, size_t max_rows);
+// the largest splits x T over batches above the decode range up to Tmax
+size_t router_tc_part_rows(int E, int H, int Tmax, int sms);
+cudaError_t launch_router_parts(const float* w, int E, int H, uint16_t* out, cudaStream_t s);
+bool make_router_map(const uint16_t* parts, int E, int H, ChunkMap* out);
+// returns the number of partial planes written, -1 on a launch or encoding
+// failure (x: bf16 [T][H], 16-byte aligned)
+int launch_router_tc(const ChunkMap& map, const uint16_t* x, int T, int E, int H, float* part,
+                     size_t max_rows, int sms, uint32_t* err, cudaStream_t s);
 
 // ---- routed experts on block-scaled MXFP4 x E4M3 GEMMs (k_mx8.cu) ----------
 // Grouped GEMMs on tcgen05.mma kind::mxf8f6f4 with the MXFP4 codes and

@@ -13,7 +13,16 @@
 //           summed in the epilogue = y[t][row].
 // bf16 x bf16 products are exact and the accumulators fp32 (tensor memory).
 //
-// One 128 x 128 (GEMM 1) or 128 x 96 (GEMM 2: 32 tokens) output tile per
+// The router logits of a batch run here too (GEMM 3): the fp32 router
+// weights are held as three bf16 parts side by side along K ([E][3H]: high,
+// middle, low; their sum is the fp32 weight), the K loop walks 3H columns
+// with x's column index taken modulo H, so the accumulator sums x . (high +
+// middle + low) = x . w with exact products. The K range is split over CTAs
+// so that the grid fills the SMs; split s writes its own partial plane
+// part[s][t][e], and the top-k kernel sums the planes in order (the same
+// sums every run).
+//
+// One 128 x 128 (GEMM 1 and 3) or 128 x 96 (GEMM 2: 32 tokens) output tile per
 // CTA, 192 threads: warp 0 loads A and B tiles
 // of 64 columns by TMA (128-byte swizzle) into a ring of stages, warp 1
 // issues tcgen05.mma (M = 128, N = 128, K = 16) and commits each stage back,
@@ -41,12 +50,15 @@ constexpr uint32_t kDCols = 128;               // tensor memory columns: the fp3
 constexpr int kXsLd = kDN + 1;                 // padded row of the up-value exchange
 
 struct DenseArgs {
-  ChunkMap a0, a1;  // A: GEMM 1 gate and up [R][H]; GEMM 2 down [H][R] (a0)
-  ChunkMap b;       // B: GEMM 1 x [T][H]; GEMM 2 hh [3T][R]
-  int mode;         // 0: gate/up, 1: down
+  ChunkMap a0, a1;  // A: GEMM 1 gate and up [R][H]; GEMM 2 down [H][R] (a0); GEMM 3 [E][3H]
+  ChunkMap b;       // B: GEMM 1 and 3 x [T][H]; GEMM 2 hh [3T][R]
+  int mode;         // 0: gate/up, 1: down, 2: router logits
   int K, T, R, H;
+  int tiles;        // GEMM 3: output tiles a K split (the grid is tiles x splits)
+  int per;          // GEMM 3: K blocks of 64 a split
+  int E;            // GEMM 3: experts (rows of A)
   uint16_t* hh;     // GEMM 1 out: [T][3][R] bf16 (high, middle, low)
-  float* y;         // GEMM 2 out: [T][H] fp32
+  float* y;         // GEMM 2 out: [T][H] fp32; GEMM 3 out: [split][T][E] fp32
   uint32_t* err;
 };
 
@@ -86,11 +98,17 @@ __global__ void __launch_bounds__(kDThr, 1) dense_kernel(const __grid_constant__
   uint8_t* sb = smem + (size_t)kDStages * kDABytes;
   DSmem* sm = reinterpret_cast<DSmem*>(sb + (size_t)kDStages * kDBBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bn = a.mode == 0 ? kDN : kDN1;          // B rows of a tile
-  const int n_rows = a.mode == 0 ? a.T : 3 * a.T;  // B rows
+  const int bn = a.mode == 1 ? kDN1 : kDN;          // B rows of a tile
+  const int n_rows = a.mode == 1 ? 3 * a.T : a.T;  // B rows
   const int ntn = (n_rows + bn - 1) / bn;
-  const int mt = blockIdx.x / ntn, nt = blockIdx.x - mt * ntn;
-  const int NK = a.K / kDK;
+  const int split = a.mode == 2 ? (int)blockIdx.x / a.tiles : 0;
+  const int tile = (int)blockIdx.x - split * (a.mode == 2 ? a.tiles : 0);
+  const int mt = tile / ntn, nt = tile - mt * ntn;
+  // this CTA's K blocks: kb0 .. kb0 + NK - 1 (GEMM 3: one split; x's column
+  // block is the A block modulo the H / 64 blocks of one part)
+  const int kb0 = split * (a.mode == 2 ? a.per : 0);
+  const int NK = a.mode == 2 ? min(a.per, a.K / kDK - kb0) : a.K / kDK;
+  const int xkb = a.H / kDK;
 
   if (warp == 2) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -132,10 +150,15 @@ __global__ void __launch_bounds__(kDThr, 1) dense_kernel(const __grid_constant__
       if (a.mode == 0) {
         tma_2d(da, &a.a0, kDK * it, 64 * mt, bar);
         tma_2d(da + kDABytes / 2, &a.a1, kDK * it, 64 * mt, bar);
-      } else {
+        tma_2d(db, &a.b, kDK * it, bn * nt, bar);
+      } else if (a.mode == 1) {
         tma_2d(da, &a.a0, kDK * it, kDM * mt, bar);
+        tma_2d(db, &a.b, kDK * it, bn * nt, bar);
+      } else {
+        const int kb = kb0 + it;
+        tma_2d(da, &a.a0, kDK * kb, kDM * mt, bar);
+        tma_2d(db, &a.b, kDK * (kb % xkb), bn * nt, bar);
       }
-      tma_2d(db, &a.b, kDK * it, bn * nt, bar);
     }
   } else if (warp == 1) {
     // ---- MMAs: four K = 16 steps a stage into the fp32 accumulator
@@ -238,6 +261,27 @@ __global__ void __launch_bounds__(kDThr, 1) dense_kernel(const __grid_constant__
             }
           }
         }
+      } else if (a.mode == 2) {
+        // partial logits of this split: lanes are experts (consecutive
+        // addresses for a token), columns tokens
+        const int e = kDM * mt + m;
+        float* dst = a.y + (size_t)split * a.T * a.E;
+        for (int c0 = 0; c0 < kDN; c0 += 16) {
+          uint32_t r[16];
+          asm volatile(
+              "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"
+              "%12,%13,%14,%15}, [%16];"
+              : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+              : "r"(d + (uint32_t)c0));
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int t = kDN * nt + c0 + i;
+            if (t < a.T && e < a.E) dst[(size_t)t * a.E + e] = __uint_as_float(r[i]);
+          }
+        }
       } else {
         const int row = kDM * mt + m;  // output row of H
         // 48 columns at a time: 16 tokens x (high, middle, low)
@@ -308,6 +352,28 @@ bool map_bf16(ChunkMap* out, const void* base, int cols, int rows, int box_rows)
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The three bf16 parts of fp32 router weights: high = bf16(w), middle =
+// bf16(w - high), low = bf16(w - high - middle); both differences are exact
+// in fp32, and high + middle + low = w for every finite w whose low part is
+// not below the bf16 subnormal range. Row e of `out` holds [high | middle |
+// low] (3H columns).
+__global__ void router_parts_kernel(const float* __restrict__ w, size_t n, int H,
+                                    uint16_t* __restrict__ out) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t e = i / H, j = i - e * H;
+    const float v = w[i];
+    const uint32_t hi = bf16_bits(v);
+    const float r1 = v - __uint_as_float(hi << 16);
+    const uint32_t mid = bf16_bits(r1);
+    const uint32_t lo = bf16_bits(r1 - __uint_as_float(mid << 16));
+    uint16_t* row = out + e * 3 * (size_t)H;
+    row[j] = (uint16_t)hi;
+    row[H + j] = (uint16_t)mid;
+    row[2 * (size_t)H + j] = (uint16_t)lo;
+  }
+}
+
 cudaError_t launch_dense(const DenseArgs& a, int tiles, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
@@ -360,6 +426,59 @@ cudaError_t launch_shared_gemm_down(const SharedMaps& m, int T, int H, int R, fl
   a.y = y;
   a.err = err;
   return launch_dense(a, (H / kDM) * ((3 * T + kDN1 - 1) / kDN1), s);
+}
+
+// ---- router logits of a batch (GEMM 3) --------------------------------------
+int router_tc_splits(int E, int H, int T, int sms, size_t max_rows) {
+  if (T < 1) return 0;
+  const int tiles = ((E + kDM - 1) / kDM) * ((T + kDN - 1) / kDN);
+  const int KB = 3 * H / kDK;
+  size_t n = (size_t)std::max(1, sms / tiles);
+  n = std::min(n, (size_t)KB);
+  if (max_rows) n = std::min(n, max_rows / (size_t)T);
+  if (n < 1) return 0;
+  const int per = (KB + (int)n - 1) / (int)n;
+  return (KB + per - 1) / per;
+}
+
+size_t router_tc_part_rows(int E, int H, int Tmax, int sms) {
+  size_t rows = 0;
+  for (int T = kDecodeMaxT + 1; T <= Tmax; ++T)
+    rows = std::max(rows, (size_t)router_tc_splits(E, H, T, sms, 0) * T);
+  return rows;
+}
+
+cudaError_t launch_router_parts(const float* w, int E, int H, uint16_t* out, cudaStream_t s) {
+  const size_t n = (size_t)E * H;
+  const int blocks = (int)std::min<size_t>((n + 255) / 256, 4096);
+  router_parts_kernel<<<blocks, 256, 0, s>>>(w, n, H, out);
+  return cudaGetLastError();
+}
+
+bool make_router_map(const uint16_t* parts, int E, int H, ChunkMap* out) {
+  return map_bf16(out, parts, 3 * H, E, kDM);
+}
+
+int launch_router_tc(const ChunkMap& map, const uint16_t* x, int T, int E, int H, float* part,
+                     size_t max_rows, int sms, uint32_t* err, cudaStream_t s) {
+  const int nsplit = router_tc_splits(E, H, T, sms, max_rows);
+  if (nsplit < 1) return -1;
+  DenseArgs a{};
+  a.a0 = map;
+  a.a1 = map;
+  if (!map_bf16(&a.b, x, H, T, kDN)) return -1;
+  a.mode = 2;
+  a.K = 3 * H;
+  a.T = T;
+  a.R = 0;
+  a.H = H;
+  a.E = E;
+  a.tiles = ((E + kDM - 1) / kDM) * ((T + kDN - 1) / kDN);
+  const int KB = 3 * H / kDK;
+  a.per = (KB + nsplit - 1) / nsplit;
+  a.y = part;
+  a.err = err;
+  return launch_dense(a, a.tiles * nsplit, s) == cudaSuccess ? nsplit : -1;
 }
 
 }  // namespace dfm

@@ -280,107 +280,7 @@ group_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
   if (tid == E - 1 && n_union) *n_union = nz + (c > 0 ? 1 : 0);
 }
 
-// Router logits of a batch as a tiled fp32 GEMM on the CUDA cores:
-// part[split][t][e] = sum over the split's columns j of Wr[e][j] x[t][j].
-// Tiles of 64 tokens x 128 experts x 32 columns staged in shared memory
-// (rows K-contiguous, padded to 36 floats so that a quarter-warp's 16-byte
-// reads of eight rows hit distinct banks); each of the 256 threads owns 4
-// tokens x 8 experts, rows tm + 16 i and tn + 16 j. fp32 FMAs in a fixed
-// order: the same sums every run. The next tile is fetched into registers
-// while the current one is multiplied.
-constexpr int kRgBM = 64, kRgBN = 128, kRgBK = 32, kRgLd = kRgBK + 4;
-
-__global__ void __launch_bounds__(256)
-router_gemm_kernel(const float* __restrict__ Wr, int E, int H, const uint16_t* __restrict__ x,
-                   int T, float* __restrict__ part, int split_len) {
-  __shared__ __align__(16) float As[kRgBM][kRgLd];
-  __shared__ __align__(16) float Bs[kRgBN][kRgLd];
-  const int tid = threadIdx.x, tm = tid >> 4, tn = tid & 15;
-  const int n0 = blockIdx.x * kRgBN, m0 = blockIdx.y * kRgBM, split = blockIdx.z;
-  const int k0 = split * split_len, k1 = min(H, k0 + split_len);
-  // loaders: A row tid/4, 8 columns at 8 (tid%4); B rows tid/8 + 32 i, 4 columns at 4 (tid%8)
-  const int ar = tid >> 2, ac = 8 * (tid & 3);
-  const int br = tid >> 3, bc = 4 * (tid & 7);
-  const bool a_ok = m0 + ar < T;
-  uint4 ra;
-  float4 rb[4];
-  auto fetch = [&](int k) {
-    ra = a_ok ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(m0 + ar) * H + k + ac))
-              : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int e = n0 + br + 32 * i;
-      rb[i] = e < E ? __ldg(reinterpret_cast<const float4*>(Wr + (size_t)e * H + k + bc))
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  };
-  auto stash = [&]() {
-    float4 lo, hi;
-    lo.x = __uint_as_float(ra.x << 16); lo.y = __uint_as_float(ra.x & 0xFFFF0000u);
-    lo.z = __uint_as_float(ra.y << 16); lo.w = __uint_as_float(ra.y & 0xFFFF0000u);
-    hi.x = __uint_as_float(ra.z << 16); hi.y = __uint_as_float(ra.z & 0xFFFF0000u);
-    hi.z = __uint_as_float(ra.w << 16); hi.w = __uint_as_float(ra.w & 0xFFFF0000u);
-    *reinterpret_cast<float4*>(&As[ar][ac]) = lo;
-    *reinterpret_cast<float4*>(&As[ar][ac + 4]) = hi;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) *reinterpret_cast<float4*>(&Bs[br + 32 * i][bc]) = rb[i];
-  };
-  float acc[4][8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-  if (k0 < k1) fetch(k0);
-  for (int k = k0; k < k1; k += kRgBK) {
-    __syncthreads();  // the previous tile has been read
-    stash();
-    __syncthreads();
-    if (k + kRgBK < k1) fetch(k + kRgBK);
-#pragma unroll
-    for (int kk = 0; kk < kRgBK; kk += 4) {
-      float4 a[4], b[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = *reinterpret_cast<const float4*>(&As[tm + 16 * i][kk]);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) b[j] = *reinterpret_cast<const float4*>(&Bs[tn + 16 * j][kk]);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          acc[i][j] = fmaf(a[i].x, b[j].x, acc[i][j]);
-          acc[i][j] = fmaf(a[i].y, b[j].y, acc[i][j]);
-          acc[i][j] = fmaf(a[i].z, b[j].z, acc[i][j]);
-          acc[i][j] = fmaf(a[i].w, b[j].w, acc[i][j]);
-        }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = m0 + tm + 16 * i;
-    if (t >= T) continue;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int e = n0 + tn + 16 * j;
-      if (e < E) part[((size_t)split * T + t) * E + e] = acc[i][j];
-    }
-  }
-}
-
 }  // namespace
-
-int launch_router_gemm(const float* Wr, int E, int H, const uint16_t* x, int T, float* part,
-                       int max_splits, int sms, cudaStream_t s) {
-  const int tiles = ((E + kRgBN - 1) / kRgBN) * ((T + kRgBM - 1) / kRgBM);
-  // one wave: a CTA holds a whole SM's registers (4 x 8 accumulators and the
-  // next tile in flight per thread)
-  int nsplit = sms / tiles;
-  nsplit = std::max(1, std::min(nsplit, std::min(max_splits, H / kRgBK)));
-  const int split_len = ((H + nsplit - 1) / nsplit + kRgBK - 1) / kRgBK * kRgBK;
-  nsplit = (H + split_len - 1) / split_len;
-  dim3 grid((E + kRgBN - 1) / kRgBN, (T + kRgBM - 1) / kRgBM, nsplit);
-  router_gemm_kernel<<<grid, 256, 0, s>>>(Wr, E, H, x, T, part, split_len);
-  return cudaGetLastError() == cudaSuccess ? nsplit : -1;
-}
 
 cudaError_t launch_router(const float* Wr, int E, int H, const uint16_t* x,
                           int T, float* part, RouterSplit sp, cudaStream_t s,

@@ -203,6 +203,20 @@ def test_errors(tiny, torch):
     with pytest.raises(dfm.DfMoeError) as ei:
         tiny.m.forward(x, 1, None, ids, w)
     assert ei.value.code == -1
+    # device arrays of the steps off a 16-byte boundary: refused before any
+    # launch (the kernels read them with vector accesses)
+    flat = torch.zeros(2 * WL.H + 8, dtype=torch.int16, device="cuda")
+    xm = flat[1:1 + WL.H]
+    lg = torch.empty((1, WL.E), dtype=torch.float32, device="cuda")
+    hb = torch.empty((WL.k, WL.I), dtype=torch.float32, device="cuda")
+    ysh = torch.empty((1, WL.H), dtype=torch.float32, device="cuda")
+    for call in (lambda: tiny.m.step_router(0, xm, 1, lg),
+                 lambda: tiny.m.step_expert_gateup(0, xm, 1, ids, hb),
+                 lambda: tiny.m.step_shared(0, xm, 1, ysh),
+                 lambda: tiny.m.step_rmsnorm(xm, 1, flat[8:8 + WL.H])):
+        with pytest.raises(dfm.DfMoeError) as ei:
+            call()
+        assert ei.value.code == -1
     with dfm.MoE(WL.H, WL.E, WL.k, WL.I, WL.n_shared, WL.Is) as fresh:
         with pytest.raises(dfm.DfMoeError) as ei:
             fresh.forward(x, 1, out, ids, w)
