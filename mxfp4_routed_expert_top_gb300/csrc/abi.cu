@@ -693,8 +693,8 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
     if (!rc) rc = dalloc(h, &h->mx_xsf, H / 128 * xrows * 16);
     if (!rc) rc = dalloc(h, &h->mx_hq, hrows * I);
     if (!rc) rc = dalloc(h, &h->mx_hsf, I / 128 * hrows * 16);
-    if (!rc && (!make_mx8_row_map(h->mx_xq, h->mx_xrows, c.hidden, &h->mx_xmap) ||
-                !make_mx8_row_map(h->mx_hq, h->mx_hrows, c.inter, &h->mx_hmap)))
+    if (!rc && (!make_mx8_row_map(h->mx_xq, h->mx_xrows, c.hidden, h->px, &h->mx_xmap) ||
+                !make_mx8_row_map(h->mx_hq, h->mx_hrows, c.inter, h->ph, &h->mx_hmap)))
       rc = fail(h, DF_MOE_ECUDA, "tensor map encoding failed");
   }
   if (h->gemm) {

@@ -300,14 +300,15 @@ int launch_router_tc(const ChunkMap& map, const uint16_t* x, int T, int E, int H
 constexpr int kPlanesX = 4, kPlanesH = 5;
 bool mx8_supported(int H, int I);
 // Rows of an expert-ordered activation buffer for nassign assignments of
-// `planes` rows each (and 32 more, read past the last row by a stage's
-// 32-row scale chunk).
+// `planes` rows each, and the rows that a stage's 32-row scale chunk or its
+// B box reads past the last one.
 int mx8_rows_cap(int nassign, int planes);
 // Tensor maps of the gate, up and down codes of an arena of E spans.
 bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E, ChunkMap* gate,
                    ChunkMap* up, ChunkMap* down);
-// Tensor map of E4M3 activation rows [rows_cap][K].
-bool make_mx8_row_map(const uint8_t* rows, int rows_cap, int K, ChunkMap* map);
+// Tensor map of E4M3 activation rows [rows_cap][K], written as `planes`
+// rows a token or assignment (its box covers one pass of the GEMM).
+bool make_mx8_row_map(const uint8_t* rows, int rows_cap, int K, int planes, ChunkMap* map);
 // Rounds the rows of the items' assignments: row n of item i is source row
 // sorted[pos + n] / div of src (bf16 or fp32, [.][K], 16-byte aligned),
 // written as `planes` E4M3 rows (pos + n) planes + p of q ([rows_cap][K])

@@ -37,9 +37,9 @@
 // consecutive 128-row tiles), two MMAs a K step into two accumulators, x the
 // item's tokens in passes (the MMA's N a multiple of 16), the contraction in
 // stages of 128 columns:
-//   warp 4     TMA: a stage's A operands (64-row boxes), its B rows (boxes of
-//              16 rows) and its scale chunks (bulk copies), on a ring of
-//              shared-memory stages;
+//   warp 4     TMA: a stage's A operands (one 128-row box each), its B rows
+//              (a pass in one or two boxes) and its scale chunks (bulk
+//              copies), on a ring of shared-memory stages;
 //   warp 5     per stage: the scale copies to tensor memory, the MMAs (M =
 //              128, K = 32) into one of 3 (gate/up) or 4 (down) accumulator
 //              sets in turn, the commits;
@@ -64,14 +64,18 @@ namespace {
 
 constexpr int kThr = 192;
 constexpr int kTmaWarp = 4, kMmaWarp = 5;
-constexpr int kM = 128, kHalfRows = 64;
+constexpr int kM = 128;
 constexpr int kKS = 128;                  // contraction columns a stage
-constexpr int kBoxRows = 16;              // B rows a TMA box
 constexpr int kABytes = kM * kKS;         // 16384: one A operand (a byte a code)
-constexpr int kAHalfTx = kHalfRows * kKS / 2;  // 4096: a 64-row box's codes as copied
+constexpr int kATx = kM * kKS / 2;       // 8192: an A operand's codes as copied (packed)
 constexpr int kSfBytes = 512;            // a stage's scale chunk (an operand's, or the tokens')
 constexpr int kSfRowBytes = 16;           // an activation row's scale words
 constexpr uint32_t kTmemCols = 512;
+// B rows a TMA box: a whole pass of exact planes (16 tokens x P planes) in
+// one box, 32 rows for one plane (passes of 32 or 64 rows). A box may run
+// past the pass into the next item's rows (or past the buffer: zero fill);
+// the MMA columns there are never read.
+__host__ __device__ constexpr int box_rows(int planes) { return planes > 1 ? 16 * planes : 32; }
 
 // Per GEMM and token tile KN (tokens a pass at most, 32 or 64): A operands
 // a stage (gate/up: gate and up), the stages that fit in shared memory, the
@@ -206,12 +210,12 @@ __device__ __forceinline__ void mma_mx(uint32_t d, uint64_t ad, uint64_t bd, uin
 // Weight tiles (read once a call): evict-first in L2, so that the streamed
 // weights do not push out the activation rows every M tile re-reads.
 // Coordinates (element, row in the tile, stage, tile, expert).
-__device__ __forceinline__ void tma5d_stream(void* dst, const ChunkMap* m, int r, int ks, int tile,
-                                             int e, uint64_t* bar, uint64_t pol) {
+__device__ __forceinline__ void tma5d_stream(void* dst, const ChunkMap* m, int ks, int tile, int e,
+                                             uint64_t* bar, uint64_t pol) {
   asm volatile(
       "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
-      "l"(m), "r"(0), "r"(r), "r"(ks), "r"(tile), "r"(e), "r"(smem_u32(bar)), "l"(pol)
+      "l"(m), "r"(0), "r"(0), "r"(ks), "r"(tile), "r"(e), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, const void* src) {
@@ -284,7 +288,8 @@ __device__ __forceinline__ Unit unit_at(const Mx8Args& a, int u) {
   w.pos = it.pos;
   w.cnt = it.cnt;
   w.ok = (unsigned)it.e < (unsigned)a.E && it.cnt >= 1 && it.pos >= 0 &&
-         it.pos + it.cnt <= a.nassign && (it.pos + it.cnt) * P + 32 <= a.rows_cap;
+         it.pos + it.cnt <= a.nassign &&
+         (it.pos + it.cnt) * P + (box_rows(P) > 32 ? box_rows(P) : 32) <= a.rows_cap;
   return w;
 }
 
@@ -306,27 +311,27 @@ __device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<
     const uint8_t* span = a.arena + (size_t)w.e * a.span_bytes;
     for (int tb = 0; tb < w.cnt && ok; tb += KN / P) {
       const int nr = min(KN / P, w.cnt - tb) * P;  // B rows of the pass (tokens x planes)
-      const int nb = (nr + kBoxRows - 1) / kBoxRows;
+      constexpr int BR = box_rows(P);
+      static_assert(KN % BR == 0, "B boxes of a pass");
+      const int nb = (nr + BR - 1) / BR;
       const int row = (w.pos + tb) * P;
       for (int ks = 0; ks < nks; ++ks, ++g) {
         const uint32_t s = g % G::S, ph = (g / G::S) & 1u;
         if (!wait_or_give_up(&b->empty[s], ph ^ 1u, &b->err)) { ok = false; break; }
         uint64_t* full = &b->full[s];
-        mbar_arrive_expect_tx(full, G::NA * (2 * kAHalfTx + kSfBytes) + nb * kBoxRows * kKS +
-                                        kSfBytes);
+        mbar_arrive_expect_tx(full, G::NA * (kATx + kSfBytes) + nb * BR * kKS + kSfBytes);
         for (int o = 0; o < G::NA; ++o) {
           uint8_t* as = smem + G::offA + ((size_t)s * G::NA + o) * kABytes;
           const ChunkMap* m = o == 0 ? &a.amap0 : &a.amap1;
           const int tile = MODE == 0 ? w.mt : 2 * w.mt + o;  // 128-row tile of the matrix
-          for (int h = 0; h < 2; ++h)
-            tma5d_stream(as + h * (kABytes / 2), m, kHalfRows * h, ks, tile, w.e, full, pol);
+          tma5d_stream(as, m, ks, tile, w.e, full, pol);
           bulk_g2s(smem + G::offSfa + ((size_t)s * G::NA + o) * kSfBytes,
                    span + (o == 0 ? a.sfa0 : a.sfa1) + ((size_t)tile * nks + ks) * kSfBytes,
                    kSfBytes, full, pol);
         }
         uint8_t* bs = smem + G::offB + (size_t)s * G::BBytes;
         for (int i = 0; i < nb; ++i)
-          tma2d(bs + i * kBoxRows * kKS, &a.bmap, ks * kKS, row + kBoxRows * i, full);
+          tma2d(bs + i * BR * kKS, &a.bmap, ks * kKS, row + BR * i, full);
         bulk_plain(smem + G::offSfb + (size_t)s * kSfBytes,
                    a.bsf + ((size_t)ks * a.rows_cap + row) * kSfRowBytes, kSfBytes, full);
         armed |= 1u << s;
@@ -823,8 +828,9 @@ cudaError_t launch_mx8(const Mx8Args& a, int planes, cudaStream_t s) {
 bool mx8_supported(int H, int I) { return H % (2 * kM) == 0 && I % kKS == 0; }
 
 int mx8_rows_cap(int nassign, int planes) {
-  // a stage's token scales are read as 32 rows from the pass's first
-  return nassign * planes + 32;
+  // a stage's token scales are read as 32 rows from the pass's first, its
+  // B rows as box_rows(planes) rows: neither runs past the buffer
+  return nassign * planes + std::max(32, box_rows(planes));
 }
 
 bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E, ChunkMap* gate,
@@ -841,7 +847,7 @@ bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E,
                                 (cuuint64_t)(rows / kM), (cuuint64_t)E};
     const cuuint64_t strides[4] = {(cuuint64_t)kKS / 2, (cuuint64_t)kM * kKS / 2,
                                    (cuuint64_t)K / kKS * kM * kKS / 2, (cuuint64_t)span_bytes};
-    const cuuint32_t box[5] = {kKS, kHalfRows, 1, 1, 1};
+    const cuuint32_t box[5] = {kKS, kM, 1, 1, 1};
     const cuuint32_t es[5] = {1, 1, 1, 1, 1};
     if (enc(reinterpret_cast<CUtensorMap*>(maps[m]), CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 5,
             const_cast<uint8_t*>(arena + offs[m]), dims, strides, box, es,
@@ -852,12 +858,12 @@ bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E,
   return true;
 }
 
-bool make_mx8_row_map(const uint8_t* rows_buf, int rows_cap, int K, ChunkMap* map) {
+bool make_mx8_row_map(const uint8_t* rows_buf, int rows_cap, int K, int planes, ChunkMap* map) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   if (!enc) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows_cap};
   const cuuint64_t strides[1] = {(cuuint64_t)K};
-  const cuuint32_t box[2] = {kKS, kBoxRows};
+  const cuuint32_t box[2] = {kKS, (cuuint32_t)box_rows(planes)};
   const cuuint32_t es[2] = {1, 1};
   return enc(reinterpret_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
              const_cast<uint8_t*>(rows_buf), dims, strides, box, es,
