@@ -104,6 +104,7 @@ struct df_moe {
   uint8_t* mx_xsf = nullptr;  // [H/128][mx_xrows][16]
   uint8_t* mx_hq = nullptr;   // [mx_hrows][I]
   uint8_t* mx_hsf = nullptr;  // [I/128][mx_hrows][16]
+  int32_t* mx_inv = nullptr;  // [Tmax*k] each assignment's position in expert order
   ChunkMap mx_xmap{}, mx_hmap{};
   bool phase = false;  // decode batches run the two phase kernels
   int sms = 0;
@@ -277,7 +278,7 @@ int route(df_moe* h, int l, const uint16_t* x, int T, int32_t* ids, float* w,
   if (!direct)
     RUN(h, K_GROUP, s, launch_group(ids, T, c.top_k, c.n_experts, nullptr,
                                     nullptr, nullptr, nullptr, h->items,
-                                    h->n_items, h->sorted, tg, h->err, s));
+                                    h->n_items, h->sorted, tg, h->err, s, h->mx_inv));
   return DF_MOE_OK;
 }
 
@@ -293,18 +294,19 @@ int expert_gateup(df_moe* h, int l, const uint16_t* x, int T, int max_items, int
   const df_moe_config& c = h->cfg;
   const uint8_t* arena = h->layers[l].arena;
   if (h->mx8) {
-    // block-scaled GEMM on E4M3 x: MXFP8 (h rounded again in its epilogue
-    // for the down GEMM) or x's planes (h exact into hbuf)
+    // block-scaled GEMM on E4M3 x (MXFP8, or x's planes); its epilogue
+    // writes h for the down GEMM (rounded to MXFP8, or as h's planes) and,
+    // when hbuf is given, h before that
     const LayerBufs& L = h->layers[l];
-    RUN(h, K_MX8_QUANT, s, launch_mx8_rows(x, true, c.hidden, c.top_k, h->px, h->items,
-                                           h->n_items, max_items, h->sorted, T * c.top_k,
-                                           c.n_experts, h->mx_xq, h->mx_xsf, h->mx_xrows, h->err,
-                                           s));
+    // (one token selected directly: item q is assignment q, no grouping)
+    RUN(h, K_MX8_QUANT, s, launch_mx8_xrows(x, c.hidden, c.top_k, T,
+                                            tg == 1 ? nullptr : h->mx_inv, h->px, h->mx_xq,
+                                            h->mx_xsf, h->mx_xrows, h->err, s));
     RUN(h, K_MX8_GU, s, launch_mx8_gateup(L.mx_gate, L.mx_up, h->mx_xmap, arena, h->span_bytes,
                                           c.hidden, c.inter, h->mx_xsf, h->mx_xrows, h->items,
                                           h->n_items, max_items, h->sorted, c.n_experts,
-                                          T * c.top_k, hbuf, h->mx_hq, h->mx_hsf, h->px, h->err,
-                                          s));
+                                          T * c.top_k, hbuf, h->mx_hq, h->mx_hsf, h->mx_hrows,
+                                          h->px, h->err, s));
     return DF_MOE_OK;
   }
   if (use_gemm(h, T, tg)) {
@@ -329,12 +331,11 @@ int expert_down(df_moe* h, int l, const float* hbuf, int T, int max_items, int t
   const uint8_t* arena = h->layers[l].arena;
   if (h->mx8) {
     // block-scaled GEMM on E4M3 h: h (when given) rounded to MXFP8 or split
-    // into its planes first; else (MXFP8) the gate/up GEMM's rounded h
+    // into its planes first; else the gate/up GEMM's rounded h or planes
     if (hbuf)
-      RUN(h, K_MX8_QUANT, s, launch_mx8_rows(hbuf, false, c.inter, 1, h->ph, h->items,
-                                             h->n_items, max_items, h->sorted, T * c.top_k,
-                                             c.n_experts, h->mx_hq, h->mx_hsf, h->mx_hrows,
-                                             h->err, s));
+      RUN(h, K_MX8_QUANT, s, launch_mx8_rows(hbuf, c.inter, h->ph, h->items, h->n_items,
+                                             max_items, h->sorted, T * c.top_k, c.n_experts,
+                                             h->mx_hq, h->mx_hsf, h->mx_hrows, h->err, s));
     RUN(h, K_MX8_DN, s, launch_mx8_down(h->layers[l].mx_down, h->mx_hmap, arena, h->span_bytes,
                                         c.hidden, c.inter, h->mx_hsf, h->mx_hrows, h->items,
                                         h->n_items, max_items, h->sorted, c.n_experts,
@@ -516,11 +517,11 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
       rc = shared_part(h, l, x, T, h->ysh, s);
       if (rc) return rc;
     }
-    // (the MXFP8 variant hands h from GEMM to GEMM already rounded)
-    const bool rounded_h = h->mx8 && h->ph == 1;
-    rc = expert_gateup(h, l, x, T, max_items, tg, rounded_h ? nullptr : h->hbuf, s);
+    // (the block-scaled GEMMs hand h from GEMM to GEMM already rounded to
+    // MXFP8 or split into its planes)
+    rc = expert_gateup(h, l, x, T, max_items, tg, h->mx8 ? nullptr : h->hbuf, s);
     if (rc) return rc;
-    rc = expert_down(h, l, rounded_h ? nullptr : h->hbuf, T, max_items, tg, s, 0,
+    rc = expert_down(h, l, h->mx8 ? nullptr : h->hbuf, T, max_items, tg, s, 0,
                      /*after_gateup=*/true);
     if (rc) return rc;
   }
@@ -693,6 +694,7 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
     if (!rc) rc = dalloc(h, &h->mx_xsf, H / 128 * xrows * 16);
     if (!rc) rc = dalloc(h, &h->mx_hq, hrows * I);
     if (!rc) rc = dalloc(h, &h->mx_hsf, I / 128 * hrows * 16);
+    if (!rc) rc = dalloc(h, &h->mx_inv, Tm * k);
     if (!rc && (!make_mx8_row_map(h->mx_xq, h->mx_xrows, c.hidden, h->px, &h->mx_xmap) ||
                 !make_mx8_row_map(h->mx_hq, h->mx_hrows, c.inter, h->ph, &h->mx_hmap)))
       rc = fail(h, DF_MOE_ECUDA, "tensor map encoding failed");
@@ -1163,7 +1165,7 @@ int df_moe_step_expert_gateup(df_moe* h, int32_t layer, const void* x_bf16,
   const int tg = kOneItemPerExpert;
   RUN(h, K_GROUP, s, launch_group(ids, T, c.top_k, c.n_experts, nullptr, nullptr,
                                   nullptr, nullptr, h->items, h->n_items,
-                                  h->sorted, tg, h->err, s));
+                                  h->sorted, tg, h->err, s, h->mx_inv));
   return expert_gateup(h, layer, (const uint16_t*)x_bf16, T,
                        std::min(T * c.top_k, c.n_experts), tg, hbuf, s);
 }

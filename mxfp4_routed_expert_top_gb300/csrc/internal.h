@@ -135,10 +135,13 @@ cudaError_t launch_topk(const float* part, int nsplit, int T, int E, int k,
                         Item* items, int32_t* n_items, int32_t* sorted,
                         cudaStream_t s);
 // ids outside [0, E) are left out and recorded in *err (DEV_ERR_RANGE).
+// inv (optional, [T*k]): the position of assignment a in expert order
+// (sorted[inv[a]] = a), -1 for an assignment left out.
 cudaError_t launch_group(const int32_t* ids, int T, int k, int E,
                          int32_t* offs, int32_t* tok, int32_t* slot,
                          int32_t* n_union, Item* items, int32_t* n_items,
-                         int32_t* sorted, int tg, uint32_t* err, cudaStream_t s);
+                         int32_t* sorted, int tg, uint32_t* err, cudaStream_t s,
+                         int32_t* inv = nullptr);
 // E: experts of the layer, nassign: T * k (range checks of the items).
 cudaError_t launch_gateup(const uint8_t* arena, size_t span_bytes, int H,
                           int I, int k, const uint16_t* x, const Item* items,
@@ -309,30 +312,39 @@ bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E,
 // Tensor map of E4M3 activation rows [rows_cap][K], written as `planes`
 // rows a token or assignment (its box covers one pass of the GEMM).
 bool make_mx8_row_map(const uint8_t* rows, int rows_cap, int K, int planes, ChunkMap* map);
-// Rounds the rows of the items' assignments: row n of item i is source row
-// sorted[pos + n] / div of src (bf16 or fp32, [.][K], 16-byte aligned),
-// written as `planes` E4M3 rows (pos + n) planes + p of q ([rows_cap][K])
-// with their scales in sf ([K/128][rows_cap][16], word q of a row the scales
-// of the row 32 q later). planes: 1, kPlanesX (bf16) or kPlanesH (fp32).
-cudaError_t launch_mx8_rows(const void* src, bool bf16, int K, int div, int planes,
-                            const Item* items, const int32_t* n_items, int max_items,
-                            const int32_t* sorted, int nassign, int E, uint8_t* q, uint8_t* sf,
-                            int rows_cap, uint32_t* err, cudaStream_t s);
+// Rounds h for the down GEMM: row n of item i is source row sorted[pos + n]
+// of src (fp32 [nassign][K], 16-byte aligned), written as `planes` E4M3 rows
+// (pos + n) planes + p of q ([rows_cap][K]) with their scales in sf
+// ([K/128][rows_cap][16], word q of a row the scales of the row 32 q later).
+// planes: 1 or kPlanesH.
+cudaError_t launch_mx8_rows(const float* src, int K, int planes, const Item* items,
+                            const int32_t* n_items, int max_items, const int32_t* sorted,
+                            int nassign, int E, uint8_t* q, uint8_t* sf, int rows_cap,
+                            uint32_t* err, cudaStream_t s);
+// Rounds x (bf16 [T][K], 16-byte aligned, K <= 8192) for the gate/up GEMM:
+// each token once, written to the rows of its k assignments, rows
+// inv[t k + j] planes + p of q, scales as above. inv: the grouping's
+// positions of the assignments (-1: none; null: position = assignment).
+// planes: 1 or kPlanesX.
+cudaError_t launch_mx8_xrows(const uint16_t* x, int K, int k, int T, const int32_t* inv,
+                             int planes, uint8_t* q, uint8_t* sf, int rows_cap, uint32_t* err,
+                             cudaStream_t s);
 // The rounding on plain rows: codes [rows][n], scales [rows][n/32].
 cudaError_t launch_mx8_plain(const float* v, int rows, int n, uint8_t* codes, uint8_t* scales,
                              cudaStream_t s);
 // Canonical spans -> the variant's span layout (inverse: back).
 cudaError_t launch_mx8_layout(const uint8_t* src, uint8_t* dst, int n_spans, int H, int I,
                               size_t span_bytes, int inverse, cudaStream_t s);
-// gate/up on x's planes (1 or kPlanesX). One plane: h rounded to MXFP8
-// into hq/hsf (and, optionally, h before the rounding into hbuf
-// [nassign][I]); planes: h into hbuf.
+// gate/up on x's planes (1 or kPlanesX). h for the down GEMM into hq/hsf
+// (hrows_cap rows): one plane, h rounded to MXFP8; kPlanesX, h as its
+// kPlanesH planes (hq may be null then). hbuf [nassign][I] (optional with
+// one plane or with hq): h before that.
 cudaError_t launch_mx8_gateup(const ChunkMap& gate, const ChunkMap& up, const ChunkMap& xmap,
                               const uint8_t* arena, size_t span_bytes, int H, int I,
                               const uint8_t* xsf, int rows_cap, const Item* items,
                               const int32_t* n_items, int max_items, const int32_t* sorted,
                               int E, int nassign, float* hbuf, uint8_t* hq, uint8_t* hsf,
-                              int planes, uint32_t* err, cudaStream_t s);
+                              int hrows_cap, int planes, uint32_t* err, cudaStream_t s);
 // down on h's planes (1 or kPlanesH): part [nassign][H].
 cudaError_t launch_mx8_down(const ChunkMap& down, const ChunkMap& hmap, const uint8_t* arena,
                             size_t span_bytes, int H, int I, const uint8_t* hsf, int rows_cap,

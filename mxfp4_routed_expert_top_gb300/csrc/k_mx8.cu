@@ -138,8 +138,9 @@ struct Mx8Args {
   const int32_t* sorted;
   int max_items, E, nassign;
   float* hbuf;            // gate/up: optional [nassign][I] h before rounding
-  uint8_t* hq;            // gate/up: [rows_cap][I] E4M3 rows of h (expert order)
-  uint8_t* hsf;           // gate/up: [I/128][rows_cap][16] their scales
+  uint8_t* hq;            // gate/up: [hrows_cap][I] E4M3 rows of h (expert order)
+  uint8_t* hsf;           // gate/up: [I/128][hrows_cap][16] their scales
+  int hrows_cap;          // gate/up: rows of hq
   float* part;            // down: [nassign][H]
   uint32_t* err;
 };
@@ -158,6 +159,13 @@ __device__ __forceinline__ float pow2f(int e) {
 __device__ __forceinline__ int mx8_shared_exp(float amax) {
   if (amax == 0.f) return -127;
   return max(-127, min(127, ilogbf(amax) - 8));
+}
+
+// E4M3 code -> its value (exact).
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)(code | code << 8)));
+  return __half2float(__ushort_as_half((uint16_t)(h2 & 0xFFFFu)));
 }
 
 // E4M3 code of v, nearest with ties to even, |v| beyond 448 saturating.
@@ -424,6 +432,25 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t addr, uint32_t (&v)[KN]) {
   if constexpr (KN % 32 == 16) tmem_ld16(addr + KN - 16, v + KN - 16);
 }
 
+// h of one (assignment, row) of the gate/up epilogue as the down GEMM's
+// kPlanesH E4M3 planes, rows pos * kPlanesH + p of a.hq: the same greedy split
+// as mx8_rows_kernel (plane p is the MXFP8 rounding of what the planes before
+// it left, the remainder exact in fp32); the 32 rows of a warp are one block
+// along I, so the block maximum is a warp maximum. Every lane of the warp
+// calls with the same pos.
+__device__ __forceinline__ void h_planes(const Mx8Args& a, float v, int pos, int r, int blk,
+                                         int lane) {
+#pragma unroll 1
+  for (int p = 0; p < kPlanesH; ++p) {
+    const int sh = mx8_shared_exp(warp_max(fabsf(v)));
+    const uint32_t code = e4m3_rn_sat(v * pow2f(-sh));
+    v -= e4m3_value(code) * pow2f(sh);
+    const int row = pos * kPlanesH + p;
+    a.hq[(size_t)row * a.I + r] = (uint8_t)code;
+    if (lane == 0) put_scale(a.hsf, a.hrows_cap, row, blk, (uint8_t)(sh + 127));
+  }
+}
+
 template <int MODE, int KN, int P>
 __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN>::S, Geo<MODE, KN>::NACC>* b,
                               uint32_t tmem, int warp, int lane) {
@@ -485,7 +512,7 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN>:
               const int sh = mx8_shared_exp(warp_max(fabsf(hv)));
               const int row = w.pos + tb + c0 + n;
               a.hq[(size_t)row * a.I + r] = (uint8_t)e4m3_rn_sat(hv * pow2f(-sh));
-              if (lane == 0) put_scale(a.hsf, a.rows_cap, row, blk, (uint8_t)(sh + 127));
+              if (lane == 0) put_scale(a.hsf, a.hrows_cap, row, blk, (uint8_t)(sh + 127));
             }
           }
         }
@@ -517,7 +544,9 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN>:
           if ((unsigned)aa < (unsigned)a.nassign) {
             if (MODE == 0) {
               const float gt = gs[n];
-              a.hbuf[(size_t)aa * a.I + r] = gt / (1.f + expf(-gt)) * y1;  // silu(gate) * up
+              const float hv = gt / (1.f + expf(-gt)) * y1;  // silu(gate) * up
+              if (a.hbuf) a.hbuf[(size_t)aa * a.I + r] = hv;
+              if (a.hq) h_planes(a, hv, w.pos + tb + n, r, 4 * w.mt + warp, lane);
             } else {
               a.part[(size_t)aa * a.H + r] = gs[n];
               a.part[(size_t)aa * a.H + r + kM] = y1;
@@ -587,27 +616,77 @@ __global__ void __launch_bounds__(kThr, 1) mx8_gemm_kernel(const __grid_constant
                  : "memory");
 }
 
-// E4M3 code -> its value (exact).
-__device__ __forceinline__ float e4m3_value(uint32_t code) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)(code | code << 8)));
-  return __half2float(__ushort_as_half((uint16_t)(h2 & 0xFFFFu)));
+// One 32-element block as P planes (P = 1: its MXFP8 rounding): plane p's
+// codes (8 words, element 4 m + c in byte c of word m) and its shared
+// exponent. Plane p is the MXFP8 rounding of what the planes before it left,
+// each with its own block exponent, and the remainder is exact in fp32 at
+// every step (the value minus its rounding), so the planes' sum reproduces
+// the block up to the last remainder.
+template <int P>
+__device__ __forceinline__ void block_planes(float (&v)[32], uint32_t (&wq)[P][8], int (&sh)[P]) {
+#pragma unroll
+  for (int pl = 0; pl < P; ++pl) {
+    float amax = 0.f;
+#pragma unroll
+    for (int m = 0; m < 32; ++m) amax = fmaxf(amax, fabsf(v[m]));
+    sh[pl] = mx8_shared_exp(amax);
+    const float sc = pow2f(-sh[pl]), back = pow2f(sh[pl]);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t code = e4m3_rn_sat(v[4 * m + c] * sc);
+        word |= code << (8 * c);
+        if (P > 1) v[4 * m + c] -= e4m3_value(code) * back;
+      }
+      wq[pl][m] = word;
+    }
+  }
 }
 
-// Rounds activation rows to MXFP8 into the expert-ordered buffers: block =
-// item, thread j = 32-column block j of each of the item's rows. Row n of
-// item i is source row sorted[pos + n] / div (x: the token; h: the
-// assignment). P = 1: the row rounded to MXFP8, written to q row pos + n.
-// P > 1: the row as P planes, q rows (pos + n) P + p: plane p is the MXFP8
-// rounding of what the planes before it left (each plane with its own block
-// exponent), the remainder exact in fp32 at every step, so the planes' sum
-// reproduces the row up to the last remainder.
-template <bool BF16, int P>
-__global__ void __launch_bounds__(256) mx8_rows_kernel(const void* src, int K, int div,
-                                                       const Item* items, const int32_t* n_items,
-                                                       int max_items, const int32_t* sorted,
-                                                       int nassign, int E, uint8_t* q,
-                                                       uint8_t* sf, int rows_cap, uint32_t* err) {
+// Writes block j of the P rows row0 .. row0 + P - 1 (codes into q [rows][K],
+// the shared exponents into the stage-major scale words of sf). A stage's
+// four scale bytes (blocks 4 ks .. 4 ks + 3, lanes 4 g .. 4 g + 3) form one
+// word, written by the group's first lane to its four places (word q of row
+// - 32 q). Every lane of the warp calls (the words are gathered by shuffles);
+// `live` lanes store.
+template <int P>
+__device__ __forceinline__ void store_planes(uint8_t* q, uint8_t* sf, int K, int rows_cap,
+                                             int row0, int j, int lane, bool live,
+                                             const uint32_t (&wq)[P][8], const int (&sh)[P]) {
+#pragma unroll
+  for (int pl = 0; pl < P; ++pl) {
+    const int row = row0 + pl;
+    if (live) {
+      uint4* d = reinterpret_cast<uint4*>(q + (size_t)row * K + 32 * j);
+      d[0] = make_uint4(wq[pl][0], wq[pl][1], wq[pl][2], wq[pl][3]);
+      d[1] = make_uint4(wq[pl][4], wq[pl][5], wq[pl][6], wq[pl][7]);
+    }
+    const uint32_t b0 = (uint32_t)(sh[pl] + 127);
+    const uint32_t word = b0 | __shfl_down_sync(0xffffffffu, b0, 1) << 8 |
+                          __shfl_down_sync(0xffffffffu, b0, 2) << 16 |
+                          __shfl_down_sync(0xffffffffu, b0, 3) << 24;
+    if (live && (lane & 3) == 0) {
+      const size_t ks = (size_t)(j >> 2);
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq)
+        if (row - 32 * qq >= 0)
+          reinterpret_cast<uint32_t*>(sf)[(ks * rows_cap + row - 32 * qq) * 4 + qq] = word;
+    }
+  }
+}
+
+// fp32 rows (h given by the caller) for the block-scaled down GEMM: block =
+// item, thread = one (row, 32-column block) pair of the item. Row n of item
+// i is source row sorted[pos + n] (an assignment); its P planes go to q rows
+// (pos + n) P + p.
+template <int P>
+__global__ void __launch_bounds__(256) mx8_rows_kernel(const float* src, int K, const Item* items,
+                                                       const int32_t* n_items, int max_items,
+                                                       const int32_t* sorted, int nassign, int E,
+                                                       uint8_t* q, uint8_t* sf, int rows_cap,
+                                                       uint32_t* err) {
   const int i = blockIdx.x;
   int ni = *n_items;
   if (ni > max_items) ni = max_items;
@@ -631,79 +710,76 @@ __global__ void __launch_bounds__(256) mx8_rows_kernel(const void* src, int K, i
     const bool bad = (unsigned)aa >= (unsigned)nassign;
     if (bad && t < total && j == 0) atomicOr(err, DEV_ERR_RANGE);
     const bool live = t < total && !bad;
-    const int srow = live ? aa / div : 0;
-    {
-      float v[32];
-      if (!live) {
+    float v[32];
+    if (live) {
+      const float4* p = reinterpret_cast<const float4*>(src + (size_t)aa * K + 32 * j);
 #pragma unroll
-        for (int m = 0; m < 32; ++m) v[m] = 0.f;
-      } else if (BF16) {
-        const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) +
-                                                        (size_t)srow * K + 32 * j);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 t = p[c];
-          const uint32_t wd[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            v[8 * c + 2 * m] = __uint_as_float(wd[m] << 16);
-            v[8 * c + 2 * m + 1] = __uint_as_float(wd[m] & 0xFFFF0000u);
-          }
-        }
-      } else {
-        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) +
-                                                          (size_t)srow * K + 32 * j);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const float4 t = p[c];
-          v[4 * c] = t.x;
-          v[4 * c + 1] = t.y;
-          v[4 * c + 2] = t.z;
-          v[4 * c + 3] = t.w;
-        }
+      for (int c = 0; c < 8; ++c) {
+        const float4 f = p[c];
+        v[4 * c] = f.x;
+        v[4 * c + 1] = f.y;
+        v[4 * c + 2] = f.z;
+        v[4 * c + 3] = f.w;
       }
-#pragma unroll 1
-      for (int pl = 0; pl < P; ++pl) {
-        float amax = 0.f;
+    } else {
 #pragma unroll
-        for (int m = 0; m < 32; ++m) amax = fmaxf(amax, fabsf(v[m]));
-        const int sh = mx8_shared_exp(amax);
-        const float sc = pow2f(-sh), back = pow2f(sh);
-        uint32_t wq[8];
+      for (int m = 0; m < 32; ++m) v[m] = 0.f;
+    }
+    uint32_t wq[P][8];
+    int sh[P];
+    block_planes<P>(v, wq, sh);
+    store_planes<P>(q, sf, K, rows_cap, (it.pos + n) * P, j, lane, live, wq, sh);
+  }
+}
+
+// x (bf16 [T][K]) for the block-scaled gate/up GEMM, one token a CTA: its P
+// planes (P = 1: its MXFP8 rounding) computed once and written to the rows
+// of each of its k assignments in expert order, q rows inv[t k + j] P + p (an
+// assignment left out of the grouping, inv = -1, gets none; no inv: the
+// position is the assignment). Thread j: 32-column block j (K <= 8192).
+template <int P>
+__global__ void __launch_bounds__(256) mx8_xrows_kernel(const uint16_t* __restrict__ x, int K,
+                                                        int k, const int32_t* __restrict__ inv,
+                                                        int nassign, uint8_t* q, uint8_t* sf,
+                                                        int rows_cap, uint32_t* err) {
+  __shared__ int dst[32];  // the token's positions in expert order (k <= 32)
+  const int t = blockIdx.x;
+  if ((int)threadIdx.x < k) {
+    int p = inv ? inv[t * k + threadIdx.x] : t * k + threadIdx.x;
+    if (p >= nassign || (p >= 0 && (p + 1) * P + max(32, box_rows(P)) > rows_cap)) {
+      atomicOr(err, DEV_ERR_RANGE);
+      p = -1;
+    }
+    dst[threadIdx.x] = p;
+  }
+  __syncthreads();
+  const int nblk = K / 32;
+  const int j = threadIdx.x, lane = j & 31;
+  if ((j & ~31) >= nblk) return;  // a whole warp past the row
+  const bool live = j < nblk;
+  float v[32];
+  if (live) {
+    const uint4* p = reinterpret_cast<const uint4*>(x + (size_t)t * K + 32 * j);
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          uint32_t word = 0;
+    for (int c = 0; c < 4; ++c) {
+      const uint4 u = p[c];
+      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint32_t code = e4m3_rn_sat(v[4 * m + c] * sc);
-            word |= code << (8 * c);
-            // the remainder for the next plane (exact: v minus its rounding)
-            if (P > 1) v[4 * m + c] -= e4m3_value(code) * back;
-          }
-          wq[m] = word;
-        }
-        const int row = (it.pos + n) * P + pl;
-        if (live) {
-          uint4* d = reinterpret_cast<uint4*>(q + (size_t)row * K + 32 * j);
-          d[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-          d[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
-        }
-        // the stage's four scale bytes (blocks 4 ks .. 4 ks + 3, lanes
-        // 4 g .. 4 g + 3) as one word, written by the group's first lane to
-        // its four places (word q of row - 32 q)
-        const uint32_t b0 = (uint32_t)(sh + 127);
-        const uint32_t word = b0 | __shfl_down_sync(0xffffffffu, b0, 1) << 8 |
-                              __shfl_down_sync(0xffffffffu, b0, 2) << 16 |
-                              __shfl_down_sync(0xffffffffu, b0, 3) << 24;
-        if (live && (lane & 3) == 0) {
-          const size_t ks = (size_t)(j >> 2);
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq)
-            if (row - 32 * qq >= 0)
-              reinterpret_cast<uint32_t*>(sf)[(ks * rows_cap + row - 32 * qq) * 4 + qq] = word;
-        }
+      for (int m = 0; m < 4; ++m) {
+        v[8 * c + 2 * m] = __uint_as_float(wd[m] << 16);
+        v[8 * c + 2 * m + 1] = __uint_as_float(wd[m] & 0xFFFF0000u);
       }
     }
+  } else {
+#pragma unroll
+    for (int m = 0; m < 32; ++m) v[m] = 0.f;
+  }
+  uint32_t wq[P][8];
+  int sh[P];
+  block_planes<P>(v, wq, sh);
+  for (int i = 0; i < k; ++i) {
+    const int p = dst[i];
+    if (p >= 0) store_planes<P>(q, sf, K, rows_cap, p * P, j, lane, live, wq, sh);
   }
 }
 
@@ -871,19 +947,32 @@ bool make_mx8_row_map(const uint8_t* rows_buf, int rows_cap, int K, int planes, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_mx8_rows(const void* src, bool bf16, int K, int div, int planes,
-                            const Item* items, const int32_t* n_items, int max_items,
-                            const int32_t* sorted, int nassign, int E, uint8_t* q, uint8_t* sf,
-                            int rows_cap, uint32_t* err, cudaStream_t s) {
+cudaError_t launch_mx8_rows(const float* src, int K, int planes, const Item* items,
+                            const int32_t* n_items, int max_items, const int32_t* sorted,
+                            int nassign, int E, uint8_t* q, uint8_t* sf, int rows_cap,
+                            uint32_t* err, cudaStream_t s) {
   if (max_items <= 0) return cudaSuccess;
   auto go = [&](auto kernel) {
-    kernel<<<max_items, 256, 0, s>>>(src, K, div, items, n_items, max_items, sorted, nassign, E,
-                                     q, sf, rows_cap, err);
+    kernel<<<max_items, 256, 0, s>>>(src, K, items, n_items, max_items, sorted, nassign, E, q,
+                                     sf, rows_cap, err);
     return cudaGetLastError();
   };
-  if (planes == 1) return bf16 ? go(mx8_rows_kernel<true, 1>) : go(mx8_rows_kernel<false, 1>);
-  if (planes == kPlanesX && bf16) return go(mx8_rows_kernel<true, kPlanesX>);
-  if (planes == kPlanesH && !bf16) return go(mx8_rows_kernel<false, kPlanesH>);
+  if (planes == 1) return go(mx8_rows_kernel<1>);
+  if (planes == kPlanesH) return go(mx8_rows_kernel<kPlanesH>);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_mx8_xrows(const uint16_t* x, int K, int k, int T, const int32_t* inv,
+                             int planes, uint8_t* q, uint8_t* sf, int rows_cap, uint32_t* err,
+                             cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  if (K > 32 * 256 || K % 128 || k > 32) return cudaErrorInvalidValue;
+  auto go = [&](auto kernel) {
+    kernel<<<T, 256, 0, s>>>(x, K, k, inv, T * k, q, sf, rows_cap, err);
+    return cudaGetLastError();
+  };
+  if (planes == 1) return go(mx8_xrows_kernel<1>);
+  if (planes == kPlanesX) return go(mx8_xrows_kernel<kPlanesX>);
   return cudaErrorInvalidValue;
 }
 
@@ -909,8 +998,10 @@ cudaError_t launch_mx8_gateup(const ChunkMap& gate, const ChunkMap& up, const Ch
                               const uint8_t* xsf, int rows_cap, const Item* items,
                               const int32_t* n_items, int max_items, const int32_t* sorted,
                               int E, int nassign, float* hbuf, uint8_t* hq, uint8_t* hsf,
-                              int planes, uint32_t* err, cudaStream_t s) {
-  if (planes > 1 && !hbuf) return cudaErrorInvalidValue;  // planes: h goes to hbuf
+                              int hrows_cap, int planes, uint32_t* err, cudaStream_t s) {
+  // one plane: h rounded to MXFP8 (hq); planes: h as fp32 rows (hbuf), as
+  // the down GEMM's planes (hq), or both
+  if (planes == 1 ? !hq : !hbuf && !hq) return cudaErrorInvalidValue;
   const size_t q = (size_t)H * I / 2, sb = (size_t)H * I / 32;
   Mx8Args a{};
   a.amap0 = gate;
@@ -935,6 +1026,7 @@ cudaError_t launch_mx8_gateup(const ChunkMap& gate, const ChunkMap& up, const Ch
   a.hbuf = hbuf;
   a.hq = hq;
   a.hsf = hsf;
+  a.hrows_cap = hrows_cap;
   a.err = err;
   return launch_mx8<0>(a, planes, s);
 }

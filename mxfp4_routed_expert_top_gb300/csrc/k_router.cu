@@ -214,7 +214,8 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 __global__ void __launch_bounds__(1024)
 group_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
              int32_t* offs, int32_t* tok, int32_t* slot, int32_t* n_union,
-             Item* items, int32_t* n_items, int32_t* sorted, int tg, uint32_t* err) {
+             Item* items, int32_t* n_items, int32_t* sorted, int tg, uint32_t* err,
+             int32_t* inv) {
   __shared__ int cnt[1024];
   __shared__ int fill[1024];
   __shared__ int warp_sums[32];
@@ -237,6 +238,7 @@ group_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
   __syncthreads();
   const int c = tid < E ? cnt[tid] : 0;
   const int start = block_exclusive_scan(c, warp_sums, &tot);
+  const int nvalid = tot;  // assignments with an id in range
   if (tid < E) {
     fill[tid] = start;
     if (offs) offs[tid] = start;
@@ -260,7 +262,11 @@ group_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
       sorted[j + 1] = v;
     }
   }
+  if (inv)
+    for (int a = tid; a < A; a += blockDim.x) inv[a] = -1;
   __syncthreads();
+  if (inv)
+    for (int p = tid; p < nvalid; p += blockDim.x) inv[sorted[p]] = p;
   if (tok) {
     for (int p = tid; p < A; p += blockDim.x) {
       tok[p] = sorted[p] / k;
@@ -319,9 +325,10 @@ cudaError_t launch_topk(const float* part, int nsplit, int T, int E, int k,
 cudaError_t launch_group(const int32_t* ids, int T, int k, int E,
                          int32_t* offs, int32_t* tok, int32_t* slot,
                          int32_t* n_union, Item* items, int32_t* n_items,
-                         int32_t* sorted, int tg, uint32_t* err, cudaStream_t s) {
+                         int32_t* sorted, int tg, uint32_t* err, cudaStream_t s,
+                         int32_t* inv) {
   return launch_after_previous(group_kernel, dim3(1), dim3(1024), 0, s, ids, T, k, E, offs, tok,
-                               slot, n_union, items, n_items, sorted, tg, err);
+                               slot, n_union, items, n_items, sorted, tg, err, inv);
 }
 
 }  // namespace dfm

@@ -126,6 +126,31 @@ def test_input_range(small, torch):
     check_out(out32, ref["out"])
 
 
+@pytest.mark.parametrize("T", [5, 40, 100])
+def test_forward_equals_steps(small, torch, T):
+    """The forward hands h from the gate/up GEMM's epilogue to the down GEMM
+    as planes; the down step splits a given fp32 h with the stand-alone
+    routine. Both splits are the same arithmetic, so the forward's output
+    equals, bit for bit, the steps' routed sum plus the shared part (added
+    in fp32, as the forward adds them)."""
+    wl = SMALL
+    x = draw_tokens(small, T, first_id=1200 + T)
+    _, out32, ids, w = _forward(small.m, x, T, torch)
+    xd = to_dev_bf16(x)
+    idd = torch.from_numpy(ids).cuda()
+    wd = torch.from_numpy(w).cuda()
+    hbuf = torch.empty((T * wl.k, wl.I), dtype=torch.float32, device="cuda")
+    small.m.step_expert_gateup(0, xd, T, idd, hbuf)
+    y = torch.empty((T, wl.H), dtype=torch.float32, device="cuda")
+    small.m.step_expert_down(0, hbuf, T, idd, wd, y)
+    ysh = torch.empty((T, wl.H), dtype=torch.float32, device="cuda")
+    small.m.step_shared(0, xd, T, ysh)
+    small.m.sync()
+    want = y.cpu().numpy() + ysh.cpu().numpy()
+    assert want.dtype == np.float32
+    assert np.array_equal(out32.view(np.uint32), want.view(np.uint32))
+
+
 @pytest.fixture(scope="module")
 def k3(torch):
     s = Setup(K3, max_tokens=512, planes=True)
