@@ -181,13 +181,22 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Places a row's scales take in the stage-major, row-interleaved layout of
+// an activation buffer of `planes` rows a token or assignment: word q of row
+// R holds the scales of row R + 32 q, and a GEMM pass reads words q <
+// ceil(pass rows / 32) of the 32 rows from its first (the other words reach
+// no MMA column). Passes hold at most 16 P rows of planes, 64 of one plane.
+__host__ __device__ constexpr int scale_places(int planes) {
+  return planes > 1 ? (16 * planes + 31) / 32 : 2;
+}
+
 // Writes the scale byte of block j (along K) of activation row `row` into
-// the stage-major, row-interleaved layout: stage j/4, byte j mod 4 of word q
-// of row row - 32 q, q = 0..3.
-__device__ __forceinline__ void put_scale(uint8_t* sf, int rows_cap, int row, int j, uint8_t v) {
+// that layout: stage j/4, byte j mod 4 of word q of row row - 32 q, q <
+// places.
+__device__ __forceinline__ void put_scale(uint8_t* sf, int rows_cap, int row, int j, uint8_t v,
+                                          int places) {
   const size_t ks = (size_t)(j >> 2);
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
+  for (int q = 0; q < places; ++q)
     if (row - 32 * q >= 0) sf[((ks * rows_cap + row - 32 * q) * 4 + q) * 4 + (j & 3)] = v;
 }
 
@@ -447,7 +456,8 @@ __device__ __forceinline__ void h_planes(const Mx8Args& a, float v, int pos, int
     v -= e4m3_value(code) * pow2f(sh);
     const int row = pos * kPlanesH + p;
     a.hq[(size_t)row * a.I + r] = (uint8_t)code;
-    if (lane == 0) put_scale(a.hsf, a.hrows_cap, row, blk, (uint8_t)(sh + 127));
+    if (lane == 0)
+      put_scale(a.hsf, a.hrows_cap, row, blk, (uint8_t)(sh + 127), scale_places(kPlanesH));
   }
 }
 
@@ -512,7 +522,8 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN>:
               const int sh = mx8_shared_exp(warp_max(fabsf(hv)));
               const int row = w.pos + tb + c0 + n;
               a.hq[(size_t)row * a.I + r] = (uint8_t)e4m3_rn_sat(hv * pow2f(-sh));
-              if (lane == 0) put_scale(a.hsf, a.hrows_cap, row, blk, (uint8_t)(sh + 127));
+              if (lane == 0)
+                put_scale(a.hsf, a.hrows_cap, row, blk, (uint8_t)(sh + 127), scale_places(1));
             }
           }
         }
@@ -645,34 +656,40 @@ __device__ __forceinline__ void block_planes(float (&v)[32], uint32_t (&wq)[P][8
   }
 }
 
-// Writes block j of the P rows row0 .. row0 + P - 1 (codes into q [rows][K],
-// the shared exponents into the stage-major scale words of sf). A stage's
-// four scale bytes (blocks 4 ks .. 4 ks + 3, lanes 4 g .. 4 g + 3) form one
-// word, written by the group's first lane to its four places (word q of row
-// - 32 q). Every lane of the warp calls (the words are gathered by shuffles);
-// `live` lanes store.
+// A stage's four scale bytes of each plane (blocks 4 ks .. 4 ks + 3, held
+// by lanes 4 g .. 4 g + 3) as one word, in the group's first lane. Every lane
+// of the warp calls.
+template <int P>
+__device__ __forceinline__ void stage_words(const int (&sh)[P], uint32_t (&sw)[P]) {
+#pragma unroll
+  for (int pl = 0; pl < P; ++pl) {
+    const uint32_t b0 = (uint32_t)(sh[pl] + 127);
+    sw[pl] = b0 | __shfl_down_sync(0xffffffffu, b0, 1) << 8 |
+             __shfl_down_sync(0xffffffffu, b0, 2) << 16 |
+             __shfl_down_sync(0xffffffffu, b0, 3) << 24;
+  }
+}
+
+// Writes block j of the P rows row0 .. row0 + P - 1: the codes into q
+// [rows][K], and (the group's first lane) the stage words into their places
+// in sf (word q of row - 32 q, q < scale_places(P)).
 template <int P>
 __device__ __forceinline__ void store_planes(uint8_t* q, uint8_t* sf, int K, int rows_cap,
-                                             int row0, int j, int lane, bool live,
-                                             const uint32_t (&wq)[P][8], const int (&sh)[P]) {
+                                             int row0, int j, int lane,
+                                             const uint32_t (&wq)[P][8],
+                                             const uint32_t (&sw)[P]) {
+  const size_t ks = (size_t)(j >> 2);
 #pragma unroll
   for (int pl = 0; pl < P; ++pl) {
     const int row = row0 + pl;
-    if (live) {
-      uint4* d = reinterpret_cast<uint4*>(q + (size_t)row * K + 32 * j);
-      d[0] = make_uint4(wq[pl][0], wq[pl][1], wq[pl][2], wq[pl][3]);
-      d[1] = make_uint4(wq[pl][4], wq[pl][5], wq[pl][6], wq[pl][7]);
-    }
-    const uint32_t b0 = (uint32_t)(sh[pl] + 127);
-    const uint32_t word = b0 | __shfl_down_sync(0xffffffffu, b0, 1) << 8 |
-                          __shfl_down_sync(0xffffffffu, b0, 2) << 16 |
-                          __shfl_down_sync(0xffffffffu, b0, 3) << 24;
-    if (live && (lane & 3) == 0) {
-      const size_t ks = (size_t)(j >> 2);
+    uint4* d = reinterpret_cast<uint4*>(q + (size_t)row * K + 32 * j);
+    d[0] = make_uint4(wq[pl][0], wq[pl][1], wq[pl][2], wq[pl][3]);
+    d[1] = make_uint4(wq[pl][4], wq[pl][5], wq[pl][6], wq[pl][7]);
+    if ((lane & 3) == 0) {
 #pragma unroll
-      for (int qq = 0; qq < 4; ++qq)
+      for (int qq = 0; qq < scale_places(P); ++qq)
         if (row - 32 * qq >= 0)
-          reinterpret_cast<uint32_t*>(sf)[(ks * rows_cap + row - 32 * qq) * 4 + qq] = word;
+          reinterpret_cast<uint32_t*>(sf)[(ks * rows_cap + row - 32 * qq) * 4 + qq] = sw[pl];
     }
   }
 }
@@ -728,7 +745,9 @@ __global__ void __launch_bounds__(256) mx8_rows_kernel(const float* src, int K, 
     uint32_t wq[P][8];
     int sh[P];
     block_planes<P>(v, wq, sh);
-    store_planes<P>(q, sf, K, rows_cap, (it.pos + n) * P, j, lane, live, wq, sh);
+    uint32_t sw[P];
+    stage_words<P>(sh, sw);
+    if (live) store_planes<P>(q, sf, K, rows_cap, (it.pos + n) * P, j, lane, wq, sw);
   }
 }
 
@@ -736,9 +755,10 @@ __global__ void __launch_bounds__(256) mx8_rows_kernel(const float* src, int K, 
 // planes (P = 1: its MXFP8 rounding) computed once and written to the rows
 // of each of its k assignments in expert order, q rows inv[t k + j] P + p (an
 // assignment left out of the grouping, inv = -1, gets none; no inv: the
-// position is the assignment). Thread j: 32-column block j (K <= 8192).
+// position is the assignment). Thread j of column group y: 32-column block
+// 128 y + j.
 template <int P>
-__global__ void __launch_bounds__(256) mx8_xrows_kernel(const uint16_t* __restrict__ x, int K,
+__global__ void __launch_bounds__(128) mx8_xrows_kernel(const uint16_t* __restrict__ x, int K,
                                                         int k, const int32_t* __restrict__ inv,
                                                         int nassign, uint8_t* q, uint8_t* sf,
                                                         int rows_cap, uint32_t* err) {
@@ -754,7 +774,7 @@ __global__ void __launch_bounds__(256) mx8_xrows_kernel(const uint16_t* __restri
   }
   __syncthreads();
   const int nblk = K / 32;
-  const int j = threadIdx.x, lane = j & 31;
+  const int j = 128 * blockIdx.y + threadIdx.x, lane = threadIdx.x & 31;
   if ((j & ~31) >= nblk) return;  // a whole warp past the row
   const bool live = j < nblk;
   float v[32];
@@ -777,9 +797,12 @@ __global__ void __launch_bounds__(256) mx8_xrows_kernel(const uint16_t* __restri
   uint32_t wq[P][8];
   int sh[P];
   block_planes<P>(v, wq, sh);
+  uint32_t sw[P];
+  stage_words<P>(sh, sw);
+  if (!live) return;
   for (int i = 0; i < k; ++i) {
     const int p = dst[i];
-    if (p >= 0) store_planes<P>(q, sf, K, rows_cap, p * P, j, lane, live, wq, sh);
+    if (p >= 0) store_planes<P>(q, sf, K, rows_cap, p * P, j, lane, wq, sw);
   }
 }
 
@@ -966,9 +989,10 @@ cudaError_t launch_mx8_xrows(const uint16_t* x, int K, int k, int T, const int32
                              int planes, uint8_t* q, uint8_t* sf, int rows_cap, uint32_t* err,
                              cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  if (K > 32 * 256 || K % 128 || k > 32) return cudaErrorInvalidValue;
+  if (K % 128 || k > 32) return cudaErrorInvalidValue;
+  const dim3 grid(T, (K / 32 + 127) / 128);
   auto go = [&](auto kernel) {
-    kernel<<<T, 256, 0, s>>>(x, K, k, inv, T * k, q, sf, rows_cap, err);
+    kernel<<<grid, 128, 0, s>>>(x, K, k, inv, T * k, q, sf, rows_cap, err);
     return cudaGetLastError();
   };
   if (planes == 1) return go(mx8_xrows_kernel<1>);
