@@ -210,11 +210,19 @@ DF_MOE_API int df_moe_forward_trace(df_moe* h, const void* x_bf16, int32_t T,
                          float* weights, void* trace_x, void* trace_xn,
                          void* stream);
 
-/* Same, with HOST buffers: copies x (and residual) to the device, runs the
- * forward, copies the results back and synchronises `stream` before
- * returning. out_f32, residual, ids and weights may be NULL. Errors as
- * df_moe_forward, and also ETIMEOUT / EDEVICE recorded by this call's own
- * kernels (checked after the synchronisation; the error is then cleared). */
+/* Same, with HOST buffers: moves x (and residual) to the device, runs the
+ * forward, brings the results back and synchronises `stream` before
+ * returning. The device moves the data itself: a small copy kernel reads the
+ * inputs from pinned host memory (the caller's buffer when it is pinned and
+ * mapped with a 16-byte-aligned device address, else a pinned staging copy
+ * the handle makes on first use), and the last kernel writes the output,
+ * ids and weights into pinned host memory (the caller's, or the staging,
+ * copied out after the synchronisation). Pinned caller buffers save the
+ * staging copies. Buffers in device or managed memory are also accepted
+ * (moved with cudaMemcpyAsync). out_f32, residual, ids and weights may be
+ * NULL. Errors as df_moe_forward, ENOMEM if the staging cannot be made, and
+ * ETIMEOUT / EDEVICE recorded by this call's own kernels (checked after the
+ * synchronisation; the error is then cleared). */
 DF_MOE_API int df_moe_forward_host(df_moe* h, const uint16_t* x_bf16, int32_t T,
                         const uint16_t* residual_bf16, uint16_t* out_bf16,
                         float* out_f32, int32_t* ids, float* weights,

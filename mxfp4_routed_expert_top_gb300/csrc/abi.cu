@@ -124,6 +124,12 @@ struct df_moe {
   float* hout32 = nullptr;
   int32_t* hids = nullptr;
   float* hw = nullptr;
+  // host-API staging in pinned, device-mapped host memory (made on first
+  // use): x, residual, out, out_f32, ids, weights, at io_off[] (host view
+  // io_h, device view io_d)
+  uint8_t* io_h = nullptr;
+  uint8_t* io_d = nullptr;
+  size_t io_off[6] = {0, 0, 0, 0, 0, 0};
   // staging for host-sourced spans
   uint8_t* staging = nullptr;
   size_t staging_spans = 0;
@@ -452,9 +458,12 @@ int cache_plan(df_moe* h, int l, int T, const int32_t* ids, cudaStream_t s) {
   return DF_MOE_OK;
 }
 
+// ids_host / w_host (or null): where the combine also copies this layer's
+// selection (host memory the device writes directly).
 int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
                   const uint16_t* residual, uint16_t* out_bf16, float* out_f32,
-                  int32_t* ids, float* w, cudaStream_t s) {
+                  int32_t* ids, float* w, cudaStream_t s, int32_t* ids_host = nullptr,
+                  float* w_host = nullptr) {
   const df_moe_config& c = h->cfg;
   const LayerBufs& L = h->layers[l];
   const int tg = T == 1 ? 1 : kOneItemPerExpert;
@@ -527,7 +536,8 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
   }
   RUN(h, K_COMBINE, s, launch_combine(h->part, w, T, c.top_k, c.hidden,
                                       c.n_shared > 0 ? h->ysh : nullptr,
-                                      residual, out_f32, out_bf16, h->err, h->err_mirror_d, s));
+                                      residual, out_f32, out_bf16, h->err, h->err_mirror_d, s,
+                                      ids, ids_host, w_host));
   return DF_MOE_OK;
 }
 
@@ -978,7 +988,8 @@ static bool mirror_set(const df_moe* h) {
 static int forward_impl(df_moe* h, const void* x_bf16, int32_t T,
                         const void* residual_bf16, void* out_bf16, float* out_f32,
                         int32_t* ids, float* weights, uint16_t* trace_x,
-                        uint16_t* trace_xn, void* stream);
+                        uint16_t* trace_xn, void* stream, int32_t* ids_host = nullptr,
+                        float* w_host = nullptr);
 
 int df_moe_forward(df_moe* h, const void* x_bf16, int32_t T,
                    const void* residual_bf16, void* out_bf16, float* out_f32,
@@ -1000,7 +1011,8 @@ int df_moe_forward_trace(df_moe* h, const void* x_bf16, int32_t T, void* out_bf1
 static int forward_impl(df_moe* h, const void* x_bf16, int32_t T,
                         const void* residual_bf16, void* out_bf16, float* out_f32,
                         int32_t* ids, float* weights, uint16_t* trace_x,
-                        uint16_t* trace_xn, void* stream) {
+                        uint16_t* trace_xn, void* stream, int32_t* ids_host,
+                        float* w_host) {
   if (!h) return fail(nullptr, DF_MOE_EINVAL, "null handle");
   const df_moe_config& c = h->cfg;
   h->launches = 0;
@@ -1027,7 +1039,7 @@ static int forward_impl(df_moe* h, const void* x_bf16, int32_t T,
   if (!stack) {
     return layer_forward(h, 0, (const uint16_t*)x_bf16, T,
                          (const uint16_t*)residual_bf16, (uint16_t*)out_bf16,
-                         out_f32, ids, weights, s);
+                         out_f32, ids, weights, s, ids_host, w_host);
   }
   const uint16_t* cur = (const uint16_t*)x_bf16;
   const size_t TH = (size_t)T * c.hidden;
@@ -1041,13 +1053,70 @@ static int forward_impl(df_moe* h, const void* x_bf16, int32_t T,
     const bool last = l == c.n_layers - 1;
     uint16_t* nxt = last ? (uint16_t*)out_bf16 : h->xbuf[l & 1];
     int rc = layer_forward(h, l, h->xn, T, cur, nxt, last ? out_f32 : nullptr,
-                           ids + (size_t)l * Tk, weights + (size_t)l * Tk, s);
+                           ids + (size_t)l * Tk, weights + (size_t)l * Tk, s,
+                           ids_host ? ids_host + (size_t)l * Tk : nullptr,
+                           w_host ? w_host + (size_t)l * Tk : nullptr);
     if (rc) return rc;
     cur = nxt;
   }
   return DF_MOE_OK;
 }
 
+namespace {
+
+// Where a host-API buffer lives: pinned host memory the device reaches
+// directly (its device address, 16-byte aligned), ordinary host memory, or
+// memory the device owns (device or managed).
+enum class Mem { pinned, host, device };
+Mem classify(const void* p, void** dev) {
+  cudaPointerAttributes a{};
+  *dev = nullptr;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return Mem::host;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer && aligned16(a.devicePointer)) {
+    *dev = a.devicePointer;
+    return Mem::pinned;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return Mem::device;
+  return Mem::host;
+}
+
+int ensure_io(df_moe* h) {
+  if (h->io_h) return DF_MOE_OK;
+  const df_moe_config& c = h->cfg;
+  const size_t n = (size_t)c.max_tokens * c.hidden, nk = (size_t)c.n_layers * c.max_tokens * c.top_k;
+  const size_t sz[6] = {n * 2, n * 2, n * 2, n * 4, nk * 4, nk * 4};
+  size_t off = 0;
+  for (int i = 0; i < 6; ++i) {
+    h->io_off[i] = off;
+    off += (sz[i] + 255) / 256 * 256;
+  }
+  void* hp = nullptr;
+  if (cudaHostAlloc(&hp, off, cudaHostAllocPortable | cudaHostAllocMapped) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(h, DF_MOE_ENOMEM, "pinned host staging of %zu bytes failed", off);
+  }
+  void* dp = nullptr;
+  if (cudaHostGetDevicePointer(&dp, hp, 0) != cudaSuccess) {
+    cudaFreeHost(hp);
+    return fail(h, DF_MOE_ECUDA, "host staging not mapped into the device");
+  }
+  h->host_allocs.push_back(hp);
+  h->io_h = static_cast<uint8_t*>(hp);
+  h->io_d = static_cast<uint8_t*>(dp);
+  return DF_MOE_OK;
+}
+
+}  // namespace
+
+// Host buffers in and out. The device moves the data itself: inputs are read
+// from pinned host memory (the caller's, when it is pinned and mapped, else a
+// staging copy) by a small copy kernel that the router's weight stream
+// overlaps; the last kernel writes the output, ids and weights straight into
+// pinned host memory. Buffers in device or managed memory go through
+// cudaMemcpyAsync.
 int df_moe_forward_host(df_moe* h, const uint16_t* x_bf16, int32_t T,
                         const uint16_t* residual_bf16, uint16_t* out_bf16,
                         float* out_f32, int32_t* ids, float* weights,
@@ -1059,24 +1128,66 @@ int df_moe_forward_host(df_moe* h, const uint16_t* x_bf16, int32_t T,
   if (T < 1 || T > c.max_tokens)
     return fail(h, DF_MOE_ERANGE, "T = %d outside [1, %d]", T, c.max_tokens);
   CUDA_OR_FAIL(h, cudaSetDevice(h->device));
+  int rc = ensure_io(h);
+  if (rc) return rc;
   cudaStream_t s = (cudaStream_t)stream;
   const size_t n = (size_t)T * c.hidden;
   const size_t nk = (size_t)c.n_layers * T * c.top_k;
-  CUDA_OR_FAIL(h, cudaMemcpyAsync(h->hx, x_bf16, n * 2, cudaMemcpyHostToDevice, s));
-  if (residual_bf16)
-    CUDA_OR_FAIL(h, cudaMemcpyAsync(h->hres, residual_bf16, n * 2,
-                                    cudaMemcpyHostToDevice, s));
-  int rc = df_moe_forward(h, h->hx, T, residual_bf16 ? h->hres : nullptr, h->hout,
-                          out_f32 ? h->hout32 : nullptr, h->hids, h->hw, stream);
+  // inputs into the device buffers
+  const void* in_src[2] = {x_bf16, residual_bf16};
+  uint16_t* in_dst[2] = {h->hx, h->hres};
+  for (int i = 0; i < 2; ++i) {
+    if (!in_src[i]) continue;
+    void* dev = nullptr;
+    switch (classify(in_src[i], &dev)) {
+      case Mem::pinned:
+        RUN(h, K_OTHER, s, launch_copy16(dev, in_dst[i], n * 2, s));
+        break;
+      case Mem::host:
+        memcpy(h->io_h + h->io_off[i], in_src[i], n * 2);
+        RUN(h, K_OTHER, s, launch_copy16(h->io_d + h->io_off[i], in_dst[i], n * 2, s));
+        break;
+      case Mem::device:
+        CUDA_OR_FAIL(h, cudaMemcpyAsync(in_dst[i], in_src[i], n * 2, cudaMemcpyDefault, s));
+        break;
+    }
+  }
+  // outputs: written by the device where it reaches them directly
+  void* const user_out[4] = {out_bf16, out_f32, ids, weights};
+  const size_t out_bytes[4] = {n * 2, n * 4, nk * 4, nk * 4};
+  void* dev_side[4] = {h->hout, h->hout32, h->hids, h->hw};  // device buffers
+  void* out_dev[4] = {nullptr, nullptr, nullptr, nullptr};   // what the kernels write
+  Mem kind[4] = {Mem::device, Mem::device, Mem::device, Mem::device};
+  for (int i = 0; i < 4; ++i) {
+    if (!user_out[i]) continue;
+    void* dev = nullptr;
+    kind[i] = classify(user_out[i], &dev);
+    out_dev[i] = kind[i] == Mem::pinned ? dev
+                 : kind[i] == Mem::host ? h->io_d + h->io_off[2 + i]
+                                        : dev_side[i];
+  }
+  // out and out_f32 are the forward's outputs; ids and weights stay in the
+  // device buffers the later kernels read, and the combine copies them
+  const bool ids_direct = ids && weights && kind[2] != Mem::device && kind[3] != Mem::device;
+  rc = forward_impl(h, h->hx, T, residual_bf16 ? h->hres : nullptr,
+                    out_dev[0], out_f32 ? static_cast<float*>(out_dev[1]) : nullptr, h->hids,
+                    h->hw, nullptr, nullptr, stream,
+                    ids_direct ? static_cast<int32_t*>(out_dev[2]) : nullptr,
+                    ids_direct ? static_cast<float*>(out_dev[3]) : nullptr);
   if (rc) return rc;
-  CUDA_OR_FAIL(h, cudaMemcpyAsync(out_bf16, h->hout, n * 2, cudaMemcpyDeviceToHost, s));
-  if (out_f32)
-    CUDA_OR_FAIL(h, cudaMemcpyAsync(out_f32, h->hout32, n * 4, cudaMemcpyDeviceToHost, s));
-  if (ids)
-    CUDA_OR_FAIL(h, cudaMemcpyAsync(ids, h->hids, nk * 4, cudaMemcpyDeviceToHost, s));
-  if (weights)
-    CUDA_OR_FAIL(h, cudaMemcpyAsync(weights, h->hw, nk * 4, cudaMemcpyDeviceToHost, s));
+  for (int i = 0; i < 4; ++i) {
+    if (!user_out[i]) continue;
+    const bool direct = i < 2 ? kind[i] != Mem::device : ids_direct;
+    if (!direct)
+      CUDA_OR_FAIL(h, cudaMemcpyAsync(user_out[i], dev_side[i], out_bytes[i], cudaMemcpyDefault,
+                                      s));
+  }
   CUDA_OR_FAIL(h, cudaStreamSynchronize(s));
+  for (int i = 0; i < 4; ++i) {
+    if (!user_out[i] || kind[i] != Mem::host) continue;
+    if (i >= 2 && !ids_direct) continue;
+    memcpy(user_out[i], h->io_h + h->io_off[2 + i], out_bytes[i]);
+  }
   // this call's own device-side errors (published by its last kernel)
   if (mirror_set(h)) return report_device_error(h, s);
   return DF_MOE_OK;

@@ -158,11 +158,17 @@ cudaError_t launch_down(const uint8_t* arena, size_t span_bytes, int H, int I,
                         uint32_t* err, cudaStream_t s, int max_ctas = 0,
                         bool after_gateup = false);
 // err_mirror (or null): the host-visible copy of the error word, written when
-// the word is nonzero.
+// the word is nonzero. ids_out / w_out (or null; k <= 128): copies of the
+// selection ids [T][k] and weights w (host memory the device writes
+// directly, for the host-buffer forward).
 cudaError_t launch_combine(const float* part, const float* w, int T, int k,
                            int H, const float* ysh, const uint16_t* residual,
                            float* out_f32, uint16_t* out_bf16, uint32_t* err,
-                           uint32_t* err_mirror, cudaStream_t s);
+                           uint32_t* err_mirror, cudaStream_t s, const int32_t* ids = nullptr,
+                           int32_t* ids_out = nullptr, float* w_out = nullptr);
+// A 16-byte-aligned copy of `bytes` (a multiple of 16) by a small kernel,
+// e.g. from host memory the device reads directly into device memory.
+cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t s);
 cudaError_t launch_shared_gateup(const uint16_t* gate, const uint16_t* up,
                                  int R, int H, const uint16_t* x, int T,
                                  float* hsh, uint32_t* err, cudaStream_t s,

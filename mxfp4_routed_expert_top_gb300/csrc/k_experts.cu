@@ -1,6 +1,8 @@
 // k_experts.cu — the routed-expert kernels: MXFP4 dequant-fused gate/up GEMV
 // with SwiGLU epilogue, down GEMV (stand-alone launches of the per-CTA
 // function in mxv.cuh), and the weighted combine.
+#include <algorithm>
+
 #include "mxv.cuh"
 
 namespace dfm {
@@ -17,19 +19,29 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) mxv_kernel(const MxvArgs a)
 // Every load of a thread is issued before the first FMA (one L2 round trip);
 // the sum runs in slot order. The last kernel of a batch forward: its first
 // thread copies the device error word, complete once the kernels before it
-// are, to the host-visible mirror.
+// are, to the host-visible mirror; with ids_out, block (0, t) also copies
+// token t's ids and weights there (host memory the device writes directly).
 constexpr int kCombineThreads = 128;
+__device__ __forceinline__ void copy_selection(const int32_t* ids, const float* w, int k, int t,
+                                               int32_t* ids_out, float* w_out) {
+  if (ids_out && blockIdx.x == 0 && (int)threadIdx.x < k) {
+    const size_t i = (size_t)t * k + threadIdx.x;
+    ids_out[i] = ids[i];
+    w_out[i] = w[i];
+  }
+}
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const float* __restrict__ part, const float* __restrict__ w, int k, int H,
                const float* __restrict__ ysh, const uint16_t* __restrict__ residual,
                float* __restrict__ out_f32, uint16_t* __restrict__ out_bf16, uint32_t* err,
-               uint32_t* err_mirror) {
+               uint32_t* err_mirror, const int32_t* ids, int32_t* ids_out, float* w_out) {
   pdl_wait();
   if (err_mirror && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
     const uint32_t e = atomicOr(err, 0u);
     if (e) *reinterpret_cast<volatile uint32_t*>(err_mirror) = e;
   }
   const int t = blockIdx.y;
+  copy_selection(ids, w, k, t, ids_out, w_out);
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= H) return;
   float pv[32], wv[32];
@@ -57,13 +69,14 @@ __global__ void __launch_bounds__(kCombineThreads)
 combine4_kernel(const float* __restrict__ part, const float* __restrict__ w, int k, int H,
                 const float* __restrict__ ysh, const uint16_t* __restrict__ residual,
                 float* __restrict__ out_f32, uint16_t* __restrict__ out_bf16, uint32_t* err,
-                uint32_t* err_mirror) {
+                uint32_t* err_mirror, const int32_t* ids, int32_t* ids_out, float* w_out) {
   pdl_wait();
   if (blockIdx.x == 0 && blockIdx.y == 0 && err_mirror && threadIdx.x == 0) {
     const uint32_t e = atomicOr(err, 0u);
     if (e) *reinterpret_cast<volatile uint32_t*>(err_mirror) = e;
   }
   const int t = blockIdx.y;
+  copy_selection(ids, w, k, t, ids_out, w_out);
   const int j = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
   if (j >= H) return;
   // slots in groups of eight: a group's loads are issued together, the sums
@@ -178,18 +191,41 @@ cudaError_t launch_down(const uint8_t* arena, size_t span_bytes, int H, int I,
 cudaError_t launch_combine(const float* part, const float* w, int T, int k,
                            int H, const float* ysh, const uint16_t* residual,
                            float* out_f32, uint16_t* out_bf16, uint32_t* err,
-                           uint32_t* err_mirror, cudaStream_t s) {
+                           uint32_t* err_mirror, cudaStream_t s, const int32_t* ids,
+                           int32_t* ids_out, float* w_out) {
+  if (ids_out && (!ids || !w_out || k > kCombineThreads)) return cudaErrorInvalidValue;
   const auto al16 = [](const void* p) { return ((uintptr_t)p & 15) == 0; };
   if (T > 8 && H % 4 == 0 && al16(part) && (!ysh || al16(ysh)) && (!out_f32 || al16(out_f32)) &&
       (!residual || ((uintptr_t)residual & 7) == 0) && (!out_bf16 || ((uintptr_t)out_bf16 & 7) == 0)) {
     // batches: four columns a thread
     dim3 grid((H / 4 + kCombineThreads - 1) / kCombineThreads, T);
     return launch_after_previous(combine4_kernel, grid, dim3(kCombineThreads), 0, s, part, w, k,
-                                 H, ysh, residual, out_f32, out_bf16, err, err_mirror);
+                                 H, ysh, residual, out_f32, out_bf16, err, err_mirror, ids,
+                                 ids_out, w_out);
   }
   dim3 grid((H + kCombineThreads - 1) / kCombineThreads, T);
   return launch_after_previous(combine_kernel, grid, dim3(kCombineThreads), 0, s, part, w, k, H, ysh,
-                               residual, out_f32, out_bf16, err, err_mirror);
+                               residual, out_f32, out_bf16, err, err_mirror, ids, ids_out, w_out);
+}
+
+// Plain 16-byte copy (an input staged in host memory that the device reads
+// directly, to its device buffer). An ordinary launch: the next kernel's
+// programmatic wait covers this whole grid.
+__global__ void __launch_bounds__(256) copy16_kernel(const uint4* __restrict__ src,
+                                                     uint4* __restrict__ dst, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
+cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t s) {
+  if (((uintptr_t)src | (uintptr_t)dst | bytes) & 15) return cudaErrorInvalidValue;
+  const size_t n = bytes / 16;
+  if (!n) return cudaSuccess;
+  const int blocks = (int)std::min<size_t>((n + 255) / 256, 64);
+  copy16_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
+                                       n);
+  return cudaGetLastError();
 }
 
 }  // namespace dfm

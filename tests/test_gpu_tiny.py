@@ -182,6 +182,46 @@ def test_forward_host_buffers(tiny, torch):
     check_out(out32, ref["out"])
 
 
+@pytest.mark.parametrize("kind", ["numpy", "pinned", "device", "mixed"])
+@pytest.mark.parametrize("T", [3, 12])
+def test_forward_host_buffer_kinds(tiny, torch, kind, T):
+    """The host-buffer forward moves data on the device where it can (pinned
+    host memory: a copy kernel in, the last kernel writes out), through a
+    staging copy for ordinary host memory, by cudaMemcpyAsync for device
+    memory; every way gives the device forward's bits."""
+    x = draw_tokens(tiny, T, first_id=7300 + T)
+    d = [torch.empty((T, WL.H), dtype=torch.int16, device="cuda"),
+         torch.empty((T, WL.H), dtype=torch.float32, device="cuda"),
+         torch.empty((T, WL.k), dtype=torch.int32, device="cuda"),
+         torch.empty((T, WL.k), dtype=torch.float32, device="cuda")]
+    tiny.m.forward(to_dev_bf16(x), T, d[0], d[2], d[3], out_f32=d[1])
+    tiny.m.sync()
+    want = [t.cpu().numpy() for t in d]   # the device forward's out, out32, ids, w
+
+    def buf(shape, dtype, k):
+        a = np.zeros(shape, dtype=dtype)
+        if k == "numpy":
+            return a, lambda b: b
+        t = torch.from_numpy(a)
+        t = t.pin_memory() if k == "pinned" else t.cuda()
+        return t, lambda b: b.cpu().numpy()
+    kinds = {"mixed": ["pinned", "numpy", "device", "pinned", "numpy"]}.get(kind, [kind] * 5)
+    xb, _ = buf((T, WL.H), np.int16, kinds[0])
+    if kind == "numpy" or kinds[0] == "numpy":
+        xb[...] = x.view(np.int16)
+    else:
+        xb.copy_(torch.from_numpy(x.view(np.int16)))
+    out, g0 = buf((T, WL.H), np.int16, kinds[1])
+    out32, g1 = buf((T, WL.H), np.float32, kinds[2])
+    ids, g2 = buf((T, WL.k), np.int32, kinds[3])
+    w, g3 = buf((T, WL.k), np.float32, kinds[4])
+    tiny.m.forward_host(xb, T, out, ids=ids, weights=w, out_f32=out32)
+    got = (g0(out), g1(out32), g2(ids), g3(w))
+    for a, b in zip(got, want):
+        assert a.shape == b.shape and a.dtype == b.dtype
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
 def test_forward_is_deterministic(tiny, torch):
     x = draw_tokens(tiny, 16, first_id=8000)
     a = _forward(tiny.m, x, 16, torch)
