@@ -70,23 +70,35 @@ constexpr int kABytes = kM * kKS;         // 16384: one A operand (a byte a code
 constexpr int kATx = kM * kKS / 2;       // 8192: an A operand's codes as copied (packed)
 constexpr int kSfBytes = 512;            // a stage's scale chunk (an operand's, or the tokens')
 constexpr int kSfRowBytes = 16;           // an activation row's scale words
-constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemCols = 512;  // an SM's tensor memory
 // B rows a TMA box: a whole pass of exact planes (16 tokens x P planes) in
 // one box, 32 rows for one plane (passes of 32 or 64 rows). A box may run
 // past the pass into the next item's rows (or past the buffer: zero fill);
 // the MMA columns there are never read.
 __host__ __device__ constexpr int box_rows(int planes) { return planes > 1 ? 16 * planes : 32; }
 
-// Per GEMM and token tile KN (tokens a pass at most, 32 or 64): A operands
-// a stage (gate/up: gate and up), the stages that fit in shared memory, the
-// accumulator sets that fit in tensor memory beside the stages' scales, and
-// the layout of one stage in shared memory and of the tensor memory columns.
-template <int MODE, int KN>
+// CTAs an SM runs of each GEMM. Two CTAs (each with half the shared and
+// tensor memory) issue the copies from two producer lanes, which measured
+// 9-11% faster on the MXFP8 GEMMs and on the planes' down GEMM at batch 512;
+// the planes' gate/up (whose epilogue also splits h) keeps one CTA with more
+// accumulator sets (two CTAs left it one, and it ran 8% slower).
+__host__ __device__ constexpr int ctas_per_sm(int mode, int planes) {
+  return mode == 0 && planes > 1 ? 1 : 2;
+}
+
+// Per GEMM, token tile KN (tokens a pass at most) and planes P: A operands
+// a stage (gate/up: gate and up), the stages that fit in the CTA's share of
+// shared memory, the accumulator sets that fit in its share of tensor memory
+// beside the stages' scales, and the layout of one stage in shared memory
+// and of the tensor memory columns.
+template <int MODE, int KN, int P>
 struct Geo {
+  static constexpr int CPS = ctas_per_sm(MODE, P);
+  static constexpr uint32_t TmemCols = kTmemCols / CPS;
   static constexpr int NA = 2;  // gate/up: gate and up; down: two 128-row tiles
   static constexpr int BBytes = KN * kKS;
   static constexpr int StageBytes = NA * kABytes + BBytes + NA * kSfBytes + kSfBytes;
-  static constexpr int S0 = (226 * 1024) / StageBytes;
+  static constexpr int S0 = (CPS == 1 ? 226 * 1024 : 111 * 1024) / StageBytes;
   static constexpr int S = S0 > 12 ? 12 : S0;
   static constexpr size_t offA = 0;
   static constexpr size_t offB = offA + (size_t)S * NA * kABytes;
@@ -95,7 +107,7 @@ struct Geo {
   static constexpr size_t offBars = offSfb + (size_t)S * kSfBytes;
   static constexpr uint32_t accCols = NA * KN;      // one accumulator set
   static constexpr uint32_t sfStride = NA * 4 + 4;  // per stage NA x 4 A, 4 B scale columns
-  static constexpr int NACC0 = (int)((kTmemCols - S * sfStride) / accCols);
+  static constexpr int NACC0 = (int)((TmemCols - S * sfStride) / accCols);
   static constexpr int NACC = NACC0 > 4 ? 4 : NACC0;  // accumulator sets (MMA runs ahead)
   static constexpr uint32_t sfCol = NACC * accCols;
 };
@@ -107,20 +119,22 @@ struct Bars {
   uint32_t tmem;
   int err;
 };
-template <int MODE, int KN>
+template <int MODE, int KN, int P>
 constexpr size_t smem_bytes() {
-  using G = Geo<MODE, KN>;
+  using G = Geo<MODE, KN, P>;
   return G::offBars + sizeof(Bars<G::S, G::NACC>);
 }
-template <int MODE, int KN>
+// Fits: the CTAs of an SM in its shared memory, at least two stages, one
+// accumulator set (two where one CTA runs on an SM), the scale columns.
+template <int MODE, int KN, int P>
 constexpr bool geo_ok() {
-  using G = Geo<MODE, KN>;
-  return smem_bytes<MODE, KN>() <= 227 * 1024 && G::NACC >= 2 &&
-         G::sfCol + G::sfStride * G::S <= kTmemCols && G::offB % 1024 == 0 &&
-         G::BBytes % 1024 == 0;
+  using G = Geo<MODE, KN, P>;
+  return smem_bytes<MODE, KN, P>() <= (G::CPS == 1 ? 227 * 1024 : 112 * 1024) && G::S >= 2 &&
+         G::NACC >= (G::CPS == 1 ? 2 : 1) && G::sfCol + G::sfStride * G::S <= G::TmemCols &&
+         G::offB % 1024 == 0 && G::BBytes % 1024 == 0;
 }
-static_assert(geo_ok<0, 32>() && geo_ok<0, 64>() && geo_ok<1, 32>() && geo_ok<1, 64>() &&
-                  geo_ok<1, 80>() && geo_ok<0, 64>(),
+static_assert(geo_ok<0, 32, 1>() && geo_ok<0, 64, 1>() && geo_ok<1, 32, 1>() &&
+                  geo_ok<1, 64, 1>() && geo_ok<0, 64, kPlanesX>() && geo_ok<1, 80, kPlanesH>(),
               "shared or tensor memory");
 
 struct Mx8Args {
@@ -315,8 +329,8 @@ __device__ __forceinline__ Unit unit_at(const Mx8Args& a, int u) {
 // ---------------------------------------------------------------------------
 
 template <int MODE, int KN, int P>
-__device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE, KN>::S, Geo<MODE, KN>::NACC>* b) {
-  using G = Geo<MODE, KN>;
+__device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE, KN, P>::S, Geo<MODE, KN, P>::NACC>* b) {
+  using G = Geo<MODE, KN, P>;
   const int nks = a.K / kKS;
   uint32_t g = 0;
   uint32_t armed = 0u, last_par = 0u;
@@ -362,9 +376,9 @@ __device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<
 }
 
 template <int MODE, int KN, int P>
-__device__ void role_mma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE, KN>::S, Geo<MODE, KN>::NACC>* b,
+__device__ void role_mma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE, KN, P>::S, Geo<MODE, KN, P>::NACC>* b,
                          uint32_t tmem) {
-  using G = Geo<MODE, KN>;
+  using G = Geo<MODE, KN, P>;
   const int nks = a.K / kKS;
   uint32_t g = 0, pc = 0;
   bool ok = true;
@@ -462,9 +476,9 @@ __device__ __forceinline__ void h_planes(const Mx8Args& a, float v, int pos, int
 }
 
 template <int MODE, int KN, int P>
-__device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN>::S, Geo<MODE, KN>::NACC>* b,
+__device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN, P>::S, Geo<MODE, KN, P>::NACC>* b,
                               uint32_t tmem, int warp, int lane) {
-  using G = Geo<MODE, KN>;
+  using G = Geo<MODE, KN, P>;
   constexpr int TPP = KN / P;  // tokens a pass
   const int L = 32 * warp + lane;
   const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
@@ -575,15 +589,15 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN>:
 }
 
 template <int MODE, int KN, int P>
-__global__ void __launch_bounds__(kThr, 1) mx8_gemm_kernel(const __grid_constant__ Mx8Args a) {
-  using G = Geo<MODE, KN>;
+__global__ void __launch_bounds__(kThr, ctas_per_sm(MODE, P)) mx8_gemm_kernel(const __grid_constant__ Mx8Args a) {
+  using G = Geo<MODE, KN, P>;
   extern __shared__ __align__(1024) uint8_t smem[];
   Bars<G::S, G::NACC>* b = reinterpret_cast<Bars<G::S, G::NACC>*>(smem + G::offBars);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&b->tmem)),
-                 "r"(kTmemCols)
+                 "r"(G::TmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -623,7 +637,7 @@ __global__ void __launch_bounds__(kThr, 1) mx8_gemm_kernel(const __grid_constant
   if (threadIdx.x == 0 && b->err) atomicOr(a.err, DEV_ERR_TIMEOUT);
   if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTmemCols)
+                 "r"(G::TmemCols)
                  : "memory");
 }
 
@@ -896,14 +910,14 @@ cudaError_t launch_mx8_kn(const Mx8Args& a, cudaStream_t s) {
     const cudaError_t e =
         cudaFuncSetAttribute(mx8_gemm_kernel<MODE, KN, P>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_bytes<MODE, KN>());
+                             (int)smem_bytes<MODE, KN, P>());
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const long long units = (long long)a.max_items * a.MT;
-  int grid = sms_mx8();
+  int grid = ctas_per_sm(MODE, P) * sms_mx8();
   if (units < grid) grid = (int)(units > 0 ? units : 1);
-  mx8_gemm_kernel<MODE, KN, P><<<grid, kThr, smem_bytes<MODE, KN>(), s>>>(a);
+  mx8_gemm_kernel<MODE, KN, P><<<grid, kThr, smem_bytes<MODE, KN, P>(), s>>>(a);
   return cudaGetLastError();
 }
 
