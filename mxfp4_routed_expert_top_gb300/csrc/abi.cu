@@ -300,9 +300,9 @@ int expert_gateup(df_moe* h, int l, const uint16_t* x, int T, int max_items, int
   const df_moe_config& c = h->cfg;
   const uint8_t* arena = h->layers[l].arena;
   if (h->mx8) {
-    // block-scaled GEMM on E4M3 x (MXFP8, or x's planes); its epilogue
-    // writes h for the down GEMM (rounded to MXFP8, or as h's planes) and,
-    // when hbuf is given, h before that
+    // block-scaled GEMM on E4M3 x (MXFP8, or x's planes): h rounded to MXFP8
+    // for the down GEMM in its epilogue (and, when hbuf is given, h before
+    // that), or, with planes, h into hbuf
     const LayerBufs& L = h->layers[l];
     // (one token selected directly: item q is assignment q, no grouping)
     RUN(h, K_MX8_QUANT, s, launch_mx8_xrows(x, c.hidden, c.top_k, T,
@@ -337,7 +337,7 @@ int expert_down(df_moe* h, int l, const float* hbuf, int T, int max_items, int t
   const uint8_t* arena = h->layers[l].arena;
   if (h->mx8) {
     // block-scaled GEMM on E4M3 h: h (when given) rounded to MXFP8 or split
-    // into its planes first; else the gate/up GEMM's rounded h or planes
+    // into its planes first; else (MXFP8) the gate/up GEMM's rounded h
     if (hbuf)
       RUN(h, K_MX8_QUANT, s, launch_mx8_rows(hbuf, c.inter, h->ph, h->items, h->n_items,
                                              max_items, h->sorted, T * c.top_k, c.n_experts,
@@ -526,11 +526,11 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
       rc = shared_part(h, l, x, T, h->ysh, s);
       if (rc) return rc;
     }
-    // (the block-scaled GEMMs hand h from GEMM to GEMM already rounded to
-    // MXFP8 or split into its planes)
-    rc = expert_gateup(h, l, x, T, max_items, tg, h->mx8 ? nullptr : h->hbuf, s);
+    // (the MXFP8 variant hands h from GEMM to GEMM already rounded)
+    const bool rounded_h = h->mx8 && h->ph == 1;
+    rc = expert_gateup(h, l, x, T, max_items, tg, rounded_h ? nullptr : h->hbuf, s);
     if (rc) return rc;
-    rc = expert_down(h, l, h->mx8 ? nullptr : h->hbuf, T, max_items, tg, s, 0,
+    rc = expert_down(h, l, rounded_h ? nullptr : h->hbuf, T, max_items, tg, s, 0,
                      /*after_gateup=*/true);
     if (rc) return rc;
   }

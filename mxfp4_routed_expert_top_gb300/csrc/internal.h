@@ -341,10 +341,10 @@ cudaError_t launch_mx8_plain(const float* v, int rows, int n, uint8_t* codes, ui
 // Canonical spans -> the variant's span layout (inverse: back).
 cudaError_t launch_mx8_layout(const uint8_t* src, uint8_t* dst, int n_spans, int H, int I,
                               size_t span_bytes, int inverse, cudaStream_t s);
-// gate/up on x's planes (1 or kPlanesX). h for the down GEMM into hq/hsf
-// (hrows_cap rows): one plane, h rounded to MXFP8; kPlanesX, h as its
-// kPlanesH planes (hq may be null then). hbuf [nassign][I] (optional with
-// one plane or with hq): h before that.
+// gate/up on x's planes (1 or kPlanesX). One plane: h rounded to MXFP8
+// into hq/hsf (hrows_cap rows) for the down GEMM, and optionally h before
+// the rounding into hbuf [nassign][I]; kPlanesX: h into hbuf (split into its
+// planes by launch_mx8_rows).
 cudaError_t launch_mx8_gateup(const ChunkMap& gate, const ChunkMap& up, const ChunkMap& xmap,
                               const uint8_t* arena, size_t span_bytes, int H, int I,
                               const uint8_t* xsf, int rows_cap, const Item* items,

@@ -77,13 +77,15 @@ constexpr uint32_t kTmemCols = 512;  // an SM's tensor memory
 // the MMA columns there are never read.
 __host__ __device__ constexpr int box_rows(int planes) { return planes > 1 ? 16 * planes : 32; }
 
-// CTAs an SM runs of each GEMM. Two CTAs (each with half the shared and
-// tensor memory) issue the copies from two producer lanes, which measured
-// 9-11% faster on the MXFP8 GEMMs and on the planes' down GEMM at batch 512;
-// the planes' gate/up (whose epilogue also splits h) keeps one CTA with more
-// accumulator sets (two CTAs left it one, and it ran 8% slower).
+// CTAs an SM runs of each GEMM: two, each with half the shared and tensor
+// memory, so that one CTA's pass and unit boundaries (accumulator hand-over,
+// ring ramp) overlap the other's streaming. Measured at batch 512 against one
+// CTA an SM: MXFP8 gate/up and down 9-11% faster, exact planes 6% (gate/up)
+// and 7% (down) faster.
 __host__ __device__ constexpr int ctas_per_sm(int mode, int planes) {
-  return mode == 0 && planes > 1 ? 1 : 2;
+  (void)mode;
+  (void)planes;
+  return 2;
 }
 
 // Per GEMM, token tile KN (tokens a pass at most) and planes P: A operands
@@ -455,26 +457,6 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t addr, uint32_t (&v)[KN]) {
   if constexpr (KN % 32 == 16) tmem_ld16(addr + KN - 16, v + KN - 16);
 }
 
-// h of one (assignment, row) of the gate/up epilogue as the down GEMM's
-// kPlanesH E4M3 planes, rows pos * kPlanesH + p of a.hq: the same greedy split
-// as mx8_rows_kernel (plane p is the MXFP8 rounding of what the planes before
-// it left, the remainder exact in fp32); the 32 rows of a warp are one block
-// along I, so the block maximum is a warp maximum. Every lane of the warp
-// calls with the same pos.
-__device__ __forceinline__ void h_planes(const Mx8Args& a, float v, int pos, int r, int blk,
-                                         int lane) {
-#pragma unroll 1
-  for (int p = 0; p < kPlanesH; ++p) {
-    const int sh = mx8_shared_exp(warp_max(fabsf(v)));
-    const uint32_t code = e4m3_rn_sat(v * pow2f(-sh));
-    v -= e4m3_value(code) * pow2f(sh);
-    const int row = pos * kPlanesH + p;
-    a.hq[(size_t)row * a.I + r] = (uint8_t)code;
-    if (lane == 0)
-      put_scale(a.hsf, a.hrows_cap, row, blk, (uint8_t)(sh + 127), scale_places(kPlanesH));
-  }
-}
-
 template <int MODE, int KN, int P>
 __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN, P>::S, Geo<MODE, KN, P>::NACC>* b,
                               uint32_t tmem, int warp, int lane) {
@@ -569,9 +551,7 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN, 
           if ((unsigned)aa < (unsigned)a.nassign) {
             if (MODE == 0) {
               const float gt = gs[n];
-              const float hv = gt / (1.f + expf(-gt)) * y1;  // silu(gate) * up
-              if (a.hbuf) a.hbuf[(size_t)aa * a.I + r] = hv;
-              if (a.hq) h_planes(a, hv, w.pos + tb + n, r, 4 * w.mt + warp, lane);
+              a.hbuf[(size_t)aa * a.I + r] = gt / (1.f + expf(-gt)) * y1;  // silu(gate) * up
             } else {
               a.part[(size_t)aa * a.H + r] = gs[n];
               a.part[(size_t)aa * a.H + r + kM] = y1;
@@ -1037,9 +1017,8 @@ cudaError_t launch_mx8_gateup(const ChunkMap& gate, const ChunkMap& up, const Ch
                               const int32_t* n_items, int max_items, const int32_t* sorted,
                               int E, int nassign, float* hbuf, uint8_t* hq, uint8_t* hsf,
                               int hrows_cap, int planes, uint32_t* err, cudaStream_t s) {
-  // one plane: h rounded to MXFP8 (hq); planes: h as fp32 rows (hbuf), as
-  // the down GEMM's planes (hq), or both
-  if (planes == 1 ? !hq : !hbuf && !hq) return cudaErrorInvalidValue;
+  // one plane: h rounded to MXFP8 (hq); planes: h as fp32 rows (hbuf)
+  if (planes == 1 ? !hq : !hbuf) return cudaErrorInvalidValue;
   const size_t q = (size_t)H * I / 2, sb = (size_t)H * I / 32;
   Mx8Args a{};
   a.amap0 = gate;

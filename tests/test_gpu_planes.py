@@ -128,11 +128,11 @@ def test_input_range(small, torch):
 
 @pytest.mark.parametrize("T", [5, 40, 100])
 def test_forward_equals_steps(small, torch, T):
-    """The forward hands h from the gate/up GEMM's epilogue to the down GEMM
-    as planes; the down step splits a given fp32 h with the stand-alone
-    routine. Both splits are the same arithmetic, so the forward's output
-    equals, bit for bit, the steps' routed sum plus the shared part (added
-    in fp32, as the forward adds them)."""
+    """The forward splits x once per token and copies the planes to every
+    assignment's rows; the gate/up step does the same from the caller's x,
+    and the down step splits the h it is given as the forward splits its
+    own. So the forward's output equals, bit for bit, the steps' routed sum
+    plus the shared part (added in fp32, as the forward adds them)."""
     wl = SMALL
     x = draw_tokens(small, T, first_id=1200 + T)
     _, out32, ids, w = _forward(small.m, x, T, torch)
