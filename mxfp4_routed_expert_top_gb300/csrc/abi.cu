@@ -105,6 +105,8 @@ struct df_moe {
   uint8_t* mx_hq = nullptr;   // [mx_hrows][I]
   uint8_t* mx_hsf = nullptr;  // [I/128][mx_hrows][16]
   int32_t* mx_inv = nullptr;  // [Tmax*k] each assignment's position in expert order
+  uint8_t* mx_xsfp = nullptr;  // [mx_xrows][H/32] row-major scales (scratch)
+  uint8_t* mx_hsfp = nullptr;  // [mx_hrows][I/32]
   ChunkMap mx_xmap{}, mx_hmap{};
   bool phase = false;  // decode batches run the two phase kernels
   int sms = 0;
@@ -307,7 +309,9 @@ int expert_gateup(df_moe* h, int l, const uint16_t* x, int T, int max_items, int
     // (one token selected directly: item q is assignment q, no grouping)
     RUN(h, K_MX8_QUANT, s, launch_mx8_xrows(x, c.hidden, c.top_k, T,
                                             tg == 1 ? nullptr : h->mx_inv, h->px, h->mx_xq,
-                                            h->mx_xsf, h->mx_xrows, h->err, s));
+                                            h->mx_xrows, h->mx_xsfp, h->err, s));
+    RUN(h, K_MX8_QUANT, s, launch_mx8_scale_lines(h->mx_xsfp, c.hidden, T * c.top_k * h->px,
+                                                  h->mx_xrows, h->px, h->mx_xsf, s));
     RUN(h, K_MX8_GU, s, launch_mx8_gateup(L.mx_gate, L.mx_up, h->mx_xmap, arena, h->span_bytes,
                                           c.hidden, c.inter, h->mx_xsf, h->mx_xrows, h->items,
                                           h->n_items, max_items, h->sorted, c.n_experts,
@@ -338,10 +342,13 @@ int expert_down(df_moe* h, int l, const float* hbuf, int T, int max_items, int t
   if (h->mx8) {
     // block-scaled GEMM on E4M3 h: h (when given) rounded to MXFP8 or split
     // into its planes first; else (MXFP8) the gate/up GEMM's rounded h
-    if (hbuf)
+    if (hbuf) {
       RUN(h, K_MX8_QUANT, s, launch_mx8_rows(hbuf, c.inter, h->ph, h->items, h->n_items,
                                              max_items, h->sorted, T * c.top_k, c.n_experts,
-                                             h->mx_hq, h->mx_hsf, h->mx_hrows, h->err, s));
+                                             h->mx_hq, h->mx_hrows, h->mx_hsfp, h->err, s));
+      RUN(h, K_MX8_QUANT, s, launch_mx8_scale_lines(h->mx_hsfp, c.inter, T * c.top_k * h->ph,
+                                                    h->mx_hrows, h->ph, h->mx_hsf, s));
+    }
     RUN(h, K_MX8_DN, s, launch_mx8_down(h->layers[l].mx_down, h->mx_hmap, arena, h->span_bytes,
                                         c.hidden, c.inter, h->mx_hsf, h->mx_hrows, h->items,
                                         h->n_items, max_items, h->sorted, c.n_experts,
@@ -705,6 +712,8 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
     if (!rc) rc = dalloc(h, &h->mx_hq, hrows * I);
     if (!rc) rc = dalloc(h, &h->mx_hsf, I / 128 * hrows * 16);
     if (!rc) rc = dalloc(h, &h->mx_inv, Tm * k);
+    if (!rc) rc = dalloc(h, &h->mx_xsfp, xrows * (H / 32));
+    if (!rc) rc = dalloc(h, &h->mx_hsfp, hrows * (I / 32));
     if (!rc && (!make_mx8_row_map(h->mx_xq, h->mx_xrows, c.hidden, h->px, &h->mx_xmap) ||
                 !make_mx8_row_map(h->mx_hq, h->mx_hrows, c.inter, h->ph, &h->mx_hmap)))
       rc = fail(h, DF_MOE_ECUDA, "tensor map encoding failed");

@@ -320,21 +320,25 @@ bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E,
 bool make_mx8_row_map(const uint8_t* rows, int rows_cap, int K, int planes, ChunkMap* map);
 // Rounds h for the down GEMM: row n of item i is source row sorted[pos + n]
 // of src (fp32 [nassign][K], 16-byte aligned), written as `planes` E4M3 rows
-// (pos + n) planes + p of q ([rows_cap][K]) with their scales in sf
-// ([K/128][rows_cap][16], word q of a row the scales of the row 32 q later).
-// planes: 1 or kPlanesH.
+// (pos + n) planes + p of q ([rows_cap][K]) with their scales as row-major
+// scale rows in sfp ([rows_cap][K/32]). planes: 1 or kPlanesH.
 cudaError_t launch_mx8_rows(const float* src, int K, int planes, const Item* items,
                             const int32_t* n_items, int max_items, const int32_t* sorted,
-                            int nassign, int E, uint8_t* q, uint8_t* sf, int rows_cap,
+                            int nassign, int E, uint8_t* q, int rows_cap, uint8_t* sfp,
                             uint32_t* err, cudaStream_t s);
 // Rounds x (bf16 [T][K], 16-byte aligned, K <= 8192) for the gate/up GEMM:
 // each token once, written to the rows of its k assignments, rows
-// inv[t k + j] planes + p of q, scales as above. inv: the grouping's
+// inv[t k + j] planes + p of q, scale rows as above. inv: the grouping's
 // positions of the assignments (-1: none; null: position = assignment).
 // planes: 1 or kPlanesX.
 cudaError_t launch_mx8_xrows(const uint16_t* x, int K, int k, int T, const int32_t* inv,
-                             int planes, uint8_t* q, uint8_t* sf, int rows_cap, uint32_t* err,
+                             int planes, uint8_t* q, int rows_cap, uint8_t* sfp, uint32_t* err,
                              cudaStream_t s);
+// The GEMM's scales sf ([K/128][rows_cap][16], word q of a row the scales
+// of the row 32 q later) from the row-major scale rows sfp of the first
+// `rows` rows.
+cudaError_t launch_mx8_scale_lines(const uint8_t* sfp, int K, int rows, int rows_cap,
+                                   int planes, uint8_t* sf, cudaStream_t s);
 // The rounding on plain rows: codes [rows][n], scales [rows][n/32].
 cudaError_t launch_mx8_plain(const float* v, int rows, int n, uint8_t* codes, uint8_t* scales,
                              cudaStream_t s);

@@ -665,26 +665,47 @@ __device__ __forceinline__ void stage_words(const int (&sh)[P], uint32_t (&sw)[P
 }
 
 // Writes block j of the P rows row0 .. row0 + P - 1: the codes into q
-// [rows][K], and (the group's first lane) the stage words into their places
-// in sf (word q of row - 32 q, q < scale_places(P)).
+// [rows][K], and (the group's first lane) the stage words into the row-major
+// scale rows sfp [rows][K/32] (a warp's words are one contiguous piece of a
+// row; mx8_scale_lines_kernel then builds the GEMM's layout from them).
 template <int P>
-__device__ __forceinline__ void store_planes(uint8_t* q, uint8_t* sf, int K, int rows_cap,
-                                             int row0, int j, int lane,
-                                             const uint32_t (&wq)[P][8],
+__device__ __forceinline__ void store_planes(uint8_t* q, uint8_t* sfp, int K, int row0, int j,
+                                             int lane, const uint32_t (&wq)[P][8],
                                              const uint32_t (&sw)[P]) {
-  const size_t ks = (size_t)(j >> 2);
 #pragma unroll
   for (int pl = 0; pl < P; ++pl) {
     const int row = row0 + pl;
     uint4* d = reinterpret_cast<uint4*>(q + (size_t)row * K + 32 * j);
     d[0] = make_uint4(wq[pl][0], wq[pl][1], wq[pl][2], wq[pl][3]);
     d[1] = make_uint4(wq[pl][4], wq[pl][5], wq[pl][6], wq[pl][7]);
-    if ((lane & 3) == 0) {
+    if ((lane & 3) == 0)
+      *reinterpret_cast<uint32_t*>(sfp + (size_t)row * (K / 32) + j) = sw[pl];
+  }
+}
+
+// The GEMM's stage-major, row-interleaved scale lines from row-major scale
+// rows: line (ks, R) = the stage-ks words of rows R, R + 32, ... (the first
+// `places` of them; the rest zero), one 16-byte store a thread, consecutive
+// threads consecutive lines. Rows at or past `rows` (never written) read as
+// zero words.
+__global__ void __launch_bounds__(256) mx8_scale_lines_kernel(const uint8_t* __restrict__ sfp,
+                                                              int nb, int rows, int lines,
+                                                              int rows_cap, int places,
+                                                              uint8_t* __restrict__ sf) {
+  const long long n = (long long)lines * (nb / 4);
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int ks = (int)(i / lines), R = (int)(i - (long long)ks * lines);
+    uint32_t w[4];
 #pragma unroll
-      for (int qq = 0; qq < scale_places(P); ++qq)
-        if (row - 32 * qq >= 0)
-          reinterpret_cast<uint32_t*>(sf)[(ks * rows_cap + row - 32 * qq) * 4 + qq] = sw[pl];
+    for (int q = 0; q < 4; ++q) {
+      const int r = R + 32 * q;
+      w[q] = q < places && r < rows
+                 ? __ldg(reinterpret_cast<const uint32_t*>(sfp + (size_t)r * nb + 4 * ks))
+                 : 0u;
     }
+    *reinterpret_cast<uint4*>(sf + ((size_t)ks * rows_cap + R) * 16) =
+        make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -696,7 +717,7 @@ template <int P>
 __global__ void __launch_bounds__(256) mx8_rows_kernel(const float* src, int K, const Item* items,
                                                        const int32_t* n_items, int max_items,
                                                        const int32_t* sorted, int nassign, int E,
-                                                       uint8_t* q, uint8_t* sf, int rows_cap,
+                                                       uint8_t* q, uint8_t* sfp, int rows_cap,
                                                        uint32_t* err) {
   const int i = blockIdx.x;
   int ni = *n_items;
@@ -741,7 +762,7 @@ __global__ void __launch_bounds__(256) mx8_rows_kernel(const float* src, int K, 
     block_planes<P>(v, wq, sh);
     uint32_t sw[P];
     stage_words<P>(sh, sw);
-    if (live) store_planes<P>(q, sf, K, rows_cap, (it.pos + n) * P, j, lane, wq, sw);
+    if (live) store_planes<P>(q, sfp, K, (it.pos + n) * P, j, lane, wq, sw);
   }
 }
 
@@ -754,7 +775,7 @@ __global__ void __launch_bounds__(256) mx8_rows_kernel(const float* src, int K, 
 template <int P>
 __global__ void __launch_bounds__(128) mx8_xrows_kernel(const uint16_t* __restrict__ x, int K,
                                                         int k, const int32_t* __restrict__ inv,
-                                                        int nassign, uint8_t* q, uint8_t* sf,
+                                                        int nassign, uint8_t* q, uint8_t* sfp,
                                                         int rows_cap, uint32_t* err) {
   __shared__ int dst[32];  // the token's positions in expert order (k <= 32)
   const int t = blockIdx.x;
@@ -796,7 +817,7 @@ __global__ void __launch_bounds__(128) mx8_xrows_kernel(const uint16_t* __restri
   if (!live) return;
   for (int i = 0; i < k; ++i) {
     const int p = dst[i];
-    if (p >= 0) store_planes<P>(q, sf, K, rows_cap, p * P, j, lane, wq, sw);
+    if (p >= 0) store_planes<P>(q, sfp, K, p * P, j, lane, wq, sw);
   }
 }
 
@@ -964,14 +985,25 @@ bool make_mx8_row_map(const uint8_t* rows_buf, int rows_cap, int K, int planes, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+cudaError_t launch_mx8_scale_lines(const uint8_t* sfp, int K, int rows, int rows_cap,
+                                   int planes, uint8_t* sf, cudaStream_t s) {
+  // a pass reads the 32 lines from its first row, which is below `rows`
+  const int lines = std::min(rows_cap, rows + 32);
+  const long long n = (long long)lines * (K / 128);
+  const int blocks = (int)std::min<long long>((n + 255) / 256, 4096);
+  mx8_scale_lines_kernel<<<blocks, 256, 0, s>>>(sfp, K / 32, rows, lines, rows_cap,
+                                                scale_places(planes), sf);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_mx8_rows(const float* src, int K, int planes, const Item* items,
                             const int32_t* n_items, int max_items, const int32_t* sorted,
-                            int nassign, int E, uint8_t* q, uint8_t* sf, int rows_cap,
+                            int nassign, int E, uint8_t* q, int rows_cap, uint8_t* sfp,
                             uint32_t* err, cudaStream_t s) {
   if (max_items <= 0) return cudaSuccess;
   auto go = [&](auto kernel) {
     kernel<<<max_items, 256, 0, s>>>(src, K, items, n_items, max_items, sorted, nassign, E, q,
-                                     sf, rows_cap, err);
+                                     sfp, rows_cap, err);
     return cudaGetLastError();
   };
   if (planes == 1) return go(mx8_rows_kernel<1>);
@@ -980,13 +1012,13 @@ cudaError_t launch_mx8_rows(const float* src, int K, int planes, const Item* ite
 }
 
 cudaError_t launch_mx8_xrows(const uint16_t* x, int K, int k, int T, const int32_t* inv,
-                             int planes, uint8_t* q, uint8_t* sf, int rows_cap, uint32_t* err,
+                             int planes, uint8_t* q, int rows_cap, uint8_t* sfp, uint32_t* err,
                              cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   if (K % 128 || k > 32) return cudaErrorInvalidValue;
   const dim3 grid(T, (K / 32 + 127) / 128);
   auto go = [&](auto kernel) {
-    kernel<<<grid, 128, 0, s>>>(x, K, k, inv, T * k, q, sf, rows_cap, err);
+    kernel<<<grid, 128, 0, s>>>(x, K, k, inv, T * k, q, sfp, rows_cap, err);
     return cudaGetLastError();
   };
   if (planes == 1) return go(mx8_xrows_kernel<1>);
