@@ -76,8 +76,9 @@ def parse():
                         "activations as sums of E4M3 planes (DF_MOE_PLANES); the default "
                         "for batch workloads (more than 8 tokens a step)")
     p.add_argument("--no-planes", action="store_true",
-                   help="batches on the default handle's GEMMs (MXFP4 decoded into tensor "
-                        "memory) instead of the planes")
+                   help="4 tokens or more on a default handle (the decode kernels up to 8 "
+                        "tokens, the GEMMs with MXFP4 decoded into tensor memory above) "
+                        "instead of the planes")
     p.add_argument("--experts", type=int, default=0,
                    help="profiling aid: override the routed-expert count (same "
                         "per-token work, smaller resident set); not a bench line")
@@ -341,9 +342,11 @@ def run_ours(args):
     if args.tokens:
         wl = dataclasses.replace(wl, T=args.tokens, name=wl.name + "-t%d" % args.tokens)
     T = wl.T
-    # batches run on the exact planes unless another batch path is asked for
-    if (T > 8 and not (args.no_planes or args.mxfp8 or args.mma_sync_prefill or args.cache_slots
-                       or wl.stack)):
+    # from 4 tokens on, layers run on the exact planes (the faster exact path
+    # there: 326 against 331 us at 4 tokens, 487 against 606 at 8) unless
+    # another path is asked for; fewer tokens run on the decode kernels
+    if (T >= 4 and not (args.no_planes or args.mxfp8 or args.mma_sync_prefill or args.cache_slots
+                        or wl.stack)):
         args.planes = True
     flags = ((dfm.STACK_RMSNORM_RESIDUAL if wl.stack else 0)
              | (dfm.PREFILL_MMA_SYNC if args.mma_sync_prefill else 0)

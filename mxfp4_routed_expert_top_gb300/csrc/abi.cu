@@ -375,7 +375,11 @@ int shared_part(df_moe* h, int l, const uint16_t* x, int T, float* ysh,
                 cudaStream_t s, int max_ctas = 0) {
   const df_moe_config& c = h->cfg;
   const LayerBufs& L = h->layers[l];
-  if (T > kDecodeMaxT && L.sh_maps_ok && ((uintptr_t)x & 15) == 0) {
+  // the dense GEMMs from 4 tokens on block-scaled handles (where the shared
+  // experts do not run beside the routed ones): at 4-8 tokens the streaming
+  // GEMV spends more time on its fp32 FMAs than on the weights
+  const bool dense = T > kDecodeMaxT || (h->mx8 && T >= 4);
+  if (dense && L.sh_maps_ok && ((uintptr_t)x & 15) == 0) {
     // a batch: two dense GEMMs on the tensor cores
     RUN(h, K_SHARED_GU, s, launch_shared_gemm_gateup(L.sh_maps, x, T, c.hidden, h->R, h->s_hh,
                                                      h->err, s));
@@ -735,7 +739,7 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
   }
   // the shared experts of batches as dense tcgen05 GEMMs (the routed
   // experts' path aside: exact GEMMs, the MXFP8 variant, or none)
-  if (!rc && (h->gemm || h->mx8) && Tm > (size_t)kDecodeMaxT && R &&
+  if (!rc && (h->gemm || h->mx8) && (Tm > (size_t)kDecodeMaxT || (h->mx8 && Tm >= 4)) && R &&
       dense_supported(c.hidden, (int)R)) {
     rc = dalloc(h, &h->s_hh, Tm * 3 * R);
     for (int l = 0; l < c.n_layers && !rc; ++l) {

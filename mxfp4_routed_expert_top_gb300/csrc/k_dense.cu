@@ -22,7 +22,8 @@
 // part[s][t][e], and the top-k kernel sums the planes in order (the same
 // sums every run).
 //
-// One 128 x 128 (GEMM 1 and 3) or 128 x 96 (GEMM 2: 32 tokens) output tile per
+// One 128 x 96 (GEMM 1: 96 tokens), 128 x 96 (GEMM 2: 32 tokens) or 128 x 128
+// (GEMM 3: 128 tokens) output tile per
 // CTA, 192 threads: warp 0 loads A and B tiles
 // of 64 columns by TMA (128-byte swizzle) into a ring of stages, warp 1
 // issues tcgen05.mma (M = 128, N = 128, K = 16) and commits each stage back,
@@ -41,6 +42,9 @@ namespace dfm {
 namespace {
 
 constexpr int kDM = 128, kDN = 128, kDK = 64;  // tile rows, B rows (columns of D), K per stage
+// GEMM 1: 96 tokens a tile (at batch 512, 288 tiles fill 1.9 waves of 152 SMs
+// where 128-token tiles left the second of two waves a quarter full)
+constexpr int kDN0 = 96;
 constexpr int kDN1 = 96;                       // GEMM 2: B rows of 32 tokens x 3 parts
 constexpr int kDStages = 6;
 constexpr int kDABytes = kDM * kDK * 2;        // 16 KB
@@ -98,7 +102,7 @@ __global__ void __launch_bounds__(kDThr, 1) dense_kernel(const __grid_constant__
   uint8_t* sb = smem + (size_t)kDStages * kDABytes;
   DSmem* sm = reinterpret_cast<DSmem*>(sb + (size_t)kDStages * kDBBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bn = a.mode == 1 ? kDN1 : kDN;          // B rows of a tile
+  const int bn = a.mode == 1 ? kDN1 : a.mode == 0 ? kDN0 : kDN;          // B rows of a tile
   const int n_rows = a.mode == 1 ? 3 * a.T : a.T;  // B rows
   const int ntn = (n_rows + bn - 1) / bn;
   const int split = a.mode == 2 ? (int)blockIdx.x / a.tiles : 0;
@@ -215,7 +219,7 @@ __global__ void __launch_bounds__(kDThr, 1) dense_kernel(const __grid_constant__
         // the stage memory the tensor copies wrote last
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         if (m >= 64) {
-          for (int c0 = 0; c0 < kDN; c0 += 16) {
+          for (int c0 = 0; c0 < kDN0; c0 += 16) {
             uint32_t r[16];
             asm volatile(
                 "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"
@@ -234,7 +238,7 @@ __global__ void __launch_bounds__(kDThr, 1) dense_kernel(const __grid_constant__
           sm->err = 1;
         } else {
           const int row = 64 * mt + m;  // intermediate index
-          for (int c0 = 0; c0 < kDN; c0 += 16) {
+          for (int c0 = 0; c0 < kDN0; c0 += 16) {
             uint32_t r[16];
             asm volatile(
                 "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"
@@ -246,7 +250,7 @@ __global__ void __launch_bounds__(kDThr, 1) dense_kernel(const __grid_constant__
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const int t = kDN * nt + c0 + i;
+              const int t = kDN0 * nt + c0 + i;
               if (t < a.T) {
                 const float h = silu_f(__uint_as_float(r[i])) * xs[m * kXsLd + c0 + i];
                 const uint32_t hi = bf16_bits(h);
@@ -401,7 +405,7 @@ cudaError_t launch_shared_gemm_gateup(const SharedMaps& m, const uint16_t* x, in
   DenseArgs a{};
   a.a0 = m.gate;
   a.a1 = m.up;
-  if (!map_bf16(&a.b, x, H, T, kDN)) return cudaErrorInvalidValue;
+  if (!map_bf16(&a.b, x, H, T, kDN0)) return cudaErrorInvalidValue;
   a.mode = 0;
   a.K = H;
   a.T = T;
@@ -409,7 +413,7 @@ cudaError_t launch_shared_gemm_gateup(const SharedMaps& m, const uint16_t* x, in
   a.H = H;
   a.hh = hh;
   a.err = err;
-  return launch_dense(a, (R / 64) * ((T + kDN - 1) / kDN), s);
+  return launch_dense(a, (R / 64) * ((T + kDN0 - 1) / kDN0), s);
 }
 
 cudaError_t launch_shared_gemm_down(const SharedMaps& m, int T, int H, int R, float* y,
