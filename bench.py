@@ -598,10 +598,11 @@ def run_ours(args):
         "config": {**workload_config(wl, ws),
                    "l2": "flushed (256 MiB write) before every timed step",
                    "launch": "cuda graph" if args.graph else "stream",
-                   "prefill_path": ("mma_sync" if args.mma_sync_prefill else
-                                    "tcgen05 block-scaled (E4M3 planes)" if args.planes else
-                                    "tcgen05 block-scaled (MXFP8)" if args.mxfp8 else
-                                    "tcgen05 (MXFP4 decoded into tensor memory)"),
+                   "expert_path": ("tcgen05 block-scaled (E4M3 planes)" if args.planes else
+                                   "tcgen05 block-scaled (MXFP8)" if args.mxfp8 else
+                                   "decode phase kernels (mma.sync GEMVs)" if T <= 8 else
+                                   "mma_sync" if args.mma_sync_prefill else
+                                   "tcgen05 (MXFP4 decoded into tensor memory)"),
                    "activations": ("MXFP8 (E4M3, E8M0 per 32) into the routed experts: "
                                    "the lossy variant") if args.mxfp8 else
                                   ("exact, as sums of E4M3 planes (x 4, h 5) on the "
