@@ -68,6 +68,7 @@ struct df_moe {
   float* router_part = nullptr;  // [nsplit][Tmax][E] (batches on tcgen05: [splits][T][E])
   size_t router_part_rows = 0;   // its rows (planes x tokens)
   bool router_tc = false;        // batches' router logits on tcgen05
+  int router_tc_min_t = kDecodeMaxT + 1;  // from this many tokens
   float* logits = nullptr;       // [Tmax][E]
   int32_t* ids_ws = nullptr;     // [Tmax][k]
   float* w_ws = nullptr;         // [Tmax][k]
@@ -265,7 +266,7 @@ int route(df_moe* h, int l, const uint16_t* x, int T, int32_t* ids, float* w,
     return DF_MOE_OK;
   }
   int nsplit = h->rsplit.nsplit;
-  if (T > kDecodeMaxT) {
+  if (h->router_tc && T >= h->router_tc_min_t) {
     // a batch: the logits as one GEMM on the tensor cores (the weights read
     // once for all tokens)
     int used = -1;
@@ -749,7 +750,11 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
     }
   }
   // batches' router on tcgen05: the weights' bf16 parts and their map
-  h->router_tc = Tm > (size_t)kDecodeMaxT;
+  // (block-scaled handles run 4-8 token batches through the batch path too,
+  // where the tensor-core router beats the GEMV's fp32 FMAs on x in shared
+  // memory)
+  h->router_tc_min_t = h->mx8 ? 4 : kDecodeMaxT + 1;
+  h->router_tc = Tm >= (size_t)h->router_tc_min_t;
   for (int l = 0; l < c.n_layers && !rc && h->router_tc; ++l) {
     LayerBufs& L = h->layers[l];
     rc = dalloc(h, &L.router3, E * 3 * H);
@@ -759,7 +764,8 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
   h->router_part_rows = (size_t)h->rsplit.nsplit * Tm;
   if (h->router_tc)
     h->router_part_rows = std::max(h->router_part_rows,
-                                   router_tc_part_rows(c.n_experts, c.hidden, (int)Tm, h->sms));
+                                   router_tc_part_rows(c.n_experts, c.hidden, h->router_tc_min_t,
+                                                       (int)Tm, h->sms));
   if (!rc) rc = dalloc(h, &h->router_part, h->router_part_rows * E);
   if (!rc) rc = dalloc(h, &h->logits, Tm * E);
   if (!rc) rc = dalloc(h, &h->ids_ws, Tm * k);

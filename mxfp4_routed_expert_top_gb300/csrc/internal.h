@@ -291,8 +291,8 @@ cudaError_t launch_shared_gemm_down(const SharedMaps& m, int T, int H, int R, fl
 // top-k kernel). max_rows bounds splits x T (the part buffer's rows; 0: no
 // bound). H: a multiple of 64.
 int router_tc_splits(int E, int H, int T, int sms, size_t max_rows);
-// the largest splits x T over batches above the decode range up to Tmax
-size_t router_tc_part_rows(int E, int H, int Tmax, int sms);
+// the largest splits x T over batches of Tmin .. Tmax tokens
+size_t router_tc_part_rows(int E, int H, int Tmin, int Tmax, int sms);
 cudaError_t launch_router_parts(const float* w, int E, int H, uint16_t* out, cudaStream_t s);
 bool make_router_map(const uint16_t* parts, int E, int H, ChunkMap* out);
 // returns the number of partial planes written, -1 on a launch or encoding

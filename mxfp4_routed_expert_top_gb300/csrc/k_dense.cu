@@ -445,9 +445,9 @@ int router_tc_splits(int E, int H, int T, int sms, size_t max_rows) {
   return (KB + per - 1) / per;
 }
 
-size_t router_tc_part_rows(int E, int H, int Tmax, int sms) {
+size_t router_tc_part_rows(int E, int H, int Tmin, int Tmax, int sms) {
   size_t rows = 0;
-  for (int T = kDecodeMaxT + 1; T <= Tmax; ++T)
+  for (int T = Tmin; T <= Tmax; ++T)
     rows = std::max(rows, (size_t)router_tc_splits(E, H, T, sms, 0) * T);
   return rows;
 }

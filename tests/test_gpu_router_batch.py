@@ -34,11 +34,11 @@ def torch():
     return t
 
 
-def _handle(H, E, max_tokens, seed, k=4):
+def _handle(H, E, max_tokens, seed, k=4, flags=0):
     """A handle whose layer 0 has only its router loaded (the router and
     top-k steps need nothing else)."""
     import mxfp4_routed_expert_top_gb300 as dfm
-    m = dfm.MoE(H, E, k, 128, 1, 64, n_layers=1, max_tokens=max_tokens)
+    m = dfm.MoE(H, E, k, 128, 1, 64, n_layers=1, max_tokens=max_tokens, flags=flags)
     router = synth.router(seed, 0, 0, E, H)
     m.load_experts(0, router=router)
     m.sync()
@@ -75,6 +75,26 @@ def test_one_hot_tokens_exact(torch, T):
         # significant bits are not all zero)
         assert np.mean((router.view(np.uint32) & 0xFF) > 0) > 0.99
         assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    finally:
+        m.close()
+
+
+@pytest.mark.parametrize("T", [4, 8])
+def test_planes_handle_small_batches(torch, T):
+    """Block-scaled handles take batches of 4-8 tokens through the tensor-core
+    router too (one-hot tokens: bit-exact; Gaussian: the 1e-5 bound)."""
+    import mxfp4_routed_expert_top_gb300 as dfm
+    H, E = 256, 200
+    m, router = _handle(H, E, 8, seed=73, flags=dfm.PLANES)
+    try:
+        cols = (np.arange(T) * 53) % H
+        x = np.zeros((T, H), dtype=np.uint16)
+        x[np.arange(T), cols] = _bf16_bits(np.ones(T))
+        got = _logits(torch, m, to_dev_bf16(x), T, E)
+        assert np.array_equal(got.view(np.uint32), router[:, cols].T.copy().view(np.uint32))
+        x = np.stack([synth.token(73, 0, 60 + t, H) for t in range(T)])
+        got = _logits(torch, m, to_dev_bf16(x), T, E)
+        assert np.all(np.abs(got - orc.router_logits(router, x)) <= _bound(router, x))
     finally:
         m.close()
 
