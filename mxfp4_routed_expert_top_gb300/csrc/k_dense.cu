@@ -46,7 +46,13 @@ constexpr int kDM = 128, kDN = 128, kDK = 64;  // tile rows, B rows (columns of 
 // where 128-token tiles left the second of two waves a quarter full)
 constexpr int kDN0 = 96;
 constexpr int kDN1 = 96;                       // GEMM 2: B rows of 32 tokens x 3 parts
-constexpr int kDStages = 6;
+// Stages a CTA: 6 with one CTA an SM, 3 with two (each with half the shared
+// and tensor memory, so that one CTA's tile prologue and epilogue overlap the
+// other's stream). Grids of more tiles than SMs take two CTAs an SM:
+// measured at batch 512 the shared GEMMs went from ~86 to ~61 us each, while
+// the router (140 CTAs) and the shared GEMMs of 8 tokens (48-56 tiles) were
+// slower with half the stages.
+constexpr int kDStagesMax = 6;
 constexpr int kDABytes = kDM * kDK * 2;        // 16 KB
 constexpr int kDBBytes = kDN * kDK * 2;        // 16 KB
 constexpr int kDThr = 6 * 32;
@@ -66,18 +72,21 @@ struct DenseArgs {
   uint32_t* err;
 };
 
+template <int NS>
 struct DSmem {
-  uint64_t full[kDStages], empty[kDStages], done;
+  uint64_t full[NS], empty[NS], done;
   uint64_t xdone;  // the two up-row warps have handed their values over
   uint32_t tmem;
   int err;
 };
 
+template <int NS>
 constexpr size_t dense_smem_bytes() {
-  return (size_t)kDStages * (kDABytes + kDBBytes) + sizeof(DSmem);
+  return (size_t)NS * (kDABytes + kDBBytes) + sizeof(DSmem<NS>);
 }
-static_assert(dense_smem_bytes() <= 227 * 1024, "shared memory");
-static_assert((size_t)64 * kXsLd * 4 <= (size_t)kDStages * kDABytes, "exchange buffer");
+static_assert(dense_smem_bytes<kDStagesMax>() <= 227 * 1024, "shared memory");
+static_assert(2 * (dense_smem_bytes<kDStagesMax / 2>() + 1024) <= 228 * 1024, "two CTAs an SM");
+static_assert((size_t)64 * kXsLd * 4 <= (size_t)(kDStagesMax / 2) * kDABytes, "exchange buffer");
 
 __device__ __forceinline__ uint32_t uni_d(uint32_t v) { return __shfl_sync(0xffffffffu, v, 0); }
 
@@ -96,11 +105,13 @@ __device__ __forceinline__ uint32_t bf16_bits(float v) {
   return *reinterpret_cast<const uint16_t*>(&b);
 }
 
-__global__ void __launch_bounds__(kDThr, 1) dense_kernel(const __grid_constant__ DenseArgs a) {
+template <int NS>
+__global__ void __launch_bounds__(kDThr, kDStagesMax / NS) dense_kernel(const __grid_constant__ DenseArgs a) {
+  constexpr int kDStages = NS;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sa = smem;
   uint8_t* sb = smem + (size_t)kDStages * kDABytes;
-  DSmem* sm = reinterpret_cast<DSmem*>(sb + (size_t)kDStages * kDBBytes);
+  DSmem<NS>* sm = reinterpret_cast<DSmem<NS>*>(sb + (size_t)kDStages * kDBBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bn = a.mode == 1 ? kDN1 : a.mode == 0 ? kDN0 : kDN;          // B rows of a tile
   const int n_rows = a.mode == 1 ? 3 * a.T : a.T;  // B rows
@@ -378,16 +389,34 @@ __global__ void router_parts_kernel(const float* __restrict__ w, size_t n, int H
   }
 }
 
-cudaError_t launch_dense(const DenseArgs& a, int tiles, cudaStream_t s) {
+template <int NS>
+cudaError_t launch_dense_ns(const DenseArgs& a, int tiles, cudaStream_t s) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)dense_smem_bytes());
+    cudaError_t e = cudaFuncSetAttribute(dense_kernel<NS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)dense_smem_bytes<NS>());
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dense_kernel<<<tiles, kDThr, dense_smem_bytes(), s>>>(a);
+  dense_kernel<NS><<<tiles, kDThr, dense_smem_bytes<NS>(), s>>>(a);
   return cudaGetLastError();
+}
+
+int dense_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+cudaError_t launch_dense(const DenseArgs& a, int tiles, cudaStream_t s) {
+  return tiles > dense_sms() ? launch_dense_ns<kDStagesMax / 2>(a, tiles, s)
+                             : launch_dense_ns<kDStagesMax>(a, tiles, s);
 }
 
 }  // namespace
