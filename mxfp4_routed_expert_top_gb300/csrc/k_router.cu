@@ -220,8 +220,13 @@ group_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
   __shared__ int fill[1024];
   __shared__ int warp_sums[32];
   __shared__ int tot;
+  // the sorted list is built in shared memory when it fits (the segment
+  // sorts then run at shared-memory latency), else in place in global memory
+  constexpr int kSortSmem = 8192;
+  __shared__ int ssort[kSortSmem];
   const int tid = threadIdx.x;
   const int A = T * k;
+  int* const buf = A <= kSortSmem ? ssort : sorted;
   cnt[tid] = 0;
   pdl_launch_dependents();  // the next kernel waits for this grid itself
   pdl_wait();  // the selected ids
@@ -229,10 +234,20 @@ group_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
   // an id outside [0, E) (the single-step entry points take the caller's
   // ids) is left out of every segment and recorded in the error word
   bool bad = false;
-  for (int a = tid; a < A; a += blockDim.x) {
-    const int e = ids[a];
-    if ((unsigned)e < (unsigned)E) atomicAdd(&cnt[e], 1);
-    else bad = true;
+  // eight loads a thread issued together (one round trip, not eight)
+  for (int a0 = tid; a0 < A; a0 += 8 * blockDim.x) {
+    int ev[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int a = a0 + u * (int)blockDim.x;
+      ev[u] = a < A ? ids[a] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (a0 + u * (int)blockDim.x >= A) break;
+      if ((unsigned)ev[u] < (unsigned)E) atomicAdd(&cnt[ev[u]], 1);
+      else bad = true;
+    }
   }
   if (bad && err) atomicOr(err, DEV_ERR_RANGE);
   __syncthreads();
@@ -245,32 +260,42 @@ group_kernel(const int32_t* __restrict__ ids, int T, int k, int E,
   }
   __syncthreads();
   if (tid == 0 && offs) offs[E] = tot;  // A when every id is in range
-  for (int a = tid; a < A; a += blockDim.x) {
-    const int e = ids[a];
-    if ((unsigned)e >= (unsigned)E) continue;
-    const int p = atomicAdd(&fill[e], 1);
-    sorted[p] = a;
+  for (int a0 = tid; a0 < A; a0 += 8 * blockDim.x) {
+    int ev[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int a = a0 + u * (int)blockDim.x;
+      ev[u] = a < A ? ids[a] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if ((unsigned)ev[u] >= (unsigned)E) continue;  // out of range, or past A
+      const int p = atomicAdd(&fill[ev[u]], 1);
+      buf[p] = a0 + u * (int)blockDim.x;
+    }
   }
   __syncthreads();
   __threadfence_block();
   // order each segment by assignment index (insertion sort, one thread each)
   if (tid < E) {
     for (int i = start + 1; i < start + c; ++i) {
-      const int v = sorted[i];
+      const int v = buf[i];
       int j = i - 1;
-      while (j >= start && sorted[j] > v) { sorted[j + 1] = sorted[j]; --j; }
-      sorted[j + 1] = v;
+      while (j >= start && buf[j] > v) { buf[j + 1] = buf[j]; --j; }
+      buf[j + 1] = v;
     }
   }
   if (inv)
     for (int a = tid; a < A; a += blockDim.x) inv[a] = -1;
   __syncthreads();
+  if (buf != sorted)
+    for (int p = tid; p < nvalid; p += blockDim.x) sorted[p] = buf[p];
   if (inv)
-    for (int p = tid; p < nvalid; p += blockDim.x) inv[sorted[p]] = p;
+    for (int p = tid; p < nvalid; p += blockDim.x) inv[buf[p]] = p;
   if (tok) {
-    for (int p = tid; p < A; p += blockDim.x) {
-      tok[p] = sorted[p] / k;
-      slot[p] = sorted[p] % k;
+    for (int p = tid; p < nvalid; p += blockDim.x) {
+      tok[p] = buf[p] / k;
+      slot[p] = buf[p] % k;
     }
   }
   // work items: ceil(count / tg) per expert, in expert order

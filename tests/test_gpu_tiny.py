@@ -96,6 +96,33 @@ def test_group_step(tiny, torch, T):
     assert nu.item() == rn
 
 
+@pytest.mark.parametrize("T, hot", [(512, False), (600, False), (600, True)])
+def test_group_step_large(torch, T, hot):
+    """Grouping of many assignments (64 experts, top-16): up to 8192 sort in
+    shared memory, more in place in global memory (600 x 16 = 9600); a hot
+    expert in every token's first slot gives the longest segment."""
+    import mxfp4_routed_expert_top_gb300 as dfm
+    E, k = 64, 16
+    rng = np.random.default_rng(T + hot)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    if hot:
+        for t in range(T):
+            row = [3] + [e for e in ids[t] if e != 3][:k - 1]
+            ids[t] = row
+    with dfm.MoE(WL.H, E, k, WL.I, WL.n_shared, WL.Is, max_tokens=T) as m:
+        offs = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+        tok = torch.empty(T * k, dtype=torch.int32, device="cuda")
+        slot = torch.empty(T * k, dtype=torch.int32, device="cuda")
+        nu = torch.empty(1, dtype=torch.int32, device="cuda")
+        m.step_group(torch.from_numpy(ids).cuda(), T, offs, tok, slot, nu)
+        torch.cuda.synchronize()
+        roffs, rtok, rslot, rn = orc.group(ids, E)
+        assert np.array_equal(offs.cpu().numpy(), roffs)
+        assert np.array_equal(tok.cpu().numpy(), rtok)
+        assert np.array_equal(slot.cpu().numpy(), rslot)
+        assert nu.item() == rn
+
+
 def _oracle_route(tiny, x):
     return orc.topk_softmax(orc.router_logits(tiny.routers[0], x), WL.k)
 
