@@ -63,7 +63,7 @@ namespace {
 
 constexpr int kThr = 192;
 constexpr int kTmaWarp = 4, kMmaWarp = 5;
-constexpr int kM = 128;
+constexpr int kM = 128, kHalfRows = 64;
 constexpr int kKS = 128;                  // contraction columns a stage
 constexpr int kABytes = kM * kKS;         // 16384: one A operand (a byte a code)
 constexpr int kATx = kM * kKS / 2;       // 8192: an A operand's codes as copied (packed)
@@ -87,38 +87,38 @@ __host__ __device__ constexpr int ctas_per_sm(int mode, int planes) {
   return 2;
 }
 
-// Per GEMM, token tile KN (tokens a pass at most) and planes P: A operands
-// a stage (gate/up: gate and up), the stages that fit in the CTA's share of
-// shared memory, the accumulator sets that fit in its share of tensor memory
-// beside the stages' scales, and the layout of one stage in shared memory
-// and of the tensor memory columns.
-// A operands of a unit: gate/up two (gate and up, one h row from both); the
-// down GEMM one 128-row tile. (Two consecutive tiles a down unit, each B stage
-// feeding two MMAs, paid with one CTA an SM; with two CTAs an SM one tile
-// leaves room for two or three accumulator sets and more stages, and measured
-// 7% faster at batch 512: planes 969 -> 907 us, MXFP8 894 -> 827 us.)
-__host__ __device__ constexpr int operands(int mode, int planes) {
-  (void)planes;
-  return mode == 1 ? 1 : 2;
-}
-
+// Per GEMM, token tile KN (tokens a pass at most) and planes P: one
+// 128-row A operand a stage (gate/up: 64 gate rows and the same 64 up rows,
+// so that one MMA gives both values of 64 h rows; down: a 128-row tile), the
+// stages that fit in the CTA's share of shared memory beside the gate/up
+// epilogue's exchange buffers, the accumulator sets that fit in its share of
+// tensor memory beside the stages' scales, and the layout of one stage in
+// shared memory and of the tensor memory columns. Gate/up stages hold the
+// two 128-row tiles' raw scale chunks; the MMA warp assembles the operand's
+// chunk from their halves in place of the first. (Units of the full 128 gate and 128 up
+// rows, two accumulators, left one accumulator set a CTA with two CTAs an
+// SM; one 128-row down tile a unit measured 7% faster than pairs of tiles.)
 template <int MODE, int KN, int P>
 struct Geo {
   static constexpr int CPS = ctas_per_sm(MODE, P);
   static constexpr uint32_t TmemCols = kTmemCols / CPS;
-  static constexpr int NA = operands(MODE, P);
-  static_assert(MODE == 1 || NA == 2, "gate/up units hold gate and up");
+  static constexpr int RawSf = MODE == 0 ? 2 : 1;  // raw A scale chunks a stage
   static constexpr int BBytes = KN * kKS;
-  static constexpr int StageBytes = NA * kABytes + BBytes + NA * kSfBytes + kSfBytes;
-  static constexpr int S0 = (CPS == 1 ? 226 * 1024 : 111 * 1024) / StageBytes;
+  static constexpr int StageBytes = kABytes + BBytes + RawSf * kSfBytes + kSfBytes;
+  // gate/up: the up rows' values handed to the gate rows, two buffers of 64
+  // rows x XW floats (one pass's tokens, 32 at a time for one plane)
+  static constexpr int XW = (P == 1 ? 32 : KN / P) + 1;
+  static constexpr size_t XBytes = MODE == 0 ? 2 * 64 * XW * 4 : 0;
+  static constexpr int S0 = (int)(((CPS == 1 ? 226 * 1024 : 111 * 1024) - XBytes) / StageBytes);
   static constexpr int S = S0 > 12 ? 12 : S0;
   static constexpr size_t offA = 0;
-  static constexpr size_t offB = offA + (size_t)S * NA * kABytes;
-  static constexpr size_t offSfa = offB + (size_t)S * BBytes;
-  static constexpr size_t offSfb = offSfa + (size_t)S * NA * kSfBytes;
-  static constexpr size_t offBars = offSfb + (size_t)S * kSfBytes;
-  static constexpr uint32_t accCols = NA * KN;      // one accumulator set
-  static constexpr uint32_t sfStride = NA * 4 + 4;  // per stage NA x 4 A, 4 B scale columns
+  static constexpr size_t offB = offA + (size_t)S * kABytes;
+  static constexpr size_t offSfRaw = offB + (size_t)S * BBytes;
+  static constexpr size_t offSfb = offSfRaw + (size_t)S * RawSf * kSfBytes;
+  static constexpr size_t offX = offSfb + (size_t)S * kSfBytes;
+  static constexpr size_t offBars = offX + XBytes;
+  static constexpr uint32_t accCols = KN;      // one accumulator set
+  static constexpr uint32_t sfStride = 4 + 4;  // per stage 4 A, 4 B scale columns
   static constexpr int NACC0 = (int)((TmemCols - S * sfStride) / accCols);
   static constexpr int NACC = NACC0 > 4 ? 4 : NACC0;  // accumulator sets (MMA runs ahead)
   static constexpr uint32_t sfCol = NACC * accCols;
@@ -128,6 +128,7 @@ template <int S, int NACC>
 struct Bars {
   uint64_t full[S], empty[S];
   uint64_t accf[NACC], acce[NACC], fin;
+  uint64_t xfull[2], xempty[2];  // gate/up: the exchange buffers written / read
   uint32_t tmem;
   int err;
 };
@@ -253,12 +254,12 @@ __device__ __forceinline__ void mma_mx(uint32_t d, uint64_t ad, uint64_t bd, uin
 // Weight tiles (read once a call): evict-first in L2, so that the streamed
 // weights do not push out the activation rows every M tile re-reads.
 // Coordinates (element, row in the tile, stage, tile, expert).
-__device__ __forceinline__ void tma5d_stream(void* dst, const ChunkMap* m, int ks, int tile, int e,
-                                             uint64_t* bar, uint64_t pol) {
+__device__ __forceinline__ void tma5d_stream(void* dst, const ChunkMap* m, int r, int ks, int tile,
+                                             int e, uint64_t* bar, uint64_t pol) {
   asm volatile(
       "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
-      "l"(m), "r"(0), "r"(0), "r"(ks), "r"(tile), "r"(e), "r"(smem_u32(bar)), "l"(pol)
+      "l"(m), "r"(0), "r"(r), "r"(ks), "r"(tile), "r"(e), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, const void* src) {
@@ -362,15 +363,23 @@ __device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<
         const uint32_t s = g % G::S, ph = (g / G::S) & 1u;
         if (!wait_or_give_up(&b->empty[s], ph ^ 1u, &b->err)) { ok = false; break; }
         uint64_t* full = &b->full[s];
-        mbar_arrive_expect_tx(full, G::NA * (kATx + kSfBytes) + nb * BR * kKS + kSfBytes);
-        for (int o = 0; o < G::NA; ++o) {
-          uint8_t* as = smem + G::offA + ((size_t)s * G::NA + o) * kABytes;
-          const ChunkMap* m = o == 0 ? &a.amap0 : &a.amap1;
-          const int tile = MODE == 0 ? w.mt : G::NA * w.mt + o;  // 128-row tile of the matrix
-          tma5d_stream(as, m, ks, tile, w.e, full, pol);
-          bulk_g2s(smem + G::offSfa + ((size_t)s * G::NA + o) * kSfBytes,
-                   span + (o == 0 ? a.sfa0 : a.sfa1) + ((size_t)tile * nks + ks) * kSfBytes,
+        mbar_arrive_expect_tx(full, kATx + G::RawSf * kSfBytes + nb * BR * kKS + kSfBytes);
+        uint8_t* as = smem + G::offA + (size_t)s * kABytes;
+        uint8_t* raw = smem + G::offSfRaw + (size_t)s * G::RawSf * kSfBytes;
+        if (MODE == 0) {
+          // 64 gate rows into operand rows 0-63, the same 64 up rows into
+          // rows 64-127; both 128-row tiles' scale chunks
+          const int tile = w.mt >> 1, r0 = kHalfRows * (w.mt & 1);
+          tma5d_stream(as, &a.amap0, r0, ks, tile, w.e, full, pol);
+          tma5d_stream(as + kABytes / 2, &a.amap1, r0, ks, tile, w.e, full, pol);
+          bulk_g2s(raw, span + a.sfa0 + ((size_t)tile * nks + ks) * kSfBytes, kSfBytes, full,
+                   pol);
+          bulk_g2s(raw + kSfBytes, span + a.sfa1 + ((size_t)tile * nks + ks) * kSfBytes,
                    kSfBytes, full, pol);
+        } else {
+          tma5d_stream(as, &a.amap0, 0, ks, w.mt, w.e, full, pol);
+          bulk_g2s(raw, span + a.sfa0 + ((size_t)w.mt * nks + ks) * kSfBytes, kSfBytes, full,
+                   pol);
         }
         uint8_t* bs = smem + G::offB + (size_t)s * G::BBytes;
         for (int i = 0; i < nb; ++i)
@@ -387,9 +396,11 @@ __device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<
     if (armed >> s & 1u) drain(&b->full[s], last_par >> s & 1u);
 }
 
+// The whole MMA warp walks the stages (its lanes assemble a gate/up stage's
+// A scale chunk); lane 0 issues the tensor-core work.
 template <int MODE, int KN, int P>
 __device__ void role_mma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE, KN, P>::S, Geo<MODE, KN, P>::NACC>* b,
-                         uint32_t tmem) {
+                         uint32_t tmem, int lane) {
   using G = Geo<MODE, KN, P>;
   const int nks = a.K / kKS;
   uint32_t g = 0, pc = 0;
@@ -400,38 +411,53 @@ __device__ void role_mma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<
     for (int tb = 0; tb < w.cnt && ok; tb += KN / P, ++pc) {
       const int N = (min(KN / P, w.cnt - tb) * P + 15) & ~15;
       const uint32_t acc = pc % G::NACC;
-      if (!wait_or_give_up(&b->acce[acc], ((pc / G::NACC) & 1u) ^ 1u, &b->err)) { ok = false; break; }
+      if (!warp_wait(&b->acce[acc], ((pc / G::NACC) & 1u) ^ 1u, &b->err)) { ok = false; break; }
       tc_fence_after();
       for (int ks = 0; ks < nks; ++ks, ++g) {
         const uint32_t s = g % G::S, ph = (g / G::S) & 1u;
-        if (!wait_or_give_up(&b->full[s], ph, &b->err)) { ok = false; break; }
+        if (!warp_wait(&b->full[s], ph, &b->err)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t bs = smem_u32(smem + G::offB + (size_t)s * G::BBytes);
-        const uint32_t col = tmem + G::sfCol + G::sfStride * s;
-        // the stage's scales into tensor memory, ahead of its MMAs
-#pragma unroll
-        for (int o = 0; o < G::NA; ++o)
-          tc_cp_sf(col + 4 * o, smem + G::offSfa + ((size_t)s * G::NA + o) * kSfBytes);
-        tc_cp_sf(col + 4 * G::NA, smem + G::offSfb + (size_t)s * kSfBytes);
-#pragma unroll
-        for (int kk = 0; kk < kKS / 32; ++kk) {
-          const uint32_t idesc = umma::idesc_mxf8f6f4_e2m1_e4m3(kM, N, kk, kk);
-          const uint64_t bd = umma::smem_desc_sw128(bs + 32 * kk);
-#pragma unroll
-          for (int o = 0; o < G::NA; ++o) {
-            const uint32_t as = smem_u32(smem + G::offA + ((size_t)s * G::NA + o) * kABytes);
-            mma_mx(tmem + acc * G::accCols + o * KN, umma::smem_desc_sw128(as + 32 * kk), bd,
-                   idesc, col + 4 * o, col + 4 * G::NA, (ks | kk) != 0);
-          }
+        const uint8_t* raw = smem + G::offSfRaw + (size_t)s * G::RawSf * kSfBytes;
+        const uint8_t* sfa = raw;
+        if (MODE == 0) {
+          // the operand's scale chunk: line i = the words of rows i and 32 + i
+          // of the 64 gate rows (words 2h, 2h + 1 of the gate tile's line i,
+          // h the tile half), then those of the 64 up rows
+          // (in place of the gate chunk: lane i alone reads and writes line i)
+          uint8_t* asm_sf = smem + G::offSfRaw + (size_t)s * G::RawSf * kSfBytes;
+          const int h = w.mt & 1;
+          const uint2 gw = *reinterpret_cast<const uint2*>(raw + 16 * lane + 8 * h);
+          const uint2 uw = *reinterpret_cast<const uint2*>(raw + kSfBytes + 16 * lane + 8 * h);
+          *reinterpret_cast<uint4*>(asm_sf + 16 * lane) = make_uint4(gw.x, gw.y, uw.x, uw.y);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          sfa = asm_sf;
         }
-        tc_commit(&b->empty[s]);
+        if (lane == 0) {
+          const uint32_t bs = smem_u32(smem + G::offB + (size_t)s * G::BBytes);
+          const uint32_t as = smem_u32(smem + G::offA + (size_t)s * kABytes);
+          const uint32_t col = tmem + G::sfCol + G::sfStride * s;
+          // the stage's scales into tensor memory, ahead of its MMAs
+          tc_cp_sf(col, sfa);
+          tc_cp_sf(col + 4, smem + G::offSfb + (size_t)s * kSfBytes);
+#pragma unroll
+          for (int kk = 0; kk < kKS / 32; ++kk) {
+            const uint32_t idesc = umma::idesc_mxf8f6f4_e2m1_e4m3(kM, N, kk, kk);
+            mma_mx(tmem + acc * G::accCols, umma::smem_desc_sw128(as + 32 * kk),
+                   umma::smem_desc_sw128(bs + 32 * kk), idesc, col, col + 4, (ks | kk) != 0);
+          }
+          tc_commit(&b->empty[s]);
+        }
+        __syncwarp();
       }
-      if (ok) tc_commit(&b->accf[acc]);
+      if (ok && lane == 0) tc_commit(&b->accf[acc]);
     }
   }
   // every MMA issued completes before the tensor memory is freed
-  tc_commit(&b->fin);
-  drain(&b->fin, 0);
+  if (lane == 0) {
+    tc_commit(&b->fin);
+    drain(&b->fin, 0);
+  }
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t addr, uint32_t (&v)[32]) {
@@ -468,23 +494,53 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t addr, uint32_t (&v)[KN]) {
 }
 
 template <int MODE, int KN, int P>
-__device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN, P>::S, Geo<MODE, KN, P>::NACC>* b,
+__device__ void role_epilogue(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE, KN, P>::S, Geo<MODE, KN, P>::NACC>* b,
                               uint32_t tmem, int warp, int lane) {
   using G = Geo<MODE, KN, P>;
   constexpr int TPP = KN / P;  // tokens a pass
   const int L = 32 * warp + lane;
   const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
-  uint32_t pc = 0;
+  // gate/up: tensor memory lanes 0-63 hold the unit's 64 gate rows (warps 0,
+  // 1), lanes 64-127 the same rows of up (warps 2, 3), which hand their
+  // values to the gate warps through the exchange buffers
+  const bool upw = MODE == 0 && warp >= 2;
+  float* const xbuf = reinterpret_cast<float*>(smem + G::offX);
+  uint32_t pc = 0, xk = 0;
   bool ok = true;
+  // one hand-over of n values a row (up warps: give vals; gate warps: the
+  // up values land in vals); false when a bounded wait gave up
+  auto exchange = [&](float* vals, int n) -> bool {
+    float* buf = xbuf + (size_t)(xk & 1u) * 64 * G::XW;
+    bool fine = true;
+    if (upw) {
+      if (xk >= 2) fine = warp_wait(&b->xempty[xk & 1u], ((xk >> 1) - 1u) & 1u, &b->err);
+      if (fine) {
+#pragma unroll
+        for (int i = 0; i < n; ++i) buf[(L - 64) * G::XW + i] = vals[i];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&b->xfull[xk & 1u]);
+      }
+    } else {
+      fine = warp_wait(&b->xfull[xk & 1u], (xk >> 1) & 1u, &b->err);
+      if (fine) {
+#pragma unroll
+        for (int i = 0; i < n; ++i) vals[i] = buf[L * G::XW + i];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&b->xempty[xk & 1u]);
+      }
+    }
+    ++xk;
+    return fine;
+  };
   for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
     const Unit w = unit_at<P>(a, u);
     if (!w.ok) {
       if (L == 0) atomicOr(a.err, DEV_ERR_RANGE);
       continue;
     }
-    // this thread's row: the h row (gate/up), or the output rows of the
-    // unit's two tiles (down)
-    const int r = MODE == 0 ? kM * w.mt + L : G::NA * kM * w.mt + L;
+    // this thread's row: gate/up, the h row of a gate warp's thread; down,
+    // the output row
+    const int r = MODE == 0 ? kHalfRows * w.mt + L : kM * w.mt + L;
     for (int tb = 0; tb < w.cnt && ok; tb += TPP, ++pc) {
       const int nv = min(TPP, w.cnt - tb);
       const uint32_t acc = pc % G::NACC;
@@ -497,42 +553,43 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN, 
           const int my_a = lane < nc ? a.sorted[w.pos + tb + c0 + lane] : -1;
           uint32_t v[32];
           tmem_ld32(lane_addr + acc * G::accCols + c0, v);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
           if (MODE == 1) {
-            uint32_t v1[32];
-            if (G::NA == 2) tmem_ld32(lane_addr + acc * G::accCols + KN + c0, v1);
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
             for (int n = 0; n < 32; ++n) {
               if (n >= nc) break;
               const int aa = __shfl_sync(0xffffffffu, my_a, n);
               if ((unsigned)aa < (unsigned)a.nassign) {
                 a.part[(size_t)aa * a.H + r] = __uint_as_float(v[n]);
-                if (G::NA == 2) a.part[(size_t)aa * a.H + r + kM] = __uint_as_float(v1[n]);
               } else if (lane == 0) {
                 atomicOr(a.err, DEV_ERR_RANGE);
               }
             }
           } else {
-            uint32_t vu[32];
-            tmem_ld32(lane_addr + acc * G::accCols + KN + c0, vu);
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            const int blk = 4 * w.mt + warp;  // MXFP8 block of h along I
+            float f[32];
 #pragma unroll
-            for (int n = 0; n < 32; ++n) {
-              if (n >= nc) break;
-              const float gt = __uint_as_float(v[n]);
-              const float hv = gt / (1.f + expf(-gt)) * __uint_as_float(vu[n]);
-              const int aa = __shfl_sync(0xffffffffu, my_a, n);
-              if (a.hbuf && (unsigned)aa < (unsigned)a.nassign)
-                a.hbuf[(size_t)aa * a.I + r] = hv;
-              const int sh = mx8_shared_exp(warp_max(fabsf(hv)));
-              const int row = w.pos + tb + c0 + n;
-              a.hq[(size_t)row * a.I + r] = (uint8_t)e4m3_rn_sat(hv * pow2f(-sh));
-              if (lane == 0)
-                put_scale(a.hsf, a.hrows_cap, row, blk, (uint8_t)(sh + 127), scale_places(1));
+            for (int n = 0; n < 32; ++n) f[n] = __uint_as_float(v[n]);
+            if (!exchange(f, 32)) { ok = false; break; }
+            if (!upw) {
+              const int blk = 2 * w.mt + warp;  // MXFP8 block of h along I
+#pragma unroll
+              for (int n = 0; n < 32; ++n) {
+                if (n >= nc) break;
+                const float gt = __uint_as_float(v[n]);
+                const float hv = gt / (1.f + expf(-gt)) * f[n];  // silu(gate) * up
+                const int aa = __shfl_sync(0xffffffffu, my_a, n);
+                if (a.hbuf && (unsigned)aa < (unsigned)a.nassign)
+                  a.hbuf[(size_t)aa * a.I + r] = hv;
+                const int sh = mx8_shared_exp(warp_max(fabsf(hv)));
+                const int row = w.pos + tb + c0 + n;
+                a.hq[(size_t)row * a.I + r] = (uint8_t)e4m3_rn_sat(hv * pow2f(-sh));
+                if (lane == 0)
+                  put_scale(a.hsf, a.hrows_cap, row, blk, (uint8_t)(sh + 127), scale_places(1));
+              }
             }
           }
         }
+        if (!ok) break;
       } else {
         // planes: token n's value is the sum of its P columns, in plane order
         static_assert(KN % 16 == 0 && KN <= 96 && TPP <= 32, "plane pass columns");
@@ -548,31 +605,27 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, Bars<Geo<MODE, KN, 
           for (int q = 1; q < P; ++q) t += __uint_as_float(v[n * P + q]);
           gs[n] = t;
         }
-        // the second operand's columns: up (gate/up) or the second tile (down)
-        if (G::NA == 2) {
-          tmem_ld_cols<KN>(lane_addr + acc * G::accCols + KN, v);
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        float us[TPP];
+        if (MODE == 0) {
+#pragma unroll
+          for (int n = 0; n < TPP; ++n) us[n] = gs[n];
+          if (!exchange(us, TPP)) { ok = false; break; }
         }
+        if (!upw) {
 #pragma unroll
-        for (int n = 0; n < TPP; ++n) {
-          if (n >= nv) break;
-          float y1 = 0.f;
-          if (G::NA == 2) {
-            y1 = __uint_as_float(v[n * P]);
-#pragma unroll
-            for (int q = 1; q < P; ++q) y1 += __uint_as_float(v[n * P + q]);
-          }
-          const int aa = __shfl_sync(0xffffffffu, my_a, n);
-          if ((unsigned)aa < (unsigned)a.nassign) {
-            if (MODE == 0) {
-              const float gt = gs[n];
-              a.hbuf[(size_t)aa * a.I + r] = gt / (1.f + expf(-gt)) * y1;  // silu(gate) * up
-            } else {
-              a.part[(size_t)aa * a.H + r] = gs[n];
-              if (G::NA == 2) a.part[(size_t)aa * a.H + r + kM] = y1;
+          for (int n = 0; n < TPP; ++n) {
+            if (n >= nv) break;
+            const int aa = __shfl_sync(0xffffffffu, my_a, n);
+            if ((unsigned)aa < (unsigned)a.nassign) {
+              if (MODE == 0) {
+                const float gt = gs[n];
+                a.hbuf[(size_t)aa * a.I + r] = gt / (1.f + expf(-gt)) * us[n];  // silu(gate) * up
+              } else {
+                a.part[(size_t)aa * a.H + r] = gs[n];
+              }
+            } else if (lane == 0) {
+              atomicOr(a.err, DEV_ERR_RANGE);
             }
-          } else if (lane == 0) {
-            atomicOr(a.err, DEV_ERR_RANGE);
           }
         }
       }
@@ -606,6 +659,10 @@ __global__ void __launch_bounds__(kThr, ctas_per_sm(MODE, P)) mx8_gemm_kernel(co
       mbar_init(&b->acce[i], 4);
     }
     mbar_init(&b->fin, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&b->xfull[i], 2);
+      mbar_init(&b->xempty[i], 2);
+    }
     b->err = 0;
     fence_barrier_init();
   }
@@ -620,11 +677,11 @@ __global__ void __launch_bounds__(kThr, ctas_per_sm(MODE, P)) mx8_gemm_kernel(co
   }
   const int n_units = n_items * a.MT;
   if (warp < 4) {
-    role_epilogue<MODE, KN, P>(a, n_units, b, tmem, warp, lane);
+    role_epilogue<MODE, KN, P>(a, n_units, smem, b, tmem, warp, lane);
   } else if (warp == kTmaWarp) {
     if (lane == 0) role_tma<MODE, KN, P>(a, n_units, smem, b);
-  } else if (warp == kMmaWarp && lane == 0) {
-    role_mma<MODE, KN, P>(a, n_units, smem, b, tmem);
+  } else if (warp == kMmaWarp) {
+    role_mma<MODE, KN, P>(a, n_units, smem, b, tmem, lane);
   }
   tc_fence_before();
   __syncthreads();
@@ -931,7 +988,7 @@ cudaError_t launch_mx8_kn(const Mx8Args& a, cudaStream_t s) {
     configured = true;
   }
   Mx8Args b = a;
-  if (MODE == 1) b.MT = b.H / (Geo<MODE, KN, P>::NA * kM);  // units of NA 128-row tiles
+  b.MT = MODE == 0 ? b.I / kHalfRows : b.H / kM;  // gate/up: 64-row halves; down: tiles
   const long long units = (long long)b.max_items * b.MT;
   int grid = ctas_per_sm(MODE, P) * sms_mx8();
   if (units < grid) grid = (int)(units > 0 ? units : 1);
@@ -978,7 +1035,8 @@ bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E,
                                 (cuuint64_t)(rows / kM), (cuuint64_t)E};
     const cuuint64_t strides[4] = {(cuuint64_t)kKS / 2, (cuuint64_t)kM * kKS / 2,
                                    (cuuint64_t)K / kKS * kM * kKS / 2, (cuuint64_t)span_bytes};
-    const cuuint32_t box[5] = {kKS, kM, 1, 1, 1};
+    // gate/up: 64-row halves of a tile (a unit's gate or up rows); down: tiles
+    const cuuint32_t box[5] = {kKS, (cuuint32_t)(m < 2 ? kHalfRows : kM), 1, 1, 1};
     const cuuint32_t es[5] = {1, 1, 1, 1, 1};
     if (enc(reinterpret_cast<CUtensorMap*>(maps[m]), CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 5,
             const_cast<uint8_t*>(arena + offs[m]), dims, strides, box, es,
@@ -1078,7 +1136,7 @@ cudaError_t launch_mx8_gateup(const ChunkMap& gate, const ChunkMap& up, const Ch
   a.sfa0 = q;
   a.sfa1 = 2 * q + sb;
   a.K = H;
-  a.MT = I / kM;
+  a.MT = I / kHalfRows;  // (set per geometry at launch)
   a.I = I;
   a.H = H;
   a.bsf = xsf;
@@ -1112,7 +1170,7 @@ cudaError_t launch_mx8_down(const ChunkMap& down, const ChunkMap& hmap, const ui
   a.sfa0 = 3 * q + 2 * sb;
   a.sfa1 = a.sfa0;
   a.K = I;
-  a.MT = H / (2 * kM);  // (set per geometry at launch)
+  a.MT = H / kM;  // (set per geometry at launch)
   a.I = I;
   a.H = H;
   a.bsf = hsf;
