@@ -109,6 +109,12 @@ struct df_moe {
   uint8_t* mx_xsfp = nullptr;  // [mx_xrows][H/32] row-major scales (scratch)
   uint8_t* mx_hsfp = nullptr;  // [mx_hrows][I/32]
   ChunkMap mx_xmap{}, mx_hmap{};
+  // one token on exact planes: two phase kernels with the routed experts on
+  // the block-scaled MMA (x's and h's planes in 16-row boxes; gate and up
+  // sums over parts of K)
+  bool phase_mx8 = false;
+  ChunkMap mx_xmap16{}, mx_hmap16{};
+  float* gu_part = nullptr;  // [kspl][k][2][I]
   bool phase = false;  // decode batches run the two phase kernels
   int sms = 0;
   cudaStream_t cap_stream = nullptr;  // CUDA-graph captures run on it
@@ -483,6 +489,8 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
   const int R = c.n_shared > 0 ? h->R : 0;
   const bool phase = T <= kDecodeMaxT && h->phase;
   const bool cached = h->cache_slots > 0;
+  // one token on exact planes: the routed experts on the block-scaled MMA
+  const bool phase_mx8 = T == 1 && h->phase_mx8 && !cached;
   int sh_gu = 0, sh_dn = 0;
   if (phase && R > 0) {
     // CTAs for the shared experts in each phase: the split that ends both
@@ -509,13 +517,60 @@ int layer_forward(df_moe* h, int l, const uint16_t* x, int T,
     sh_gu = split(gu_sh, gu_rt, T == 1 ? 6.0 : 0.0);
     sh_dn = split(dn_sh, dn_rt, 0.0);
   }
-  int rc = route(h, l, x, T, ids, w, s, nullptr, tg, /*planes_only=*/phase && !cached);
+  if (phase_mx8 && R > 0) {
+    // the same balance with the block-scaled routed pipelines (~40 GB/s an
+    // SM for gate/up and down) against the shared GEMV at one token
+    const double n_rt = std::min(c.top_k, c.n_experts);
+    const double gu_rt = n_rt * 2.0 * c.inter * c.hidden * 17 / 32 / 40e3;
+    const double dn_rt = n_rt * (double)c.hidden * c.inter * 17 / 32 / 40e3;
+    const double gu_sh = 2.0 * R * c.hidden * 2 / 60e3, dn_sh = (double)R * c.hidden * 2 / 68e3;
+    auto split = [&](double sh, double rt, double rt_delay) {
+      int best = 1;
+      double best_t = 1e30;
+      for (int n = 1; n < h->sms; ++n) {
+        const double t = std::max(sh / n, rt / (h->sms - n) + rt_delay);
+        if (t < best_t) { best_t = t; best = n; }
+      }
+      return best;
+    };
+    sh_gu = split(gu_sh, gu_rt, 6.0);
+    sh_dn = split(dn_sh, dn_rt, 0.0);
+  }
+  if (phase_mx8) {
+    // x's planes at the rows of every rank (item j reads rows 4j ..)
+    RUN(h, K_MX8_QUANT, s, launch_mx8_xrows(x, c.hidden, c.top_k, 1, nullptr, h->px, h->mx_xq,
+                                            h->mx_xrows, h->mx_xsfp, h->err, s));
+    RUN(h, K_MX8_QUANT, s, launch_mx8_scale_lines(h->mx_xsfp, c.hidden, c.top_k * h->px,
+                                                  h->mx_xrows, h->px, h->mx_xsf, s));
+  }
+  int rc = route(h, l, x, T, ids, w, s, nullptr, tg,
+                 /*planes_only=*/(phase || phase_mx8) && !cached);
   if (rc) return rc;
   if (cached) {
     rc = cache_plan(h, l, T, ids, s);
     if (rc) return rc;
   }
-  if (phase) {
+  if (phase_mx8) {
+    // gate/up phase (selection, routed gate/up sums, shared h), h = SwiGLU
+    // of the sums as planes, down phase (routed and shared)
+    RUN(h, K_MX8_GU, s, launch_mx8_phase_gateup(L.mx_gate, L.mx_up, h->mx_xmap16, L.arena,
+                                                h->span_bytes, c.hidden, c.inter, h->mx_xsf,
+                                                h->mx_xrows, h->items, h->n_items, h->sorted,
+                                                c.n_experts, c.top_k, h->router_part,
+                                                h->rsplit.nsplit, ids, w, h->gu_part, L.sh_gate,
+                                                L.sh_up, R, x, h->hsh, h->err, sh_gu, s));
+    RUN(h, K_MX8_QUANT, s, launch_mx8_rows(nullptr, c.inter, h->ph, h->items, h->n_items,
+                                           c.top_k, h->sorted, c.top_k, c.n_experts, h->mx_hq,
+                                           h->mx_hrows, h->mx_hsfp, h->err, s, h->gu_part,
+                                           mx8_phase_kspl(c.hidden)));
+    RUN(h, K_MX8_QUANT, s, launch_mx8_scale_lines(h->mx_hsfp, c.inter, c.top_k * h->ph,
+                                                  h->mx_hrows, h->ph, h->mx_hsf, s));
+    RUN(h, K_MX8_DN, s, launch_mx8_phase_down(L.mx_down, h->mx_hmap16, L.arena, h->span_bytes,
+                                              c.hidden, c.inter, h->mx_hsf, h->mx_hrows,
+                                              h->items, h->n_items, h->sorted, c.n_experts,
+                                              c.top_k, h->part, L.sh_down, R, h->hsh, h->ysh,
+                                              h->err, sh_dn, s));
+  } else if (phase) {
     // decode batches: routed and shared experts together on every SM, each
     // kernel a programmatic dependent of the one before
     RUN(h, K_GATEUP, s, launch_phase_gateup(L.sh_gate, L.sh_up, R, L.arena, h->span_bytes,
@@ -722,6 +777,15 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
     if (!rc && (!make_mx8_row_map(h->mx_xq, h->mx_xrows, c.hidden, h->px, &h->mx_xmap) ||
                 !make_mx8_row_map(h->mx_hq, h->mx_hrows, c.inter, h->ph, &h->mx_hmap)))
       rc = fail(h, DF_MOE_ECUDA, "tensor map encoding failed");
+    h->phase_mx8 = h->px > 1 && !slots && k <= 32 && E <= 1024 &&
+                   mx8_phase_supported(c.hidden, c.inter, (int)R);
+    if (!rc && h->phase_mx8) {
+      rc = dalloc(h, &h->gu_part, (size_t)mx8_phase_kspl(c.hidden) * k * 2 * I);
+      if (!rc &&
+          (!make_mx8_row_map(h->mx_xq, h->mx_xrows, c.hidden, h->px, &h->mx_xmap16, 16) ||
+           !make_mx8_row_map(h->mx_hq, h->mx_hrows, c.inter, h->ph, &h->mx_hmap16, 16)))
+        rc = fail(h, DF_MOE_ECUDA, "tensor map encoding failed");
+    }
   }
   if (h->gemm) {
     for (int l = 0; l < c.n_layers && !rc; ++l) {

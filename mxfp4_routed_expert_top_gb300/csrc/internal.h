@@ -317,15 +317,19 @@ bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E,
                    ChunkMap* up, ChunkMap* down);
 // Tensor map of E4M3 activation rows [rows_cap][K], written as `planes`
 // rows a token or assignment (its box covers one pass of the GEMM).
-bool make_mx8_row_map(const uint8_t* rows, int rows_cap, int K, int planes, ChunkMap* map);
+bool make_mx8_row_map(const uint8_t* rows, int rows_cap, int K, int planes, ChunkMap* map,
+                      int box_rows = 0);
 // Rounds h for the down GEMM: row n of item i is source row sorted[pos + n]
 // of src (fp32 [nassign][K], 16-byte aligned), written as `planes` E4M3 rows
 // (pos + n) planes + p of q ([rows_cap][K]) with their scales as row-major
-// scale rows in sfp ([rows_cap][K/32]). planes: 1 or kPlanesH.
+// scale rows in sfp ([rows_cap][K/32]). planes: 1 or kPlanesH. With gu_part
+// (kPlanesH only) the source rows are h = silu(gate) * up of the kspl parts'
+// gate and up sums ([kspl][nassign][2][K], added in part order); src unused.
 cudaError_t launch_mx8_rows(const float* src, int K, int planes, const Item* items,
                             const int32_t* n_items, int max_items, const int32_t* sorted,
                             int nassign, int E, uint8_t* q, int rows_cap, uint8_t* sfp,
-                            uint32_t* err, cudaStream_t s);
+                            uint32_t* err, cudaStream_t s, const float* gu_part = nullptr,
+                            int kspl = 0);
 // Rounds x (bf16 [T][K], 16-byte aligned, K <= 8192) for the gate/up GEMM:
 // each token once, written to the rows of its k assignments, rows
 // inv[t k + j] planes + p of q, scale rows as above. inv: the grouping's
@@ -361,5 +365,32 @@ cudaError_t launch_mx8_down(const ChunkMap& down, const ChunkMap& hmap, const ui
                             const Item* items, const int32_t* n_items, int max_items,
                             const int32_t* sorted, int E, int nassign, float* part,
                             int planes, uint32_t* err, cudaStream_t s);
+
+// One token on an exact-planes handle as two phase kernels (one CTA an SM;
+// the first n_sh CTAs stream the shared experts, R > 0). Gate/up: x's planes
+// at rows 4j .. 4j + 3 for every rank j (launch_mx8_xrows with k, no inv);
+// each routed CTA selects the experts from the router's partial logits
+// (nsplit planes) and the first publishes them (items, sorted, n_items, ids,
+// w); the routed gate/up writes gate and up sums over mx8_phase_kspl(H)
+// parts of K into gu_part [kspl][k][2][I] (SwiGLU by launch_mx8_rows); the
+// shared CTAs write hsh. Down: h's planes at rows 5j .. 5j + 4; part [k][H]
+// and ysh. Row maps: boxes of 16 rows.
+int mx8_phase_kspl(int H);
+bool mx8_phase_supported(int H, int I, int R);
+cudaError_t launch_mx8_phase_gateup(const ChunkMap& gate, const ChunkMap& up,
+                                    const ChunkMap& xmap16, const uint8_t* arena,
+                                    size_t span_bytes, int H, int I, const uint8_t* xsf,
+                                    int rows_cap, Item* items, int32_t* n_items,
+                                    int32_t* sorted, int E, int k, const float* router_part,
+                                    int nsplit, int32_t* ids, float* w, float* gu_part,
+                                    const uint16_t* sh_gate, const uint16_t* sh_up, int R,
+                                    const uint16_t* x, float* hsh, uint32_t* err, int n_sh,
+                                    cudaStream_t s);
+cudaError_t launch_mx8_phase_down(const ChunkMap& down, const ChunkMap& hmap16,
+                                  const uint8_t* arena, size_t span_bytes, int H, int I,
+                                  const uint8_t* hsf, int rows_cap, const Item* items,
+                                  const int32_t* n_items, const int32_t* sorted, int E, int k,
+                                  float* part, const uint16_t* sh_down, int R, const float* hsh,
+                                  float* ysh, uint32_t* err, int n_sh, cudaStream_t s);
 
 }  // namespace dfm

@@ -54,8 +54,10 @@
 
 #include <algorithm>
 
+#include "bfv.cuh"
 #include "internal.h"
 #include "pipeline.cuh"
+#include "select.cuh"
 #include "umma.cuh"
 
 namespace dfm {
@@ -103,6 +105,7 @@ struct Geo {
   static constexpr int CPS = ctas_per_sm(MODE, P);
   static constexpr uint32_t TmemCols = kTmemCols / CPS;
   static constexpr int RawSf = MODE == 0 ? 2 : 1;  // raw A scale chunks a stage
+  static constexpr int BR = KN < box_rows(P) ? KN : box_rows(P);  // B rows a box
   static constexpr int BBytes = KN * kKS;
   static constexpr int StageBytes = kABytes + BBytes + RawSf * kSfBytes + kSfBytes;
   // gate/up: the up rows' values handed to the gate rows, two buffers of 64
@@ -170,6 +173,11 @@ struct Mx8Args {
   int hrows_cap;          // gate/up: rows of hq
   float* part;            // down: [nassign][H]
   uint32_t* err;
+  // gate/up of one token beside the shared experts: each unit covers
+  // 1/kspl of K and writes its gate and up sums, before SwiGLU, to
+  // gu_part [kspl][nassign][2][I] (kspl 0 or 1: whole K, h out)
+  int kspl;
+  float* gu_part;
 };
 
 // ---------------------------------------------------------------------------
@@ -316,18 +324,25 @@ __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// The sequence every role walks: the CTA's units (u = blockIdx.x + j *
-// gridDim.x), each one's passes of at most KN tokens, each pass's stages.
+// The sequence every role walks: the pipeline's units (u = vcta + j *
+// nvcta), each one's passes of at most KN tokens, each pass's stages
+// [kb, ke) (all of K, or the unit's part of it).
 struct Unit {
   bool ok;
-  int e, mt, pos, cnt;
+  int e, mt, pos, cnt, ks, kb, ke;
 };
+__device__ __forceinline__ int kspl_of(const Mx8Args& a) { return a.kspl > 1 ? a.kspl : 1; }
 template <int P>
-__device__ __forceinline__ Unit unit_at(const Mx8Args& a, int u) {
+__device__ __forceinline__ Unit unit_at(const Mx8Args& a, const Item* items, int u) {
   Unit w;
-  const int item = u / a.MT;
-  w.mt = u - item * a.MT;
-  const Item it = a.items[item];
+  const int ksp = kspl_of(a), per_item = a.MT * ksp;
+  const int item = u / per_item, rem = u - item * per_item;
+  w.mt = rem / ksp;
+  w.ks = rem - w.mt * ksp;
+  const int nks = a.K / kKS;
+  w.kb = nks * w.ks / ksp;
+  w.ke = nks * (w.ks + 1) / ksp;
+  const Item it = items[item];
   w.e = it.e;
   w.pos = it.pos;
   w.cnt = it.cnt;
@@ -341,25 +356,41 @@ __device__ __forceinline__ Unit unit_at(const Mx8Args& a, int u) {
 // roles
 // ---------------------------------------------------------------------------
 
+// Where one pipeline (a TMA warp, an MMA warp, four epilogue warps) lives:
+// its shared memory (the Geo layout) and barriers, its first tensor memory
+// column, its index among the grid's pipelines, and the selection it reads
+// (global, or a copy in shared memory).
 template <int MODE, int KN, int P>
-__device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE, KN, P>::S, Geo<MODE, KN, P>::NACC>* b) {
+struct Pipe {
+  uint8_t* smem;
+  Bars<Geo<MODE, KN, P>::S, Geo<MODE, KN, P>::NACC>* b;
+  uint32_t tmem;
+  int vcta, nvcta;
+  const Item* items;
+  const int32_t* sorted;
+};
+
+template <int MODE, int KN, int P>
+__device__ void role_tma(const Mx8Args& a, int n_units, const Pipe<MODE, KN, P>& c) {
   using G = Geo<MODE, KN, P>;
+  uint8_t* const smem = c.smem;
+  auto* const b = c.b;
   const int nks = a.K / kKS;
   uint32_t g = 0;
   uint32_t armed = 0u, last_par = 0u;
   bool ok = true;
   const uint64_t pol = l2_evict_first_policy();
-  for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-    const Unit w = unit_at<P>(a, u);
+  for (int u = c.vcta; u < n_units && ok; u += c.nvcta) {
+    const Unit w = unit_at<P>(a, c.items, u);
     if (!w.ok) continue;
     const uint8_t* span = a.arena + (size_t)w.e * a.span_bytes;
     for (int tb = 0; tb < w.cnt && ok; tb += KN / P) {
       const int nr = min(KN / P, w.cnt - tb) * P;  // B rows of the pass (tokens x planes)
-      constexpr int BR = box_rows(P);
+      constexpr int BR = G::BR;
       static_assert(KN % BR == 0, "B boxes of a pass");
       const int nb = (nr + BR - 1) / BR;
       const int row = (w.pos + tb) * P;
-      for (int ks = 0; ks < nks; ++ks, ++g) {
+      for (int ks = w.kb; ks < w.ke; ++ks, ++g) {
         const uint32_t s = g % G::S, ph = (g / G::S) & 1u;
         if (!wait_or_give_up(&b->empty[s], ph ^ 1u, &b->err)) { ok = false; break; }
         uint64_t* full = &b->full[s];
@@ -399,21 +430,22 @@ __device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<
 // The whole MMA warp walks the stages (its lanes assemble a gate/up stage's
 // A scale chunk); lane 0 issues the tensor-core work.
 template <int MODE, int KN, int P>
-__device__ void role_mma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE, KN, P>::S, Geo<MODE, KN, P>::NACC>* b,
-                         uint32_t tmem, int lane) {
+__device__ void role_mma(const Mx8Args& a, int n_units, const Pipe<MODE, KN, P>& c, int lane) {
   using G = Geo<MODE, KN, P>;
-  const int nks = a.K / kKS;
+  uint8_t* const smem = c.smem;
+  auto* const b = c.b;
+  const uint32_t tmem = c.tmem;
   uint32_t g = 0, pc = 0;
   bool ok = true;
-  for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-    const Unit w = unit_at<P>(a, u);
+  for (int u = c.vcta; u < n_units && ok; u += c.nvcta) {
+    const Unit w = unit_at<P>(a, c.items, u);
     if (!w.ok) continue;
     for (int tb = 0; tb < w.cnt && ok; tb += KN / P, ++pc) {
       const int N = (min(KN / P, w.cnt - tb) * P + 15) & ~15;
       const uint32_t acc = pc % G::NACC;
       if (!warp_wait(&b->acce[acc], ((pc / G::NACC) & 1u) ^ 1u, &b->err)) { ok = false; break; }
       tc_fence_after();
-      for (int ks = 0; ks < nks; ++ks, ++g) {
+      for (int ks = w.kb; ks < w.ke; ++ks, ++g) {
         const uint32_t s = g % G::S, ph = (g / G::S) & 1u;
         if (!warp_wait(&b->full[s], ph, &b->err)) { ok = false; break; }
         tc_fence_after();
@@ -444,7 +476,8 @@ __device__ void role_mma(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<
           for (int kk = 0; kk < kKS / 32; ++kk) {
             const uint32_t idesc = umma::idesc_mxf8f6f4_e2m1_e4m3(kM, N, kk, kk);
             mma_mx(tmem + acc * G::accCols, umma::smem_desc_sw128(as + 32 * kk),
-                   umma::smem_desc_sw128(bs + 32 * kk), idesc, col, col + 4, (ks | kk) != 0);
+                   umma::smem_desc_sw128(bs + 32 * kk), idesc, col, col + 4,
+                   ks != w.kb || kk != 0);
           }
           tc_commit(&b->empty[s]);
         }
@@ -493,10 +526,14 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t addr, uint32_t (&v)[KN]) {
   if constexpr (KN % 32 == 16) tmem_ld16(addr + KN - 16, v + KN - 16);
 }
 
+// `warp`: the warp's tensor memory lane quarter (its index mod 4).
 template <int MODE, int KN, int P>
-__device__ void role_epilogue(const Mx8Args& a, int n_units, uint8_t* smem, Bars<Geo<MODE, KN, P>::S, Geo<MODE, KN, P>::NACC>* b,
-                              uint32_t tmem, int warp, int lane) {
+__device__ void role_epilogue(const Mx8Args& a, int n_units, const Pipe<MODE, KN, P>& c, int warp,
+                              int lane) {
   using G = Geo<MODE, KN, P>;
+  uint8_t* const smem = c.smem;
+  auto* const b = c.b;
+  const uint32_t tmem = c.tmem;
   constexpr int TPP = KN / P;  // tokens a pass
   const int L = 32 * warp + lane;
   const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
@@ -532,8 +569,9 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, uint8_t* smem, Bars
     ++xk;
     return fine;
   };
-  for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-    const Unit w = unit_at<P>(a, u);
+  const bool split = kspl_of(a) > 1;
+  for (int u = c.vcta; u < n_units && ok; u += c.nvcta) {
+    const Unit w = unit_at<P>(a, c.items, u);
     if (!w.ok) {
       if (L == 0) atomicOr(a.err, DEV_ERR_RANGE);
       continue;
@@ -547,10 +585,11 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, uint8_t* smem, Bars
       if (!warp_wait(&b->accf[acc], (pc / G::NACC) & 1u, &b->err)) { ok = false; break; }
       tc_fence_after();
       if constexpr (P == 1) {
+        // (one plane: whole K only)
         for (int c0 = 0; c0 < nv; c0 += 32) {
           const int nc = min(32, nv - c0);
           // the chunk's assignment indices, one a lane, fetched together
-          const int my_a = lane < nc ? a.sorted[w.pos + tb + c0 + lane] : -1;
+          const int my_a = lane < nc ? c.sorted[w.pos + tb + c0 + lane] : -1;
           uint32_t v[32];
           tmem_ld32(lane_addr + acc * G::accCols + c0, v);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -593,7 +632,7 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, uint8_t* smem, Bars
       } else {
         // planes: token n's value is the sum of its P columns, in plane order
         static_assert(KN % 16 == 0 && KN <= 96 && TPP <= 32, "plane pass columns");
-        const int my_a = lane < nv ? a.sorted[w.pos + tb + lane] : -1;
+        const int my_a = lane < nv ? c.sorted[w.pos + tb + lane] : -1;
         uint32_t v[KN];
         float gs[TPP];
         tmem_ld_cols<KN>(lane_addr + acc * G::accCols, v);
@@ -606,12 +645,25 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, uint8_t* smem, Bars
           gs[n] = t;
         }
         float us[TPP];
-        if (MODE == 0) {
+        if (MODE == 0 && split) {
+          // a part of K: every row's sum as it stands (gate rows from warps
+          // 0, 1; up rows from warps 2, 3), SwiGLU after the parts are added
+          const int rr = kHalfRows * w.mt + (L & (kHalfRows - 1));
+#pragma unroll
+          for (int n = 0; n < TPP; ++n) {
+            if (n >= nv) break;
+            const int aa = __shfl_sync(0xffffffffu, my_a, n);
+            if ((unsigned)aa < (unsigned)a.nassign)
+              a.gu_part[(((size_t)w.ks * a.nassign + aa) * 2 + (upw ? 1 : 0)) * a.I + rr] = gs[n];
+            else if (lane == 0)
+              atomicOr(a.err, DEV_ERR_RANGE);
+          }
+        } else if (MODE == 0) {
 #pragma unroll
           for (int n = 0; n < TPP; ++n) us[n] = gs[n];
           if (!exchange(us, TPP)) { ok = false; break; }
         }
-        if (!upw) {
+        if (!upw && !(MODE == 0 && split)) {
 #pragma unroll
           for (int n = 0; n < TPP; ++n) {
             if (n >= nv) break;
@@ -675,13 +727,14 @@ __global__ void __launch_bounds__(kThr, ctas_per_sm(MODE, P)) mx8_gemm_kernel(co
     if (threadIdx.x == 0) atomicOr(a.err, DEV_ERR_RANGE);
     n_items = n_items < 0 ? 0 : a.max_items;
   }
-  const int n_units = n_items * a.MT;
+  const int n_units = n_items * a.MT * kspl_of(a);
+  const Pipe<MODE, KN, P> c{smem, b, tmem, (int)blockIdx.x, (int)gridDim.x, a.items, a.sorted};
   if (warp < 4) {
-    role_epilogue<MODE, KN, P>(a, n_units, smem, b, tmem, warp, lane);
+    role_epilogue<MODE, KN, P>(a, n_units, c, warp, lane);
   } else if (warp == kTmaWarp) {
-    if (lane == 0) role_tma<MODE, KN, P>(a, n_units, smem, b);
+    if (lane == 0) role_tma<MODE, KN, P>(a, n_units, c);
   } else if (warp == kMmaWarp) {
-    role_mma<MODE, KN, P>(a, n_units, smem, b, tmem, lane);
+    role_mma<MODE, KN, P>(a, n_units, c, lane);
   }
   tc_fence_before();
   __syncthreads();
@@ -690,6 +743,182 @@ __global__ void __launch_bounds__(kThr, ctas_per_sm(MODE, P)) mx8_gemm_kernel(co
   if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(G::TmemCols)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// One token on a block-scaled handle, beside the shared experts
+// ---------------------------------------------------------------------------
+
+// One token's selection inside a kernel that runs its experts: the router's
+// partial logits and where the selection goes.
+struct SelArgs {
+  const float* part;   // router partial logits [nsplit][E]; null: selected already
+  int nsplit, E, k;
+  int32_t* ids;        // [k] outputs, best first
+  float* w;
+};
+
+// The token's top k by the whole CTA (NW warps), from the logits summed in
+// plane order. Every CTA that calls gets the same selection (same sums, same
+// network). Item q is the expert of rank q with its one assignment q: the
+// items and the sorted list go to shared memory (sel_items, sel_sorted,
+// *sel_n); with `pub` also the ids and softmax weights and the items,
+// sorted list and count to global memory, followed by a fence. `scratch`:
+// NW * 32 floats and as many ints. Every thread calls; on return the shared
+// copies are complete after a __syncthreads.
+template <int NW>
+__device__ void select_one_token(const SelArgs& sel, uint8_t* scratch, Item* sel_items,
+                                 int32_t* sel_sorted, int32_t* sel_n, Item* g_items,
+                                 int32_t* g_sorted, int32_t* g_n, bool pub) {
+  float sel_v = 0.f;
+  int sel_e = 0;
+  block_topk<NW>([&](int i) { return sum_planes<true>(sel.part + i, sel.E, sel.nsplit); },
+                 sel.E, reinterpret_cast<float*>(scratch),
+                 reinterpret_cast<int*>(scratch + NW * 32 * sizeof(float)), sel_v, sel_e);
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const float wt = pub ? selected_softmax(sel.k, sel_v) : 0.f;
+    if (lane < sel.k) {
+      sel_items[lane] = Item{sel_e, lane, 1, 0};
+      sel_sorted[lane] = lane;
+      if (pub) {
+        sel.ids[lane] = sel_e;
+        sel.w[lane] = wt;
+        g_items[lane] = Item{sel_e, lane, 1, 0};
+        g_sorted[lane] = lane;
+      }
+    }
+    if (lane == 0) {
+      *sel_n = sel.k;
+      if (pub) *g_n = sel.k;
+    }
+    if (pub) __threadfence();
+  }
+}
+
+constexpr int kPhThr = 512;
+constexpr int kPhKN = 16;  // B rows a pass: the token's planes (4 of x, 5 of h), MMA N 16
+template <int MODE>
+struct PhGeo {
+  static constexpr int P = MODE == 0 ? kPlanesX : kPlanesH;
+  using G = Geo<MODE, kPhKN, P>;
+  // a pipeline's share of the CTA's shared memory (the batch GEMM's layout
+  // for two CTAs an SM), a multiple of 1024 bytes
+  static constexpr size_t Pipe = (smem_bytes<MODE, kPhKN, P>() + 1023) & ~(size_t)1023;
+};
+static_assert(geo_ok<0, kPhKN, kPlanesX>() && geo_ok<1, kPhKN, kPlanesH>(), "phase pipelines");
+
+// A decode step of one token as two phase kernels whose routed experts run
+// on the block-scaled MMA: the CTAs below n_sh stream the shared experts
+// (the bf16 GEMV), every other CTA runs two pipelines of the batch GEMM
+// (warps 0-5 and 6-11, each with half the CTA's shared and tensor memory, as
+// two CTAs an SM do in the batch GEMM) over the 16 selected experts. Gate/up
+// (MODE 0): each routed CTA selects the experts itself from the router's
+// partial logits (the first one publishes them), and each unit covers 1/kspl
+// of K and writes its gate and up sums (SwiGLU follows once the parts are
+// added, in mx8_rows_kernel). Down (MODE 1): the selection comes from the
+// gate/up phase, h's planes from the kernels between. The K split evens out
+// the load: 16 experts x 24 half-tiles are too few units for the routed CTAs.
+template <int MODE>
+__global__ void __launch_bounds__(kPhThr, 1)
+    mx8_phase_kernel(const __grid_constant__ Mx8Args a, const BfvArgs sh, const SelArgs sel,
+                     int n_sh) {
+  constexpr int P = PhGeo<MODE>::P;
+  using G = typename PhGeo<MODE>::G;
+  using Bs = Bars<G::S, G::NACC>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ uint64_t bfv_bars[kBfvBars];
+  __shared__ Item sel_items[32];
+  __shared__ int32_t sel_sorted[32];
+  __shared__ int32_t sel_n;
+  if ((int)blockIdx.x < n_sh) {
+    // gate/up: x is complete when the grid starts; down: the shared h is
+    // the gate/up phase's
+    bfv_cta<MODE, 1>(sh, smem, bfv_bars, blockIdx.x, n_sh, /*wait=*/MODE == 1);
+    return;
+  }
+  const int cta = blockIdx.x - n_sh, ncta = gridDim.x - n_sh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pipe = warp / 6, role = warp - 6 * pipe;  // warps 12-15 only help select
+  Bs* const b0 = reinterpret_cast<Bs*>(smem + G::offBars);
+  // set-up while the preceding kernel finishes: the SM's tensor memory (half
+  // a pipeline) and each pipeline's barriers
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&b0->tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (lane == 0 && role == 5 && pipe < 2) {
+    Bs* b = reinterpret_cast<Bs*>(smem + pipe * PhGeo<MODE>::Pipe + G::offBars);
+    for (int i = 0; i < G::S; ++i) {
+      mbar_init(&b->full[i], 1);
+      mbar_init(&b->empty[i], 1);
+    }
+    for (int i = 0; i < G::NACC; ++i) {
+      mbar_init(&b->accf[i], 1);
+      mbar_init(&b->acce[i], 4);
+    }
+    mbar_init(&b->fin, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&b->xfull[i], 2);
+      mbar_init(&b->xempty[i], 2);
+    }
+    b->err = 0;
+    fence_barrier_init();
+  }
+  pdl_wait();  // gate/up: the router's partial logits; down: h's planes
+  const Item* items = a.items;
+  const int32_t* sorted = a.sorted;
+  int n_items;
+  if (MODE == 0) {
+    select_one_token<kPhThr / 32>(sel, smem, sel_items, sel_sorted, &sel_n,
+                                  const_cast<Item*>(a.items), const_cast<int32_t*>(a.sorted),
+                                  const_cast<int32_t*>(a.n_items), cta == 0);
+    // (the selection's scratch is stage memory the copies fill next)
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    items = sel_items;
+    sorted = sel_sorted;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (MODE == 0) {
+    n_items = sel_n;
+  } else {
+    n_items = __ldcg(a.n_items);
+    if (n_items < 0 || n_items > a.max_items) {
+      if (threadIdx.x == 0) atomicOr(a.err, DEV_ERR_RANGE);
+      n_items = n_items < 0 ? 0 : a.max_items;
+    }
+  }
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(&b0->tmem);
+  const int n_units = n_items * a.MT * kspl_of(a);
+  if (pipe < 2) {
+    const Pipe<MODE, kPhKN, P> c{smem + pipe * PhGeo<MODE>::Pipe,
+                                 reinterpret_cast<Bs*>(smem + pipe * PhGeo<MODE>::Pipe + G::offBars),
+                                 tmem + pipe * (kTmemCols / 2), 2 * cta + pipe, 2 * ncta, items,
+                                 sorted};
+    if (role < 4) {
+      role_epilogue<MODE, kPhKN, P>(a, n_units, c, warp & 3, lane);
+    } else if (role == 4) {
+      if (lane == 0) role_tma<MODE, kPhKN, P>(a, n_units, c);
+    } else {
+      role_mma<MODE, kPhKN, P>(a, n_units, c, lane);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0) {
+    const Bs* b1 = reinterpret_cast<const Bs*>(smem + PhGeo<MODE>::Pipe + G::offBars);
+    if (b0->err || b1->err) atomicOr(a.err, DEV_ERR_TIMEOUT);
+  }
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
                  : "memory");
 }
 
@@ -785,12 +1014,15 @@ __global__ void __launch_bounds__(256) mx8_scale_lines_kernel(const uint8_t* __r
 // item, thread = one (row, 32-column block) pair of the item. Row n of item
 // i is source row sorted[pos + n] (an assignment); its P planes go to q rows
 // (pos + n) P + p.
+// With gu_part (gate and up sums over kspl parts of K, [kspl][nassign][2][K])
+// the rows are h = SwiGLU of the parts' sums, added in part order.
 template <int P>
 __global__ void __launch_bounds__(256) mx8_rows_kernel(const float* src, int K, const Item* items,
                                                        const int32_t* n_items, int max_items,
                                                        const int32_t* sorted, int nassign, int E,
                                                        uint8_t* q, uint8_t* sfp, int rows_cap,
-                                                       uint32_t* err) {
+                                                       uint32_t* err, const float* gu_part,
+                                                       int kspl) {
   const int i = blockIdx.x;
   int ni = *n_items;
   if (ni > max_items) ni = max_items;
@@ -815,7 +1047,30 @@ __global__ void __launch_bounds__(256) mx8_rows_kernel(const float* src, int K, 
     if (bad && t < total && j == 0) atomicOr(err, DEV_ERR_RANGE);
     const bool live = t < total && !bad;
     float v[32];
-    if (live) {
+    if (live && gu_part) {
+      float gs[32], us[32];
+#pragma unroll
+      for (int m = 0; m < 32; ++m) gs[m] = us[m] = 0.f;
+      for (int ks = 0; ks < kspl; ++ks) {
+        const float4* pg =
+            reinterpret_cast<const float4*>(gu_part + ((size_t)ks * nassign + aa) * 2 * K + 32 * j);
+        const float4* pu = pg + K / 4;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 f = pg[c], g = pu[c];
+          gs[4 * c] += f.x;
+          gs[4 * c + 1] += f.y;
+          gs[4 * c + 2] += f.z;
+          gs[4 * c + 3] += f.w;
+          us[4 * c] += g.x;
+          us[4 * c + 1] += g.y;
+          us[4 * c + 2] += g.z;
+          us[4 * c + 3] += g.w;
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < 32; ++m) v[m] = gs[m] / (1.f + expf(-gs[m])) * us[m];  // silu(gate) * up
+    } else if (live) {
       const float4* p = reinterpret_cast<const float4*>(src + (size_t)aa * K + 32 * j);
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
@@ -1047,12 +1302,13 @@ bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E,
   return true;
 }
 
-bool make_mx8_row_map(const uint8_t* rows_buf, int rows_cap, int K, int planes, ChunkMap* map) {
+bool make_mx8_row_map(const uint8_t* rows_buf, int rows_cap, int K, int planes, ChunkMap* map,
+                      int box_r) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   if (!enc) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows_cap};
   const cuuint64_t strides[1] = {(cuuint64_t)K};
-  const cuuint32_t box[2] = {kKS, (cuuint32_t)box_rows(planes)};
+  const cuuint32_t box[2] = {kKS, (cuuint32_t)(box_r > 0 ? box_r : box_rows(planes))};
   const cuuint32_t es[2] = {1, 1};
   return enc(reinterpret_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
              const_cast<uint8_t*>(rows_buf), dims, strides, box, es,
@@ -1074,11 +1330,12 @@ cudaError_t launch_mx8_scale_lines(const uint8_t* sfp, int K, int rows, int rows
 cudaError_t launch_mx8_rows(const float* src, int K, int planes, const Item* items,
                             const int32_t* n_items, int max_items, const int32_t* sorted,
                             int nassign, int E, uint8_t* q, int rows_cap, uint8_t* sfp,
-                            uint32_t* err, cudaStream_t s) {
+                            uint32_t* err, cudaStream_t s, const float* gu_part, int kspl) {
   if (max_items <= 0) return cudaSuccess;
+  if (gu_part && (planes == 1 || kspl < 1)) return cudaErrorInvalidValue;
   auto go = [&](auto kernel) {
     kernel<<<max_items, 256, 0, s>>>(src, K, items, n_items, max_items, sorted, nassign, E, q,
-                                     sfp, rows_cap, err);
+                                     sfp, rows_cap, err, gu_part, kspl);
     return cudaGetLastError();
   };
   if (planes == 1) return go(mx8_rows_kernel<1>);
@@ -1184,6 +1441,113 @@ cudaError_t launch_mx8_down(const ChunkMap& down, const ChunkMap& hmap, const ui
   a.part = part;
   a.err = err;
   return launch_mx8<1>(a, planes, s);
+}
+
+namespace {
+
+template <int MODE>
+cudaError_t launch_phase_mx8(const Mx8Args& a, const BfvArgs& sh, const SelArgs& sel, int n_sh,
+                             cudaStream_t s) {
+  const int sms = sms_mx8();
+  if (n_sh < 0 || n_sh >= sms || (n_sh > 0 && sh.rows <= 0)) return cudaErrorInvalidValue;
+  const size_t smem =
+      std::max(2 * PhGeo<MODE>::Pipe, n_sh > 0 ? bfv_smem_bytes(sh.K) : (size_t)0);
+  static size_t configured = 0;
+  if (configured < smem) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        mx8_phase_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  return launch_after_previous(mx8_phase_kernel<MODE>, dim3(sms), dim3(kPhThr), smem, s, a, sh,
+                               sel, n_sh);
+}
+
+}  // namespace
+
+int mx8_phase_kspl(int H) {
+  // parts of K a gate/up unit: 16 x (I/64) half-tiles are too few units for
+  // ~230 routed pipelines; eight parts give each ~13
+  const int nks = H / kKS;
+  return std::max(1, std::min(8, nks));
+}
+
+bool mx8_phase_supported(int H, int I, int R) {
+  return mx8_supported(H, I) && I % kHalfRows == 0 && (R == 0 || bfv_smem_bytes(H) <= 220 * 1024);
+}
+
+cudaError_t launch_mx8_phase_gateup(const ChunkMap& gate, const ChunkMap& up,
+                                    const ChunkMap& xmap16, const uint8_t* arena,
+                                    size_t span_bytes, int H, int I, const uint8_t* xsf,
+                                    int rows_cap, Item* items, int32_t* n_items,
+                                    int32_t* sorted, int E, int k, const float* router_part,
+                                    int nsplit, int32_t* ids, float* w, float* gu_part,
+                                    const uint16_t* sh_gate, const uint16_t* sh_up, int R,
+                                    const uint16_t* x, float* hsh, uint32_t* err, int n_sh,
+                                    cudaStream_t s) {
+  if (!router_part || !gu_part || k > 32 || (R > 0 && !hsh)) return cudaErrorInvalidValue;
+  const size_t q = (size_t)H * I / 2, sb = (size_t)H * I / 32;
+  Mx8Args a{};
+  a.amap0 = gate;
+  a.amap1 = up;
+  a.bmap = xmap16;
+  a.arena = arena;
+  a.span_bytes = span_bytes;
+  a.sfa0 = q;
+  a.sfa1 = 2 * q + sb;
+  a.K = H;
+  a.MT = I / kHalfRows;
+  a.I = I;
+  a.H = H;
+  a.bsf = xsf;
+  a.rows_cap = rows_cap;
+  a.items = items;
+  a.n_items = n_items;
+  a.sorted = sorted;
+  a.max_items = k;
+  a.E = E;
+  a.nassign = k;
+  a.err = err;
+  a.kspl = mx8_phase_kspl(H);
+  a.gu_part = gu_part;
+  const BfvArgs sh{sh_gate, sh_up, R, H, x, 1, hsh, err};
+  const SelArgs sel{router_part, nsplit, E, k, ids, w};
+  return launch_phase_mx8<0>(a, sh, sel, R > 0 ? n_sh : 0, s);
+}
+
+cudaError_t launch_mx8_phase_down(const ChunkMap& down, const ChunkMap& hmap16,
+                                  const uint8_t* arena, size_t span_bytes, int H, int I,
+                                  const uint8_t* hsf, int rows_cap, const Item* items,
+                                  const int32_t* n_items, const int32_t* sorted, int E, int k,
+                                  float* part, const uint16_t* sh_down, int R, const float* hsh,
+                                  float* ysh, uint32_t* err, int n_sh, cudaStream_t s) {
+  if (k > 32 || (R > 0 && (!hsh || !ysh))) return cudaErrorInvalidValue;
+  const size_t q = (size_t)H * I / 2, sb = (size_t)H * I / 32;
+  Mx8Args a{};
+  a.amap0 = down;
+  a.amap1 = down;
+  a.bmap = hmap16;
+  a.arena = arena;
+  a.span_bytes = span_bytes;
+  a.sfa0 = 3 * q + 2 * sb;
+  a.sfa1 = a.sfa0;
+  a.K = I;
+  a.MT = H / kM;
+  a.I = I;
+  a.H = H;
+  a.bsf = hsf;
+  a.rows_cap = rows_cap;
+  a.items = items;
+  a.n_items = n_items;
+  a.sorted = sorted;
+  a.max_items = k;
+  a.E = E;
+  a.nassign = k;
+  a.part = part;
+  a.err = err;
+  const BfvArgs sh{sh_down, nullptr, R > 0 ? H : 0, R > 0 ? R : I, hsh, 1, ysh, err};
+  const SelArgs sel{nullptr, 0, E, k, nullptr, nullptr};
+  return launch_phase_mx8<1>(a, sh, sel, R > 0 ? n_sh : 0, s);
 }
 
 }  // namespace dfm

@@ -171,3 +171,47 @@ def test_k3_batch512(k3, torch):
     ref = orc.moe_layer(k3.layers[0], x[sample])
     check_out(out32[sample], ref["out"])
     assert np.all(np.isfinite(out32))
+
+
+def test_k3_decode_batch1(k3, torch):
+    """One token on a planes handle runs the two phase kernels with the
+    routed experts on the block-scaled MMA (gate/up in eight parts of K, h =
+    SwiGLU of the parts' sums): full outputs at the layer bars, ids exact."""
+    for t in range(3):
+        x = np.stack([synth.token(K3.seed, K3.cfg_id, 9700 + t, K3.H)])
+        out, out32, ids, w = _forward(k3.m, x, 1, torch)
+        ref = orc.moe_layer(k3.layers[0], x)
+        check_ids_weights(ids, w, ref["ids"], ref["w"])
+        check_out(out32, ref["out"])
+        rne = torch.from_numpy(out32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(out, rne)
+
+
+def test_k3_decode_batch1_repeatable(k3, torch):
+    """The phase path's sums run in a fixed order: the same token twice gives
+    the same bits."""
+    x = np.stack([synth.token(K3.seed, K3.cfg_id, 9750, K3.H)])
+    a = _forward(k3.m, x, 1, torch)[1]
+    b = _forward(k3.m, x, 1, torch)[1]
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+# no shared experts (every CTA of the phase kernels routed), and a K that
+# the eight parts split unevenly (H = 1280: 10 stages of 128, parts of one
+# and two stages)
+NOSH = Workload("noshared-h1280-i384-e12-top3", 6, H=1280, I=384, E=12, k=3, n_shared=0,
+                Is=0, T=1)
+
+
+@pytest.mark.parametrize("wl", [NOSH])
+def test_decode_batch1_shapes(wl, torch):
+    s = Setup(wl, max_tokens=4, planes=True)
+    try:
+        for t in range(2):
+            x = draw_tokens(s, 1, first_id=4100 + t)
+            out, out32, ids, w = _forward(s.m, x, 1, torch)
+            ref = orc.moe_layer(s.layers[0], x)
+            check_ids_weights(ids, w, ref["ids"], ref["w"])
+            check_out(out32, ref["out"])
+    finally:
+        s.close()
