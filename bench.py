@@ -150,8 +150,8 @@ KERNEL_SOURCES = {
     "expert_down": ("k_phase.cu", "mxv.cuh", "bfv.cuh", "mxfrag.cuh", "pipeline.cuh"),
     "gemm_gateup": ("k_gemm.cu", "umma.cuh", "mxfrag.cuh", "pipeline.cuh"),
     "gemm_down": ("k_gemm.cu", "umma.cuh", "mxfrag.cuh", "pipeline.cuh"),
-    "mx8_gateup": ("k_mx8.cu", "umma.cuh", "pipeline.cuh"),
-    "mx8_down": ("k_mx8.cu", "umma.cuh", "pipeline.cuh"),
+    "mx8_gateup": ("k_mx8.cu", "umma.cuh", "pipeline.cuh", "bfv.cuh", "select.cuh"),
+    "mx8_down": ("k_mx8.cu", "umma.cuh", "pipeline.cuh", "bfv.cuh", "select.cuh"),
 }
 
 

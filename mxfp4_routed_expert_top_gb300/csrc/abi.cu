@@ -774,8 +774,10 @@ static int create_impl(const df_moe_config* cfg, int cuda_device, int slots, df_
     if (!rc) rc = dalloc(h, &h->mx_inv, Tm * k);
     if (!rc) rc = dalloc(h, &h->mx_xsfp, xrows * (H / 32));
     if (!rc) rc = dalloc(h, &h->mx_hsfp, hrows * (I / 32));
-    if (!rc && (!make_mx8_row_map(h->mx_xq, h->mx_xrows, c.hidden, h->px, &h->mx_xmap) ||
-                !make_mx8_row_map(h->mx_hq, h->mx_hrows, c.inter, h->ph, &h->mx_hmap)))
+    if (!rc && (!make_mx8_row_map(h->mx_xq, h->mx_xrows, c.hidden, h->px, &h->mx_xmap,
+                                  mx8_box_rows(h->px)) ||
+                !make_mx8_row_map(h->mx_hq, h->mx_hrows, c.inter, h->ph, &h->mx_hmap,
+                                  mx8_box_rows(h->ph))))
       rc = fail(h, DF_MOE_ECUDA, "tensor map encoding failed");
     h->phase_mx8 = h->px > 1 && !slots && k <= 32 && E <= 1024 &&
                    mx8_phase_supported(c.hidden, c.inter, (int)R);

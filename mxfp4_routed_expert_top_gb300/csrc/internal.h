@@ -312,6 +312,9 @@ bool mx8_supported(int H, int I);
 // `planes` rows each, and the rows that a stage's 32-row scale chunk or its
 // B box reads past the last one.
 int mx8_rows_cap(int nassign, int planes);
+// B rows a box of the batch GEMM's activation map for `planes` (the row map
+// of a handle's x or h rows is made with it).
+int mx8_box_rows(int planes);
 // Tensor maps of the gate, up and down codes of an arena of E spans.
 bool make_mx8_maps(const uint8_t* arena, size_t span_bytes, int H, int I, int E, ChunkMap* gate,
                    ChunkMap* up, ChunkMap* down);

@@ -332,10 +332,13 @@ struct Unit {
   int e, mt, pos, cnt, ks, kb, ke;
 };
 __device__ __forceinline__ int kspl_of(const Mx8Args& a) { return a.kspl > 1 ? a.kspl : 1; }
-template <int P>
+// Only the one-token phase kernels (token tile 16) split K; the batch GEMM's
+// instantiations compile without it.
+constexpr int kSplitKN = 16;
+template <int P, bool SPLIT>
 __device__ __forceinline__ Unit unit_at(const Mx8Args& a, const Item* items, int u) {
   Unit w;
-  const int ksp = kspl_of(a), per_item = a.MT * ksp;
+  const int ksp = SPLIT ? kspl_of(a) : 1, per_item = a.MT * ksp;
   const int item = u / per_item, rem = u - item * per_item;
   w.mt = rem / ksp;
   w.ks = rem - w.mt * ksp;
@@ -381,7 +384,7 @@ __device__ void role_tma(const Mx8Args& a, int n_units, const Pipe<MODE, KN, P>&
   bool ok = true;
   const uint64_t pol = l2_evict_first_policy();
   for (int u = c.vcta; u < n_units && ok; u += c.nvcta) {
-    const Unit w = unit_at<P>(a, c.items, u);
+    const Unit w = unit_at<P, KN == kSplitKN>(a, c.items, u);
     if (!w.ok) continue;
     const uint8_t* span = a.arena + (size_t)w.e * a.span_bytes;
     for (int tb = 0; tb < w.cnt && ok; tb += KN / P) {
@@ -438,7 +441,7 @@ __device__ void role_mma(const Mx8Args& a, int n_units, const Pipe<MODE, KN, P>&
   uint32_t g = 0, pc = 0;
   bool ok = true;
   for (int u = c.vcta; u < n_units && ok; u += c.nvcta) {
-    const Unit w = unit_at<P>(a, c.items, u);
+    const Unit w = unit_at<P, KN == kSplitKN>(a, c.items, u);
     if (!w.ok) continue;
     for (int tb = 0; tb < w.cnt && ok; tb += KN / P, ++pc) {
       const int N = (min(KN / P, w.cnt - tb) * P + 15) & ~15;
@@ -569,9 +572,9 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, const Pipe<MODE, KN
     ++xk;
     return fine;
   };
-  const bool split = kspl_of(a) > 1;
+  const bool split = KN == kSplitKN && kspl_of(a) > 1;
   for (int u = c.vcta; u < n_units && ok; u += c.nvcta) {
-    const Unit w = unit_at<P>(a, c.items, u);
+    const Unit w = unit_at<P, KN == kSplitKN>(a, c.items, u);
     if (!w.ok) {
       if (L == 0) atomicOr(a.err, DEV_ERR_RANGE);
       continue;
@@ -727,7 +730,7 @@ __global__ void __launch_bounds__(kThr, ctas_per_sm(MODE, P)) mx8_gemm_kernel(co
     if (threadIdx.x == 0) atomicOr(a.err, DEV_ERR_RANGE);
     n_items = n_items < 0 ? 0 : a.max_items;
   }
-  const int n_units = n_items * a.MT * kspl_of(a);
+  const int n_units = n_items * a.MT;  // (whole K)
   const Pipe<MODE, KN, P> c{smem, b, tmem, (int)blockIdx.x, (int)gridDim.x, a.items, a.sorted};
   if (warp < 4) {
     role_epilogue<MODE, KN, P>(a, n_units, c, warp, lane);
@@ -798,7 +801,7 @@ __device__ void select_one_token(const SelArgs& sel, uint8_t* scratch, Item* sel
 }
 
 constexpr int kPhThr = 512;
-constexpr int kPhKN = 16;  // B rows a pass: the token's planes (4 of x, 5 of h), MMA N 16
+constexpr int kPhKN = kSplitKN;  // B rows a pass: the token's planes (4 of x, 5 of h), MMA N 16
 template <int MODE>
 struct PhGeo {
   static constexpr int P = MODE == 0 ? kPlanesX : kPlanesH;
@@ -1254,7 +1257,10 @@ cudaError_t launch_mx8_kn(const Mx8Args& a, cudaStream_t s) {
 // MXFP8 (planes = 1): the token tile is 32 when the items average up to 24
 // tokens (a smaller B slot leaves room for more stages, i.e. more weight
 // bytes in flight), else 64 (fewer passes over each expert's weights).
-// Planes: 16 tokens a pass (64 B rows of x's 4 planes, 80 of h's 5).
+// Planes: 16 tokens a pass (64 B rows of x's 4 planes, 80 of h's 5; 12
+// tokens of h, N 64, leave three accumulator sets instead of two but measured
+// 14% slower at batch 512: items of 13-16 tokens take a second pass over
+// their weights).
 template <int MODE>
 cudaError_t launch_mx8(const Mx8Args& a, int planes, cudaStream_t s) {
   if (planes > 1) {
@@ -1269,6 +1275,8 @@ cudaError_t launch_mx8(const Mx8Args& a, int planes, cudaStream_t s) {
 }  // namespace
 
 bool mx8_supported(int H, int I) { return H % (2 * kM) == 0 && I % kKS == 0; }
+
+int mx8_box_rows(int planes) { return box_rows(planes); }
 
 int mx8_rows_cap(int nassign, int planes) {
   // a stage's token scales are read as 32 rows from the pass's first, its
