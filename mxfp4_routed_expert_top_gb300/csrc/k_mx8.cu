@@ -338,13 +338,24 @@ constexpr int kSplitKN = 16;
 template <int P, bool SPLIT>
 __device__ __forceinline__ Unit unit_at(const Mx8Args& a, const Item* items, int u) {
   Unit w;
-  const int ksp = SPLIT ? kspl_of(a) : 1, per_item = a.MT * ksp;
-  const int item = u / per_item, rem = u - item * per_item;
-  w.mt = rem / ksp;
-  w.ks = rem - w.mt * ksp;
-  const int nks = a.K / kKS;
-  w.kb = nks * w.ks / ksp;
-  w.ke = nks * (w.ks + 1) / ksp;
+  int item;
+  if constexpr (SPLIT) {
+    const int ksp = kspl_of(a), per_item = a.MT * ksp;
+    item = u / per_item;
+    const int rem = u - item * per_item;
+    w.mt = rem / ksp;
+    w.ks = rem - w.mt * ksp;
+    const int nks = a.K / kKS;
+    w.kb = nks * w.ks / ksp;
+    w.ke = nks * (w.ks + 1) / ksp;
+  } else {
+    item = u / a.MT;
+    w.mt = u - item * a.MT;
+    w.ks = 0;
+    w.kb = 0;
+    w.ke = a.K / kKS;
+    items = a.items;
+  }
   const Item it = items[item];
   w.e = it.e;
   w.pos = it.pos;
@@ -359,25 +370,22 @@ __device__ __forceinline__ Unit unit_at(const Mx8Args& a, const Item* items, int
 // roles
 // ---------------------------------------------------------------------------
 
-// Where one pipeline (a TMA warp, an MMA warp, four epilogue warps) lives:
-// its shared memory (the Geo layout) and barriers, its first tensor memory
-// column, its index among the grid's pipelines, and the selection it reads
-// (global, or a copy in shared memory).
-template <int MODE, int KN, int P>
+// Where one pipeline (a TMA warp, an MMA warp, four epilogue warps) works:
+// its index among the grid's pipelines and the selection it reads (global,
+// or a copy in shared memory). Its shared memory (the Geo layout), barriers
+// and first tensor memory column are passed as plain arguments, which keeps
+// the shared-memory accesses of the batch GEMM's roles in the shared window
+// (a struct holding them measured 3% slower there).
 struct Pipe {
-  uint8_t* smem;
-  Bars<Geo<MODE, KN, P>::S, Geo<MODE, KN, P>::NACC>* b;
-  uint32_t tmem;
   int vcta, nvcta;
   const Item* items;
   const int32_t* sorted;
 };
 
 template <int MODE, int KN, int P>
-__device__ void role_tma(const Mx8Args& a, int n_units, const Pipe<MODE, KN, P>& c) {
+__device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem,
+                         Bars<Geo<MODE, KN, P>::S, Geo<MODE, KN, P>::NACC>* b, const Pipe& c) {
   using G = Geo<MODE, KN, P>;
-  uint8_t* const smem = c.smem;
-  auto* const b = c.b;
   const int nks = a.K / kKS;
   uint32_t g = 0;
   uint32_t armed = 0u, last_par = 0u;
@@ -393,7 +401,8 @@ __device__ void role_tma(const Mx8Args& a, int n_units, const Pipe<MODE, KN, P>&
       static_assert(KN % BR == 0, "B boxes of a pass");
       const int nb = (nr + BR - 1) / BR;
       const int row = (w.pos + tb) * P;
-      for (int ks = w.kb; ks < w.ke; ++ks, ++g) {
+      const int kb = KN == kSplitKN ? w.kb : 0, ke = KN == kSplitKN ? w.ke : nks;
+      for (int ks = kb; ks < ke; ++ks, ++g) {
         const uint32_t s = g % G::S, ph = (g / G::S) & 1u;
         if (!wait_or_give_up(&b->empty[s], ph ^ 1u, &b->err)) { ok = false; break; }
         uint64_t* full = &b->full[s];
@@ -433,11 +442,11 @@ __device__ void role_tma(const Mx8Args& a, int n_units, const Pipe<MODE, KN, P>&
 // The whole MMA warp walks the stages (its lanes assemble a gate/up stage's
 // A scale chunk); lane 0 issues the tensor-core work.
 template <int MODE, int KN, int P>
-__device__ void role_mma(const Mx8Args& a, int n_units, const Pipe<MODE, KN, P>& c, int lane) {
+__device__ void role_mma(const Mx8Args& a, int n_units, uint8_t* smem,
+                         Bars<Geo<MODE, KN, P>::S, Geo<MODE, KN, P>::NACC>* b, uint32_t tmem,
+                         const Pipe& c, int lane) {
   using G = Geo<MODE, KN, P>;
-  uint8_t* const smem = c.smem;
-  auto* const b = c.b;
-  const uint32_t tmem = c.tmem;
+  const int nks = a.K / kKS;
   uint32_t g = 0, pc = 0;
   bool ok = true;
   for (int u = c.vcta; u < n_units && ok; u += c.nvcta) {
@@ -448,7 +457,8 @@ __device__ void role_mma(const Mx8Args& a, int n_units, const Pipe<MODE, KN, P>&
       const uint32_t acc = pc % G::NACC;
       if (!warp_wait(&b->acce[acc], ((pc / G::NACC) & 1u) ^ 1u, &b->err)) { ok = false; break; }
       tc_fence_after();
-      for (int ks = w.kb; ks < w.ke; ++ks, ++g) {
+      const int kb = KN == kSplitKN ? w.kb : 0, ke = KN == kSplitKN ? w.ke : nks;
+      for (int ks = kb; ks < ke; ++ks, ++g) {
         const uint32_t s = g % G::S, ph = (g / G::S) & 1u;
         if (!warp_wait(&b->full[s], ph, &b->err)) { ok = false; break; }
         tc_fence_after();
@@ -480,7 +490,7 @@ __device__ void role_mma(const Mx8Args& a, int n_units, const Pipe<MODE, KN, P>&
             const uint32_t idesc = umma::idesc_mxf8f6f4_e2m1_e4m3(kM, N, kk, kk);
             mma_mx(tmem + acc * G::accCols, umma::smem_desc_sw128(as + 32 * kk),
                    umma::smem_desc_sw128(bs + 32 * kk), idesc, col, col + 4,
-                   ks != w.kb || kk != 0);
+                   ks != kb || kk != 0);
           }
           tc_commit(&b->empty[s]);
         }
@@ -531,12 +541,10 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t addr, uint32_t (&v)[KN]) {
 
 // `warp`: the warp's tensor memory lane quarter (its index mod 4).
 template <int MODE, int KN, int P>
-__device__ void role_epilogue(const Mx8Args& a, int n_units, const Pipe<MODE, KN, P>& c, int warp,
-                              int lane) {
+__device__ void role_epilogue(const Mx8Args& a, int n_units, uint8_t* smem,
+                              Bars<Geo<MODE, KN, P>::S, Geo<MODE, KN, P>::NACC>* b,
+                              uint32_t tmem, const Pipe& c, int warp, int lane) {
   using G = Geo<MODE, KN, P>;
-  uint8_t* const smem = c.smem;
-  auto* const b = c.b;
-  const uint32_t tmem = c.tmem;
   constexpr int TPP = KN / P;  // tokens a pass
   const int L = 32 * warp + lane;
   const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
@@ -592,7 +600,7 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, const Pipe<MODE, KN
         for (int c0 = 0; c0 < nv; c0 += 32) {
           const int nc = min(32, nv - c0);
           // the chunk's assignment indices, one a lane, fetched together
-          const int my_a = lane < nc ? c.sorted[w.pos + tb + c0 + lane] : -1;
+          const int my_a = lane < nc ? a.sorted[w.pos + tb + c0 + lane] : -1;
           uint32_t v[32];
           tmem_ld32(lane_addr + acc * G::accCols + c0, v);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -635,7 +643,7 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, const Pipe<MODE, KN
       } else {
         // planes: token n's value is the sum of its P columns, in plane order
         static_assert(KN % 16 == 0 && KN <= 96 && TPP <= 32, "plane pass columns");
-        const int my_a = lane < nv ? c.sorted[w.pos + tb + lane] : -1;
+        const int my_a = lane < nv ? (KN == kSplitKN ? c.sorted : a.sorted)[w.pos + tb + lane] : -1;
         uint32_t v[KN];
         float gs[TPP];
         tmem_ld_cols<KN>(lane_addr + acc * G::accCols, v);
@@ -731,13 +739,13 @@ __global__ void __launch_bounds__(kThr, ctas_per_sm(MODE, P)) mx8_gemm_kernel(co
     n_items = n_items < 0 ? 0 : a.max_items;
   }
   const int n_units = n_items * a.MT;  // (whole K)
-  const Pipe<MODE, KN, P> c{smem, b, tmem, (int)blockIdx.x, (int)gridDim.x, a.items, a.sorted};
+  const Pipe c{(int)blockIdx.x, (int)gridDim.x, a.items, a.sorted};
   if (warp < 4) {
-    role_epilogue<MODE, KN, P>(a, n_units, c, warp, lane);
+    role_epilogue<MODE, KN, P>(a, n_units, smem, b, tmem, c, warp, lane);
   } else if (warp == kTmaWarp) {
-    if (lane == 0) role_tma<MODE, KN, P>(a, n_units, c);
+    if (lane == 0) role_tma<MODE, KN, P>(a, n_units, smem, b, c);
   } else if (warp == kMmaWarp) {
-    role_mma<MODE, KN, P>(a, n_units, c, lane);
+    role_mma<MODE, KN, P>(a, n_units, smem, b, tmem, c, lane);
   }
   tc_fence_before();
   __syncthreads();
@@ -900,16 +908,16 @@ __global__ void __launch_bounds__(kPhThr, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(&b0->tmem);
   const int n_units = n_items * a.MT * kspl_of(a);
   if (pipe < 2) {
-    const Pipe<MODE, kPhKN, P> c{smem + pipe * PhGeo<MODE>::Pipe,
-                                 reinterpret_cast<Bs*>(smem + pipe * PhGeo<MODE>::Pipe + G::offBars),
-                                 tmem + pipe * (kTmemCols / 2), 2 * cta + pipe, 2 * ncta, items,
-                                 sorted};
+    uint8_t* const ps = smem + pipe * PhGeo<MODE>::Pipe;
+    Bs* const pb = reinterpret_cast<Bs*>(ps + G::offBars);
+    const uint32_t pt = tmem + pipe * (kTmemCols / 2);
+    const Pipe c{2 * cta + pipe, 2 * ncta, items, sorted};
     if (role < 4) {
-      role_epilogue<MODE, kPhKN, P>(a, n_units, c, warp & 3, lane);
+      role_epilogue<MODE, kPhKN, P>(a, n_units, ps, pb, pt, c, warp & 3, lane);
     } else if (role == 4) {
-      if (lane == 0) role_tma<MODE, kPhKN, P>(a, n_units, c);
+      if (lane == 0) role_tma<MODE, kPhKN, P>(a, n_units, ps, pb, c);
     } else {
-      role_mma<MODE, kPhKN, P>(a, n_units, c, lane);
+      role_mma<MODE, kPhKN, P>(a, n_units, ps, pb, pt, c, lane);
     }
   }
   tc_fence_before();
