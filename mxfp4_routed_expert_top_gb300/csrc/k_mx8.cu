@@ -391,7 +391,10 @@ __device__ void role_tma(const Mx8Args& a, int n_units, uint8_t* smem,
   uint32_t armed = 0u, last_par = 0u;
   bool ok = true;
   const uint64_t pol = l2_evict_first_policy();
-  for (int u = c.vcta; u < n_units && ok; u += c.nvcta) {
+  // (the batch GEMM: one pipeline a CTA, its units blockIdx.x + j gridDim.x)
+  const int u0 = KN == kSplitKN ? c.vcta : (int)blockIdx.x;
+  const int du = KN == kSplitKN ? c.nvcta : (int)gridDim.x;
+  for (int u = u0; u < n_units && ok; u += du) {
     const Unit w = unit_at<P, KN == kSplitKN>(a, c.items, u);
     if (!w.ok) continue;
     const uint8_t* span = a.arena + (size_t)w.e * a.span_bytes;
@@ -449,7 +452,10 @@ __device__ void role_mma(const Mx8Args& a, int n_units, uint8_t* smem,
   const int nks = a.K / kKS;
   uint32_t g = 0, pc = 0;
   bool ok = true;
-  for (int u = c.vcta; u < n_units && ok; u += c.nvcta) {
+  // (the batch GEMM: one pipeline a CTA, its units blockIdx.x + j gridDim.x)
+  const int u0 = KN == kSplitKN ? c.vcta : (int)blockIdx.x;
+  const int du = KN == kSplitKN ? c.nvcta : (int)gridDim.x;
+  for (int u = u0; u < n_units && ok; u += du) {
     const Unit w = unit_at<P, KN == kSplitKN>(a, c.items, u);
     if (!w.ok) continue;
     for (int tb = 0; tb < w.cnt && ok; tb += KN / P, ++pc) {
@@ -581,7 +587,10 @@ __device__ void role_epilogue(const Mx8Args& a, int n_units, uint8_t* smem,
     return fine;
   };
   const bool split = KN == kSplitKN && kspl_of(a) > 1;
-  for (int u = c.vcta; u < n_units && ok; u += c.nvcta) {
+  // (the batch GEMM: one pipeline a CTA, its units blockIdx.x + j gridDim.x)
+  const int u0 = KN == kSplitKN ? c.vcta : (int)blockIdx.x;
+  const int du = KN == kSplitKN ? c.nvcta : (int)gridDim.x;
+  for (int u = u0; u < n_units && ok; u += du) {
     const Unit w = unit_at<P, KN == kSplitKN>(a, c.items, u);
     if (!w.ok) {
       if (L == 0) atomicOr(a.err, DEV_ERR_RANGE);
