@@ -370,12 +370,11 @@ __device__ __forceinline__ Unit unit_at(const Mx8Args& a, const Item* items, int
 // roles
 // ---------------------------------------------------------------------------
 
-// Where one pipeline (a TMA warp, an MMA warp, four epilogue warps) works:
-// its index among the grid's pipelines and the selection it reads (global,
-// or a copy in shared memory). Its shared memory (the Geo layout), barriers
-// and first tensor memory column are passed as plain arguments, which keeps
-// the shared-memory accesses of the batch GEMM's roles in the shared window
-// (a struct holding them measured 3% slower there).
+// Where one pipeline (a TMA warp, an MMA warp, four epilogue warps) of the
+// one-token phase kernels works: its index among the grid's pipelines and the
+// selection it reads (a copy in shared memory at gate/up). The batch GEMM's
+// roles walk their units from the block index instead: a start and stride
+// read from here cost its gate/up 3%.
 struct Pipe {
   int vcta, nvcta;
   const Item* items;
