@@ -824,7 +824,7 @@ struct PhGeo {
   using G = Geo<MODE, kPhKN, P>;
   // a pipeline's share of the CTA's shared memory (the batch GEMM's layout
   // for two CTAs an SM), a multiple of 1024 bytes
-  static constexpr size_t Pipe = (smem_bytes<MODE, kPhKN, P>() + 1023) & ~(size_t)1023;
+  static constexpr size_t Bytes = (smem_bytes<MODE, kPhKN, P>() + 1023) & ~(size_t)1023;
 };
 static_assert(geo_ok<0, kPhKN, kPlanesX>() && geo_ok<1, kPhKN, kPlanesH>(), "phase pipelines");
 
@@ -862,7 +862,7 @@ __global__ void __launch_bounds__(kPhThr, 1)
   const int pipe = warp / 6, role = warp - 6 * pipe;  // warps 12-15 only help select
   Bs* const b0 = reinterpret_cast<Bs*>(smem + G::offBars);
   // set-up while the preceding kernel finishes: the SM's tensor memory (half
-  // a pipeline) and each pipeline's barriers
+  // of it to each pipeline) and each pipeline's barriers
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&b0->tmem)),
@@ -871,7 +871,7 @@ __global__ void __launch_bounds__(kPhThr, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (lane == 0 && role == 5 && pipe < 2) {
-    Bs* b = reinterpret_cast<Bs*>(smem + pipe * PhGeo<MODE>::Pipe + G::offBars);
+    Bs* b = reinterpret_cast<Bs*>(smem + pipe * PhGeo<MODE>::Bytes + G::offBars);
     for (int i = 0; i < G::S; ++i) {
       mbar_init(&b->full[i], 1);
       mbar_init(&b->empty[i], 1);
@@ -916,7 +916,7 @@ __global__ void __launch_bounds__(kPhThr, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(&b0->tmem);
   const int n_units = n_items * a.MT * kspl_of(a);
   if (pipe < 2) {
-    uint8_t* const ps = smem + pipe * PhGeo<MODE>::Pipe;
+    uint8_t* const ps = smem + pipe * PhGeo<MODE>::Bytes;
     Bs* const pb = reinterpret_cast<Bs*>(ps + G::offBars);
     const uint32_t pt = tmem + pipe * (kTmemCols / 2);
     const Pipe c{2 * cta + pipe, 2 * ncta, items, sorted};
@@ -932,7 +932,7 @@ __global__ void __launch_bounds__(kPhThr, 1)
   __syncthreads();
   tc_fence_after();
   if (threadIdx.x == 0) {
-    const Bs* b1 = reinterpret_cast<const Bs*>(smem + PhGeo<MODE>::Pipe + G::offBars);
+    const Bs* b1 = reinterpret_cast<const Bs*>(smem + PhGeo<MODE>::Bytes + G::offBars);
     if (b0->err || b1->err) atomicOr(a.err, DEV_ERR_TIMEOUT);
   }
   if (warp == 0)
@@ -1475,7 +1475,7 @@ cudaError_t launch_phase_mx8(const Mx8Args& a, const BfvArgs& sh, const SelArgs&
   const int sms = sms_mx8();
   if (n_sh < 0 || n_sh >= sms || (n_sh > 0 && sh.rows <= 0)) return cudaErrorInvalidValue;
   const size_t smem =
-      std::max(2 * PhGeo<MODE>::Pipe, n_sh > 0 ? bfv_smem_bytes(sh.K) : (size_t)0);
+      std::max(2 * PhGeo<MODE>::Bytes, n_sh > 0 ? bfv_smem_bytes(sh.K) : (size_t)0);
   static size_t configured = 0;
   if (configured < smem) {
     const cudaError_t e = cudaFuncSetAttribute(
