@@ -86,8 +86,10 @@ extern "C" {
  * rounding of what the planes before it left, so that the sum reproduces the
  * activation to fp32 precision; the results are the exact path's, within its
  * tolerances. Meant for batches (prefill): on such a handle decode calls run
- * these GEMMs too, slower than the default decode kernels. Same shape rules
- * as DF_MOE_MXFP8_ACT, and not together with it. */
+ * these GEMMs too (one token: two phase kernels that run them beside the
+ * shared experts, the gate/up sums taken over eight parts of K), slower than
+ * the default decode kernels below 4 tokens. Same shape rules as
+ * DF_MOE_MXFP8_ACT, and not together with it. */
 #define DF_MOE_PLANES 16u
 
 typedef struct df_moe df_moe; /* opaque, library-owned */
