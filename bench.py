@@ -119,6 +119,19 @@ def mx8_gateup_bytes(wl, n_union, T, planes=1):
     return n_union * per_expert + rows * planes * (wl.H + wl.H // 32) + h_out
 
 
+def mx8_phase_gateup_bytes(wl, n_union):
+    """Algorithmic bytes of the one-token gate/up phase kernel of an exact-planes
+    handle: the routed experts' gate and up halves (codes + scales) and x's four
+    E4M3 planes in, the gate and up sums of its eight parts of K out (fp32),
+    and beside them the shared experts' gate and up rows (bf16), x (bf16) and
+    their h (fp32)."""
+    per_expert = 2 * wl.I * wl.H * 17 // 32
+    kspl = max(1, min(8, wl.H // 128))
+    routed = n_union * per_expert + 4 * (wl.H + wl.H // 32) + kspl * wl.k * 2 * wl.I * 4
+    shared = wl.n_shared * 2 * wl.Is * wl.H * 2 + wl.H * 2 + wl.n_shared * wl.Is * 4
+    return routed + shared
+
+
 def gateup_flops(wl, T):
     """Useful flops of the routed gate/up contraction: 2 per multiply-add of
     each of the T*k assignments' 2I x H products."""
@@ -572,7 +585,11 @@ def run_ours(args):
     lb = layer_bytes(wl, u_mean, T) * wl.L
     # dominant kernel: the routed gate/up GEMM (tcgen05, larger batches),
     # else the gate/up phase of decode batches
-    if kt.get("mx8_gateup", (0, 0.0))[0]:
+    if kt.get("mx8_gateup", (0, 0.0))[0] and args.planes and T == 1 and not args.cache_slots:
+        # one token on exact planes: the gate/up phase kernel, shared experts
+        # beside the routed ones
+        dom, dom_bytes = "mx8_gateup", mx8_phase_gateup_bytes(wl, u_mean)
+    elif kt.get("mx8_gateup", (0, 0.0))[0]:
         dom, dom_bytes = "mx8_gateup", mx8_gateup_bytes(wl, u_mean, T, 4 if args.planes else 1)
     elif kt.get("gemm_gateup", (0, 0.0))[0]:
         dom, dom_bytes = "gemm_gateup", gateup_bytes(wl, u_mean, T)

@@ -51,3 +51,12 @@ def test_bytes_grow_with_distinct_experts_only():
     one = bench.layer_bytes(K3, 16, 1)
     assert bench.layer_bytes(K3, 16, 2) - one == 2 * H * 2
     assert bench.layer_bytes(K3, 17, 1) - one == 17_547_264
+
+
+def test_batch1_planes_phase_gateup_bytes():
+    # the one-token gate/up phase of an exact-planes handle: the routed experts,
+    # x's 4 E4M3 planes with one scale byte per 32, the gate and up sums of 8
+    # parts of K (fp32); beside them the shared gate/up rows, x (bf16), their h
+    routed = 16 * 11_698_176 + 4 * (H + H // 32) + 8 * k * 2 * I * 4
+    shared = 2 * 2 * 1536 * H * 2 + H * 2 + 2 * 1536 * 4
+    assert bench.mx8_phase_gateup_bytes(K3, 16) == routed + shared == 276_880_256
