@@ -615,7 +615,10 @@ def run_ours(args):
         "config": {**workload_config(wl, ws),
                    "l2": "flushed (256 MiB write) before every timed step",
                    "launch": "cuda graph" if args.graph else "stream",
-                   "expert_path": ("tcgen05 block-scaled (E4M3 planes)" if args.planes else
+                   "expert_path": ("decode phase kernels with the routed experts on the tcgen05 "
+                                   "block-scaled MMA (E4M3 planes) beside the shared GEMV"
+                                   if args.planes and T == 1 and not args.cache_slots else
+                                   "tcgen05 block-scaled (E4M3 planes)" if args.planes else
                                    "tcgen05 block-scaled (MXFP8)" if args.mxfp8 else
                                    "decode phase kernels (mma.sync GEMVs)" if T <= 8 else
                                    "mma_sync" if args.mma_sync_prefill else
